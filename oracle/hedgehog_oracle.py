@@ -1,0 +1,257 @@
+"""Plain fp64 restatement of Hedgehog / Taylor causal linear attention.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the product path never
+imports this module.  All arithmetic is float64; inputs are promoted exactly
+from whatever precision the caller holds (bf16-rounded values are exactly
+representable in float64).
+
+Sources (page title, then section / equation):
+
+* "The Hedgehog & the Porcupine: Expressive Linear Attentions with Softmax
+  Mimicry" (paper-graph-ui summary of arXiv 2402.04347), referred to below as
+  *HH summary*; and the paperlayer.ai summary of the same paper, *HH digest*.
+
+Readings taken where the pages are silent or inconsistent:
+
+* W orientation: ``h = x @ W + b`` with ``W[k][l]`` = input k -> output l, so
+  the direction w_l of Choice 1 is column l of W.
+* The negated half negates the bias too: ``exp(-(xW + b))`` (Choice 3 writes
+  ``exp(-w.x - b)``); the positive block comes first.
+* No 1/sqrt(d) or temperature inside phi; 1/sqrt(d) only in the softmax
+  target of the distillation loss.
+* Causal sums include the diagonal (j <= i).
+* Taylor map: ``[1, x, (x_i x_j / sqrt2) for i, j in [d]]`` with the pair
+  index i-major; the 1/sqrt2 makes phi(q).phi(k) = 1 + q.k + (q.k)^2 / 2.
+* Natural logarithm in the loss; the per-head result is the sum over queries.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "hedgehog_feature_map",
+    "taylor2_feature_map",
+    "taylor2_feature_dim",
+    "feature_map",
+    "causal_weights",
+    "linattn_quadratic",
+    "linattn_rows",
+    "linattn_recurrent",
+    "decode_step",
+    "softmax_target",
+    "mimicry_loss",
+    "mimicry_loss_rows",
+    "fwd_causal",
+    "loss_causal",
+]
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Feature maps
+# ---------------------------------------------------------------------------
+
+def hedgehog_feature_map(x, W, b) -> np.ndarray:
+    """Hedgehog single-layer MLP map with the negation block.
+
+    HH summary, "The Hedgehog MLP Feature Map": Choice 1 (element-wise
+    exponential of a learned affine map) and Choice 3 (negation mapping
+    R^d -> R^2d).  ``x``: [..., d]; ``W``: [d, d] (input-major); ``b``: [d].
+    Returns [..., 2d] = [exp(h), exp(-h)] with h = x W + b.
+    """
+    x, W, b = _f64(x), _f64(W), _f64(b)
+    h = x @ W + b
+    return np.concatenate([np.exp(h), np.exp(-h)], axis=-1)
+
+
+def taylor2_feature_dim(d: int) -> int:
+    """d' = 1 + d + d^2 (HH summary, "The Taylor Exponential as a Bridge Result")."""
+    return 1 + d + d * d
+
+
+def taylor2_feature_map(x) -> np.ndarray:
+    """Degree-2 Taylor map [1, x, vec(x x^T) / sqrt 2], pair index i-major.
+
+    HH summary, "The Taylor Exponential as a Bridge Result" (the feature
+    construction for 1 + q.k + (q.k)^2/2).  ``x``: [..., d] -> [..., 1+d+d^2].
+    """
+    x = _f64(x)
+    d = x.shape[-1]
+    one = np.ones(x.shape[:-1] + (1,), dtype=np.float64)
+    outer = (x[..., :, None] * x[..., None, :]).reshape(x.shape[:-1] + (d * d,))
+    return np.concatenate([one, x, outer / math.sqrt(2.0)], axis=-1)
+
+
+def feature_map(kind: str, x, W=None, b=None) -> np.ndarray:
+    """Dispatch on the map name: ``"hedgehog"`` or ``"taylor2"``."""
+    if kind == "hedgehog":
+        return hedgehog_feature_map(x, W, b)
+    if kind == "taylor2":
+        return taylor2_feature_map(x)
+    raise ValueError(f"unknown feature map {kind!r}")
+
+
+# ---------------------------------------------------------------------------
+# Causal linear attention
+# ---------------------------------------------------------------------------
+
+def causal_weights(phi_q, phi_k) -> np.ndarray:
+    """Row-normalised linear-attention weights a_ij / sum_{m<=i} a_im, j <= i.
+
+    HH summary, section 2 (the kernel form, paper Eq. 2): the unnormalised
+    weight of key j for query i is phi(q_i) . phi(k_j); entries above the
+    diagonal are zero.  ``phi_q``, ``phi_k``: [n, d'] -> [n, n].
+    """
+    a = _f64(phi_q) @ _f64(phi_k).T
+    a = np.tril(a)
+    return a / a.sum(axis=-1, keepdims=True)
+
+
+def linattn_quadratic(phi_q, phi_k, v) -> np.ndarray:
+    """Quadratic (brute-force) causal linear attention for one head.
+
+    HH summary, section 2 and "Complexity Analysis" (paper Eq. 2):
+    y_i = sum_{j<=i} (phi(q_i).phi(k_j)) v_j / sum_{j<=i} phi(q_i).phi(k_j).
+    ``phi_q``, ``phi_k``: [n, d']; ``v``: [n, d] -> y [n, d].
+    """
+    a = np.tril(_f64(phi_q) @ _f64(phi_k).T)
+    return (a @ _f64(v)) / a.sum(axis=-1, keepdims=True)
+
+
+def linattn_rows(phi_q, phi_k, v, rows) -> np.ndarray:
+    """The same definition evaluated one query row at a time.
+
+    For sampled checks on long sequences: row i needs phi_k[:i+1] and
+    v[:i+1] only.  Returns [len(rows), d].
+    """
+    phi_q, phi_k, v = _f64(phi_q), _f64(phi_k), _f64(v)
+    out = np.empty((len(rows), v.shape[-1]), dtype=np.float64)
+    for r, i in enumerate(rows):
+        a = phi_k[: i + 1] @ phi_q[i]
+        out[r] = (a @ v[: i + 1]) / a.sum()
+    return out
+
+
+def decode_step(phi_q_t, phi_k_t, v_t, S, z):
+    """One recurrent step: fold token t into the state, then read it out.
+
+    HH summary, "Complexity Analysis": S_t = S_{t-1} + phi(k_t)^T v_t,
+    z_t = z_{t-1} + phi(k_t), y_t = phi(q_t) S_t / (phi(q_t) . z_t).  The
+    state after the step includes token t (the causal sum runs to j = i).
+    ``S``: [d', d]; ``z``: [d'].  Returns (y_t, S_t, z_t); inputs unchanged.
+    """
+    phi_q_t, phi_k_t, v_t = _f64(phi_q_t), _f64(phi_k_t), _f64(v_t)
+    S = _f64(S) + np.outer(phi_k_t, v_t)
+    z = _f64(z) + phi_k_t
+    y = (phi_q_t @ S) / (phi_q_t @ z)
+    return y, S, z
+
+
+def linattn_recurrent(phi_q, phi_k, v, S0=None, z0=None):
+    """Recurrent causal linear attention over a whole sequence.
+
+    Runs :func:`decode_step` token by token from state (S0, z0) (zeros by
+    default).  Returns (y [n, d], S_n [d', d], z_n [d']).
+    """
+    phi_q, phi_k, v = _f64(phi_q), _f64(phi_k), _f64(v)
+    n, dp = phi_k.shape
+    d = v.shape[-1]
+    S = np.zeros((dp, d)) if S0 is None else _f64(S0).copy()
+    z = np.zeros(dp) if z0 is None else _f64(z0).copy()
+    y = np.empty((n, d))
+    for t in range(n):
+        y[t], S, z = decode_step(phi_q[t], phi_k[t], v[t], S, z)
+    return y, S, z
+
+
+# ---------------------------------------------------------------------------
+# Attention-weight distillation (mimicry) loss
+# ---------------------------------------------------------------------------
+
+def softmax_target(q, k) -> np.ndarray:
+    """Causal softmax(q k^T / sqrt d) over j <= i, max-subtracted per row.
+
+    HH summary, "The Attention Weight Distillation Loss" (paper Eq. 4, the
+    target fraction).  ``q``, ``k``: [n, d] -> [n, n].
+    """
+    q, k = _f64(q), _f64(k)
+    n, d = q.shape
+    s = (q @ k.T) / math.sqrt(d)
+    mask = np.tril(np.ones((n, n), dtype=bool))
+    s = np.where(mask, s, -np.inf)
+    s = s - s.max(axis=-1, keepdims=True)
+    e = np.where(mask, np.exp(s), 0.0)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def mimicry_loss(q, k, phi_q, phi_k) -> np.ndarray:
+    """Per-query cross-entropy L_i of paper Eq. 4 for one head.
+
+    HH summary, "The Attention Weight Distillation Loss":
+    L_i = - sum_{j<=i} p_ij log( a_ij / sum_{m<=i} a_im ),
+    p = causal softmax(q k^T / sqrt d), a_ij = phi(q_i).phi(k_j).
+    Natural log.  Returns [n].
+    """
+    p = softmax_target(q, k)
+    w = causal_weights(phi_q, phi_k)
+    n = p.shape[0]
+    out = np.empty(n)
+    for i in range(n):
+        out[i] = -np.sum(p[i, : i + 1] * np.log(w[i, : i + 1]))
+    return out
+
+
+def mimicry_loss_rows(q, k, phi_q, phi_k, rows) -> np.ndarray:
+    """Eq. 4 evaluated for selected query rows only (sampled checks)."""
+    q, k, phi_q, phi_k = _f64(q), _f64(k), _f64(phi_q), _f64(phi_k)
+    d = q.shape[-1]
+    out = np.empty(len(rows))
+    for r, i in enumerate(rows):
+        s = (k[: i + 1] @ q[i]) / math.sqrt(d)
+        e = np.exp(s - s.max())
+        p = e / e.sum()
+        a = phi_k[: i + 1] @ phi_q[i]
+        out[r] = -np.sum(p * np.log(a / a.sum()))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Batched wrappers over [B, H, n, d] inputs (per-head maps W[H], b[H])
+# ---------------------------------------------------------------------------
+
+def _map_head(kind, x, W, b, h):
+    if kind == "hedgehog":
+        return hedgehog_feature_map(x, W[h], b[h])
+    return taylor2_feature_map(x)
+
+
+def fwd_causal(kind, q, k, v, W=None, b=None):
+    """Quadratic-form outputs y [B, H, n, d] for every (batch, head)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H = q.shape[:2]
+    y = np.empty(v.shape, dtype=np.float64)
+    for bi in range(B):
+        for h in range(H):
+            pq = _map_head(kind, q[bi, h], W, b, h)
+            pk = _map_head(kind, k[bi, h], W, b, h)
+            y[bi, h] = linattn_quadratic(pq, pk, v[bi, h])
+    return y
+
+
+def loss_causal(kind, q, k, W=None, b=None):
+    """Per-row losses [B, H, n] and per-head sums [B, H]."""
+    q, k = _f64(q), _f64(k)
+    B, H, n = q.shape[:3]
+    rows = np.empty((B, H, n))
+    for bi in range(B):
+        for h in range(H):
+            pq = _map_head(kind, q[bi, h], W, b, h)
+            pk = _map_head(kind, k[bi, h], W, b, h)
+            rows[bi, h] = mimicry_loss(q[bi, h], k[bi, h], pq, pk)
+    return rows, rows.sum(axis=-1)

@@ -1,0 +1,248 @@
+"""Pins for the fp64 oracle: checks against what the pages and mathematics fix.
+
+Each check below ties the oracle to something other than itself: hand-worked
+tiny cases (tests/golden/hand_worked.json), closed forms (the Taylor kernel
+1 + s + s^2/2; the Hedgehog kernel as a sum of cosh), special cases that
+reduce to a known answer (identity / zero maps, constant values), invariants
+(weights form a distribution; Gibbs' inequality for the loss) and the
+agreement of two independent forms (quadratic vs recurrent).
+
+``test_planted_mistakes_are_caught`` plants plausible mistakes in copies of
+the oracle (on the CPU) and asserts that at least one pin fails for each.
+"""
+
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+
+import oracle as ORACLE
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+RNG = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------------------
+# pin checks, written against a module-like object O so mutants can be run
+# ---------------------------------------------------------------------------
+
+def _head(O, kind, q, k, v, W=None, b=None):
+    pq = O.feature_map(kind, q, W, b)
+    pk = O.feature_map(kind, k, W, b)
+    return pq, pk, O.linattn_quadratic(pq, pk, v), O.mimicry_loss(q, k, pq, pk)
+
+
+def check_hand_worked(O, golden):
+    for name in ("E1", "E2", "E3", "E4"):
+        g = golden[name]
+        W = np.array(g["W"]) if "W" in g else None
+        b = np.array(g["b"]) if "b" in g else None
+        q, k, v = (np.array(g[t]) for t in ("q", "k", "v"))
+        pq, pk, y, L = _head(O, g["kind"], q, k, v, W, b)
+        np.testing.assert_allclose(y, np.array(g["y"]), rtol=0, atol=2e-10, err_msg=name)
+        np.testing.assert_allclose(L, np.array(g["L"]), rtol=0, atol=2e-11, err_msg=name)
+    g = golden["E4"]
+    pq = O.feature_map("hedgehog", np.array(g["q"]), np.array(g["W"]), np.array(g["b"]))
+    pk = O.feature_map("hedgehog", np.array(g["k"]), np.array(g["W"]), np.array(g["b"]))
+    assert abs(pq[3] @ pk[1] - g["pair_4_2"]) < 1e-8
+    # exact closed forms of E1 / E2
+    assert abs(_head(O, "hedgehog", np.array([[0.0], [0.0]]), np.array([[0.0], [math.log(2)]]),
+                     np.array([[1.0], [3.0]]), np.eye(1), np.zeros(1))[2][1, 0] - 19 / 9) < 1e-14
+    y2 = _head(O, "taylor2", np.array([[1.0], [0.5], [-1.0]]), np.array([[0.5], [1.0], [2.0]]),
+               np.array([[1.0], [2.0], [3.0]]))[2]
+    assert abs(y2[1, 0] - 145 / 93) < 1e-14 and abs(y2[2, 0] - 37 / 17) < 1e-14
+
+
+def check_taylor_closed_form(O, golden):
+    for d in (1, 3, 16):
+        q = RNG.normal(size=(50, d))
+        k = RNG.normal(size=(50, d))
+        pq, pk = O.taylor2_feature_map(q), O.taylor2_feature_map(k)
+        s = np.sum(q * k, axis=-1)
+        np.testing.assert_allclose(np.sum(pq * pk, axis=-1), 1 + s + s * s / 2, rtol=1e-12)
+        assert pq.shape[-1] == 1 + d + d * d == O.taylor2_feature_dim(d)
+    g = golden["taylor_dim_d64"]
+    assert O.taylor2_feature_dim(g["d"]) == g["dprime"]
+    # layout: [1, x, x_i x_j / sqrt2 (i-major)]
+    x = np.array([2.0, 3.0, 5.0])
+    p = O.taylor2_feature_map(x)
+    assert p[0] == 1 and list(p[1:4]) == [2, 3, 5]
+    assert abs(p[4 + 0 * 3 + 2] - 10 / math.sqrt(2)) < 1e-14
+
+
+def check_hedgehog_cosh(O, golden):
+    for d in (1, 4, 16):
+        W = RNG.normal(size=(d, d)) / math.sqrt(d)
+        b = RNG.normal(size=d) * 0.3
+        q = RNG.normal(size=(20, d))
+        k = RNG.normal(size=(20, d))
+        pq = O.hedgehog_feature_map(q, W, b)
+        pk = O.hedgehog_feature_map(k, W, b)
+        hq, hk = q @ W + b, k @ W + b
+        # phi(q).phi(k) = sum_l e^{hq+hk} + e^{-(hq+hk)} = 2 sum_l cosh(hq_l + hk_l)
+        np.testing.assert_allclose(np.sum(pq * pk, axis=-1),
+                                   2 * np.sum(np.cosh(hq + hk), axis=-1), rtol=1e-12)
+        assert pq.shape[-1] == 2 * d and np.all(pq > 0)
+
+
+def check_identity_and_zero_maps(O, golden):
+    d = 5
+    x = RNG.normal(size=(7, d))
+    np.testing.assert_allclose(O.hedgehog_feature_map(x, np.eye(d), np.zeros(d)),
+                               np.concatenate([np.exp(x), np.exp(-x)], -1), rtol=1e-15)
+    np.testing.assert_array_equal(O.hedgehog_feature_map(x, np.zeros((d, d)), np.zeros(d)),
+                                  np.ones((7, 2 * d)))
+
+
+def check_orientation(O, golden):
+    # W[0][1] = 1: input dimension 0 drives output feature 1 (h = x W + b).
+    W = np.zeros((3, 3))
+    W[0, 1] = 1.0
+    x = np.array([0.7, -0.2, 0.4])
+    p = O.hedgehog_feature_map(x, W, np.array([0.0, 0.25, 0.0]))
+    np.testing.assert_allclose(p, [1, math.exp(0.95), 1, 1, math.exp(-0.95), 1], rtol=1e-15)
+
+
+def check_weight_rows(O, golden):
+    pq = np.exp(RNG.normal(size=(33, 8)))
+    pk = np.exp(RNG.normal(size=(33, 8)))
+    w = O.causal_weights(pq, pk)
+    assert np.all(w >= 0)
+    np.testing.assert_allclose(w.sum(-1), 1.0, rtol=1e-13)
+    assert np.all(np.triu(w, 1) == 0)
+
+
+def check_constant_values_and_first_row(O, golden):
+    d = 4
+    W = RNG.normal(size=(d, d)) * 0.5
+    b = RNG.normal(size=d) * 0.1
+    q, k = RNG.normal(size=(2, 40, d))
+    v = np.full((40, 3), -1.75)
+    y = _head(O, "hedgehog", q, k, v, W, b)[2]
+    np.testing.assert_allclose(y, -1.75, rtol=1e-13)
+    v = RNG.normal(size=(40, 3))
+    for kind in ("hedgehog", "taylor2"):
+        y = _head(O, kind, q, k, v, W, b)[2]
+        np.testing.assert_allclose(y[0], v[0], rtol=1e-13)
+
+
+def check_uniform_cases(O, golden):
+    n, d = 30, 4
+    q, k = RNG.normal(size=(2, n, d))
+    v = RNG.normal(size=(n, 3))
+    prefix_mean = np.cumsum(v, 0) / np.arange(1, n + 1)[:, None]
+    y = _head(O, "hedgehog", q, k, v, np.zeros((d, d)), np.zeros(d))[2]
+    np.testing.assert_allclose(y, prefix_mean, rtol=1e-12, atol=1e-14)
+    y = _head(O, "taylor2", np.zeros((n, d)), k, v)[2]
+    np.testing.assert_allclose(y, prefix_mean, rtol=1e-12, atol=1e-14)
+
+
+def check_quadratic_vs_recurrent(O, golden):
+    for kind, d in (("hedgehog", 6), ("taylor2", 3)):
+        W = RNG.normal(size=(d, d)) / math.sqrt(d)
+        b = RNG.normal(size=d) * 0.1
+        q, k = RNG.normal(size=(2, 45, d))
+        v = RNG.normal(size=(45, d))
+        pq, pk = O.feature_map(kind, q, W, b), O.feature_map(kind, k, W, b)
+        yq = O.linattn_quadratic(pq, pk, v)
+        yr, S, z = O.linattn_recurrent(pq, pk, v)
+        np.testing.assert_allclose(yr, yq, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(S, pk.T @ v, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(z, pk.sum(0), rtol=1e-12)
+        np.testing.assert_allclose(O.linattn_rows(pq, pk, v, [0, 7, 44]), yq[[0, 7, 44]], rtol=1e-12)
+        # continuation: a prefill to n1, then steps from that state == the full sequence
+        y1, S1, z1 = O.linattn_recurrent(pq[:20], pk[:20], v[:20])
+        y2, S2, z2 = O.linattn_recurrent(pq[20:], pk[20:], v[20:], S1, z1)
+        np.testing.assert_allclose(np.concatenate([y1, y2]), yq, rtol=1e-11, atol=1e-13)
+        y2b = O.linattn_quadratic(pq, pk, v)[20:]
+        np.testing.assert_allclose(y2, y2b, rtol=1e-11, atol=1e-13)
+
+
+def check_softmax_target(O, golden):
+    d = 4
+    q = RNG.normal(size=(2, d))
+    k = RNG.normal(size=(2, d))
+    p = O.softmax_target(q, k)
+    # two keys: p_21 = logistic((q2.k1 - q2.k2) / sqrt d)
+    p21 = 1.0 / (1.0 + math.exp((q[1] @ k[1] - q[1] @ k[0]) / math.sqrt(d)))
+    assert abs(p[1, 0] - p21) < 1e-14 and p[0, 0] == 1.0 and p[0, 1] == 0.0
+    big = O.softmax_target(np.full((5, 2), 30.0), np.full((5, 2), 30.0))
+    np.testing.assert_allclose(big.sum(-1), 1.0, rtol=1e-14)
+
+
+def check_loss_properties(O, golden):
+    n, d = 40, 4
+    W = RNG.normal(size=(d, d)) * 0.7
+    b = RNG.normal(size=d) * 0.2
+    q, k = RNG.normal(size=(2, n, d))
+    pq, pk = O.feature_map("hedgehog", q, W, b), O.feature_map("hedgehog", k, W, b)
+    L = O.mimicry_loss(q, k, pq, pk)
+    p = O.softmax_target(q, k)
+    H = -np.sum(np.where(p > 0, p * np.log(np.where(p > 0, p, 1)), 0), axis=-1)
+    assert abs(L[0]) < 1e-15
+    assert np.all(H >= -1e-15) and np.all(L >= H - 1e-12)          # Gibbs
+    np.testing.assert_allclose(O.mimicry_loss_rows(q, k, pq, pk, [0, 5, 39]), L[[0, 5, 39]], rtol=1e-12)
+    # W = 0, b = 0: uniform prediction, L_i = ln i for any q, k
+    p0 = O.feature_map("hedgehog", q, np.zeros((d, d)), np.zeros(d))
+    L0 = O.mimicry_loss(q, k, p0, p0)
+    np.testing.assert_allclose(L0, np.log(np.arange(1, n + 1)), rtol=1e-13, atol=1e-15)
+
+
+PINS = [check_hand_worked, check_taylor_closed_form, check_hedgehog_cosh,
+        check_identity_and_zero_maps, check_orientation, check_weight_rows,
+        check_constant_values_and_first_row, check_uniform_cases,
+        check_quadratic_vs_recurrent, check_softmax_target, check_loss_properties]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin, golden):
+    pin(ORACLE, golden)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must trip at least one pin
+# ---------------------------------------------------------------------------
+
+MUTANTS = {
+    "negated_half_keeps_bias": ("np.exp(-h)]", "np.exp(-(x @ W) + b)]"),
+    "taylor_without_sqrt2": ("outer / math.sqrt(2.0)", "outer"),
+    "taylor_constant_dropped": ("[one, x, outer", "[0 * one, x, outer"),
+    "W_transposed": ("h = x @ W + b", "h = x @ W.T + b"),
+    "bias_dropped": ("h = x @ W + b", "h = x @ W"),
+    "softmax_scale_1_over_d": ("(q @ k.T) / math.sqrt(d)", "(q @ k.T) / d"),
+    "diagonal_excluded": ("a = np.tril(a)", "a = np.tril(a, -1) + np.diag(np.diag(a)) * 0 + 1e-300"),
+    "quadratic_excludes_diagonal": ("a = np.tril(_f64(phi_q) @ _f64(phi_k).T)",
+                                    "a = np.tril(_f64(phi_q) @ _f64(phi_k).T, -1) + 1e-300"),
+    "readout_before_update": ("    S = _f64(S) + np.outer(phi_k_t, v_t)\n    z = _f64(z) + phi_k_t\n    y = (phi_q_t @ S) / (phi_q_t @ z)",
+                              "    y = (phi_q_t @ (_f64(S) + 1e-300)) / (phi_q_t @ (_f64(z) + 1e-300))\n    S = _f64(S) + np.outer(phi_k_t, v_t)\n    z = _f64(z) + phi_k_t"),
+    "loss_unnormalised_prediction": ("np.log(w[i, : i + 1])", "np.log(np.tril(_f64(phi_q) @ _f64(phi_k).T)[i, : i + 1])"),
+    "loss_log2": ("out[i] = -np.sum(p[i, : i + 1] * np.log(w[i, : i + 1]))",
+                  "out[i] = -np.sum(p[i, : i + 1] * np.log2(w[i, : i + 1]))"),
+    "loss_sign_flipped": ("out[i] = -np.sum(p[i, : i + 1]", "out[i] = np.sum(p[i, : i + 1]"),
+    "softmax_no_max_subtraction": ("    s = s - s.max(axis=-1, keepdims=True)\n", "    s = s * 1.0\n"),
+}
+
+
+def _mutant(old, new):
+    path = os.path.join(ROOT, "oracle", "hedgehog_oracle.py")
+    src = open(path).read()
+    assert old in src, f"mutation anchor not found: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    with np.errstate(all="ignore"):
+        exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name, golden):
+    mod = _mutant(*MUTANTS[name])
+    failed = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(mod, golden)
+        except (AssertionError, FloatingPointError, ValueError, ZeroDivisionError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
