@@ -1,0 +1,173 @@
+/*
+ * hh.h -- C ABI of the Hedgehog / Taylor causal linear-attention library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "The Hedgehog & the Porcupine: Expressive Linear
+ * Attentions with Softmax Mimicry" (summary of arXiv 2402.04347):
+ *
+ *   feature maps   phi_hh(x) = [exp(xW + b); exp(-(xW + b))]          (R^d -> R^2d)
+ *                  ("The Hedgehog MLP Feature Map", Choices 1 and 3)
+ *                  phi_t2(x) = [1, x, (x_i x_j / sqrt 2)_{i,j}]       (R^d -> R^{1+d+d^2})
+ *                  ("The Taylor Exponential as a Bridge Result")
+ *   causal output  y_i = sum_{j<=i} (phi(q_i).phi(k_j)) v_j / sum_{j<=i} phi(q_i).phi(k_j)
+ *                  (section 2, paper Eq. 2; running sums S, z in "Complexity Analysis")
+ *   mimicry loss   L_i = -sum_{j<=i} softmax_j(q_i.k_j / sqrt d) log(a_ij / sum_{m<=i} a_im),
+ *                  a_ij = phi(q_i).phi(k_j)
+ *                  ("The Attention Weight Distillation Loss", paper Eq. 4)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Ownership: the caller allocates and owns every buffer.  The library
+ *   allocates no device or host memory in any call and keeps no state other
+ *   than cached device attributes.
+ * - Pointers: q, k, v, x, y, phi, W, b, S, z, loss buffers and the workspace
+ *   are DEVICE pointers on the current CUDA device and must be 16-byte
+ *   aligned (HH_ERR_ALIGNMENT otherwise).  ``stream`` is a cudaStream_t
+ *   (NULL = legacy default stream).
+ * - Asynchrony: every call validates its arguments on the host, enqueues its
+ *   kernels on ``stream`` and returns.  HH_OK means "validated and
+ *   enqueued"; a launch failure returns HH_ERR_CUDA.  Nothing is launched
+ *   when validation fails.
+ * - Layouts (row-major, contiguous):
+ *     q, k, v, y, x    [B][H][n][d]         (decode: [B][H][d])
+ *     W                [H][d][d]            W[h][k][l]: input k -> output l, h = x W + b
+ *     b                [H][d]  float32      (NULL = zero bias)
+ *     phi              [B][H][n][d'p]
+ *     S                [B][H][d'p][d] float32,  z  [B][H][d'p] float32
+ *     loss_rows        [B][H][n] float32,   loss_head_sum [B][H] float32
+ *   d'p is hh_fmap_dim(kind, d, 1): 2d for Hedgehog, 1+d+d^2 rounded up
+ *   to a multiple of 32 for Taylor (273 -> 288 at d = 16).  Padding
+ *   features are identically zero.
+ * - Types: HH_F32 means q, k, v, x, W, y, phi are float32; HH_BF16 means
+ *   they are bfloat16 (round-to-nearest-even outputs).  b, S, z and loss
+ *   buffers are always float32.  Arithmetic is float32 (tensor-core
+ *   operands in bfloat16 for HH_BF16).
+ * - Supported shapes: Hedgehog d in {64, 128}; Taylor d = 16; any
+ *   HH_F32 call additionally accepts Hedgehog 1 <= d <= 128 and Taylor
+ *   1 <= d <= 16.  B, n >= 0 (an empty problem launches nothing), H >= 1.
+ * - Numerical domain: the exponential is not clamped; |xW + b| beyond ~80
+ *   overflows float32 and produces inf/NaN (outside the supported domain).
+ * - Device-detected problems: kernels that wait on asynchronous copies or
+ *   tensor-core operations bound every wait in time.  When a wait passes
+ *   its soft limit the kernel stores HH_ERR_TIMEOUT into ``*dev_status``
+ *   (when that pointer is non-NULL) and keeps waiting up to a hard limit;
+ *   past the hard limit it abandons the work, releases its tensor memory
+ *   and returns.  The caller reads ``*dev_status`` after synchronising.
+ *   The environment variable HH_WAIT_SOFT_LIMIT_NS overrides the soft
+ *   limit (default 1e9 ns) for testing.
+ * - No C++ exception crosses this interface.
+ */
+#ifndef HH_H_
+#define HH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HH_API __attribute__((visibility("default")))
+#else
+#define HH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HH_OK = 0,
+  HH_ERR_INVALID_ARG = 1,  /* null pointer, negative size, overflow, unknown enum  */
+  HH_ERR_UNSUPPORTED = 2,  /* valid but not implemented: head dim, chunk, device   */
+  HH_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned                     */
+  HH_ERR_WORKSPACE = 4,    /* workspace missing or smaller than the queried size   */
+  HH_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed                    */
+  HH_ERR_TIMEOUT = 6       /* device-side: a bounded wait passed its limit         */
+} hh_status;
+
+typedef enum { HH_F32 = 0, HH_BF16 = 1 } hh_dtype;
+
+typedef enum { HH_FMAP_HEDGEHOG = 0, HH_FMAP_TAYLOR2 = 1 } hh_fmap_kind;
+
+/* A per-layer feature map.  For Hedgehog, Wq/bq map the queries and Wk/bk
+ * the keys; Wk == NULL means the keys share Wq/bq (one map per head used for
+ * both queries and keys, as the pages describe).  Taylor ignores W and b. */
+typedef struct {
+  int32_t kind;        /* hh_fmap_kind                                      */
+  int32_t d;           /* head dimension                                    */
+  const void* Wq;      /* [H][d][d] in the call's dtype (Hedgehog only)     */
+  const float* bq;     /* [H][d] float32 or NULL                            */
+  const void* Wk;      /* [H][d][d] or NULL (shared with Wq)                */
+  const float* bk;     /* [H][d] or NULL; ignored when Wk is NULL           */
+} hh_fmap;
+
+/* Library version, major*10000 + minor*100 + patch. */
+HH_API int hh_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+HH_API const char* hh_status_str(int status);
+
+/* Feature dimension d' of a map: 2d (Hedgehog) or 1+d+d^2 (Taylor, the
+ * count printed in "The Taylor Exponential as a Bridge Result").  With
+ * padded != 0 the Taylor count is rounded up to a multiple of 32.  Returns
+ * -1 for an unknown kind or d < 1. */
+HH_API int hh_fmap_dim(int kind, int d, int padded);
+
+/* phi(x) for every row of x.
+ * Source: "The Hedgehog MLP Feature Map", Choices 1 and 3 (Hedgehog);
+ * "The Taylor Exponential as a Bridge Result" (Taylor).
+ * x: [B][H][n][d] (dtype); is_key selects Wk/bk instead of Wq/bq;
+ * phi_out: [B][H][n][d'p] (dtype), fully overwritten including padding.
+ * Hedgehog output order: feature l < d is exp(h_l), feature d + l is exp(-h_l). */
+HH_API hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, int is_key,
+                         int64_t B, int H, int64_t n, void* phi_out, void* stream);
+
+/* Bytes of device workspace hh_linattn_fwd_causal needs for this problem
+ * on the current device (0 when none).  Returns 0 for invalid arguments. */
+HH_API size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
+                              int chunk);
+
+/* Causal linear attention over whole sequences (chunked prefill).
+ * Source: section 2 (paper Eq. 2) for y; "Complexity Analysis" for the
+ * running sums S_i = sum_{j<=i} phi(k_j)^T v_j and z_i = sum_{j<=i} phi(k_j).
+ * q, k, v: [B][H][n][d] (dtype); y: [B][H][n][d] (dtype), overwritten.
+ * chunk: 0 (library default), 64 or 128 -- the intra-chunk block length of
+ * the chunked evaluation; the result is the same causal sum for any value.
+ * S_out / z_out: NULL, or [B][H][d'p][d] / [B][H][d'p] float32 receiving the
+ * state after the last token (S_n, z_n), the input of
+ * hh_linattn_decode_step.  Both or neither must be given.
+ * workspace: device scratch of at least hh_fwd_workspace_bytes(...) bytes
+ * (may be NULL when that is 0); its contents on entry are ignored.
+ * dev_status: NULL or a device int the kernels may set to HH_ERR_TIMEOUT. */
+HH_API hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                const void* v, int64_t B, int H, int64_t n, int chunk, void* y,
+                                float* S_out, float* z_out, void* workspace, size_t ws_bytes,
+                                int* dev_status, void* stream);
+
+/* One recurrent decode step for B sequences x H heads.
+ * Source: "Complexity Analysis" (running sums S and z, output
+ * phi(q_t) S_t / phi(q_t).z_t); the state after the step includes token t.
+ * q, k, v: [B][H][d] (dtype); S: [B][H][d'p][d] float32 and z: [B][H][d'p]
+ * float32 are read and updated in place; y: [B][H][d] (dtype), overwritten.
+ * Element order of every floating-point sum is fixed (deterministic). */
+HH_API hh_status hh_linattn_decode_step(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                 const void* v, int64_t B, int H, float* S, float* z, void* y,
+                                 void* stream);
+
+/* Bytes of device workspace hh_mimicry_loss needs (0 when none). */
+HH_API size_t hh_loss_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n);
+
+/* Attention-weight distillation cross-entropy (paper Eq. 4) per query.
+ * Source: "The Attention Weight Distillation Loss".  Target: causal
+ * softmax(q k^T / sqrt d); prediction: a_ij / sum_{m<=i} a_im with
+ * a_ij = phi(q_i).phi(k_j); natural logarithm.
+ * q, k: [B][H][n][d] (dtype).  loss_rows: NULL or [B][H][n] float32
+ * receiving L_i; loss_head_sum: [B][H] float32 receiving sum_i L_i (summed in
+ * a fixed order).  workspace: at least hh_loss_workspace_bytes(...) bytes. */
+HH_API hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                          int64_t B, int H, int64_t n, float* loss_rows, float* loss_head_sum,
+                          void* workspace, size_t ws_bytes, int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HH_H_ */

@@ -1,0 +1,163 @@
+"""Thin PyTorch binding of the C ABI: same names, argument marshalling only.
+
+Tensors supply device memory and streams; every step of the computation runs
+in the library's CUDA kernels.  Output buffers and workspaces are allocated
+here with torch (the library itself never allocates) unless passed in.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _abi
+
+__all__ = ["FeatureMap", "fmap_dim", "feature_map", "fwd_workspace_bytes",
+           "linattn_fwd_causal", "linattn_decode_step", "loss_workspace_bytes",
+           "mimicry_loss", "HHError"]
+
+HHError = _abi.HHError
+
+_DTYPES = {torch.float32: _abi.HH_F32, torch.bfloat16: _abi.HH_BF16}
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16") from None
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be CUDA device tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class FeatureMap:
+    """A per-layer feature map: kind "hedgehog" (W [H,d,d], b [H,d]) or "taylor2"."""
+    kind: str
+    d: int
+    Wq: Optional[torch.Tensor] = None
+    bq: Optional[torch.Tensor] = None
+    Wk: Optional[torch.Tensor] = None
+    bk: Optional[torch.Tensor] = None
+
+    @property
+    def kind_id(self) -> int:
+        return {"hedgehog": _abi.HH_FMAP_HEDGEHOG, "taylor2": _abi.HH_FMAP_TAYLOR2}[self.kind]
+
+    def struct(self) -> _abi.HHFmap:
+        s = _abi.HHFmap()
+        s.kind = self.kind_id
+        s.d = self.d
+        s.Wq = _ptr(self.Wq)
+        s.bq = _ptr(self.bq)
+        s.Wk = _ptr(self.Wk)
+        s.bk = _ptr(self.bk)
+        return s
+
+    def dim(self, padded: bool = True) -> int:
+        return fmap_dim(self.kind, self.d, padded)
+
+
+def fmap_dim(kind: str, d: int, padded: bool = True) -> int:
+    k = {"hedgehog": _abi.HH_FMAP_HEDGEHOG, "taylor2": _abi.HH_FMAP_TAYLOR2}[kind]
+    return int(_abi.lib().hh_fmap_dim(k, int(d), int(bool(padded))))
+
+
+def feature_map(fm: FeatureMap, x: torch.Tensor, is_key: bool = False,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """phi(x) for x [B, H, n, d] -> [B, H, n, d'p] (hh_feature_map)."""
+    B, H, n, d = x.shape
+    if out is None:
+        out = torch.empty(B, H, n, fm.dim(), dtype=x.dtype, device=x.device)
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_feature_map(ctypes.byref(s), _dt(x), _ptr(x), int(is_key), B, H, n,
+                                         _ptr(out), _stream(stream)), "hh_feature_map")
+    return out
+
+
+def fwd_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int,
+                        chunk: int = 0) -> int:
+    s = fm.struct()
+    return int(_abi.lib().hh_fwd_workspace_bytes(ctypes.byref(s), _DTYPES[dtype], B, H, n, chunk))
+
+
+def linattn_fwd_causal(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       chunk: int = 0, y: Optional[torch.Tensor] = None,
+                       return_state: bool = False, workspace: Optional[torch.Tensor] = None,
+                       dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Causal linear attention (hh_linattn_fwd_causal).
+
+    Returns y, or (y, S, z) with ``return_state``: S [B,H,d'p,d] and
+    z [B,H,d'p] float32 hold the state after the last token.
+    """
+    B, H, n, d = q.shape
+    if y is None:
+        y = torch.empty_like(q)
+    S = z = None
+    if return_state:
+        S = torch.empty(B, H, fm.dim(), d, dtype=torch.float32, device=q.device)
+        z = torch.empty(B, H, fm.dim(), dtype=torch.float32, device=q.device)
+    need = fwd_workspace_bytes(fm, q.dtype, B, H, n, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_linattn_fwd_causal(
+        ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), _ptr(v), B, H, n, chunk, _ptr(y), _ptr(S),
+        _ptr(z), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
+        "hh_linattn_fwd_causal")
+    return (y, S, z) if return_state else y
+
+
+def linattn_decode_step(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        S: torch.Tensor, z: torch.Tensor, y: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """One decode step for q, k, v [B, H, d]; updates S, z in place (hh_linattn_decode_step)."""
+    B, H, d = q.shape
+    if y is None:
+        y = torch.empty_like(q)
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_linattn_decode_step(
+        ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), _ptr(v), B, H, _ptr(S), _ptr(z), _ptr(y),
+        _stream(stream)), "hh_linattn_decode_step")
+    return y
+
+
+def loss_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int) -> int:
+    s = fm.struct()
+    return int(_abi.lib().hh_loss_workspace_bytes(ctypes.byref(s), _DTYPES[dtype], B, H, n))
+
+
+def mimicry_loss(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, return_rows: bool = True,
+                 workspace: Optional[torch.Tensor] = None,
+                 dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Distillation cross-entropy (hh_mimicry_loss): returns (rows [B,H,n] or None, head_sum [B,H])."""
+    B, H, n, d = q.shape
+    rows = torch.empty(B, H, n, dtype=torch.float32, device=q.device) if return_rows else None
+    head = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    need = loss_workspace_bytes(fm, q.dtype, B, H, n)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_mimicry_loss(
+        ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), B, H, n, _ptr(rows), _ptr(head),
+        _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)), "hh_mimicry_loss")
+    return rows, head

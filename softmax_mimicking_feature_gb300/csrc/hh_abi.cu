@@ -1,0 +1,264 @@
+// C ABI entry points: argument validation, workspace sizing and dispatch to
+// the kernels.  Every check happens on the host before anything is enqueued.
+
+#include <stdlib.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "hh_internal.cuh"
+
+namespace hh {
+
+// ---- cached device attributes ---------------------------------------------
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+int g_smem_optin[kMaxDevices];
+int g_cc[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
+
+void query_device(int dev) {
+  std::call_once(g_once[dev], [dev] {
+    int v = 0;
+    g_sm_count[dev] = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? v : 1;
+    g_smem_optin[dev] =
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess ? v : 48 * 1024;
+    int ma = 0, mi = 0;
+    cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev);
+    g_cc[dev] = ma * 10 + mi;
+  });
+}
+}  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  query_device(dev);
+  return g_sm_count[dev];
+}
+int device_max_smem_optin() {
+  const int dev = current_device();
+  query_device(dev);
+  return g_smem_optin[dev];
+}
+static int device_cc() {
+  const int dev = current_device();
+  query_device(dev);
+  return g_cc[dev];
+}
+
+uint64_t wait_soft_limit_ns() {
+  const char* e = getenv("HH_WAIT_SOFT_LIMIT_NS");
+  if (e && *e) return strtoull(e, nullptr, 10);
+  return 1000000000ull;
+}
+
+// ---- validation -----------------------------------------------------------
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Fills *p from the ABI arguments; checks shapes, kinds, overflow.
+hh_status make_problem(const hh_fmap* fm, int dtype, int64_t B, int H, int64_t n, Problem* p) {
+  if (!fm) return HH_ERR_INVALID_ARG;
+  if (dtype != HH_F32 && dtype != HH_BF16) return HH_ERR_INVALID_ARG;
+  if (fm->kind != HH_FMAP_HEDGEHOG && fm->kind != HH_FMAP_TAYLOR2) return HH_ERR_INVALID_ARG;
+  if (B < 0 || n < 0 || H < 1 || fm->d < 1) return HH_ERR_INVALID_ARG;
+  const int d = fm->d;
+  if (fm->kind == HH_FMAP_HEDGEHOG) {
+    const bool ok = dtype == HH_F32 ? (d <= 128) : (d == 64 || d == 128);
+    if (!ok) return HH_ERR_UNSUPPORTED;
+    if (!fm->Wq) return HH_ERR_INVALID_ARG;
+  } else {
+    const bool ok = dtype == HH_F32 ? (d <= 16) : (d == 16);
+    if (!ok) return HH_ERR_UNSUPPORTED;
+  }
+  // element counts must fit comfortably in int64 and index math
+  const int64_t lim = (int64_t)1 << 40;
+  if (B > lim || n > lim || (B && n && B * (int64_t)H > lim / std::max<int64_t>(n, 1)) ||
+      B * (int64_t)H * n > lim / 512)
+    return HH_ERR_INVALID_ARG;
+  p->kind = fm->kind;
+  p->dtype = dtype;
+  p->d = d;
+  p->dp = hh_fmap_dim(fm->kind, d, 0);
+  p->dpp = hh_fmap_dim(fm->kind, d, 1);
+  p->B = B;
+  p->H = H;
+  p->n = n;
+  if (fm->kind == HH_FMAP_HEDGEHOG) {
+    p->Wq = fm->Wq;
+    p->bq = fm->bq;
+    p->Wk = fm->Wk;
+    p->bk = fm->Wk ? fm->bk : nullptr;
+  } else {
+    p->Wq = p->Wk = nullptr;
+    p->bq = p->bk = nullptr;
+  }
+  return HH_OK;
+}
+
+hh_status check_ptrs_aligned(std::initializer_list<const void*> ptrs) {
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return HH_ERR_ALIGNMENT;
+  return HH_OK;
+}
+
+hh_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HH_OK : HH_ERR_CUDA; }
+
+size_t elem_size(int dtype) { return dtype == HH_F32 ? 4 : 2; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool device_ok() {
+  // sm_103a code only; anything else is reported, not attempted
+  return device_cc() == 103;
+}
+
+// Loss workspace: phi(Q), phi(K) in the call's dtype, then per-tile partial sums.
+size_t loss_ws(const Problem& p) {
+  const size_t phi = align256((size_t)p.B * p.H * p.n * p.dpp * elem_size(p.dtype));
+  const size_t part = align256((size_t)p.B * p.H * ceil_div(p.n, loss_simt_tile()) * sizeof(float));
+  return 2 * phi + part;
+}
+
+}  // namespace
+}  // namespace hh
+
+using namespace hh;
+
+extern "C" {
+
+int hh_version(void) { return 100; }
+
+const char* hh_status_str(int s) {
+  switch (s) {
+    case HH_OK: return "HH_OK";
+    case HH_ERR_INVALID_ARG: return "HH_ERR_INVALID_ARG";
+    case HH_ERR_UNSUPPORTED: return "HH_ERR_UNSUPPORTED";
+    case HH_ERR_ALIGNMENT: return "HH_ERR_ALIGNMENT";
+    case HH_ERR_WORKSPACE: return "HH_ERR_WORKSPACE";
+    case HH_ERR_CUDA: return "HH_ERR_CUDA";
+    case HH_ERR_TIMEOUT: return "HH_ERR_TIMEOUT";
+    default: return "HH_ERR_UNKNOWN";
+  }
+}
+
+int hh_fmap_dim(int kind, int d, int padded) {
+  if (d < 1) return -1;
+  if (kind == HH_FMAP_HEDGEHOG) return 2 * d;
+  if (kind == HH_FMAP_TAYLOR2) {
+    const int dp = 1 + d + d * d;
+    return padded ? (dp + 31) / 32 * 32 : dp;
+  }
+  return -1;
+}
+
+hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, int is_key, int64_t B,
+                         int H, int64_t n, void* phi_out, void* stream) {
+  Problem p;
+  hh_status st = make_problem(fmap, dtype, B, H, n, &p);
+  if (st != HH_OK) return st;
+  if (B * H * n == 0) return HH_OK;
+  if (!x || !phi_out) return HH_ERR_INVALID_ARG;
+  const void* W = is_key && p.Wk ? p.Wk : p.Wq;
+  const float* b = is_key && p.Wk ? p.bk : p.bq;
+  if ((st = check_ptrs_aligned({x, phi_out, W, b})) != HH_OK) return st;
+  if (!device_ok()) return HH_ERR_UNSUPPORTED;
+  return cuda_status(launch_fmap_simt(p, x, is_key, phi_out, (cudaStream_t)stream));
+}
+
+size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
+                              int chunk) {
+  Problem p;
+  if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
+  (void)chunk;
+  return 0;
+}
+
+hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                const void* v, int64_t B, int H, int64_t n, int chunk, void* y,
+                                float* S_out, float* z_out, void* workspace, size_t ws_bytes,
+                                int* dev_status, void* stream) {
+  Problem p;
+  hh_status st = make_problem(fmap, dtype, B, H, n, &p);
+  if (st != HH_OK) return st;
+  if (chunk != 0 && chunk != 64 && chunk != 128) return HH_ERR_UNSUPPORTED;
+  if ((S_out == nullptr) != (z_out == nullptr)) return HH_ERR_INVALID_ARG;
+  if (B == 0) return HH_OK;
+  if (n > 0 && (!q || !k || !v || !y)) return HH_ERR_INVALID_ARG;
+  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, p.Wq, p.bq, p.Wk, p.bk, workspace,
+                                dev_status})) != HH_OK)
+    return st;
+  const size_t need = hh_fwd_workspace_bytes(fmap, dtype, B, H, n, chunk);
+  if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
+  if (!device_ok()) return HH_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (n == 0) {
+    // empty sequences: the state is the empty sum
+    if (S_out) {
+      cudaError_t e = cudaMemsetAsync(S_out, 0, sizeof(float) * B * H * p.dpp * p.d, s);
+      if (e == cudaSuccess) e = cudaMemsetAsync(z_out, 0, sizeof(float) * B * H * p.dpp, s);
+      return cuda_status(e);
+    }
+    return HH_OK;
+  }
+  return cuda_status(launch_prefill_simt(p, q, k, v, y, S_out, z_out, s));
+}
+
+hh_status hh_linattn_decode_step(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                 const void* v, int64_t B, int H, float* S, float* z, void* y,
+                                 void* stream) {
+  Problem p;
+  hh_status st = make_problem(fmap, dtype, B, H, 1, &p);
+  if (st != HH_OK) return st;
+  if (B == 0) return HH_OK;
+  if (!q || !k || !v || !S || !z || !y) return HH_ERR_INVALID_ARG;
+  if ((st = check_ptrs_aligned({q, k, v, S, z, y, p.Wq, p.bq, p.Wk, p.bk})) != HH_OK) return st;
+  if (!device_ok()) return HH_ERR_UNSUPPORTED;
+  return cuda_status(launch_decode(p, q, k, v, S, z, y, (cudaStream_t)stream));
+}
+
+size_t hh_loss_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n) {
+  Problem p;
+  if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
+  if (B * H * n == 0) return 0;
+  return loss_ws(p);
+}
+
+hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const void* k, int64_t B,
+                          int H, int64_t n, float* loss_rows, float* loss_head_sum,
+                          void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+  Problem p;
+  hh_status st = make_problem(fmap, dtype, B, H, n, &p);
+  if (st != HH_OK) return st;
+  if (B == 0) return HH_OK;
+  if (!loss_head_sum) return HH_ERR_INVALID_ARG;
+  if (n > 0 && (!q || !k)) return HH_ERR_INVALID_ARG;
+  if ((st = check_ptrs_aligned({q, k, loss_rows, loss_head_sum, p.Wq, p.bq, p.Wk, p.bk,
+                                workspace, dev_status})) != HH_OK)
+    return st;
+  const size_t need = hh_loss_workspace_bytes(fmap, dtype, B, H, n);
+  if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
+  if (!device_ok()) return HH_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (n == 0) return cuda_status(cudaMemsetAsync(loss_head_sum, 0, sizeof(float) * B * H, s));
+  char* ws = (char*)workspace;
+  const size_t phi_bytes = align256((size_t)B * H * n * p.dpp * elem_size(dtype));
+  void* phq = ws;
+  void* phk = ws + phi_bytes;
+  float* partial = (float*)(ws + 2 * phi_bytes);
+  cudaError_t e = launch_fmap_simt(p, q, 0, phq, s);
+  if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, s);
+  if (e == cudaSuccess)
+    e = launch_loss_simt(p, q, k, phq, phk, loss_rows, partial, loss_simt_tile(), loss_head_sum, s);
+  return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hh.h"
+
+namespace hh {
+
+// A validated problem description handed from the ABI layer to launchers.
+struct Problem {
+  int kind;        // hh_fmap_kind
+  int dtype;       // hh_dtype
+  int d;           // head dim
+  int dp;          // unpadded feature dim
+  int dpp;         // padded feature dim (row length of phi and S)
+  int64_t B;
+  int H;
+  int64_t n;
+  const void* Wq;
+  const float* bq;
+  const void* Wk;
+  const float* bk;
+};
+
+// ---- element access in float32 for either storage type -------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// 1/sqrt(2) rounded to float32: the Taylor map's pair scale.
+constexpr float kInvSqrt2 = 0.70710678118654752440f;
+
+inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Cached device attributes (the only state the library keeps).
+int device_sm_count();
+int device_max_smem_optin();
+// Soft wait limit for device-side bounded waits, from HH_WAIT_SOFT_LIMIT_NS.
+uint64_t wait_soft_limit_ns();
+
+// ---- launchers (return cudaSuccess or the launch error) ------------------
+// SIMT kernels: float32 arithmetic, any supported d; T = float or bf16.
+cudaError_t launch_fmap_simt(const Problem& p, const void* x, int is_key, void* phi,
+                             cudaStream_t s);
+cudaError_t launch_prefill_simt(const Problem& p, const void* q, const void* k, const void* v,
+                                void* y, float* S_out, float* z_out, cudaStream_t s);
+cudaError_t launch_loss_simt(const Problem& p, const void* q, const void* k, const void* phq,
+                             const void* phk, float* loss_rows, float* partial, int tile,
+                             float* head_sum, cudaStream_t s);
+int loss_simt_tile();
+
+// Decode step (SIMT, HBM-streaming).
+cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
+                          float* S, float* z, void* y, cudaStream_t s);
+
+}  // namespace hh

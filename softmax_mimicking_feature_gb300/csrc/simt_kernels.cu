@@ -1,0 +1,387 @@
+// Float32 CUDA-core kernels: feature map, chunked causal prefill and the
+// mimicry loss.  These carry the float32 workloads (1e-5 parity), where the
+// tensor cores' bf16/tf32 operands would not be precise enough, and accept
+// any head dimension up to 128 (Taylor: up to 16).
+//
+// Math follows "The Hedgehog & the Porcupine" summary: Choices 1/3 of "The
+// Hedgehog MLP Feature Map", "The Taylor Exponential as a Bridge Result",
+// section 2 / paper Eq. 2 and "Complexity Analysis" for the causal output,
+// and "The Attention Weight Distillation Loss" (paper Eq. 4).
+
+#include <math.h>
+
+#include "hh_internal.cuh"
+
+namespace hh {
+namespace {
+
+constexpr int kThreads = 256;
+
+// phi of one row held in shared memory (xs[0..d)), written to out[0..dpp).
+// Hedgehog: out[l] = exp(h_l), out[d+l] = exp(-h_l), h = x W + b.
+// Taylor: [1, x, x_i x_j / sqrt2 (i-major)], zero padding.
+template <typename T>
+__device__ __forceinline__ void phi_row(int kind, int d, int dpp, const float* xs, const T* W,
+                                        const float* b, float* out, int lane, int nlanes) {
+  if (kind == HH_FMAP_HEDGEHOG) {
+    for (int l = lane; l < d; l += nlanes) {
+      float h = b ? b[l] : 0.f;
+      for (int k = 0; k < d; ++k) h = fmaf(xs[k], to_f(W[(size_t)k * d + l]), h);
+      out[l] = expf(h);
+      out[d + l] = expf(-h);
+    }
+  } else {
+    for (int f = lane; f < dpp; f += nlanes) {
+      float val;
+      if (f == 0) {
+        val = 1.f;
+      } else if (f <= d) {
+        val = xs[f - 1];
+      } else if (f <= d + d * d) {
+        int p = f - 1 - d;
+        val = xs[p / d] * xs[p % d] * kInvSqrt2;
+      } else {
+        val = 0.f;
+      }
+      out[f] = val;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Feature map: one block per group of rows; one warp per row.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* __restrict__ bias,
+                 T* __restrict__ phi, int kind, int d, int dpp, int H, int64_t n, int64_t rows) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = kThreads / 32;
+  float* xs = sm + warp * (128 + 320);
+  float* out = xs + 128;
+  for (int64_t r = (int64_t)blockIdx.x * nwarps + warp; r < rows; r += (int64_t)gridDim.x * nwarps) {
+    const int h = (int)((r / n) % H);
+    for (int k = lane; k < d; k += 32) xs[k] = to_f(x[r * d + k]);
+    __syncwarp();
+    const T* Wh = W ? W + (size_t)h * d * d : nullptr;
+    const float* bh = bias ? bias + (size_t)h * d : nullptr;
+    phi_row<T>(kind, d, dpp, xs, Wh, bh, out, lane, 32);
+    __syncwarp();
+    for (int f = lane; f < dpp; f += 32) phi[r * dpp + f] = from_f<T>(out[f]);
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Chunked causal prefill: one block per (batch, head); chunks of C tokens.
+//   A = tril(phi(Q_c) phi(K_c)^T);  y = (A V_c + phi(Q_c) S) / (rowsum A + phi(Q_c) z)
+//   S += phi(K_c)^T V_c;  z += phi(K_c)^T 1
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                    T* __restrict__ y, float* __restrict__ S_out, float* __restrict__ z_out,
+                    const T* __restrict__ Wq, const float* __restrict__ bq,
+                    const T* __restrict__ Wk, const float* __restrict__ bk, int kind, int d,
+                    int dpp, int H, int64_t n, int C) {
+  extern __shared__ float sm[];
+  float* S = sm;                       // [dpp][d]
+  float* z = S + (size_t)dpp * d;      // [dpp]
+  float* phq = z + dpp;                // [C][dpp]
+  float* phk = phq + (size_t)C * dpp;  // [C][dpp]
+  float* vv = phk + (size_t)C * dpp;   // [C][d]
+  float* A = vv + (size_t)C * d;       // [C][C]
+  float* xs = A + (size_t)C * C;       // [C][d]  raw rows
+  float* xk = xs + (size_t)C * d;      // [C][d]
+  float* den = xk + (size_t)C * d;     // [C]
+
+  const int64_t bh = blockIdx.x;
+  const int h = (int)(bh % H);
+  const size_t base = (size_t)bh * n * d;
+  const T* Wqh = Wq ? Wq + (size_t)h * d * d : nullptr;
+  const T* Wkh = Wk ? Wk + (size_t)h * d * d : nullptr;
+  const float* bqh = bq ? bq + (size_t)h * d : nullptr;
+  const float* bkh = bk ? bk + (size_t)h * d : nullptr;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  for (int i = tid; i < dpp * d; i += kThreads) S[i] = 0.f;
+  for (int i = tid; i < dpp; i += kThreads) z[i] = 0.f;
+  __syncthreads();
+
+  for (int64_t c0 = 0; c0 < n; c0 += C) {
+    const int nc = (int)min((int64_t)C, n - c0);
+    for (int i = tid; i < C * d; i += kThreads) {
+      const int r = i / d;
+      const bool ok = r < nc;
+      xs[i] = ok ? to_f(q[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
+      xk[i] = ok ? to_f(k[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
+      vv[i] = ok ? to_f(v[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
+    }
+    __syncthreads();
+    for (int r = warp; r < C; r += kThreads / 32) {
+      phi_row<T>(kind, d, dpp, xs + (size_t)r * d, Wqh, bqh, phq + (size_t)r * dpp, lane, 32);
+      phi_row<T>(kind, d, dpp, xk + (size_t)r * d, Wkh, bkh, phk + (size_t)r * dpp, lane, 32);
+      if (r >= nc)  // ragged tail: padded keys contribute nothing
+        for (int f = lane; f < dpp; f += 32) phk[(size_t)r * dpp + f] = 0.f;
+    }
+    __syncthreads();
+    for (int i = tid; i < C * C; i += kThreads) {
+      const int r = i / C, j = i % C;
+      float a = 0.f;
+      if (j <= r)
+        for (int f = 0; f < dpp; ++f) a = fmaf(phq[(size_t)r * dpp + f], phk[(size_t)j * dpp + f], a);
+      A[i] = a;
+    }
+    __syncthreads();
+    for (int r = tid; r < C; r += kThreads) {
+      float dn = 0.f;
+      for (int j = 0; j <= r; ++j) dn += A[r * C + j];
+      float di = 0.f;
+      for (int f = 0; f < dpp; ++f) di = fmaf(phq[(size_t)r * dpp + f], z[f], di);
+      den[r] = dn + di;
+    }
+    __syncthreads();
+    for (int i = tid; i < nc * d; i += kThreads) {
+      const int r = i / d, c = i % d;
+      float num = 0.f;
+      for (int j = 0; j <= r; ++j) num = fmaf(A[r * C + j], vv[j * d + c], num);
+      float ni = 0.f;
+      for (int f = 0; f < dpp; ++f) ni = fmaf(phq[(size_t)r * dpp + f], S[(size_t)f * d + c], ni);
+      y[base + (size_t)(c0 + r) * d + c] = from_f<T>((num + ni) / den[r]);
+    }
+    __syncthreads();
+    for (int i = tid; i < dpp * d; i += kThreads) {
+      const int f = i / d, c = i % d;
+      float acc = 0.f;
+      for (int j = 0; j < nc; ++j) acc = fmaf(phk[(size_t)j * dpp + f], vv[j * d + c], acc);
+      S[i] += acc;
+    }
+    for (int f = tid; f < dpp; f += kThreads) {
+      float acc = 0.f;
+      for (int j = 0; j < nc; ++j) acc += phk[(size_t)j * dpp + f];
+      z[f] += acc;
+    }
+    __syncthreads();
+  }
+  if (S_out) {
+    for (int i = tid; i < dpp * d; i += kThreads) S_out[(size_t)bh * dpp * d + i] = S[i];
+    for (int i = tid; i < dpp; i += kThreads) z_out[(size_t)bh * dpp + i] = z[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Mimicry loss: one block per (batch*head, tile of 64 queries).  Four threads
+// share a query row; each keeps an online-softmax state over its keys:
+//   M = running max of s, Z = sum e^{s-M}, T = sum e^{s-M} log a, A = sum a
+// and the row's loss is log A - T / Z (= -sum_j p_j log(a_j / A)).
+// ---------------------------------------------------------------------------
+constexpr int kLossRows = 64;
+constexpr int kLossKeys = 32;
+
+struct OnlineCE {
+  float M, Z, T, A;
+};
+
+__device__ __forceinline__ OnlineCE ce_merge(OnlineCE x, OnlineCE y) {
+  OnlineCE r;
+  r.M = fmaxf(x.M, y.M);
+  const float fx = (x.M == -INFINITY) ? 0.f : expf(x.M - r.M);
+  const float fy = (y.M == -INFINITY) ? 0.f : expf(y.M - r.M);
+  r.Z = x.Z * fx + y.Z * fy;
+  r.T = x.T * fx + y.T * fy;
+  r.A = x.A + y.A;
+  return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
+                 const T* __restrict__ phk, float* __restrict__ loss_rows,
+                 float* __restrict__ partial, int d, int dpp, int64_t n, int ntiles) {
+  extern __shared__ float sm[];
+  float* qs = sm;                                  // [64][d]
+  float* pq = qs + kLossRows * d;                  // [64][dpp]
+  float* ks = pq + (size_t)kLossRows * dpp;        // [32][d]
+  float* pk = ks + kLossKeys * d;                  // [32][dpp]
+  float* rowL = pk + (size_t)kLossKeys * dpp;      // [64]
+
+  const int64_t bh = blockIdx.x / ntiles;
+  const int tile = (int)(blockIdx.x % ntiles);
+  const int64_t r0 = (int64_t)tile * kLossRows;
+  const int tid = threadIdx.x;
+  const int row = tid >> 2, part = tid & 3;
+  const int64_t i = r0 + row;
+  const float scale = rsqrtf((float)d);
+
+  for (int e = tid; e < kLossRows * d; e += kThreads) {
+    const int64_t rr = r0 + e / d;
+    qs[e] = rr < n ? to_f(q[((size_t)bh * n + rr) * d + e % d]) : 0.f;
+  }
+  for (int e = tid; e < kLossRows * dpp; e += kThreads) {
+    const int64_t rr = r0 + e / dpp;
+    pq[e] = rr < n ? to_f(phq[((size_t)bh * n + rr) * dpp + e % dpp]) : 0.f;
+  }
+  OnlineCE st = {-INFINITY, 0.f, 0.f, 0.f};
+  const int64_t last = min(n, r0 + kLossRows) - 1;
+  for (int64_t k0 = 0; k0 <= last; k0 += kLossKeys) {
+    __syncthreads();
+    for (int e = tid; e < kLossKeys * d; e += kThreads) {
+      const int64_t j = k0 + e / d;
+      ks[e] = j < n ? to_f(k[((size_t)bh * n + j) * d + e % d]) : 0.f;
+    }
+    for (int e = tid; e < kLossKeys * dpp; e += kThreads) {
+      const int64_t j = k0 + e / dpp;
+      pk[e] = j < n ? to_f(phk[((size_t)bh * n + j) * dpp + e % dpp]) : 0.f;
+    }
+    __syncthreads();
+    if (i < n) {
+      for (int jj = 0; jj < kLossKeys / 4; ++jj) {
+        const int jl = part * (kLossKeys / 4) + jj;
+        const int64_t j = k0 + jl;
+        if (j > i) break;
+        float s = 0.f, a = 0.f;
+        for (int t = 0; t < d; ++t) s = fmaf(qs[row * d + t], ks[jl * d + t], s);
+        for (int f = 0; f < dpp; ++f) a = fmaf(pq[(size_t)row * dpp + f], pk[(size_t)jl * dpp + f], a);
+        s *= scale;
+        if (s > st.M) {
+          const float c = (st.M == -INFINITY) ? 0.f : expf(st.M - s);
+          st.Z *= c;
+          st.T *= c;
+          st.M = s;
+        }
+        const float e = expf(s - st.M);
+        st.Z += e;
+        st.T = fmaf(e, logf(a), st.T);
+        st.A += a;
+      }
+    }
+  }
+  // merge the four partial states of a row (adjacent lanes)
+  for (int off = 1; off < 4; off <<= 1) {
+    OnlineCE o;
+    o.M = __shfl_xor_sync(0xffffffffu, st.M, off);
+    o.Z = __shfl_xor_sync(0xffffffffu, st.Z, off);
+    o.T = __shfl_xor_sync(0xffffffffu, st.T, off);
+    o.A = __shfl_xor_sync(0xffffffffu, st.A, off);
+    st = ce_merge(st, o);
+  }
+  if (part == 0) {
+    const float L = (i < n) ? (logf(st.A) - st.T / st.Z) : 0.f;
+    rowL[row] = L;
+    if (loss_rows && i < n) loss_rows[(size_t)bh * n + i] = L;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int r = 0; r < kLossRows; ++r) acc += rowL[r];
+    partial[(size_t)bh * ntiles + tile] = acc;
+  }
+}
+
+// Per-head sum of the per-tile partial sums, in tile order.
+__global__ void sum_partials_kernel(const float* __restrict__ partial, float* __restrict__ out,
+                                    int64_t heads, int ntiles) {
+  const int64_t bh = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (bh >= heads) return;
+  float acc = 0.f;
+  for (int t = 0; t < ntiles; ++t) acc += partial[(size_t)bh * ntiles + t];
+  out[bh] = acc;
+}
+
+size_t prefill_smem_bytes(int d, int dpp, int C) {
+  return sizeof(float) * ((size_t)dpp * d + dpp + 2 * (size_t)C * dpp + (size_t)C * d +
+                          (size_t)C * C + 2 * (size_t)C * d + C);
+}
+
+}  // namespace
+
+int loss_simt_tile() { return kLossRows; }
+
+template <typename T>
+static cudaError_t fmap_simt_t(const Problem& p, const void* x, int is_key, void* phi,
+                               cudaStream_t s) {
+  const int64_t rows = p.B * p.H * p.n;
+  if (rows == 0) return cudaSuccess;
+  const T* W = (const T*)(is_key && p.Wk ? p.Wk : p.Wq);
+  const float* b = is_key && p.Wk ? p.bk : p.bq;
+  const int warps = kThreads / 32;
+  const int64_t blocks64 = (rows + warps - 1) / warps;
+  const int blocks = (int)std::min<int64_t>(blocks64, (int64_t)device_sm_count() * 16);
+  const size_t smem = sizeof(float) * warps * (128 + 320);
+  fmap_simt_kernel<T><<<blocks, kThreads, smem, s>>>((const T*)x, W, b, (T*)phi, p.kind, p.d,
+                                                     p.dpp, p.H, p.n, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fmap_simt(const Problem& p, const void* x, int is_key, void* phi,
+                             cudaStream_t s) {
+  return p.dtype == HH_F32 ? fmap_simt_t<float>(p, x, is_key, phi, s)
+                           : fmap_simt_t<__nv_bfloat16>(p, x, is_key, phi, s);
+}
+
+template <typename T>
+static cudaError_t prefill_simt_t(const Problem& p, const void* q, const void* k, const void* v,
+                                  void* y, float* S_out, float* z_out, cudaStream_t s) {
+  const int64_t units = p.B * p.H;
+  if (units == 0) return cudaSuccess;
+  const size_t cap = (size_t)std::min(device_max_smem_optin(), 200 * 1024);
+  int C = 64;
+  while (C > 8 && prefill_smem_bytes(p.d, p.dpp, C) > cap) C >>= 1;
+  const size_t smem = prefill_smem_bytes(p.d, p.dpp, C);
+  if (smem > cap) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const T* Wk = (const T*)(p.Wk ? p.Wk : p.Wq);
+  const float* bk = p.Wk ? p.bk : p.bq;
+  prefill_simt_kernel<T><<<(unsigned)units, kThreads, smem, s>>>(
+      (const T*)q, (const T*)k, (const T*)v, (T*)y, S_out, z_out, (const T*)p.Wq, p.bq, Wk, bk,
+      p.kind, p.d, p.dpp, p.H, p.n, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_simt(const Problem& p, const void* q, const void* k, const void* v,
+                                void* y, float* S_out, float* z_out, cudaStream_t s) {
+  return p.dtype == HH_F32 ? prefill_simt_t<float>(p, q, k, v, y, S_out, z_out, s)
+                           : prefill_simt_t<__nv_bfloat16>(p, q, k, v, y, S_out, z_out, s);
+}
+
+template <typename T>
+static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, const void* phq,
+                               const void* phk, float* loss_rows, float* partial, int tile,
+                               float* head_sum, cudaStream_t s) {
+  const int64_t units = p.B * p.H;
+  if (units == 0) return cudaSuccess;
+  const int ntiles = ceil_div(p.n, kLossRows);
+  const size_t smem = sizeof(float) * ((size_t)kLossRows * p.d + (size_t)kLossRows * p.dpp +
+                                       (size_t)kLossKeys * p.d + (size_t)kLossKeys * p.dpp +
+                                       kLossRows);
+  cudaError_t e = cudaFuncSetAttribute(loss_simt_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (ntiles > 0) {
+    const int64_t blocks = units * ntiles;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    loss_simt_kernel<T><<<(unsigned)blocks, kThreads, smem, s>>>((const T*)q, (const T*)k, (const T*)phq,
+                                                     (const T*)phk, loss_rows, partial, p.d,
+                                                     p.dpp, p.n, ntiles);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  sum_partials_kernel<<<ceil_div(units, 128), 128, 0, s>>>(partial, head_sum, units, ntiles);
+  (void)tile;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_simt(const Problem& p, const void* q, const void* k, const void* phq,
+                             const void* phk, float* loss_rows, float* partial, int tile,
+                             float* head_sum, cudaStream_t s) {
+  return p.dtype == HH_F32
+             ? loss_simt_t<float>(p, q, k, phq, phk, loss_rows, partial, tile, head_sum, s)
+             : loss_simt_t<__nv_bfloat16>(p, q, k, phq, phk, loss_rows, partial, tile, head_sum,
+                                          s);
+}
+
+}  // namespace hh

@@ -1,0 +1,242 @@
+"""GPU parity against the fp64 oracle on seeded inputs, through the C ABI.
+
+Sizes here span several 128-token tiles and a ragged tail while the oracle
+still finishes in seconds.  Tolerances: max per-head relative L2 error
+<= 5e-3 for bf16 inputs (fp32 accumulation) and <= 1e-5 for float32."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import softmax_mimicking_feature_gb300 as hh
+from softmax_mimicking_feature_gb300 import workloads as wl
+from tests._util import BF16_TOL, F32_TOL, f64, need_gpu, rel_l2_per_head
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+    from tests._util import lib_or_build
+    lib_or_build()
+
+
+def _dev(x):
+    return {k: (None if t is None else t.cuda()) for k, t in x.items()}
+
+
+def _fm(w, xd):
+    if w.kind == "hedgehog":
+        return hh.FeatureMap("hedgehog", w.d, xd["W"], xd["b"])
+    return hh.FeatureMap("taylor2", w.d)
+
+
+def _oracle_y(w, x):
+    W = None if x["W"] is None else f64(x["W"])
+    b = None if x["b"] is None else f64(x["b"])
+    return O.fwd_causal(w.kind, f64(x["q"]), f64(x["k"]), f64(x["v"]), W, b)
+
+
+def _oracle_loss(w, x):
+    W = None if x["W"] is None else f64(x["W"])
+    b = None if x["b"] is None else f64(x["b"])
+    return O.loss_causal(w.kind, f64(x["q"]), f64(x["k"]), W, b)
+
+
+def _tol(w):
+    return F32_TOL if w.dtype == "f32" else BF16_TOL
+
+
+# ---------------------------------------------------------------------------
+# hand-worked cases through the float32 kernels
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["E1", "E2", "E3", "E4"])
+def test_hand_worked_cases_fp32(name, golden):
+    g = golden[name]
+    dev = "cuda"
+    q, k, v = (torch.tensor(g[t], dtype=torch.float32, device=dev)[None, None].contiguous()
+               for t in ("q", "k", "v"))
+    d = q.shape[-1]
+    if g["kind"] == "hedgehog":
+        fm = hh.FeatureMap("hedgehog", d, torch.tensor(g["W"], dtype=torch.float32, device=dev)[None].contiguous(),
+                           torch.tensor(g["b"], dtype=torch.float32, device=dev)[None].contiguous())
+    else:
+        fm = hh.FeatureMap("taylor2", d)
+    y = hh.linattn_fwd_causal(fm, q, k, v)
+    rows, head = hh.mimicry_loss(fm, q, k)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(f64(y)[0, 0], np.array(g["y"]), rtol=2e-6, atol=2e-6)
+    np.testing.assert_allclose(f64(rows)[0, 0], np.array(g["L"]), rtol=2e-6, atol=2e-6)
+    assert abs(float(head[0, 0]) - sum(g["L"])) < 1e-5
+
+
+# ---------------------------------------------------------------------------
+# float32 workload: 1 x 1 x 256, d = 64, output + loss + feature map
+# ---------------------------------------------------------------------------
+
+def test_fp32_workload_prefill_loss_fmap():
+    w = wl.WORKLOADS["hedgehog_f32_1x1x256_d64"]
+    x = wl.make_inputs(w, seed=0)
+    xd = _dev(x)
+    fm = _fm(w, xd)
+    y = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"], chunk=64)
+    rows, head = hh.mimicry_loss(fm, xd["q"], xd["k"])
+    phq = hh.feature_map(fm, xd["q"])
+    torch.cuda.synchronize()
+    assert rel_l2_per_head(f64(y), _oracle_y(w, x)) <= F32_TOL
+    L_ref, Lh_ref = _oracle_loss(w, x)
+    assert rel_l2_per_head(f64(rows), L_ref) <= F32_TOL
+    assert abs(float(head[0, 0]) - Lh_ref[0, 0]) <= F32_TOL * abs(Lh_ref[0, 0])
+    phi_ref = O.hedgehog_feature_map(f64(x["q"])[0, 0], f64(x["W"])[0], f64(x["b"])[0])
+    assert rel_l2_per_head(f64(phq)[0], phi_ref[None]) <= F32_TOL
+
+
+# ---------------------------------------------------------------------------
+# bf16 workloads at reduced sizes (several tiles + ragged tails)
+# ---------------------------------------------------------------------------
+
+SMALL = {
+    "gpt2_d64": ("gpt2_prefill_8x12x1024_d64", dict(B=2, H=3, n=300)),
+    "llama_d128": ("llama2_prefill_1x32x4096_d128", dict(B=1, H=3, n=389)),
+    "taylor_d16": ("taylor2_prefill_4x8x8192_d16", dict(B=2, H=2, n=333)),
+    "gpt2_n1": ("gpt2_prefill_8x12x1024_d64", dict(B=1, H=2, n=1)),
+    "llama_n128": ("llama2_prefill_1x32x4096_d128", dict(B=1, H=2, n=128)),
+    "taylor_n129": ("taylor2_prefill_4x8x8192_d16", dict(B=1, H=3, n=129)),
+    "gpt2_f32_d64": ("hedgehog_f32_1x1x256_d64", dict(B=2, H=2, n=190)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+@pytest.mark.parametrize("chunk", [64, 128])
+def test_prefill_parity_small(case, chunk):
+    name, kw = SMALL[case]
+    w = wl.WORKLOADS[name].with_(**kw)
+    x = wl.make_inputs(w, seed=11)
+    xd = _dev(x)
+    y = hh.linattn_fwd_causal(_fm(w, xd), xd["q"], xd["k"], xd["v"], chunk=chunk)
+    torch.cuda.synchronize()
+    err = rel_l2_per_head(f64(y), _oracle_y(w, x))
+    assert err <= _tol(w), err
+
+
+@pytest.mark.parametrize("case", ["gpt2_d64", "llama_d128", "taylor_d16", "gpt2_f32_d64", "gpt2_n1"])
+def test_loss_parity_small(case):
+    name, kw = SMALL[case]
+    w = wl.WORKLOADS[name].with_(**kw)
+    x = wl.make_inputs(w, seed=5)
+    xd = _dev(x)
+    rows, head = hh.mimicry_loss(_fm(w, xd), xd["q"], xd["k"])
+    torch.cuda.synchronize()
+    L_ref, Lh_ref = _oracle_loss(w, x)
+    assert rel_l2_per_head(f64(rows), L_ref) <= _tol(w)
+    np.testing.assert_allclose(f64(head), Lh_ref, rtol=_tol(w), atol=1e-6)
+
+
+@pytest.mark.parametrize("case", ["gpt2_d64", "llama_d128", "taylor_d16", "gpt2_f32_d64"])
+@pytest.mark.parametrize("is_key", [0, 1])
+def test_feature_map_parity(case, is_key):
+    name, kw = SMALL[case]
+    w = wl.WORKLOADS[name].with_(**kw)
+    x = wl.make_inputs(w, seed=3)
+    xd = _dev(x)
+    t = "k" if is_key else "q"
+    phi = hh.feature_map(_fm(w, xd), xd[t], is_key=bool(is_key))
+    torch.cuda.synchronize()
+    xs = f64(x[t])
+    dp = O.taylor2_feature_dim(w.d) if w.kind == "taylor2" else 2 * w.d
+    ref = np.empty(xs.shape[:3] + (dp,))
+    for h in range(w.H):
+        if w.kind == "hedgehog":
+            ref[:, h] = O.hedgehog_feature_map(xs[:, h], f64(x["W"])[h], f64(x["b"])[h])
+        else:
+            ref[:, h] = O.taylor2_feature_map(xs[:, h])
+    got = f64(phi)
+    assert rel_l2_per_head(got[..., :dp], ref) <= _tol(w)
+    assert np.all(got[..., dp:] == 0)
+
+
+def test_separate_query_and_key_maps():
+    w = wl.WORKLOADS["gpt2_prefill_8x12x1024_d64"].with_(B=1, H=2, n=140)
+    x = wl.make_inputs(w, seed=21)
+    x2 = wl.make_inputs(w, seed=22)
+    xd = _dev(x)
+    Wk, bk = x2["W"].cuda(), x2["b"].cuda()
+    fm = hh.FeatureMap("hedgehog", w.d, xd["W"], xd["b"], Wk, bk)
+    y = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"])
+    torch.cuda.synchronize()
+    ref = np.empty(f64(x["v"]).shape)
+    for h in range(w.H):
+        pq = O.hedgehog_feature_map(f64(x["q"])[0, h], f64(x["W"])[h], f64(x["b"])[h])
+        pk = O.hedgehog_feature_map(f64(x["k"])[0, h], f64(x2["W"])[h], f64(x2["b"])[h])
+        ref[0, h] = O.linattn_quadratic(pq, pk, f64(x["v"])[0, h])
+    assert rel_l2_per_head(f64(y), ref) <= BF16_TOL
+
+
+# ---------------------------------------------------------------------------
+# state export and decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", ["gpt2_d64", "llama_d128", "taylor_d16", "gpt2_f32_d64"])
+def test_state_export_and_decode(case):
+    name, kw = SMALL[case]
+    w = wl.WORKLOADS[name].with_(**kw)
+    x = wl.make_inputs(w, seed=9)
+    xd = _dev(x)
+    fm = _fm(w, xd)
+    n1 = w.n - 7
+    pre = [xd[t][:, :, :n1].contiguous() for t in ("q", "k", "v")]
+    _, S, z = hh.linattn_fwd_causal(fm, *pre, return_state=True)
+    ys = []
+    for t in range(n1, w.n):
+        ys.append(hh.linattn_decode_step(fm, *(xd[u][:, :, t].contiguous() for u in ("q", "k", "v")), S, z))
+    y_full, S_full, z_full = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"], return_state=True)
+    torch.cuda.synchronize()
+    tol = _tol(w)
+    y_dec = torch.stack(ys, dim=2)
+    y_ref = _oracle_y(w, x)
+    assert rel_l2_per_head(f64(y_dec), y_ref[:, :, n1:]) <= tol
+    # final state against the definition S = sum_j phi(k_j)^T v_j, z = sum_j phi(k_j)
+    dp = O.taylor2_feature_dim(w.d) if w.kind == "taylor2" else 2 * w.d
+    for bi in range(w.B):
+        for h in range(w.H):
+            kk = f64(x["k"])[bi, h]
+            pk = (O.hedgehog_feature_map(kk, f64(x["W"])[h], f64(x["b"])[h]) if w.kind == "hedgehog"
+                  else O.taylor2_feature_map(kk))
+            S_ref = pk.T @ f64(x["v"])[bi, h]
+            z_ref = pk.sum(0)
+            for SS, zz in ((S_full, z_full), (S, z)):
+                Sg, zg = f64(SS)[bi, h], f64(zz)[bi, h]
+                assert np.linalg.norm(Sg[:dp] - S_ref) <= tol * np.linalg.norm(S_ref)
+                assert np.linalg.norm(zg[:dp] - z_ref) <= tol * np.linalg.norm(z_ref)
+                assert np.all(Sg[dp:] == 0) and np.all(zg[dp:] == 0)
+
+
+def test_empty_and_zero_length():
+    w = wl.WORKLOADS["gpt2_prefill_8x12x1024_d64"].with_(B=1, H=2, n=16)
+    x = _dev(wl.make_inputs(w, seed=1))
+    fm = _fm(w, x)
+    q0 = x["q"][:, :, :0].contiguous()
+    y, S, z = hh.linattn_fwd_causal(fm, q0, q0, q0, return_state=True)
+    rows, head = hh.mimicry_loss(fm, q0, q0)
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and float(S.abs().sum()) == 0 and float(z.abs().sum()) == 0
+    assert float(head.abs().sum()) == 0
+    e = x["q"][:0].contiguous()
+    assert hh.linattn_fwd_causal(fm, e, e, e).numel() == 0
+
+
+def test_output_canaries_untouched():
+    """Kernels write exactly their outputs: guard words around y stay intact."""
+    w = wl.WORKLOADS["llama2_prefill_1x32x4096_d128"].with_(B=1, H=2, n=131)
+    x = _dev(wl.make_inputs(w, seed=4))
+    n_el = x["q"].numel()
+    buf = torch.full((n_el + 2048,), 7.0, dtype=x["q"].dtype, device="cuda")
+    y = buf[1024:1024 + n_el].view_as(x["q"])
+    hh.linattn_fwd_causal(_fm(w, x), x["q"], x["k"], x["v"], y=y)
+    torch.cuda.synchronize()
+    assert bool((buf[:1024] == 7).all()) and bool((buf[1024 + n_el:] == 7).all())
