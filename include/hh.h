@@ -125,6 +125,12 @@ HH_API hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, i
 HH_API size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
                               int chunk);
 
+/* Planning query for hh_linattn_fwd_causal on the current device: the
+ * number of sequence segments each (batch, head) is split into and the
+ * number of kernel launches one call makes.  Either output may be NULL. */
+HH_API hh_status hh_fwd_plan(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
+                             int chunk, int* segments, int* launches);
+
 /* Causal linear attention over whole sequences (chunked prefill).
  * Source: section 2 (paper Eq. 2) for y; "Complexity Analysis" for the
  * running sums S_i = sum_{j<=i} phi(k_j)^T v_j and z_i = sum_{j<=i} phi(k_j).

@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     HHError,
     feature_map,
     fmap_dim,
+    fwd_plan,
     fwd_workspace_bytes,
     linattn_decode_step,
     linattn_fwd_causal,

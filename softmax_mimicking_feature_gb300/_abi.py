@@ -18,7 +18,7 @@ HH_F32, HH_BF16 = 0, 1
 HH_FMAP_HEDGEHOG, HH_FMAP_TAYLOR2 = 0, 1
 
 EXPORTED = ("hh_version", "hh_status_str", "hh_fmap_dim", "hh_feature_map",
-            "hh_fwd_workspace_bytes", "hh_linattn_fwd_causal", "hh_linattn_decode_step",
+            "hh_fwd_workspace_bytes", "hh_fwd_plan", "hh_linattn_fwd_causal", "hh_linattn_decode_step",
             "hh_loss_workspace_bytes", "hh_mimicry_loss")
 
 
@@ -46,6 +46,7 @@ _SIGS = {
     "hh_fmap_dim": ([_i32, _i32, _i32], _i32),
     "hh_feature_map": ([_P, _i32, _vp, _i32, _i64, _i32, _i64, _vp, _vp], _i32),
     "hh_fwd_workspace_bytes": ([_P, _i32, _i64, _i32, _i64, _i32], _sz),
+    "hh_fwd_plan": ([_P, _i32, _i64, _i32, _i64, _i32, _vp, _vp], _i32),
     "hh_linattn_fwd_causal": ([_P, _i32, _vp, _vp, _vp, _i64, _i32, _i64, _i32, _vp, _vp, _vp,
                                _vp, _sz, _vp, _vp], _i32),
     "hh_linattn_decode_step": ([_P, _i32, _vp, _vp, _vp, _i64, _i32, _vp, _vp, _vp, _vp], _i32),

@@ -15,7 +15,7 @@ import torch
 
 from . import _abi
 
-__all__ = ["FeatureMap", "fmap_dim", "feature_map", "fwd_workspace_bytes",
+__all__ = ["FeatureMap", "fmap_dim", "feature_map", "fwd_workspace_bytes", "fwd_plan",
            "linattn_fwd_causal", "linattn_decode_step", "loss_workspace_bytes",
            "mimicry_loss", "HHError"]
 
@@ -96,6 +96,15 @@ def fwd_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: i
                         chunk: int = 0) -> int:
     s = fm.struct()
     return int(_abi.lib().hh_fwd_workspace_bytes(ctypes.byref(s), _DTYPES[dtype], B, H, n, chunk))
+
+
+def fwd_plan(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int, chunk: int = 0):
+    """(segments, launches) one hh_linattn_fwd_causal call uses (hh_fwd_plan)."""
+    seg, lau = ctypes.c_int(0), ctypes.c_int(0)
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_fwd_plan(ctypes.byref(s), _DTYPES[dtype], B, H, n, chunk,
+                                      ctypes.byref(seg), ctypes.byref(lau)), "hh_fwd_plan")
+    return seg.value, lau.value
 
 
 def linattn_fwd_causal(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -179,7 +179,28 @@ size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, 
   Problem p;
   if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
   (void)chunk;
-  return 0;
+  if (B * H * n == 0) return 0;
+  const TcPlan pl = plan_prefill_tc(p);
+  return pl.supported ? align256(pl.ws_bytes) : 0;
+}
+
+hh_status hh_fwd_plan(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n, int chunk,
+                      int* segments, int* launches) {
+  Problem p;
+  hh_status st = make_problem(fmap, dtype, B, H, n, &p);
+  if (st != HH_OK) return st;
+  if (chunk != 0 && chunk != 64 && chunk != 128) return HH_ERR_UNSUPPORTED;
+  int seg = 1, lau = (B * H * n > 0) ? 1 : 0;
+  if (lau) {
+    const TcPlan pl = plan_prefill_tc(p);
+    if (pl.supported) {
+      seg = pl.P;
+      lau = pl.launches;
+    }
+  }
+  if (segments) *segments = seg;
+  if (launches) *launches = lau;
+  return HH_OK;
 }
 
 hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, const void* k,
@@ -193,9 +214,10 @@ hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, c
   if ((S_out == nullptr) != (z_out == nullptr)) return HH_ERR_INVALID_ARG;
   if (B == 0) return HH_OK;
   if (n > 0 && (!q || !k || !v || !y)) return HH_ERR_INVALID_ARG;
-  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, p.Wq, p.bq, p.Wk, p.bk, workspace,
-                                dev_status})) != HH_OK)
+  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, p.Wq, p.bq, p.Wk, p.bk, workspace})) !=
+      HH_OK)
     return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
   const size_t need = hh_fwd_workspace_bytes(fmap, dtype, B, H, n, chunk);
   if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;
@@ -209,6 +231,9 @@ hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, c
     }
     return HH_OK;
   }
+  const TcPlan pl = plan_prefill_tc(p);
+  if (pl.supported)
+    return cuda_status(launch_prefill_tc(p, pl, q, k, v, y, S_out, z_out, workspace, dev_status, s));
   return cuda_status(launch_prefill_simt(p, q, k, v, y, S_out, z_out, s));
 }
 
@@ -242,8 +267,9 @@ hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const v
   if (!loss_head_sum) return HH_ERR_INVALID_ARG;
   if (n > 0 && (!q || !k)) return HH_ERR_INVALID_ARG;
   if ((st = check_ptrs_aligned({q, k, loss_rows, loss_head_sum, p.Wq, p.bq, p.Wk, p.bk,
-                                workspace, dev_status})) != HH_OK)
+                                workspace})) != HH_OK)
     return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
   const size_t need = hh_loss_workspace_bytes(fmap, dtype, B, H, n);
   if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;

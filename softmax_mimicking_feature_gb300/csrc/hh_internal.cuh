@@ -56,6 +56,20 @@ cudaError_t launch_loss_simt(const Problem& p, const void* q, const void* k, con
                              float* head_sum, cudaStream_t s);
 int loss_simt_tile();
 
+// Tensor-core (tcgen05) chunked prefill for bf16.
+struct TcPlan {
+  bool supported = false;
+  int NT = 0;        // 128-token tiles per sequence
+  int P = 1;         // segments per sequence
+  int L = 1;         // tiles per segment
+  int launches = 1;  // kernel launches per call
+  size_t ws_bytes = 0;
+};
+TcPlan plan_prefill_tc(const Problem& p);
+cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q, const void* k,
+                              const void* v, void* y, float* S_out, float* z_out, void* ws,
+                              int* dev_status, cudaStream_t s);
+
 // Decode step (SIMT, HBM-streaming).
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
                           float* S, float* z, void* y, cudaStream_t s);

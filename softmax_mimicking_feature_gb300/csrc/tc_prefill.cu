@@ -1,0 +1,843 @@
+// Chunked causal linear attention on the 5th-generation tensor cores.
+//
+// "The Hedgehog & the Porcupine" summary: section 2 (paper Eq. 2) defines
+//   y_i = phi(q_i) sum_{j<=i} phi(k_j)^T v_j / phi(q_i) sum_{j<=i} phi(k_j),
+// "Complexity Analysis" the running sums S = sum phi(k)^T v and z = sum phi(k);
+// the maps are "The Hedgehog MLP Feature Map" (Choices 1 and 3) and "The
+// Taylor Exponential as a Bridge Result".
+//
+// Evaluation order (per 128-token tile t of one (batch, head) sequence segment):
+//   H_Q = Q_t W, H_K = K_t W                          (tcgen05, Hedgehog only)
+//   phi(Q_t) -> TMEM (bf16 pairs, the A operand of the next MMAs)
+//   phi(K_t) -> shared memory (bf16, 128B-swizzled panels); z += colsum phi(K_t)
+//   S_bf16 <- S (TMEM fp32 state of the tokens before tile t)
+//   Sc = phi(Q_t) phi(K_t)^T;  S += phi(K_t)^T V_t     (tcgen05)
+//   P = bf16(tril(Sc)), rowsum(P)
+//   O = P V_t + phi(Q_t) S_bf16                         (tcgen05)
+//   y = O / (rowsum(P) + phi(Q_t) . z_before)
+// A 128-row tile covers two 64-token chunks with the exact causal mask, so
+// the result is the same causal sum for chunk 64 or 128.
+//
+// Long sequences are cut into segments processed by different CTAs.  A
+// state pass (OUT_PASS = false) computes each segment's sum of phi(k)^T v and
+// phi(k) into the workspace; the output pass starts segment s from the sum of
+// the segments before it (added in segment order).
+//
+// Roles: thread 0 issues TMA loads and MMAs; all 8 warps run the epilogues
+// (warp w owns TMEM lanes 32*(w%4).. and one half of the columns).  Every
+// wait on an mbarrier is bounded in time (see tc_ptx.cuh).
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "tc_ptx.cuh"
+
+namespace hh {
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+template <int KIND, int D>
+struct Cfg;
+
+// Hedgehog, d in {64, 128}: features [exp(h_0..h_{d-1}), exp(-h_0..-h_{d-1})].
+template <int D>
+struct Cfg<HH_FMAP_HEDGEHOG, D> {
+  static constexpr int DP = 2 * D;           // feature dim
+  static constexpr int DPP = 2 * D;          // padded feature dim (rows of S)
+  static constexpr int NMB = DP / 128;       // 128-feature M blocks of S
+  static constexpr int PHK_PANELS = DP / 64; // 64-feature panels of phi(K)
+  static constexpr int KSTEPS_F = DP / 16;   // MMA k-steps over features
+  // TMEM columns
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t TM_Y = NMB * D;       // H_Q (fp32) -> phi(Q) (bf16 pairs)
+  static constexpr uint32_t TM_X = TM_Y + D;      // H_K -> Sc -> O
+  static constexpr uint32_t TM_COLS = (TM_X + 128 <= 256) ? 256 : 512;
+  // shared memory (byte offsets from a 1024-aligned base)
+  static constexpr uint32_t W_BYTES = D * D * 2;
+  static constexpr uint32_t XT_BYTES = kTile * D * 2;     // one Q or K tile
+  static constexpr uint32_t OFF_W = 0;
+  static constexpr uint32_t OFF_WK = OFF_W + W_BYTES;     // second map (d = 64 only)
+  static constexpr uint32_t OFF_R1 = OFF_WK + (D == 64 ? W_BYTES : 0);
+  static constexpr uint32_t OFF_Q = OFF_R1;
+  static constexpr uint32_t OFF_K = OFF_R1 + XT_BYTES;
+  static constexpr uint32_t OFF_SB = OFF_R1;              // S_bf16 [DP][D] aliases Q/K
+  static constexpr uint32_t OFF_V = OFF_R1 + 2 * XT_BYTES;
+  static constexpr uint32_t OFF_PHK = OFF_V + XT_BYTES;   // phi(K) panels; P aliases
+  static constexpr uint32_t OFF_END = OFF_PHK + PHK_PANELS * 16384;
+  static_assert(DP * D * 2 <= 2 * XT_BYTES, "S_bf16 must fit in the Q/K region");
+};
+
+// Taylor, d = 16: features [1, x, x_i x_j / sqrt2], 273 used, 288 stored.
+template <>
+struct Cfg<HH_FMAP_TAYLOR2, 16> {
+  static constexpr int D = 16;
+  static constexpr int DP = 288;             // padded feature dim used by the MMAs
+  static constexpr int DPP = 288;
+  static constexpr int NMB = 3;              // S rows as 3 blocks of 128 (384 >= 288)
+  static constexpr int PHK_PANELS = 6;       // 384 features; 288.. are zero
+  static constexpr int KSTEPS_F = DP / 16;   // 18
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t TM_Y = 64;       // phi(Q): 144 columns of bf16 pairs
+  static constexpr uint32_t TM_X = 256;      // Sc -> O
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr uint32_t XT_BYTES = kTile * D * 2;     // 4 KB
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + XT_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + XT_BYTES;
+  static constexpr uint32_t OFF_SB = OFF_V + XT_BYTES;    // [288][16] bf16, 32B-swizzled
+  static constexpr uint32_t OFF_PHK = 24576;              // 1024-aligned, after SB (9 KB)
+  static constexpr uint32_t OFF_END = OFF_PHK + PHK_PANELS * 16384;
+  static constexpr uint32_t OFF_W = 0, OFF_WK = 0, W_BYTES = 0;
+};
+
+template <int KIND, int D>
+struct Smem {
+  using C = Cfg<KIND, D>;
+  static constexpr int ZN = 384;
+  // scalars after the operand area
+  static constexpr uint32_t OFF_Z = C::OFF_END;                  // float[ZN]
+  static constexpr uint32_t OFF_ZP = OFF_Z + ZN * 4;             // float[4][ZN]
+  static constexpr uint32_t OFF_DQ = OFF_ZP + 4 * ZN * 4;        // float[2][128]
+  static constexpr uint32_t OFF_RS = OFF_DQ + 2 * 128 * 4;       // float[2][128]
+  static constexpr uint32_t OFF_BQ = OFF_RS + 2 * 128 * 4;       // float[128]
+  static constexpr uint32_t OFF_BK = OFF_BQ + 128 * 4;           // float[128]
+  static constexpr uint32_t OFF_BAR = OFF_BK + 128 * 4;          // 4 x u64
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 4 * 8;          // tmem base, abort
+  static constexpr uint32_t BYTES = OFF_MISC + 16;
+  static constexpr uint32_t ALLOC = BYTES + 1024;                // slack for alignment
+};
+
+struct PrefillArgs {
+  CUtensorMap tq, tk, tv, twq, twk;
+  void* y;
+  float* ws_S;      // [U][P-1][DPP][D]
+  float* ws_z;      // [U][P-1][DPP]
+  float* S_out;     // [U][DPP][D] or null
+  float* z_out;     // [U][DPP] or null
+  const float* bq;
+  const float* bk;
+  int* dev_status;
+  uint64_t soft_ns, hard_ns;
+  int64_t n;
+  int H;
+  int P;            // segments per unit
+  int L;            // tiles per segment
+  int NT;           // tiles per unit
+  int sep_wk;       // distinct key map loaded in the second W buffer
+};
+
+// ---------------------------------------------------------------------------
+// warp-level helpers
+// ---------------------------------------------------------------------------
+
+// Sum of 32 per-lane vectors a[0..31] across the warp: afterwards lane L holds
+// the sum over lanes of a[L] in a[0].  31 shuffles (recursive halving).
+__device__ __forceinline__ void warp_transpose_sum(float (&a)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? a[i] : a[i + o];
+      const float keep = upper ? a[i + o] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+
+// Write 8 consecutive bf16 (4 packed words) of row r, 16-byte chunk `chunk`
+// (0..7) of a 128B-swizzled panel at byte address `panel`.
+__device__ __forceinline__ void st_panel_chunk(uint32_t panel, int r, int chunk, uint32_t a,
+                                               uint32_t b, uint32_t c, uint32_t d) {
+  st_shared_v4(panel + sw128_chunk(r, chunk), a, b, c, d);
+}
+
+__device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+// Hedgehog d = 64 needs 256 TMEM columns and ~108 KB of shared memory, so two
+// CTAs share an SM (one's MMAs overlap the other's epilogues).
+template <int KIND, int D>
+constexpr int min_blocks() { return (KIND == HH_FMAP_HEDGEHOG && D == 64) ? 2 : 1; }
+
+template <int KIND, int D, bool OUT>
+__global__ void __launch_bounds__(kThreads, min_blocks<KIND, D>())
+prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
+  using C = Cfg<KIND, D>;
+  using SM = Smem<KIND, D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* z_s = reinterpret_cast<float*>(sm + SM::OFF_Z);
+  float* zp_s = reinterpret_cast<float*>(sm + SM::OFF_ZP);
+  float* dq_s = reinterpret_cast<float*>(sm + SM::OFF_DQ);
+  float* rs_s = reinterpret_cast<float*>(sm + SM::OFF_RS);
+  float* bq_s = reinterpret_cast<float*>(sm + SM::OFF_BQ);
+  float* bk_s = reinterpret_cast<float*>(sm + SM::OFF_BK);
+  const uint32_t bar_load = sb + SM::OFF_BAR;
+  const uint32_t bar_w = bar_load + 8;
+  const uint32_t bar_mma = bar_load + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(sm + SM::OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = warp & 3, half = warp >> 2;
+  const int row = 32 * g + lane;  // TMEM lane / tile row owned by this thread
+
+  const int nseg_grid = OUT ? A.P : (A.P - 1);
+  const int64_t unit = blockIdx.x / nseg_grid;
+  const int seg = blockIdx.x % nseg_grid;
+  const int h = (int)(unit % A.H);
+  const int t_begin = seg * A.L;
+  const int t_end = min(A.NT, t_begin + A.L);
+
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+  bool failed = false;
+
+  // ---- setup ----
+  if (tid == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_w, 1);
+    mbar_init(bar_mma, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&A.tk);
+    prefetch_tmap(&A.tv);
+    if (OUT) prefetch_tmap(&A.tq);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  if (KIND == HH_FMAP_HEDGEHOG) {
+    for (int i = tid; i < D; i += kThreads) {
+      bq_s[i] = A.bq ? A.bq[(size_t)h * D + i] : 0.f;
+      bk_s[i] = A.bk ? A.bk[(size_t)h * D + i] : 0.f;
+    }
+  }
+  // initial z: sum of the preceding segments' partial sums (output pass)
+  for (int f = tid; f < SM::ZN; f += kThreads) {
+    float acc = 0.f;
+    if (OUT && f < C::DPP)
+      for (int s2 = 0; s2 < seg; ++s2)
+        acc += A.ws_z[((size_t)unit * (A.P - 1) + s2) * C::DPP + f];
+    z_s[f] = acc;
+  }
+  if (KIND == HH_FMAP_TAYLOR2) {
+    // zero the phi(K) panels once: features >= 288 stay zero for the whole run
+    for (uint32_t i = tid * 16; i < C::PHK_PANELS * 16384u; i += kThreads * 16)
+      st_shared_v4(sb + C::OFF_PHK + i, 0, 0, 0, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // initial S in TMEM (zeros, or the preceding segments' sum)
+  {
+    for (int mb = half; mb < C::NMB; mb += 2) {
+      const int f = mb * 128 + row;
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t r[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float acc = 0.f;
+          if (OUT && f < C::DPP)
+            for (int s2 = 0; s2 < seg; ++s2)
+              acc += A.ws_S[(((size_t)unit * (A.P - 1) + s2) * C::DPP + f) * D + c0 + j];
+          r[j] = __float_as_uint(acc);
+        }
+        tmem_st16(tmem + lane_base(warp) + C::TM_S + mb * D + c0, r);
+      }
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  uint32_t ph_load = 0, ph_w = 0, ph_mma = 0;
+
+  // ---- loads of one tile ----
+  auto issue_loads = [&](int t) {
+    const int r0 = t * kTile;
+    uint32_t bytes = C::XT_BYTES * (OUT ? 3 : 2);
+    mbar_expect_tx(bar_load, bytes);
+    if (KIND == HH_FMAP_HEDGEHOG) {
+      for (int i = 0; i < D / 64; ++i) {
+        if (OUT) tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, (int)unit);
+        tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, (int)unit);
+        tma_load_3d(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, (int)unit);
+      }
+    } else {
+      if (OUT) tma_load_3d(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, (int)unit);
+      tma_load_3d(sb + C::OFF_K, &A.tk, bar_load, 0, r0, (int)unit);
+      tma_load_3d(sb + C::OFF_V, &A.tv, bar_load, 0, r0, (int)unit);
+    }
+  };
+
+  if (tid == 0) {
+    if (KIND == HH_FMAP_HEDGEHOG) {
+      const int nmaps = A.sep_wk ? 2 : 1;
+      mbar_expect_tx(bar_w, C::W_BYTES * nmaps);
+      for (int i = 0; i < D / 64; ++i) {
+        tma_load_3d(sb + C::OFF_W + i * (D * 128), &A.twq, bar_w, 64 * i, 0, h);
+        if (A.sep_wk) tma_load_3d(sb + C::OFF_WK + i * (D * 128), &A.twk, bar_w, 64 * i, 0, h);
+      }
+    }
+    issue_loads(t_begin);
+  }
+
+  // descriptors of fixed operands
+  constexpr uint32_t IDESC_H = idesc_bf16(128, D, 0, 1);       // X[K-major] * W[MN-major]
+  constexpr uint32_t IDESC_SC = idesc_bf16(128, 128, 0, 0);    // phiQ[tmem] * phiK[K-major]
+  constexpr uint32_t IDESC_SU = idesc_bf16(128, D, 1, 1);      // phiK^T[MN] * V[MN]
+  constexpr uint32_t IDESC_PV = idesc_bf16(128, D, 0, 1);      // P[K-major] * V[MN]
+  constexpr uint32_t IDESC_QS = idesc_bf16(128, D, 0, 1);      // phiQ[tmem] * S_bf16[MN]
+  // V as an MN-major B operand (rows = tokens = K, columns = d = N)
+  auto v_desc = [&](int ks) -> uint64_t {
+    if (KIND == HH_FMAP_HEDGEHOG)
+      return smem_desc(sb + C::OFF_V + ks * 2048, kTile * 128, 1024, 2);
+    return smem_desc(sb + C::OFF_V + ks * 512, 16, 256, 6);
+  };
+  const uint32_t w_key_off = (KIND == HH_FMAP_HEDGEHOG && A.sep_wk) ? C::OFF_WK : C::OFF_W;
+
+  for (int t = t_begin; t < t_end && !failed; ++t) {
+    const int r0 = t * kTile;
+    const int nvalid = (int)min((int64_t)kTile, A.n - r0);
+
+    // ================= group 1: H = X W (Hedgehog) =================
+    if (KIND == HH_FMAP_HEDGEHOG) {
+      if (tid == 0) {
+        bool ok = mbar_wait(bar_load, ph_load, wp);
+        if (t == t_begin) ok = ok && mbar_wait(bar_w, ph_w, wp);
+        tc_fence_after();
+        if (ok) {
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+            const uint64_t bq = smem_desc(sb + C::OFF_W + ks * 2048, D * 128, 1024, 2);
+            const uint64_t bk = smem_desc(sb + w_key_off + ks * 2048, D * 128, 1024, 2);
+            if (OUT)
+              mma_ss(tmem + C::TM_Y, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2), bq, IDESC_H,
+                     ks > 0);
+            mma_ss(tmem + C::TM_X, smem_desc(sb + C::OFF_K + koff, 16, 1024, 2), bk, IDESC_H,
+                   ks > 0);
+          }
+          mma_commit(bar_mma);
+        } else {
+          failed = true;
+        }
+      }
+      ph_load ^= 1;
+      if (t == t_begin) ph_w ^= 1;
+      if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
+      ph_mma ^= 1;
+      tc_fence_after();
+    } else {
+      if (!mbar_wait(bar_load, ph_load, wp)) failed = true;
+      ph_load ^= 1;
+    }
+    if (__syncthreads_or(failed)) { failed = true; break; }
+
+    // ================= epilogue 1: features, S_bf16, z =================
+    // -- phi(Q) into TMEM (output pass), denominator part phi(q) . z_before
+    if (OUT) {
+      float dq = 0.f;
+      if (KIND == HH_FMAP_HEDGEHOG) {
+        constexpr int HC = D / 2;  // H columns per warp half
+        uint32_t hv[HC];
+#pragma unroll
+        for (int c = 0; c < HC; c += 32)
+          tmem_ld32(tmem + lane_base(warp) + C::TM_Y + half * HC + c,
+                    *reinterpret_cast<uint32_t(*)[32]>(&hv[c]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncthreads();  // every warp holds its H_Q columns before any overwrite
+        tc_fence_after();
+        uint32_t pp[HC / 2], pn[HC / 2];
+#pragma unroll
+        for (int j = 0; j < HC; j += 2) {
+          const int l = half * HC + j;
+          const float h0 = __uint_as_float(hv[j]) + bq_s[l];
+          const float h1 = __uint_as_float(hv[j + 1]) + bq_s[l + 1];
+          const uint32_t p = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
+          const uint32_t m = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+          pp[j / 2] = p;
+          pn[j / 2] = m;
+          dq += bf16_lo(p) * z_s[l] + bf16_hi(p) * z_s[l + 1] + bf16_lo(m) * z_s[D + l] +
+                bf16_hi(m) * z_s[D + l + 1];
+        }
+        // feature f -> packed column f/2: positive block at half*HC/2, negative at D/2 + half*HC/2
+#pragma unroll
+        for (int c = 0; c < HC / 2; c += 16) {
+          tmem_st16(tmem + lane_base(warp) + C::TM_Y + half * (HC / 2) + c,
+                    *reinterpret_cast<const uint32_t(*)[16]>(&pp[c]));
+          tmem_st16(tmem + lane_base(warp) + C::TM_Y + D / 2 + half * (HC / 2) + c,
+                    *reinterpret_cast<const uint32_t(*)[16]>(&pn[c]));
+        }
+      } else {
+        // Taylor: features of row `row` from the q tile (no swizzle, 32 B per row)
+        const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_Q) + row * 16;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(qrow[i]);
+        // half 0 builds features [0, 160) = packed columns [0, 80); half 1 [160, 288)
+        const int f0 = half ? 160 : 0, f1 = half ? 288 : 160;
+        for (int fb = f0; fb < f1; fb += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float v2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int f = fb + j + e;
+              float val;
+              if (f == 0) val = 1.f;
+              else if (f <= 16) val = x[f - 1];
+              else if (f <= 272) { const int p = f - 17; val = x[p >> 4] * x[p & 15] * kInvSqrt2; }
+              else val = 0.f;
+              v2[e] = val;
+            }
+            const uint32_t w2 = pack_bf16(v2[0], v2[1]);
+            pk[j / 2] = w2;
+            dq += bf16_lo(w2) * z_s[fb + j] + bf16_hi(w2) * z_s[fb + j + 1];
+          }
+          tmem_st16(tmem + lane_base(warp) + C::TM_Y + fb / 2, pk);
+        }
+      }
+      dq_s[half * 128 + row] = dq;
+    }
+
+    // -- phi(K) into shared memory panels, column sums into zp
+    {
+      const bool valid = row < nvalid;
+      if (KIND == HH_FMAP_HEDGEHOG) {
+        constexpr int HC = D / 2;
+#pragma unroll
+        for (int c = 0; c < HC; c += 32) {
+          uint32_t hv[32];
+          tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, hv);
+          tmem_ld_wait();
+          float ep[32], en[32];
+          uint32_t wp_[16], wn_[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int l = half * HC + c + j;
+            const float h0 = __uint_as_float(hv[j]) + bk_s[l];
+            const float h1 = __uint_as_float(hv[j + 1]) + bk_s[l + 1];
+            uint32_t p = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
+            uint32_t m = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+            if (!valid) p = m = 0u;
+            wp_[j / 2] = p;
+            wn_[j / 2] = m;
+            ep[j] = bf16_lo(p); ep[j + 1] = bf16_hi(p);
+            en[j] = bf16_lo(m); en[j + 1] = bf16_hi(m);
+          }
+          const int fpos = half * HC + c;          // first positive feature of this chunk
+          const int fneg = D + half * HC + c;      // first negative feature
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            st_panel_chunk(sb + C::OFF_PHK + (fpos / 64) * 16384, row, (fpos % 64) / 8 + q4,
+                           wp_[4 * q4], wp_[4 * q4 + 1], wp_[4 * q4 + 2], wp_[4 * q4 + 3]);
+            st_panel_chunk(sb + C::OFF_PHK + (fneg / 64) * 16384, row, (fneg % 64) / 8 + q4,
+                           wn_[4 * q4], wn_[4 * q4 + 1], wn_[4 * q4 + 2], wn_[4 * q4 + 3]);
+          }
+          warp_transpose_sum(ep, lane);
+          warp_transpose_sum(en, lane);
+          zp_s[g * SM::ZN + fpos + lane] = ep[0];
+          zp_s[g * SM::ZN + fneg + lane] = en[0];
+        }
+      } else {
+        const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_K) + row * 16;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(krow[i]);
+        const int f0 = half ? 160 : 0, f1 = half ? 288 : 160;
+        for (int fb = f0; fb < f1; fb += 32) {
+          float e[32];
+          uint32_t wv[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float v2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int f = fb + j + u;
+              float val;
+              if (f == 0) val = 1.f;
+              else if (f <= 16) val = x[f - 1];
+              else if (f <= 272) { const int p = f - 17; val = x[p >> 4] * x[p & 15] * kInvSqrt2; }
+              else val = 0.f;
+              v2[u] = val;
+            }
+            uint32_t w2 = pack_bf16(v2[0], v2[1]);
+            if (!valid) w2 = 0u;
+            wv[j / 2] = w2;
+            e[j] = bf16_lo(w2);
+            e[j + 1] = bf16_hi(w2);
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_panel_chunk(sb + C::OFF_PHK + (fb / 64) * 16384, row, (fb % 64) / 8 + q4,
+                           wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
+          warp_transpose_sum(e, lane);
+          zp_s[g * SM::ZN + fb + lane] = e[0];
+        }
+      }
+    }
+
+    // -- S_bf16 <- S (state before this tile), the B operand of phi(Q) S
+    if (OUT) {
+      if (KIND == HH_FMAP_HEDGEHOG) {
+        // S_bf16 panel: [DP rows][D cols] as D/64 column blocks of [DP rows x 128 B]
+        constexpr int CPW = (C::NMB == 2) ? D : D / 2;   // columns handled by this warp
+        const int mb = (C::NMB == 2) ? half : 0;
+        const int cbase = (C::NMB == 2) ? 0 : half * (D / 2);
+        const int f = mb * 128 + row;
+#pragma unroll
+        for (int c = 0; c < CPW; c += 32) {
+          uint32_t sv[32];
+          tmem_ld32(tmem + lane_base(warp) + C::TM_S + mb * D + cbase + c, sv);
+          tmem_ld_wait();
+          const int col = cbase + c;
+          const uint32_t panel = sb + C::OFF_SB + (col / 64) * (C::DP * 128);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int j = 8 * q4;
+            st_panel_chunk(panel, f, (col % 64) / 8 + q4,
+                           pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                           pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
+                           pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
+                           pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
+          }
+        }
+      } else {
+        // Taylor: S_bf16 [288 rows][16 cols] 32B-swizzled (16B chunk ^= bit 2 of the row)
+        for (int mb = half; mb < C::NMB; mb += 2) {
+          const int f = mb * 128 + row;
+          uint32_t sv[16];
+          tmem_ld16(tmem + lane_base(warp) + C::TM_S + mb * D, sv);
+          tmem_ld_wait();
+          if (f < C::DP) {
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              const int j = 8 * ch;
+              const uint32_t addr = sb + C::OFF_SB + f * 32 + ((ch ^ ((f >> 2) & 1)) << 4);
+              st_shared_v4(addr, pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                           pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
+                           pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
+                           pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
+            }
+          }
+        }
+      }
+    }
+    tmem_st_wait();
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // z += column sums of this tile's phi(K) (after every reader of z_before)
+    for (int f = tid; f < C::DPP; f += kThreads)
+      z_s[f] += ((zp_s[f] + zp_s[SM::ZN + f]) + zp_s[2 * SM::ZN + f]) + zp_s[3 * SM::ZN + f];
+
+    // ================= group 2: Sc, S update =================
+    if (tid == 0) {
+      if (OUT) {
+        for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
+          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+          mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8,
+                 smem_desc(sb + C::OFF_PHK + koff, 16, 1024, 2), IDESC_SC, ks > 0);
+        }
+      }
+      for (int mb = 0; mb < C::NMB; ++mb)
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ss(tmem + C::TM_S + mb * D,
+                 smem_desc(sb + C::OFF_PHK + (2 * mb) * 16384 + ks * 2048, 16384, 1024, 2),
+                 v_desc(ks), IDESC_SU, 1);
+      mma_commit(bar_mma);
+    }
+    if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
+    ph_mma ^= 1;
+    tc_fence_after();
+
+    if (!OUT) {
+      if (tid == 0 && t + 1 < t_end) issue_loads(t + 1);
+      if (__syncthreads_or(failed)) { failed = true; break; }
+      continue;
+    }
+
+    // ================= epilogue 2: P = bf16(tril(Sc)), row sums =================
+    {
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; c += 32) {
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * 64 + c, sv);
+        tmem_ld_wait();
+        uint32_t pw[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int key = half * 64 + c + j;
+          const float a0 = (key <= row) ? __uint_as_float(sv[j]) : 0.f;
+          const float a1 = (key + 1 <= row) ? __uint_as_float(sv[j + 1]) : 0.f;
+          const uint32_t w2 = pack_bf16(a0, a1);
+          pw[j / 2] = w2;
+          rs += bf16_lo(w2) + bf16_hi(w2);
+        }
+        // P panel: [128 rows][128 keys] K-major, key block = half (16 KB each)
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_panel_chunk(sb + C::OFF_PHK + half * 16384, row, c / 8 + q4, pw[4 * q4],
+                         pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
+      }
+      rs_s[half * 128 + row] = rs;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ================= group 3: O = P V + phi(Q) S_bf16 =================
+    if (tid == 0) {
+      for (int ks = 0; ks < kTile / 16; ++ks) {
+        const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+        mma_ss(tmem + C::TM_X, smem_desc(sb + C::OFF_PHK + koff, 16, 1024, 2), v_desc(ks),
+               IDESC_PV, ks > 0);
+      }
+      for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
+        uint64_t bdesc;
+        if (KIND == HH_FMAP_HEDGEHOG)
+          bdesc = smem_desc(sb + C::OFF_SB + ks * 2048, C::DP * 128, 1024, 2);
+        else
+          bdesc = smem_desc(sb + C::OFF_SB + ks * 512, 16, 256, 6);
+        mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8, bdesc, IDESC_QS, 1);
+      }
+      mma_commit(bar_mma);
+    }
+    if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
+    ph_mma ^= 1;
+    tc_fence_after();
+    if (tid == 0 && t + 1 < t_end && !failed) issue_loads(t + 1);
+
+    // ================= epilogue 3: y = O / den =================
+    {
+      const float den = (dq_s[row] + dq_s[128 + row]) + (rs_s[row] + rs_s[128 + row]);
+      const float inv = 1.f / den;
+      const bool valid = row < nvalid;
+      __nv_bfloat16* yrow =
+          reinterpret_cast<__nv_bfloat16*>(A.y) + ((size_t)unit * A.n + r0 + row) * D;
+      if (KIND == HH_FMAP_HEDGEHOG) {
+        constexpr int HC = D / 2;
+#pragma unroll
+        for (int c = 0; c < HC; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, ov);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + half * HC + c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int j = 8 * q4;
+              uint4 v4;
+              v4.x = pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+              v4.y = pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+              v4.z = pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+              v4.w = pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+              dst[q4] = v4;
+            }
+          }
+        }
+      } else {
+        if (half == 0) {
+          uint32_t ov[16];
+          tmem_ld16(tmem + lane_base(warp) + C::TM_X, ov);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow);
+#pragma unroll
+            for (int q4 = 0; q4 < 2; ++q4) {
+              const int j = 8 * q4;
+              uint4 v4;
+              v4.x = pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+              v4.y = pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+              v4.z = pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+              v4.w = pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+              dst[q4] = v4;
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    if (__syncthreads_or(failed)) { failed = true; break; }
+    tc_fence_after();
+  }
+
+  // ---- export the state ----
+  __syncthreads();
+  const bool export_out = OUT && A.S_out && seg == A.P - 1;
+  if (!failed && (!OUT || export_out)) {
+    float* Sdst = OUT ? A.S_out + (size_t)unit * C::DPP * D
+                      : A.ws_S + ((size_t)unit * (A.P - 1) + seg) * C::DPP * D;
+    float* zdst = OUT ? A.z_out + (size_t)unit * C::DPP
+                      : A.ws_z + ((size_t)unit * (A.P - 1) + seg) * C::DPP;
+    for (int mb = half; mb < C::NMB; mb += 2) {
+      const int f = mb * 128 + row;
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t sv[16];
+        tmem_ld16(tmem + lane_base(warp) + C::TM_S + mb * D + c0, sv);
+        tmem_ld_wait();
+        if (f < C::DPP) {
+          float4* dst = reinterpret_cast<float4*>(Sdst + (size_t)f * D + c0);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_float4(__uint_as_float(sv[4 * q4]), __uint_as_float(sv[4 * q4 + 1]),
+                                  __uint_as_float(sv[4 * q4 + 2]), __uint_as_float(sv[4 * q4 + 3]));
+        }
+      }
+    }
+    for (int f = tid; f < C::DPP; f += kThreads) zdst[f] = z_s[f];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map over [planes][rows][cols] with a {box_cols, box_rows, 1} box.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                     uint64_t planes, uint32_t box_cols, uint32_t box_rows,
+                     CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int D>
+static size_t smem_bytes() { return Smem<KIND, D>::ALLOC; }
+
+TcPlan plan_prefill_tc(const Problem& p) {
+  TcPlan pl;
+  pl.supported = (p.dtype == HH_BF16) &&
+                 ((p.kind == HH_FMAP_HEDGEHOG && (p.d == 64 || (p.d == 128 && !p.Wk))) ||
+                  (p.kind == HH_FMAP_TAYLOR2 && p.d == 16));
+  const int64_t U = p.B * p.H;
+  pl.NT = ceil_div(p.n, kTile);
+  const int per_sm = (p.kind == HH_FMAP_HEDGEHOG && p.d == 64) ? 2 : 1;
+  const int64_t slots = (int64_t)device_sm_count() * per_sm;
+  int64_t P = U > 0 ? std::max<int64_t>(1, slots / U) : 1;
+  const char* e = getenv("HH_PREFILL_SEGMENTS");
+  if (e && *e) P = std::max(1, atoi(e));
+  P = std::min<int64_t>(P, std::max(1, pl.NT));
+  pl.L = pl.NT > 0 ? ceil_div(pl.NT, P) : 1;
+  pl.P = pl.NT > 0 ? ceil_div(pl.NT, pl.L) : 1;
+  pl.launches = (pl.P > 1 ? 2 : 1);
+  pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * ((size_t)p.dpp * p.d + p.dpp) * sizeof(float)
+                         : 0;
+  return pl;
+}
+
+template <int KIND, int D>
+static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q, const void* k,
+                               const void* v, void* y, float* S_out, float* z_out, void* ws,
+                               int* dev_status, cudaStream_t s) {
+  PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t U = (uint64_t)p.B * p.H;
+  bool ok = true;
+  if (KIND == HH_FMAP_HEDGEHOG) {
+    ok &= make_map(&a.tq, q, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&a.tk, k, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&a.tv, v, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&a.twq, p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    ok &= make_map(&a.tq, q, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&a.tk, k, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&a.tv, v, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_32B);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  a.y = y;
+  a.ws_S = reinterpret_cast<float*>(ws);
+  a.ws_z = ws ? reinterpret_cast<float*>(ws) + U * (pl.P - 1) * (size_t)p.dpp * p.d : nullptr;
+  a.S_out = S_out;
+  a.z_out = z_out;
+  a.bq = p.bq;
+  a.bk = p.Wk ? p.bk : p.bq;
+  a.dev_status = dev_status;
+  a.soft_ns = wait_soft_limit_ns();
+  a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+  a.n = p.n;
+  a.H = p.H;
+  a.P = pl.P;
+  a.L = pl.L;
+  a.NT = pl.NT;
+  a.sep_wk = p.Wk ? 1 : 0;
+  const size_t smem = smem_bytes<KIND, D>();
+  if (pl.P > 1) {
+    auto kern = prefill_tc_kernel<KIND, D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  auto kern = prefill_tc_kernel<KIND, D, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)(U * pl.P), kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q, const void* k,
+                              const void* v, void* y, float* S_out, float* z_out, void* ws,
+                              int* dev_status, cudaStream_t s) {
+  if (p.kind == HH_FMAP_TAYLOR2)
+    return launch_kind<HH_FMAP_TAYLOR2, 16>(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
+  if (p.d == 64)
+    return launch_kind<HH_FMAP_HEDGEHOG, 64>(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
+  return launch_kind<HH_FMAP_HEDGEHOG, 128>(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
+}
+
+}  // namespace hh
