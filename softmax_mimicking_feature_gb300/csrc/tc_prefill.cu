@@ -19,9 +19,9 @@
 // the result is the same causal sum for chunk 64 or 128.
 //
 // Long sequences are cut into segments processed by different CTAs.  A
-// state pass (OUT_PASS = false) computes each segment's sum of phi(k)^T v and
-// phi(k) into the workspace; the output pass starts segment s from the sum of
-// the segments before it (added in segment order).
+// state pass (OUT = false) writes each segment's sum of phi(k)^T v and phi(k)
+// into the workspace, a scan kernel turns those into inclusive prefix sums
+// (in segment order), and the output pass starts segment s from prefix s-1.
 //
 // Roles: thread 0 issues TMA loads and MMAs; all 8 warps run the epilogues
 // (warp w owns TMEM lanes 32*(w%4).. and one half of the columns).  Every
@@ -118,8 +118,7 @@ struct Smem {
 struct PrefillArgs {
   CUtensorMap tq, tk, tv, twq, twk;
   void* y;
-  float* ws_S;      // [U][P-1][DPP][D]
-  float* ws_z;      // [U][P-1][DPP]
+  float* ws;        // [U][P-1][DPP*D + DPP]: segment states (S then z), scanned in place
   float* S_out;     // [U][DPP][D] or null
   float* z_out;     // [U][DPP] or null
   const float* bq;
@@ -216,59 +215,6 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     prefetch_tmap(&A.tv);
     if (OUT) prefetch_tmap(&A.tq);
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
-    tmem_relinquish();
-  }
-  if (KIND == HH_FMAP_HEDGEHOG) {
-    for (int i = tid; i < D; i += kThreads) {
-      bq_s[i] = A.bq ? A.bq[(size_t)h * D + i] : 0.f;
-      bk_s[i] = A.bk ? A.bk[(size_t)h * D + i] : 0.f;
-    }
-  }
-  // initial z: sum of the preceding segments' partial sums (output pass)
-  for (int f = tid; f < SM::ZN; f += kThreads) {
-    float acc = 0.f;
-    if (OUT && f < C::DPP)
-      for (int s2 = 0; s2 < seg; ++s2)
-        acc += A.ws_z[((size_t)unit * (A.P - 1) + s2) * C::DPP + f];
-    z_s[f] = acc;
-  }
-  if (KIND == HH_FMAP_TAYLOR2) {
-    // zero the phi(K) panels once: features >= 288 stay zero for the whole run
-    for (uint32_t i = tid * 16; i < C::PHK_PANELS * 16384u; i += kThreads * 16)
-      st_shared_v4(sb + C::OFF_PHK + i, 0, 0, 0, 0);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  // initial S in TMEM (zeros, or the preceding segments' sum)
-  {
-    for (int mb = half; mb < C::NMB; mb += 2) {
-      const int f = mb * 128 + row;
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t r[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float acc = 0.f;
-          if (OUT && f < C::DPP)
-            for (int s2 = 0; s2 < seg; ++s2)
-              acc += A.ws_S[(((size_t)unit * (A.P - 1) + s2) * C::DPP + f) * D + c0 + j];
-          r[j] = __float_as_uint(acc);
-        }
-        tmem_st16(tmem + lane_base(warp) + C::TM_S + mb * D + c0, r);
-      }
-    }
-    tmem_st_wait();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  uint32_t ph_load = 0, ph_w = 0, ph_mma = 0;
-
   // ---- loads of one tile ----
   auto issue_loads = [&](int t) {
     const int r0 = t * kTile;
@@ -286,7 +232,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
       tma_load_3d(sb + C::OFF_V, &A.tv, bar_load, 0, r0, (int)unit);
     }
   };
-
+  __syncthreads();  // barriers initialised before the first copy is issued
   if (tid == 0) {
     if (KIND == HH_FMAP_HEDGEHOG) {
       const int nmaps = A.sep_wk ? 2 : 1;
@@ -298,6 +244,68 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     }
     issue_loads(t_begin);
   }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  if (KIND == HH_FMAP_HEDGEHOG) {
+    for (int i = tid; i < D; i += kThreads) {
+      bq_s[i] = A.bq ? A.bq[(size_t)h * D + i] : 0.f;
+      bk_s[i] = A.bk ? A.bk[(size_t)h * D + i] : 0.f;
+    }
+  }
+  const size_t seg_elems = (size_t)C::DPP * D + C::DPP;
+  const float* prefix = (OUT && seg > 0) ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * seg_elems
+                                         : nullptr;
+  // initial z: the state of the tokens before this segment
+  for (int f = tid; f < SM::ZN; f += kThreads)
+    z_s[f] = (prefix && f < C::DPP) ? __ldcg(prefix + (size_t)C::DPP * D + f) : 0.f;
+  if (KIND == HH_FMAP_TAYLOR2) {
+    // zero the phi(K) panels once: features >= 288 stay zero for the whole run
+    for (uint32_t i = tid * 16; i < C::PHK_PANELS * 16384u; i += kThreads * 16)
+      st_shared_v4(sb + C::OFF_PHK + i, 0, 0, 0, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // initial S in TMEM: zeros, or the prefix state of the preceding segments
+  {
+    for (int mb = half; mb < C::NMB; mb += 2) {
+      const int f = mb * 128 + row;
+      const bool frow = prefix && f < C::DPP;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 64) {
+        constexpr int CW = D < 64 ? D : 64;
+        float4 v4[CW / 4];
+#pragma unroll
+        for (int j = 0; j < CW / 4; ++j)
+          v4[j] = frow ? __ldcg(reinterpret_cast<const float4*>(prefix + (size_t)f * D + c0) + j)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < CW; j += 16) {
+          uint32_t r[16];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            r[4 * e] = __float_as_uint(v4[j / 4 + e].x);
+            r[4 * e + 1] = __float_as_uint(v4[j / 4 + e].y);
+            r[4 * e + 2] = __float_as_uint(v4[j / 4 + e].z);
+            r[4 * e + 3] = __float_as_uint(v4[j / 4 + e].w);
+          }
+          tmem_st16(tmem + lane_base(warp) + C::TM_S + mb * D + c0 + j, r);
+        }
+      }
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  uint32_t ph_load = 0, ph_w = 0, ph_mma = 0;
+
+
 
   // descriptors of fixed operands
   constexpr uint32_t IDESC_H = idesc_bf16(128, D, 0, 1);       // X[K-major] * W[MN-major]
@@ -689,9 +697,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   const bool export_out = OUT && A.S_out && seg == A.P - 1;
   if (!failed && (!OUT || export_out)) {
     float* Sdst = OUT ? A.S_out + (size_t)unit * C::DPP * D
-                      : A.ws_S + ((size_t)unit * (A.P - 1) + seg) * C::DPP * D;
-    float* zdst = OUT ? A.z_out + (size_t)unit * C::DPP
-                      : A.ws_z + ((size_t)unit * (A.P - 1) + seg) * C::DPP;
+                      : A.ws + ((size_t)unit * (A.P - 1) + seg) * seg_elems;
+    float* zdst = OUT ? A.z_out + (size_t)unit * C::DPP : Sdst + (size_t)C::DPP * D;
     for (int mb = half; mb < C::NMB; mb += 2) {
       const int f = mb * 128 + row;
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -712,6 +719,25 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// In-place inclusive scan over the P-1 segment states of every unit, one
+// float4 position per thread, summed in segment order.
+__global__ void segment_scan_kernel(float4* __restrict__ ws, int64_t units, int pm1,
+                                    int64_t elems4) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= units * elems4) return;
+  const int64_t u = i / elems4, e = i % elems4;
+  float4* p = ws + (size_t)u * pm1 * elems4 + e;
+  float4 acc = p[0];
+  for (int s = 1; s < pm1; ++s) {
+    const float4 x = p[(size_t)s * elems4];
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
+    p[(size_t)s * elems4] = acc;
+  }
 }
 
 }  // namespace
@@ -773,7 +799,7 @@ TcPlan plan_prefill_tc(const Problem& p) {
   P = std::min<int64_t>(P, std::max(1, pl.NT));
   pl.L = pl.NT > 0 ? ceil_div(pl.NT, P) : 1;
   pl.P = pl.NT > 0 ? ceil_div(pl.NT, pl.L) : 1;
-  pl.launches = (pl.P > 1 ? 2 : 1);
+  pl.launches = pl.P > 2 ? 3 : (pl.P > 1 ? 2 : 1);
   pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * ((size_t)p.dpp * p.d + p.dpp) * sizeof(float)
                          : 0;
   return pl;
@@ -800,8 +826,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   }
   if (!ok) return cudaErrorInvalidValue;
   a.y = y;
-  a.ws_S = reinterpret_cast<float*>(ws);
-  a.ws_z = ws ? reinterpret_cast<float*>(ws) + U * (pl.P - 1) * (size_t)p.dpp * p.d : nullptr;
+  a.ws = reinterpret_cast<float*>(ws);
   a.S_out = S_out;
   a.z_out = z_out;
   a.bq = p.bq;
@@ -822,6 +847,13 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (pl.P > 2) {
+      const int64_t elems4 = ((int64_t)p.dpp * p.d + p.dpp) / 4;
+      const int64_t n4 = (int64_t)U * elems4;
+      segment_scan_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
+          reinterpret_cast<float4*>(ws), (int64_t)U, pl.P - 1, elems4);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   auto kern = prefill_tc_kernel<KIND, D, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

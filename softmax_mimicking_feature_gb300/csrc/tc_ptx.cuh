@@ -56,17 +56,26 @@ struct WaitPolicy {
   int* abort_flag;      // shared
 };
 
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitPolicy& w) {
-  const uint64_t t0 = globaltimer();
+__device__ __forceinline__ void report_timeout(const WaitPolicy& w) {
+  if (w.dev_status) atomicExch(w.dev_status, (int)HH_ERR_TIMEOUT);
+}
+
+// Slow path: t0 is the time the wait began (try_wait may already have
+// blocked inside the hardware for a while).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitPolicy& w,
+                                            uint64_t t0) {
   bool reported = false;
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test(bar, parity)) {
+      if (!reported && globaltimer() - t0 >= w.soft_ns) report_timeout(w);
+      return true;
+    }
     if (it == 1 || (it & 31) == 0) {
       if (*(volatile int*)w.abort_flag) return false;
       const uint64_t dt = globaltimer() - t0;
       if (!reported && dt >= w.soft_ns) {
         reported = true;
-        if (w.dev_status) atomicExch(w.dev_status, (int)HH_ERR_TIMEOUT);
+        report_timeout(w);
       }
       if (dt >= w.hard_ns) {
         *(volatile int*)w.abort_flag = 1;
@@ -76,9 +85,15 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const
   }
 }
 
+// Bounded wait for the given phase parity of an mbarrier.  The elapsed time
+// counts from entry, including any time try_wait spends suspended.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitPolicy& w) {
-  if (mbar_test(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, w);
+  const uint64_t t0 = globaltimer();
+  if (mbar_test(bar, parity)) {
+    if (globaltimer() - t0 >= w.soft_ns) report_timeout(w);
+    return true;
+  }
+  return mbar_wait_slow(bar, parity, w, t0);
 }
 
 // ---- TMA ------------------------------------------------------------------

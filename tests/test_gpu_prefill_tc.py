@@ -58,7 +58,7 @@ def test_segment_count_does_not_change_the_result(case, segments, env):
     w, x, xd, fm = _setup(case, seed=31)
     P, launches = hh.fwd_plan(fm, w.torch_dtype, w.B, w.H, w.n, 64)
     assert P == min(segments, (w.n + 127) // 128) or P <= segments
-    assert launches == (2 if P > 1 else 1)
+    assert launches == (1 if P == 1 else (2 if P == 2 else 3))
     y, S, z = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"], chunk=64, return_state=True)
     torch.cuda.synchronize()
     W = None if x["W"] is None else f64(x["W"])
@@ -78,7 +78,7 @@ def test_segment_count_does_not_change_the_result(case, segments, env):
 def test_plan_splits_long_sequences():
     w, x, xd, fm = _setup("llama_d128", seed=1)
     P, launches = hh.fwd_plan(fm, torch.bfloat16, 1, 32, 4096, 64)
-    assert P > 1 and launches == 2
+    assert P > 1 and launches == (2 if P == 2 else 3)
     need = hh.fwd_workspace_bytes(fm, torch.bfloat16, 1, 32, 4096, 64)
     assert need >= 32 * (P - 1) * (256 * 128 + 256) * 4
 
