@@ -148,6 +148,24 @@ HH_API hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const voi
                                 float* S_out, float* z_out, void* workspace, size_t ws_bytes,
                                 int* dev_status, void* stream);
 
+/* hh_linattn_fwd_causal without a workspace argument.  The paper has no
+ * counterpart to this entry point: it exists for callers that cannot allocate
+ * device memory when they run the prefill (a plugin interface that only
+ * passes its input and output buffers, a serving loop that forbids allocation
+ * after start-up, a C host program without a device allocator).  Arguments
+ * and results are those of hh_linattn_fwd_causal.
+ * Scratch: a fixed 16 MiB device array inside the library, present on every
+ * GPU that loads the library until the process exits.  A problem needing more
+ * scratch than that (hh_fwd_workspace_bytes > 16 MiB) returns
+ * HH_ERR_WORKSPACE and launches nothing.  The first call on each device looks
+ * up the array's address once; make it before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU race and must not be issued.
+ * Nothing is allocated by this call. */
+HH_API hh_status hh_linattn_fwd_causal_noalloc(const hh_fmap* fmap, int dtype, const void* q,
+                                               const void* k, const void* v, int64_t B, int H,
+                                               int64_t n, int chunk, void* y, float* S_out,
+                                               float* z_out, int* dev_status, void* stream);
+
 /* One recurrent decode step for B sequences x H heads.
  * Source: "Complexity Analysis" (running sums S and z, output
  * phi(q_t) S_t / phi(q_t).z_t); the state after the step includes token t.
