@@ -171,6 +171,8 @@ hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, int is_k
   const float* b = is_key && p.Wk ? p.bk : p.bq;
   if ((st = check_ptrs_aligned({x, phi_out, W, b})) != HH_OK) return st;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;
+  if (fmap_tc_supported(p))
+    return cuda_status(launch_fmap_tc(p, x, is_key, phi_out, nullptr, (cudaStream_t)stream));
   return cuda_status(launch_fmap_simt(p, x, is_key, phi_out, (cudaStream_t)stream));
 }
 
@@ -280,6 +282,13 @@ hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const v
   void* phq = ws;
   void* phk = ws + phi_bytes;
   float* partial = (float*)(ws + 2 * phi_bytes);
+  if (fmap_tc_supported(p)) {
+    cudaError_t e = launch_fmap_tc(p, q, 0, phq, dev_status, s);
+    if (e == cudaSuccess) e = launch_fmap_tc(p, k, 1, phk, dev_status, s);
+    if (e == cudaSuccess)
+      e = launch_loss_tc(p, q, k, phq, phk, loss_rows, partial, loss_head_sum, dev_status, s);
+    return cuda_status(e);
+  }
   cudaError_t e = launch_fmap_simt(p, q, 0, phq, s);
   if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, s);
   if (e == cudaSuccess)

@@ -70,6 +70,15 @@ cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q,
                               const void* v, void* y, float* S_out, float* z_out, void* ws,
                               int* dev_status, cudaStream_t s);
 
+// Tensor-core (tcgen05) feature map and mimicry loss for bf16 Hedgehog d in {64, 128}.
+bool fmap_tc_supported(const Problem& p);
+cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,
+                           int* dev_status, cudaStream_t s);
+cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
+                           const void* phk, float* loss_rows, float* partial, float* head_sum,
+                           int* dev_status, cudaStream_t s);
+int loss_tc_tile();
+
 // Decode step (SIMT, HBM-streaming).
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
                           float* S, float* z, void* y, cudaStream_t s);

@@ -1,0 +1,480 @@
+// Tensor-core Hedgehog feature map and attention-weight distillation loss.
+//
+// "The Hedgehog & the Porcupine" summary: "The Hedgehog MLP Feature Map"
+// (Choices 1 and 3) for phi(x) = [exp(xW + b); exp(-(xW + b))], and "The
+// Attention Weight Distillation Loss" (paper Eq. 4) for
+//   L_i = -sum_{j<=i} softmax_j(q_i.k_j / sqrt d) log(a_ij / sum_{m<=i} a_im),
+//   a_ij = phi(q_i).phi(k_j).
+//
+// fmap_tc_kernel: one CTA per 128-row tile of one (batch, head) sequence.
+//   H = X W on tcgen05 (fp32 in TMEM); the epilogue adds b, exponentiates
+//   both signs and stores phi rows as bf16.
+//
+// loss_tc_kernel: one CTA per (batch*head, 128-query tile); key tiles of 128
+//   run j = 0 .. i.  A producer warp TMA-loads K_j and phi(K_j) and issues
+//   S = Q K_j^T and A = phi(Q) phi(K_j)^T into one of two TMEM stages; eight
+//   epilogue warps keep, per query row, an online-softmax state
+//     m (running max of s log2 e), Z = sum 2^{s' - m}, T = sum 2^{s' - m} log2 a,
+//     Asum = sum a
+//   so that L = ln Asum - ln 2 * T / Z, which equals Eq. 4 because the target
+//   weights sum to one.  The smem operands of tile j+1 are loaded as soon as
+//   the MMAs of tile j have read them, and those MMAs run while the epilogue
+//   works on tile j.
+
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "tc_ptx.cuh"
+
+namespace hh {
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map over [planes][rows][cols], {64, box_rows, 1} boxes, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+              uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__device__ __forceinline__ uint32_t lane_base(int warp) {
+  return (uint32_t)(32 * (warp & 3)) << 16;
+}
+
+// ===========================================================================
+// feature map
+// ===========================================================================
+struct FmapArgs {
+  CUtensorMap tx, tw;
+  __nv_bfloat16* phi;   // [U][n][2D]
+  const float* bias;    // [H][D] or null
+  int* dev_status;
+  uint64_t soft_ns, hard_ns;
+  int64_t n;
+  int H;
+  int NT;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ FmapArgs A) {
+  constexpr uint32_t W_BYTES = D * D * 2, X_BYTES = kTile * D * 2;
+  constexpr uint32_t TM_COLS = D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t OFF_W = 0, OFF_X = W_BYTES;
+  float* bias_s = reinterpret_cast<float*>(sm + W_BYTES + X_BYTES);
+  const uint32_t bar_load = smem_u32(bias_s + 128);
+  const uint32_t bar_mma = bar_load + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bias_s + 128 + 4);
+  int* abort_flag = reinterpret_cast<int*>(bias_s + 128 + 5);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = warp >> 2, row = 32 * (warp & 3) + lane;
+  const int64_t unit = blockIdx.x / A.NT;
+  const int t = blockIdx.x % A.NT;
+  const int h = (int)(unit % A.H);
+  const int64_t r0 = (int64_t)t * kTile;
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+
+  if (tid == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_expect_tx(bar_load, W_BYTES + X_BYTES);
+    for (int i = 0; i < D / 64; ++i) {
+      tma_load_3d(sb + OFF_W + i * (D * 128), &A.tw, bar_load, 64 * i, 0, h);
+      tma_load_3d(sb + OFF_X + i * 16384, &A.tx, bar_load, 64 * i, (int)r0, (int)unit);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    tmem_relinquish();
+  }
+  for (int i = tid; i < D; i += 256) bias_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  if (tid == 0) {
+    ok = mbar_wait(bar_load, 0, wp);
+    tc_fence_after();
+    if (ok) {
+      constexpr uint32_t IDESC = idesc_bf16(128, D, 0, 1);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+        mma_ss(tmem, smem_desc(sb + OFF_X + koff, 16, 1024, 2),
+               smem_desc(sb + OFF_W + ks * 2048, D * 128, 1024, 2), IDESC, ks > 0);
+      }
+      mma_commit(bar_mma);
+    }
+  }
+  if (__syncthreads_or(!ok)) {
+    ok = false;
+  } else {
+    ok = mbar_wait(bar_mma, 0, wp);
+    tc_fence_after();
+  }
+  if (__syncthreads_and(ok)) {
+    constexpr int HC = D / 2;
+    const bool valid = r0 + row < A.n;
+    __nv_bfloat16* prow = A.phi + ((size_t)unit * A.n + r0 + row) * (2 * D);
+#pragma unroll
+    for (int c = 0; c < HC; c += 32) {
+      uint32_t hv[32];
+      tmem_ld32(tmem + lane_base(warp) + half * HC + c, hv);
+      uint32_t pp[16], pn[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const int l = half * HC + c + j;
+        const float h0 = __uint_as_float(hv[j]) + bias_s[l];
+        const float h1 = __uint_as_float(hv[j + 1]) + bias_s[l + 1];
+        pp[j / 2] = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
+        pn[j / 2] = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+      }
+      if (valid) {
+        uint4* dp = reinterpret_cast<uint4*>(prow + half * HC + c);
+        uint4* dn = reinterpret_cast<uint4*>(prow + D + half * HC + c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          dp[q4] = make_uint4(pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
+          dn[q4] = make_uint4(pn[4 * q4], pn[4 * q4 + 1], pn[4 * q4 + 2], pn[4 * q4 + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+// ===========================================================================
+// mimicry loss
+// ===========================================================================
+struct LossArgs {
+  CUtensorMap tq, tk, tpq, tpk;
+  float* loss_rows;    // [U][n] or null
+  float* partial;      // [U][NT]
+  int* dev_status;
+  uint64_t soft_ns, hard_ns;
+  int64_t n;
+  int64_t U;
+  int NT;
+  float s_scale;       // log2(e) / sqrt(d)
+};
+
+template <int D>
+struct LossCfg {
+  static constexpr int DP = 2 * D;
+  static constexpr uint32_t Q_BYTES = kTile * D * 2;
+  static constexpr uint32_t PQ_BYTES = kTile * DP * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_PQ = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_K = OFF_PQ + PQ_BYTES;
+  static constexpr uint32_t OFF_PK = OFF_K + Q_BYTES;
+  static constexpr uint32_t OFF_END = OFF_PK + PQ_BYTES;
+  // scalars
+  static constexpr uint32_t OFF_ST = OFF_END;              // float[4][128]: m, Z, T, Asum (half 1)
+  static constexpr uint32_t OFF_RL = OFF_ST + 4 * 128 * 4; // float[128] row losses
+  static constexpr uint32_t OFF_BAR = OFF_RL + 128 * 4;    // 8 x u64
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * 8;
+  static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
+};
+
+constexpr int kLossThreads = 288;  // 8 epilogue warps + 1 producer warp
+
+template <int D>
+__global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_constant__ LossArgs A) {
+  using C = LossCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* st_s = reinterpret_cast<float*>(sm + C::OFF_ST);
+  float* rl_s = reinterpret_cast<float*>(sm + C::OFF_RL);
+  const uint32_t bar_q = sb + C::OFF_BAR;        // Q, phi(Q) loaded
+  const uint32_t bar_kv = bar_q + 8;             // K_j, phi(K_j) loaded
+  const uint32_t bar_mma0 = bar_q + 16;          // stage 0 MMAs done (2 barriers)
+  const uint32_t bar_free0 = bar_q + 32;         // stage 0 drained by the epilogue (2 barriers)
+  const uint32_t bar_smem = bar_q + 48;          // smem K/phiK no longer read by MMAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heavy query tiles first: block b -> query tile NT-1 - b / U
+  const int qt = A.NT - 1 - (int)(blockIdx.x / A.U);
+  const int64_t unit = blockIdx.x % A.U;
+  const int64_t q0 = (int64_t)qt * kTile;
+  const int nkt = qt + 1;
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+
+  if (tid == 0) {
+    mbar_init(bar_q, 1);
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_mma0, 1);
+    mbar_init(bar_mma0 + 8, 1);
+    mbar_init(bar_free0, 8);
+    mbar_init(bar_free0 + 8, 8);
+    mbar_init(bar_smem, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+
+  if (warp == 8) {
+    // ---------------- producer: TMA + MMA issue ----------------
+    if (lane == 0) {
+      auto load_kv = [&](int j) {
+        mbar_expect_tx(bar_kv, C::Q_BYTES + C::PQ_BYTES);
+        for (int i = 0; i < D / 64; ++i)
+          tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_kv, 64 * i, j * kTile, (int)unit);
+        for (int i = 0; i < C::DP / 64; ++i)
+          tma_load_3d(sb + C::OFF_PK + i * 16384, &A.tpk, bar_kv, 64 * i, j * kTile, (int)unit);
+      };
+      mbar_expect_tx(bar_q, C::Q_BYTES + C::PQ_BYTES);
+      for (int i = 0; i < D / 64; ++i)
+        tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, (int)unit);
+      for (int i = 0; i < C::DP / 64; ++i)
+        tma_load_3d(sb + C::OFF_PQ + i * 16384, &A.tpq, bar_q, 64 * i, (int)q0, (int)unit);
+      load_kv(0);
+      bool ok = mbar_wait(bar_q, 0, wp);
+      constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int stg = j & 1;
+        ok = mbar_wait(bar_kv, j & 1, wp);                              // K_j landed
+        if (ok && j >= 2) ok = mbar_wait(bar_free0 + 8 * stg, ((j >> 1) - 1) & 1, wp);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ts = tmem + stg * 256;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+          mma_ss(ts, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2),
+                 smem_desc(sb + C::OFF_K + koff, 16, 1024, 2), IDESC, ks > 0);
+        }
+        for (int ks = 0; ks < C::DP / 16; ++ks) {
+          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+          mma_ss(ts + 128, smem_desc(sb + C::OFF_PQ + koff, 16, 1024, 2),
+                 smem_desc(sb + C::OFF_PK + koff, 16, 1024, 2), IDESC, ks > 0);
+        }
+        mma_commit(bar_mma0 + 8 * stg);
+        mma_commit(bar_smem);
+        if (j + 1 < nkt) {
+          ok = mbar_wait(bar_smem, j & 1, wp);                          // MMAs read smem
+          if (ok) load_kv(j + 1);
+        }
+      }
+      if (!ok) failed = true;
+    }
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int half = warp >> 2, row = 32 * (warp & 3) + lane;
+    const int64_t qi = q0 + row;
+    float m = -INFINITY, Z = 0.f, T = 0.f, As = 0.f;
+    for (int j = 0; j < nkt; ++j) {
+      const int stg = j & 1;
+      if (!mbar_wait(bar_mma0 + 8 * stg, (j >> 1) & 1, wp)) { failed = true; break; }
+      tc_fence_after();
+      const int64_t k0 = (int64_t)j * kTile + half * 64;
+#pragma unroll
+      for (int c = 0; c < 64; c += 32) {
+        uint32_t sv[32], av[32];
+        tmem_ld32(tmem + lane_base(warp) + stg * 256 + half * 64 + c, sv);
+        tmem_ld32(tmem + lane_base(warp) + stg * 256 + 128 + half * 64 + c, av);
+        // keys admitted for this row: k <= qi and k < n
+        const int64_t kmax = min(qi, A.n - 1);
+        const int nval = (int)max((int64_t)0, min((int64_t)32, kmax - (k0 + c) + 1));
+        float cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e < nval) cm = fmaxf(cm, __uint_as_float(sv[e]) * A.s_scale);
+        if (cm != -INFINITY) {
+          const float mn = fmaxf(m, cm);
+          const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+          Z *= f;
+          T *= f;
+          m = mn;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (e < nval) {
+              const float a = __uint_as_float(av[e]);
+              const float p = ex2_approx(__uint_as_float(sv[e]) * A.s_scale - m);
+              Z += p;
+              T = fmaf(p, __log2f(a), T);
+              As += a;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_free0 + 8 * stg) : "memory");
+    }
+    // merge the two column halves of each row
+    if (half == 1) {
+      st_s[row] = m;
+      st_s[128 + row] = Z;
+      st_s[256 + row] = T;
+      st_s[384 + row] = As;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (half == 0) {
+      const float m2 = st_s[row], Z2 = st_s[128 + row], T2 = st_s[256 + row], A2 = st_s[384 + row];
+      const float mn = fmaxf(m, m2);
+      const float f1 = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+      const float f2 = (m2 == -INFINITY) ? 0.f : ex2_approx(m2 - mn);
+      const float Zt = Z * f1 + Z2 * f2, Tt = T * f1 + T2 * f2, At = As + A2;
+      const bool valid = qi < A.n;
+      const float L = valid ? (logf(At) - 0.69314718055994531f * (Tt / Zt)) : 0.f;
+      rl_s[row] = L;
+      if (valid && A.loss_rows) A.loss_rows[(size_t)unit * A.n + qi] = L;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (tid == 0) {
+      float acc = 0.f;
+      for (int r = 0; r < kTile; ++r) acc += rl_s[r];
+      A.partial[(size_t)unit * A.NT + qt] = acc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+  (void)failed;
+}
+
+__global__ void sum_partials_tc_kernel(const float* __restrict__ partial, float* __restrict__ out,
+                                       int64_t heads, int ntiles) {
+  const int64_t bh = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (bh >= heads) return;
+  float acc = 0.f;
+  for (int t = 0; t < ntiles; ++t) acc += partial[(size_t)bh * ntiles + t];
+  out[bh] = acc;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+bool fmap_tc_supported(const Problem& p) {
+  return p.dtype == HH_BF16 && p.kind == HH_FMAP_HEDGEHOG && (p.d == 64 || p.d == 128);
+}
+
+template <int D>
+static cudaError_t fmap_tc_t(const Problem& p, const void* x, int is_key, void* phi,
+                             int* dev_status, cudaStream_t s) {
+  FmapArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t U = (uint64_t)p.B * p.H;
+  const void* W = is_key && p.Wk ? p.Wk : p.Wq;
+  if (!make_map(&a.tx, x, D, p.n, U, kTile) || !make_map(&a.tw, W, D, D, p.H, D))
+    return cudaErrorInvalidValue;
+  a.phi = reinterpret_cast<__nv_bfloat16*>(phi);
+  a.bias = is_key && p.Wk ? p.bk : p.bq;
+  a.dev_status = dev_status;
+  a.soft_ns = wait_soft_limit_ns();
+  a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+  a.n = p.n;
+  a.H = p.H;
+  a.NT = ceil_div(p.n, kTile);
+  const size_t smem = D * D * 2 + kTile * D * 2 + 128 * 4 + 64 + 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(fmap_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  fmap_tc_kernel<D><<<(unsigned)(U * a.NT), 256, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,
+                           int* dev_status, cudaStream_t s) {
+  if (p.B * p.H * p.n == 0) return cudaSuccess;
+  return p.d == 64 ? fmap_tc_t<64>(p, x, is_key, phi, dev_status, s)
+                   : fmap_tc_t<128>(p, x, is_key, phi, dev_status, s);
+}
+
+template <int D>
+static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, const void* phq,
+                             const void* phk, float* loss_rows, float* partial, float* head_sum,
+                             int* dev_status, cudaStream_t s) {
+  LossArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t U = (uint64_t)p.B * p.H;
+  bool ok = make_map(&a.tq, q, D, p.n, U, kTile) && make_map(&a.tk, k, D, p.n, U, kTile) &&
+            make_map(&a.tpq, phq, 2 * D, p.n, U, kTile) && make_map(&a.tpk, phk, 2 * D, p.n, U, kTile);
+  if (!ok) return cudaErrorInvalidValue;
+  a.loss_rows = loss_rows;
+  a.partial = partial;
+  a.dev_status = dev_status;
+  a.soft_ns = wait_soft_limit_ns();
+  a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+  a.n = p.n;
+  a.U = (int64_t)U;
+  a.NT = ceil_div(p.n, kTile);
+  a.s_scale = 1.4426950408889634f / sqrtf((float)D);
+  const size_t smem = LossCfg<D>::ALLOC;
+  cudaError_t e =
+      cudaFuncSetAttribute(loss_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  loss_tc_kernel<D><<<(unsigned)(U * a.NT), kLossThreads, smem, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  sum_partials_tc_kernel<<<ceil_div(U, 128), 128, 0, s>>>(partial, head_sum, (int64_t)U, a.NT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
+                           const void* phk, float* loss_rows, float* partial, float* head_sum,
+                           int* dev_status, cudaStream_t s) {
+  return p.d == 64 ? loss_tc_t<64>(p, q, k, phq, phk, loss_rows, partial, head_sum, dev_status, s)
+                   : loss_tc_t<128>(p, q, k, phq, phk, loss_rows, partial, head_sum, dev_status, s);
+}
+
+int loss_tc_tile() { return kTile; }
+
+}  // namespace hh

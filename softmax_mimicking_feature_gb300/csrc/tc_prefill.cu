@@ -791,8 +791,9 @@ TcPlan plan_prefill_tc(const Problem& p) {
                   (p.kind == HH_FMAP_TAYLOR2 && p.d == 16));
   const int64_t U = p.B * p.H;
   pl.NT = ceil_div(p.n, kTile);
-  const int per_sm = (p.kind == HH_FMAP_HEDGEHOG && p.d == 64) ? 2 : 1;
-  const int64_t slots = (int64_t)device_sm_count() * per_sm;
+  // One sequence per CTA while there are at least as many sequences as SMs;
+  // below that, split each sequence so the grid covers the SMs once.
+  const int64_t slots = (int64_t)device_sm_count();
   int64_t P = U > 0 ? std::max<int64_t>(1, slots / U) : 1;
   const char* e = getenv("HH_PREFILL_SEGMENTS");
   if (e && *e) P = std::max(1, atoi(e));

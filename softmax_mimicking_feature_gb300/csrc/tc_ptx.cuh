@@ -62,7 +62,7 @@ __device__ __forceinline__ void report_timeout(const WaitPolicy& w) {
 
 // Slow path: t0 is the time the wait began (try_wait may already have
 // blocked inside the hardware for a while).
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitPolicy& w,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitPolicy& w,
                                             uint64_t t0) {
   bool reported = false;
   for (uint32_t it = 1;; ++it) {
