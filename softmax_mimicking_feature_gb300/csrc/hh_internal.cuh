@@ -70,6 +70,11 @@ cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q,
                               const void* v, void* y, float* S_out, float* z_out, void* ws,
                               int* dev_status, cudaStream_t s);
 
+// Output pass of the d = 64 Hedgehog prefill with two tiles in flight per CTA.
+cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const void* q,
+                                   const void* k, const void* v, void* y, float* S_out,
+                                   float* z_out, const void* ws, int* dev_status, cudaStream_t s);
+
 // Tensor-core (tcgen05) feature map and mimicry loss for bf16 Hedgehog d in {64, 128}.
 bool fmap_tc_supported(const Problem& p);
 cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,

@@ -477,4 +477,5 @@ cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const
 
 int loss_tc_tile() { return kTile; }
 
+
 }  // namespace hh

@@ -161,6 +161,55 @@ __device__ __forceinline__ void st_panel_chunk(uint32_t panel, int r, int chunk,
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
+// ---- Taylor feature construction with compile-time feature indices ----
+// feature f of [1, x, x_i x_j / sqrt2 (i-major)], zero past 1 + 16 + 256
+__device__ __forceinline__ float taylor_feature(int f, const float (&x)[16]) {
+  if (f == 0) return 1.f;
+  if (f <= 16) return x[f - 1];
+  if (f <= 272) return x[(f - 17) >> 4] * x[(f - 17) & 15] * kInvSqrt2;
+  return 0.f;
+}
+
+// 32 features starting at FB as 16 bf16 pairs
+template <int FB>
+__device__ __forceinline__ void taylor_chunk(const float (&x)[16], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(taylor_feature(FB + j, x), taylor_feature(FB + j + 1, x));
+}
+
+// phi(q) chunk into TMEM (packed column FB/2), adding its part of phi(q) . z
+template <int FB>
+__device__ __forceinline__ void taylor_q_chunk(const float (&x)[16], const float* z, uint32_t taddr,
+                                               float& dq) {
+  uint32_t w[16];
+  taylor_chunk<FB>(x, w);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) dq += bf16_lo(w[j]) * z[FB + 2 * j] + bf16_hi(w[j]) * z[FB + 2 * j + 1];
+  tmem_st16(taddr + FB / 2, w);
+}
+
+// phi(k) chunk into the swizzled panels, column sums of the warp into zp[FB + lane]
+template <int FB>
+__device__ __forceinline__ void taylor_k_chunk(const float (&x)[16], bool valid, uint32_t phk,
+                                               int row, float* zp, int lane) {
+  uint32_t w[16];
+  taylor_chunk<FB>(x, w);
+  float e[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (!valid) w[j] = 0u;
+    e[2 * j] = bf16_lo(w[j]);
+    e[2 * j + 1] = bf16_hi(w[j]);
+  }
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4)
+    st_shared_v4(phk + (FB / 64) * 16384 + sw128_chunk(row, (FB % 64) / 8 + q4), w[4 * q4],
+                 w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+  warp_transpose_sum(e, lane);
+  zp[FB + lane] = e[0];
+}
+
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -401,27 +450,18 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(qrow[i]);
         // half 0 builds features [0, 160) = packed columns [0, 80); half 1 [160, 288)
-        const int f0 = half ? 160 : 0, f1 = half ? 288 : 160;
-        for (int fb = f0; fb < f1; fb += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float v2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int f = fb + j + e;
-              float val;
-              if (f == 0) val = 1.f;
-              else if (f <= 16) val = x[f - 1];
-              else if (f <= 272) { const int p = f - 17; val = x[p >> 4] * x[p & 15] * kInvSqrt2; }
-              else val = 0.f;
-              v2[e] = val;
-            }
-            const uint32_t w2 = pack_bf16(v2[0], v2[1]);
-            pk[j / 2] = w2;
-            dq += bf16_lo(w2) * z_s[fb + j] + bf16_hi(w2) * z_s[fb + j + 1];
-          }
-          tmem_st16(tmem + lane_base(warp) + C::TM_Y + fb / 2, pk);
+        const uint32_t ty = tmem + lane_base(warp) + C::TM_Y;
+        if (half == 0) {
+          taylor_q_chunk<0>(x, z_s, ty, dq);
+          taylor_q_chunk<32>(x, z_s, ty, dq);
+          taylor_q_chunk<64>(x, z_s, ty, dq);
+          taylor_q_chunk<96>(x, z_s, ty, dq);
+          taylor_q_chunk<128>(x, z_s, ty, dq);
+        } else {
+          taylor_q_chunk<160>(x, z_s, ty, dq);
+          taylor_q_chunk<192>(x, z_s, ty, dq);
+          taylor_q_chunk<224>(x, z_s, ty, dq);
+          taylor_q_chunk<256>(x, z_s, ty, dq);
         }
       }
       dq_s[half * 128 + row] = dq;
@@ -471,35 +511,19 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
         float x[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(krow[i]);
-        const int f0 = half ? 160 : 0, f1 = half ? 288 : 160;
-        for (int fb = f0; fb < f1; fb += 32) {
-          float e[32];
-          uint32_t wv[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float v2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int f = fb + j + u;
-              float val;
-              if (f == 0) val = 1.f;
-              else if (f <= 16) val = x[f - 1];
-              else if (f <= 272) { const int p = f - 17; val = x[p >> 4] * x[p & 15] * kInvSqrt2; }
-              else val = 0.f;
-              v2[u] = val;
-            }
-            uint32_t w2 = pack_bf16(v2[0], v2[1]);
-            if (!valid) w2 = 0u;
-            wv[j / 2] = w2;
-            e[j] = bf16_lo(w2);
-            e[j + 1] = bf16_hi(w2);
-          }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            st_panel_chunk(sb + C::OFF_PHK + (fb / 64) * 16384, row, (fb % 64) / 8 + q4,
-                           wv[4 * q4], wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
-          warp_transpose_sum(e, lane);
-          zp_s[g * SM::ZN + fb + lane] = e[0];
+        const uint32_t phk = sb + C::OFF_PHK;
+        float* zp = zp_s + g * SM::ZN;
+        if (half == 0) {
+          taylor_k_chunk<0>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<32>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<64>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<96>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<128>(x, valid, phk, row, zp, lane);
+        } else {
+          taylor_k_chunk<160>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<192>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<224>(x, valid, phk, row, zp, lane);
+          taylor_k_chunk<256>(x, valid, phk, row, zp, lane);
         }
       }
     }
@@ -856,6 +880,8 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
+  if (KIND == HH_FMAP_HEDGEHOG && D == 64)
+    return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
   auto kern = prefill_tc_kernel<KIND, D, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

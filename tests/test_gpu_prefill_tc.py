@@ -116,3 +116,4 @@ def test_first_row_equals_first_value():
         y = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"])
         torch.cuda.synchronize()
         np.testing.assert_allclose(f64(y)[:, :, 0], f64(x["v"])[:, :, 0], rtol=2 ** -7, atol=1e-6)
+
