@@ -522,20 +522,62 @@ def other_rows(torch, hh, wl, dev, peaks, l2):
     return rows
 
 
+def run_row(args):
+    """One hot-path row alone (for profiling): prefill:<workload>, loss:<workload>, decode."""
+    import torch
+    import softmax_mimicking_feature_gb300 as hh
+    from softmax_mimicking_feature_gb300 import workloads as wl
+    from softmax_mimicking_feature_gb300 import _abi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _abi.lib()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2**20)
+    kind, _, name = args.row.partition(":")
+    if kind == "prefill":
+        w = wl.WORKLOADS[name]
+        r = bench_prefill(torch, hh, wl, w, args.steps, args.warmup, dev, l2=l2)
+        s = r["ms_total"] / 1e3 / args.steps
+        out = {"row": args.row, "us_per_call": s * 1e6, "tokens_per_s": w.B * w.n / s,
+               "hbm_gbs_alg": r["counts"]["bytes"] / s / 1e9, "segments": r["segments"]}
+    elif kind == "loss":
+        w = wl.WORKLOADS[name]
+        r = bench_loss(torch, hh, wl, w, args.steps, args.warmup, dev)
+        s = r["ms_total"] / 1e3 / args.steps
+        out = {"row": args.row, "us_per_call": s * 1e6, "pairs_per_s": r["counts"]["pairs"] / s}
+    elif kind == "decode":
+        w = wl.WORKLOADS["llama2_decode_128x32_d128"]
+        if args.decode_seqs:
+            w = w.with_(B=args.decode_seqs)
+        r = bench_decode(torch, hh, wl, w, args.steps, args.warmup, dev)
+        s = r["ms_total"] / 1e3 / args.steps
+        out = {"row": args.row, "B": w.B, "us_per_step": s * 1e6,
+               "gb_per_s": r["counts"]["bytes"] / s / 1e9}
+    else:
+        raise SystemExit(f"unknown row {args.row!r}")
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=30000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--row", default=None,
+                    help="time one row alone: prefill:<workload>, loss:<workload> or decode")
+    ap.add_argument("--decode-seqs", type=int, default=0,
+                    help="with --row decode: number of sequences (default: the workload's 128)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.row:
+        return run_row(args)
     return run_ours(args)
 
 
