@@ -880,7 +880,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
-  if (KIND == HH_FMAP_HEDGEHOG && D == 64)
+  if (KIND == HH_FMAP_HEDGEHOG && D == 64 && !p.Wk)
     return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
   auto kern = prefill_tc_kernel<KIND, D, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

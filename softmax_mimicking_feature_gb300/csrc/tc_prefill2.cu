@@ -10,15 +10,17 @@
 //     G1(t): H_Q = Q_t W, H_K = K_t W
 //     G2(t): Sc = phi(Q_t) phi(K_t)^T;  S += phi(K_t)^T V_t;  Z += phi(K_t)^T 1
 //     G3(t): O = P_t V_t + phi(Q_t) S_bf16(t)
-//   warps 0-3 / 4-7 (two epilogue groups) take alternate tiles:
+//   warps 0-7 (epilogue) run the phases below for both slots, interleaved as
+//   E2(t-1), E1(t), E3(t-1):
 //     E1 : phi(Q_t) -> TMEM (bf16 pairs), phi(K_t) -> smem          (after G1(t))
 //          S_bf16(t) <- S, z(t) <- Z  (state of the tokens before t)  (after G2(t-1))
 //          -- only then may G2(t) update S --
 //          den(t) = phi(Q_t) . z(t)
 //     E2 : P_t = bf16(tril(Sc)), den += rowsum                      (after G2(t))
 //     E3 : y = O / den                                              (after G3(t))
-// Each group owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (Q/K ->
-// S_bf16, V, phi(K) -> P); the running state S (fp32) and its normaliser Z
+// Each tile owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (Q, K, V,
+// S_bf16, phi(K) -> P); the next tile's Q and K are fetched as soon as
+// H = X W has read the current ones; the running state S (fp32) and its normaliser Z
 // (fp32, as an MMA with an all-ones operand) stay in TMEM and pass between
 // the groups in tile order.  All mbarrier waits are bounded (tc_ptx.cuh).
 
@@ -44,31 +46,35 @@ __host__ __device__ constexpr uint32_t TM_Y(int s) { return 128 + 192 * s; }    
 __host__ __device__ constexpr uint32_t TM_X(int s) { return 128 + 192 * s + 64; }   // 128 cols
 
 // shared memory
-constexpr uint32_t OFF_W = 0, OFF_WK = 8192, OFF_ONES = 16384;
-constexpr uint32_t SLOT_BASE = 20480, SLOT_BYTES = 81920;
-constexpr uint32_t S_Q = 0, S_K = 16384, S_V = 32768, S_PHK = 49152;  // S_bf16 aliases S_Q
+constexpr uint32_t OFF_W = 0, OFF_ONES = 8192;
+constexpr uint32_t SLOT_BASE = 12288, SLOT_BYTES = 98304;
+// per slot: Q, K (free once H = X W has run), V (free after G3), S_bf16, phi(K) -> P
+constexpr uint32_t S_Q = 0, S_K = 16384, S_V = 32768, S_SB = 49152, S_PHK = 65536;
 __host__ __device__ constexpr uint32_t slot_off(int s) { return SLOT_BASE + s * SLOT_BYTES; }
-constexpr uint32_t OFF_ZS = SLOT_BASE + 2 * SLOT_BYTES;   // float[2][128]
-constexpr uint32_t OFF_BQ = OFF_ZS + 1024;                // float[64]
-constexpr uint32_t OFF_BK = OFF_BQ + 256;                 // float[64]
-constexpr uint32_t OFF_BAR = OFF_BK + 256;                // 16 x u64
-constexpr uint32_t OFF_TM = OFF_BAR + 128;
+constexpr uint32_t OFF_ZS = SLOT_BASE + 2 * SLOT_BYTES;   // float[2][128] z snapshots
+constexpr uint32_t OFF_DQ = OFF_ZS + 1024;                // float[2 slots][2 halves][128]
+constexpr uint32_t OFF_RS = OFF_DQ + 2048;                // float[2 slots][2 halves][128]
+constexpr uint32_t OFF_BQ = OFF_RS + 2048;                // float[64]
+constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 20 x u64
+constexpr uint32_t OFF_TM = OFF_BAR + 160;
 constexpr uint32_t SMEM_BYTES = OFF_TM + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-enum Bar { B_W = 0, B_LD = 1, B_G1 = 3, B_G2 = 5, B_G3 = 7, B_E1A = 9, B_E12 = 11, B_E3 = 13 };
+enum Bar {
+  B_W = 0, B_LDQK = 1, B_LDV = 3, B_G1 = 5, B_G2 = 7, B_G3 = 9, B_E1A = 11, B_E12 = 13, B_E3 = 15
+};
 
 struct Args2 {
-  CUtensorMap tq, tk, tv, twq, twk;
+  CUtensorMap tq, tk, tv, tw;
   __nv_bfloat16* y;
   const float* ws;   // [U][P-1][DP*D + DP] inclusive prefixes of segment states
   float* S_out;
   float* z_out;
-  const float* bq;
-  const float* bk;
+  const float* bias;
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
-  int H, P, L, NT, sep_wk;
+  int H, P, L, NT;
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -82,7 +88,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
   const uint32_t sb = smem_u32(sm);
   float* zs = reinterpret_cast<float*>(sm + OFF_ZS);
   float* bq_s = reinterpret_cast<float*>(sm + OFF_BQ);
-  float* bk_s = reinterpret_cast<float*>(sm + OFF_BK);
   const uint32_t bars = sb + OFF_BAR;
   auto bar = [&](int b) { return bars + 8u * b; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TM);
@@ -99,13 +104,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
   if (tid == 0) {
     mbar_init(bar(B_W), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_LD + s), 1);
+      mbar_init(bar(B_LDQK + s), 1);
+      mbar_init(bar(B_LDV + s), 1);
       mbar_init(bar(B_G1 + s), 1);
       mbar_init(bar(B_G2 + s), 1);
       mbar_init(bar(B_G3 + s), 1);
-      mbar_init(bar(B_E1A + s), 4);
-      mbar_init(bar(B_E12 + s), 4);
-      mbar_init(bar(B_E3 + s), 4);
+      mbar_init(bar(B_E1A + s), 8);
+      mbar_init(bar(B_E12 + s), 8);
+      mbar_init(bar(B_E3 + s), 8);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -115,30 +121,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
   }
   __syncthreads();
 
-  auto issue_loads = [&](int i) {
+  auto load_qk = [&](int i) {
     const int s = i & 1;
     const int r0 = (t_begin + i) * TILE;
     const uint32_t base = sb + slot_off(s);
-    mbar_expect_tx(bar(B_LD + s), 3 * 16384);
-    tma_load_3d(base + S_Q, &A.tq, bar(B_LD + s), 0, r0, (int)unit);
-    tma_load_3d(base + S_K, &A.tk, bar(B_LD + s), 0, r0, (int)unit);
-    tma_load_3d(base + S_V, &A.tv, bar(B_LD + s), 0, r0, (int)unit);
+    mbar_expect_tx(bar(B_LDQK + s), 2 * 16384);
+    tma_load_3d(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, (int)unit);
+    tma_load_3d(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, (int)unit);
+  };
+  auto load_v = [&](int i) {
+    const int s = i & 1;
+    mbar_expect_tx(bar(B_LDV + s), 16384);
+    tma_load_3d(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, (int)unit);
   };
   if (warp == 8 && lane == 0) {
-    mbar_expect_tx(bar(B_W), 8192u * (A.sep_wk ? 2 : 1));
-    tma_load_3d(sb + OFF_W, &A.twq, bar(B_W), 0, 0, h);
-    if (A.sep_wk) tma_load_3d(sb + OFF_WK, &A.twk, bar(B_W), 0, 0, h);
-    issue_loads(0);
-    if (nt > 1) issue_loads(1);
+    mbar_expect_tx(bar(B_W), 8192u);
+    tma_load_3d(sb + OFF_W, &A.tw, bar(B_W), 0, 0, h);
+    for (int i = 0; i < 2 && i < nt; ++i) {
+      load_qk(i);
+      load_v(i);
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  for (int i = tid; i < D; i += kThreads) {
-    bq_s[i] = A.bq ? A.bq[(size_t)h * D + i] : 0.f;
-    bk_s[i] = A.bk ? A.bk[(size_t)h * D + i] : 0.f;
-  }
+  for (int i = tid; i < D; i += kThreads) bq_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
   for (int i = tid; i < 4096 / 16; i += kThreads)   // bf16 ones: the B operand of Z += phi(K)^T 1
     st_shared_v4(sb + OFF_ONES + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   fence_proxy_async();
@@ -184,71 +192,92 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       constexpr uint32_t ID_SU = idesc_bf16(128, D, 1, 1);
       constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);
       constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
-      const uint32_t wk_off = A.sep_wk ? OFF_WK : OFF_W;
       bool ok = mbar_wait(bar(B_W), 0, wp);
+      // Descriptor bases: a k-step only moves the 14-bit start-address field
+      // (address >> 4), so each MMA below is one 64-bit add plus the instruction.
+      struct SlotDesc { uint64_t q, k, pk, pm, v, sbf; };
+      auto slot_desc = [&](int s2) {
+        const uint32_t base = sb + slot_off(s2);
+        SlotDesc d;
+        d.q = smem_desc(base + S_Q, 16, 1024, 2);         // K-major, 32 B per k-step
+        d.k = smem_desc(base + S_K, 16, 1024, 2);
+        d.pk = smem_desc(base + S_PHK, 16, 1024, 2);      // phi(K) / P as K-major operand
+        d.pm = smem_desc(base + S_PHK, 16384, 1024, 2);   // phi(K)^T as MN-major operand
+        d.v = smem_desc(base + S_V, 16384, 1024, 2);      // MN-major, 2048 B per k-step
+        d.sbf = smem_desc(base + S_SB, DP * 128, 1024, 2);
+        return d;
+      };
+      const SlotDesc sd0 = slot_desc(0), sd1 = slot_desc(1);
+      const uint64_t dW = smem_desc(sb + OFF_W, D * 128, 1024, 2);
+      const uint64_t dOnes = smem_desc(sb + OFF_ONES, 16, 256, 6);
+      // k-step offsets in 16-byte units: K-major inside 64-element panels, MN-major rows
+      auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
       auto G1 = [&](int i) {
         const int s = i & 1;
+        const SlotDesc& d = s ? sd1 : sd0;
         tc_fence_after();
-        const uint32_t base = sb + slot_off(s);
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t bw = smem_desc(sb + OFF_W + ks * 2048, D * 128, 1024, 2);
-          const uint64_t bwk = smem_desc(sb + wk_off + ks * 2048, D * 128, 1024, 2);
-          mma_ss(tmem + TM_Y(s), smem_desc(base + S_Q + ks * 32, 16, 1024, 2), bw, ID_H, ks > 0);
-          mma_ss(tmem + TM_X(s), smem_desc(base + S_K + ks * 32, 16, 1024, 2), bwk, ID_H, ks > 0);
+          mma_ss(tmem + TM_Y(s), d.q + 2 * ks, dW + 128 * ks, ID_H, ks > 0);
+          mma_ss(tmem + TM_X(s), d.k + 2 * ks, dW + 128 * ks, ID_H, ks > 0);
         }
         mma_commit(bar(B_G1 + s));
       };
       auto G2 = [&](int i) {
         const int s = i & 1;
+        const SlotDesc& d = s ? sd1 : sd0;
         tc_fence_after();
-        const uint32_t base = sb + slot_off(s);
+#pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks)
-          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8,
-                 smem_desc(base + S_PHK + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, 2), ID_SC,
-                 ks > 0);
+          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.pk + kmaj(ks), ID_SC, ks > 0);
+#pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks) {
-          const uint64_t a = smem_desc(base + S_PHK + ks * 2048, 16384, 1024, 2);
-          mma_ss(tmem + TM_S, a, smem_desc(base + S_V + ks * 2048, 16384, 1024, 2), ID_SU, 1);
-          mma_ss(tmem + TM_Z, a, smem_desc(sb + OFF_ONES + ks * 512, 16, 256, 6), ID_Z, 1);
+          mma_ss(tmem + TM_S, d.pm + 128 * ks, d.v + 128 * ks, ID_SU, 1);
+          mma_ss(tmem + TM_Z, d.pm + 128 * ks, dOnes + 32 * ks, ID_Z, 1);
         }
         mma_commit(bar(B_G2 + s));
       };
       auto G3 = [&](int i) {
         const int s = i & 1;
+        const SlotDesc& d = s ? sd1 : sd0;
         tc_fence_after();
-        const uint32_t base = sb + slot_off(s);
+#pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks)
-          mma_ss(tmem + TM_X(s),
-                 smem_desc(base + S_PHK + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, 2),
-                 smem_desc(base + S_V + ks * 2048, 16384, 1024, 2), ID_PV, ks > 0);
+          mma_ss(tmem + TM_X(s), d.pk + kmaj(ks), d.v + 128 * ks, ID_PV, ks > 0);
+#pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks)
-          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8,
-                 smem_desc(base + S_Q + ks * 2048, DP * 128, 1024, 2), ID_PV, 1);
+          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.sbf + 128 * ks, ID_PV, 1);
         mma_commit(bar(B_G3 + s));
       };
       // Each action runs once its inputs are ready; per kind they run in tile order.
-      //   L(i)  loads into slot i&1   needs G3(i-2) complete (S_bf16, V, P no longer read)
-      //   G1(i)                       needs L(i) landed and E3(i-2) done (TMEM slot free)
-      //   G2(i)                       needs E1(i) done
-      //   G3(i)                       needs E2(i) done
-      int nL = nt < 2 ? nt : 2, n1 = 0, n2 = 0, n3 = 0;
+      //   LQK(i)  Q, K into slot i&1   needs G1(i-2) complete (H = X W has read them)
+      //   LV(i)   V into slot i&1      needs G3(i-2) complete (S += phi(K)^T V, P V done)
+      //   G1(i)                        needs LQK(i) landed and E3(i-2) done (TMEM slot free)
+      //   G2(i)                        needs E1(i) done and LV(i) landed
+      //   G3(i)                        needs E2(i) done
+      int nqk = nt < 2 ? nt : 2, nv = nqk, n1 = 0, n2 = 0, n3 = 0;
       uint64_t t_last = globaltimer();
       bool reported = false;
       while (ok && n3 < nt) {
         bool progress = false;
-        if (n2 < n1 && mbar_probe(bar(B_E1A + (n2 & 1)), (n2 >> 1) & 1)) {
+        if (n2 < n1 && mbar_probe(bar(B_E1A + (n2 & 1)), (n2 >> 1) & 1) &&
+            mbar_probe(bar(B_LDV + (n2 & 1)), (n2 >> 1) & 1)) {
           G2(n2++);
+          progress = true;
+        } else if (n1 < nqk && mbar_probe(bar(B_LDQK + (n1 & 1)), (n1 >> 1) & 1) &&
+                   (n1 < 2 || mbar_probe(bar(B_E3 + (n1 & 1)), ((n1 - 2) >> 1) & 1))) {
+          G1(n1++);
           progress = true;
         } else if (n3 < n2 && mbar_probe(bar(B_E12 + (n3 & 1)), (n3 >> 1) & 1)) {
           G3(n3++);
           progress = true;
-        } else if (nL < nt && n3 > nL - 2 &&
-                   mbar_probe(bar(B_G3 + (nL & 1)), ((nL - 2) >> 1) & 1)) {
-          issue_loads(nL++);
+        } else if (nv < nt && n3 > nv - 2 &&
+                   mbar_probe(bar(B_G3 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
+          load_v(nv++);
           progress = true;
-        } else if (n1 < nL && mbar_probe(bar(B_LD + (n1 & 1)), (n1 >> 1) & 1) &&
-                   (n1 < 2 || mbar_probe(bar(B_E3 + (n1 & 1)), ((n1 - 2) >> 1) & 1))) {
-          G1(n1++);
+        } else if (nqk < nt && n1 > nqk - 2 &&
+                   mbar_probe(bar(B_G1 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
+          load_qk(nqk++);
           progress = true;
         }
         if (progress) {
@@ -268,139 +297,174 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       }
     }
   } else {
-    // ======================= epilogue groups =======================
-    const int eg = warp >> 2;
+    // ======================= epilogue warps =======================
+    // All eight warps work on one phase at a time; phases of the two slots are
+    // software-pipelined as E2(i-1), E1(i), E3(i-1) so that G3(i-1) runs under
+    // E1(i), G2(i) under E3(i-1) and G1(i+1) under the next E2.  Warp w owns
+    // TMEM lanes 32*(w%4).. (rows / features) and column half c = w / 4.
+    const int c = warp >> 2;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lb = lane_base(warp);
-    const uint32_t base = sb + slot_off(eg);
-    float* zsn = zs + eg * 128;
-    for (int i = eg; i < nt; i += 2) {
-      const uint32_t par = (i >> 1) & 1;
-      const int64_t r0 = (int64_t)(t_begin + i) * TILE;
-      const bool valid = r0 + row < A.n;
+    float* dq_s = reinterpret_cast<float*>(sm + OFF_DQ);
+    float* rs_s = reinterpret_cast<float*>(sm + OFF_RS);
+    bool good = true;
 
-      // ---- E1: phi(Q) into TMEM, phi(K) into smem panels ----
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + eg), par, wp))) break;
+    auto E1 = [&](int i) {
+      const int s = i & 1;
+      const uint32_t par = (i >> 1) & 1;
+      const uint32_t base = sb + slot_off(s);
+      const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + s), par, wp))) { good = false; return; }
       tc_fence_after();
+      // phi(Q): H_Q columns [32c, 32c+32) -> packed columns [16c, +16) and [32 + 16c, +16)
       {
-        uint32_t hv[64];
-        tmem_ld64(tmem + lb + TM_Y(eg), hv);
-        uint32_t pp[32], pn[32];
+        uint32_t hv[32];
+        tmem_ld32(tmem + lb + TM_Y(s) + 32 * c, hv);
+        uint32_t pp[16], pn[16];
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float h0 = __uint_as_float(hv[j]) + bq_s[j];
-          const float h1 = __uint_as_float(hv[j + 1]) + bq_s[j + 1];
+        for (int j = 0; j < 32; j += 2) {
+          const float h0 = __uint_as_float(hv[j]) + bq_s[32 * c + j];
+          const float h1 = __uint_as_float(hv[j + 1]) + bq_s[32 * c + j + 1];
           pp[j / 2] = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
           pn[j / 2] = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
         }
-        tmem_st32(tmem + lb + TM_Y(eg), pp);
-        tmem_st32(tmem + lb + TM_Y(eg) + 32, pn);
+        tc_fence_before();
+        named_bar_sync(1, 256);   // every warp holds its H_Q columns before any overwrite
+        tc_fence_after();
+        tmem_st16(tmem + lb + TM_Y(s) + 16 * c, pp);
+        tmem_st16(tmem + lb + TM_Y(s) + 32 + 16 * c, pn);
       }
+      // phi(K): features [32c, +32) -> panel 0 chunks [4c, +4); [64 + 32c, +32) -> panel 1
       {
-        uint32_t hv[64];
-        tmem_ld64(tmem + lb + TM_X(eg), hv);
+        uint32_t hv[32];
+        tmem_ld32(tmem + lb + TM_X(s) + 32 * c, hv);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t wpos[4], wneg[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int j = 8 * c + 2 * e;
-            const float h0 = __uint_as_float(hv[j]) + bk_s[j];
-            const float h1 = __uint_as_float(hv[j + 1]) + bk_s[j + 1];
+            const int j = 8 * q4 + 2 * e;
+            const float h0 = __uint_as_float(hv[j]) + bq_s[32 * c + j];
+            const float h1 = __uint_as_float(hv[j + 1]) + bq_s[32 * c + j + 1];
             wpos[e] = valid ? pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e)) : 0u;
             wneg[e] = valid ? pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e)) : 0u;
           }
-          st_shared_v4(base + S_PHK + sw128_chunk(row, c), wpos[0], wpos[1], wpos[2], wpos[3]);
-          st_shared_v4(base + S_PHK + 16384 + sw128_chunk(row, c), wneg[0], wneg[1], wneg[2],
-                       wneg[3]);
+          st_shared_v4(base + S_PHK + sw128_chunk(row, 4 * c + q4), wpos[0], wpos[1], wpos[2],
+                       wpos[3]);
+          st_shared_v4(base + S_PHK + 16384 + sw128_chunk(row, 4 * c + q4), wneg[0], wneg[1],
+                       wneg[2], wneg[3]);
         }
       }
-      // S_bf16 and z of the tokens before this tile; G2(t) may run only after this
+      // S_bf16 and z of the tokens before this tile; G2(i) may run only after this
       if (i > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp))) {
+          good = false;
+          return;
+        }
         tc_fence_after();
       }
       {
-        uint32_t sv[64];
-        tmem_ld64(tmem + lb + TM_S, sv);
+        uint32_t sv[32];
+        tmem_ld32(tmem + lb + TM_S + 32 * c, sv);   // feature `row`, columns [32c, +32)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int j = 8 * c;
-          st_shared_v4(base + S_Q + sw128_chunk(row, c),
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = 8 * q4;
+          st_shared_v4(base + S_SB + sw128_chunk(row, 4 * c + q4),
                        pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
                        pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
                        pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
                        pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
         }
-        uint32_t zv[16];
-        tmem_ld16(tmem + lb + TM_Z, zv);
-        zsn[row] = __uint_as_float(zv[0]);
+        if (c == 0) {
+          uint32_t zv[16];
+          tmem_ld16(tmem + lb + TM_Z, zv);
+          zs[s * 128 + row] = __uint_as_float(zv[0]);
+        }
       }
-
       tmem_st_wait();
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_E1A + eg));
-      named_bar_sync(1 + eg, 128);   // z snapshot of every feature written
-      float den = 0.f;
+      if (lane == 0) mbar_arrive(bar(B_E1A + s));
+      named_bar_sync(1, 256);   // z snapshot of every feature written
+      // this half's part of phi(q) . z: packed columns [32c, +32) = features [64c, +64)
       {
-        uint32_t qp[64];
-        tmem_ld64(tmem + lb + TM_Y(eg), qp);
+        uint32_t qp[32];
+        tmem_ld32(tmem + lb + TM_Y(s) + 32 * c, qp);
+        const float* zz = zs + s * 128 + 64 * c;
+        float d = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          den += bf16_lo(qp[c]) * zsn[2 * c] + bf16_hi(qp[c]) * zsn[2 * c + 1];
+        for (int j = 0; j < 32; ++j) d += bf16_lo(qp[j]) * zz[2 * j] + bf16_hi(qp[j]) * zz[2 * j + 1];
+        dq_s[(s * 2 + c) * 128 + row] = d;
       }
+    };
 
-      // ---- E2: P = bf16(tril(Sc)) and its row sums ----
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + eg), par, wp))) break;
+    auto E2 = [&](int i) {
+      const int s = i & 1;
+      const uint32_t par = (i >> 1) & 1;
+      const uint32_t base = sb + slot_off(s);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + s), par, wp))) { good = false; return; }
       tc_fence_after();
+      float rs = 0.f;
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t sv[64];
-        tmem_ld64(tmem + lb + TM_X(eg) + 64 * hb, sv);
+      for (int h2 = 0; h2 < 2; ++h2) {   // keys [64c + 32 h2, +32)
+        uint32_t sv[32];
+        tmem_ld32(tmem + lb + TM_X(s) + 64 * c + 32 * h2, sv);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int key = 64 * hb + 8 * c + 2 * e;
-            const float a0 = key <= row ? __uint_as_float(sv[8 * c + 2 * e]) : 0.f;
-            const float a1 = key + 1 <= row ? __uint_as_float(sv[8 * c + 2 * e + 1]) : 0.f;
+            const int key = 64 * c + 32 * h2 + 8 * q4 + 2 * e;
+            const float a0 = key <= row ? __uint_as_float(sv[8 * q4 + 2 * e]) : 0.f;
+            const float a1 = key + 1 <= row ? __uint_as_float(sv[8 * q4 + 2 * e + 1]) : 0.f;
             w4[e] = pack_bf16(a0, a1);
-            den += bf16_lo(w4[e]) + bf16_hi(w4[e]);
+            rs += bf16_lo(w4[e]) + bf16_hi(w4[e]);
           }
-          st_shared_v4(base + S_PHK + hb * 16384 + sw128_chunk(row, c), w4[0], w4[1], w4[2], w4[3]);
+          st_shared_v4(base + S_PHK + c * 16384 + sw128_chunk(row, 4 * h2 + q4), w4[0], w4[1],
+                       w4[2], w4[3]);
         }
       }
+      rs_s[(s * 2 + c) * 128 + row] = rs;
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_E12 + eg));
+      if (lane == 0) mbar_arrive(bar(B_E12 + s));
+    };
 
-      // ---- E3: y = O / den ----
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G3 + eg), par, wp))) break;
+    auto E3 = [&](int i) {
+      const int s = i & 1;
+      const uint32_t par = (i >> 1) & 1;
+      const int64_t r0 = (int64_t)(t_begin + i) * TILE;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G3 + s), par, wp))) { good = false; return; }
       tc_fence_after();
-      {
-        uint32_t ov[64];
-        tmem_ld64(tmem + lb + TM_X(eg), ov);
-        const float inv = 1.f / den;
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D);
+      uint32_t ov[32];
+      tmem_ld32(tmem + lb + TM_X(s) + 32 * c, ov);
+      // both halves' partial denominators were written before G3(i) could be issued
+      const float den = (dq_s[(s * 2) * 128 + row] + dq_s[(s * 2 + 1) * 128 + row]) +
+                        (rs_s[(s * 2) * 128 + row] + rs_s[(s * 2 + 1) * 128 + row]);
+      const float inv = 1.f / den;
+      if (r0 + row < A.n) {
+        uint4* dst = reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D + 32 * c);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int j = 8 * c;
-            dst[c] = make_uint4(
-                pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
-                pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
-                pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
-                pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = 8 * q4;
+          dst[q4] = make_uint4(
+              pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
+              pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
+              pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
+              pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_E3 + eg));
+      if (lane == 0) mbar_arrive(bar(B_E3 + s));
+    };
+
+    for (int step = 0; step <= nt && good; ++step) {
+      if (step >= 1) E2(step - 1);
+      if (step < nt && good) E1(step);
+      if (step >= 1 && good) E3(step - 1);
     }
   }
 
@@ -456,23 +520,23 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 
 }  // namespace
 
-// Output pass of the d = 64 Hedgehog prefill (two tiles in flight per CTA).
+// Output pass of the d = 64 Hedgehog prefill (two tiles in flight per CTA) for a
+// feature map shared by queries and keys.
 cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const void* q,
                                    const void* k, const void* v, void* y, float* S_out,
                                    float* z_out, const void* ws, int* dev_status, cudaStream_t s) {
   Args2 a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
+  if (p.Wk) return cudaErrorInvalidValue;  // one map shared by queries and keys
   bool ok = make_map(&a.tq, q, D, p.n, U, TILE) && make_map(&a.tk, k, D, p.n, U, TILE) &&
-            make_map(&a.tv, v, D, p.n, U, TILE) && make_map(&a.twq, p.Wq, D, D, p.H, D) &&
-            make_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, D);
+            make_map(&a.tv, v, D, p.n, U, TILE) && make_map(&a.tw, p.Wq, D, D, p.H, D);
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
   a.S_out = S_out;
   a.z_out = z_out;
-  a.bq = p.bq;
-  a.bk = p.Wk ? p.bk : p.bq;
+  a.bias = p.bq;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
@@ -481,7 +545,6 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
-  a.sep_wk = p.Wk ? 1 : 0;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc2_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
