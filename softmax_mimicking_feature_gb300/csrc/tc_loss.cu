@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
     // ---------------- epilogue warps ----------------
     const int half = warp >> 2, row = 32 * (warp & 3) + lane;
     const int64_t qi = q0 + row;
-    float m = -INFINITY, Z = 0.f, T = 0.f, As = 0.f;
+    // online state; Z, T and the weight sum are kept as two interleaved partial
+    // sums so consecutive keys do not form one long dependency chain
+    float m = -INFINITY, Z0 = 0.f, Z1 = 0.f, T0 = 0.f, T1 = 0.f, A0 = 0.f, A1 = 0.f;
+    const int64_t kmax = min(qi, A.n - 1);   // last key admitted for this row
     for (int j = 0; j < nkt; ++j) {
       const int stg = j & 1;
       if (!mbar_wait(bar_mma0 + 8 * stg, (j >> 1) & 1, wp)) { failed = true; break; }
@@ -325,37 +328,62 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
         uint32_t sv[32], av[32];
-        tmem_ld32(tmem + lane_base(warp) + stg * 256 + half * 64 + c, sv);
-        tmem_ld32(tmem + lane_base(warp) + stg * 256 + 128 + half * 64 + c, av);
-        // keys admitted for this row: k <= qi and k < n
-        const int64_t kmax = min(qi, A.n - 1);
+        tmem_ld32x2(tmem + lane_base(warp) + stg * 256 + half * 64 + c, sv,
+                    tmem + lane_base(warp) + stg * 256 + 128 + half * 64 + c, av);
         const int nval = (int)max((int64_t)0, min((int64_t)32, kmax - (k0 + c) + 1));
-        float cm = -INFINITY;
+        if (nval == 32) {
+          // every key of the chunk is admitted: no masking
+          float c0 = __uint_as_float(sv[0]), c1 = __uint_as_float(sv[1]);
+          float c2 = __uint_as_float(sv[2]), c3 = __uint_as_float(sv[3]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e < nval) cm = fmaxf(cm, __uint_as_float(sv[e]) * A.s_scale);
-        if (cm != -INFINITY) {
-          const float mn = fmaxf(m, cm);
+          for (int e = 4; e < 32; e += 4) {
+            c0 = fmaxf(c0, __uint_as_float(sv[e]));
+            c1 = fmaxf(c1, __uint_as_float(sv[e + 1]));
+            c2 = fmaxf(c2, __uint_as_float(sv[e + 2]));
+            c3 = fmaxf(c3, __uint_as_float(sv[e + 3]));
+          }
+          const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * A.s_scale);
           const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-          Z *= f;
-          T *= f;
+          Z0 *= f; Z1 *= f; T0 *= f; T1 *= f;
+          m = mn;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float a0 = __uint_as_float(av[e]), a1 = __uint_as_float(av[e + 1]);
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), A.s_scale, -m));
+            Z0 += p0;
+            Z1 += p1;
+            T0 = fmaf(p0, __log2f(a0), T0);
+            T1 = fmaf(p1, __log2f(a1), T1);
+            A0 += a0;
+            A1 += a1;
+          }
+        } else if (nval > 0) {
+          float cm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e < nval) cm = fmaxf(cm, __uint_as_float(sv[e]));
+          const float mn = fmaxf(m, cm * A.s_scale);
+          const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+          Z0 *= f; Z1 *= f; T0 *= f; T1 *= f;
           m = mn;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             if (e < nval) {
               const float a = __uint_as_float(av[e]);
-              const float p = ex2_approx(__uint_as_float(sv[e]) * A.s_scale - m);
-              Z += p;
-              T = fmaf(p, __log2f(a), T);
-              As += a;
+              const float p = ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
+              Z0 += p;
+              T0 = fmaf(p, __log2f(a), T0);
+              A0 += a;
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_free0 + 8 * stg) : "memory");
+      if (lane == 0) mbar_arrive(bar_free0 + 8 * stg);
     }
+    float Z = Z0 + Z1, T = T0 + T1, As = A0 + A1;
     // merge the two column halves of each row
     if (half == 1) {
       st_s[row] = m;
