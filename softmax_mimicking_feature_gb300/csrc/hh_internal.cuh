@@ -70,6 +70,11 @@ cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q,
                               const void* v, void* y, float* S_out, float* z_out, void* ws,
                               int* dev_status, cudaStream_t s);
 
+// Segment-state pass (P > 1): per segment but the last, sum phi(k)^T v and
+// sum phi(k) into the workspace.
+cudaError_t launch_state_tc(const Problem& p, const TcPlan& pl, const void* k, const void* v,
+                            void* ws, int* dev_status, cudaStream_t s);
+
 // Output pass of the d = 64 Hedgehog prefill with two tiles in flight per CTA.
 cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const void* q,
                                    const void* k, const void* v, void* y, float* S_out,

@@ -867,11 +867,8 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   a.sep_wk = p.Wk ? 1 : 0;
   const size_t smem = smem_bytes<KIND, D>();
   if (pl.P > 1) {
-    auto kern = prefill_tc_kernel<KIND, D, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = launch_state_tc(p, pl, k, v, ws, dev_status, s);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (pl.P > 2) {
       const int64_t elems4 = ((int64_t)p.dpp * p.d + p.dpp) / 4;
       const int64_t n4 = (int64_t)U * elems4;

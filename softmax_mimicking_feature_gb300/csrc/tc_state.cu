@@ -1,0 +1,459 @@
+// Segment-state pass of the chunked prefill on the 5th-generation tensor cores.
+//
+// For each segment of a (batch, head) sequence it writes
+//   S_seg = sum_j phi(k_j)^T v_j   and   z_seg = sum_j phi(k_j)
+// over the segment's tokens: the running sums of "Complexity Analysis" in
+// "The Hedgehog & the Porcupine" summary (section 2, paper Eq. 2), for the
+// Hedgehog map ("The Hedgehog MLP Feature Map", Choices 1 and 3) or the
+// degree-2 Taylor map ("The Taylor Exponential as a Bridge Result").  The
+// output pass starts segment s from the inclusive scan of segments < s.
+//
+// One CTA per segment.  Warp 8 (one lane) issues TMA loads and MMAs; warps
+// 0-7 build phi(K) (warp w owns TMEM lanes 32*(w%4).. and column half w/4).
+// Per 128-token tile t:
+//   G1(t): H_K = K_t W into TMEM                          (Hedgehog)
+//   E1(t): H_K -> registers ("H read"), exponentials, then phi(K_t) ->
+//          128B-swizzled shared panels once G2(t-1) has consumed the old ones
+//   G2(t): S += phi(K_t)^T V_t,  z += phi(K_t)^T 1         (tcgen05)
+// G1(t+1) is issued as soon as E1(t) has read H_K, so it and G2(t) run
+// under the exponentials of the next tile.  K is double-buffered; V is
+// double-buffered where shared memory allows (single at d = 128).
+// Every mbarrier wait is bounded in time (tc_ptx.cuh).
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "tc_ptx.cuh"
+
+namespace hh {
+namespace {
+
+using namespace tc;
+
+constexpr int TILE = 128;
+constexpr int kThreads = 288;  // 8 feature warps + 1 issue warp
+
+template <int KIND, int D>
+struct SCfg;
+
+// Hedgehog, d in {64, 128}: 2d features, S rows as 128-feature M blocks.
+template <int D>
+struct SCfg<HH_FMAP_HEDGEHOG, D> {
+  static constexpr int DPP = 2 * D;
+  static constexpr int NMB = 2 * D / 128;
+  static constexpr int NV = D == 128 ? 1 : 2;                  // V stages
+  static constexpr uint32_t TM_S = 0;                          // NMB x [128 x D]
+  static constexpr uint32_t TM_Z = NMB * D;                    // NMB x [128 x 16]
+  static constexpr uint32_t TM_H = D == 64 ? 192 : 384;        // [128 x D]
+  static constexpr uint32_t TM_COLS = D == 64 ? 256 : 512;
+  static_assert(TM_Z + 16 * NMB <= TM_H && TM_H + D <= TM_COLS, "TMEM layout");
+  static constexpr uint32_t XT = TILE * D * 2;                 // one K or V tile
+  static constexpr uint32_t OFF_W = 0;
+  static constexpr uint32_t OFF_ONES = D * D * 2;              // [128 x 16] bf16 ones, SW32
+  static constexpr uint32_t OFF_K = OFF_ONES + 4096;
+  static constexpr uint32_t OFF_V = OFF_K + 2 * XT;
+  static constexpr uint32_t OFF_PHK = OFF_V + NV * XT;         // [2D/64] panels of 16 KB
+  static constexpr uint32_t OFF_END = OFF_PHK + (2 * D / 64) * 16384;
+};
+
+// Taylor, d = 16: 273 features stored as 288, panels cover 384 (tail zero).
+template <>
+struct SCfg<HH_FMAP_TAYLOR2, 16> {
+  static constexpr int DPP = 288;
+  static constexpr int NMB = 3;
+  static constexpr int NV = 2;
+  static constexpr uint32_t TM_S = 0;                          // 3 x [128 x 16]
+  static constexpr uint32_t TM_Z = 48;                         // 3 x [128 x 16]
+  static constexpr uint32_t TM_H = 0;                          // unused
+  static constexpr uint32_t TM_COLS = 128;
+  static constexpr uint32_t XT = TILE * 16 * 2;                // 4 KB
+  static constexpr uint32_t OFF_W = 0;                         // unused
+  static constexpr uint32_t OFF_ONES = 0;
+  static constexpr uint32_t OFF_K = 4096;
+  static constexpr uint32_t OFF_V = OFF_K + 2 * XT;            // 256-aligned for SW32
+  static constexpr uint32_t OFF_PHK = 24576;
+  static constexpr uint32_t OFF_END = OFF_PHK + 6 * 16384;
+};
+
+enum {
+  SB_W = 0, SB_LDK = 1 /* 2 */, SB_LDV = 3 /* 2 */, SB_G1 = 5, SB_HREAD = 6, SB_E1 = 7,
+  SB_G2 = 8, SB_COUNT = 9
+};
+
+template <int KIND, int D>
+struct SSmem {
+  using C = SCfg<KIND, D>;
+  static constexpr uint32_t OFF_B = C::OFF_END;                // bias float[128]
+  static constexpr uint32_t OFF_BAR = OFF_B + 512;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * SB_COUNT; // tmem base, abort flag
+  static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;      // + alignment slack
+  static_assert(ALLOC <= 227 * 1024, "shared memory");
+};
+
+struct StateArgs {
+  CUtensorMap tk, tv, tw;
+  float* ws;          // [U][P-1][DPP*D + DPP]: S (row-major [DPP][D]) then z
+  const float* bias;  // [H][D] of the key map (Hedgehog) or null
+  int* dev_status;
+  uint64_t soft_ns, hard_ns;
+  int64_t n;
+  int H, P, L, NT;
+};
+
+__device__ __forceinline__ uint32_t lane_base(int warp) {
+  return (uint32_t)(32 * (warp & 3)) << 16;
+}
+
+// Taylor feature f of [1, x, x_i x_j / sqrt2 (i-major)]; zero past 272.
+__device__ __forceinline__ float taylor_feature(int f, const float (&x)[16]) {
+  if (f == 0) return 1.f;
+  if (f <= 16) return x[f - 1];
+  if (f <= 272) return x[(f - 17) >> 4] * x[(f - 17) & 15] * kInvSqrt2;
+  return 0.f;
+}
+
+// 32 features from FB as 16 bf16 pairs into w[WB..WB+16)
+template <int FB, int WB, int NW>
+__device__ __forceinline__ void taylor_pack(const float (&x)[16], bool valid, uint32_t (&w)[NW]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    w[WB + j] = valid ? pack_bf16(taylor_feature(FB + 2 * j, x), taylor_feature(FB + 2 * j + 1, x))
+                      : 0u;
+}
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_constant__ StateArgs A) {
+  using C = SCfg<KIND, D>;
+  using SM = SSmem<KIND, D>;
+  constexpr bool HH = KIND == HH_FMAP_HEDGEHOG;
+  constexpr int NV = C::NV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  float* b_s = reinterpret_cast<float*>(sm + SM::OFF_B);
+  const uint32_t bars = sb + SM::OFF_BAR;
+  auto bar = [&](int b) { return bars + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(sm + SM::OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t unit = blockIdx.x / (A.P - 1);
+  const int seg = blockIdx.x % (A.P - 1);
+  const int h = (int)(unit % A.H);
+  const int t_begin = seg * A.L;
+  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+
+  if (tid == 0) {
+    for (int b = 0; b < SB_COUNT; ++b)
+      mbar_init(bar(b), (b == SB_HREAD || b == SB_E1) ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto load_k = [&](int i) {
+    const uint32_t dst = sb + C::OFF_K + (i & 1) * C::XT;
+    const uint32_t b = bar(SB_LDK + (i & 1));
+    mbar_expect_tx(b, C::XT);
+    for (int x = 0; x < (D + 63) / 64; ++x)
+      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+  };
+  auto load_v = [&](int i) {
+    const uint32_t dst = sb + C::OFF_V + (i % NV) * C::XT;
+    const uint32_t b = bar(SB_LDV + (i % NV));
+    mbar_expect_tx(b, C::XT);
+    for (int x = 0; x < (D + 63) / 64; ++x)
+      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+  };
+  if (warp == 8 && lane == 0 && nt > 0) {
+    if (HH) {
+      mbar_expect_tx(bar(SB_W), D * D * 2);
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d(sb + C::OFF_W + x * (D * 128), &A.tw, bar(SB_W), 64 * x, 0, h);
+    }
+    load_k(0);
+    load_v(0);
+    if (nt > 1) {
+      load_k(1);
+      if (NV == 2) load_v(1);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  if (HH)
+    for (int i = tid; i < D; i += kThreads) b_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
+  // ones operand of the z MMA ([128 tokens x 16] bf16)
+  for (int i = tid; i < 4096 / 16; i += kThreads)
+    st_shared_v4(sb + C::OFF_ONES + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  if (!HH) {
+    // Taylor: features 288..383 of the panels stay zero for the whole run
+    for (uint32_t i = tid * 16; i < 6 * 16384u; i += kThreads * 16)
+      st_shared_v4(sb + C::OFF_PHK + i, 0, 0, 0, 0);
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // S = 0, z = 0 (lanes = features)
+  if (warp < 4) {
+    uint32_t zr[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) zr[j] = 0u;
+    for (int mb = 0; mb < C::NMB; ++mb) {
+      for (int c0 = 0; c0 < D; c0 += 16)
+        tmem_st16(tmem + lane_base(warp) + C::TM_S + mb * D + c0, zr);
+      tmem_st16(tmem + lane_base(warp) + C::TM_Z + 16 * mb, zr);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 8) {
+    // ======================= issue warp =======================
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t ID_H = idesc_bf16(128, D, 0, 1);   // K[K-major] W[MN-major]
+      constexpr uint32_t ID_SU = idesc_bf16(128, D, 1, 1);  // phiK^T[MN] V[MN]
+      constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);  // phiK^T[MN] ones[MN]
+      auto g1 = [&](int i) {
+        const uint32_t kb = sb + C::OFF_K + (i & 1) * C::XT;
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + C::TM_H, smem_desc(kb + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, 2),
+                 smem_desc(sb + C::OFF_W + ks * 2048, D * 128, 1024, 2), ID_H, ks > 0);
+        mma_commit(bar(SB_G1));
+      };
+      bool ok = true;
+      if (HH) {
+        ok = mbar_wait(bar(SB_W), 0, wp) && mbar_wait(bar(SB_LDK), 0, wp);
+        tc_fence_after();
+        if (ok) g1(0);
+      }
+      for (int i = 0; i < nt && ok; ++i) {
+        if (HH && i + 1 < nt) {
+          // H_K is free once every feature warp has read H_K(i)
+          ok = mbar_wait(bar(SB_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
+               mbar_wait(bar(SB_HREAD), i & 1, wp);
+          if (!ok) break;
+          tc_fence_after();
+          g1(i + 1);
+        }
+        ok = mbar_wait(bar(SB_E1), i & 1, wp) &&
+             mbar_wait(bar(SB_LDV + (i % NV)), (i / NV) & 1, wp);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vb = sb + C::OFF_V + (i % NV) * C::XT;
+        for (int mb = 0; mb < C::NMB; ++mb)
+          for (int ks = 0; ks < TILE / 16; ++ks) {
+            const uint64_t a =
+                smem_desc(sb + C::OFF_PHK + (2 * mb) * 16384 + ks * 2048, 16384, 1024, 2);
+            const uint64_t bv = HH ? smem_desc(vb + ks * 2048, TILE * 128, 1024, 2)
+                                   : smem_desc(vb + ks * 512, 16, 256, 6);
+            mma_ss(tmem + C::TM_S + mb * D, a, bv, ID_SU, 1);
+            mma_ss(tmem + C::TM_Z + 16 * mb, a,
+                   smem_desc(sb + C::OFF_ONES + ks * 512, 16, 256, 6), ID_Z, 1);
+          }
+        mma_commit(bar(SB_G2));
+        // K stage i&1: G1(i) (Hedgehog) or the feature warps (Taylor) are done with it
+        if (i + 2 < nt) load_k(i + 2);
+        if (NV == 2) {
+          // V stage (i+1)&1 held V(i-1), consumed by G2(i-1) (E1(i) waited for it)
+          if (i + 1 < nt && i + 1 >= 2) load_v(i + 1);
+        } else if (i + 1 < nt) {
+          ok = mbar_wait(bar(SB_G2), i & 1, wp);
+          if (ok) load_v(i + 1);
+        }
+      }
+      if (!ok) *(volatile int*)abort_flag = 1;
+    }
+  } else {
+    // ======================= feature warps =======================
+    const int c = warp >> 2;
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t phk = sb + C::OFF_PHK;
+    for (int i = 0; i < nt; ++i) {
+      const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
+      if constexpr (HH) {
+        constexpr int HC = D / 2;  // H columns of this warp's half
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(SB_G1), i & 1, wp))) break;
+        tc_fence_after();
+        uint32_t hv[HC];
+        if constexpr (HC == 64) tmem_ld64(tmem + lane_base(warp) + C::TM_H + HC * c, hv);
+        else tmem_ld32(tmem + lane_base(warp) + C::TM_H + HC * c, hv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(SB_HREAD));
+        uint32_t wpos[HC / 2], wneg[HC / 2];
+#pragma unroll
+        for (int j = 0; j < HC; j += 2) {
+          const float h0 = __uint_as_float(hv[j]) + b_s[HC * c + j];
+          const float h1 = __uint_as_float(hv[j + 1]) + b_s[HC * c + j + 1];
+          wpos[j / 2] = valid ? pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e)) : 0u;
+          wneg[j / 2] = valid ? pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e)) : 0u;
+        }
+        // the panels are free once G2(i-1) has read them
+        if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(SB_G2), (i - 1) & 1, wp))) break;
+#pragma unroll
+        for (int q = 0; q < HC / 8; ++q) {
+          const int fp = HC * c + 8 * q;      // positive feature of this 16-byte chunk
+          const int fn = D + HC * c + 8 * q;  // its negative twin
+          st_shared_v4(phk + (fp / 64) * 16384 + sw128_chunk(row, (fp % 64) / 8), wpos[4 * q],
+                       wpos[4 * q + 1], wpos[4 * q + 2], wpos[4 * q + 3]);
+          st_shared_v4(phk + (fn / 64) * 16384 + sw128_chunk(row, (fn % 64) / 8), wneg[4 * q],
+                       wneg[4 * q + 1], wneg[4 * q + 2], wneg[4 * q + 3]);
+        }
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(SB_LDK + (i & 1)), (i >> 1) & 1, wp))) break;
+        const __nv_bfloat16* krow =
+            reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_K + (i & 1) * C::XT) + row * 16;
+        float x[16];
+#pragma unroll
+        for (int k2 = 0; k2 < 16; ++k2) x[k2] = __bfloat162float(krow[k2]);
+        // half 0: features [0, 160), half 1: [160, 288)
+        uint32_t w[80];
+        if (c == 0) {
+          taylor_pack<0, 0>(x, valid, w);
+          taylor_pack<32, 16>(x, valid, w);
+          taylor_pack<64, 32>(x, valid, w);
+          taylor_pack<96, 48>(x, valid, w);
+          taylor_pack<128, 64>(x, valid, w);
+        } else {
+          taylor_pack<160, 0>(x, valid, w);
+          taylor_pack<192, 16>(x, valid, w);
+          taylor_pack<224, 32>(x, valid, w);
+          taylor_pack<256, 48>(x, valid, w);
+        }
+        if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(SB_G2), (i - 1) & 1, wp))) break;
+        const int f0 = c == 0 ? 0 : 160;
+        const int nq = c == 0 ? 20 : 16;   // 16-byte chunks (8 features each)
+#pragma unroll
+        for (int q = 0; q < 20; ++q) {
+          if (q < nq) {
+            const int f = f0 + 8 * q;
+            st_shared_v4(phk + (f / 64) * 16384 + sw128_chunk(row, (f % 64) / 8), w[4 * q],
+                         w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SB_E1));
+    }
+  }
+
+  // ---- export this segment's S and z ----
+  tc_fence_before();
+  __syncthreads();
+  if (nt > 0 && !*(volatile int*)abort_flag) mbar_wait(bar(SB_G2), (nt - 1) & 1, wp);
+  tc_fence_after();
+  __syncthreads();
+  if (warp < 8 && !*(volatile int*)abort_flag) {
+    const int c = warp >> 2;
+    float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)C::DPP * D + C::DPP);
+    for (int mb = c; mb < C::NMB; mb += 2) {
+      const int f = mb * 128 + 32 * (warp & 3) + lane;
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t sv[16];
+        tmem_ld16(tmem + lane_base(warp) + C::TM_S + mb * D + c0, sv);
+        if (f < C::DPP) {
+          float4* d4 = reinterpret_cast<float4*>(dst + (size_t)f * D + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                                __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+        }
+      }
+      uint32_t zv[16];
+      tmem_ld16(tmem + lane_base(warp) + C::TM_Z + 16 * mb, zv);
+      if (f < C::DPP) dst[(size_t)C::DPP * D + f] = __uint_as_float(zv[0]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 3-D bf16 tensor map over [planes][rows][cols] with a {box_cols, box_rows, 1} box.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int D>
+cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const void* v, void* ws,
+                    int* dev_status, cudaStream_t s) {
+  StateArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t U = (uint64_t)p.B * p.H;
+  bool ok;
+  if (KIND == HH_FMAP_HEDGEHOG) {
+    ok = make_map(&a.tk, k, D, p.n, U, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&a.tv, v, D, p.n, U, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&a.tw, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    ok = make_map(&a.tk, k, 16, p.n, U, 16, TILE, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_map(&a.tv, v, 16, p.n, U, 16, TILE, CU_TENSOR_MAP_SWIZZLE_32B);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  a.ws = reinterpret_cast<float*>(ws);
+  a.bias = p.Wk ? p.bk : p.bq;
+  a.dev_status = dev_status;
+  a.soft_ns = wait_soft_limit_ns();
+  a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+  a.n = p.n;
+  a.H = p.H;
+  a.P = pl.P;
+  a.L = pl.L;
+  a.NT = pl.NT;
+  const size_t smem = SSmem<KIND, D>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<KIND, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  state_tc_kernel<KIND, D><<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// State pass for P > 1 segments: U * (P - 1) CTAs, one per segment but the last.
+cudaError_t launch_state_tc(const Problem& p, const TcPlan& pl, const void* k, const void* v,
+                            void* ws, int* dev_status, cudaStream_t s) {
+  if (pl.P < 2) return cudaSuccess;
+  if (p.kind == HH_FMAP_TAYLOR2) return state_t<HH_FMAP_TAYLOR2, 16>(p, pl, k, v, ws, dev_status, s);
+  if (p.d == 64) return state_t<HH_FMAP_HEDGEHOG, 64>(p, pl, k, v, ws, dev_status, s);
+  return state_t<HH_FMAP_HEDGEHOG, 128>(p, pl, k, v, ws, dev_status, s);
+}
+
+}  // namespace hh
