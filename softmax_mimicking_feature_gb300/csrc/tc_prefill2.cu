@@ -5,18 +5,22 @@
 // "The Hedgehog MLP Feature Map", Choices 1 and 3), reorganised so that the
 // serial chain of one 128-token tile overlaps the next tile's:
 //
-//   warp 8 (producer): TMA loads and every tcgen05.mma, each issued as soon as
-//   its inputs are ready (the producer polls the barriers without blocking)
+//   warp 8 (MMA issuer): every tcgen05.mma, each group issued as soon as its
+//   inputs are ready (it polls the barriers without blocking); issuing a group
+//   can stall while the tensor pipe is busy, so
+//   warp 9 (loader) issues the TMA loads of the next tiles on its own
 //     G1(t): H_Q = Q_t W, H_K = K_t W
 //     G2(t): Sc = phi(Q_t) phi(K_t)^T;  S += phi(K_t)^T V_t;  Z += phi(K_t)^T 1
 //     G3(t): O = P_t V_t + phi(Q_t) S_bf16(t)
+//            den = P_t [1 0] + phi(Q_t) [z_hi(t) z_lo(t)]  (row sums and phi(q) . z)
 //   warps 0-7 (epilogue) run the phases below for both slots, interleaved as
 //   E2(t-1), E1(t), E3(t-1):
 //     E1 : phi(Q_t) -> TMEM (bf16 pairs), phi(K_t) -> smem          (after G1(t))
-//          S_bf16(t) <- S, z(t) <- Z  (state of the tokens before t)  (after G2(t-1))
+//          S_bf16(t) <- S, z(t) <- Z as a bf16 hi/lo pair (state of the
+//          tokens before t)                                         (after G2(t-1))
 //          -- only then may G2(t) update S --
-//          den(t) = phi(Q_t) . z(t)
-//     E2 : P_t = bf16(tril(Sc)), den += rowsum                      (after G2(t))
+//     E2 : P_t = bf16(tril(Sc)); blocks above the diagonal are zero
+//          without reading Sc, blocks below it need no mask         (after G2(t))
 //     E3 : y = O / den                                              (after G3(t))
 // Each tile owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (Q, K, V,
 // S_bf16, phi(K) -> P); the next tile's Q and K are fetched as soon as
@@ -37,13 +41,14 @@ namespace {
 using namespace tc;
 
 constexpr int D = 64, DP = 128, TILE = 128;
-constexpr int kThreads = 288;
+constexpr int kThreads = 320;   // 8 epilogue warps, warp 8 issues MMAs, warp 9 issues loads
 
 // TMEM columns
 constexpr uint32_t TM_S = 0;     // S: features (lanes) x 64
 constexpr uint32_t TM_Z = 64;    // z: 16 identical columns
 __host__ __device__ constexpr uint32_t TM_Y(int s) { return 128 + 192 * s; }        // 64 cols
 __host__ __device__ constexpr uint32_t TM_X(int s) { return 128 + 192 * s + 64; }   // 128 cols
+__host__ __device__ constexpr uint32_t TM_D(int s) { return 80 + 16 * s; }          // 16 cols
 
 // shared memory
 constexpr uint32_t OFF_W = 0, OFF_ONES = 8192;
@@ -51,10 +56,10 @@ constexpr uint32_t SLOT_BASE = 12288, SLOT_BYTES = 98304;
 // per slot: Q, K (free once H = X W has run), V (free after G3), S_bf16, phi(K) -> P
 constexpr uint32_t S_Q = 0, S_K = 16384, S_V = 32768, S_SB = 49152, S_PHK = 65536;
 __host__ __device__ constexpr uint32_t slot_off(int s) { return SLOT_BASE + s * SLOT_BYTES; }
-constexpr uint32_t OFF_ZS = SLOT_BASE + 2 * SLOT_BYTES;   // float[2][128] z snapshots
-constexpr uint32_t OFF_DQ = OFF_ZS + 1024;                // float[2 slots][2 halves][128]
-constexpr uint32_t OFF_RS = OFF_DQ + 2048;                // float[2 slots][2 halves][128]
-constexpr uint32_t OFF_BQ = OFF_RS + 2048;                // float[64]
+// per slot [128 features x 16] bf16, 32B-swizzled: (z_hi, z_lo, 0, ...), B of den
+constexpr uint32_t OFF_ZM = SLOT_BASE + 2 * SLOT_BYTES;
+constexpr uint32_t OFF_E0 = OFF_ZM + 8192;                // [128 x 16] bf16, column 0 = 1
+constexpr uint32_t OFF_BQ = OFF_E0 + 4096;                // float[64]: b * log2(e)
 constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 20 x u64
 constexpr uint32_t OFF_TM = OFF_BAR + 160;
 constexpr uint32_t SMEM_BYTES = OFF_TM + 16 + 1024;
@@ -81,12 +86,13 @@ __device__ __forceinline__ uint32_t lane_base(int warp) {
   return (uint32_t)(32 * (warp & 3)) << 16;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_constant__ Args2 A) {
+// The bound of 384 threads caps registers at 168 per thread: warps 0, 4, 8
+// (and 1, 5, 9) share one SM sub-partition's 16K registers.
+__global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_constant__ Args2 A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
-  float* zs = reinterpret_cast<float*>(sm + OFF_ZS);
   float* bq_s = reinterpret_cast<float*>(sm + OFF_BQ);
   const uint32_t bars = sb + OFF_BAR;
   auto bar = [&](int b) { return bars + 8u * b; };
@@ -146,7 +152,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  for (int i = tid; i < D; i += kThreads) bq_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
+  for (int i = tid; i < D; i += kThreads)
+    bq_s[i] = A.bias ? A.bias[(size_t)h * D + i] * kLog2e : 0.f;
+  for (int i = tid; i < 8192 / 16; i += kThreads) st_shared_v4(sb + OFF_ZM + 16 * i, 0, 0, 0, 0);
+  for (int r = tid; r < 128; r += kThreads) {   // e0: row r = (1, 0, ..., 0), 32B-swizzled
+    const uint32_t row_addr = sb + OFF_E0 + r * 32;
+    const uint32_t c0 = ((r >> 2) & 1) << 4;
+    st_shared_v4(row_addr + c0, 0x3F80u, 0u, 0u, 0u);
+    st_shared_v4(row_addr + (16 - c0), 0u, 0u, 0u, 0u);
+  }
   for (int i = tid; i < 4096 / 16; i += kThreads)   // bf16 ones: the B operand of Z += phi(K)^T 1
     st_shared_v4(sb + OFF_ONES + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   fence_proxy_async();
@@ -192,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       constexpr uint32_t ID_SU = idesc_bf16(128, D, 1, 1);
       constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);
       constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t ID_DEN = idesc_bf16(128, 16, 0, 1);
       bool ok = mbar_wait(bar(B_W), 0, wp);
       // Descriptor bases: a k-step only moves the 14-bit start-address field
       // (address >> 4), so each MMA below is one 64-bit add plus the instruction.
@@ -210,6 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       const SlotDesc sd0 = slot_desc(0), sd1 = slot_desc(1);
       const uint64_t dW = smem_desc(sb + OFF_W, D * 128, 1024, 2);
       const uint64_t dOnes = smem_desc(sb + OFF_ONES, 16, 256, 6);
+      const uint64_t dE0 = smem_desc(sb + OFF_E0, 16, 256, 6);
+      const uint64_t dZm0 = smem_desc(sb + OFF_ZM, 16, 256, 6);
+      const uint64_t dZm1 = smem_desc(sb + OFF_ZM + 4096, 16, 256, 6);
       // k-step offsets in 16-byte units: K-major inside 64-element panels, MN-major rows
       auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
       auto G1 = [&](int i) {
@@ -247,6 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
 #pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks)
           mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.sbf + 128 * ks, ID_PV, 1);
+        const uint64_t dZm = s ? dZm1 : dZm0;
+#pragma unroll
+        for (int ks = 0; ks < TILE / 16; ++ks)
+          mma_ss(tmem + TM_D(s), d.pk + kmaj(ks), dE0 + 32 * ks, ID_DEN, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < DP / 16; ++ks)
+          mma_ts(tmem + TM_D(s), tmem + TM_Y(s) + ks * 8, dZm + 32 * ks, ID_DEN, 1);
         mma_commit(bar(B_G3 + s));
       };
       // Each action runs once its inputs are ready; per kind they run in tile order.
@@ -255,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       //   G1(i)                        needs LQK(i) landed and E3(i-2) done (TMEM slot free)
       //   G2(i)                        needs E1(i) done and LV(i) landed
       //   G3(i)                        needs E2(i) done
-      int nqk = nt < 2 ? nt : 2, nv = nqk, n1 = 0, n2 = 0, n3 = 0;
+      int n1 = 0, n2 = 0, n3 = 0;
       uint64_t t_last = globaltimer();
       bool reported = false;
       while (ok && n3 < nt) {
@@ -264,20 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             mbar_probe(bar(B_LDV + (n2 & 1)), (n2 >> 1) & 1)) {
           G2(n2++);
           progress = true;
-        } else if (n1 < nqk && mbar_probe(bar(B_LDQK + (n1 & 1)), (n1 >> 1) & 1) &&
+        } else if (n1 < nt && mbar_probe(bar(B_LDQK + (n1 & 1)), (n1 >> 1) & 1) &&
                    (n1 < 2 || mbar_probe(bar(B_E3 + (n1 & 1)), ((n1 - 2) >> 1) & 1))) {
           G1(n1++);
           progress = true;
         } else if (n3 < n2 && mbar_probe(bar(B_E12 + (n3 & 1)), (n3 >> 1) & 1)) {
           G3(n3++);
-          progress = true;
-        } else if (nv < nt && n3 > nv - 2 &&
-                   mbar_probe(bar(B_G3 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
-          load_v(nv++);
-          progress = true;
-        } else if (nqk < nt && n1 > nqk - 2 &&
-                   mbar_probe(bar(B_G1 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
-          load_qk(nqk++);
           progress = true;
         }
         if (progress) {
@@ -296,6 +313,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         }
       }
     }
+  } else if (warp == 9) {
+    // ======================= loader =======================
+    //   LQK(i)  Q, K into slot i&1   once G1(i-2) has completed (H = X W has read them)
+    //   LV(i)   V into slot i&1      once G3(i-2) has completed (S += phi(K)^T V, P V done)
+    if (lane == 0) {
+      int nqk = nt < 2 ? nt : 2, nv = nqk;
+      uint64_t t_last = globaltimer();
+      bool reported = false;
+      while ((nqk < nt || nv < nt) && !*(volatile int*)abort_flag) {
+        bool progress = false;
+        if (nqk < nt && mbar_probe(bar(B_G1 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
+          load_qk(nqk++);
+          progress = true;
+        }
+        if (nv < nt && mbar_probe(bar(B_G3 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
+          load_v(nv++);
+          progress = true;
+        }
+        if (progress) {
+          t_last = globaltimer();
+        } else {
+          const uint64_t dt = globaltimer() - t_last;
+          if (!reported && dt >= A.soft_ns) {
+            reported = true;
+            report_timeout(wp);
+          }
+          if (dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
+          __nanosleep(32);
+        }
+      }
+    }
   } else {
     // ======================= epilogue warps =======================
     // All eight warps work on one phase at a time; phases of the two slots are
@@ -305,8 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
     const int c = warp >> 2;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lb = lane_base(warp);
-    float* dq_s = reinterpret_cast<float*>(sm + OFF_DQ);
-    float* rs_s = reinterpret_cast<float*>(sm + OFF_RS);
+    const int g = warp & 3;
     bool good = true;
 
     auto E1 = [&](int i) {
@@ -323,13 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         uint32_t pp[16], pn[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const float h0 = __uint_as_float(hv[j]) + bq_s[32 * c + j];
-          const float h1 = __uint_as_float(hv[j + 1]) + bq_s[32 * c + j + 1];
-          pp[j / 2] = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
-          pn[j / 2] = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+          // (h + b) log2(e) in one FFMA: the bias is stored pre-scaled
+          const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, bq_s[32 * c + j]);
+          const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, bq_s[32 * c + j + 1]);
+          pp[j / 2] = pack_bf16(ex2_approx(a0), ex2_approx(a1));
+          pn[j / 2] = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
         }
         tc_fence_before();
-        named_bar_sync(1, 256);   // every warp holds its H_Q columns before any overwrite
+        named_bar_sync(2 + g, 64);   // both warps of these lanes hold their H_Q columns
         tc_fence_after();
         tmem_st16(tmem + lb + TM_Y(s) + 16 * c, pp);
         tmem_st16(tmem + lb + TM_Y(s) + 32 + 16 * c, pn);
@@ -344,10 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = 8 * q4 + 2 * e;
-            const float h0 = __uint_as_float(hv[j]) + bq_s[32 * c + j];
-            const float h1 = __uint_as_float(hv[j + 1]) + bq_s[32 * c + j + 1];
-            wpos[e] = valid ? pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e)) : 0u;
-            wneg[e] = valid ? pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e)) : 0u;
+            const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, bq_s[32 * c + j]);
+            const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, bq_s[32 * c + j + 1]);
+            wpos[e] = valid ? pack_bf16(ex2_approx(a0), ex2_approx(a1)) : 0u;
+            wneg[e] = valid ? pack_bf16(ex2_approx(-a0), ex2_approx(-a1)) : 0u;
           }
           st_shared_v4(base + S_PHK + sw128_chunk(row, 4 * c + q4), wpos[0], wpos[1], wpos[2],
                        wpos[3]);
@@ -376,9 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                        pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
         }
         if (c == 0) {
-          uint32_t zv[16];
-          tmem_ld16(tmem + lb + TM_Z, zv);
-          zs[s * 128 + row] = __uint_as_float(zv[0]);
+          // z of feature `row` as z_hi + z_lo (both bf16) in columns 0, 1 of its row
+          uint32_t z0, z1;
+          tmem_ld2(tmem + lb + TM_Z, z0, z1);
+          const float z = __uint_as_float(z0);
+          const float zl = z - __bfloat162float(__float2bfloat16_rn(z));
+          st_shared_v4(sb + OFF_ZM + 4096 * s + row * 32 + (((row >> 2) & 1) << 4),
+                       pack_bf16(z, zl), 0u, 0u, 0u);
         }
       }
       tmem_st_wait();
@@ -386,46 +438,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_E1A + s));
-      named_bar_sync(1, 256);   // z snapshot of every feature written
-      // this half's part of phi(q) . z: packed columns [32c, +32) = features [64c, +64)
-      {
-        uint32_t qp[32];
-        tmem_ld32(tmem + lb + TM_Y(s) + 32 * c, qp);
-        const float* zz = zs + s * 128 + 64 * c;
-        float d = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) d += bf16_lo(qp[j]) * zz[2 * j] + bf16_hi(qp[j]) * zz[2 * j + 1];
-        dq_s[(s * 2 + c) * 128 + row] = d;
-      }
     };
 
     auto E2 = [&](int i) {
       const int s = i & 1;
       const uint32_t par = (i >> 1) & 1;
       const uint32_t base = sb + slot_off(s);
+      // phi(K) in the P panels has been read once G2 completes
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + s), par, wp))) { good = false; return; }
       tc_fence_after();
-      float rs = 0.f;
+      if (c == 1 && g < 2) {
+        // keys 64..127 of rows 0..63: above the diagonal
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {   // keys [64c + 32 h2, +32)
-        uint32_t sv[32];
-        tmem_ld32(tmem + lb + TM_X(s) + 64 * c + 32 * h2, sv);
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(base + S_PHK + 16384 + sw128_chunk(row, q), 0u, 0u, 0u, 0u);
+      } else {
+        const bool diag = (c == 0) == (g < 2);   // the 64 x 64 blocks on the diagonal
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t w4[4];
+        for (int h2 = 0; h2 < 2; ++h2) {   // keys [64c + 32 h2, +32)
+          uint32_t sv[32];
+          tmem_ld32(tmem + lb + TM_X(s) + 64 * c + 32 * h2, sv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int key = 64 * c + 32 * h2 + 8 * q4 + 2 * e;
-            const float a0 = key <= row ? __uint_as_float(sv[8 * q4 + 2 * e]) : 0.f;
-            const float a1 = key + 1 <= row ? __uint_as_float(sv[8 * q4 + 2 * e + 1]) : 0.f;
-            w4[e] = pack_bf16(a0, a1);
-            rs += bf16_lo(w4[e]) + bf16_hi(w4[e]);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = 64 * c + 32 * h2 + 8 * q4 + 2 * e;
+              float a0 = __uint_as_float(sv[8 * q4 + 2 * e]);
+              float a1 = __uint_as_float(sv[8 * q4 + 2 * e + 1]);
+              if (diag) {
+                a0 = key <= row ? a0 : 0.f;
+                a1 = key + 1 <= row ? a1 : 0.f;
+              }
+              w4[e] = pack_bf16(a0, a1);
+            }
+            st_shared_v4(base + S_PHK + c * 16384 + sw128_chunk(row, 4 * h2 + q4), w4[0], w4[1],
+                         w4[2], w4[3]);
           }
-          st_shared_v4(base + S_PHK + c * 16384 + sw128_chunk(row, 4 * h2 + q4), w4[0], w4[1],
-                       w4[2], w4[3]);
         }
       }
-      rs_s[(s * 2 + c) * 128 + row] = rs;
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
@@ -438,12 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
       const int64_t r0 = (int64_t)(t_begin + i) * TILE;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G3 + s), par, wp))) { good = false; return; }
       tc_fence_after();
-      uint32_t ov[32];
+      uint32_t ov[32], d0, d1;
       tmem_ld32(tmem + lb + TM_X(s) + 32 * c, ov);
-      // both halves' partial denominators were written before G3(i) could be issued
-      const float den = (dq_s[(s * 2) * 128 + row] + dq_s[(s * 2 + 1) * 128 + row]) +
-                        (rs_s[(s * 2) * 128 + row] + rs_s[(s * 2 + 1) * 128 + row]);
-      const float inv = 1.f / den;
+      tmem_ld2(tmem + lb + TM_D(s), d0, d1);   // rowsum(P) + phi(q) . z_hi, phi(q) . z_lo
+      const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
       if (r0 + row < A.n) {
         uint4* dst = reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D + 32 * c);
 #pragma unroll
