@@ -10,23 +10,24 @@
 //   can stall while the tensor pipe is busy, so
 //   warp 9 (loader) issues the TMA loads of the next tiles on its own
 //     G1(t): H_Q = Q_t W, H_K = K_t W
-//     G2(t): Sc = phi(Q_t) phi(K_t)^T;  S += phi(K_t)^T V_t;  Z += phi(K_t)^T 1
-//     G3(t): O = P_t V_t + phi(Q_t) S_bf16(t)
-//            den = P_t [1 0] + phi(Q_t) [z_hi(t) z_lo(t)]  (row sums and phi(q) . z)
+//     G2(t): Sc = phi(Q_t) phi(K_t)^T;  [S z] += phi(K_t)^T [V_t 1]
+//     G3(t): [O den] = P_t [V_t e0] + phi(Q_t) [S_bf16(t) z2(t)]
+//   The normaliser rides along as extra columns of the same MMAs (N = 80):
+//   column 64 of the state is z; for the output, e0 = (1, 0, ...) gives the
+//   row sums of P and z2 = (z_hi, z_lo, 0, ...) = z split into two bf16, so
+//   columns 64 and 65 of O sum to the denominator rowsum(P) + phi(q) . z.
 //   warps 0-7 (epilogue) run the phases below for both slots, interleaved as
 //   E2(t-1), E1(t), E3(t-1):
 //     E1 : phi(Q_t) -> TMEM (bf16 pairs), phi(K_t) -> smem          (after G1(t))
-//          S_bf16(t) <- S, z(t) <- Z as a bf16 hi/lo pair (state of the
+//          S_bf16(t) <- S, z2(t) <- z as a bf16 hi/lo pair (state of the
 //          tokens before t)                                         (after G2(t-1))
 //          -- only then may G2(t) update S --
 //     E2 : P_t = bf16(tril(Sc)); blocks above the diagonal are zero
 //          without reading Sc, blocks below it need no mask         (after G2(t))
 //     E3 : y = O / den                                              (after G3(t))
-// Each tile owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (Q, K, V,
-// S_bf16, phi(K) -> P); the next tile's Q and K are fetched as soon as
-// H = X W has read the current ones; the running state S (fp32) and its normaliser Z
-// (fp32, as an MMA with an all-ones operand) stay in TMEM and pass between
-// the groups in tile order.  All mbarrier waits are bounded (tc_ptx.cuh).
+// Each tile owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (Q -> S_bf16,
+// K, V, phi(K) -> P, z2); the running state [S z] (fp32) stays in TMEM and
+// passes between the groups in tile order.  All mbarrier waits are bounded (tc_ptx.cuh).
 
 #include <math.h>
 #include <string.h>
@@ -44,22 +45,20 @@ constexpr int D = 64, DP = 128, TILE = 128;
 constexpr int kThreads = 320;   // 8 epilogue warps, warp 8 issues MMAs, warp 9 issues loads
 
 // TMEM columns
-constexpr uint32_t TM_S = 0;     // S: features (lanes) x 64
-constexpr uint32_t TM_Z = 64;    // z: 16 identical columns
+constexpr uint32_t TM_S = 0;     // [S z 0]: features (lanes) x 80, column 64 = z
 __host__ __device__ constexpr uint32_t TM_Y(int s) { return 128 + 192 * s; }        // 64 cols
 __host__ __device__ constexpr uint32_t TM_X(int s) { return 128 + 192 * s + 64; }   // 128 cols
-__host__ __device__ constexpr uint32_t TM_D(int s) { return 80 + 16 * s; }          // 16 cols
 
 // shared memory
-constexpr uint32_t OFF_W = 0, OFF_ONES = 8192;
-constexpr uint32_t SLOT_BASE = 12288, SLOT_BYTES = 98304;
-// per slot: Q, K (free once H = X W has run), V (free after G3), S_bf16, phi(K) -> P
-constexpr uint32_t S_Q = 0, S_K = 16384, S_V = 32768, S_SB = 49152, S_PHK = 65536;
+constexpr uint32_t OFF_W = 0;
+constexpr uint32_t SLOT_BASE = 8192, SLOT_BYTES = 98304;
+// per slot: Q (free once H = X W has run) -> S_bf16 (read by G3), K, V, phi(K) -> P,
+// z2 ([128 features x 64] panel whose first 16 columns extend S_bf16 to N = 80)
+constexpr uint32_t S_Q = 0, S_SB = 0, S_K = 16384, S_V = 32768, S_PHK = 49152, S_Z2 = 81920;
 __host__ __device__ constexpr uint32_t slot_off(int s) { return SLOT_BASE + s * SLOT_BYTES; }
-// per slot [128 features x 16] bf16, 32B-swizzled: (z_hi, z_lo, 0, ...), B of den
-constexpr uint32_t OFF_ZM = SLOT_BASE + 2 * SLOT_BYTES;
-constexpr uint32_t OFF_E0 = OFF_ZM + 8192;                // [128 x 16] bf16, column 0 = 1
-constexpr uint32_t OFF_BQ = OFF_E0 + 4096;                // float[64]: b * log2(e)
+// e0: [128 x 64] panel, row r = (1, 0, ...), the extra N block of V
+constexpr uint32_t OFF_E0 = SLOT_BASE + 2 * SLOT_BYTES;
+constexpr uint32_t OFF_BQ = OFF_E0 + 16384;               // float[64]: b * log2(e)
 constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 20 x u64
 constexpr uint32_t OFF_TM = OFF_BAR + 160;
 constexpr uint32_t SMEM_BYTES = OFF_TM + 16 + 1024;
@@ -154,15 +153,14 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
   }
   for (int i = tid; i < D; i += kThreads)
     bq_s[i] = A.bias ? A.bias[(size_t)h * D + i] * kLog2e : 0.f;
-  for (int i = tid; i < 8192 / 16; i += kThreads) st_shared_v4(sb + OFF_ZM + 16 * i, 0, 0, 0, 0);
-  for (int r = tid; r < 128; r += kThreads) {   // e0: row r = (1, 0, ..., 0), 32B-swizzled
-    const uint32_t row_addr = sb + OFF_E0 + r * 32;
-    const uint32_t c0 = ((r >> 2) & 1) << 4;
-    st_shared_v4(row_addr + c0, 0x3F80u, 0u, 0u, 0u);
-    st_shared_v4(row_addr + (16 - c0), 0u, 0u, 0u, 0u);
+  for (int i = tid; i < 2 * 1024; i += kThreads) {   // z2 panels: zero (row chunks 1.. stay zero)
+    const int s2 = i >> 10, j = i & 1023;
+    st_shared_v4(sb + slot_off(s2) + S_Z2 + 16 * j, 0u, 0u, 0u, 0u);
   }
-  for (int i = tid; i < 4096 / 16; i += kThreads)   // bf16 ones: the B operand of Z += phi(K)^T 1
-    st_shared_v4(sb + OFF_ONES + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  for (int i = tid; i < 1024; i += kThreads) {       // e0: logical column 0 of every row = 1
+    const int r = i >> 3, ch = i & 7;
+    st_shared_v4(sb + OFF_E0 + sw128_chunk(r, ch), ch == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+  }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -190,8 +188,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     const float z0 = prefix ? __ldcg(prefix + (size_t)DP * D + f) : 0.f;
     uint32_t zr[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) zr[j] = __float_as_uint(z0);
-    tmem_st16(tmem + lane_base(warp) + TM_Z, zr);
+    for (int j = 0; j < 16; ++j) zr[j] = 0u;
+    zr[0] = __float_as_uint(z0);
+    tmem_st16(tmem + lane_base(warp) + TM_S + 64, zr);
     tmem_st_wait();
   }
   tc_fence_before();
@@ -203,13 +202,13 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t ID_H = idesc_bf16(128, D, 0, 1);
       constexpr uint32_t ID_SC = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t ID_SU = idesc_bf16(128, D, 1, 1);
-      constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);
-      constexpr uint32_t ID_PV = idesc_bf16(128, D, 0, 1);
-      constexpr uint32_t ID_DEN = idesc_bf16(128, 16, 0, 1);
+      constexpr uint32_t ID_SU = idesc_bf16(128, D + 16, 1, 1);   // [S z] += phiK^T [V 1]
+      constexpr uint32_t ID_PV = idesc_bf16(128, D + 16, 0, 1);   // [O den]
       bool ok = mbar_wait(bar(B_W), 0, wp);
       // Descriptor bases: a k-step only moves the 14-bit start-address field
       // (address >> 4), so each MMA below is one 64-bit add plus the instruction.
+      // MN-major B operands with N = 80 span two 64-column blocks: the second
+      // block (e0 for V, z2 for S_bf16) sits one leading-byte offset further.
       struct SlotDesc { uint64_t q, k, pk, pm, v, sbf; };
       auto slot_desc = [&](int s2) {
         const uint32_t base = sb + slot_off(s2);
@@ -218,16 +217,12 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
         d.k = smem_desc(base + S_K, 16, 1024, 2);
         d.pk = smem_desc(base + S_PHK, 16, 1024, 2);      // phi(K) / P as K-major operand
         d.pm = smem_desc(base + S_PHK, 16384, 1024, 2);   // phi(K)^T as MN-major operand
-        d.v = smem_desc(base + S_V, 16384, 1024, 2);      // MN-major, 2048 B per k-step
-        d.sbf = smem_desc(base + S_SB, DP * 128, 1024, 2);
+        d.v = smem_desc(base + S_V, OFF_E0 - (slot_off(s2) + S_V), 1024, 2);  // 2048 B per k-step
+        d.sbf = smem_desc(base + S_SB, S_Z2 - S_SB, 1024, 2);
         return d;
       };
       const SlotDesc sd0 = slot_desc(0), sd1 = slot_desc(1);
       const uint64_t dW = smem_desc(sb + OFF_W, D * 128, 1024, 2);
-      const uint64_t dOnes = smem_desc(sb + OFF_ONES, 16, 256, 6);
-      const uint64_t dE0 = smem_desc(sb + OFF_E0, 16, 256, 6);
-      const uint64_t dZm0 = smem_desc(sb + OFF_ZM, 16, 256, 6);
-      const uint64_t dZm1 = smem_desc(sb + OFF_ZM + 4096, 16, 256, 6);
       // k-step offsets in 16-byte units: K-major inside 64-element panels, MN-major rows
       auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
       auto G1 = [&](int i) {
@@ -249,10 +244,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
         for (int ks = 0; ks < DP / 16; ++ks)
           mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.pk + kmaj(ks), ID_SC, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < TILE / 16; ++ks) {
+        for (int ks = 0; ks < TILE / 16; ++ks)
           mma_ss(tmem + TM_S, d.pm + 128 * ks, d.v + 128 * ks, ID_SU, 1);
-          mma_ss(tmem + TM_Z, d.pm + 128 * ks, dOnes + 32 * ks, ID_Z, 1);
-        }
         mma_commit(bar(B_G2 + s));
       };
       auto G3 = [&](int i) {
@@ -265,18 +258,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
 #pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks)
           mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.sbf + 128 * ks, ID_PV, 1);
-        const uint64_t dZm = s ? dZm1 : dZm0;
-#pragma unroll
-        for (int ks = 0; ks < TILE / 16; ++ks)
-          mma_ss(tmem + TM_D(s), d.pk + kmaj(ks), dE0 + 32 * ks, ID_DEN, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < DP / 16; ++ks)
-          mma_ts(tmem + TM_D(s), tmem + TM_Y(s) + ks * 8, dZm + 32 * ks, ID_DEN, 1);
         mma_commit(bar(B_G3 + s));
       };
       // Each action runs once its inputs are ready; per kind they run in tile order.
-      //   LQK(i)  Q, K into slot i&1   needs G1(i-2) complete (H = X W has read them)
-      //   LV(i)   V into slot i&1      needs G3(i-2) complete (S += phi(K)^T V, P V done)
       //   G1(i)                        needs LQK(i) landed and E3(i-2) done (TMEM slot free)
       //   G2(i)                        needs E1(i) done and LV(i) landed
       //   G3(i)                        needs E2(i) done
@@ -315,7 +299,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ======================= loader =======================
-    //   LQK(i)  Q, K into slot i&1   once G1(i-2) has completed (H = X W has read them)
+    //   LQK(i)  Q, K into slot i&1   once G3(i-2) has completed (it read S_bf16, which
+    //           replaces Q in the slot)
     //   LV(i)   V into slot i&1      once G3(i-2) has completed (S += phi(K)^T V, P V done)
     if (lane == 0) {
       int nqk = nt < 2 ? nt : 2, nv = nqk;
@@ -323,7 +308,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       bool reported = false;
       while ((nqk < nt || nv < nt) && !*(volatile int*)abort_flag) {
         bool progress = false;
-        if (nqk < nt && mbar_probe(bar(B_G1 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
+        if (nqk < nt && mbar_probe(bar(B_G3 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
           load_qk(nqk++);
           progress = true;
         }
@@ -424,13 +409,12 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
                        pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
         }
         if (c == 0) {
-          // z of feature `row` as z_hi + z_lo (both bf16) in columns 0, 1 of its row
+          // z of feature `row` as z_hi + z_lo (both bf16) in columns 0, 1 of its z2 row
           uint32_t z0, z1;
-          tmem_ld2(tmem + lb + TM_Z, z0, z1);
+          tmem_ld2(tmem + lb + TM_S + 64, z0, z1);
           const float z = __uint_as_float(z0);
           const float zl = z - __bfloat162float(__float2bfloat16_rn(z));
-          st_shared_v4(sb + OFF_ZM + 4096 * s + row * 32 + (((row >> 2) & 1) << 4),
-                       pack_bf16(z, zl), 0u, 0u, 0u);
+          st_shared_v4(base + S_Z2 + sw128_chunk(row, 0), pack_bf16(z, zl), 0u, 0u, 0u);
         }
       }
       tmem_st_wait();
@@ -491,7 +475,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       tc_fence_after();
       uint32_t ov[32], d0, d1;
       tmem_ld32(tmem + lb + TM_X(s) + 32 * c, ov);
-      tmem_ld2(tmem + lb + TM_D(s), d0, d1);   // rowsum(P) + phi(q) . z_hi, phi(q) . z_lo
+      tmem_ld2(tmem + lb + TM_X(s) + 64, d0, d1);   // rowsum(P) + phi(q) . z_hi, phi(q) . z_lo
       const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
       if (r0 + row < A.n) {
         uint4* dst = reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D + 32 * c);
@@ -530,9 +514,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     for (int j = 0; j < 16; ++j)
       dst[j] = make_float4(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]),
                            __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
-    uint32_t zv[16];
-    tmem_ld16(tmem + lane_base(warp) + TM_Z, zv);
-    A.z_out[(size_t)unit * DP + f] = __uint_as_float(zv[0]);
+    uint32_t z0, z1;
+    tmem_ld2(tmem + lane_base(warp) + TM_S + 64, z0, z1);
+    A.z_out[(size_t)unit * DP + f] = __uint_as_float(z0);
   }
   tc_fence_before();
   __syncthreads();
