@@ -382,6 +382,425 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
   if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Hedgehog d = 128: transposed form.  H_K^T = W^T K_t^T lands in TMEM with the
+// 128 hidden units on the lanes and the tile's tokens on the columns; the
+// feature warps overwrite it in place with phi(K_t)^T as bf16 pairs
+// (exp(+h) and exp(-h) blocks), which is directly the A operand of
+//   S[+/-] += phi(K_t)^T[+/-] V_t     (A from TMEM, M = 128 features)
+// so phi(K) never goes through shared memory, and z is a per-thread running
+// sum over the thread's tokens.  Two H buffers let G1(t+1) run while the
+// feature warps work on tile t; warp 8 issues MMAs, warp 9 issues loads.
+// ---------------------------------------------------------------------------
+namespace t128 {
+constexpr int D = 128;
+constexpr uint32_t XT = TILE * D * 2;                  // 32 KB
+constexpr uint32_t OFF_W = 0;                          // W: 2 panels [128 i x 64 j]
+constexpr uint32_t OFF_K = 32768;                      // 2 stages
+constexpr uint32_t OFF_V = OFF_K + 2 * XT;             // 2 stages
+constexpr uint32_t OFF_ZX = OFF_V + 2 * XT;            // float[2][128] z exchange
+constexpr uint32_t OFF_BAR = OFF_ZX + 1024;
+enum { B_W = 0, B_LDK = 1, B_LDV = 3, B_G1 = 5, B_E1 = 7, B_G2 = 9, B_COUNT = 11 };
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
+constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
+static_assert(ALLOC <= 227 * 1024, "shared memory");
+constexpr uint32_t TM_S = 0;                           // S+ [0,128), S- [128,256)
+__host__ __device__ constexpr uint32_t TM_H(int b) { return 256 + 128 * b; }
+constexpr int kThreads = 320;
+}  // namespace t128
+
+// The bound of 384 threads caps registers at 168 per thread (warps 0, 4, 8
+// and 1, 5, 9 share one SM sub-partition's registers).
+__global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constant__ StateArgs A) {
+  using namespace t128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t bars = sb + OFF_BAR;
+  auto bar = [&](int b) { return bars + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 4);
+  float* zx = reinterpret_cast<float*>(sm + OFF_ZX);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t unit = blockIdx.x / (A.P - 1);
+  const int seg = blockIdx.x % (A.P - 1);
+  const int h = (int)(unit % A.H);
+  const int t_begin = seg * A.L;
+  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+
+  if (tid == 0) {
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(bar(b), (b == B_E1 || b == B_E1 + 1) ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto load_k = [&](int i) {
+    const uint32_t dst = sb + OFF_K + (i & 1) * XT, b = bar(B_LDK + (i & 1));
+    mbar_expect_tx(b, XT);
+    for (int x = 0; x < 2; ++x)
+      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+  };
+  auto load_v = [&](int i) {
+    const uint32_t dst = sb + OFF_V + (i & 1) * XT, b = bar(B_LDV + (i & 1));
+    mbar_expect_tx(b, XT);
+    for (int x = 0; x < 2; ++x)
+      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+  };
+  if (warp == 8 && lane == 0 && nt > 0) {
+    mbar_expect_tx(bar(B_W), D * D * 2);
+    for (int x = 0; x < 2; ++x) tma_load_3d(sb + OFF_W + x * 16384, &A.tw, bar(B_W), 64 * x, 0, h);
+    for (int i = 0; i < 2 && i < nt; ++i) {
+      load_k(i);
+      load_v(i);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp < 4) {   // S = 0
+    uint32_t zr[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) zr[j] = 0u;
+    for (int c0 = 0; c0 < 256; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  float zp = 0.f, zn = 0.f;   // this thread's share of z (hidden unit j, tokens of its half)
+  if (warp == 8) {
+    // ======================= MMA issuer =======================
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t ID_H = idesc_bf16(128, 128, 1, 0);   // W^T[MN-major] K^T[K-major]
+      constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 1);   // phiK^T[TMEM] V[MN-major]
+      auto g1 = [&](int i) {
+        const uint32_t kb = sb + OFF_K + (i & 1) * XT;
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + TM_H(i & 1), smem_desc(sb + OFF_W + ks * 2048, 16384, 1024, 2),
+                 smem_desc(kb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2), ID_H, ks > 0);
+        mma_commit(bar(B_G1 + (i & 1)));
+      };
+      bool ok = mbar_wait(bar(B_W), 0, wp) && mbar_wait(bar(B_LDK), 0, wp);
+      tc_fence_after();
+      if (ok) g1(0);
+      for (int i = 0; i < nt && ok; ++i) {
+        if (i + 1 < nt) {
+          // H buffer (i+1)&1 held phi(i-1), the A operand of G2(i-1)
+          ok = mbar_wait(bar(B_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
+               (i == 0 || mbar_wait(bar(B_G2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp));
+          if (!ok) break;
+          tc_fence_after();
+          g1(i + 1);
+        }
+        ok = mbar_wait(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
+             mbar_wait(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vb = sb + OFF_V + (i & 1) * XT;
+        for (int mb = 0; mb < 2; ++mb)
+          for (int ks = 0; ks < TILE / 16; ++ks)
+            mma_ts(tmem + TM_S + 128 * mb, tmem + TM_H(i & 1) + 64 * (ks >> 2) + 8 * (ks & 3) + 32 * mb,
+                   smem_desc(vb + ks * 2048, 16384, 1024, 2), ID_S, 1);
+        mma_commit(bar(B_G2 + (i & 1)));
+      }
+      if (!ok) *(volatile int*)abort_flag = 1;
+    }
+  } else if (warp == 9) {
+    // ======================= loader =======================
+    //   K(i+2) into stage i&1 once G1(i) has read K(i); V(i+2) once G2(i) has read V(i)
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i + 2 < nt && ok; ++i) {
+        ok = mbar_wait(bar(B_G1 + (i & 1)), (i >> 1) & 1, wp);
+        if (ok) load_k(i + 2);
+        ok = ok && mbar_wait(bar(B_G2 + (i & 1)), (i >> 1) & 1, wp);
+        if (ok) load_v(i + 2);
+      }
+      if (!ok) *(volatile int*)abort_flag = 1;
+    }
+  } else {
+    // ======================= feature warps =======================
+    // warp w: hidden unit j = 32 (w % 4) + lane (TMEM lane), tokens [64 c, 64 c + 64) of the tile
+    const int c = warp >> 2;
+    const int j = 32 * (warp & 3) + lane;
+    const uint32_t lb = lane_base(warp);
+    const float bj = A.bias ? A.bias[(size_t)h * D + j] * kLog2e : 0.f;
+    for (int i = 0; i < nt; ++i) {
+      const int b = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + b), (i >> 1) & 1, wp))) break;
+      tc_fence_after();
+      const int64_t tok0 = (int64_t)(t_begin + i) * TILE + 64 * c;
+      uint32_t hv[64];
+      tmem_ld64(tmem + lb + TM_H(b) + 64 * c, hv);
+      uint32_t pp[32], pn[32];
+#pragma unroll
+      for (int t = 0; t < 64; t += 2) {
+        const float a0 = fmaf(__uint_as_float(hv[t]), kLog2e, bj);
+        const float a1 = fmaf(__uint_as_float(hv[t + 1]), kLog2e, bj);
+        uint32_t wpos = pack_bf16(ex2_approx(a0), ex2_approx(a1));
+        uint32_t wneg = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+        if (tok0 + t >= A.n) wpos = wneg = 0u;
+        else if (tok0 + t + 1 >= A.n) { wpos &= 0xFFFFu; wneg &= 0xFFFFu; }
+        pp[t / 2] = wpos;
+        pn[t / 2] = wneg;
+        zp += bf16_lo(wpos) + bf16_hi(wpos);
+        zn += bf16_lo(wneg) + bf16_hi(wneg);
+      }
+      // tokens [64c, +64) -> packed columns [64c, +32) (exp(+h)) and [64c + 32, +32) (exp(-h))
+      tmem_st32(tmem + lb + TM_H(b) + 64 * c, pp);
+      tmem_st32(tmem + lb + TM_H(b) + 64 * c + 32, pn);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_E1 + b));
+    }
+  }
+
+  // ---- export: S (features x 128) and z of this segment ----
+  tc_fence_before();
+  __syncthreads();
+  if (nt > 0 && !*(volatile int*)abort_flag)
+    mbar_wait(bar(B_G2 + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, wp);
+  tc_fence_after();
+  if (warp >= 4 && warp < 8) {
+    zx[32 * (warp & 3) + lane] = zp;
+    zx[128 + 32 * (warp & 3) + lane] = zn;
+  }
+  __syncthreads();
+  if (warp < 8 && !*(volatile int*)abort_flag) {
+    const int c = warp >> 2;   // feature block: exp(+h) for c = 0, exp(-h) for c = 1
+    const int j = 32 * (warp & 3) + lane;
+    float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)2 * D * D + 2 * D);
+    const int f = 128 * c + j;
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t sv[32];
+      tmem_ld32(tmem + lane_base(warp) + TM_S + 128 * c + c0, sv);
+      float4* d4 = reinterpret_cast<float4*>(dst + (size_t)f * D + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                            __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+    }
+    if (c == 0) {
+      dst[(size_t)2 * D * D + j] = zp + zx[j];
+      dst[(size_t)2 * D * D + D + j] = zn + zx[128 + j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Taylor, d = 16.  phi(K_t) is built row-wise (thread = token) into one of two
+// shared-memory buffers, so tile t+1's features are written while G2(t)
+// still reads tile t's.  z rides along the state update as an extra column:
+//   [S z] += phi(K_t)^T [V_t e0]     (N = 32, e0 = (1, 0, ..., 0))
+// Warp 8 issues MMAs, warp 9 issues loads.
+// ---------------------------------------------------------------------------
+namespace tay {
+constexpr int DP = 288;                                // stored features (273 used)
+constexpr uint32_t XT = TILE * 16 * 2;                 // 4 KB
+constexpr uint32_t OFF_K = 0;                          // 2 stages, 32 B rows
+constexpr uint32_t OFF_V = 8192;                       // 2 stages, 32B-swizzled
+constexpr uint32_t OFF_E0 = 16384;                     // [128 x 16], column 0 = 1
+constexpr uint32_t OFF_PHK = 24576;                    // 2 buffers x 6 panels of 16 KB
+constexpr uint32_t PHK_BYTES = 6 * 16384;
+constexpr uint32_t OFF_BAR = OFF_PHK + 2 * PHK_BYTES;
+enum { B_LDK = 0, B_LDV = 2, B_E1 = 4, B_G2 = 6, B_COUNT = 8 };
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
+constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
+static_assert(ALLOC <= 227 * 1024, "shared memory");
+constexpr uint32_t TM_S = 0;                           // 3 blocks x [S (16) | z, 0... (16)]
+constexpr int kThreads = 320;
+}  // namespace tay
+
+__global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_constant__ StateArgs A) {
+  using namespace tay;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t bars = sb + OFF_BAR;
+  auto bar = [&](int b) { return bars + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t unit = blockIdx.x / (A.P - 1);
+  const int seg = blockIdx.x % (A.P - 1);
+  const int t_begin = seg * A.L;
+  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+
+  if (tid == 0) {
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(bar(b), (b == B_E1 || b == B_E1 + 1) ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto load_k = [&](int i) {
+    const uint32_t b = bar(B_LDK + (i & 1));
+    mbar_expect_tx(b, XT);
+    tma_load_3d(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, (int)unit);
+  };
+  auto load_v = [&](int i) {
+    const uint32_t b = bar(B_LDV + (i & 1));
+    mbar_expect_tx(b, XT);
+    tma_load_3d(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, (int)unit);
+  };
+  if (warp == 8 && lane == 0)
+    for (int i = 0; i < 2 && i < nt; ++i) {
+      load_k(i);
+      load_v(i);
+    }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 128);
+    tmem_relinquish();
+  }
+  // e0 rows (1, 0, ..., 0) with the 32-byte swizzle; phi(K) buffers zero (features 288.. stay 0)
+  for (int r = tid; r < 128; r += tay::kThreads) {
+    const uint32_t c0 = ((r >> 2) & 1) << 4;
+    st_shared_v4(sb + OFF_E0 + r * 32 + c0, 0x3F80u, 0u, 0u, 0u);
+    st_shared_v4(sb + OFF_E0 + r * 32 + (16 - c0), 0u, 0u, 0u, 0u);
+  }
+  for (uint32_t i = tid * 16; i < 2 * PHK_BYTES; i += tay::kThreads * 16)
+    st_shared_v4(sb + OFF_PHK + i, 0u, 0u, 0u, 0u);
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp < 4) {   // [S z] = 0
+    uint32_t zr[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) zr[j] = 0u;
+    for (int c0 = 0; c0 < 96; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 8) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t ID_S = idesc_bf16(128, 32, 1, 1);   // phiK^T[MN] [V e0][MN]
+      bool ok = true;
+      for (int i = 0; i < nt && ok; ++i) {
+        ok = mbar_wait(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
+             mbar_wait(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t pb = sb + OFF_PHK + (i & 1) * PHK_BYTES;
+        const uint32_t vb = sb + OFF_V + (i & 1) * XT;
+        for (int mb = 0; mb < 3; ++mb)
+          for (int ks = 0; ks < TILE / 16; ++ks)
+            mma_ss(tmem + TM_S + 32 * mb,
+                   smem_desc(pb + (2 * mb) * 16384 + ks * 2048, 16384, 1024, 2),
+                   smem_desc(vb + ks * 512, OFF_E0 - (OFF_V + (i & 1) * XT), 256, 6), ID_S, 1);
+        mma_commit(bar(B_G2 + (i & 1)));
+      }
+      if (!ok) *(volatile int*)abort_flag = 1;
+    }
+  } else if (warp == 9) {
+    // ======================= loader =======================
+    //   K(i+2) once the feature warps have read K(i); V(i+2) once G2(i) has read V(i)
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i + 2 < nt && ok; ++i) {
+        ok = mbar_wait(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp);
+        if (ok) load_k(i + 2);
+        ok = ok && mbar_wait(bar(B_G2 + (i & 1)), (i >> 1) & 1, wp);
+        if (ok) load_v(i + 2);
+      }
+      if (!ok) *(volatile int*)abort_flag = 1;
+    }
+  } else {
+    // ======================= feature warps =======================
+    const int c = warp >> 2;
+    const int row = 32 * (warp & 3) + lane;
+    for (int i = 0; i < nt; ++i) {
+      const int b = i & 1;
+      const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_LDK + b), (i >> 1) & 1, wp))) break;
+      const __nv_bfloat16* krow =
+          reinterpret_cast<const __nv_bfloat16*>(sm + OFF_K + b * XT) + row * 16;
+      float x[16];
+#pragma unroll
+      for (int k2 = 0; k2 < 16; ++k2) x[k2] = __bfloat162float(krow[k2]);
+      // half 0: features [0, 160), half 1: [160, 288)
+      uint32_t w[80];
+      if (c == 0) {
+        taylor_pack<0, 0>(x, valid, w);
+        taylor_pack<32, 16>(x, valid, w);
+        taylor_pack<64, 32>(x, valid, w);
+        taylor_pack<96, 48>(x, valid, w);
+        taylor_pack<128, 64>(x, valid, w);
+      } else {
+        taylor_pack<160, 0>(x, valid, w);
+        taylor_pack<192, 16>(x, valid, w);
+        taylor_pack<224, 32>(x, valid, w);
+        taylor_pack<256, 48>(x, valid, w);
+      }
+      // buffer b held phi(K(i-2)), read by G2(i-2)
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + b), ((i - 2) >> 1) & 1, wp)))
+        break;
+      const uint32_t phk = sb + OFF_PHK + b * PHK_BYTES;
+      const int f0 = c == 0 ? 0 : 160;
+      const int nq = c == 0 ? 20 : 16;   // 16-byte chunks (8 features each)
+#pragma unroll
+      for (int q = 0; q < 20; ++q) {
+        if (q < nq) {
+          const int f = f0 + 8 * q;
+          st_shared_v4(phk + (f / 64) * 16384 + sw128_chunk(row, (f % 64) / 8), w[4 * q],
+                       w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_E1 + b));
+    }
+  }
+
+  // ---- export this segment's S and z ----
+  tc_fence_before();
+  __syncthreads();
+  if (nt > 0 && !*(volatile int*)abort_flag)
+    mbar_wait(bar(B_G2 + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, wp);
+  tc_fence_after();
+  __syncthreads();
+  if (warp < 8 && !*(volatile int*)abort_flag) {
+    const int c = warp >> 2;
+    float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)DP * 16 + DP);
+    for (int mb = c; mb < 3; mb += 2) {
+      const int f = mb * 128 + 32 * (warp & 3) + lane;
+      uint32_t sv[32];
+      tmem_ld32(tmem + lane_base(warp) + TM_S + 32 * mb, sv);
+      if (f < DP) {
+        float4* d4 = reinterpret_cast<float4*>(dst + (size_t)f * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                              __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+        dst[(size_t)DP * 16 + f] = __uint_as_float(sv[16]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -437,6 +856,22 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
+  if (KIND == HH_FMAP_TAYLOR2) {
+    cudaError_t e = cudaFuncSetAttribute(state_taylor_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tay::ALLOC);
+    if (e != cudaSuccess) return e;
+    state_taylor_kernel<<<(unsigned)(U * (pl.P - 1)), tay::kThreads, tay::ALLOC, s>>>(a);
+    return cudaGetLastError();
+  }
+  if (KIND == HH_FMAP_HEDGEHOG && D == 128) {
+    cudaError_t e = cudaFuncSetAttribute(state_t128_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)t128::ALLOC);
+    if (e != cudaSuccess) return e;
+    state_t128_kernel<<<(unsigned)(U * (pl.P - 1)), t128::kThreads, t128::ALLOC, s>>>(a);
+    return cudaGetLastError();
+  }
   const size_t smem = SSmem<KIND, D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<KIND, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
