@@ -19,9 +19,9 @@
 // the result is the same causal sum for chunk 64 or 128.
 //
 // Long sequences are cut into segments processed by different CTAs.  A
-// state pass (OUT = false) writes each segment's sum of phi(k)^T v and phi(k)
+// state pass (tc_state.cu) writes each segment's sum of phi(k)^T v and phi(k)
 // into the workspace, a scan kernel turns those into inclusive prefix sums
-// (in segment order), and the output pass starts segment s from prefix s-1.
+// (in segment order), and this output pass starts segment s from prefix s-1.
 //
 // Roles: thread 0 issues TMA loads and MMAs; all 8 warps run the epilogues
 // (warp w owns TMEM lanes 32*(w%4).. and one half of the columns).  Every
@@ -218,7 +218,7 @@ __device__ __forceinline__ void taylor_k_chunk(const float (&x)[16], bool valid,
 template <int KIND, int D>
 constexpr int min_blocks() { return (KIND == HH_FMAP_HEDGEHOG && D == 64) ? 2 : 1; }
 
-template <int KIND, int D, bool OUT>
+template <int KIND, int D>
 __global__ void __launch_bounds__(kThreads, min_blocks<KIND, D>())
 prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   using C = Cfg<KIND, D>;
@@ -243,9 +243,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   const int g = warp & 3, half = warp >> 2;
   const int row = 32 * g + lane;  // TMEM lane / tile row owned by this thread
 
-  const int nseg_grid = OUT ? A.P : (A.P - 1);
-  const int64_t unit = blockIdx.x / nseg_grid;
-  const int seg = blockIdx.x % nseg_grid;
+  const int64_t unit = blockIdx.x / A.P;
+  const int seg = blockIdx.x % A.P;
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
   const int t_end = min(A.NT, t_begin + A.L);
@@ -262,21 +261,21 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     fence_mbar_init();
     prefetch_tmap(&A.tk);
     prefetch_tmap(&A.tv);
-    if (OUT) prefetch_tmap(&A.tq);
+    prefetch_tmap(&A.tq);
   }
   // ---- loads of one tile ----
   auto issue_loads = [&](int t) {
     const int r0 = t * kTile;
-    uint32_t bytes = C::XT_BYTES * (OUT ? 3 : 2);
+    uint32_t bytes = C::XT_BYTES * 3;
     mbar_expect_tx(bar_load, bytes);
     if (KIND == HH_FMAP_HEDGEHOG) {
       for (int i = 0; i < D / 64; ++i) {
-        if (OUT) tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, (int)unit);
+        tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, (int)unit);
         tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, (int)unit);
         tma_load_3d(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, (int)unit);
       }
     } else {
-      if (OUT) tma_load_3d(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, (int)unit);
+      tma_load_3d(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, (int)unit);
       tma_load_3d(sb + C::OFF_K, &A.tk, bar_load, 0, r0, (int)unit);
       tma_load_3d(sb + C::OFF_V, &A.tv, bar_load, 0, r0, (int)unit);
     }
@@ -304,7 +303,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     }
   }
   const size_t seg_elems = (size_t)C::DPP * D + C::DPP;
-  const float* prefix = (OUT && seg > 0) ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * seg_elems
+  const float* prefix = seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * seg_elems
                                          : nullptr;
   // initial z: the state of the tokens before this segment
   for (int f = tid; f < SM::ZN; f += kThreads)
@@ -330,7 +329,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
         float4 v4[CW / 4];
 #pragma unroll
         for (int j = 0; j < CW / 4; ++j)
-          v4[j] = frow ? __ldcg(reinterpret_cast<const float4*>(prefix + (size_t)f * D + c0) + j)
+          v4[j] = frow ? __ldcg(reinterpret_cast<const float4*>(prefix + ws_s_index(f, c0 + 4 * j, D)))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < CW; j += 16) {
@@ -385,9 +384,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
             const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
             const uint64_t bq = smem_desc(sb + C::OFF_W + ks * 2048, D * 128, 1024, 2);
             const uint64_t bk = smem_desc(sb + w_key_off + ks * 2048, D * 128, 1024, 2);
-            if (OUT)
-              mma_ss(tmem + C::TM_Y, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2), bq, IDESC_H,
-                     ks > 0);
+            mma_ss(tmem + C::TM_Y, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2), bq, IDESC_H,
+                   ks > 0);
             mma_ss(tmem + C::TM_X, smem_desc(sb + C::OFF_K + koff, 16, 1024, 2), bk, IDESC_H,
                    ks > 0);
           }
@@ -408,8 +406,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     if (__syncthreads_or(failed)) { failed = true; break; }
 
     // ================= epilogue 1: features, S_bf16, z =================
-    // -- phi(Q) into TMEM (output pass), denominator part phi(q) . z_before
-    if (OUT) {
+    // -- phi(Q) into TMEM, denominator part phi(q) . z_before
+    {
       float dq = 0.f;
       if (KIND == HH_FMAP_HEDGEHOG) {
         constexpr int HC = D / 2;  // H columns per warp half
@@ -529,7 +527,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     }
 
     // -- S_bf16 <- S (state before this tile), the B operand of phi(Q) S
-    if (OUT) {
+    {
       if (KIND == HH_FMAP_HEDGEHOG) {
         // S_bf16 panel: [DP rows][D cols] as D/64 column blocks of [DP rows x 128 B]
         constexpr int CPW = (C::NMB == 2) ? D : D / 2;   // columns handled by this warp
@@ -585,12 +583,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 
     // ================= group 2: Sc, S update =================
     if (tid == 0) {
-      if (OUT) {
-        for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
-          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
-          mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8,
-                 smem_desc(sb + C::OFF_PHK + koff, 16, 1024, 2), IDESC_SC, ks > 0);
-        }
+      for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
+        const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+        mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8,
+               smem_desc(sb + C::OFF_PHK + koff, 16, 1024, 2), IDESC_SC, ks > 0);
       }
       for (int mb = 0; mb < C::NMB; ++mb)
         for (int ks = 0; ks < kTile / 16; ++ks)
@@ -602,12 +598,6 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
     ph_mma ^= 1;
     tc_fence_after();
-
-    if (!OUT) {
-      if (tid == 0 && t + 1 < t_end) issue_loads(t + 1);
-      if (__syncthreads_or(failed)) { failed = true; break; }
-      continue;
-    }
 
     // ================= epilogue 2: P = bf16(tril(Sc)), row sums =================
     {
@@ -716,13 +706,11 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     tc_fence_after();
   }
 
-  // ---- export the state ----
+  // ---- export the final state of the last segment (row-major S_out, z_out) ----
   __syncthreads();
-  const bool export_out = OUT && A.S_out && seg == A.P - 1;
-  if (!failed && (!OUT || export_out)) {
-    float* Sdst = OUT ? A.S_out + (size_t)unit * C::DPP * D
-                      : A.ws + ((size_t)unit * (A.P - 1) + seg) * seg_elems;
-    float* zdst = OUT ? A.z_out + (size_t)unit * C::DPP : Sdst + (size_t)C::DPP * D;
+  if (!failed && A.S_out && seg == A.P - 1) {
+    float* Sdst = A.S_out + (size_t)unit * C::DPP * D;
+    float* zdst = A.z_out + (size_t)unit * C::DPP;
     for (int mb = half; mb < C::NMB; mb += 2) {
       const int f = mb * 128 + row;
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -879,7 +867,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   }
   if (KIND == HH_FMAP_HEDGEHOG && D == 64 && !p.Wk)
     return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
-  auto kern = prefill_tc_kernel<KIND, D, true>;
+  auto kern = prefill_tc_kernel<KIND, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)(U * pl.P), kThreads, smem, s>>>(a);

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     for (int c0 = 0; c0 < D; c0 += 32) {
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
-        const float4 v4 = prefix ? __ldcg(reinterpret_cast<const float4*>(prefix + (size_t)f * D + c0 + j))
+        const float4 v4 = prefix ? __ldcg(reinterpret_cast<const float4*>(prefix + ws_s_index(f, c0 + j, D)))
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         r[j] = __float_as_uint(v4.x);
         r[j + 1] = __float_as_uint(v4.y);

@@ -109,6 +109,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow(bar, parity, w, t0);
 }
 
+// Bounded wait for a single issuing thread: polls with test_wait (never
+// suspends), so the thread resumes as soon as the phase completes.  Same
+// time limits and abort behaviour as mbar_wait.
+static __device__ __noinline__ bool mbar_wait_poll_slow(uint32_t bar, uint32_t parity,
+                                                       const WaitPolicy& w, uint64_t t0) {
+  bool reported = false;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_probe(bar, parity)) {
+      if (!reported && globaltimer() - t0 >= w.soft_ns) report_timeout(w);
+      return true;
+    }
+    if ((it & 63) == 0) {
+      if (*(volatile int*)w.abort_flag) return false;
+      const uint64_t dt = globaltimer() - t0;
+      if (!reported && dt >= w.soft_ns) {
+        reported = true;
+        report_timeout(w);
+      }
+      if (dt >= w.hard_ns) {
+        *(volatile int*)w.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, const WaitPolicy& w) {
+  if (mbar_probe(bar, parity)) return true;
+  return mbar_wait_poll_slow(bar, parity, w, globaltimer());
+}
+
 // ---- TMA ------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y, int z) {
@@ -347,6 +377,15 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- segment-state workspace layout ---------------------------------------
+// S [DPP features][D columns] is stored in 128-float blocks of 32 features x
+// 4 columns (DPP a multiple of 32), so the float4 accesses of a warp holding
+// 32 consecutive features touch 512 contiguous bytes; z [DPP] follows S.
+__host__ __device__ constexpr size_t ws_s_index(int f, int c, int D) {
+  return ((size_t)(f >> 5) * (size_t)(D >> 2) + (size_t)(c >> 2)) * 128 + (size_t)(f & 31) * 4 +
+         (size_t)(c & 3);
 }
 
 // ---- small numerics -------------------------------------------------------

@@ -95,7 +95,7 @@ struct SSmem {
 
 struct StateArgs {
   CUtensorMap tk, tv, tw;
-  float* ws;          // [U][P-1][DPP*D + DPP]: S (row-major [DPP][D]) then z
+  float* ws;          // [U][P-1][DPP*D + DPP]: S (ws_s_index layout) then z
   const float* bias;  // [H][D] of the key map (Hedgehog) or null
   int* dev_status;
   uint64_t soft_ns, hard_ns;
@@ -227,40 +227,44 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
       constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);  // phiK^T[MN] ones[MN]
       auto g1 = [&](int i) {
         const uint32_t kb = sb + C::OFF_K + (i & 1) * C::XT;
+        // descriptor bases; a k-step only moves the start-address field (16-byte units)
+        const uint64_t dk = smem_desc(kb, 16, 1024, 2);
+        const uint64_t dw = smem_desc(sb + C::OFF_W, D * 128, 1024, 2);
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + C::TM_H, smem_desc(kb + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, 2),
-                 smem_desc(sb + C::OFF_W + ks * 2048, D * 128, 1024, 2), ID_H, ks > 0);
+          mma_ss(tmem + C::TM_H, dk + (ks / 4) * 1024 + (ks % 4) * 2, dw + ks * 128, ID_H, ks > 0);
         mma_commit(bar(SB_G1));
       };
       bool ok = true;
       if (HH) {
-        ok = mbar_wait(bar(SB_W), 0, wp) && mbar_wait(bar(SB_LDK), 0, wp);
+        ok = mbar_wait_poll(bar(SB_W), 0, wp) && mbar_wait_poll(bar(SB_LDK), 0, wp);
         tc_fence_after();
         if (ok) g1(0);
       }
       for (int i = 0; i < nt && ok; ++i) {
         if (HH && i + 1 < nt) {
           // H_K is free once every feature warp has read H_K(i)
-          ok = mbar_wait(bar(SB_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
-               mbar_wait(bar(SB_HREAD), i & 1, wp);
+          ok = mbar_wait_poll(bar(SB_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
+               mbar_wait_poll(bar(SB_HREAD), i & 1, wp);
           if (!ok) break;
           tc_fence_after();
           g1(i + 1);
         }
-        ok = mbar_wait(bar(SB_E1), i & 1, wp) &&
-             mbar_wait(bar(SB_LDV + (i % NV)), (i / NV) & 1, wp);
+        ok = mbar_wait_poll(bar(SB_E1), i & 1, wp) &&
+             mbar_wait_poll(bar(SB_LDV + (i % NV)), (i / NV) & 1, wp);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vb = sb + C::OFF_V + (i % NV) * C::XT;
+        const uint64_t dphk = smem_desc(sb + C::OFF_PHK, 16384, 1024, 2);
+        const uint64_t dv = HH ? smem_desc(vb, TILE * 128, 1024, 2) : smem_desc(vb, 16, 256, 6);
+        const uint64_t dones = smem_desc(sb + C::OFF_ONES, 16, 256, 6);
+#pragma unroll
         for (int mb = 0; mb < C::NMB; ++mb)
+#pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks) {
-            const uint64_t a =
-                smem_desc(sb + C::OFF_PHK + (2 * mb) * 16384 + ks * 2048, 16384, 1024, 2);
-            const uint64_t bv = HH ? smem_desc(vb + ks * 2048, TILE * 128, 1024, 2)
-                                   : smem_desc(vb + ks * 512, 16, 256, 6);
-            mma_ss(tmem + C::TM_S + mb * D, a, bv, ID_SU, 1);
-            mma_ss(tmem + C::TM_Z + 16 * mb, a,
-                   smem_desc(sb + C::OFF_ONES + ks * 512, 16, 256, 6), ID_Z, 1);
+            const uint64_t a = dphk + (2 * mb) * 1024 + ks * 128;
+            mma_ss(tmem + C::TM_S + mb * D, a, dv + ks * (HH ? 128 : 32), ID_SU, 1);
+            mma_ss(tmem + C::TM_Z + 16 * mb, a, dones + ks * 32, ID_Z, 1);
           }
         mma_commit(bar(SB_G2));
         // K stage i&1: G1(i) (Hedgehog) or the feature warps (Taylor) are done with it
@@ -365,11 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
         uint32_t sv[16];
         tmem_ld16(tmem + lane_base(warp) + C::TM_S + mb * D + c0, sv);
         if (f < C::DPP) {
-          float4* d4 = reinterpret_cast<float4*>(dst + (size_t)f * D + c0);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
-                                __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+            *reinterpret_cast<float4*>(dst + ws_s_index(f, c0 + 4 * q, D)) =
+                make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                            __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
         }
       }
       uint32_t zv[16];
@@ -484,48 +488,72 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
       constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 1);   // phiK^T[TMEM] V[MN-major]
       auto g1 = [&](int i) {
         const uint32_t kb = sb + OFF_K + (i & 1) * XT;
+        // descriptor bases; a k-step only moves the start-address field (16-byte units)
+        const uint64_t dw = smem_desc(sb + OFF_W, 16384, 1024, 2);
+        const uint64_t dk = smem_desc(kb, 16, 1024, 2);
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + TM_H(i & 1), smem_desc(sb + OFF_W + ks * 2048, 16384, 1024, 2),
-                 smem_desc(kb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2), ID_H, ks > 0);
+          mma_ss(tmem + TM_H(i & 1), dw + ks * 128, dk + (ks >> 2) * 1024 + (ks & 3) * 2, ID_H,
+                 ks > 0);
         mma_commit(bar(B_G1 + (i & 1)));
       };
-      bool ok = mbar_wait(bar(B_W), 0, wp) && mbar_wait(bar(B_LDK), 0, wp);
+      bool ok = mbar_wait_poll(bar(B_W), 0, wp) && mbar_wait_poll(bar(B_LDK), 0, wp);
       tc_fence_after();
       if (ok) g1(0);
       for (int i = 0; i < nt && ok; ++i) {
         if (i + 1 < nt) {
           // H buffer (i+1)&1 held phi(i-1), the A operand of G2(i-1)
-          ok = mbar_wait(bar(B_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
-               (i == 0 || mbar_wait(bar(B_G2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp));
+          ok = mbar_wait_poll(bar(B_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
+               (i == 0 || mbar_wait_poll(bar(B_G2 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp));
           if (!ok) break;
           tc_fence_after();
           g1(i + 1);
         }
-        ok = mbar_wait(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
-             mbar_wait(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
+        ok = mbar_wait_poll(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
+             mbar_wait_poll(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vb = sb + OFF_V + (i & 1) * XT;
+        const uint64_t dv = smem_desc(vb, 16384, 1024, 2);
+        const uint32_t th = tmem + TM_H(i & 1);
+#pragma unroll
         for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ts(tmem + TM_S + 128 * mb, tmem + TM_H(i & 1) + 64 * (ks >> 2) + 8 * (ks & 3) + 32 * mb,
-                   smem_desc(vb + ks * 2048, 16384, 1024, 2), ID_S, 1);
+            mma_ts(tmem + TM_S + 128 * mb, th + 64 * (ks >> 2) + 8 * (ks & 3) + 32 * mb,
+                   dv + ks * 128, ID_S, 1);
         mma_commit(bar(B_G2 + (i & 1)));
       }
       if (!ok) *(volatile int*)abort_flag = 1;
     }
   } else if (warp == 9) {
     // ======================= loader =======================
-    //   K(i+2) into stage i&1 once G1(i) has read K(i); V(i+2) once G2(i) has read V(i)
+    //   K(i) into stage i&1 once G1(i-2) has read K(i-2); V(i) once G2(i-2) has read V(i-2)
     if (lane == 0) {
-      bool ok = true;
-      for (int i = 0; i + 2 < nt && ok; ++i) {
-        ok = mbar_wait(bar(B_G1 + (i & 1)), (i >> 1) & 1, wp);
-        if (ok) load_k(i + 2);
-        ok = ok && mbar_wait(bar(B_G2 + (i & 1)), (i >> 1) & 1, wp);
-        if (ok) load_v(i + 2);
+      int nk = nt < 2 ? nt : 2, nv = nk;
+      uint64_t t_last = globaltimer();
+      bool reported = false;
+      while ((nk < nt || nv < nt) && !*(volatile int*)abort_flag) {
+        bool progress = false;
+        if (nk < nt && mbar_probe(bar(B_G1 + (nk & 1)), ((nk - 2) >> 1) & 1)) {
+          load_k(nk++);
+          progress = true;
+        }
+        if (nv < nt && mbar_probe(bar(B_G2 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
+          load_v(nv++);
+          progress = true;
+        }
+        if (progress) {
+          t_last = globaltimer();
+        } else {
+          const uint64_t dt = globaltimer() - t_last;
+          if (!reported && dt >= A.soft_ns) {
+            reported = true;
+            report_timeout(wp);
+          }
+          if (dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
+        }
       }
-      if (!ok) *(volatile int*)abort_flag = 1;
     }
   } else {
     // ======================= feature warps =======================
@@ -584,11 +612,11 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base(warp) + TM_S + 128 * c + c0, sv);
-      float4* d4 = reinterpret_cast<float4*>(dst + (size_t)f * D + c0);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
-                            __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+        *reinterpret_cast<float4*>(dst + ws_s_index(f, c0 + 4 * q, D)) =
+            make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                        __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
     }
     if (c == 0) {
       dst[(size_t)2 * D * D + j] = zp + zx[j];
@@ -697,33 +725,51 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
       constexpr uint32_t ID_S = idesc_bf16(128, 32, 1, 1);   // phiK^T[MN] [V e0][MN]
       bool ok = true;
       for (int i = 0; i < nt && ok; ++i) {
-        ok = mbar_wait(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
-             mbar_wait(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
+        ok = mbar_wait_poll(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
+             mbar_wait_poll(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
         if (!ok) break;
         tc_fence_after();
         const uint32_t pb = sb + OFF_PHK + (i & 1) * PHK_BYTES;
         const uint32_t vb = sb + OFF_V + (i & 1) * XT;
+        const uint64_t da = smem_desc(pb, 16384, 1024, 2);
+        const uint64_t dv = smem_desc(vb, OFF_E0 - (OFF_V + (i & 1) * XT), 256, 6);
+#pragma unroll
         for (int mb = 0; mb < 3; ++mb)
+#pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ss(tmem + TM_S + 32 * mb,
-                   smem_desc(pb + (2 * mb) * 16384 + ks * 2048, 16384, 1024, 2),
-                   smem_desc(vb + ks * 512, OFF_E0 - (OFF_V + (i & 1) * XT), 256, 6), ID_S, 1);
+            mma_ss(tmem + TM_S + 32 * mb, da + (2 * mb) * 1024 + ks * 128, dv + ks * 32, ID_S, 1);
         mma_commit(bar(B_G2 + (i & 1)));
       }
       if (!ok) *(volatile int*)abort_flag = 1;
     }
   } else if (warp == 9) {
     // ======================= loader =======================
-    //   K(i+2) once the feature warps have read K(i); V(i+2) once G2(i) has read V(i)
+    //   K(i) once the feature warps have read K(i-2); V(i) once G2(i-2) has read V(i-2)
     if (lane == 0) {
-      bool ok = true;
-      for (int i = 0; i + 2 < nt && ok; ++i) {
-        ok = mbar_wait(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp);
-        if (ok) load_k(i + 2);
-        ok = ok && mbar_wait(bar(B_G2 + (i & 1)), (i >> 1) & 1, wp);
-        if (ok) load_v(i + 2);
+      int nk = nt < 2 ? nt : 2, nv = nk;
+      uint64_t t_last = globaltimer();
+      bool reported = false;
+      while ((nk < nt || nv < nt) && !*(volatile int*)abort_flag) {
+        bool progress = false;
+        if (nk < nt && mbar_probe(bar(B_E1 + (nk & 1)), ((nk - 2) >> 1) & 1)) {
+          load_k(nk++);
+          progress = true;
+        }
+        if (nv < nt && mbar_probe(bar(B_G2 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
+          load_v(nv++);
+          progress = true;
+        }
+        if (progress) {
+          t_last = globaltimer();
+        } else {
+          const uint64_t dt = globaltimer() - t_last;
+          if (!reported && dt >= A.soft_ns) {
+            reported = true;
+            report_timeout(wp);
+          }
+          if (dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
+        }
       }
-      if (!ok) *(volatile int*)abort_flag = 1;
     }
   } else {
     // ======================= feature warps =======================
@@ -787,11 +833,11 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base(warp) + TM_S + 32 * mb, sv);
       if (f < DP) {
-        float4* d4 = reinterpret_cast<float4*>(dst + (size_t)f * 16);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          d4[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
-                              __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+          *reinterpret_cast<float4*>(dst + ws_s_index(f, 4 * q, 16)) =
+              make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                          __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
         dst[(size_t)DP * 16 + f] = __uint_as_float(sv[16]);
       }
     }
