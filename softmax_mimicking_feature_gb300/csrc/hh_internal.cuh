@@ -80,6 +80,13 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
                                    const void* k, const void* v, void* y, float* S_out,
                                    float* z_out, const void* ws, int* dev_status, cudaStream_t s);
 
+// Output pass of the Taylor (d = 16) prefill: scores from the closed form
+// 1 + s + s^2/2 with s = q . k, state contractions on the features.
+cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const void* q,
+                                      const void* k, const void* v, void* y, float* S_out,
+                                      float* z_out, const void* ws, int* dev_status,
+                                      cudaStream_t s);
+
 // Tensor-core (tcgen05) feature map and mimicry loss for bf16 Hedgehog d in {64, 128}.
 bool fmap_tc_supported(const Problem& p);
 cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,

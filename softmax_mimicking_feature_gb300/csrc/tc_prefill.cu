@@ -867,6 +867,8 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   }
   if (KIND == HH_FMAP_HEDGEHOG && D == 64 && !p.Wk)
     return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
+  if (KIND == HH_FMAP_TAYLOR2)
+    return launch_prefill_out_taylor(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
   auto kern = prefill_tc_kernel<KIND, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,539 @@
+// Chunked causal prefill, output pass, for the degree-2 Taylor map (d = 16).
+//
+// "The Taylor Exponential as a Bridge Result" (Hedgehog & Porcupine summary)
+// gives phi(x) = [1, x, vec(x x^T) / sqrt2], so phi(q) . phi(k) = 1 + s + s^2/2
+// with s = q . k.  The intra-tile scores therefore need one K = 16 MMA of
+// Q K^T and two FMAs per element instead of a 288-deep feature contraction;
+// the running state (section 2, paper Eq. 2; "Complexity Analysis") still
+// needs the features:
+//   Sc(t) = Q_t K_t^T                         -> P = bf16(tril(1 + Sc + Sc^2/2))
+//   [S z] += phi(K_t)^T [V_t e0]             (N = 32, z rides in column 16)
+//   [O den] = P [V_t e0] + phi(Q_t) [S_bf16 z2]   (z2 = z as a bf16 hi/lo pair)
+//   y = O / (den_hi + den_lo)
+// Roles: warp 8 issues every tcgen05.mma as soon as its inputs are ready,
+// warp 9 issues TMA loads, warps 0-7 run the epilogue phases
+//   E1(t): phi(Q_t) -> TMEM (two buffers), phi(K_t) -> smem, S_bf16/z2 snapshot
+//   E2(t): P from Sc(t);   E3(t): y from [O den]
+// in the order E1(0), then E2(t), E1(t+1), E3(t) per step.  Every mbarrier
+// wait is bounded in time (tc_ptx.cuh).
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "tc_ptx.cuh"
+
+namespace hh {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 16, DP = 288, TILE = 128;
+constexpr int kThreads = 320;
+constexpr uint32_t XT = TILE * D * 2;                   // one Q, K or V tile: 4 KB
+// shared memory (1024-aligned base); Q, K, V tiles are 32B-swizzled rows
+constexpr uint32_t OFF_Q = 0, OFF_K = 8192, OFF_V = 16384;   // 2 stages each
+constexpr uint32_t OFF_E0 = 24576;                      // [128 x 16], column 0 = 1
+constexpr uint32_t SB_BYTES = DP * 32;                  // [288 x 16] bf16, 32B-swizzled
+constexpr uint32_t OFF_SB = 28672;                      // 2 x (S_bf16 | z2)
+constexpr uint32_t OFF_PHK = 65536;                     // phi(K): 6 panels [128 tok x 64 feat]
+constexpr uint32_t OFF_P = OFF_PHK + 6 * 16384;         // P: 2 panels [128 rows x 64 keys]
+constexpr uint32_t OFF_BAR = OFF_P + 2 * 16384;
+enum { B_LD = 0, B_SC = 2, B_SU = 4, B_G3 = 6, B_E1 = 8, B_E2 = 10, B_E3 = 12, B_COUNT = 14 };
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_SB + 4 * SB_BYTES <= OFF_PHK, "S_bf16 buffers");
+// TMEM columns
+constexpr uint32_t TM_S = 0;                            // 3 blocks x [S (16) | z, 0.. (16)]
+__host__ __device__ constexpr uint32_t TM_Y(int b) { return 96 + 144 * b; }   // phi(Q) pairs
+constexpr uint32_t TM_X = 384;                          // Sc (128) -> [O den] (32)
+
+struct ArgsT {
+  CUtensorMap tq, tk, tv;
+  __nv_bfloat16* y;
+  const float* ws;   // [U][P-1][DP*D + DP] inclusive prefixes (ws_s_index layout, then z)
+  float* S_out;      // [U][DP][D] or null
+  float* z_out;      // [U][DP]
+  int* dev_status;
+  uint64_t soft_ns, hard_ns;
+  int64_t n;
+  int P, L, NT;
+};
+
+__device__ __forceinline__ uint32_t lane_base(int warp) {
+  return (uint32_t)(32 * (warp & 3)) << 16;
+}
+
+// Row r (16 bf16) of a 32B-swizzled [128 x 16] tile as floats.
+__device__ __forceinline__ void load_row16(const uint8_t* tile, int r, float (&x)[16]) {
+  const int sw = ((r >> 2) & 1) << 4;
+  const uint4 a = *reinterpret_cast<const uint4*>(tile + r * 32 + sw);
+  const uint4 b = *reinterpret_cast<const uint4*>(tile + r * 32 + (16 - sw));
+  x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+  x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+  x[8] = bf16_lo(b.x); x[9] = bf16_hi(b.x); x[10] = bf16_lo(b.y); x[11] = bf16_hi(b.y);
+  x[12] = bf16_lo(b.z); x[13] = bf16_hi(b.z); x[14] = bf16_lo(b.w); x[15] = bf16_hi(b.w);
+}
+
+// Feature f of [1, x, x_i x_j / sqrt2 (i-major)]; zero past 272.
+__device__ __forceinline__ float tfeat(int f, const float (&x)[16]) {
+  if (f == 0) return 1.f;
+  if (f <= 16) return x[f - 1];
+  if (f <= 272) return x[(f - 17) >> 4] * x[(f - 17) & 15] * kInvSqrt2;
+  return 0.f;
+}
+
+// 32 features from FB as 16 bf16 pairs.
+template <int FB>
+__device__ __forceinline__ void tpack(const float (&x)[16], bool valid, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    w[j] = valid ? pack_bf16(tfeat(FB + 2 * j, x), tfeat(FB + 2 * j + 1, x)) : 0u;
+}
+
+template <int FB>
+__device__ __forceinline__ void phiq_chunk(const float (&x)[16], uint32_t ty) {
+  uint32_t w[16];
+  tpack<FB>(x, true, w);
+  tmem_st16(ty + FB / 2, w);
+}
+
+template <int FB>
+__device__ __forceinline__ void phik_chunk(const float (&x)[16], bool valid, uint32_t phk, int row) {
+  uint32_t w[16];
+  tpack<FB>(x, valid, w);
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4)
+    st_shared_v4(phk + (FB / 64) * 16384 + sw128_chunk(row, (FB % 64) / 8 + q4), w[4 * q4],
+                 w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+}
+
+// The bound of 384 threads caps registers at 168 per thread (warps 0, 4, 8 and
+// 1, 5, 9 share one SM sub-partition's registers).
+__global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constant__ ArgsT A) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const uint32_t bars = sb + OFF_BAR;
+  auto bar = [&](int b) { return bars + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t unit = blockIdx.x / A.P;
+  const int seg = blockIdx.x % A.P;
+  const int t_begin = seg * A.L;
+  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
+
+  if (tid == 0) {
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(bar(b), b >= B_E1 ? 8 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&A.tq);
+    prefetch_tmap(&A.tk);
+    prefetch_tmap(&A.tv);
+  }
+  __syncthreads();
+  auto load = [&](int i) {
+    const int s = i & 1;
+    const int r0 = (t_begin + i) * TILE;
+    mbar_expect_tx(bar(B_LD + s), 3 * XT);
+    tma_load_3d(sb + OFF_Q + s * XT, &A.tq, bar(B_LD + s), 0, r0, (int)unit);
+    tma_load_3d(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, (int)unit);
+    tma_load_3d(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, (int)unit);
+  };
+  if (warp == 8 && lane == 0)
+    for (int i = 0; i < 2 && i < nt; ++i) load(i);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  // e0 rows (1, 0, ..., 0); z2 buffers zero (only column pair 0-1 is rewritten);
+  // phi(K) panels zero (features 288..383 stay zero)
+  for (int r = tid; r < 128; r += kThreads) {
+    const uint32_t c0 = ((r >> 2) & 1) << 4;
+    st_shared_v4(sb + OFF_E0 + r * 32 + c0, 0x3F80u, 0u, 0u, 0u);
+    st_shared_v4(sb + OFF_E0 + r * 32 + (16 - c0), 0u, 0u, 0u, 0u);
+  }
+  for (uint32_t i = tid * 16; i < 2 * SB_BYTES; i += kThreads * 16) {
+    const uint32_t b = i / SB_BYTES, o = i % SB_BYTES;
+    st_shared_v4(sb + OFF_SB + b * 2 * SB_BYTES + SB_BYTES + o, 0u, 0u, 0u, 0u);
+  }
+  for (uint32_t i = tid * 16; i < 6 * 16384u; i += kThreads * 16)
+    st_shared_v4(sb + OFF_PHK + i, 0u, 0u, 0u, 0u);
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // initial [S z]: zeros, or the prefix of the preceding segments
+  if (warp < 8) {
+    const int c = warp >> 2;
+    const float* prefix =
+        seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * (size_t)(DP * D + DP) : nullptr;
+    for (int mb = c; mb < 3; mb += 2) {
+      const int f = 128 * mb + 32 * (warp & 3) + lane;
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+      if (prefix && f < DP) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v4 = __ldcg(reinterpret_cast<const float4*>(prefix + ws_s_index(f, 4 * q, D)));
+          r[4 * q] = __float_as_uint(v4.x);
+          r[4 * q + 1] = __float_as_uint(v4.y);
+          r[4 * q + 2] = __float_as_uint(v4.z);
+          r[4 * q + 3] = __float_as_uint(v4.w);
+        }
+        r[16] = __float_as_uint(__ldcg(prefix + (size_t)DP * D + f));
+      }
+      tmem_st32(tmem + lane_base(warp) + TM_S + 32 * mb, r);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 8) {
+    // ======================= MMA issuer =======================
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t ID_SC = idesc_bf16(128, 128, 0, 0);   // Q[K-major] K[K-major]
+      constexpr uint32_t ID_SU = idesc_bf16(128, 32, 1, 1);    // phiK^T[MN] [V e0][MN]
+      constexpr uint32_t ID_O = idesc_bf16(128, 32, 0, 1);     // P or phiQ x [V e0] or [S z2]
+      // descriptor bases; a k-step only moves the start-address field (16-byte units)
+      const uint64_t dphk = smem_desc(sb + OFF_PHK, 16384, 1024, 2);
+      const uint64_t dp = smem_desc(sb + OFF_P, 16, 1024, 2);
+      auto dv = [&](int s) {   // [V e0]: the e0 block one leading-byte offset after V
+        return smem_desc(sb + OFF_V + s * XT, OFF_E0 - (OFF_V + s * XT), 256, 6);
+      };
+      auto Sc = [&](int i) {
+        const int s = i & 1;
+        tc_fence_after();
+        mma_ss(tmem + TM_X, smem_desc(sb + OFF_Q + s * XT, 16, 256, 6),
+               smem_desc(sb + OFF_K + s * XT, 16, 256, 6), ID_SC, 0);
+        mma_commit(bar(B_SC + s));
+      };
+      auto SU = [&](int i) {
+        const int s = i & 1;
+        const uint64_t v = dv(s);
+        tc_fence_after();
+#pragma unroll
+        for (int mb = 0; mb < 3; ++mb)
+#pragma unroll
+          for (int ks = 0; ks < TILE / 16; ++ks)
+            mma_ss(tmem + TM_S + 32 * mb, dphk + (2 * mb) * 1024 + ks * 128, v + ks * 32, ID_SU, 1);
+        mma_commit(bar(B_SU + s));
+      };
+      auto G3 = [&](int i) {
+        const int s = i & 1;
+        const uint64_t v = dv(s);
+        const uint64_t dsb = smem_desc(sb + OFF_SB + s * 2 * SB_BYTES, SB_BYTES, 256, 6);
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < TILE / 16; ++ks)
+          mma_ss(tmem + TM_X, dp + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32, ID_O, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < DP / 16; ++ks)
+          mma_ts(tmem + TM_X, tmem + TM_Y(s) + ks * 8, dsb + ks * 32, ID_O, 1);
+        mma_commit(bar(B_G3 + s));
+      };
+      // Per tile the MMAs go in the order Sc, SU, G3:
+      //   Sc(i)  needs Q, K landed and E3(i-1) done (the X columns free)
+      //   SU(i)  needs Sc(i) issued and E1(i) done (phi(K) written)
+      //   G3(i)  needs SU(i) issued and E2(i) done (P written; E1(i) came before E2(i))
+      int na = 0, nb = 0, n3 = 0;
+      uint64_t t_last = globaltimer();
+      bool reported = false, ok = true;
+      while (ok && n3 < nt) {
+        bool progress = false;
+        if (n3 < nb && mbar_probe(bar(B_E2 + (n3 & 1)), (n3 >> 1) & 1)) {
+          G3(n3++);
+          progress = true;
+        } else if (na < nt && mbar_probe(bar(B_LD + (na & 1)), (na >> 1) & 1) &&
+                   (na == 0 || mbar_probe(bar(B_E3 + ((na - 1) & 1)), ((na - 1) >> 1) & 1))) {
+          Sc(na++);
+          progress = true;
+        } else if (nb < na && mbar_probe(bar(B_E1 + (nb & 1)), (nb >> 1) & 1)) {
+          SU(nb++);
+          progress = true;
+        }
+        if (progress) {
+          t_last = globaltimer();
+        } else {
+          const uint64_t dt = globaltimer() - t_last;
+          if (!reported && dt >= A.soft_ns) {
+            reported = true;
+            report_timeout(wp);
+          }
+          if (dt >= A.hard_ns) {
+            *(volatile int*)abort_flag = 1;
+            ok = false;
+          }
+          if (*(volatile int*)abort_flag) ok = false;
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ======================= loader =======================
+    // Q, K, V of tile i into stage i&1 once G3(i-2) has completed: every MMA
+    // and epilogue read of tile i-2 precedes it.
+    if (lane == 0) {
+      for (int i = 2; i < nt; ++i) {
+        if (!mbar_wait_poll(bar(B_G3 + (i & 1)), ((i - 2) >> 1) & 1, wp)) break;
+        load(i);
+      }
+    }
+  } else {
+    // ======================= epilogue warps =======================
+    // warp w: TMEM lanes / tile rows 32 (w % 4).., half c = w / 4 of the columns
+    const int c = warp >> 2;
+    const int g = warp & 3;
+    const int row = 32 * g + lane;
+    const uint32_t lb = lane_base(warp);
+    bool good = true;
+
+    auto E1 = [&](int i) {
+      const int s = i & 1;
+      const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_LD + s), (i >> 1) & 1, wp))) { good = false; return; }
+      // phi(Q): half 0 features [0, 160), half 1 [160, 288) -> packed TMEM columns
+      {
+        float x[16];
+        load_row16(sm + OFF_Q + s * XT, row, x);
+        const uint32_t ty = tmem + lb + TM_Y(s);
+        if (c == 0) {
+          phiq_chunk<0>(x, ty);
+          phiq_chunk<32>(x, ty);
+          phiq_chunk<64>(x, ty);
+          phiq_chunk<96>(x, ty);
+          phiq_chunk<128>(x, ty);
+        } else {
+          phiq_chunk<160>(x, ty);
+          phiq_chunk<192>(x, ty);
+          phiq_chunk<224>(x, ty);
+          phiq_chunk<256>(x, ty);
+        }
+      }
+      // phi(K) and the state snapshot need SU(i-1) done (it read phi(K(i-1)), updated S)
+      if (i > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SU + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp))) {
+          good = false;
+          return;
+        }
+        tc_fence_after();
+      }
+      {
+        float x[16];
+        load_row16(sm + OFF_K + s * XT, row, x);
+        const uint32_t phk = sb + OFF_PHK;
+        if (c == 0) {
+          phik_chunk<0>(x, valid, phk, row);
+          phik_chunk<32>(x, valid, phk, row);
+          phik_chunk<64>(x, valid, phk, row);
+          phik_chunk<96>(x, valid, phk, row);
+          phik_chunk<128>(x, valid, phk, row);
+        } else {
+          phik_chunk<160>(x, valid, phk, row);
+          phik_chunk<192>(x, valid, phk, row);
+          phik_chunk<224>(x, valid, phk, row);
+          phik_chunk<256>(x, valid, phk, row);
+        }
+      }
+      // S_bf16 and z2 (z as z_hi + z_lo) of the tokens before this tile
+      const uint32_t sbb = sb + OFF_SB + s * 2 * SB_BYTES;
+      for (int mb = c; mb < 3; mb += 2) {
+        const int f = 128 * mb + row;
+        uint32_t sv[32];
+        tmem_ld32(tmem + lb + TM_S + 32 * mb, sv);
+        if (f < DP) {
+          const uint32_t sw = ((f >> 2) & 1) << 4;
+          st_shared_v4(sbb + f * 32 + sw,
+                       pack_bf16(__uint_as_float(sv[0]), __uint_as_float(sv[1])),
+                       pack_bf16(__uint_as_float(sv[2]), __uint_as_float(sv[3])),
+                       pack_bf16(__uint_as_float(sv[4]), __uint_as_float(sv[5])),
+                       pack_bf16(__uint_as_float(sv[6]), __uint_as_float(sv[7])));
+          st_shared_v4(sbb + f * 32 + (16 - sw),
+                       pack_bf16(__uint_as_float(sv[8]), __uint_as_float(sv[9])),
+                       pack_bf16(__uint_as_float(sv[10]), __uint_as_float(sv[11])),
+                       pack_bf16(__uint_as_float(sv[12]), __uint_as_float(sv[13])),
+                       pack_bf16(__uint_as_float(sv[14]), __uint_as_float(sv[15])));
+          const float z = __uint_as_float(sv[16]);
+          const float zl = z - __bfloat162float(__float2bfloat16_rn(z));
+          st_shared_v4(sbb + SB_BYTES + f * 32 + sw, pack_bf16(z, zl), 0u, 0u, 0u);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_E1 + s));
+    };
+
+    auto E2 = [&](int i) {
+      const int s = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SC + s), (i >> 1) & 1, wp))) { good = false; return; }
+      tc_fence_after();
+      // keys [64c + 32 h2, +32) = block kc of 32 keys: above the diagonal (kc > g)
+      // zero, below it no mask; p = 1 + s + s^2/2 = phi(q) . phi(k)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int kc = 2 * c + h2;
+        const uint32_t panel = sb + OFF_P + c * 16384;
+        if (kc > g) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_shared_v4(panel + sw128_chunk(row, 4 * h2 + q4), 0u, 0u, 0u, 0u);
+        } else {
+          uint32_t sv[32];
+          tmem_ld32(tmem + lb + TM_X + 32 * kc, sv);
+          const bool diag = kc == g;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = 8 * q4 + 2 * e;   // within this 32-key block
+              const float s0 = __uint_as_float(sv[key]), s1 = __uint_as_float(sv[key + 1]);
+              float p0 = fmaf(s0, fmaf(s0, 0.5f, 1.f), 1.f);
+              float p1 = fmaf(s1, fmaf(s1, 0.5f, 1.f), 1.f);
+              if (diag) {
+                p0 = key <= lane ? p0 : 0.f;
+                p1 = key + 1 <= lane ? p1 : 0.f;
+              }
+              w4[e] = pack_bf16(p0, p1);
+            }
+            st_shared_v4(panel + sw128_chunk(row, 4 * h2 + q4), w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_E2 + s));
+    };
+
+    auto E3 = [&](int i) {
+      const int s = i & 1;
+      const int64_t r0 = (int64_t)(t_begin + i) * TILE;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G3 + s), (i >> 1) & 1, wp))) { good = false; return; }
+      tc_fence_after();
+      uint32_t ov[16], d0, d1;
+      tmem_ld16(tmem + lb + TM_X, ov);
+      tmem_ld2(tmem + lb + TM_X + 16, d0, d1);   // rowsum(P) + phi(q).z_hi, phi(q).z_lo
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_E3 + s));   // the X columns are free for Sc(i+1)
+      const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
+      if (r0 + row < A.n) {
+        const int j = 8 * c;
+        *reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D + j) = make_uint4(
+            pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
+            pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
+            pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
+            pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
+      }
+    };
+
+    if (nt > 0) E1(0);
+    for (int i = 0; i < nt && good; ++i) {
+      E2(i);
+      if (good && i + 1 < nt) E1(i + 1);
+      if (good) E3(i);
+    }
+  }
+
+  // ---- export the final state of the last segment ----
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (A.S_out && seg == A.P - 1 && warp < 8 && !*(volatile int*)abort_flag) {
+    // the last SU completed before the last G3 (issue order), which E3 waited for
+    const int c = warp >> 2;
+    for (int mb = c; mb < 3; mb += 2) {
+      const int f = 128 * mb + 32 * (warp & 3) + lane;
+      uint32_t sv[32];
+      tmem_ld32(tmem + lane_base(warp) + TM_S + 32 * mb, sv);
+      if (f < DP) {
+        float4* dst = reinterpret_cast<float4*>(A.S_out + ((size_t)unit * DP + f) * D);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
+                               __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+        A.z_out[(size_t)unit * DP + f] = __uint_as_float(sv[16]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// [planes][rows][16] bf16 with a {16, 128, 1} box and the 32-byte swizzle
+bool make_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes) {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  if (!fn) return false;
+  cuuint64_t dims[3] = {16, rows, planes};
+  cuuint64_t strides[2] = {32, 32 * rows};
+  cuuint32_t box[3] = {16, TILE, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Output pass of the Taylor (d = 16) prefill: U * P CTAs, one per segment.
+cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const void* q,
+                                      const void* k, const void* v, void* y, float* S_out,
+                                      float* z_out, const void* ws, int* dev_status,
+                                      cudaStream_t s) {
+  ArgsT a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t U = (uint64_t)p.B * p.H;
+  if (p.kind != HH_FMAP_TAYLOR2 || p.d != 16) return cudaErrorInvalidValue;
+  bool ok = make_map16(&a.tq, q, p.n, U) && make_map16(&a.tk, k, p.n, U) &&
+            make_map16(&a.tv, v, p.n, U);
+  if (!ok) return cudaErrorInvalidValue;
+  a.y = reinterpret_cast<__nv_bfloat16*>(y);
+  a.ws = reinterpret_cast<const float*>(ws);
+  a.S_out = S_out;
+  a.z_out = z_out;
+  a.dev_status = dev_status;
+  a.soft_ns = wait_soft_limit_ns();
+  a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+  a.n = p.n;
+  a.P = pl.P;
+  a.L = pl.L;
+  a.NT = pl.NT;
+  cudaError_t e = cudaFuncSetAttribute(taylor_out_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  taylor_out_kernel<<<(unsigned)(U * pl.P), kThreads, SMEM_BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace hh
