@@ -214,8 +214,8 @@ struct LossCfg {
   // scalars
   static constexpr uint32_t OFF_ST = OFF_END;              // float[4][128]: m, Z, T, Asum (half 1)
   static constexpr uint32_t OFF_RL = OFF_ST + 4 * 128 * 4; // float[128] row losses
-  static constexpr uint32_t OFF_BAR = OFF_RL + 128 * 4;    // 8 x u64
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * 8;
+  static constexpr uint32_t OFF_BAR = OFF_RL + 128 * 4;    // 9 x u64
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 9 * 8;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
 };
 
@@ -231,10 +231,12 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   float* st_s = reinterpret_cast<float*>(sm + C::OFF_ST);
   float* rl_s = reinterpret_cast<float*>(sm + C::OFF_RL);
   const uint32_t bar_q = sb + C::OFF_BAR;        // Q, phi(Q) loaded
-  const uint32_t bar_kv = bar_q + 8;             // K_j, phi(K_j) loaded
+  const uint32_t bar_k = bar_q + 8;              // K_j loaded
   const uint32_t bar_mma0 = bar_q + 16;          // stage 0 MMAs done (2 barriers)
   const uint32_t bar_free0 = bar_q + 32;         // stage 0 drained by the epilogue (2 barriers)
-  const uint32_t bar_smem = bar_q + 48;          // smem K/phiK no longer read by MMAs
+  const uint32_t bar_pk = bar_q + 48;            // phi(K_j) loaded
+  const uint32_t bar_kread = bar_q + 56;         // the Q K_j^T MMAs have read K_j
+  const uint32_t bar_pkread = bar_q + 64;        // the phi(Q) phi(K_j)^T MMAs have read phi(K_j)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
 
@@ -248,12 +250,14 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(bar_kv, 1);
+    mbar_init(bar_k, 1);
     mbar_init(bar_mma0, 1);
     mbar_init(bar_mma0 + 8, 1);
     mbar_init(bar_free0, 8);
     mbar_init(bar_free0 + 8, 8);
-    mbar_init(bar_smem, 1);
+    mbar_init(bar_pk, 1);
+    mbar_init(bar_kread, 1);
+    mbar_init(bar_pkread, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -271,43 +275,58 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   if (warp == 8) {
     // ---------------- producer: TMA + MMA issue ----------------
     if (lane == 0) {
-      auto load_kv = [&](int j) {
-        mbar_expect_tx(bar_kv, C::Q_BYTES + C::PQ_BYTES);
+      // K_j and phi(K_j) arrive on separate barriers: the next K is fetched as
+      // soon as the Q K^T MMAs have read the current one, under the phi MMAs.
+      auto load_k = [&](int j) {
+        mbar_expect_tx(bar_k, C::Q_BYTES);
         for (int i = 0; i < D / 64; ++i)
-          tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_kv, 64 * i, j * kTile, (int)unit);
+          tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, (int)unit);
+      };
+      auto load_pk = [&](int j) {
+        mbar_expect_tx(bar_pk, C::PQ_BYTES);
         for (int i = 0; i < C::DP / 64; ++i)
-          tma_load_3d(sb + C::OFF_PK + i * 16384, &A.tpk, bar_kv, 64 * i, j * kTile, (int)unit);
+          tma_load_3d(sb + C::OFF_PK + i * 16384, &A.tpk, bar_pk, 64 * i, j * kTile, (int)unit);
       };
       mbar_expect_tx(bar_q, C::Q_BYTES + C::PQ_BYTES);
       for (int i = 0; i < D / 64; ++i)
         tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, (int)unit);
       for (int i = 0; i < C::DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PQ + i * 16384, &A.tpq, bar_q, 64 * i, (int)q0, (int)unit);
-      load_kv(0);
-      bool ok = mbar_wait(bar_q, 0, wp);
+      load_k(0);
+      load_pk(0);
+      bool ok = mbar_wait_poll(bar_q, 0, wp);
       constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
+      // descriptor bases (K-major, 128B-swizzled 64-element panels); a k-step
+      // only moves the start-address field (16-byte units)
+      const uint64_t dq = smem_desc(sb + C::OFF_Q, 16, 1024, 2);
+      const uint64_t dk = smem_desc(sb + C::OFF_K, 16, 1024, 2);
+      const uint64_t dpq = smem_desc(sb + C::OFF_PQ, 16, 1024, 2);
+      const uint64_t dpk = smem_desc(sb + C::OFF_PK, 16, 1024, 2);
+      auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
       for (int j = 0; j < nkt && ok; ++j) {
         const int stg = j & 1;
-        ok = mbar_wait(bar_kv, j & 1, wp);                              // K_j landed
-        if (ok && j >= 2) ok = mbar_wait(bar_free0 + 8 * stg, ((j >> 1) - 1) & 1, wp);
+        ok = mbar_wait_poll(bar_k, j & 1, wp);                           // K_j landed
+        if (ok && j >= 2) ok = mbar_wait_poll(bar_free0 + 8 * stg, ((j >> 1) - 1) & 1, wp);
         if (!ok) break;
         tc_fence_after();
         const uint32_t ts = tmem + stg * 256;
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
-          mma_ss(ts, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2),
-                 smem_desc(sb + C::OFF_K + koff, 16, 1024, 2), IDESC, ks > 0);
-        }
-        for (int ks = 0; ks < C::DP / 16; ++ks) {
-          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
-          mma_ss(ts + 128, smem_desc(sb + C::OFF_PQ + koff, 16, 1024, 2),
-                 smem_desc(sb + C::OFF_PK + koff, 16, 1024, 2), IDESC, ks > 0);
-        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(ts, dq + kmaj(ks), dk + kmaj(ks), IDESC, ks > 0);
+        mma_commit(bar_kread);
+        ok = mbar_wait_poll(bar_pk, j & 1, wp);                          // phi(K_j) landed
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < C::DP / 16; ++ks)
+          mma_ss(ts + 128, dpq + kmaj(ks), dpk + kmaj(ks), IDESC, ks > 0);
         mma_commit(bar_mma0 + 8 * stg);
-        mma_commit(bar_smem);
+        mma_commit(bar_pkread);
         if (j + 1 < nkt) {
-          ok = mbar_wait(bar_smem, j & 1, wp);                          // MMAs read smem
-          if (ok) load_kv(j + 1);
+          ok = mbar_wait_poll(bar_kread, j & 1, wp);
+          if (ok) load_k(j + 1);
+          ok = ok && mbar_wait_poll(bar_pkread, j & 1, wp);
+          if (ok) load_pk(j + 1);
         }
       }
       if (!ok) failed = true;

@@ -203,46 +203,64 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
 
   if (warp == 8) {
     // ======================= MMA issuer =======================
-    if (lane == 0 && nt > 0) {
+    // The whole warp runs the issue loop (warp-uniform control flow and
+    // descriptors); lane 0 alone executes the tcgen05 instructions.
+    if (nt > 0) {
       constexpr uint32_t ID_SC = idesc_bf16(128, 128, 0, 0);   // Q[K-major] K[K-major]
       constexpr uint32_t ID_SU = idesc_bf16(128, 32, 1, 1);    // phiK^T[MN] [V e0][MN]
       constexpr uint32_t ID_O = idesc_bf16(128, 32, 0, 1);     // P or phiQ x [V e0] or [S z2]
+      const bool leader = lane == 0;
       // descriptor bases; a k-step only moves the start-address field (16-byte units)
       const uint64_t dphk = smem_desc(sb + OFF_PHK, 16384, 1024, 2);
       const uint64_t dp = smem_desc(sb + OFF_P, 16, 1024, 2);
       auto dv = [&](int s) {   // [V e0]: the e0 block one leading-byte offset after V
         return smem_desc(sb + OFF_V + s * XT, OFF_E0 - (OFF_V + s * XT), 256, 6);
       };
+      auto probe = [&](int b, uint32_t parity) {   // lane 0's view, broadcast
+        return __shfl_sync(0xffffffffu, (int)mbar_probe(bar(b), parity), 0) != 0;
+      };
       auto Sc = [&](int i) {
         const int s = i & 1;
+        const uint64_t da = smem_desc(sb + OFF_Q + s * XT, 16, 256, 6);
+        const uint64_t db = smem_desc(sb + OFF_K + s * XT, 16, 256, 6);
         tc_fence_after();
-        mma_ss(tmem + TM_X, smem_desc(sb + OFF_Q + s * XT, 16, 256, 6),
-               smem_desc(sb + OFF_K + s * XT, 16, 256, 6), ID_SC, 0);
-        mma_commit(bar(B_SC + s));
+        if (leader) {
+          mma_ss(tmem + TM_X, da, db, ID_SC, 0);
+          mma_commit(bar(B_SC + s));
+        }
+        __syncwarp();
       };
       auto SU = [&](int i) {
         const int s = i & 1;
         const uint64_t v = dv(s);
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int mb = 0; mb < 3; ++mb)
+          for (int mb = 0; mb < 3; ++mb)
 #pragma unroll
-          for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ss(tmem + TM_S + 32 * mb, dphk + (2 * mb) * 1024 + ks * 128, v + ks * 32, ID_SU, 1);
-        mma_commit(bar(B_SU + s));
+            for (int ks = 0; ks < TILE / 16; ++ks)
+              mma_ss(tmem + TM_S + 32 * mb, dphk + (2 * mb) * 1024 + ks * 128, v + ks * 32, ID_SU,
+                     1);
+          mma_commit(bar(B_SU + s));
+        }
+        __syncwarp();
       };
       auto G3 = [&](int i) {
         const int s = i & 1;
         const uint64_t v = dv(s);
         const uint64_t dsb = smem_desc(sb + OFF_SB + s * 2 * SB_BYTES, SB_BYTES, 256, 6);
+        const uint32_t ty = tmem + TM_Y(s);
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int ks = 0; ks < TILE / 16; ++ks)
-          mma_ss(tmem + TM_X, dp + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32, ID_O, ks > 0);
+          for (int ks = 0; ks < TILE / 16; ++ks)
+            mma_ss(tmem + TM_X, dp + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32, ID_O, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < DP / 16; ++ks)
-          mma_ts(tmem + TM_X, tmem + TM_Y(s) + ks * 8, dsb + ks * 32, ID_O, 1);
-        mma_commit(bar(B_G3 + s));
+          for (int ks = 0; ks < DP / 16; ++ks)
+            mma_ts(tmem + TM_X, ty + ks * 8, dsb + ks * 32, ID_O, 1);
+          mma_commit(bar(B_G3 + s));
+        }
+        __syncwarp();
       };
       // Per tile the MMAs go in the order Sc, SU, G3:
       //   Sc(i)  needs Q, K landed and E3(i-1) done (the X columns free)
@@ -253,14 +271,14 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       bool reported = false, ok = true;
       while (ok && n3 < nt) {
         bool progress = false;
-        if (n3 < nb && mbar_probe(bar(B_E2 + (n3 & 1)), (n3 >> 1) & 1)) {
+        if (n3 < nb && probe(B_E2 + (n3 & 1), (n3 >> 1) & 1)) {
           G3(n3++);
           progress = true;
-        } else if (na < nt && mbar_probe(bar(B_LD + (na & 1)), (na >> 1) & 1) &&
-                   (na == 0 || mbar_probe(bar(B_E3 + ((na - 1) & 1)), ((na - 1) >> 1) & 1))) {
+        } else if (na < nt && probe(B_LD + (na & 1), (na >> 1) & 1) &&
+                   (na == 0 || probe(B_E3 + ((na - 1) & 1), ((na - 1) >> 1) & 1))) {
           Sc(na++);
           progress = true;
-        } else if (nb < na && mbar_probe(bar(B_E1 + (nb & 1)), (nb >> 1) & 1)) {
+        } else if (nb < na && probe(B_E1 + (nb & 1), (nb >> 1) & 1)) {
           SU(nb++);
           progress = true;
         }
@@ -268,15 +286,11 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
           t_last = globaltimer();
         } else {
           const uint64_t dt = globaltimer() - t_last;
-          if (!reported && dt >= A.soft_ns) {
-            reported = true;
-            report_timeout(wp);
-          }
-          if (dt >= A.hard_ns) {
-            *(volatile int*)abort_flag = 1;
-            ok = false;
-          }
-          if (*(volatile int*)abort_flag) ok = false;
+          if (leader && !reported && dt >= A.soft_ns) report_timeout(wp);
+          if (dt >= A.soft_ns) reported = true;
+          if (leader && dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
+          __syncwarp();
+          ok = __shfl_sync(0xffffffffu, (int)!*(volatile int*)abort_flag, 0) != 0;
         }
       }
     }
