@@ -66,6 +66,11 @@ struct TcPlan {
   size_t ws_bytes = 0;
 };
 TcPlan plan_prefill_tc(const Problem& p);
+// Floats of one segment state in the prefill workspace: S then z.  The Taylor
+// kernels keep 160 packed features (taylor_pack.cuh) instead of 288.
+inline int64_t ws_segment_floats(const Problem& p) {
+  return p.kind == HH_FMAP_TAYLOR2 ? (int64_t)160 * 16 + 160 : (int64_t)p.dpp * p.d + p.dpp;
+}
 cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q, const void* k,
                               const void* v, void* y, float* S_out, float* z_out, void* ws,
                               int* dev_status, cudaStream_t s);

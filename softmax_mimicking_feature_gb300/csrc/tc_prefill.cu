@@ -813,7 +813,7 @@ TcPlan plan_prefill_tc(const Problem& p) {
   pl.L = pl.NT > 0 ? ceil_div(pl.NT, P) : 1;
   pl.P = pl.NT > 0 ? ceil_div(pl.NT, pl.L) : 1;
   pl.launches = pl.P > 2 ? 3 : (pl.P > 1 ? 2 : 1);
-  pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * ((size_t)p.dpp * p.d + p.dpp) * sizeof(float)
+  pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * (size_t)ws_segment_floats(p) * sizeof(float)
                          : 0;
   return pl;
 }
@@ -858,7 +858,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     cudaError_t e = launch_state_tc(p, pl, k, v, ws, dev_status, s);
     if (e != cudaSuccess) return e;
     if (pl.P > 2) {
-      const int64_t elems4 = ((int64_t)p.dpp * p.d + p.dpp) / 4;
+      const int64_t elems4 = ws_segment_floats(p) / 4;
       const int64_t n4 = (int64_t)U * elems4;
       segment_scan_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
           reinterpret_cast<float4*>(ws), (int64_t)U, pl.P - 1, elems4);
@@ -867,13 +867,16 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   }
   if (KIND == HH_FMAP_HEDGEHOG && D == 64 && !p.Wk)
     return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
-  if (KIND == HH_FMAP_TAYLOR2)
+  if constexpr (KIND == HH_FMAP_TAYLOR2) {
     return launch_prefill_out_taylor(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
-  auto kern = prefill_tc_kernel<KIND, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(U * pl.P), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  } else {
+    auto kern = prefill_tc_kernel<KIND, D>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(U * pl.P), kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+  }
 }
 
 cudaError_t launch_prefill_tc(const Problem& p, const TcPlan& pl, const void* q, const void* k,

@@ -26,6 +26,7 @@
 
 #include <algorithm>
 
+#include "taylor_pack.cuh"
 #include "tc_ptx.cuh"
 
 namespace hh {
@@ -629,26 +630,28 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// Taylor, d = 16.  phi(K_t) is built row-wise (thread = token) into one of two
-// shared-memory buffers, so tile t+1's features are written while G2(t)
-// still reads tile t's.  z rides along the state update as an extra column:
+// Taylor, d = 16.  The state is kept over the 160 packed features of
+// taylor_pack.cuh (the same dot products as the 288 public ones).  phi(K_t)
+// is built row-wise (thread = token) into one of two shared-memory buffers,
+// so tile t+1's features are written while G2(t) still reads tile t's.  z
+// rides along the state update as an extra column:
 //   [S z] += phi(K_t)^T [V_t e0]     (N = 32, e0 = (1, 0, ..., 0))
 // Warp 8 issues MMAs, warp 9 issues loads.
 // ---------------------------------------------------------------------------
 namespace tay {
-constexpr int DP = 288;                                // stored features (273 used)
+constexpr int DP = tp::F;                              // packed features (153 used)
 constexpr uint32_t XT = TILE * 16 * 2;                 // 4 KB
 constexpr uint32_t OFF_K = 0;                          // 2 stages, 32 B rows
 constexpr uint32_t OFF_V = 8192;                       // 2 stages, 32B-swizzled
 constexpr uint32_t OFF_E0 = 16384;                     // [128 x 16], column 0 = 1
-constexpr uint32_t OFF_PHK = 24576;                    // 2 buffers x 6 panels of 16 KB
-constexpr uint32_t PHK_BYTES = 6 * 16384;
+constexpr uint32_t OFF_PHK = 24576;                    // 2 buffers x 4 panels of 16 KB
+constexpr uint32_t PHK_BYTES = 4 * 16384;              // features 160..255 stay zero
 constexpr uint32_t OFF_BAR = OFF_PHK + 2 * PHK_BYTES;
 enum { B_LDK = 0, B_LDV = 2, B_E1 = 4, B_G2 = 6, B_COUNT = 8 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
 static_assert(ALLOC <= 227 * 1024, "shared memory");
-constexpr uint32_t TM_S = 0;                           // 3 blocks x [S (16) | z, 0... (16)]
+constexpr uint32_t TM_S = 0;                           // 2 blocks x [S (16) | z, 0... (16)]
 constexpr int kThreads = 320;
 }  // namespace tay
 
@@ -695,7 +698,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     tmem_alloc(smem_u32(tmem_slot), 128);
     tmem_relinquish();
   }
-  // e0 rows (1, 0, ..., 0) with the 32-byte swizzle; phi(K) buffers zero (features 288.. stay 0)
+  // e0 rows (1, 0, ..., 0) with the 32-byte swizzle; phi(K) buffers zero (features 160.. stay 0)
   for (int r = tid; r < 128; r += tay::kThreads) {
     const uint32_t c0 = ((r >> 2) & 1) << 4;
     st_shared_v4(sb + OFF_E0 + r * 32 + c0, 0x3F80u, 0u, 0u, 0u);
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     uint32_t zr[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) zr[j] = 0u;
-    for (int c0 = 0; c0 < 96; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
+    for (int c0 = 0; c0 < 64; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
     tmem_st_wait();
   }
   tc_fence_before();
@@ -734,7 +737,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
         const uint64_t da = smem_desc(pb, 16384, 1024, 2);
         const uint64_t dv = smem_desc(vb, OFF_E0 - (OFF_V + (i & 1) * XT), 256, 6);
 #pragma unroll
-        for (int mb = 0; mb < 3; ++mb)
+        for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks)
             mma_ss(tmem + TM_S + 32 * mb, da + (2 * mb) * 1024 + ks * 128, dv + ks * 32, ID_S, 1);
@@ -784,33 +787,30 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
       float x[16];
 #pragma unroll
       for (int k2 = 0; k2 < 16; ++k2) x[k2] = __bfloat162float(krow[k2]);
-      // half 0: features [0, 160), half 1: [160, 288)
-      uint32_t w[80];
+      // packed features: half 0 [0, 80), half 1 [80, 160); 16-byte chunks of 8
+      uint32_t w[10][4];
       if (c == 0) {
-        taylor_pack<0, 0>(x, valid, w);
-        taylor_pack<32, 16>(x, valid, w);
-        taylor_pack<64, 32>(x, valid, w);
-        taylor_pack<96, 48>(x, valid, w);
-        taylor_pack<128, 64>(x, valid, w);
+        tp::chunk8<0>(x, valid, w[0]);   tp::chunk8<8>(x, valid, w[1]);
+        tp::chunk8<16>(x, valid, w[2]);  tp::chunk8<24>(x, valid, w[3]);
+        tp::chunk8<32>(x, valid, w[4]);  tp::chunk8<40>(x, valid, w[5]);
+        tp::chunk8<48>(x, valid, w[6]);  tp::chunk8<56>(x, valid, w[7]);
+        tp::chunk8<64>(x, valid, w[8]);  tp::chunk8<72>(x, valid, w[9]);
       } else {
-        taylor_pack<160, 0>(x, valid, w);
-        taylor_pack<192, 16>(x, valid, w);
-        taylor_pack<224, 32>(x, valid, w);
-        taylor_pack<256, 48>(x, valid, w);
+        tp::chunk8<80>(x, valid, w[0]);  tp::chunk8<88>(x, valid, w[1]);
+        tp::chunk8<96>(x, valid, w[2]);  tp::chunk8<104>(x, valid, w[3]);
+        tp::chunk8<112>(x, valid, w[4]); tp::chunk8<120>(x, valid, w[5]);
+        tp::chunk8<128>(x, valid, w[6]); tp::chunk8<136>(x, valid, w[7]);
+        tp::chunk8<144>(x, valid, w[8]); tp::chunk8<152>(x, valid, w[9]);
       }
       // buffer b held phi(K(i-2)), read by G2(i-2)
       if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + b), ((i - 2) >> 1) & 1, wp)))
         break;
       const uint32_t phk = sb + OFF_PHK + b * PHK_BYTES;
-      const int f0 = c == 0 ? 0 : 160;
-      const int nq = c == 0 ? 20 : 16;   // 16-byte chunks (8 features each)
 #pragma unroll
-      for (int q = 0; q < 20; ++q) {
-        if (q < nq) {
-          const int f = f0 + 8 * q;
-          st_shared_v4(phk + (f / 64) * 16384 + sw128_chunk(row, (f % 64) / 8), w[4 * q],
-                       w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
+      for (int q = 0; q < 10; ++q) {
+        const int f = 80 * c + 8 * q;
+        st_shared_v4(phk + (f / 64) * 16384 + sw128_chunk(row, (f % 64) / 8), w[q][0], w[q][1],
+                     w[q][2], w[q][3]);
       }
       fence_proxy_async();
       __syncwarp();
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   if (warp < 8 && !*(volatile int*)abort_flag) {
     const int c = warp >> 2;
     float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)DP * 16 + DP);
-    for (int mb = c; mb < 3; mb += 2) {
+    for (int mb = c; mb < 2; mb += 2) {
       const int f = mb * 128 + 32 * (warp & 3) + lane;
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base(warp) + TM_S + 32 * mb, sv);
@@ -918,12 +918,15 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
     state_t128_kernel<<<(unsigned)(U * (pl.P - 1)), t128::kThreads, t128::ALLOC, s>>>(a);
     return cudaGetLastError();
   }
-  const size_t smem = SSmem<KIND, D>::ALLOC;
-  cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<KIND, D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  state_tc_kernel<KIND, D><<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  if constexpr (KIND == HH_FMAP_HEDGEHOG && D == 64) {
+    const size_t smem = SSmem<KIND, D>::ALLOC;
+    cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<KIND, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    state_tc_kernel<KIND, D><<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -5,7 +5,8 @@
 // with s = q . k.  The intra-tile scores therefore need one K = 16 MMA of
 // Q K^T and two FMAs per element instead of a 288-deep feature contraction;
 // the running state (section 2, paper Eq. 2; "Complexity Analysis") still
-// needs the features:
+// needs features, kept as the 160 packed features of taylor_pack.cuh (the 136
+// unordered pairs carry the same dot products as the 256 ordered ones):
 //   Sc(t) = Q_t K_t^T                         -> P = bf16(tril(1 + Sc + Sc^2/2))
 //   [S z] += phi(K_t)^T [V_t e0]             (N = 32, z rides in column 16)
 //   [O den] = P [V_t e0] + phi(Q_t) [S_bf16 z2]   (z2 = z as a bf16 hi/lo pair)
@@ -23,6 +24,7 @@
 
 #include <algorithm>
 
+#include "taylor_pack.cuh"
 #include "tc_ptx.cuh"
 
 namespace hh {
@@ -30,16 +32,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int D = 16, DP = 288, TILE = 128;
+constexpr int D = 16, DP = tp::F, TILE = 128;   // DP: packed features (153 used)
 constexpr int kThreads = 320;
 constexpr uint32_t XT = TILE * D * 2;                   // one Q, K or V tile: 4 KB
 // shared memory (1024-aligned base); Q, K, V tiles are 32B-swizzled rows
 constexpr uint32_t OFF_Q = 0, OFF_K = 8192, OFF_V = 16384;   // 2 stages each
 constexpr uint32_t OFF_E0 = 24576;                      // [128 x 16], column 0 = 1
-constexpr uint32_t SB_BYTES = DP * 32;                  // [288 x 16] bf16, 32B-swizzled
+constexpr uint32_t SB_BYTES = DP * 32;                  // [160 x 16] bf16, 32B-swizzled
 constexpr uint32_t OFF_SB = 28672;                      // 2 x (S_bf16 | z2)
-constexpr uint32_t OFF_PHK = 65536;                     // phi(K): 6 panels [128 tok x 64 feat]
-constexpr uint32_t OFF_P = OFF_PHK + 6 * 16384;         // P: 2 panels [128 rows x 64 keys]
+constexpr uint32_t OFF_PHK = 49152;                     // phi(K): 4 panels [128 tok x 64 feat]
+constexpr uint32_t OFF_P = OFF_PHK + 4 * 16384;         // P: 2 panels [128 rows x 64 keys]
 constexpr uint32_t OFF_BAR = OFF_P + 2 * 16384;
 enum { B_LD = 0, B_SC = 2, B_SU = 4, B_G3 = 6, B_E1 = 8, B_E2 = 10, B_E3 = 12, B_COUNT = 14 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
@@ -47,16 +49,16 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_SB + 4 * SB_BYTES <= OFF_PHK, "S_bf16 buffers");
 // TMEM columns
-constexpr uint32_t TM_S = 0;                            // 3 blocks x [S (16) | z, 0.. (16)]
-__host__ __device__ constexpr uint32_t TM_Y(int b) { return 96 + 144 * b; }   // phi(Q) pairs
-constexpr uint32_t TM_X = 384;                          // Sc (128) -> [O den] (32)
+constexpr uint32_t TM_S = 0;                            // 2 blocks x [S (16) | z, 0.. (16)]
+__host__ __device__ constexpr uint32_t TM_Y(int b) { return 64 + 80 * b; }    // phi(Q) pairs
+constexpr uint32_t TM_X = 256;                          // Sc (128) -> [O den] (32)
 
 struct ArgsT {
   CUtensorMap tq, tk, tv;
   __nv_bfloat16* y;
   const float* ws;   // [U][P-1][DP*D + DP] inclusive prefixes (ws_s_index layout, then z)
-  float* S_out;      // [U][DP][D] or null
-  float* z_out;      // [U][DP]
+  float* S_out;      // [U][288][D] (public feature order) or null
+  float* z_out;      // [U][288]
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -78,37 +80,29 @@ __device__ __forceinline__ void load_row16(const uint8_t* tile, int r, float (&x
   x[12] = bf16_lo(b.z); x[13] = bf16_hi(b.z); x[14] = bf16_lo(b.w); x[15] = bf16_hi(b.w);
 }
 
-// Feature f of [1, x, x_i x_j / sqrt2 (i-major)]; zero past 272.
-__device__ __forceinline__ float tfeat(int f, const float (&x)[16]) {
-  if (f == 0) return 1.f;
-  if (f <= 16) return x[f - 1];
-  if (f <= 272) return x[(f - 17) >> 4] * x[(f - 17) & 15] * kInvSqrt2;
-  return 0.f;
-}
-
-// 32 features from FB as 16 bf16 pairs.
-template <int FB>
-__device__ __forceinline__ void tpack(const float (&x)[16], bool valid, uint32_t (&w)[16]) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    w[j] = valid ? pack_bf16(tfeat(FB + 2 * j, x), tfeat(FB + 2 * j + 1, x)) : 0u;
-}
-
-template <int FB>
-__device__ __forceinline__ void phiq_chunk(const float (&x)[16], uint32_t ty) {
+// phi(q): 32 packed features from F0 -> 16 TMEM columns (bf16 pairs)
+template <int F0>
+__device__ __forceinline__ void phiq32(const float (&x)[16], uint32_t ty) {
   uint32_t w[16];
-  tpack<FB>(x, true, w);
-  tmem_st16(ty + FB / 2, w);
+  tp::chunk8<F0>(x, true, *reinterpret_cast<uint32_t(*)[4]>(&w[0]));
+  tp::chunk8<F0 + 8>(x, true, *reinterpret_cast<uint32_t(*)[4]>(&w[4]));
+  tp::chunk8<F0 + 16>(x, true, *reinterpret_cast<uint32_t(*)[4]>(&w[8]));
+  tp::chunk8<F0 + 24>(x, true, *reinterpret_cast<uint32_t(*)[4]>(&w[12]));
+  tmem_st16(ty + F0 / 2, w);
 }
-
-template <int FB>
-__device__ __forceinline__ void phik_chunk(const float (&x)[16], bool valid, uint32_t phk, int row) {
-  uint32_t w[16];
-  tpack<FB>(x, valid, w);
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4)
-    st_shared_v4(phk + (FB / 64) * 16384 + sw128_chunk(row, (FB % 64) / 8 + q4), w[4 * q4],
-                 w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+template <int F0>
+__device__ __forceinline__ void phiq16(const float (&x)[16], uint32_t ty) {
+  uint32_t w[8];
+  tp::chunk8<F0>(x, true, *reinterpret_cast<uint32_t(*)[4]>(&w[0]));
+  tp::chunk8<F0 + 8>(x, true, *reinterpret_cast<uint32_t(*)[4]>(&w[4]));
+  tmem_st8(ty + F0 / 2, w);
+}
+// phi(k): 8 packed features from F0 -> one 16-byte chunk of the swizzled panels
+template <int F0>
+__device__ __forceinline__ void phik8(const float (&x)[16], bool valid, uint32_t phk, int row) {
+  uint32_t w[4];
+  tp::chunk8<F0>(x, valid, w);
+  st_shared_v4(phk + (F0 / 64) * 16384 + sw128_chunk(row, (F0 % 64) / 8), w[0], w[1], w[2], w[3]);
 }
 
 // The bound of 384 threads caps registers at 168 per thread (warps 0, 4, 8 and
@@ -154,7 +148,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     tmem_relinquish();
   }
   // e0 rows (1, 0, ..., 0); z2 buffers zero (only column pair 0-1 is rewritten);
-  // phi(K) panels zero (features 288..383 stay zero)
+  // phi(K) panels zero (features 160..255 stay zero)
   for (int r = tid; r < 128; r += kThreads) {
     const uint32_t c0 = ((r >> 2) & 1) << 4;
     st_shared_v4(sb + OFF_E0 + r * 32 + c0, 0x3F80u, 0u, 0u, 0u);
@@ -164,7 +158,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     const uint32_t b = i / SB_BYTES, o = i % SB_BYTES;
     st_shared_v4(sb + OFF_SB + b * 2 * SB_BYTES + SB_BYTES + o, 0u, 0u, 0u, 0u);
   }
-  for (uint32_t i = tid * 16; i < 6 * 16384u; i += kThreads * 16)
+  for (uint32_t i = tid * 16; i < 4 * 16384u; i += kThreads * 16)
     st_shared_v4(sb + OFF_PHK + i, 0u, 0u, 0u, 0u);
   fence_proxy_async();
   tc_fence_before();
@@ -177,7 +171,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     const int c = warp >> 2;
     const float* prefix =
         seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * (size_t)(DP * D + DP) : nullptr;
-    for (int mb = c; mb < 3; mb += 2) {
+    for (int mb = c; mb < 2; mb += 2) {
       const int f = 128 * mb + 32 * (warp & 3) + lane;
       uint32_t r[32];
 #pragma unroll
@@ -236,7 +230,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
         tc_fence_after();
         if (leader) {
 #pragma unroll
-          for (int mb = 0; mb < 3; ++mb)
+          for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
             for (int ks = 0; ks < TILE / 16; ++ks)
               mma_ss(tmem + TM_S + 32 * mb, dphk + (2 * mb) * 1024 + ks * 128, v + ks * 32, ID_SU,
@@ -317,22 +311,19 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       const int s = i & 1;
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_LD + s), (i >> 1) & 1, wp))) { good = false; return; }
-      // phi(Q): half 0 features [0, 160), half 1 [160, 288) -> packed TMEM columns
+      // phi(Q): half 0 packed features [0, 80), half 1 [80, 160) -> TMEM column pairs
       {
         float x[16];
         load_row16(sm + OFF_Q + s * XT, row, x);
         const uint32_t ty = tmem + lb + TM_Y(s);
         if (c == 0) {
-          phiq_chunk<0>(x, ty);
-          phiq_chunk<32>(x, ty);
-          phiq_chunk<64>(x, ty);
-          phiq_chunk<96>(x, ty);
-          phiq_chunk<128>(x, ty);
+          phiq32<0>(x, ty);
+          phiq32<32>(x, ty);
+          phiq16<64>(x, ty);
         } else {
-          phiq_chunk<160>(x, ty);
-          phiq_chunk<192>(x, ty);
-          phiq_chunk<224>(x, ty);
-          phiq_chunk<256>(x, ty);
+          phiq32<80>(x, ty);
+          phiq32<112>(x, ty);
+          phiq16<144>(x, ty);
         }
       }
       // phi(K) and the state snapshot need SU(i-1) done (it read phi(K(i-1)), updated S)
@@ -348,21 +339,22 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
         load_row16(sm + OFF_K + s * XT, row, x);
         const uint32_t phk = sb + OFF_PHK;
         if (c == 0) {
-          phik_chunk<0>(x, valid, phk, row);
-          phik_chunk<32>(x, valid, phk, row);
-          phik_chunk<64>(x, valid, phk, row);
-          phik_chunk<96>(x, valid, phk, row);
-          phik_chunk<128>(x, valid, phk, row);
+          phik8<0>(x, valid, phk, row);   phik8<8>(x, valid, phk, row);
+          phik8<16>(x, valid, phk, row);  phik8<24>(x, valid, phk, row);
+          phik8<32>(x, valid, phk, row);  phik8<40>(x, valid, phk, row);
+          phik8<48>(x, valid, phk, row);  phik8<56>(x, valid, phk, row);
+          phik8<64>(x, valid, phk, row);  phik8<72>(x, valid, phk, row);
         } else {
-          phik_chunk<160>(x, valid, phk, row);
-          phik_chunk<192>(x, valid, phk, row);
-          phik_chunk<224>(x, valid, phk, row);
-          phik_chunk<256>(x, valid, phk, row);
+          phik8<80>(x, valid, phk, row);  phik8<88>(x, valid, phk, row);
+          phik8<96>(x, valid, phk, row);  phik8<104>(x, valid, phk, row);
+          phik8<112>(x, valid, phk, row); phik8<120>(x, valid, phk, row);
+          phik8<128>(x, valid, phk, row); phik8<136>(x, valid, phk, row);
+          phik8<144>(x, valid, phk, row); phik8<152>(x, valid, phk, row);
         }
       }
       // S_bf16 and z2 (z as z_hi + z_lo) of the tokens before this tile
       const uint32_t sbb = sb + OFF_SB + s * 2 * SB_BYTES;
-      for (int mb = c; mb < 3; mb += 2) {
+      for (int mb = c; mb < 2; mb += 2) {
         const int f = 128 * mb + row;
         uint32_t sv[32];
         tmem_ld32(tmem + lb + TM_S + 32 * mb, sv);
@@ -468,20 +460,34 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   if (A.S_out && seg == A.P - 1 && warp < 8 && !*(volatile int*)abort_flag) {
-    // the last SU completed before the last G3 (issue order), which E3 waited for
+    // the last SU completed before the last G3 (issue order), which E3 waited for;
+    // packed feature f goes to its public row(s) [1, x, x_i x_j / sqrt2 (i-major)]
     const int c = warp >> 2;
-    for (int mb = c; mb < 3; mb += 2) {
+    float* Sd = A.S_out + (size_t)unit * tp::DPUB * D;
+    float* zd = A.z_out + (size_t)unit * tp::DPUB;
+    for (int mb = c; mb < 2; mb += 2) {
       const int f = 128 * mb + 32 * (warp & 3) + lane;
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base(warp) + TM_S + 32 * mb, sv);
-      if (f < DP) {
-        float4* dst = reinterpret_cast<float4*>(A.S_out + ((size_t)unit * DP + f) * D);
+      int r[2];
+      float scale;
+      const int nr = f < DP ? tp::public_rows(f, r[0], r[1], scale) : 0;
+      for (int t = 0; t < nr; ++t) {
+        float4* dst = reinterpret_cast<float4*>(Sd + (size_t)r[t] * D);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          dst[q] = make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
-                               __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
-        A.z_out[(size_t)unit * DP + f] = __uint_as_float(sv[16]);
+          dst[q] = make_float4(__uint_as_float(sv[4 * q]) * scale,
+                               __uint_as_float(sv[4 * q + 1]) * scale,
+                               __uint_as_float(sv[4 * q + 2]) * scale,
+                               __uint_as_float(sv[4 * q + 3]) * scale);
+        zd[r[t]] = __uint_as_float(sv[16]) * scale;
       }
+    }
+    if (warp == 0 && lane < tp::DPUB - 273) {   // zero pad rows 273..287
+      float4* dst = reinterpret_cast<float4*>(Sd + (size_t)(273 + lane) * D);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zd[273 + lane] = 0.f;
     }
   }
   tc_fence_before();
