@@ -13,10 +13,12 @@
 //   y = O / (den_hi + den_lo)
 // Roles: warp 8 issues every tcgen05.mma as soon as its inputs are ready,
 // warp 9 issues TMA loads, warps 0-7 run the epilogue phases
-//   E1(t): phi(Q_t) -> TMEM (two buffers), phi(K_t) -> smem, S_bf16/z2 snapshot
+//   E1(t): phi(Q_t) -> TMEM, phi(K_t) -> smem, S_bf16/z2 snapshot
 //   E2(t): P from Sc(t);   E3(t): y from [O den]
-// in the order E1(0), then E2(t), E1(t+1), E3(t) per step.  Every mbarrier
-// wait is bounded in time (tc_ptx.cuh).
+// in the order E1(t), E2(t), E3(t-1) per step.  phi(Q), S_bf16/z2, the score /
+// output TMEM columns and P have two buffers (tile parity), so Sc(t+1) and
+// E2(t+1) need not wait for E3(t).  Every mbarrier wait is bounded in time
+// (tc_ptx.cuh).
 
 #include <math.h>
 #include <stdlib.h>
@@ -41,8 +43,8 @@ constexpr uint32_t OFF_E0 = 24576;                      // [128 x 16], column 0 
 constexpr uint32_t SB_BYTES = DP * 32;                  // [160 x 16] bf16, 32B-swizzled
 constexpr uint32_t OFF_SB = 28672;                      // 2 x (S_bf16 | z2)
 constexpr uint32_t OFF_PHK = 49152;                     // phi(K): 4 panels [128 tok x 64 feat]
-constexpr uint32_t OFF_P = OFF_PHK + 4 * 16384;         // P: 2 panels [128 rows x 64 keys]
-constexpr uint32_t OFF_BAR = OFF_P + 2 * 16384;
+constexpr uint32_t OFF_P = OFF_PHK + 4 * 16384;         // P: 2 buffers x 2 panels [128 x 64 keys]
+constexpr uint32_t OFF_BAR = OFF_P + 4 * 16384;
 enum { B_LD = 0, B_SC = 2, B_SU = 4, B_G3 = 6, B_E1 = 8, B_E2 = 10, B_E3 = 12, B_COUNT = 14 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -51,7 +53,7 @@ static_assert(OFF_SB + 4 * SB_BYTES <= OFF_PHK, "S_bf16 buffers");
 // TMEM columns
 constexpr uint32_t TM_S = 0;                            // 2 blocks x [S (16) | z, 0.. (16)]
 __host__ __device__ constexpr uint32_t TM_Y(int b) { return 64 + 80 * b; }    // phi(Q) pairs
-constexpr uint32_t TM_X = 256;                          // Sc (128) -> [O den] (32)
+__host__ __device__ constexpr uint32_t TM_X(int b) { return 256 + 128 * b; }  // Sc -> [O den]
 
 struct ArgsT {
   CUtensorMap tq, tk, tv;
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       const bool leader = lane == 0;
       // descriptor bases; a k-step only moves the start-address field (16-byte units)
       const uint64_t dphk = smem_desc(sb + OFF_PHK, 16384, 1024, 2);
-      const uint64_t dp = smem_desc(sb + OFF_P, 16, 1024, 2);
+      const uint64_t dp0 = smem_desc(sb + OFF_P, 16, 1024, 2);
       auto dv = [&](int s) {   // [V e0]: the e0 block one leading-byte offset after V
         return smem_desc(sb + OFF_V + s * XT, OFF_E0 - (OFF_V + s * XT), 256, 6);
       };
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
         const uint64_t db = smem_desc(sb + OFF_K + s * XT, 16, 256, 6);
         tc_fence_after();
         if (leader) {
-          mma_ss(tmem + TM_X, da, db, ID_SC, 0);
+          mma_ss(tmem + TM_X(s), da, db, ID_SC, 0);
           mma_commit(bar(B_SC + s));
         }
         __syncwarp();
@@ -248,16 +250,17 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
         if (leader) {
 #pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ss(tmem + TM_X, dp + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32, ID_O, ks > 0);
+            mma_ss(tmem + TM_X(s), dp0 + s * 2048 + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32,
+                   ID_O, ks > 0);
 #pragma unroll
           for (int ks = 0; ks < DP / 16; ++ks)
-            mma_ts(tmem + TM_X, ty + ks * 8, dsb + ks * 32, ID_O, 1);
+            mma_ts(tmem + TM_X(s), ty + ks * 8, dsb + ks * 32, ID_O, 1);
           mma_commit(bar(B_G3 + s));
         }
         __syncwarp();
       };
       // Per tile the MMAs go in the order Sc, SU, G3:
-      //   Sc(i)  needs Q, K landed and E3(i-1) done (the X columns free)
+      //   Sc(i)  needs Q, K landed and E3(i-2) done (its X columns free)
       //   SU(i)  needs Sc(i) issued and E1(i) done (phi(K) written)
       //   G3(i)  needs SU(i) issued and E2(i) done (P written; E1(i) came before E2(i))
       int na = 0, nb = 0, n3 = 0;
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
           G3(n3++);
           progress = true;
         } else if (na < nt && probe(B_LD + (na & 1), (na >> 1) & 1) &&
-                   (na == 0 || probe(B_E3 + ((na - 1) & 1), ((na - 1) >> 1) & 1))) {
+                   (na < 2 || probe(B_E3 + (na & 1), ((na - 2) >> 1) & 1))) {
           Sc(na++);
           progress = true;
         } else if (nb < na && probe(B_E1 + (nb & 1), (nb >> 1) & 1)) {
@@ -391,14 +394,14 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int kc = 2 * c + h2;
-        const uint32_t panel = sb + OFF_P + c * 16384;
+        const uint32_t panel = sb + OFF_P + s * 32768 + c * 16384;
         if (kc > g) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
             st_shared_v4(panel + sw128_chunk(row, 4 * h2 + q4), 0u, 0u, 0u, 0u);
         } else {
           uint32_t sv[32];
-          tmem_ld32(tmem + lb + TM_X + 32 * kc, sv);
+          tmem_ld32(tmem + lb + TM_X(s) + 32 * kc, sv);
           const bool diag = kc == g;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -431,8 +434,8 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G3 + s), (i >> 1) & 1, wp))) { good = false; return; }
       tc_fence_after();
       uint32_t ov[16], d0, d1;
-      tmem_ld16(tmem + lb + TM_X, ov);
-      tmem_ld2(tmem + lb + TM_X + 16, d0, d1);   // rowsum(P) + phi(q).z_hi, phi(q).z_lo
+      tmem_ld16(tmem + lb + TM_X(s), ov);
+      tmem_ld2(tmem + lb + TM_X(s) + 16, d0, d1);   // rowsum(P) + phi(q).z_hi, phi(q).z_lo
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_E3 + s));   // the X columns are free for Sc(i+1)
@@ -447,11 +450,12 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       }
     };
 
-    if (nt > 0) E1(0);
-    for (int i = 0; i < nt && good; ++i) {
-      E2(i);
-      if (good && i + 1 < nt) E1(i + 1);
-      if (good) E3(i);
+    for (int i = 0; i <= nt && good; ++i) {
+      if (i < nt) {
+        E1(i);
+        if (good) E2(i);
+      }
+      if (good && i >= 1) E3(i - 1);
     }
   }
 
