@@ -28,5 +28,7 @@ from .hedgehog_oracle import (  # noqa: F401
     mimicry_loss,
     mimicry_loss_rows,
     fwd_causal,
+    mimicry_loss_grad,
+    loss_grad_causal,
     loss_causal,
 )

@@ -46,6 +46,8 @@ __all__ = [
     "mimicry_loss_rows",
     "fwd_causal",
     "loss_causal",
+    "mimicry_loss_grad",
+    "loss_grad_causal",
 ]
 
 
@@ -221,6 +223,43 @@ def mimicry_loss_rows(q, k, phi_q, phi_k, rows) -> np.ndarray:
     return out
 
 
+def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None):
+    """Gradient of sum_i L_i (paper Eq. 4, one head) w.r.t. the Hedgehog map.
+
+    HH summary, "The Attention Weight Distillation Loss": only the feature-map
+    MLPs are trained; q, k (and so the softmax target p) are frozen.  With
+    h = xW + b, phi = [e^h; e^-h] ("The Hedgehog MLP Feature Map", Choices 1
+    and 3), a_ij = phi(q_i).phi(k_j), A_i = sum_{j<=i} a_ij and
+    L_i = ln A_i - sum_j p_ij ln a_ij, the chain rule gives
+        g_ij = dL/da_ij = 1/A_i - p_ij / a_ij                (j <= i, else 0)
+        dL/dphi(q_i) = sum_j g_ij phi(k_j),  dL/dphi(k_j) = sum_i g_ij phi(q_i)
+        dL/dh = dL/dphi_+ * e^h - dL/dphi_- * e^-h
+        dL/dW = sum_x x^T dL/dh(x),  dL/db = sum_x dL/dh(x)
+    over the query rows (query map) and the key rows (key map).  Returns
+    (dWq, dbq, dWk, dbk); with one shared map (Wk None) the gradient with
+    respect to it is dWq + dWk, dbq + dbk.
+    """
+    q, k = _f64(q), _f64(k)
+    Wq, bq = _f64(W), _f64(b)
+    Wk_, bk_ = (Wq, bq) if Wk is None else (_f64(Wk), _f64(bk))
+    d = q.shape[-1]
+    hq = q @ Wq + bq
+    hk = k @ Wk_ + bk_
+    pq = np.concatenate([np.exp(hq), np.exp(-hq)], axis=-1)
+    pk = np.concatenate([np.exp(hk), np.exp(-hk)], axis=-1)
+    n = q.shape[0]
+    mask = np.tril(np.ones((n, n), dtype=bool))
+    a = pq @ pk.T
+    A = np.where(mask, a, 0.0).sum(axis=-1)
+    p = softmax_target(q, k)
+    g = np.where(mask, 1.0 / A[:, None] - p / np.where(mask, a, 1.0), 0.0)
+    dpq = g @ pk
+    dpk = g.T @ pq
+    dhq = dpq[:, :d] * pq[:, :d] - dpq[:, d:] * pq[:, d:]
+    dhk = dpk[:, :d] * pk[:, :d] - dpk[:, d:] * pk[:, d:]
+    return q.T @ dhq, dhq.sum(axis=0), k.T @ dhk, dhk.sum(axis=0)
+
+
 # ---------------------------------------------------------------------------
 # Batched wrappers over [B, H, n, d] inputs (per-head maps W[H], b[H])
 # ---------------------------------------------------------------------------
@@ -255,3 +294,30 @@ def loss_causal(kind, q, k, W=None, b=None):
             pk = _map_head(kind, k[bi, h], W, b, h)
             rows[bi, h] = mimicry_loss(q[bi, h], k[bi, h], pq, pk)
     return rows, rows.sum(axis=-1)
+
+
+def loss_grad_causal(q, k, W, b, Wk=None, bk=None):
+    """Gradient of the loss summed over [B, H, n] w.r.t. per-head maps.
+
+    Returns (dWq [H, d, d], dbq [H, d], dWk, dbk), each summed over the batch.
+    With one shared map (Wk None) dWk and dbk are None and the query and key
+    sides are added into dWq, dbq.
+    """
+    q, k = _f64(q), _f64(k)
+    B, H, n, d = q.shape
+    dWq = np.zeros((H, d, d))
+    dbq = np.zeros((H, d))
+    dWk = np.zeros((H, d, d))
+    dbk = np.zeros((H, d))
+    for bi in range(B):
+        for h in range(H):
+            g = mimicry_loss_grad(q[bi, h], k[bi, h], _f64(W)[h], _f64(b)[h],
+                                  None if Wk is None else _f64(Wk)[h],
+                                  None if bk is None else _f64(bk)[h])
+            dWq[h] += g[0]
+            dbq[h] += g[1]
+            dWk[h] += g[2]
+            dbk[h] += g[3]
+    if Wk is None:
+        return dWq + dWk, dbq + dbk, None, None
+    return dWq, dbq, dWk, dbk

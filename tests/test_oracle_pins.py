@@ -190,10 +190,71 @@ def check_loss_properties(O, golden):
     np.testing.assert_allclose(L0, np.log(np.arange(1, n + 1)), rtol=1e-13, atol=1e-15)
 
 
+def check_loss_grad_finite_differences(O, golden):
+    """The loss gradient w.r.t. W, b against central differences of the loss."""
+    rng = np.random.default_rng(11)
+    n, d, eps = 6, 3, 1e-6
+
+    def total(Wq, bq, Wk, bk, q, k):
+        pq = O.hedgehog_feature_map(q, Wq, bq)
+        pk = O.hedgehog_feature_map(k, Wk, bk)
+        return O.mimicry_loss(q, k, pq, pk).sum()
+
+    def fd(f, X):
+        g = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            g[idx] = (f(Xp) - f(Xm)) / (2 * eps)
+        return g
+
+    for trial in range(2):
+        q, k = rng.normal(size=(2, n, d)) * 0.6
+        Wq, Wk = rng.normal(size=(2, d, d)) * 0.5
+        bq, bk = rng.normal(size=(2, d)) * 0.3
+        # one map shared by queries and keys
+        g = O.mimicry_loss_grad(q, k, Wq, bq)
+        np.testing.assert_allclose(g[0] + g[2], fd(lambda X: total(X, bq, X, bq, q, k), Wq),
+                                   rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(g[1] + g[3], fd(lambda X: total(Wq, X, Wq, X, q, k), bq),
+                                   rtol=1e-6, atol=1e-8)
+        # separate query and key maps
+        g = O.mimicry_loss_grad(q, k, Wq, bq, Wk, bk)
+        np.testing.assert_allclose(g[0], fd(lambda X: total(X, bq, Wk, bk, q, k), Wq), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(g[1], fd(lambda X: total(Wq, X, Wk, bk, q, k), bq), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(g[2], fd(lambda X: total(Wq, bq, X, bk, q, k), Wk), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(g[3], fd(lambda X: total(Wq, bq, Wk, X, q, k), bk), rtol=1e-6, atol=1e-8)
+    # batched wrapper: sum over batch of per-head gradients of the summed loss
+    B, H = 2, 2
+    q = rng.normal(size=(B, H, 4, d)) * 0.6
+    k = rng.normal(size=(B, H, 4, d)) * 0.6
+    W = rng.normal(size=(H, d, d)) * 0.5
+    b = rng.normal(size=(H, d)) * 0.3
+    dW, db, _, _ = O.loss_grad_causal(q, k, W, b)
+
+    def batch_total(Wx, bx):
+        return O.loss_causal("hedgehog", q, k, Wx, bx)[1].sum()
+
+    for h in range(H):
+        for idx in [(0, 1), (2, 0)]:
+            Wp, Wm = W.copy(), W.copy()
+            Wp[(h,) + idx] += eps
+            Wm[(h,) + idx] -= eps
+            f = (batch_total(Wp, b) - batch_total(Wm, b)) / (2 * eps)
+            assert abs(f - dW[(h,) + idx]) <= 1e-6 * max(1.0, abs(f))
+        bp, bm = b.copy(), b.copy()
+        bp[h, 1] += eps
+        bm[h, 1] -= eps
+        f = (batch_total(W, bp) - batch_total(W, bm)) / (2 * eps)
+        assert abs(f - db[h, 1]) <= 1e-6 * max(1.0, abs(f))
+
+
 PINS = [check_hand_worked, check_taylor_closed_form, check_hedgehog_cosh,
         check_identity_and_zero_maps, check_orientation, check_weight_rows,
         check_constant_values_and_first_row, check_uniform_cases,
-        check_quadratic_vs_recurrent, check_softmax_target, check_loss_properties]
+        check_quadratic_vs_recurrent, check_softmax_target, check_loss_properties,
+        check_loss_grad_finite_differences]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -222,6 +283,11 @@ MUTANTS = {
                   "out[i] = -np.sum(p[i, : i + 1] * np.log2(w[i, : i + 1]))"),
     "loss_sign_flipped": ("out[i] = -np.sum(p[i, : i + 1]", "out[i] = np.sum(p[i, : i + 1]"),
     "softmax_no_max_subtraction": ("    s = s - s.max(axis=-1, keepdims=True)\n", "    s = s * 1.0\n"),
+    "grad_without_partition_term": ("1.0 / A[:, None] - p / np.where", "0.0 / A[:, None] - p / np.where"),
+    "grad_negative_half_sign": ("dhq = dpq[:, :d] * pq[:, :d] - dpq[:, d:]", "dhq = dpq[:, :d] * pq[:, :d] + dpq[:, d:]"),
+    "grad_no_key_side": ("k.T @ dhk, dhk.sum(axis=0)\n", "0 * (k.T @ dhk), 0 * dhk.sum(axis=0)\n"),
+    "grad_W_transposed": ("return q.T @ dhq, dhq.sum(axis=0)", "return (q.T @ dhq).T, dhq.sum(axis=0)"),
+    "grad_acausal": ("g = np.where(mask, 1.0 / A", "g = np.where(True, 1.0 / A"),
 }
 
 
