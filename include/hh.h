@@ -190,6 +190,29 @@ HH_API hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, 
                           int64_t B, int H, int64_t n, float* loss_rows, float* loss_head_sum,
                           void* workspace, size_t ws_bytes, int* dev_status, void* stream);
 
+/* Bytes of device workspace hh_mimicry_loss_grad needs (0 when none). */
+HH_API size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H,
+                                           int64_t n);
+
+/* Gradient of the summed distillation loss sum_{b,h,i} L_i (paper Eq. 4) with
+ * respect to the Hedgehog feature-map parameters.  Source: "The Attention
+ * Weight Distillation Loss" (only the feature maps are trained; q, k and the
+ * softmax target are frozen) and "The Hedgehog MLP Feature Map", Choices 1
+ * and 3.  With g_ij = 1/A_i - p_ij / a_ij (j <= i):
+ *   dL/dphi(q_i) = sum_j g_ij phi(k_j), dL/dphi(k_j) = sum_i g_ij phi(q_i),
+ *   dL/dh = dL/dphi_+ e^h - dL/dphi_- e^-h, dW = sum_x x^T dL/dh, db = sum_x dL/dh.
+ * q, k: [B][H][n][d] (dtype).  dWq [H][d][d], dbq [H][d] float32 receive the
+ * gradient w.r.t. Wq, bq summed over the batch (overwritten, not accumulated).
+ * With a separate key map (fmap->Wk set and != Wq) dWk [H][d][d] and dbk [H][d]
+ * receive the key-side gradient and must be non-NULL; with one shared map both
+ * sides are summed into dWq, dbq and dWk, dbk are ignored.  Hedgehog only
+ * (Taylor has no parameters: HH_ERR_UNSUPPORTED); d a multiple of 8, at most 128.
+ * workspace: at least hh_loss_grad_workspace_bytes(...) bytes. */
+HH_API hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q,
+                                      const void* k, int64_t B, int H, int64_t n, float* dWq,
+                                      float* dbq, float* dWk, float* dbk, void* workspace,
+                                      size_t ws_bytes, int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,5 +14,7 @@ from .api import (  # noqa: F401
     linattn_decode_step,
     linattn_fwd_causal,
     loss_workspace_bytes,
+    loss_grad_workspace_bytes,
     mimicry_loss,
+    mimicry_loss_grad,
 )

@@ -19,7 +19,8 @@ HH_FMAP_HEDGEHOG, HH_FMAP_TAYLOR2 = 0, 1
 
 EXPORTED = ("hh_version", "hh_status_str", "hh_fmap_dim", "hh_feature_map",
             "hh_fwd_workspace_bytes", "hh_fwd_plan", "hh_linattn_fwd_causal", "hh_linattn_decode_step",
-            "hh_loss_workspace_bytes", "hh_mimicry_loss", "hh_linattn_fwd_causal_noalloc")
+            "hh_loss_workspace_bytes", "hh_mimicry_loss", "hh_linattn_fwd_causal_noalloc",
+            "hh_loss_grad_workspace_bytes", "hh_mimicry_loss_grad")
 
 
 class HHFmap(ctypes.Structure):
@@ -54,6 +55,9 @@ _SIGS = {
     "hh_mimicry_loss": ([_P, _i32, _vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _vp, _vp], _i32),
     "hh_linattn_fwd_causal_noalloc": ([_P, _i32, _vp, _vp, _vp, _i64, _i32, _i64, _i32, _vp, _vp,
                                        _vp, _vp, _vp], _i32),
+    "hh_loss_grad_workspace_bytes": ([_P, _i32, _i64, _i32, _i64], _sz),
+    "hh_mimicry_loss_grad": ([_P, _i32, _vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _sz,
+                              _vp, _vp], _i32),
 }
 
 

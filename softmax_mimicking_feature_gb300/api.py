@@ -17,7 +17,7 @@ from . import _abi
 
 __all__ = ["FeatureMap", "fmap_dim", "feature_map", "fwd_workspace_bytes", "fwd_plan",
            "linattn_fwd_causal", "linattn_decode_step", "loss_workspace_bytes",
-           "mimicry_loss", "HHError"]
+           "mimicry_loss", "loss_grad_workspace_bytes", "mimicry_loss_grad", "HHError"]
 
 HHError = _abi.HHError
 
@@ -170,3 +170,35 @@ def mimicry_loss(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, return_rows: 
         ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), B, H, n, _ptr(rows), _ptr(head),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)), "hh_mimicry_loss")
     return rows, head
+
+
+def loss_grad_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int) -> int:
+    s = fm.struct()
+    return int(_abi.lib().hh_loss_grad_workspace_bytes(ctypes.byref(s), _DTYPES[dtype], B, H, n))
+
+
+def mimicry_loss_grad(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
+                      workspace: Optional[torch.Tensor] = None,
+                      dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Gradient of the summed distillation loss (hh_mimicry_loss_grad).
+
+    Returns (dWq, dbq, dWk, dbk), float32, summed over the batch; dWk, dbk are
+    None when the keys share the query map (both sides are then in dWq, dbq).
+    """
+    B, H, n, d = q.shape
+    dev = q.device
+    separate = fm.Wk is not None and fm.Wk.data_ptr() != fm.Wq.data_ptr()
+    dWq = torch.empty(H, d, d, dtype=torch.float32, device=dev)
+    dbq = torch.empty(H, d, dtype=torch.float32, device=dev)
+    dWk = torch.empty_like(dWq) if separate else None
+    dbk = torch.empty_like(dbq) if separate else None
+    need = loss_grad_workspace_bytes(fm, q.dtype, B, H, n)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_mimicry_loss_grad(
+        ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), B, H, n, _ptr(dWq), _ptr(dbq), _ptr(dWk),
+        _ptr(dbk), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
+        "hh_mimicry_loss_grad")
+    return dWq, dbq, dWk, dbk

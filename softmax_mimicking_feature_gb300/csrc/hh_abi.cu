@@ -296,4 +296,66 @@ hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const v
   return cuda_status(e);
 }
 
+static size_t loss_grad_ws(const Problem& p) {
+  const size_t phi = align256((size_t)p.B * p.H * p.n * p.dpp * elem_size(p.dtype));
+  const size_t stats = align256((size_t)p.B * p.H * p.n * 3 * sizeof(float));
+  const size_t dh = align256((size_t)p.B * p.H * p.n * p.d * sizeof(float));
+  return 2 * phi + stats + 2 * dh;
+}
+
+size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n) {
+  Problem p;
+  if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
+  if (p.kind != HH_FMAP_HEDGEHOG || B * H * n == 0) return 0;
+  return loss_grad_ws(p);
+}
+
+hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                               int64_t B, int H, int64_t n, float* dWq, float* dbq, float* dWk,
+                               float* dbk, void* workspace, size_t ws_bytes, int* dev_status,
+                               void* stream) {
+  Problem p;
+  hh_status st = make_problem(fmap, dtype, B, H, n, &p);
+  if (st != HH_OK) return st;
+  if (p.kind != HH_FMAP_HEDGEHOG || p.d % 8 != 0 || p.d > 128) return HH_ERR_UNSUPPORTED;
+  const bool separate = fmap->Wk && fmap->Wk != fmap->Wq;
+  if (!dWq || !dbq || (separate && (!dWk || !dbk))) return HH_ERR_INVALID_ARG;
+  if (!separate) dWk = dbk = nullptr;
+  if (B * n > 0 && (!q || !k)) return HH_ERR_INVALID_ARG;
+  if ((st = check_ptrs_aligned({q, k, dWq, dbq, dWk, dbk, p.Wq, p.bq, p.Wk, p.bk, workspace})) !=
+      HH_OK)
+    return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
+  const size_t need = hh_loss_grad_workspace_bytes(fmap, dtype, B, H, n);
+  if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
+  if (!device_ok()) return HH_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t wbytes = sizeof(float) * H * p.d * p.d, bbytes = sizeof(float) * H * p.d;
+  if (B * n == 0) {   // empty sum: zero gradient
+    cudaError_t e = cudaMemsetAsync(dWq, 0, wbytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dbq, 0, bbytes, s);
+    if (e == cudaSuccess && dWk) e = cudaMemsetAsync(dWk, 0, wbytes, s);
+    if (e == cudaSuccess && dbk) e = cudaMemsetAsync(dbk, 0, bbytes, s);
+    return cuda_status(e);
+  }
+  if (loss_grad_smem_bytes(p) > (size_t)device_max_smem_optin()) return HH_ERR_UNSUPPORTED;
+  char* ws = (char*)workspace;
+  const size_t phi_bytes = align256((size_t)B * H * n * p.dpp * elem_size(dtype));
+  const size_t st_bytes = align256((size_t)B * H * n * 3 * sizeof(float));
+  const size_t dh_bytes = align256((size_t)B * H * n * p.d * sizeof(float));
+  void* phq = ws;
+  void* phk = ws + phi_bytes;
+  float* stats = (float*)(ws + 2 * phi_bytes);
+  float* dhq = (float*)(ws + 2 * phi_bytes + st_bytes);
+  float* dhk = (float*)(ws + 2 * phi_bytes + st_bytes + dh_bytes);
+  cudaError_t e = fmap_tc_supported(p) ? launch_fmap_tc(p, q, 0, phq, dev_status, s)
+                                       : launch_fmap_simt(p, q, 0, phq, s);
+  if (e == cudaSuccess)
+    e = fmap_tc_supported(p) ? launch_fmap_tc(p, k, 1, phk, dev_status, s)
+                             : launch_fmap_simt(p, k, 1, phk, s);
+  if (e == cudaSuccess)
+    e = launch_loss_grad(p, q, k, phq, phk, stats, dhq, dhk, dWq, dbq, dWk, dbk, s);
+  return cuda_status(e);
+}
+
 }  // extern "C"

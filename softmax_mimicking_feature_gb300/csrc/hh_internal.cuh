@@ -92,6 +92,13 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
                                       float* z_out, const void* ws, int* dev_status,
                                       cudaStream_t s);
 
+// Gradient of the summed mimicry loss w.r.t. the Hedgehog map (CUDA cores,
+// fp32 arithmetic): phi(q), phi(k) precomputed; stats [U][n][3]; dh [U][n][d].
+size_t loss_grad_smem_bytes(const Problem& p);
+cudaError_t launch_loss_grad(const Problem& p, const void* q, const void* k, const void* phq,
+                             const void* phk, float* stats, float* dhq, float* dhk, float* dWq,
+                             float* dbq, float* dWk, float* dbk, cudaStream_t s);
+
 // Tensor-core (tcgen05) feature map and mimicry loss for bf16 Hedgehog d in {64, 128}.
 bool fmap_tc_supported(const Problem& p);
 cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,
