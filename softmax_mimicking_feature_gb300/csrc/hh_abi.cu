@@ -286,7 +286,8 @@ hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const v
     cudaError_t e = launch_fmap_tc(p, q, 0, phq, dev_status, s);
     if (e == cudaSuccess) e = launch_fmap_tc(p, k, 1, phk, dev_status, s);
     if (e == cudaSuccess)
-      e = launch_loss_tc(p, q, k, phq, phk, loss_rows, partial, loss_head_sum, dev_status, s);
+      e = launch_loss_tc(p, q, k, phq, phk, loss_rows, partial, loss_head_sum, nullptr, dev_status,
+                         s);
     return cuda_status(e);
   }
   cudaError_t e = launch_fmap_simt(p, q, 0, phq, s);
@@ -296,18 +297,38 @@ hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const v
   return cuda_status(e);
 }
 
-static size_t loss_grad_ws(const Problem& p) {
-  const size_t phi = align256((size_t)p.B * p.H * p.n * p.dpp * elem_size(p.dtype));
-  const size_t stats = align256((size_t)p.B * p.H * p.n * 3 * sizeof(float));
-  const size_t dh = align256((size_t)p.B * p.H * p.n * p.d * sizeof(float));
-  return 2 * phi + stats + 2 * dh;
+// Workspace of hh_mimicry_loss_grad.
+//   tensor-core path (bf16, d in {64, 128}): phi(q) | phi(k) | row stats
+//     [U][NT*128] (c_i, 1/A_i) | loss partials [U][NT] | loss sums [U] |
+//     per-CTA dW, db shares [2][U][NT][d*d + d]
+//   CUDA-core path: phi(q) | phi(k) | row stats [U][n][3] | dL/dh(q) | dL/dh(k)
+struct GradWs {
+  size_t phi, stats, a, b, c, total;
+};
+static GradWs loss_grad_ws(const Problem& p) {
+  GradWs w;
+  const size_t U = (size_t)p.B * p.H;
+  const size_t NT = (size_t)ceil_div(p.n, 128);
+  w.phi = align256(U * p.n * p.dpp * elem_size(p.dtype));
+  if (loss_grad_tc_shape(p)) {
+    w.stats = align256(U * NT * 128 * 2 * sizeof(float));
+    w.a = align256(U * NT * sizeof(float));
+    w.b = align256(U * sizeof(float));
+    w.c = align256(loss_grad_tc_partial_floats(p) * sizeof(float));
+  } else {
+    w.stats = align256(U * p.n * 3 * sizeof(float));
+    w.a = w.b = align256(U * p.n * p.d * sizeof(float));
+    w.c = 0;
+  }
+  w.total = 2 * w.phi + w.stats + w.a + w.b + w.c;
+  return w;
 }
 
 size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n) {
   Problem p;
   if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
   if (p.kind != HH_FMAP_HEDGEHOG || B * H * n == 0) return 0;
-  return loss_grad_ws(p);
+  return loss_grad_ws(p).total;
 }
 
 hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, const void* k,
@@ -338,23 +359,33 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
     if (e == cudaSuccess && dbk) e = cudaMemsetAsync(dbk, 0, bbytes, s);
     return cuda_status(e);
   }
-  if (loss_grad_smem_bytes(p) > (size_t)device_max_smem_optin()) return HH_ERR_UNSUPPORTED;
+  const bool tc = loss_grad_tc_shape(p);
+  if (tc ? !loss_grad_tc_supported(p)
+         : loss_grad_smem_bytes(p) > (size_t)device_max_smem_optin())
+    return HH_ERR_UNSUPPORTED;
+  const GradWs w = loss_grad_ws(p);
   char* ws = (char*)workspace;
-  const size_t phi_bytes = align256((size_t)B * H * n * p.dpp * elem_size(dtype));
-  const size_t st_bytes = align256((size_t)B * H * n * 3 * sizeof(float));
-  const size_t dh_bytes = align256((size_t)B * H * n * p.d * sizeof(float));
   void* phq = ws;
-  void* phk = ws + phi_bytes;
-  float* stats = (float*)(ws + 2 * phi_bytes);
-  float* dhq = (float*)(ws + 2 * phi_bytes + st_bytes);
-  float* dhk = (float*)(ws + 2 * phi_bytes + st_bytes + dh_bytes);
+  void* phk = ws + w.phi;
+  float* stats = (float*)(ws + 2 * w.phi);
+  float* wa = (float*)(ws + 2 * w.phi + w.stats);
+  float* wb = (float*)(ws + 2 * w.phi + w.stats + w.a);
+  float* wc = (float*)(ws + 2 * w.phi + w.stats + w.a + w.b);
   cudaError_t e = fmap_tc_supported(p) ? launch_fmap_tc(p, q, 0, phq, dev_status, s)
                                        : launch_fmap_simt(p, q, 0, phq, s);
   if (e == cudaSuccess)
     e = fmap_tc_supported(p) ? launch_fmap_tc(p, k, 1, phk, dev_status, s)
                              : launch_fmap_simt(p, k, 1, phk, s);
-  if (e == cudaSuccess)
-    e = launch_loss_grad(p, q, k, phq, phk, stats, dhq, dhk, dWq, dbq, dWk, dbk, s);
+  if (tc) {
+    // wa: loss partials, wb: loss sums, wc: dW, db shares
+    if (e == cudaSuccess)
+      e = launch_loss_tc(p, q, k, phq, phk, nullptr, wa, wb, stats, dev_status, s);
+    if (e == cudaSuccess)
+      e = launch_loss_grad_tc(p, q, k, phq, phk, stats, wc, dWq, dbq, dWk, dbk, dev_status, s);
+  } else if (e == cudaSuccess) {
+    // wa, wb: dL/dh of the query and key rows
+    e = launch_loss_grad(p, q, k, phq, phk, stats, wa, wb, dWq, dbq, dWk, dbk, s);
+  }
   return cuda_status(e);
 }
 

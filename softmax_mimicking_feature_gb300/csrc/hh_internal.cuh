@@ -103,10 +103,30 @@ cudaError_t launch_loss_grad(const Problem& p, const void* q, const void* k, con
 bool fmap_tc_supported(const Problem& p);
 cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,
                            int* dev_status, cudaStream_t s);
+// stats (nullable): [U][NT * 128] pairs (c_i, 1 / A_i) with c_i = m_i + log2 Z_i,
+// so that the target weight is p_ij = 2^(s_ij log2(e) / sqrt(d) - c_i).
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
-                           int* dev_status, cudaStream_t s);
+                           float* stats, int* dev_status, cudaStream_t s);
 int loss_tc_tile();
+
+// Tensor-core gradient of the summed mimicry loss for bf16 Hedgehog d in
+// {64, 128}: from phi(q), phi(k) and the loss kernel's row stats, per-CTA
+// dW, db shares in `part` (loss_grad_tc_partial_floats floats), then summed
+// per head in a fixed order into dWq, dbq (and dWk, dbk for a separate key map).
+bool loss_grad_tc_shape(const Problem& p);
+bool loss_grad_tc_supported(const Problem& p);
+size_t loss_grad_tc_smem_bytes(const Problem& p);
+size_t loss_grad_tc_partial_floats(const Problem& p);
+cudaError_t launch_loss_grad_tc(const Problem& p, const void* q, const void* k, const void* phq,
+                                const void* phk, const float* stats, float* part, float* dWq,
+                                float* dbq, float* dWk, float* dbk, int* dev_status,
+                                cudaStream_t s);
+// dW[h] = sum x^T dh, db[h] = sum dh over the batch (CUDA cores); with one
+// shared map (dWk null) both sides go into dWq, dbq.
+cudaError_t launch_grad_reduce(const Problem& p, const void* q, const void* k, const float* dhq,
+                               const float* dhk, float* dWq, float* dbq, float* dWk, float* dbk,
+                               cudaStream_t s);
 
 // Decode step (SIMT, HBM-streaming).
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,

@@ -15,7 +15,8 @@
 //     row statistics (softmax max and sum, A_i; kept for the key side), a
 //     second forms g and dL/dh(q)
 //   grad_key_kernel:   per 32-key tile, sweeps the later query tiles for dL/dh(k)
-//   grad_reduce_kernel: dW, db per head (summed over the batch)
+//   grad_reduce_kernel: dW, db per head (summed over the batch); also used
+//     after the tensor-core kernels for bf16
 
 #include <math.h>
 
@@ -308,12 +309,20 @@ cudaError_t grad_t(const Problem& p, const void* q, const void* k, const void* p
   grad_key_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhk, p.d, p.dpp, p.n, ntiles);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_grad_reduce(p, q, k, dhq, dhk, dWq, dbq, dWk, dbk, s);
+}
+
+template <typename T>
+cudaError_t reduce_t(const Problem& p, const void* q, const void* k, const float* dhq,
+                     const float* dhk, float* dWq, float* dbq, float* dWk, float* dbk,
+                     cudaStream_t s) {
   const int nb = (p.d + 31) / 32;
   const unsigned grid = (unsigned)(p.H * nb * nb);
   if (dWk) {   // separate key map: each side to its own parameters
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)q, dhq, (const T*)nullptr, nullptr,
                                                     dWq, dbq, p.B, p.H, p.n, p.d);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)k, dhk, (const T*)nullptr, nullptr,
                                                     dWk, dbk, p.B, p.H, p.n, p.d);
   } else {
@@ -326,6 +335,13 @@ cudaError_t grad_t(const Problem& p, const void* q, const void* k, const void* p
 }  // namespace
 
 size_t loss_grad_smem_bytes(const Problem& p) { return grad_smem_bytes(p.d, p.dpp); }
+
+cudaError_t launch_grad_reduce(const Problem& p, const void* q, const void* k, const float* dhq,
+                               const float* dhk, float* dWq, float* dbq, float* dWk, float* dbk,
+                               cudaStream_t s) {
+  if (p.dtype == HH_F32) return reduce_t<float>(p, q, k, dhq, dhk, dWq, dbq, dWk, dbk, s);
+  return reduce_t<__nv_bfloat16>(p, q, k, dhq, dhk, dWq, dbq, dWk, dbk, s);
+}
 
 cudaError_t launch_loss_grad(const Problem& p, const void* q, const void* k, const void* phq,
                              const void* phk, float* stats, float* dhq, float* dhk, float* dWq,

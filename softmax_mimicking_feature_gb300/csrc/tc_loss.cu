@@ -193,6 +193,7 @@ struct LossArgs {
   CUtensorMap tq, tk, tpq, tpk;
   float* loss_rows;    // [U][n] or null
   float* partial;      // [U][NT]
+  float2* stats;       // [U][NT * 128] (c_i, 1 / A_i) or null; c_i = m_i + log2 Z_i
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -421,6 +422,10 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       const float L = valid ? (logf(At) - 0.69314718055994531f * (Tt / Zt)) : 0.f;
       rl_s[row] = L;
       if (valid && A.loss_rows) A.loss_rows[(size_t)unit * A.n + qi] = L;
+      // row statistics for the gradient: p_ij = 2^(s_ij log2e / sqrt d - c_i)
+      if (A.stats)
+        A.stats[(size_t)unit * A.NT * kTile + qi] =
+            valid ? make_float2(mn + __log2f(Zt), 1.f / At) : make_float2(0.f, 0.f);
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
     if (tid == 0) {
@@ -489,7 +494,7 @@ cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* ph
 template <int D>
 static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, const void* phq,
                              const void* phk, float* loss_rows, float* partial, float* head_sum,
-                             int* dev_status, cudaStream_t s) {
+                             float* stats, int* dev_status, cudaStream_t s) {
   LossArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
@@ -498,6 +503,7 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   if (!ok) return cudaErrorInvalidValue;
   a.loss_rows = loss_rows;
   a.partial = partial;
+  a.stats = reinterpret_cast<float2*>(stats);
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
@@ -517,9 +523,10 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
 
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
-                           int* dev_status, cudaStream_t s) {
-  return p.d == 64 ? loss_tc_t<64>(p, q, k, phq, phk, loss_rows, partial, head_sum, dev_status, s)
-                   : loss_tc_t<128>(p, q, k, phq, phk, loss_rows, partial, head_sum, dev_status, s);
+                           float* stats, int* dev_status, cudaStream_t s) {
+  return p.d == 64
+             ? loss_tc_t<64>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, dev_status, s)
+             : loss_tc_t<128>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, dev_status, s);
 }
 
 int loss_tc_tile() { return kTile; }
