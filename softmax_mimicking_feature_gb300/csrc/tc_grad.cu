@@ -99,8 +99,8 @@ struct GradCfg {
   static constexpr uint32_t OFF_Y = OFF_PX + PX_BYTES;       // 2 stages, D/64 panels of 8 KB
   static constexpr uint32_t OFF_PY = OFF_Y + 2 * Y_BYTES;    // 3 stages, DP/64 panels of 8 KB
   static constexpr uint32_t OFF_ST = OFF_PY + 3 * PY_BYTES;  // 3 stages of 64 (c, 1/A)
-  static constexpr uint32_t OFF_BAR = OFF_ST + 3 * ST_BYTES; // 16 barriers
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 16 * 8;
+  static constexpr uint32_t OFF_BAR = OFF_ST + 3 * ST_BYTES; // 18 barriers
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 18 * 8;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
   // end phase: dL/dh as bf16 hi and lo tiles [128 rows][D] (MN-major, 16 KB
   // panels of 64 columns) over the phi(Y) stages; the ones operand of the db
@@ -110,10 +110,15 @@ struct GradCfg {
   static constexpr uint32_t OFF_ONES = OFF_Y;
   static_assert(2 * DH_BYTES <= 3 * PY_BYTES, "dh tiles exceed the phi(Y) stages");
   static_assert(2 * Y_BYTES >= (D == 64 ? 16384u : 32768u), "ones operand exceeds the Y stages");
-  // TMEM columns: S(s) = 128 s (G(s) over its first 16 columns of each
-  // 32-column half), A(s) = 128 s + 64, dPhi = 256 .. 256 + DP; end phase:
-  // X^T dh at 0 (D columns), for D = 128 also 1^T dh at 128
+  // TMEM columns: S(s) = 128 s, A(s) = 128 s + 64, dPhi = 256 .. 256 + DP.
+  // G(s): D = 64 has room for two stages of its own at 384 + 32 s, so S/A of
+  // step t+2 waits only for the epilogue to have read step t; for D = 128
+  // G(s) goes over the first 16 columns of each 32-column half of S(s) (read
+  // already), and S/A of step t+2 waits for G phi(Y) of step t.
+  // End phase: X^T dh at 0 (D columns), for D = 128 also 1^T dh at 128.
+  static constexpr bool SEP_G = D == 64;
   static constexpr uint32_t TM_ACC = 256;
+  static constexpr uint32_t TM_G = 384;
   static constexpr uint32_t TM_DW = 0, TM_DB = 128;
 };
 
@@ -162,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
   const uint32_t bar_g = bar_x + 88;        // (2) G of TMEM stage s written
   const uint32_t bar_gphi = bar_x + 104;    // (2) G phi(Y) of TMEM stage s done
   const uint32_t bar_acc = bar_x + 120;     // all accumulation done (one barrier)
+  const uint32_t bar_free = bar_x + 128;    // (2) epilogue has read S, A of stage s (SEP_G)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
   // bar_acc is reused for the final dW / db product (phase 1)
@@ -186,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       mbar_init(bar_sa + 8 * s, 1);
       mbar_init(bar_g + 8 * s, 8);
       mbar_init(bar_gphi + 8 * s, 1);
+      mbar_init(bar_free + 8 * s, 8);
     }
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar_py + 8 * s, 1);
@@ -256,9 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         // G: 16 rows of k per step = 8 TMEM columns; the two 32-row halves
         // of the step sit 32 columns apart
 #pragma unroll
-        for (int ks = 0; ks < kST / 16; ++ks)
-          mma_ts(tmem + C::TM_ACC, tmem + 128 * s + 32 * (ks >> 1) + 8 * (ks & 1),
-                 dPYmn + 128 * ks, ID_G, (u > 0 || ks > 0) ? 1 : 0);
+        for (int ks = 0; ks < kST / 16; ++ks) {
+          const uint32_t ga = C::SEP_G ? tmem + C::TM_G + 32 * s + 8 * ks
+                                       : tmem + 128 * s + 32 * (ks >> 1) + 8 * (ks & 1);
+          mma_ts(tmem + C::TM_ACC, ga, dPYmn + 128 * ks, ID_G, (u > 0 || ks > 0) ? 1 : 0);
+        }
         mma_commit(bar_gphi + 8 * s);
         mma_commit(bar_pyfree + 8 * p);
         return true;
@@ -268,8 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         const int s = t & 1, p = t % 3;
         ok = mbar_wait_poll(bar_y + 8 * s, (t >> 1) & 1, wp);
         ok = ok && mbar_wait_poll(bar_py + 8 * p, (t / 3) & 1, wp);
-        // TMEM stage s holds G(t-2) until its G phi(Y) MMAs are done
-        if (ok && t >= 2) ok = mbar_wait_poll(bar_gphi + 8 * s, ((t >> 1) - 1) & 1, wp);
+        // TMEM stage s is free once the epilogue has read S/A(t-2) (SEP_G) or
+        // once G(t-2) written over it has been consumed
+        if (ok && t >= 2)
+          ok = mbar_wait_poll((C::SEP_G ? bar_free : bar_gphi) + 8 * s, ((t >> 1) - 1) & 1, wp);
         if (!ok) break;
         tc_fence_after();
         const uint64_t dY = smem_desc(sb + C::OFF_Y + s * C::Y_BYTES, 16, 1024, 2);
@@ -306,6 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       const uint32_t ts = tmem + lb + 128 * s + 32 * half;
       uint32_t sv[32], av[32];
       tmem_ld32x2(ts, sv, ts + 64, av);
+      if (C::SEP_G) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_free + 8 * s);
+      }
       // admitted columns of this 32-column chunk
       // the key side reads this step's query stats (landed with phi(Y))
       if (side && !mbar_wait(bar_py + 8 * p, (t / 3) & 1, wp)) { ok = false; break; }
@@ -326,8 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         make_g<true>(sv, av, c_row, ia_row, stc, lo, hi, A.s_scale, gw);
       else
         make_g<false>(sv, av, c_row, ia_row, stc, lo, hi, A.s_scale, gw);
-      // G over the first 16 of this half's 32 S columns (already read)
-      tmem_st16(ts, gw);
+      if (C::SEP_G) {
+        // G stage s: free once G phi(Y) of step t-2 is done
+        if (t >= 2 && !mbar_wait(bar_gphi + 8 * s, ((t >> 1) - 1) & 1, wp)) { ok = false; break; }
+        tmem_st16(tmem + lb + C::TM_G + 32 * s + 16 * half, gw);
+      } else {
+        // over the first 16 of this half's 32 S columns (already read)
+        tmem_st16(ts, gw);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
