@@ -9,9 +9,9 @@ every step streams from HBM.  Steps are replayed from CUDA graphs (each step
 is one hh_linattn_fwd_causal call through the C ABI) and timed with CUDA
 events on the launching stream.
 
-The other hot-path rows (Llama-2-shaped prefill and loss, Taylor prefill,
-recurrent decode, the float32 workload) are measured in the same run and
-reported under "rows".
+The other hot-path rows (Llama-2-shaped prefill, Taylor prefill, recurrent
+decode, the float32 workload, the loss and its gradient) are measured in the
+same run and reported under "rows".
 
 ``--impl reference`` times the fp64 CPU oracle on bounded samples of the
 same workload (the baseline arm; no GPU work).
@@ -182,6 +182,20 @@ def loss_counts(w):
     return {"pairs": pairs, "flops": pairs * 2 * (d + dp), "bytes": w.B * w.H * w.n * 2 * d * 2}
 
 
+def grad_counts(w):
+    """Gradient of the summed loss w.r.t. W, b (bf16 Hedgehog).
+
+    Algorithmic FLOP per causal pair: the scores s and a (2d + 2d') once and the
+    two feature-side contractions dPhi(q) += g phi(k), dPhi(k) += g phi(q)
+    (2 x 2d').  Executed: s and a three times (row statistics, query side, key
+    side) plus the two contractions."""
+    d = w.d
+    dp = 2 * d
+    pairs = w.B * w.H * w.n * (w.n + 1) // 2
+    return {"pairs": pairs, "flops": pairs * (2 * d + 2 * dp + 4 * dp),
+            "flops_executed": pairs * (3 * (2 * d + 2 * dp) + 4 * dp)}
+
+
 # ---------------------------------------------------------------------------
 # GPU timing helpers
 # ---------------------------------------------------------------------------
@@ -297,6 +311,16 @@ def bench_loss(torch, hh, wl, w, K, W, dev):
     fns = [lambda: hh.mimicry_loss(fm, x["q"], x["k"], return_rows=False, workspace=ws)]
     ms = time_graphs(torch, fns, K, W)
     return {"ms_total": ms, "K": K, "counts": loss_counts(w)}
+
+
+def bench_grad(torch, hh, wl, w, K, W, dev):
+    x = wl.make_inputs(w, seed=500, device=dev)
+    fm = _fm(hh, w, x)
+    need = hh.loss_grad_workspace_bytes(fm, w.torch_dtype, w.B, w.H, w.n)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    fns = [lambda: hh.mimicry_loss_grad(fm, x["q"], x["k"], workspace=ws)]
+    ms = time_graphs(torch, fns, K, W)
+    return {"ms_total": ms, "K": K, "counts": grad_counts(w)}
 
 
 def e2e_prefill(torch, hh, w, sets, fm, ws, E, dev):
@@ -519,11 +543,25 @@ def other_rows(torch, hh, wl, dev, peaks, l2):
         except Exception as e:
             rows["loss:" + name] = {"error": repr(e)}
         torch.cuda.empty_cache()
+
+    for name in ("llama2_prefill_1x32x4096_d128", "gpt2_prefill_8x12x1024_d64"):
+        try:
+            w = wl.WORKLOADS[name]
+            r = bench_grad(torch, hh, wl, w, 5, 2, dev)
+            s = r["ms_total"] / 1e3 / r["K"]
+            c = r["counts"]
+            rows["grad:" + name] = {"ms_per_call": s * 1e3, "pairs_per_s": c["pairs"] / s,
+                                    "tensor_frac_alg": c["flops"] / s / 1e12 / peaks["bf16_tflops"],
+                                    "tensor_frac_executed":
+                                        c["flops_executed"] / s / 1e12 / peaks["bf16_tflops"]}
+        except Exception as e:
+            rows["grad:" + name] = {"error": repr(e)}
+        torch.cuda.empty_cache()
     return rows
 
 
 def run_row(args):
-    """One hot-path row alone (for profiling): prefill:<workload>, loss:<workload>, decode."""
+    """One hot-path row alone (for profiling): prefill:, loss:, grad:<workload>, or decode."""
     import torch
     import softmax_mimicking_feature_gb300 as hh
     from softmax_mimicking_feature_gb300 import workloads as wl
@@ -542,6 +580,11 @@ def run_row(args):
     elif kind == "loss":
         w = wl.WORKLOADS[name]
         r = bench_loss(torch, hh, wl, w, args.steps, args.warmup, dev)
+        s = r["ms_total"] / 1e3 / args.steps
+        out = {"row": args.row, "us_per_call": s * 1e6, "pairs_per_s": r["counts"]["pairs"] / s}
+    elif kind == "grad":
+        w = wl.WORKLOADS[name]
+        r = bench_grad(torch, hh, wl, w, args.steps, args.warmup, dev)
         s = r["ms_total"] / 1e3 / args.steps
         out = {"row": args.row, "us_per_call": s * 1e6, "pairs_per_s": r["counts"]["pairs"] / s}
     elif kind == "decode":
@@ -569,7 +612,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--row", default=None,
-                    help="time one row alone: prefill:<workload>, loss:<workload> or decode")
+                    help="time one row alone: prefill:<workload>, loss:<workload>, "
+                         "grad:<workload> or decode")
     ap.add_argument("--decode-seqs", type=int, default=0,
                     help="with --row decode: number of sequences (default: the workload's 128)")
     args = ap.parse_args(argv)

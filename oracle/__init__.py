@@ -16,6 +16,7 @@ tiny cases).  Every function has at least one pin; none is "parity unpinned".
 
 from .hedgehog_oracle import (  # noqa: F401
     hedgehog_feature_map,
+    hedgehog_softmax_feature_map,
     taylor2_feature_map,
     taylor2_feature_dim,
     feature_map,
@@ -30,5 +31,8 @@ from .hedgehog_oracle import (  # noqa: F401
     fwd_causal,
     mimicry_loss_grad,
     loss_grad_causal,
+    attention_entropy,
+    mimicry_stats,
+    stats_causal,
     loss_causal,
 )

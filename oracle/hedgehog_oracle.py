@@ -23,6 +23,11 @@ Readings taken where the pages are silent or inconsistent:
 * Taylor map: ``[1, x, (x_i x_j / sqrt2) for i, j in [d]]`` with the pair
   index i-major; the 1/sqrt2 makes phi(q).phi(k) = 1 + q.k + (q.k)^2 / 2.
 * Natural logarithm in the loss; the per-head result is the sum over queries.
+* Softmax-over-features map (Choice 4, Eq. 5): the printed equation
+  normalises exp(w_l . x) over the d learned directions and drops the bias.
+  Choice 3's negation block is kept as in practice, each half normalised over
+  its own d directions: phi = [softmax(x W), softmax(-x W)] (2d features).
+* Entropies use the natural logarithm with 0 log 0 = 0; KL = CE - H(p).
 """
 
 from __future__ import annotations
@@ -33,6 +38,7 @@ import numpy as np
 
 __all__ = [
     "hedgehog_feature_map",
+    "hedgehog_softmax_feature_map",
     "taylor2_feature_map",
     "taylor2_feature_dim",
     "feature_map",
@@ -48,6 +54,9 @@ __all__ = [
     "loss_causal",
     "mimicry_loss_grad",
     "loss_grad_causal",
+    "attention_entropy",
+    "mimicry_stats",
+    "stats_causal",
 ]
 
 
@@ -72,6 +81,24 @@ def hedgehog_feature_map(x, W, b) -> np.ndarray:
     return np.concatenate([np.exp(h), np.exp(-h)], axis=-1)
 
 
+def hedgehog_softmax_feature_map(x, W) -> np.ndarray:
+    """Softmax-over-features Hedgehog map, no bias.
+
+    HH summary, "The Hedgehog MLP Feature Map", Choice 4 (Eq. 5): feature l
+    is exp(w_l . x) / sum_i exp(w_i . x) over the d learned directions (the
+    columns of W); with the negation block of Choice 3 the second half is the
+    same normalisation of exp(-w_l . x).  Returns [..., 2d]
+    = [softmax(x W), softmax(-x W)], each half summing to one.
+    """
+    x, W = _f64(x), _f64(W)
+    h = x @ W
+    pos = np.exp(h)
+    neg = np.exp(-h)
+    pos = pos / pos.sum(axis=-1, keepdims=True)
+    neg = neg / neg.sum(axis=-1, keepdims=True)
+    return np.concatenate([pos, neg], axis=-1)
+
+
 def taylor2_feature_dim(d: int) -> int:
     """d' = 1 + d + d^2 (HH summary, "The Taylor Exponential as a Bridge Result")."""
     return 1 + d + d * d
@@ -91,9 +118,12 @@ def taylor2_feature_map(x) -> np.ndarray:
 
 
 def feature_map(kind: str, x, W=None, b=None) -> np.ndarray:
-    """Dispatch on the map name: ``"hedgehog"`` or ``"taylor2"``."""
+    """Dispatch on the map name: ``"hedgehog"``, ``"hedgehog_softmax"`` (b unused)
+    or ``"taylor2"``."""
     if kind == "hedgehog":
         return hedgehog_feature_map(x, W, b)
+    if kind == "hedgehog_softmax":
+        return hedgehog_softmax_feature_map(x, W)
     if kind == "taylor2":
         return taylor2_feature_map(x)
     raise ValueError(f"unknown feature map {kind!r}")
@@ -260,6 +290,39 @@ def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None):
     return q.T @ dhq, dhq.sum(axis=0), k.T @ dhk, dhk.sum(axis=0)
 
 
+def attention_entropy(weights) -> np.ndarray:
+    """Per-row entropy H(a_i) = -sum_{j<=i} a_ij log a_ij of causal weights.
+
+    HH summary, "The Two Missing Properties as Design Specifications" (the
+    spikiness measure: 0 for one-hot rows, log i for uniform rows).
+    ``weights``: [n, n] row-normalised, zero above the diagonal; 0 log 0 = 0.
+    """
+    w = _f64(weights)
+    n = w.shape[0]
+    out = np.empty(n)
+    for i in range(n):
+        row = w[i, : i + 1]
+        nz = row[row > 0]
+        out[i] = -np.sum(nz * np.log(nz))
+    return out
+
+
+def mimicry_stats(q, k, phi_q, phi_k) -> np.ndarray:
+    """Per-query [CE, KL, H(p), H(w)] for one head.
+
+    CE is paper Eq. 4 (mimicry_loss); H(p) and H(w) are the entropies of the
+    softmax target and of the linear-attention weights (spikiness, as above);
+    KL(p || w) = CE - H(p), the divergence named next to the cross-entropy in
+    the HH digest (section A.3, attention distillation).  Returns [n, 4].
+    """
+    p = softmax_target(q, k)
+    w = causal_weights(phi_q, phi_k)
+    ce = mimicry_loss(q, k, phi_q, phi_k)
+    hp = attention_entropy(p)
+    hw = attention_entropy(w)
+    return np.stack([ce, ce - hp, hp, hw], axis=-1)
+
+
 # ---------------------------------------------------------------------------
 # Batched wrappers over [B, H, n, d] inputs (per-head maps W[H], b[H])
 # ---------------------------------------------------------------------------
@@ -267,6 +330,8 @@ def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None):
 def _map_head(kind, x, W, b, h):
     if kind == "hedgehog":
         return hedgehog_feature_map(x, W[h], b[h])
+    if kind == "hedgehog_softmax":
+        return hedgehog_softmax_feature_map(x, W[h])
     return taylor2_feature_map(x)
 
 
@@ -294,6 +359,19 @@ def loss_causal(kind, q, k, W=None, b=None):
             pk = _map_head(kind, k[bi, h], W, b, h)
             rows[bi, h] = mimicry_loss(q[bi, h], k[bi, h], pq, pk)
     return rows, rows.sum(axis=-1)
+
+
+def stats_causal(kind, q, k, W=None, b=None):
+    """Per-row [CE, KL, H(p), H(w)] for every (batch, head): [B, H, n, 4]."""
+    q, k = _f64(q), _f64(k)
+    B, H, n = q.shape[:3]
+    out = np.empty((B, H, n, 4))
+    for bi in range(B):
+        for h in range(H):
+            pq = _map_head(kind, q[bi, h], W, b, h)
+            pk = _map_head(kind, k[bi, h], W, b, h)
+            out[bi, h] = mimicry_stats(q[bi, h], k[bi, h], pq, pk)
+    return out
 
 
 def loss_grad_causal(q, k, W, b, Wk=None, bk=None):

@@ -250,11 +250,88 @@ def check_loss_grad_finite_differences(O, golden):
         assert abs(f - db[h, 1]) <= 1e-6 * max(1.0, abs(f))
 
 
+def check_softmax_feature_map(O, golden):
+    """Choice 4 (Eq. 5): softmax over the d learned directions, bias omitted."""
+    rng = np.random.default_rng(21)
+    n, d = 5, 4
+    x = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, d)) * 0.8
+    b = rng.normal(size=d)
+    phi = O.feature_map("hedgehog_softmax", x, W, b)
+    assert phi.shape == (n, 2 * d)
+    # Eq. 5 written out feature by feature, for both signs of the directions
+    for i in range(n):
+        for sign, off in ((1.0, 0), (-1.0, d)):
+            dots = [sign * sum(W[kk, l] * x[i, kk] for kk in range(d)) for l in range(d)]
+            den = sum(math.exp(t) for t in dots)
+            for l in range(d):
+                assert abs(phi[i, off + l] - math.exp(dots[l]) / den) <= 1e-14
+    # each half is a distribution over the directions; the bias is not used
+    np.testing.assert_allclose(phi[:, :d].sum(-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(phi[:, d:].sum(-1), 1.0, rtol=1e-14)
+    np.testing.assert_array_equal(phi, O.feature_map("hedgehog_softmax", x, W, 0 * b))
+    # adding the same projection to every direction changes nothing
+    u = rng.normal(size=d)
+    np.testing.assert_allclose(O.hedgehog_softmax_feature_map(x, W + u[:, None]), phi, rtol=1e-12)
+    # x = 0: uniform over the directions
+    np.testing.assert_allclose(O.hedgehog_softmax_feature_map(np.zeros((2, d)), W), 1.0 / d, rtol=1e-15)
+
+
+def check_entropies_and_kl(O, golden):
+    """H(a_i) of the spikiness section, KL = CE - H(p) (Gibbs), known extremes."""
+    n = 7
+    # uniform rows: log i; one-hot rows: 0
+    U = np.tril(np.ones((n, n))) / np.arange(1, n + 1)[:, None]
+    np.testing.assert_allclose(O.attention_entropy(U), np.log(np.arange(1, n + 1)), rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(O.attention_entropy(np.eye(n)), 0.0, atol=1e-15)
+    rng = np.random.default_rng(5)
+    d = 3
+    q, k = rng.normal(size=(2, n, d))
+    # weights equal to the target: phi(k_j) = e_j, phi(q_i)_j = exp(q_i . k_j / sqrt d)
+    pk = np.eye(n)
+    pq = np.exp(q @ k.T / math.sqrt(d))
+    st = O.mimicry_stats(q, k, pq, pk)
+    p = O.softmax_target(q, k)
+    Hp = -np.sum(np.where(p > 0, p * np.log(np.where(p > 0, p, 1.0)), 0.0), axis=-1)
+    np.testing.assert_allclose(st[:, 1], 0.0, atol=1e-13)
+    np.testing.assert_allclose(st[:, 0], Hp, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(st[:, 2], Hp, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(st[:, 3], Hp, rtol=1e-12, atol=1e-14)
+    # a generic map: KL written directly as sum p log(p / w), and non-negative
+    W = rng.normal(size=(d, d)) * 0.6
+    bb = rng.normal(size=d) * 0.2
+    pq, pk = O.feature_map("hedgehog", q, W, bb), O.feature_map("hedgehog", k, W, bb)
+    st = O.mimicry_stats(q, k, pq, pk)
+    a = np.tril(pq @ pk.T)
+    w = a / a.sum(-1, keepdims=True)
+    kl = np.array([sum(p[i, j] * math.log(p[i, j] / w[i, j]) for j in range(i + 1)) for i in range(n)])
+    np.testing.assert_allclose(st[:, 1], kl, rtol=1e-10, atol=1e-13)
+    assert np.all(st[:, 1] >= -1e-13)
+    np.testing.assert_allclose(st[:, 0], O.mimicry_loss(q, k, pq, pk), rtol=1e-13)
+    # W = 0, b = 0: uniform linear-attention weights, H(w) = log i
+    p0 = O.feature_map("hedgehog", q, np.zeros((d, d)), np.zeros(d))
+    st0 = O.mimicry_stats(q, k, p0, p0)
+    np.testing.assert_allclose(st0[:, 3], np.log(np.arange(1, n + 1)), rtol=1e-13, atol=1e-15)
+    # batched wrapper agrees per head
+    B, H = 2, 2
+    qb = rng.normal(size=(B, H, 5, d))
+    kb = rng.normal(size=(B, H, 5, d))
+    Wb = rng.normal(size=(H, d, d)) * 0.5
+    bbb = rng.normal(size=(H, d)) * 0.2
+    sb = O.stats_causal("hedgehog_softmax", qb, kb, Wb, bbb)
+    for bi in range(B):
+        for h in range(H):
+            ph_q = O.hedgehog_softmax_feature_map(qb[bi, h], Wb[h])
+            ph_k = O.hedgehog_softmax_feature_map(kb[bi, h], Wb[h])
+            np.testing.assert_allclose(sb[bi, h], O.mimicry_stats(qb[bi, h], kb[bi, h], ph_q, ph_k),
+                                       rtol=1e-14)
+
+
 PINS = [check_hand_worked, check_taylor_closed_form, check_hedgehog_cosh,
         check_identity_and_zero_maps, check_orientation, check_weight_rows,
         check_constant_values_and_first_row, check_uniform_cases,
         check_quadratic_vs_recurrent, check_softmax_target, check_loss_properties,
-        check_loss_grad_finite_differences]
+        check_loss_grad_finite_differences, check_softmax_feature_map, check_entropies_and_kl]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -288,6 +365,16 @@ MUTANTS = {
     "grad_no_key_side": ("k.T @ dhk, dhk.sum(axis=0)\n", "0 * (k.T @ dhk), 0 * dhk.sum(axis=0)\n"),
     "grad_W_transposed": ("return q.T @ dhq, dhq.sum(axis=0)", "return (q.T @ dhq).T, dhq.sum(axis=0)"),
     "grad_acausal": ("g = np.where(mask, 1.0 / A", "g = np.where(True, 1.0 / A"),
+    "softmax_map_over_rows": ("pos = pos / pos.sum(axis=-1, keepdims=True)",
+                              "pos = pos / pos.sum(axis=0, keepdims=True)"),
+    "softmax_map_shared_normaliser": ("neg = neg / neg.sum(axis=-1, keepdims=True)",
+                                      "neg = neg / pos.sum(axis=-1, keepdims=True)"),
+    "softmax_map_negation_dropped": ("    neg = np.exp(-h)\n", "    neg = np.exp(h)\n"),
+    "softmax_map_raw_dispatch": ("return hedgehog_softmax_feature_map(x, W)\n",
+                                 "return hedgehog_feature_map(x, W, b)\n"),
+    "entropy_log2": ("out[i] = -np.sum(nz * np.log(nz))", "out[i] = -np.sum(nz * np.log2(nz))"),
+    "kl_sign_flipped": ("np.stack([ce, ce - hp, hp, hw]", "np.stack([ce, hp - ce, hp, hw]"),
+    "model_entropy_of_target": ("hw = attention_entropy(w)", "hw = attention_entropy(p)"),
 }
 
 
