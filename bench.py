@@ -200,9 +200,12 @@ def grad_counts(w):
 # GPU timing helpers
 # ---------------------------------------------------------------------------
 
-def _fm(hh, w, x):
-    if w.kind == "hedgehog":
+def _fm(hh, w, x, kind=None):
+    kind = kind or w.kind
+    if kind == "hedgehog":
         return hh.FeatureMap("hedgehog", w.d, x["W"], x["b"])
+    if kind == "hedgehog_softmax":
+        return hh.FeatureMap("hedgehog_softmax", w.d, x["W"])
     return hh.FeatureMap("taylor2", w.d)
 
 
@@ -266,13 +269,13 @@ def n_rotation(bytes_per_set, l2_bytes):
 # rows
 # ---------------------------------------------------------------------------
 
-def bench_prefill(torch, hh, wl, w, K, W, dev, sampler=None, dist=None, l2=0):
+def bench_prefill(torch, hh, wl, w, K, W, dev, sampler=None, dist=None, l2=0, kind=None):
     cnt = prefill_counts(w)
     esz = 4 if w.dtype == "f32" else 2
     per_set = cnt["bytes"]
     R = n_rotation(per_set, l2)
     sets = [wl.make_inputs(w, seed=100 + i, device=dev) for i in range(R)]
-    fm = _fm(hh, w, sets[0])
+    fm = _fm(hh, w, sets[0], kind)
     ys = [torch.empty_like(x["q"]) for x in sets]
     need = hh.fwd_workspace_bytes(fm, w.torch_dtype, w.B, w.H, w.n, w.chunk)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -500,23 +503,26 @@ def run_ours(args):
 def other_rows(torch, hh, wl, dev, peaks, l2):
     rows = {}
 
-    def prefill_row(name, K):
+    def prefill_row(name, K, kind=None):
         w = wl.WORKLOADS[name]
-        r = bench_prefill(torch, hh, wl, w, K, 3, dev, l2=l2)
+        r = bench_prefill(torch, hh, wl, w, K, 3, dev, l2=l2, kind=kind)
         s = r["ms_total"] / 1e3 / K
         c = r["counts"]
-        rows[name] = {"tokens_per_s": w.B * w.n / s, "ms_per_call": s * 1e3,
+        rows[(kind + ":" if kind else "") + name] = {"tokens_per_s": w.B * w.n / s, "ms_per_call": s * 1e3,
                       "hbm_gbs_alg": c["bytes"] / s / 1e9,
                       "hbm_frac": c["bytes"] / s / 1e9 / peaks["hbm_gbs"],
                       "tensor_frac_alg": c["flops"] / s / 1e12 / peaks["bf16_tflops"],
                       "segments": r["segments"], "launches": r["launches"]}
 
-    for name, K in (("llama2_prefill_1x32x4096_d128", 20), ("taylor2_prefill_4x8x8192_d16", 20),
-                    ("hedgehog_f32_1x1x256_d64", 50)):
+    for name, K, kind in (("llama2_prefill_1x32x4096_d128", 20, None),
+                          ("taylor2_prefill_4x8x8192_d16", 20, None),
+                          ("hedgehog_f32_1x1x256_d64", 50, None),
+                          ("gpt2_prefill_8x12x1024_d64", 200, "hedgehog_softmax"),
+                          ("llama2_prefill_1x32x4096_d128", 20, "hedgehog_softmax")):
         try:
-            prefill_row(name, K)
+            prefill_row(name, K, kind)
         except Exception as e:  # report, do not hide
-            rows[name] = {"error": repr(e)}
+            rows[(kind + ":" if kind else "") + name] = {"error": repr(e)}
         torch.cuda.empty_cache()
 
     try:
@@ -561,7 +567,8 @@ def other_rows(torch, hh, wl, dev, peaks, l2):
 
 
 def run_row(args):
-    """One hot-path row alone (for profiling): prefill:, loss:, grad:<workload>, or decode."""
+    """One hot-path row alone (for profiling): prefill:, softmax_prefill:, loss:,
+    grad:<workload>, or decode."""
     import torch
     import softmax_mimicking_feature_gb300 as hh
     from softmax_mimicking_feature_gb300 import workloads as wl
@@ -571,9 +578,10 @@ def run_row(args):
     _abi.lib()
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2**20)
     kind, _, name = args.row.partition(":")
-    if kind == "prefill":
+    if kind in ("prefill", "softmax_prefill"):
         w = wl.WORKLOADS[name]
-        r = bench_prefill(torch, hh, wl, w, args.steps, args.warmup, dev, l2=l2)
+        r = bench_prefill(torch, hh, wl, w, args.steps, args.warmup, dev, l2=l2,
+                          kind="hedgehog_softmax" if kind == "softmax_prefill" else None)
         s = r["ms_total"] / 1e3 / args.steps
         out = {"row": args.row, "us_per_call": s * 1e6, "tokens_per_s": w.B * w.n / s,
                "hbm_gbs_alg": r["counts"]["bytes"] / s / 1e9, "segments": r["segments"]}

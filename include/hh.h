@@ -85,11 +85,24 @@ typedef enum {
 
 typedef enum { HH_F32 = 0, HH_BF16 = 1 } hh_dtype;
 
-typedef enum { HH_FMAP_HEDGEHOG = 0, HH_FMAP_TAYLOR2 = 1 } hh_fmap_kind;
+/* HH_FMAP_HEDGEHOG: [exp(xW + b); exp(-(xW + b))] ("The Hedgehog MLP
+ *   Feature Map", Choices 1 and 3).
+ * HH_FMAP_TAYLOR2: [1, x, vec(x x^T) / sqrt 2] ("The Taylor Exponential as a
+ *   Bridge Result").
+ * HH_FMAP_HEDGEHOG_SOFTMAX: [softmax(xW); softmax(-xW)], each half a softmax
+ *   over the d learned directions, no bias (Choice 4, Eq. 5, with the
+ *   negation block of Choice 3 normalised the same way).  bq and bk must be
+ *   NULL.  Every call that takes a Hedgehog map takes this one except
+ *   hh_mimicry_loss_grad. */
+typedef enum {
+  HH_FMAP_HEDGEHOG = 0,
+  HH_FMAP_TAYLOR2 = 1,
+  HH_FMAP_HEDGEHOG_SOFTMAX = 2
+} hh_fmap_kind;
 
-/* A per-layer feature map.  For Hedgehog, Wq/bq map the queries and Wk/bk
- * the keys; Wk == NULL means the keys share Wq/bq (one map per head used for
- * both queries and keys, as the pages describe).  Taylor ignores W and b. */
+/* A per-layer feature map.  For the Hedgehog kinds, Wq/bq map the queries and
+ * Wk/bk the keys; Wk == NULL means the keys share Wq/bq (one map per head used
+ * for both queries and keys, as the pages describe).  Taylor ignores W and b. */
 typedef struct {
   int32_t kind;        /* hh_fmap_kind                                      */
   int32_t d;           /* head dimension                                    */
@@ -105,7 +118,7 @@ HH_API int hh_version(void);
 /* Human-readable name of a status code (static string, never NULL). */
 HH_API const char* hh_status_str(int status);
 
-/* Feature dimension d' of a map: 2d (Hedgehog) or 1+d+d^2 (Taylor, the
+/* Feature dimension d' of a map: 2d (Hedgehog kinds) or 1+d+d^2 (Taylor, the
  * count printed in "The Taylor Exponential as a Bridge Result").  With
  * padded != 0 the Taylor count is rounded up to a multiple of 32.  Returns
  * -1 for an unknown kind or d < 1. */
@@ -116,7 +129,8 @@ HH_API int hh_fmap_dim(int kind, int d, int padded);
  * "The Taylor Exponential as a Bridge Result" (Taylor).
  * x: [B][H][n][d] (dtype); is_key selects Wk/bk instead of Wq/bq;
  * phi_out: [B][H][n][d'p] (dtype), fully overwritten including padding.
- * Hedgehog output order: feature l < d is exp(h_l), feature d + l is exp(-h_l). */
+ * Hedgehog output order: feature l < d is exp(h_l), feature d + l is exp(-h_l);
+ * the softmax kind divides each half by its sum over l. */
 HH_API hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, int is_key,
                          int64_t B, int H, int64_t n, void* phi_out, void* stream);
 
@@ -176,7 +190,7 @@ HH_API hh_status hh_linattn_decode_step(const hh_fmap* fmap, int dtype, const vo
                                  const void* v, int64_t B, int H, float* S, float* z, void* y,
                                  void* stream);
 
-/* Bytes of device workspace hh_mimicry_loss needs (0 when none). */
+/* Bytes of device workspace hh_mimicry_loss and hh_mimicry_stats need (0 when none). */
 HH_API size_t hh_loss_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n);
 
 /* Attention-weight distillation cross-entropy (paper Eq. 4) per query.
@@ -189,6 +203,21 @@ HH_API size_t hh_loss_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B,
 HH_API hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const void* k,
                           int64_t B, int H, int64_t n, float* loss_rows, float* loss_head_sum,
                           void* workspace, size_t ws_bytes, int* dev_status, void* stream);
+
+/* Per-query attention statistics next to the loss, one float4 per row:
+ *   [0] CE_i    the cross-entropy of hh_mimicry_loss (paper Eq. 4)
+ *   [1] KL_i    KL(p_i || w_i) = CE_i - H(p_i), the divergence the HH digest
+ *               (section A.3, attention distillation) names beside CE
+ *   [2] H(p_i)  entropy of the causal softmax target
+ *   [3] H(w_i)  entropy of the linear-attention weights w_ij = a_ij / A_i
+ * (entropies as in "The Two Missing Properties as Design Specifications":
+ * -sum_j w log w, natural log).
+ * q, k: [B][H][n][d] (dtype); stats_rows: [B][H][n][4] float32, 16-byte
+ * aligned, overwritten.  workspace: at least hh_loss_workspace_bytes(...). */
+HH_API hh_status hh_mimicry_stats(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                  int64_t B, int H, int64_t n, float* stats_rows,
+                                  void* workspace, size_t ws_bytes, int* dev_status,
+                                  void* stream);
 
 /* Bytes of device workspace hh_mimicry_loss_grad needs (0 when none). */
 HH_API size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H,

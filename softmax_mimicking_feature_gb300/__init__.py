@@ -17,4 +17,5 @@ from .api import (  # noqa: F401
     loss_grad_workspace_bytes,
     mimicry_loss,
     mimicry_loss_grad,
+    mimicry_stats,
 )

@@ -15,12 +15,12 @@ from . import build as _build
 HH_OK, HH_ERR_INVALID_ARG, HH_ERR_UNSUPPORTED, HH_ERR_ALIGNMENT = 0, 1, 2, 3
 HH_ERR_WORKSPACE, HH_ERR_CUDA, HH_ERR_TIMEOUT = 4, 5, 6
 HH_F32, HH_BF16 = 0, 1
-HH_FMAP_HEDGEHOG, HH_FMAP_TAYLOR2 = 0, 1
+HH_FMAP_HEDGEHOG, HH_FMAP_TAYLOR2, HH_FMAP_HEDGEHOG_SOFTMAX = 0, 1, 2
 
 EXPORTED = ("hh_version", "hh_status_str", "hh_fmap_dim", "hh_feature_map",
             "hh_fwd_workspace_bytes", "hh_fwd_plan", "hh_linattn_fwd_causal", "hh_linattn_decode_step",
             "hh_loss_workspace_bytes", "hh_mimicry_loss", "hh_linattn_fwd_causal_noalloc",
-            "hh_loss_grad_workspace_bytes", "hh_mimicry_loss_grad")
+            "hh_loss_grad_workspace_bytes", "hh_mimicry_loss_grad", "hh_mimicry_stats")
 
 
 class HHFmap(ctypes.Structure):
@@ -56,6 +56,7 @@ _SIGS = {
     "hh_linattn_fwd_causal_noalloc": ([_P, _i32, _vp, _vp, _vp, _i64, _i32, _i64, _i32, _vp, _vp,
                                        _vp, _vp, _vp], _i32),
     "hh_loss_grad_workspace_bytes": ([_P, _i32, _i64, _i32, _i64], _sz),
+    "hh_mimicry_stats": ([_P, _i32, _vp, _vp, _i64, _i32, _i64, _vp, _vp, _sz, _vp, _vp], _i32),
     "hh_mimicry_loss_grad": ([_P, _i32, _vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _sz,
                               _vp, _vp], _i32),
 }

@@ -17,11 +17,14 @@ from . import _abi
 
 __all__ = ["FeatureMap", "fmap_dim", "feature_map", "fwd_workspace_bytes", "fwd_plan",
            "linattn_fwd_causal", "linattn_decode_step", "loss_workspace_bytes",
-           "mimicry_loss", "loss_grad_workspace_bytes", "mimicry_loss_grad", "HHError"]
+           "mimicry_loss", "mimicry_stats", "loss_grad_workspace_bytes", "mimicry_loss_grad",
+           "HHError"]
 
 HHError = _abi.HHError
 
 _DTYPES = {torch.float32: _abi.HH_F32, torch.bfloat16: _abi.HH_BF16}
+_KINDS = {"hedgehog": _abi.HH_FMAP_HEDGEHOG, "taylor2": _abi.HH_FMAP_TAYLOR2,
+          "hedgehog_softmax": _abi.HH_FMAP_HEDGEHOG_SOFTMAX}
 
 
 def _dt(t: torch.Tensor) -> int:
@@ -49,7 +52,9 @@ def _stream(stream) -> ctypes.c_void_p:
 
 @dataclass
 class FeatureMap:
-    """A per-layer feature map: kind "hedgehog" (W [H,d,d], b [H,d]) or "taylor2"."""
+    """A per-layer feature map: kind "hedgehog" (W [H,d,d], b [H,d]),
+    "hedgehog_softmax" (W only: softmax over the d directions of each sign)
+    or "taylor2"."""
     kind: str
     d: int
     Wq: Optional[torch.Tensor] = None
@@ -59,7 +64,7 @@ class FeatureMap:
 
     @property
     def kind_id(self) -> int:
-        return {"hedgehog": _abi.HH_FMAP_HEDGEHOG, "taylor2": _abi.HH_FMAP_TAYLOR2}[self.kind]
+        return _KINDS[self.kind]
 
     def struct(self) -> _abi.HHFmap:
         s = _abi.HHFmap()
@@ -76,7 +81,7 @@ class FeatureMap:
 
 
 def fmap_dim(kind: str, d: int, padded: bool = True) -> int:
-    k = {"hedgehog": _abi.HH_FMAP_HEDGEHOG, "taylor2": _abi.HH_FMAP_TAYLOR2}[kind]
+    k = _KINDS[kind]
     return int(_abi.lib().hh_fmap_dim(k, int(d), int(bool(padded))))
 
 
@@ -170,6 +175,23 @@ def mimicry_loss(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, return_rows: 
         ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), B, H, n, _ptr(rows), _ptr(head),
         _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)), "hh_mimicry_loss")
     return rows, head
+
+
+def mimicry_stats(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
+                  workspace: Optional[torch.Tensor] = None,
+                  dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Per-query (CE, KL, H(p), H(w)) as float32 [B, H, n, 4] (hh_mimicry_stats)."""
+    B, H, n, d = q.shape
+    out = torch.empty(B, H, n, 4, dtype=torch.float32, device=q.device)
+    need = loss_workspace_bytes(fm, q.dtype, B, H, n)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_mimicry_stats(
+        ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), B, H, n, _ptr(out), _ptr(workspace), ws_bytes,
+        _ptr(dev_status), _stream(stream)), "hh_mimicry_stats")
+    return out
 
 
 def loss_grad_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int) -> int:

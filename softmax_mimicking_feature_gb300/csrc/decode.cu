@@ -34,12 +34,13 @@ __global__ void __launch_bounds__(kDecThreads)
 decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
               float* __restrict__ S, float* __restrict__ z, T* __restrict__ y,
               const T* __restrict__ Wq, const float* __restrict__ bq,
-              const T* __restrict__ Wk, const float* __restrict__ bk, int kind, int d, int dpp,
-              int H) {
+              const T* __restrict__ Wk, const float* __restrict__ bk, int kind, int softmax,
+              int d, int dpp, int H) {
   __shared__ float qs[128], ks[128], vs[128];
   __shared__ float phq[320], phk[320];
   __shared__ __align__(16) float ypart[kDecThreads * 4];
   __shared__ float dpart[kDecThreads / 32];
+  __shared__ float lse[2][2];   // softmax map: (c+, c-) of the query and of the key
 
   const int64_t u = blockIdx.x;  // (sequence, head) unit
   const int h = (int)(u % H);
@@ -63,8 +64,50 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
       float hv = bb ? bb[(size_t)h * d + l] : 0.f;
       for (int kk = 0; kk < d; ++kk) hv = fmaf(xs[kk], to_f(Wh[(size_t)kk * d + l]), hv);
       float* out = key ? phk : phq;
-      out[l] = expf(hv);
-      out[d + l] = expf(-hv);
+      if (softmax) {
+        out[l] = hv;
+      } else {
+        out[l] = expf(hv);
+        out[d + l] = expf(-hv);
+      }
+    }
+    if (softmax) {
+      // "The Hedgehog MLP Feature Map", Choice 4 (Eq. 5): each half divided by
+      // its sum over the d directions; warp 0 reduces the query, warp 4 the key
+      __syncthreads();
+      const int warp = tid >> 5, lane = tid & 31;
+      if (warp == 0 || warp == 4) {
+        const float* hs = warp ? phk : phq;
+        float mx = -INFINITY, mn = INFINITY;
+        for (int i = lane; i < d; i += 32) {
+          mx = fmaxf(mx, hs[i]);
+          mn = fminf(mn, hs[i]);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        float sp = 0.f, sn = 0.f;
+        for (int i = lane; i < d; i += 32) {
+          sp += expf(hs[i] - mx);
+          sn += expf(mn - hs[i]);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          sp += __shfl_xor_sync(0xffffffffu, sp, o);
+          sn += __shfl_xor_sync(0xffffffffu, sn, o);
+        }
+        if (lane == 0) {
+          lse[warp ? 1 : 0][0] = mx + logf(sp);
+          lse[warp ? 1 : 0][1] = logf(sn) - mn;
+        }
+      }
+      __syncthreads();
+      if (l < d) {
+        float* out = key ? phk : phq;
+        const float hv = out[l];
+        out[l] = expf(hv - lse[key][0]);
+        out[d + l] = expf(-hv - lse[key][1]);
+      }
     }
   } else {
     for (int f = tid; f < dpp; f += kDecThreads) {
@@ -159,11 +202,11 @@ static cudaError_t decode_t(const Problem& p, const void* q, const void* k, cons
   if (p.d % 4 == 0)
     decode_kernel<T, 4><<<(unsigned)units, kDecThreads, 0, s>>>(
         (const T*)q, (const T*)k, (const T*)v, S, z, (T*)y, (const T*)p.Wq, p.bq, Wk, bk,
-        p.kind, p.d, p.dpp, p.H);
+        p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H);
   else
     decode_kernel<T, 1><<<(unsigned)units, kDecThreads, 0, s>>>(
         (const T*)q, (const T*)k, (const T*)v, S, z, (T*)y, (const T*)p.Wq, p.bq, Wk, bk,
-        p.kind, p.d, p.dpp, p.H);
+        p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H);
   return cudaGetLastError();
 }
 

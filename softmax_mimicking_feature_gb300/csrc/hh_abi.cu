@@ -69,13 +69,17 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 hh_status make_problem(const hh_fmap* fm, int dtype, int64_t B, int H, int64_t n, Problem* p) {
   if (!fm) return HH_ERR_INVALID_ARG;
   if (dtype != HH_F32 && dtype != HH_BF16) return HH_ERR_INVALID_ARG;
-  if (fm->kind != HH_FMAP_HEDGEHOG && fm->kind != HH_FMAP_TAYLOR2) return HH_ERR_INVALID_ARG;
+  if (fm->kind != HH_FMAP_HEDGEHOG && fm->kind != HH_FMAP_TAYLOR2 &&
+      fm->kind != HH_FMAP_HEDGEHOG_SOFTMAX)
+    return HH_ERR_INVALID_ARG;
   if (B < 0 || n < 0 || H < 1 || fm->d < 1) return HH_ERR_INVALID_ARG;
   const int d = fm->d;
-  if (fm->kind == HH_FMAP_HEDGEHOG) {
+  const bool softmax = fm->kind == HH_FMAP_HEDGEHOG_SOFTMAX;
+  if (fm->kind == HH_FMAP_HEDGEHOG || softmax) {
     const bool ok = dtype == HH_F32 ? (d <= 128) : (d == 64 || d == 128);
     if (!ok) return HH_ERR_UNSUPPORTED;
     if (!fm->Wq) return HH_ERR_INVALID_ARG;
+    if (softmax && (fm->bq || fm->bk)) return HH_ERR_INVALID_ARG;   // Eq. 5 has no bias
   } else {
     const bool ok = dtype == HH_F32 ? (d <= 16) : (d == 16);
     if (!ok) return HH_ERR_UNSUPPORTED;
@@ -85,15 +89,17 @@ hh_status make_problem(const hh_fmap* fm, int dtype, int64_t B, int H, int64_t n
   if (B > lim || n > lim || (B && n && B * (int64_t)H > lim / std::max<int64_t>(n, 1)) ||
       B * (int64_t)H * n > lim / 512)
     return HH_ERR_INVALID_ARG;
-  p->kind = fm->kind;
+  p->kind = softmax ? HH_FMAP_HEDGEHOG : fm->kind;
+  p->softmax = softmax;
+  p->offq = p->offk = nullptr;
   p->dtype = dtype;
   p->d = d;
-  p->dp = hh_fmap_dim(fm->kind, d, 0);
-  p->dpp = hh_fmap_dim(fm->kind, d, 1);
+  p->dp = hh_fmap_dim(p->kind, d, 0);
+  p->dpp = hh_fmap_dim(p->kind, d, 1);
   p->B = B;
   p->H = H;
   p->n = n;
-  if (fm->kind == HH_FMAP_HEDGEHOG) {
+  if (p->kind == HH_FMAP_HEDGEHOG) {
     p->Wq = fm->Wq;
     p->bq = fm->bq;
     p->Wk = fm->Wk;
@@ -116,6 +122,11 @@ hh_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HH_OK : HH_ERR_
 size_t elem_size(int dtype) { return dtype == HH_F32 ? 4 : 2; }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Bytes of one softmax-map offset array ([U][off_stride(n)] float2).
+size_t softmax_off_bytes(const Problem& p) {
+  return align256((size_t)p.B * p.H * off_stride(p.n) * sizeof(float2));
+}
+
 bool device_ok() {
   // sm_103a code only; anything else is reported, not attempted
   return device_cc() == 103;
@@ -124,7 +135,10 @@ bool device_ok() {
 // Loss workspace: phi(Q), phi(K) in the call's dtype, then per-tile partial sums.
 size_t loss_ws(const Problem& p) {
   const size_t phi = align256((size_t)p.B * p.H * p.n * p.dpp * elem_size(p.dtype));
-  const size_t part = align256((size_t)p.B * p.H * ceil_div(p.n, loss_simt_tile()) * sizeof(float));
+  // per-tile partial sums (64-row tiles cover the 128-row ones), then the
+  // per-head sums when the caller passes none (statistics only)
+  const size_t part = align256((size_t)p.B * p.H * (ceil_div(p.n, loss_simt_tile()) + 1) *
+                               sizeof(float));
   return 2 * phi + part;
 }
 
@@ -152,7 +166,7 @@ const char* hh_status_str(int s) {
 
 int hh_fmap_dim(int kind, int d, int padded) {
   if (d < 1) return -1;
-  if (kind == HH_FMAP_HEDGEHOG) return 2 * d;
+  if (kind == HH_FMAP_HEDGEHOG || kind == HH_FMAP_HEDGEHOG_SOFTMAX) return 2 * d;
   if (kind == HH_FMAP_TAYLOR2) {
     const int dp = 1 + d + d * d;
     return padded ? (dp + 31) / 32 * 32 : dp;
@@ -172,8 +186,9 @@ hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, int is_k
   if ((st = check_ptrs_aligned({x, phi_out, W, b})) != HH_OK) return st;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;
   if (fmap_tc_supported(p))
-    return cuda_status(launch_fmap_tc(p, x, is_key, phi_out, nullptr, (cudaStream_t)stream));
-  return cuda_status(launch_fmap_simt(p, x, is_key, phi_out, (cudaStream_t)stream));
+    return cuda_status(
+        launch_fmap_tc(p, x, is_key, phi_out, nullptr, nullptr, (cudaStream_t)stream));
+  return cuda_status(launch_fmap_simt(p, x, is_key, phi_out, nullptr, (cudaStream_t)stream));
 }
 
 size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
@@ -183,7 +198,9 @@ size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, 
   (void)chunk;
   if (B * H * n == 0) return 0;
   const TcPlan pl = plan_prefill_tc(p);
-  return pl.supported ? align256(pl.ws_bytes) : 0;
+  if (!pl.supported) return 0;
+  // softmax map: the q and k row offsets follow the segment states
+  return align256(pl.ws_bytes) + (p.softmax ? 2 * softmax_off_bytes(p) : 0);
 }
 
 hh_status hh_fwd_plan(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n, int chunk,
@@ -234,8 +251,19 @@ hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, c
     return HH_OK;
   }
   const TcPlan pl = plan_prefill_tc(p);
-  if (pl.supported)
+  if (pl.supported) {
+    if (p.softmax) {
+      // per-row offsets of the softmax map, from the feature-map kernel
+      char* ob = (char*)workspace + align256(pl.ws_bytes);
+      float2* offq = (float2*)ob;
+      float2* offk = (float2*)(ob + softmax_off_bytes(p));
+      cudaError_t e = launch_fmap_tc_qk(p, q, k, nullptr, nullptr, offq, offk, dev_status, s);
+      if (e != cudaSuccess) return cuda_status(e);
+      p.offq = offq;
+      p.offk = offk;
+    }
     return cuda_status(launch_prefill_tc(p, pl, q, k, v, y, S_out, z_out, workspace, dev_status, s));
+  }
   return cuda_status(launch_prefill_simt(p, q, k, v, y, S_out, z_out, s));
 }
 
@@ -259,16 +287,18 @@ size_t hh_loss_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H,
   return loss_ws(p);
 }
 
-hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const void* k, int64_t B,
-                          int H, int64_t n, float* loss_rows, float* loss_head_sum,
-                          void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+// Shared body of hh_mimicry_loss and hh_mimicry_stats.
+static hh_status mimicry_loss_impl(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                   int64_t B, int H, int64_t n, float* loss_rows,
+                                   float* loss_head_sum, float4* rows4, void* workspace,
+                                   size_t ws_bytes, int* dev_status, void* stream) {
   Problem p;
   hh_status st = make_problem(fmap, dtype, B, H, n, &p);
   if (st != HH_OK) return st;
   if (B == 0) return HH_OK;
-  if (!loss_head_sum) return HH_ERR_INVALID_ARG;
+  if (!loss_head_sum && !rows4) return HH_ERR_INVALID_ARG;
   if (n > 0 && (!q || !k)) return HH_ERR_INVALID_ARG;
-  if ((st = check_ptrs_aligned({q, k, loss_rows, loss_head_sum, p.Wq, p.bq, p.Wk, p.bk,
+  if ((st = check_ptrs_aligned({q, k, loss_rows, loss_head_sum, rows4, p.Wq, p.bq, p.Wk, p.bk,
                                 workspace})) != HH_OK)
     return st;
   if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
@@ -276,25 +306,43 @@ hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const v
   if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
-  if (n == 0) return cuda_status(cudaMemsetAsync(loss_head_sum, 0, sizeof(float) * B * H, s));
+  if (n == 0)
+    return loss_head_sum ? cuda_status(cudaMemsetAsync(loss_head_sum, 0, sizeof(float) * B * H, s))
+                         : HH_OK;
   char* ws = (char*)workspace;
   const size_t phi_bytes = align256((size_t)B * H * n * p.dpp * elem_size(dtype));
   void* phq = ws;
   void* phk = ws + phi_bytes;
   float* partial = (float*)(ws + 2 * phi_bytes);
+  float* head = loss_head_sum ? loss_head_sum : partial + (size_t)B * H * ceil_div(n, 64);
   if (fmap_tc_supported(p)) {
-    cudaError_t e = launch_fmap_tc(p, q, 0, phq, dev_status, s);
-    if (e == cudaSuccess) e = launch_fmap_tc(p, k, 1, phk, dev_status, s);
+    cudaError_t e = launch_fmap_tc_qk(p, q, k, phq, phk, nullptr, nullptr, dev_status, s);
     if (e == cudaSuccess)
-      e = launch_loss_tc(p, q, k, phq, phk, loss_rows, partial, loss_head_sum, nullptr, dev_status,
+      e = launch_loss_tc(p, q, k, phq, phk, loss_rows, partial, head, nullptr, rows4, dev_status,
                          s);
     return cuda_status(e);
   }
-  cudaError_t e = launch_fmap_simt(p, q, 0, phq, s);
-  if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, s);
+  cudaError_t e = launch_fmap_simt(p, q, 0, phq, nullptr, s);
+  if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, nullptr, s);
   if (e == cudaSuccess)
-    e = launch_loss_simt(p, q, k, phq, phk, loss_rows, partial, loss_simt_tile(), loss_head_sum, s);
+    e = launch_loss_simt(p, q, k, phq, phk, loss_rows, partial, loss_simt_tile(), head, rows4, s);
   return cuda_status(e);
+}
+
+hh_status hh_mimicry_loss(const hh_fmap* fmap, int dtype, const void* q, const void* k, int64_t B,
+                          int H, int64_t n, float* loss_rows, float* loss_head_sum,
+                          void* workspace, size_t ws_bytes, int* dev_status, void* stream) {
+  if (B > 0 && !loss_head_sum) return HH_ERR_INVALID_ARG;
+  return mimicry_loss_impl(fmap, dtype, q, k, B, H, n, loss_rows, loss_head_sum, nullptr,
+                           workspace, ws_bytes, dev_status, stream);
+}
+
+hh_status hh_mimicry_stats(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                           int64_t B, int H, int64_t n, float* stats_rows, void* workspace,
+                           size_t ws_bytes, int* dev_status, void* stream) {
+  if (B > 0 && n > 0 && !stats_rows) return HH_ERR_INVALID_ARG;
+  return mimicry_loss_impl(fmap, dtype, q, k, B, H, n, nullptr, nullptr, (float4*)stats_rows,
+                           workspace, ws_bytes, dev_status, stream);
 }
 
 // Workspace of hh_mimicry_loss_grad.
@@ -327,7 +375,7 @@ static GradWs loss_grad_ws(const Problem& p) {
 size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n) {
   Problem p;
   if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
-  if (p.kind != HH_FMAP_HEDGEHOG || B * H * n == 0) return 0;
+  if (p.kind != HH_FMAP_HEDGEHOG || p.softmax || B * H * n == 0) return 0;
   return loss_grad_ws(p).total;
 }
 
@@ -338,7 +386,8 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   Problem p;
   hh_status st = make_problem(fmap, dtype, B, H, n, &p);
   if (st != HH_OK) return st;
-  if (p.kind != HH_FMAP_HEDGEHOG || p.d % 8 != 0 || p.d > 128) return HH_ERR_UNSUPPORTED;
+  if (p.kind != HH_FMAP_HEDGEHOG || p.softmax || p.d % 8 != 0 || p.d > 128)
+    return HH_ERR_UNSUPPORTED;
   const bool separate = fmap->Wk && fmap->Wk != fmap->Wq;
   if (!dWq || !dbq || (separate && (!dWk || !dbk))) return HH_ERR_INVALID_ARG;
   if (!separate) dWk = dbk = nullptr;
@@ -371,15 +420,17 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   float* wa = (float*)(ws + 2 * w.phi + w.stats);
   float* wb = (float*)(ws + 2 * w.phi + w.stats + w.a);
   float* wc = (float*)(ws + 2 * w.phi + w.stats + w.a + w.b);
-  cudaError_t e = fmap_tc_supported(p) ? launch_fmap_tc(p, q, 0, phq, dev_status, s)
-                                       : launch_fmap_simt(p, q, 0, phq, s);
-  if (e == cudaSuccess)
-    e = fmap_tc_supported(p) ? launch_fmap_tc(p, k, 1, phk, dev_status, s)
-                             : launch_fmap_simt(p, k, 1, phk, s);
+  cudaError_t e;
+  if (fmap_tc_supported(p)) {
+    e = launch_fmap_tc_qk(p, q, k, phq, phk, nullptr, nullptr, dev_status, s);
+  } else {
+    e = launch_fmap_simt(p, q, 0, phq, nullptr, s);
+    if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, nullptr, s);
+  }
   if (tc) {
     // wa: loss partials, wb: loss sums, wc: dW, db shares
     if (e == cudaSuccess)
-      e = launch_loss_tc(p, q, k, phq, phk, nullptr, wa, wb, stats, dev_status, s);
+      e = launch_loss_tc(p, q, k, phq, phk, nullptr, wa, wb, stats, nullptr, dev_status, s);
     if (e == cudaSuccess)
       e = launch_loss_grad_tc(p, q, k, phq, phk, stats, wc, dWq, dbq, dWk, dbk, dev_status, s);
   } else if (e == cudaSuccess) {

@@ -11,7 +11,7 @@ namespace hh {
 
 // A validated problem description handed from the ABI layer to launchers.
 struct Problem {
-  int kind;        // hh_fmap_kind
+  int kind;        // HH_FMAP_HEDGEHOG (also for the softmax map) or HH_FMAP_TAYLOR2
   int dtype;       // hh_dtype
   int d;           // head dim
   int dp;          // unpadded feature dim
@@ -23,6 +23,14 @@ struct Problem {
   const float* bq;
   const void* Wk;
   const float* bk;
+  // Softmax-over-features map: phi = [exp(h - c+); exp(-h - c-)] with the
+  // per-row offsets c+- = logsumexp(+-h) (bias null).  Kernels that build phi
+  // from h = x W read the offsets, in log2 units (c * log2 e), from offq /
+  // offk, set once they have been computed: pairs [U][off_stride(n)] (rows
+  // padded to whole 128-row tiles, so a tile's offsets start 16-byte aligned).
+  bool softmax = false;
+  const float2* offq = nullptr;
+  const float2* offk = nullptr;
 };
 
 // ---- element access in float32 for either storage type -------------------
@@ -38,6 +46,8 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 constexpr float kInvSqrt2 = 0.70710678118654752440f;
 
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+// Row stride of the softmax-map offset arrays.
+inline int64_t off_stride(int64_t n) { return (n + 127) / 128 * 128; }
 
 // Cached device attributes (the only state the library keeps).
 int device_sm_count();
@@ -47,13 +57,16 @@ uint64_t wait_soft_limit_ns();
 
 // ---- launchers (return cudaSuccess or the launch error) ------------------
 // SIMT kernels: float32 arithmetic, any supported d; T = float or bf16.
+// phi (nullable): [U][n][dpp]; off (nullable, softmax map only): per-row
+// offsets in log2 units, [U][off_stride(n)].
 cudaError_t launch_fmap_simt(const Problem& p, const void* x, int is_key, void* phi,
-                             cudaStream_t s);
+                             float2* off, cudaStream_t s);
 cudaError_t launch_prefill_simt(const Problem& p, const void* q, const void* k, const void* v,
                                 void* y, float* S_out, float* z_out, cudaStream_t s);
+// rows4 (nullable): per-row (CE, KL, H(p), H(w)).
 cudaError_t launch_loss_simt(const Problem& p, const void* q, const void* k, const void* phq,
                              const void* phk, float* loss_rows, float* partial, int tile,
-                             float* head_sum, cudaStream_t s);
+                             float* head_sum, float4* rows4, cudaStream_t s);
 int loss_simt_tile();
 
 // Tensor-core (tcgen05) chunked prefill for bf16.
@@ -101,13 +114,18 @@ cudaError_t launch_loss_grad(const Problem& p, const void* q, const void* k, con
 
 // Tensor-core (tcgen05) feature map and mimicry loss for bf16 Hedgehog d in {64, 128}.
 bool fmap_tc_supported(const Problem& p);
-cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,
+cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi, float2* off,
                            int* dev_status, cudaStream_t s);
+// Queries and keys in one launch (outputs nullable as above).
+cudaError_t launch_fmap_tc_qk(const Problem& p, const void* q, const void* k, void* phq,
+                              void* phk, float2* offq, float2* offk, int* dev_status,
+                              cudaStream_t s);
 // stats (nullable): [U][NT * 128] pairs (c_i, 1 / A_i) with c_i = m_i + log2 Z_i,
 // so that the target weight is p_ij = 2^(s_ij log2(e) / sqrt(d) - c_i).
+// rows4 (nullable): per-row (CE, KL, H(p), H(w)).
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
-                           float* stats, int* dev_status, cudaStream_t s);
+                           float* stats, float4* rows4, int* dev_status, cudaStream_t s);
 int loss_tc_tile();
 
 // Tensor-core gradient of the summed mimicry loss for bf16 Hedgehog d in

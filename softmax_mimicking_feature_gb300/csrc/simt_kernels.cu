@@ -17,21 +17,60 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// phi of one row held in shared memory (xs[0..d)), written to out[0..dpp).
+__device__ __forceinline__ float warp_max(float v) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// phi of one row held in shared memory (xs[0..d)), written to out[0..dpp) by
+// one whole warp.
 // Hedgehog: out[l] = exp(h_l), out[d+l] = exp(-h_l), h = x W + b.
+// Softmax map (Choice 4, Eq. 5; no bias): out[l] = exp(h_l - c+),
+//   out[d+l] = exp(-h_l - c-), c+- = logsumexp over l of +-h; *off (if given)
+//   receives (c+, c-) log2 e.
 // Taylor: [1, x, x_i x_j / sqrt2 (i-major)], zero padding.
 template <typename T>
-__device__ __forceinline__ void phi_row(int kind, int d, int dpp, const float* xs, const T* W,
-                                        const float* b, float* out, int lane, int nlanes) {
+__device__ __forceinline__ void phi_row(int kind, bool softmax, int d, int dpp, const float* xs,
+                                        const T* W, const float* b, float* out, float2* off,
+                                        int lane) {
   if (kind == HH_FMAP_HEDGEHOG) {
-    for (int l = lane; l < d; l += nlanes) {
+    float mx = -INFINITY, mn = INFINITY;
+    for (int l = lane; l < d; l += 32) {
       float h = b ? b[l] : 0.f;
       for (int k = 0; k < d; ++k) h = fmaf(xs[k], to_f(W[(size_t)k * d + l]), h);
-      out[l] = expf(h);
-      out[d + l] = expf(-h);
+      if (softmax) {
+        out[l] = h;
+        mx = fmaxf(mx, h);
+        mn = fminf(mn, h);
+      } else {
+        out[l] = expf(h);
+        out[d + l] = expf(-h);
+      }
+    }
+    if (softmax) {
+      mx = warp_max(mx);
+      mn = -warp_max(-mn);
+      float sp = 0.f, sn = 0.f;
+      for (int l = lane; l < d; l += 32) {
+        sp += expf(out[l] - mx);
+        sn += expf(mn - out[l]);
+      }
+      sp = warp_sum(sp);
+      sn = warp_sum(sn);
+      const float cp = mx + logf(sp), cn = logf(sn) - mn;
+      for (int l = lane; l < d; l += 32) {
+        const float h = out[l];
+        out[l] = expf(h - cp);
+        out[d + l] = expf(-h - cn);
+      }
+      if (off && lane == 0) *off = make_float2(cp * 1.4426950408889634f, cn * 1.4426950408889634f);
     }
   } else {
-    for (int f = lane; f < dpp; f += nlanes) {
+    for (int f = lane; f < dpp; f += 32) {
       float val;
       if (f == 0) {
         val = 1.f;
@@ -54,7 +93,8 @@ __device__ __forceinline__ void phi_row(int kind, int d, int dpp, const float* x
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* __restrict__ bias,
-                 T* __restrict__ phi, int kind, int d, int dpp, int H, int64_t n, int64_t rows) {
+                 T* __restrict__ phi, float2* __restrict__ off, int kind, int softmax, int d,
+                 int dpp, int H, int64_t n, int64_t rows) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = kThreads / 32;
@@ -66,9 +106,11 @@ fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* 
     __syncwarp();
     const T* Wh = W ? W + (size_t)h * d * d : nullptr;
     const float* bh = bias ? bias + (size_t)h * d : nullptr;
-    phi_row<T>(kind, d, dpp, xs, Wh, bh, out, lane, 32);
+    float2* orow = off ? off + (r / n) * ((n + 127) / 128 * 128) + r % n : nullptr;
+    phi_row<T>(kind, softmax != 0, d, dpp, xs, Wh, bh, out, orow, lane);
     __syncwarp();
-    for (int f = lane; f < dpp; f += 32) phi[r * dpp + f] = from_f<T>(out[f]);
+    if (phi)
+      for (int f = lane; f < dpp; f += 32) phi[r * dpp + f] = from_f<T>(out[f]);
     __syncwarp();
   }
 }
@@ -83,8 +125,8 @@ __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                     T* __restrict__ y, float* __restrict__ S_out, float* __restrict__ z_out,
                     const T* __restrict__ Wq, const float* __restrict__ bq,
-                    const T* __restrict__ Wk, const float* __restrict__ bk, int kind, int d,
-                    int dpp, int H, int64_t n, int C) {
+                    const T* __restrict__ Wk, const float* __restrict__ bk, int kind,
+                    int softmax, int d, int dpp, int H, int64_t n, int C) {
   extern __shared__ float sm[];
   float* S = sm;                       // [dpp][d]
   float* z = S + (size_t)dpp * d;      // [dpp]
@@ -121,8 +163,10 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     }
     __syncthreads();
     for (int r = warp; r < C; r += kThreads / 32) {
-      phi_row<T>(kind, d, dpp, xs + (size_t)r * d, Wqh, bqh, phq + (size_t)r * dpp, lane, 32);
-      phi_row<T>(kind, d, dpp, xk + (size_t)r * d, Wkh, bkh, phk + (size_t)r * dpp, lane, 32);
+      phi_row<T>(kind, softmax != 0, d, dpp, xs + (size_t)r * d, Wqh, bqh, phq + (size_t)r * dpp,
+                 nullptr, lane);
+      phi_row<T>(kind, softmax != 0, d, dpp, xk + (size_t)r * d, Wkh, bkh, phk + (size_t)r * dpp,
+                 nullptr, lane);
       if (r >= nc)  // ragged tail: padded keys contribute nothing
         for (int f = lane; f < dpp; f += 32) phk[(size_t)r * dpp + f] = 0.f;
     }
@@ -174,14 +218,16 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 // ---------------------------------------------------------------------------
 // Mimicry loss: one block per (batch*head, tile of 64 queries).  Four threads
 // share a query row; each keeps an online-softmax state over its keys:
-//   M = running max of s, Z = sum e^{s-M}, T = sum e^{s-M} log a, A = sum a
-// and the row's loss is log A - T / Z (= -sum_j p_j log(a_j / A)).
+//   M = running max of s, Z = sum e^{s-M}, T = sum e^{s-M} log a, A = sum a,
+//   U = sum e^{s-M} s, V = sum a log a
+// and the row's loss is log A - T / Z (= -sum_j p_j log(a_j / A)); the
+// entropies are H(p) = log Z + M - U / Z and H(w) = log A - V / A.
 // ---------------------------------------------------------------------------
 constexpr int kLossRows = 64;
 constexpr int kLossKeys = 32;
 
 struct OnlineCE {
-  float M, Z, T, A;
+  float M, Z, T, A, U, V;
 };
 
 __device__ __forceinline__ OnlineCE ce_merge(OnlineCE x, OnlineCE y) {
@@ -192,6 +238,8 @@ __device__ __forceinline__ OnlineCE ce_merge(OnlineCE x, OnlineCE y) {
   r.Z = x.Z * fx + y.Z * fy;
   r.T = x.T * fx + y.T * fy;
   r.A = x.A + y.A;
+  r.U = x.U * fx + y.U * fy;
+  r.V = x.V + y.V;
   return r;
 }
 
@@ -199,7 +247,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
                  const T* __restrict__ phk, float* __restrict__ loss_rows,
-                 float* __restrict__ partial, int d, int dpp, int64_t n, int ntiles) {
+                 float* __restrict__ partial, float4* __restrict__ rows4, int d, int dpp,
+                 int64_t n, int ntiles) {
   extern __shared__ float sm[];
   float* qs = sm;                                  // [64][d]
   float* pq = qs + kLossRows * d;                  // [64][dpp]
@@ -223,7 +272,7 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     const int64_t rr = r0 + e / dpp;
     pq[e] = rr < n ? to_f(phq[((size_t)bh * n + rr) * dpp + e % dpp]) : 0.f;
   }
-  OnlineCE st = {-INFINITY, 0.f, 0.f, 0.f};
+  OnlineCE st = {-INFINITY, 0.f, 0.f, 0.f, 0.f, 0.f};
   const int64_t last = min(n, r0 + kLossRows) - 1;
   for (int64_t k0 = 0; k0 <= last; k0 += kLossKeys) {
     __syncthreads();
@@ -249,12 +298,16 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
           const float c = (st.M == -INFINITY) ? 0.f : expf(st.M - s);
           st.Z *= c;
           st.T *= c;
+          st.U *= c;
           st.M = s;
         }
         const float e = expf(s - st.M);
+        const float la = logf(a);
         st.Z += e;
-        st.T = fmaf(e, logf(a), st.T);
+        st.T = fmaf(e, la, st.T);
         st.A += a;
+        st.U = fmaf(e, s, st.U);
+        st.V = fmaf(a, la, st.V);
       }
     }
   }
@@ -265,12 +318,19 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     o.Z = __shfl_xor_sync(0xffffffffu, st.Z, off);
     o.T = __shfl_xor_sync(0xffffffffu, st.T, off);
     o.A = __shfl_xor_sync(0xffffffffu, st.A, off);
+    o.U = __shfl_xor_sync(0xffffffffu, st.U, off);
+    o.V = __shfl_xor_sync(0xffffffffu, st.V, off);
     st = ce_merge(st, o);
   }
   if (part == 0) {
     const float L = (i < n) ? (logf(st.A) - st.T / st.Z) : 0.f;
     rowL[row] = L;
     if (loss_rows && i < n) loss_rows[(size_t)bh * n + i] = L;
+    if (rows4 && i < n) {
+      const float Hp = logf(st.Z) + st.M - st.U / st.Z;
+      const float Hw = logf(st.A) - st.V / st.A;
+      rows4[(size_t)bh * n + i] = make_float4(L, L - Hp, Hp, Hw);
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -301,7 +361,7 @@ int loss_simt_tile() { return kLossRows; }
 
 template <typename T>
 static cudaError_t fmap_simt_t(const Problem& p, const void* x, int is_key, void* phi,
-                               cudaStream_t s) {
+                               float2* off, cudaStream_t s) {
   const int64_t rows = p.B * p.H * p.n;
   if (rows == 0) return cudaSuccess;
   const T* W = (const T*)(is_key && p.Wk ? p.Wk : p.Wq);
@@ -310,15 +370,16 @@ static cudaError_t fmap_simt_t(const Problem& p, const void* x, int is_key, void
   const int64_t blocks64 = (rows + warps - 1) / warps;
   const int blocks = (int)std::min<int64_t>(blocks64, (int64_t)device_sm_count() * 16);
   const size_t smem = sizeof(float) * warps * (128 + 320);
-  fmap_simt_kernel<T><<<blocks, kThreads, smem, s>>>((const T*)x, W, b, (T*)phi, p.kind, p.d,
-                                                     p.dpp, p.H, p.n, rows);
+  fmap_simt_kernel<T><<<blocks, kThreads, smem, s>>>((const T*)x, W, b, (T*)phi,
+                                                     p.softmax ? off : nullptr, p.kind,
+                                                     p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.n, rows);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fmap_simt(const Problem& p, const void* x, int is_key, void* phi,
-                             cudaStream_t s) {
-  return p.dtype == HH_F32 ? fmap_simt_t<float>(p, x, is_key, phi, s)
-                           : fmap_simt_t<__nv_bfloat16>(p, x, is_key, phi, s);
+                             float2* off, cudaStream_t s) {
+  return p.dtype == HH_F32 ? fmap_simt_t<float>(p, x, is_key, phi, off, s)
+                           : fmap_simt_t<__nv_bfloat16>(p, x, is_key, phi, off, s);
 }
 
 template <typename T>
@@ -338,7 +399,7 @@ static cudaError_t prefill_simt_t(const Problem& p, const void* q, const void* k
   const float* bk = p.Wk ? p.bk : p.bq;
   prefill_simt_kernel<T><<<(unsigned)units, kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)v, (T*)y, S_out, z_out, (const T*)p.Wq, p.bq, Wk, bk,
-      p.kind, p.d, p.dpp, p.H, p.n, C);
+      p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.n, C);
   return cudaGetLastError();
 }
 
@@ -351,7 +412,7 @@ cudaError_t launch_prefill_simt(const Problem& p, const void* q, const void* k, 
 template <typename T>
 static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, const void* phq,
                                const void* phk, float* loss_rows, float* partial, int tile,
-                               float* head_sum, cudaStream_t s) {
+                               float* head_sum, float4* rows4, cudaStream_t s) {
   const int64_t units = p.B * p.H;
   if (units == 0) return cudaSuccess;
   const int ntiles = ceil_div(p.n, kLossRows);
@@ -365,8 +426,8 @@ static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, c
     const int64_t blocks = units * ntiles;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     loss_simt_kernel<T><<<(unsigned)blocks, kThreads, smem, s>>>((const T*)q, (const T*)k, (const T*)phq,
-                                                     (const T*)phk, loss_rows, partial, p.d,
-                                                     p.dpp, p.n, ntiles);
+                                                     (const T*)phk, loss_rows, partial, rows4,
+                                                     p.d, p.dpp, p.n, ntiles);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -377,11 +438,11 @@ static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, c
 
 cudaError_t launch_loss_simt(const Problem& p, const void* q, const void* k, const void* phq,
                              const void* phk, float* loss_rows, float* partial, int tile,
-                             float* head_sum, cudaStream_t s) {
+                             float* head_sum, float4* rows4, cudaStream_t s) {
   return p.dtype == HH_F32
-             ? loss_simt_t<float>(p, q, k, phq, phk, loss_rows, partial, tile, head_sum, s)
+             ? loss_simt_t<float>(p, q, k, phq, phk, loss_rows, partial, tile, head_sum, rows4, s)
              : loss_simt_t<__nv_bfloat16>(p, q, k, phq, phk, loss_rows, partial, tile, head_sum,
-                                          s);
+                                          rows4, s);
 }
 
 }  // namespace hh

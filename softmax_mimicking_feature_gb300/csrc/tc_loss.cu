@@ -8,7 +8,12 @@
 //
 // fmap_tc_kernel: one CTA per 128-row tile of one (batch, head) sequence.
 //   H = X W on tcgen05 (fp32 in TMEM); the epilogue adds b, exponentiates
-//   both signs and stores phi rows as bf16.
+//   both signs and stores phi rows as bf16.  For the softmax-over-features map
+//   (Choice 4, Eq. 5; no bias) it first forms the row offsets
+//   c+- = logsumexp(+-h) over the d directions (max, then sum of exponentials,
+//   each combined across the two warp halves that share a row) and stores
+//   exp(+-h - c+-), and/or the offsets themselves for kernels that build phi
+//   from h on their own.
 //
 // loss_tc_kernel: one CTA per (batch*head, 128-query tile); key tiles of 128
 //   run j = 0 .. i.  A producer warp TMA-loads K_j and phi(K_j) and issues
@@ -17,7 +22,11 @@
 //     m (running max of s log2 e), Z = sum 2^{s' - m}, T = sum 2^{s' - m} log2 a,
 //     Asum = sum a
 //   so that L = ln Asum - ln 2 * T / Z, which equals Eq. 4 because the target
-//   weights sum to one.  The smem operands of tile j+1 are loaded as soon as
+//   weights sum to one.  The statistics variant also keeps
+//     U = sum 2^{s' - m} s'  and  V = sum a log2 a
+//   for the entropies H(p) = ln Z + ln 2 (m - U / Z) and
+//   H(w) = ln Asum - ln 2 V / Asum of "The Two Missing Properties as Design
+//   Specifications", and KL = L - H(p).  The smem operands of tile j+1 are loaded as soon as
 //   the MMAs of tile j have read them, and those MMAs run while the epilogue
 //   works on tile j.
 
@@ -76,10 +85,15 @@ __device__ __forceinline__ uint32_t lane_base(int warp) {
 // ===========================================================================
 // feature map
 // ===========================================================================
+// One launch maps one or two inputs ("sides", e.g. q and k); the grid is
+// sides x U x NT tiles.
 struct FmapArgs {
-  CUtensorMap tx, tw;
-  __nv_bfloat16* phi;   // [U][n][2D]
-  const float* bias;    // [H][D] or null
+  CUtensorMap tx[2], tw[2];
+  __nv_bfloat16* phi[2];   // [U][n][2D] or null
+  float2* off[2];          // [U][NT*128] softmax-map offsets (log2 units) or null
+  const float* bias[2];    // [H][D] or null
+  int sides;
+  int softmax;
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -97,6 +111,7 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
   const uint32_t sb = smem_u32(sm);
   const uint32_t OFF_W = 0, OFF_X = W_BYTES;
   float* bias_s = reinterpret_cast<float*>(sm + W_BYTES + X_BYTES);
+  float2* red = reinterpret_cast<float2*>(bias_s + 136);   // [2 halves][128 rows]
   const uint32_t bar_load = smem_u32(bias_s + 128);
   const uint32_t bar_mma = bar_load + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bias_s + 128 + 4);
@@ -104,8 +119,10 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = warp >> 2, row = 32 * (warp & 3) + lane;
-  const int64_t unit = blockIdx.x / A.NT;
-  const int t = blockIdx.x % A.NT;
+  const unsigned per_side = gridDim.x / A.sides;
+  const int side = (int)(blockIdx.x / per_side);
+  const int64_t unit = (blockIdx.x % per_side) / A.NT;
+  const int t = (blockIdx.x % per_side) % A.NT;
   const int h = (int)(unit % A.H);
   const int64_t r0 = (int64_t)t * kTile;
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
@@ -120,15 +137,16 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
   if (tid == 0) {
     mbar_expect_tx(bar_load, W_BYTES + X_BYTES);
     for (int i = 0; i < D / 64; ++i) {
-      tma_load_3d(sb + OFF_W + i * (D * 128), &A.tw, bar_load, 64 * i, 0, h);
-      tma_load_3d(sb + OFF_X + i * 16384, &A.tx, bar_load, 64 * i, (int)r0, (int)unit);
+      tma_load_3d(sb + OFF_W + i * (D * 128), &A.tw[side], bar_load, 64 * i, 0, h);
+      tma_load_3d(sb + OFF_X + i * 16384, &A.tx[side], bar_load, 64 * i, (int)r0, (int)unit);
     }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     tmem_relinquish();
   }
-  for (int i = tid; i < D; i += 256) bias_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
+  const float* bias = A.bias[side];
+  for (int i = tid; i < D; i += 256) bias_s[i] = bias ? bias[(size_t)h * D + i] : 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -156,19 +174,60 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
   if (__syncthreads_and(ok)) {
     constexpr int HC = D / 2;
     const bool valid = r0 + row < A.n;
-    __nv_bfloat16* prow = A.phi + ((size_t)unit * A.n + r0 + row) * (2 * D);
+    const uint32_t trow = tmem + lane_base(warp) + half * HC;
+    // softmax map: row offsets op = c+ log2 e, on = c- log2 e (zero otherwise)
+    float op = 0.f, on = 0.f;
+    if (A.softmax) {
+      float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+      for (int c = 0; c < HC; c += 32) {
+        uint32_t hv[32];
+        tmem_ld32(trow + c, hv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          mx = fmaxf(mx, __uint_as_float(hv[j]));
+          mn = fminf(mn, __uint_as_float(hv[j]));
+        }
+      }
+      red[half * 128 + row] = make_float2(mx, mn);
+      __syncthreads();
+      float2 o = red[(1 - half) * 128 + row];
+      const float mp = fmaxf(mx, o.x) * kLog2e, mq = -fminf(mn, o.y) * kLog2e;
+      float sp = 0.f, sn = 0.f;
+#pragma unroll
+      for (int c = 0; c < HC; c += 32) {
+        uint32_t hv[32];
+        tmem_ld32(trow + c, hv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          sp += ex2_approx(fmaf(__uint_as_float(hv[j]), kLog2e, -mp));
+          sn += ex2_approx(fmaf(-__uint_as_float(hv[j]), kLog2e, -mq));
+        }
+      }
+      __syncthreads();   // the partner has read red before it is overwritten
+      red[half * 128 + row] = make_float2(sp, sn);
+      __syncthreads();
+      o = red[(1 - half) * 128 + row];
+      op = mp + __log2f(sp + o.x);
+      on = mq + __log2f(sn + o.y);
+      if (A.off[side] && half == 0 && valid)
+        A.off[side][(size_t)unit * A.NT * kTile + r0 + row] = make_float2(op, on);
+    }
+    __nv_bfloat16* prow =
+        A.phi[side] ? A.phi[side] + ((size_t)unit * A.n + r0 + row) * (2 * D) : nullptr;
 #pragma unroll
     for (int c = 0; c < HC; c += 32) {
+      if (!prow) break;
       uint32_t hv[32];
-      tmem_ld32(tmem + lane_base(warp) + half * HC + c, hv);
+      tmem_ld32(trow + c, hv);
       uint32_t pp[16], pn[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int l = half * HC + c + j;
         const float h0 = __uint_as_float(hv[j]) + bias_s[l];
         const float h1 = __uint_as_float(hv[j + 1]) + bias_s[l + 1];
-        pp[j / 2] = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
-        pn[j / 2] = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+        pp[j / 2] = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -op)), ex2_approx(fmaf(h1, kLog2e, -op)));
+        pn[j / 2] = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -on)), ex2_approx(fmaf(-h1, kLog2e, -on)));
       }
       if (valid) {
         uint4* dp = reinterpret_cast<uint4*>(prow + half * HC + c);
@@ -194,6 +253,7 @@ struct LossArgs {
   float* loss_rows;    // [U][n] or null
   float* partial;      // [U][NT]
   float2* stats;       // [U][NT * 128] (c_i, 1 / A_i) or null; c_i = m_i + log2 Z_i
+  float4* rows4;       // [U][n] (CE, KL, H(p), H(w)); used by the STATS variant
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -213,8 +273,8 @@ struct LossCfg {
   static constexpr uint32_t OFF_PK = OFF_K + Q_BYTES;
   static constexpr uint32_t OFF_END = OFF_PK + PQ_BYTES;
   // scalars
-  static constexpr uint32_t OFF_ST = OFF_END;              // float[4][128]: m, Z, T, Asum (half 1)
-  static constexpr uint32_t OFF_RL = OFF_ST + 4 * 128 * 4; // float[128] row losses
+  static constexpr uint32_t OFF_ST = OFF_END;              // float[6][128]: m, Z, T, Asum, U, V (half 1)
+  static constexpr uint32_t OFF_RL = OFF_ST + 6 * 128 * 4; // float[128] row losses
   static constexpr uint32_t OFF_BAR = OFF_RL + 128 * 4;    // 9 x u64
   static constexpr uint32_t OFF_MISC = OFF_BAR + 9 * 8;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
@@ -222,7 +282,7 @@ struct LossCfg {
 
 constexpr int kLossThreads = 288;  // 8 epilogue warps + 1 producer warp
 
-template <int D>
+template <int D, bool STATS>
 __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_constant__ LossArgs A) {
   using C = LossCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -339,6 +399,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
     // online state; Z, T and the weight sum are kept as two interleaved partial
     // sums so consecutive keys do not form one long dependency chain
     float m = -INFINITY, Z0 = 0.f, Z1 = 0.f, T0 = 0.f, T1 = 0.f, A0 = 0.f, A1 = 0.f;
+    float U0 = 0.f, U1 = 0.f, V0 = 0.f, V1 = 0.f;   // STATS only
     const int64_t kmax = min(qi, A.n - 1);   // last key admitted for this row
     for (int j = 0; j < nkt; ++j) {
       const int stg = j & 1;
@@ -365,16 +426,32 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           const float mn = fmaxf(m, fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * A.s_scale);
           const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
           Z0 *= f; Z1 *= f; T0 *= f; T1 *= f;
+          if constexpr (STATS) { U0 *= f; U1 *= f; }
           m = mn;
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float a0 = __uint_as_float(av[e]), a1 = __uint_as_float(av[e + 1]);
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), A.s_scale, -m));
-            Z0 += p0;
-            Z1 += p1;
-            T0 = fmaf(p0, __log2f(a0), T0);
-            T1 = fmaf(p1, __log2f(a1), T1);
+            const float l0 = __log2f(a0), l1 = __log2f(a1);
+            if constexpr (STATS) {
+              const float s0 = __uint_as_float(sv[e]) * A.s_scale;
+              const float s1 = __uint_as_float(sv[e + 1]) * A.s_scale;
+              const float p0 = ex2_approx(s0 - m), p1 = ex2_approx(s1 - m);
+              Z0 += p0;
+              Z1 += p1;
+              T0 = fmaf(p0, l0, T0);
+              T1 = fmaf(p1, l1, T1);
+              U0 = fmaf(p0, s0, U0);
+              U1 = fmaf(p1, s1, U1);
+              V0 = fmaf(a0, l0, V0);
+              V1 = fmaf(a1, l1, V1);
+            } else {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), A.s_scale, -m));
+              Z0 += p0;
+              Z1 += p1;
+              T0 = fmaf(p0, l0, T0);
+              T1 = fmaf(p1, l1, T1);
+            }
             A0 += a0;
             A1 += a1;
           }
@@ -386,15 +463,22 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           const float mn = fmaxf(m, cm * A.s_scale);
           const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
           Z0 *= f; Z1 *= f; T0 *= f; T1 *= f;
+          if constexpr (STATS) { U0 *= f; U1 *= f; }
           m = mn;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             if (e < nval) {
               const float a = __uint_as_float(av[e]);
-              const float p = ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
+              const float la = __log2f(a);
+              const float sl = __uint_as_float(sv[e]) * A.s_scale;
+              const float p = ex2_approx(sl - m);
               Z0 += p;
-              T0 = fmaf(p, __log2f(a), T0);
+              T0 = fmaf(p, la, T0);
               A0 += a;
+              if constexpr (STATS) {
+                U0 = fmaf(p, sl, U0);
+                V0 = fmaf(a, la, V0);
+              }
             }
           }
         }
@@ -403,13 +487,17 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_free0 + 8 * stg);
     }
-    float Z = Z0 + Z1, T = T0 + T1, As = A0 + A1;
+    float Z = Z0 + Z1, T = T0 + T1, As = A0 + A1, Us = U0 + U1, Vs = V0 + V1;
     // merge the two column halves of each row
     if (half == 1) {
       st_s[row] = m;
       st_s[128 + row] = Z;
       st_s[256 + row] = T;
       st_s[384 + row] = As;
+      if constexpr (STATS) {
+        st_s[512 + row] = Us;
+        st_s[640 + row] = Vs;
+      }
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
     if (half == 0) {
@@ -426,6 +514,13 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       if (A.stats)
         A.stats[(size_t)unit * A.NT * kTile + qi] =
             valid ? make_float2(mn + __log2f(Zt), 1.f / At) : make_float2(0.f, 0.f);
+      if constexpr (STATS) {
+        const float Ut = Us * f1 + st_s[512 + row] * f2, Vt = Vs + st_s[640 + row];
+        constexpr float kLn2 = 0.69314718055994531f;
+        const float Hp = logf(Zt) + kLn2 * (mn - Ut / Zt);
+        const float Hw = logf(At) - kLn2 * (Vt / At);
+        if (valid) A.rows4[(size_t)unit * A.n + qi] = make_float4(L, L - Hp, Hp, Hw);
+      }
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
     if (tid == 0) {
@@ -459,42 +554,61 @@ bool fmap_tc_supported(const Problem& p) {
   return p.dtype == HH_BF16 && p.kind == HH_FMAP_HEDGEHOG && (p.d == 64 || p.d == 128);
 }
 
+// sides: inputs x[i] (is_key[i] picks the key map), outputs phi[i] / off[i]
 template <int D>
-static cudaError_t fmap_tc_t(const Problem& p, const void* x, int is_key, void* phi,
+static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
+                             const int* is_key, void* const* phi, float2* const* off,
                              int* dev_status, cudaStream_t s) {
   FmapArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
-  const void* W = is_key && p.Wk ? p.Wk : p.Wq;
-  if (!make_map(&a.tx, x, D, p.n, U, kTile) || !make_map(&a.tw, W, D, D, p.H, D))
-    return cudaErrorInvalidValue;
-  a.phi = reinterpret_cast<__nv_bfloat16*>(phi);
-  a.bias = is_key && p.Wk ? p.bk : p.bq;
+  for (int i = 0; i < sides; ++i) {
+    const void* W = is_key[i] && p.Wk ? p.Wk : p.Wq;
+    if (!make_map(&a.tx[i], x[i], D, p.n, U, kTile) || !make_map(&a.tw[i], W, D, D, p.H, D))
+      return cudaErrorInvalidValue;
+    a.phi[i] = reinterpret_cast<__nv_bfloat16*>(phi[i]);
+    a.off[i] = p.softmax ? off[i] : nullptr;
+    a.bias[i] = is_key[i] && p.Wk ? p.bk : p.bq;
+  }
+  a.sides = sides;
+  a.softmax = p.softmax ? 1 : 0;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
   a.n = p.n;
   a.H = p.H;
   a.NT = ceil_div(p.n, kTile);
-  const size_t smem = D * D * 2 + kTile * D * 2 + 128 * 4 + 64 + 1024;
+  const size_t smem = D * D * 2 + kTile * D * 2 + 136 * 4 + 256 * 8 + 1024;
   cudaError_t e =
       cudaFuncSetAttribute(fmap_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  fmap_tc_kernel<D><<<(unsigned)(U * a.NT), 256, smem, s>>>(a);
+  fmap_tc_kernel<D><<<(unsigned)(sides * U * a.NT), 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi,
+cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi, float2* off,
                            int* dev_status, cudaStream_t s) {
   if (p.B * p.H * p.n == 0) return cudaSuccess;
-  return p.d == 64 ? fmap_tc_t<64>(p, x, is_key, phi, dev_status, s)
-                   : fmap_tc_t<128>(p, x, is_key, phi, dev_status, s);
+  return p.d == 64 ? fmap_tc_t<64>(p, 1, &x, &is_key, &phi, &off, dev_status, s)
+                   : fmap_tc_t<128>(p, 1, &x, &is_key, &phi, &off, dev_status, s);
+}
+
+cudaError_t launch_fmap_tc_qk(const Problem& p, const void* q, const void* k, void* phq,
+                              void* phk, float2* offq, float2* offk, int* dev_status,
+                              cudaStream_t s) {
+  if (p.B * p.H * p.n == 0) return cudaSuccess;
+  const void* x[2] = {q, k};
+  const int key[2] = {0, 1};
+  void* phi[2] = {phq, phk};
+  float2* off[2] = {offq, offk};
+  return p.d == 64 ? fmap_tc_t<64>(p, 2, x, key, phi, off, dev_status, s)
+                   : fmap_tc_t<128>(p, 2, x, key, phi, off, dev_status, s);
 }
 
 template <int D>
 static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, const void* phq,
                              const void* phk, float* loss_rows, float* partial, float* head_sum,
-                             float* stats, int* dev_status, cudaStream_t s) {
+                             float* stats, float4* rows4, int* dev_status, cudaStream_t s) {
   LossArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
@@ -504,6 +618,7 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.loss_rows = loss_rows;
   a.partial = partial;
   a.stats = reinterpret_cast<float2*>(stats);
+  a.rows4 = rows4;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
@@ -512,10 +627,10 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.NT = ceil_div(p.n, kTile);
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   const size_t smem = LossCfg<D>::ALLOC;
-  cudaError_t e =
-      cudaFuncSetAttribute(loss_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = rows4 ? loss_tc_kernel<D, true> : loss_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  loss_tc_kernel<D><<<(unsigned)(U * a.NT), kLossThreads, smem, s>>>(a);
+  kern<<<(unsigned)(U * a.NT), kLossThreads, smem, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   sum_partials_tc_kernel<<<ceil_div(U, 128), 128, 0, s>>>(partial, head_sum, (int64_t)U, a.NT);
   return cudaGetLastError();
@@ -523,10 +638,11 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
 
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
-                           float* stats, int* dev_status, cudaStream_t s) {
-  return p.d == 64
-             ? loss_tc_t<64>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, dev_status, s)
-             : loss_tc_t<128>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, dev_status, s);
+                           float* stats, float4* rows4, int* dev_status, cudaStream_t s) {
+  return p.d == 64 ? loss_tc_t<64>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, rows4,
+                                   dev_status, s)
+                   : loss_tc_t<128>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, rows4,
+                                    dev_status, s);
 }
 
 int loss_tc_tile() { return kTile; }

@@ -123,6 +123,8 @@ struct PrefillArgs {
   float* z_out;     // [U][DPP] or null
   const float* bq;
   const float* bk;
+  const float2* offq;   // softmax map: [U][NT*128] per-row offsets (log2 units), else null
+  const float2* offk;
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -406,6 +408,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     if (__syncthreads_or(failed)) { failed = true; break; }
 
     // ================= epilogue 1: features, S_bf16, z =================
+    // softmax map: phi = [exp(h - c+); exp(-h - c-)] with this row's offsets
+    float2 oq = make_float2(0.f, 0.f), ok_ = make_float2(0.f, 0.f);
+    if (KIND == HH_FMAP_HEDGEHOG && A.offq && row < nvalid) {
+      const size_t r = (size_t)unit * A.NT * kTile + (size_t)r0 + row;
+      oq = A.offq[r];
+      ok_ = A.offk[r];
+    }
     // -- phi(Q) into TMEM, denominator part phi(q) . z_before
     {
       float dq = 0.f;
@@ -426,8 +435,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
           const int l = half * HC + j;
           const float h0 = __uint_as_float(hv[j]) + bq_s[l];
           const float h1 = __uint_as_float(hv[j + 1]) + bq_s[l + 1];
-          const uint32_t p = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
-          const uint32_t m = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+          const uint32_t p = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -oq.x)),
+                                       ex2_approx(fmaf(h1, kLog2e, -oq.x)));
+          const uint32_t m = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -oq.y)),
+                                       ex2_approx(fmaf(-h1, kLog2e, -oq.y)));
           pp[j / 2] = p;
           pn[j / 2] = m;
           dq += bf16_lo(p) * z_s[l] + bf16_hi(p) * z_s[l + 1] + bf16_lo(m) * z_s[D + l] +
@@ -482,8 +493,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
             const int l = half * HC + c + j;
             const float h0 = __uint_as_float(hv[j]) + bk_s[l];
             const float h1 = __uint_as_float(hv[j + 1]) + bk_s[l + 1];
-            uint32_t p = pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e));
-            uint32_t m = pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e));
+            uint32_t p = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -ok_.x)),
+                                   ex2_approx(fmaf(h1, kLog2e, -ok_.x)));
+            uint32_t m = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -ok_.y)),
+                                   ex2_approx(fmaf(-h1, kLog2e, -ok_.y)));
             if (!valid) p = m = 0u;
             wp_[j / 2] = p;
             wn_[j / 2] = m;
@@ -844,6 +857,9 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   a.z_out = z_out;
   a.bq = p.bq;
   a.bk = p.Wk ? p.bk : p.bq;
+  a.offq = p.offq;
+  a.offk = p.offk;
+  if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);

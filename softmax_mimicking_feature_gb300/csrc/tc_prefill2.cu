@@ -75,6 +75,8 @@ struct Args2 {
   float* S_out;
   float* z_out;
   const float* bias;
+  const float2* offq;   // softmax map: [U][NT*128] per-row offsets (log2 units) of q and k
+  const float2* offk;
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -87,6 +89,9 @@ __device__ __forceinline__ uint32_t lane_base(int warp) {
 
 // The bound of 384 threads caps registers at 168 per thread: warps 0, 4, 8
 // (and 1, 5, 9) share one SM sub-partition's 16K registers.
+// SM: softmax-over-features map, phi = [exp(h - c+); exp(-h - c-)] with the
+// per-row offsets from offq / offk (no bias).
+template <bool SM>
 __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_constant__ Args2 A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -346,6 +351,14 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       const uint32_t par = (i >> 1) & 1;
       const uint32_t base = sb + slot_off(s);
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
+      float2 oq = make_float2(0.f, 0.f), ok_ = make_float2(0.f, 0.f);
+      if constexpr (SM) {
+        if (valid) {
+          const size_t r = (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE + row;
+          oq = A.offq[r];
+          ok_ = A.offk[r];
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + s), par, wp))) { good = false; return; }
       tc_fence_after();
       // phi(Q): H_Q columns [32c, 32c+32) -> packed columns [16c, +16) and [32 + 16c, +16)
@@ -358,8 +371,13 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
           // (h + b) log2(e) in one FFMA: the bias is stored pre-scaled
           const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, bq_s[32 * c + j]);
           const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, bq_s[32 * c + j + 1]);
-          pp[j / 2] = pack_bf16(ex2_approx(a0), ex2_approx(a1));
-          pn[j / 2] = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+          if constexpr (SM) {
+            pp[j / 2] = pack_bf16(ex2_approx(a0 - oq.x), ex2_approx(a1 - oq.x));
+            pn[j / 2] = pack_bf16(ex2_approx(-a0 - oq.y), ex2_approx(-a1 - oq.y));
+          } else {
+            pp[j / 2] = pack_bf16(ex2_approx(a0), ex2_approx(a1));
+            pn[j / 2] = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+          }
         }
         tc_fence_before();
         named_bar_sync(2 + g, 64);   // both warps of these lanes hold their H_Q columns
@@ -379,8 +397,13 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
             const int j = 8 * q4 + 2 * e;
             const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, bq_s[32 * c + j]);
             const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, bq_s[32 * c + j + 1]);
-            wpos[e] = valid ? pack_bf16(ex2_approx(a0), ex2_approx(a1)) : 0u;
-            wneg[e] = valid ? pack_bf16(ex2_approx(-a0), ex2_approx(-a1)) : 0u;
+            if constexpr (SM) {
+              wpos[e] = valid ? pack_bf16(ex2_approx(a0 - ok_.x), ex2_approx(a1 - ok_.x)) : 0u;
+              wneg[e] = valid ? pack_bf16(ex2_approx(-a0 - ok_.y), ex2_approx(-a1 - ok_.y)) : 0u;
+            } else {
+              wpos[e] = valid ? pack_bf16(ex2_approx(a0), ex2_approx(a1)) : 0u;
+              wneg[e] = valid ? pack_bf16(ex2_approx(-a0), ex2_approx(-a1)) : 0u;
+            }
           }
           st_shared_v4(base + S_PHK + sw128_chunk(row, 4 * c + q4), wpos[0], wpos[1], wpos[2],
                        wpos[3]);
@@ -570,6 +593,9 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   a.S_out = S_out;
   a.z_out = z_out;
   a.bias = p.bq;
+  a.offq = p.offq;
+  a.offk = p.offk;
+  if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
@@ -578,10 +604,11 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc2_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  auto kern = p.softmax ? prefill_tc2_kernel<true> : prefill_tc2_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  prefill_tc2_kernel<<<(unsigned)(U * pl.P), kThreads, SMEM_BYTES, s>>>(a);
+  kern<<<(unsigned)(U * pl.P), kThreads, SMEM_BYTES, s>>>(a);
   return cudaGetLastError();
 }
 

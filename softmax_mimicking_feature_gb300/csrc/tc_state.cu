@@ -98,6 +98,7 @@ struct StateArgs {
   CUtensorMap tk, tv, tw;
   float* ws;          // [U][P-1][DPP*D + DPP]: S (ws_s_index layout) then z
   const float* bias;  // [H][D] of the key map (Hedgehog) or null
+  const float2* off;  // [U][NT*128] softmax-map offsets of the keys (log2 units) or null
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -289,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
       if constexpr (HH) {
         constexpr int HC = D / 2;  // H columns of this warp's half
+        // softmax map: phi = [exp(h - c+); exp(-h - c-)], offsets in log2 units
+        float2 o = make_float2(0.f, 0.f);
+        if (A.off && valid)
+          o = A.off[(size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE + row];
         if (!__all_sync(0xffffffffu, mbar_wait(bar(SB_G1), i & 1, wp))) break;
         tc_fence_after();
         uint32_t hv[HC];
@@ -302,8 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
         for (int j = 0; j < HC; j += 2) {
           const float h0 = __uint_as_float(hv[j]) + b_s[HC * c + j];
           const float h1 = __uint_as_float(hv[j + 1]) + b_s[HC * c + j + 1];
-          wpos[j / 2] = valid ? pack_bf16(ex2_approx(h0 * kLog2e), ex2_approx(h1 * kLog2e)) : 0u;
-          wneg[j / 2] = valid ? pack_bf16(ex2_approx(-h0 * kLog2e), ex2_approx(-h1 * kLog2e)) : 0u;
+          wpos[j / 2] = valid ? pack_bf16(ex2_approx(fmaf(h0, kLog2e, -o.x)),
+                                          ex2_approx(fmaf(h1, kLog2e, -o.x)))
+                              : 0u;
+          wneg[j / 2] = valid ? pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -o.y)),
+                                          ex2_approx(fmaf(-h1, kLog2e, -o.y)))
+                              : 0u;
         }
         // the panels are free once G2(i-1) has read them
         if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(SB_G2), (i - 1) & 1, wp))) break;
@@ -404,7 +413,8 @@ constexpr uint32_t OFF_W = 0;                          // W: 2 panels [128 i x 6
 constexpr uint32_t OFF_K = 32768;                      // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * XT;             // 2 stages
 constexpr uint32_t OFF_ZX = OFF_V + 2 * XT;            // float[2][128] z exchange
-constexpr uint32_t OFF_BAR = OFF_ZX + 1024;
+constexpr uint32_t OFF_OX = OFF_ZX + 1024;             // float2[2][128] softmax-map offsets
+constexpr uint32_t OFF_BAR = OFF_OX + 2048;
 enum { B_W = 0, B_LDK = 1, B_LDV = 3, B_G1 = 5, B_E1 = 7, B_G2 = 9, B_COUNT = 11 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
@@ -448,11 +458,16 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     for (int x = 0; x < 2; ++x)
       tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)unit);
   };
+  // V(i) (and, for the softmax map, the tile's per-token offsets, whose smem
+  // buffer is free for the same reason as V's: E1(i-2) and G2(i-2) are done)
   auto load_v = [&](int i) {
     const uint32_t dst = sb + OFF_V + (i & 1) * XT, b = bar(B_LDV + (i & 1));
-    mbar_expect_tx(b, XT);
+    mbar_expect_tx(b, XT + (A.off ? TILE * 8 : 0));
     for (int x = 0; x < 2; ++x)
       tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+    if (A.off)
+      bulk_load(sb + OFF_OX + (i & 1) * TILE * 8,
+                A.off + (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE, TILE * 8, b);
   };
   if (warp == 8 && lane == 0 && nt > 0) {
     mbar_expect_tx(bar(B_W), D * D * 2);
@@ -563,20 +578,31 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const int j = 32 * (warp & 3) + lane;
     const uint32_t lb = lane_base(warp);
     const float bj = A.bias ? A.bias[(size_t)h * D + j] * kLog2e : 0.f;
+    float2* ox = reinterpret_cast<float2*>(sm + OFF_OX);
     for (int i = 0; i < nt; ++i) {
       const int b = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + b), (i >> 1) & 1, wp))) break;
+      // softmax map: the offsets of tile i landed with V(i)
+      if (A.off && !__all_sync(0xffffffffu, mbar_wait(bar(B_LDV + b), (i >> 1) & 1, wp))) break;
       tc_fence_after();
       const int64_t tok0 = (int64_t)(t_begin + i) * TILE + 64 * c;
       uint32_t hv[64];
       tmem_ld64(tmem + lb + TM_H(b) + 64 * c, hv);
       uint32_t pp[32], pn[32];
+      const float2* oxt = ox + b * TILE + 64 * c;
 #pragma unroll
       for (int t = 0; t < 64; t += 2) {
         const float a0 = fmaf(__uint_as_float(hv[t]), kLog2e, bj);
         const float a1 = fmaf(__uint_as_float(hv[t + 1]), kLog2e, bj);
-        uint32_t wpos = pack_bf16(ex2_approx(a0), ex2_approx(a1));
-        uint32_t wneg = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+        uint32_t wpos, wneg;
+        if (A.off) {
+          const float4 o2 = *reinterpret_cast<const float4*>(oxt + t);   // tokens t, t+1
+          wpos = pack_bf16(ex2_approx(a0 - o2.x), ex2_approx(a1 - o2.z));
+          wneg = pack_bf16(ex2_approx(-a0 - o2.y), ex2_approx(-a1 - o2.w));
+        } else {
+          wpos = pack_bf16(ex2_approx(a0), ex2_approx(a1));
+          wneg = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+        }
         if (tok0 + t >= A.n) wpos = wneg = 0u;
         else if (tok0 + t + 1 >= A.n) { wpos &= 0xFFFFu; wneg &= 0xFFFFu; }
         pp[t / 2] = wpos;
@@ -894,6 +920,8 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   if (!ok) return cudaErrorInvalidValue;
   a.ws = reinterpret_cast<float*>(ws);
   a.bias = p.Wk ? p.bk : p.bq;
+  a.off = p.offk;
+  if (p.softmax && !p.offk) return cudaErrorInvalidValue;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
