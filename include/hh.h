@@ -180,6 +180,28 @@ HH_API hh_status hh_linattn_fwd_causal_noalloc(const hh_fmap* fmap, int dtype, c
                                                int64_t n, int chunk, void* y, float* S_out,
                                                float* z_out, int* dev_status, void* stream);
 
+/* Bytes of device workspace hh_linattn_fwd_causal_from_state needs (0 when none). */
+HH_API size_t hh_fwd_from_state_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H,
+                                                int64_t n, int chunk);
+
+/* Causal prefill continuing from a given state: token t of this call sees
+ * S0 + sum_{j<=t} phi(k_j)^T v_j and z0 + sum_{j<=t} phi(k_j), as if the
+ * tokens that produced S0, z0 had come first.  Source: "Complexity Analysis"
+ * (the running sums S and z carry all earlier tokens).
+ * S0: [B][H][d'p][d] and z0: [B][H][d'p] float32 in the layout of S_out /
+ * z_out (what hh_linattn_fwd_causal exports and hh_linattn_decode_step
+ * updates); both required.  S_out / z_out may alias S0 / z0 (updated in
+ * place).  Other arguments as hh_linattn_fwd_causal; the workspace must be at
+ * least hh_fwd_from_state_workspace_bytes(...) bytes.  Taylor states are
+ * folded onto the symmetric feature pairs (rows (i, j) and (j, i) enter as
+ * their sum), which leaves every output unchanged. */
+HH_API hh_status hh_linattn_fwd_causal_from_state(const hh_fmap* fmap, int dtype, const void* q,
+                                                  const void* k, const void* v, int64_t B, int H,
+                                                  int64_t n, int chunk, const float* S0,
+                                                  const float* z0, void* y, float* S_out,
+                                                  float* z_out, void* workspace, size_t ws_bytes,
+                                                  int* dev_status, void* stream);
+
 /* One recurrent decode step for B sequences x H heads.
  * Source: "Complexity Analysis" (running sums S and z, output
  * phi(q_t) S_t / phi(q_t).z_t); the state after the step includes token t.

@@ -13,6 +13,8 @@ from .api import (  # noqa: F401
     fwd_workspace_bytes,
     linattn_decode_step,
     linattn_fwd_causal,
+    linattn_fwd_causal_from_state,
+    fwd_from_state_workspace_bytes,
     loss_workspace_bytes,
     loss_grad_workspace_bytes,
     mimicry_loss,

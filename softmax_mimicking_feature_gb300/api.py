@@ -17,7 +17,8 @@ from . import _abi
 
 __all__ = ["FeatureMap", "fmap_dim", "feature_map", "fwd_workspace_bytes", "fwd_plan",
            "linattn_fwd_causal", "linattn_decode_step", "loss_workspace_bytes",
-           "mimicry_loss", "mimicry_stats", "loss_grad_workspace_bytes", "mimicry_loss_grad",
+           "mimicry_loss", "mimicry_stats", "fwd_from_state_workspace_bytes",
+           "linattn_fwd_causal_from_state", "loss_grad_workspace_bytes", "mimicry_loss_grad",
            "HHError"]
 
 HHError = _abi.HHError
@@ -138,6 +139,46 @@ def linattn_fwd_causal(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, v: torc
         _ptr(z), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
         "hh_linattn_fwd_causal")
     return (y, S, z) if return_state else y
+
+
+def fwd_from_state_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int,
+                                   chunk: int = 0) -> int:
+    s = fm.struct()
+    return int(_abi.lib().hh_fwd_from_state_workspace_bytes(ctypes.byref(s), _DTYPES[dtype], B, H,
+                                                            n, chunk))
+
+
+def linattn_fwd_causal_from_state(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
+                                  v: torch.Tensor, S0: torch.Tensor, z0: torch.Tensor,
+                                  chunk: int = 0, y: Optional[torch.Tensor] = None,
+                                  return_state: bool = False, in_place: bool = False,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Causal linear attention continuing from state (S0, z0)
+    (hh_linattn_fwd_causal_from_state).
+
+    Returns y, or (y, S, z) with ``return_state``; ``in_place`` writes the
+    final state over S0, z0 (and returns them as S, z).
+    """
+    B, H, n, d = q.shape
+    if y is None:
+        y = torch.empty_like(q)
+    S = z = None
+    if in_place:
+        S, z = S0, z0
+    elif return_state:
+        S = torch.empty_like(S0)
+        z = torch.empty_like(z0)
+    need = fwd_from_state_workspace_bytes(fm, q.dtype, B, H, n, chunk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = fm.struct()
+    _abi.check(_abi.lib().hh_linattn_fwd_causal_from_state(
+        ctypes.byref(s), _dt(q), _ptr(q), _ptr(k), _ptr(v), B, H, n, chunk, _ptr(S0), _ptr(z0),
+        _ptr(y), _ptr(S), _ptr(z), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
+        "hh_linattn_fwd_causal_from_state")
+    return (y, S, z) if (return_state or in_place) else y
 
 
 def linattn_decode_step(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -191,16 +191,29 @@ hh_status hh_feature_map(const hh_fmap* fmap, int dtype, const void* x, int is_k
   return cuda_status(launch_fmap_simt(p, x, is_key, phi_out, nullptr, (cudaStream_t)stream));
 }
 
-size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
-                              int chunk) {
+// Workspace of the prefill (with or without an initial state).
+static size_t fwd_ws_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
+                           bool from_state) {
   Problem p;
   if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
-  (void)chunk;
   if (B * H * n == 0) return 0;
+  p.has_init = from_state;
   const TcPlan pl = plan_prefill_tc(p);
   if (!pl.supported) return 0;
   // softmax map: the q and k row offsets follow the segment states
   return align256(pl.ws_bytes) + (p.softmax ? 2 * softmax_off_bytes(p) : 0);
+}
+
+size_t hh_fwd_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n,
+                              int chunk) {
+  (void)chunk;
+  return fwd_ws_bytes(fmap, dtype, B, H, n, false);
+}
+
+size_t hh_fwd_from_state_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H,
+                                         int64_t n, int chunk) {
+  (void)chunk;
+  return fwd_ws_bytes(fmap, dtype, B, H, n, true);
 }
 
 hh_status hh_fwd_plan(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n, int chunk,
@@ -222,34 +235,49 @@ hh_status hh_fwd_plan(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t 
   return HH_OK;
 }
 
-hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, const void* k,
-                                const void* v, int64_t B, int H, int64_t n, int chunk, void* y,
-                                float* S_out, float* z_out, void* workspace, size_t ws_bytes,
-                                int* dev_status, void* stream) {
+// Shared body of the prefill entry points; S0 / z0 null = start from zero.
+static hh_status fwd_impl(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                          const void* v, int64_t B, int H, int64_t n, int chunk, const float* S0,
+                          const float* z0, void* y, float* S_out, float* z_out, void* workspace,
+                          size_t ws_bytes, int* dev_status, void* stream) {
   Problem p;
   hh_status st = make_problem(fmap, dtype, B, H, n, &p);
   if (st != HH_OK) return st;
   if (chunk != 0 && chunk != 64 && chunk != 128) return HH_ERR_UNSUPPORTED;
   if ((S_out == nullptr) != (z_out == nullptr)) return HH_ERR_INVALID_ARG;
+  const bool from_state = S0 != nullptr;
+  if (from_state && !z0) return HH_ERR_INVALID_ARG;
   if (B == 0) return HH_OK;
   if (n > 0 && (!q || !k || !v || !y)) return HH_ERR_INVALID_ARG;
-  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, p.Wq, p.bq, p.Wk, p.bk, workspace})) !=
-      HH_OK)
+  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, S0, z0, p.Wq, p.bq, p.Wk, p.bk,
+                                workspace})) != HH_OK)
     return st;
   if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
-  const size_t need = hh_fwd_workspace_bytes(fmap, dtype, B, H, n, chunk);
+  const size_t need = fwd_ws_bytes(fmap, dtype, B, H, n, from_state);
   if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
+  const size_t s_bytes = sizeof(float) * B * H * p.dpp * p.d, z_bytes = sizeof(float) * B * H * p.dpp;
   if (n == 0) {
-    // empty sequences: the state is the empty sum
+    // no tokens: the state is the initial one (or the empty sum)
     if (S_out) {
-      cudaError_t e = cudaMemsetAsync(S_out, 0, sizeof(float) * B * H * p.dpp * p.d, s);
-      if (e == cudaSuccess) e = cudaMemsetAsync(z_out, 0, sizeof(float) * B * H * p.dpp, s);
+      cudaError_t e;
+      if (from_state) {
+        e = S_out == S0 ? cudaSuccess
+                        : cudaMemcpyAsync(S_out, S0, s_bytes, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess && z_out != z0)
+          e = cudaMemcpyAsync(z_out, z0, z_bytes, cudaMemcpyDeviceToDevice, s);
+      } else {
+        e = cudaMemsetAsync(S_out, 0, s_bytes, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(z_out, 0, z_bytes, s);
+      }
       return cuda_status(e);
     }
     return HH_OK;
   }
+  p.has_init = from_state;
+  p.S0 = S0;
+  p.z0 = z0;
   const TcPlan pl = plan_prefill_tc(p);
   if (pl.supported) {
     if (p.softmax) {
@@ -265,6 +293,25 @@ hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, c
     return cuda_status(launch_prefill_tc(p, pl, q, k, v, y, S_out, z_out, workspace, dev_status, s));
   }
   return cuda_status(launch_prefill_simt(p, q, k, v, y, S_out, z_out, s));
+}
+
+hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                                const void* v, int64_t B, int H, int64_t n, int chunk, void* y,
+                                float* S_out, float* z_out, void* workspace, size_t ws_bytes,
+                                int* dev_status, void* stream) {
+  return fwd_impl(fmap, dtype, q, k, v, B, H, n, chunk, nullptr, nullptr, y, S_out, z_out,
+                  workspace, ws_bytes, dev_status, stream);
+}
+
+hh_status hh_linattn_fwd_causal_from_state(const hh_fmap* fmap, int dtype, const void* q,
+                                           const void* k, const void* v, int64_t B, int H,
+                                           int64_t n, int chunk, const float* S0,
+                                           const float* z0, void* y, float* S_out, float* z_out,
+                                           void* workspace, size_t ws_bytes, int* dev_status,
+                                           void* stream) {
+  if (B > 0 && (!S0 || !z0)) return HH_ERR_INVALID_ARG;
+  return fwd_impl(fmap, dtype, q, k, v, B, H, n, chunk, S0, z0, y, S_out, z_out, workspace,
+                  ws_bytes, dev_status, stream);
 }
 
 hh_status hh_linattn_decode_step(const hh_fmap* fmap, int dtype, const void* q, const void* k,

@@ -31,6 +31,12 @@ struct Problem {
   bool softmax = false;
   const float2* offq = nullptr;
   const float2* offk = nullptr;
+  // Continuation: the prefill starts from this state (public layout, as the
+  // S_out / z_out of a prefill or the state of decode) instead of zero.
+  // has_init sizes the workspace; S0 / z0 are set for the launch.
+  bool has_init = false;
+  const float* S0 = nullptr;
+  const float* z0 = nullptr;
 };
 
 // ---- element access in float32 for either storage type -------------------
@@ -77,6 +83,7 @@ struct TcPlan {
   int L = 1;         // tiles per segment
   int launches = 1;  // kernel launches per call
   size_t ws_bytes = 0;
+  size_t init_offset = 0;   // continuation: byte offset of the initial state in the workspace
 };
 TcPlan plan_prefill_tc(const Problem& p);
 // Floats of one segment state in the prefill workspace: S then z.  The Taylor
@@ -94,16 +101,18 @@ cudaError_t launch_state_tc(const Problem& p, const TcPlan& pl, const void* k, c
                             void* ws, int* dev_status, cudaStream_t s);
 
 // Output pass of the d = 64 Hedgehog prefill with two tiles in flight per CTA.
+// init: the initial state in workspace layout (continuation) or null.
 cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const void* q,
                                    const void* k, const void* v, void* y, float* S_out,
-                                   float* z_out, const void* ws, int* dev_status, cudaStream_t s);
+                                   float* z_out, const void* ws, const float* init,
+                                   int* dev_status, cudaStream_t s);
 
 // Output pass of the Taylor (d = 16) prefill: scores from the closed form
 // 1 + s + s^2/2 with s = q . k, state contractions on the features.
 cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const void* q,
                                       const void* k, const void* v, void* y, float* S_out,
-                                      float* z_out, const void* ws, int* dev_status,
-                                      cudaStream_t s);
+                                      float* z_out, const void* ws, const float* init,
+                                      int* dev_status, cudaStream_t s);
 
 // Gradient of the summed mimicry loss w.r.t. the Hedgehog map (CUDA cores,
 // fp32 arithmetic): phi(q), phi(k) precomputed; stats [U][n][3]; dh [U][n][d].

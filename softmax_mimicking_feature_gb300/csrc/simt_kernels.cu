@@ -124,6 +124,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                     T* __restrict__ y, float* __restrict__ S_out, float* __restrict__ z_out,
+                    const float* __restrict__ S0, const float* __restrict__ z0,
                     const T* __restrict__ Wq, const float* __restrict__ bq,
                     const T* __restrict__ Wk, const float* __restrict__ bk, int kind,
                     int softmax, int d, int dpp, int H, int64_t n, int C) {
@@ -148,8 +149,9 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
-  for (int i = tid; i < dpp * d; i += kThreads) S[i] = 0.f;
-  for (int i = tid; i < dpp; i += kThreads) z[i] = 0.f;
+  // the state before the first token: zero, or the given one (continuation)
+  for (int i = tid; i < dpp * d; i += kThreads) S[i] = S0 ? S0[(size_t)bh * dpp * d + i] : 0.f;
+  for (int i = tid; i < dpp; i += kThreads) z[i] = z0 ? z0[(size_t)bh * dpp + i] : 0.f;
   __syncthreads();
 
   for (int64_t c0 = 0; c0 < n; c0 += C) {
@@ -398,7 +400,8 @@ static cudaError_t prefill_simt_t(const Problem& p, const void* q, const void* k
   const T* Wk = (const T*)(p.Wk ? p.Wk : p.Wq);
   const float* bk = p.Wk ? p.bk : p.bq;
   prefill_simt_kernel<T><<<(unsigned)units, kThreads, smem, s>>>(
-      (const T*)q, (const T*)k, (const T*)v, (T*)y, S_out, z_out, (const T*)p.Wq, p.bq, Wk, bk,
+      (const T*)q, (const T*)k, (const T*)v, (T*)y, S_out, z_out, p.S0, p.z0, (const T*)p.Wq,
+      p.bq, Wk, bk,
       p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.n, C);
   return cudaGetLastError();
 }

@@ -33,6 +33,7 @@
 
 #include <algorithm>
 
+#include "taylor_pack.cuh"
 #include "tc_ptx.cuh"
 
 namespace hh {
@@ -119,6 +120,7 @@ struct PrefillArgs {
   CUtensorMap tq, tk, tv, twq, twk;
   void* y;
   float* ws;        // [U][P-1][DPP*D + DPP]: segment states (S then z), scanned in place
+  const float* init;  // [U][DPP*D + DPP] initial state in the same layout, or null
   float* S_out;     // [U][DPP][D] or null
   float* z_out;     // [U][DPP] or null
   const float* bq;
@@ -305,8 +307,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     }
   }
   const size_t seg_elems = (size_t)C::DPP * D + C::DPP;
+  // the state before this segment: the scanned prefix, the initial state
+  // (continuation) or none
   const float* prefix = seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * seg_elems
-                                         : nullptr;
+                                : (A.init ? A.init + (size_t)unit * seg_elems : nullptr);
   // initial z: the state of the tokens before this segment
   for (int f = tid; f < SM::ZN; f += kThreads)
     z_s[f] = (prefix && f < C::DPP) ? __ldcg(prefix + (size_t)C::DPP * D + f) : 0.f;
@@ -747,14 +751,23 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 }
 
 // In-place inclusive scan over the P-1 segment states of every unit, one
-// float4 position per thread, summed in segment order.
-__global__ void segment_scan_kernel(float4* __restrict__ ws, int64_t units, int pm1,
-                                    int64_t elems4) {
+// float4 position per thread, summed in segment order after the initial
+// state (continuation) when there is one.
+__global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __restrict__ init,
+                                    int64_t units, int pm1, int64_t elems4) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units * elems4) return;
   const int64_t u = i / elems4, e = i % elems4;
   float4* p = ws + (size_t)u * pm1 * elems4 + e;
   float4 acc = p[0];
+  if (init) {
+    const float4 x = init[(size_t)u * elems4 + e];
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
+    p[0] = acc;
+  }
   for (int s = 1; s < pm1; ++s) {
     const float4 x = p[(size_t)s * elems4];
     acc.x += x.x;
@@ -763,6 +776,41 @@ __global__ void segment_scan_kernel(float4* __restrict__ ws, int64_t units, int 
     acc.w += x.w;
     p[(size_t)s * elems4] = acc;
   }
+}
+
+// Initial state (continuation) from the public layout -- S [dp_pub][D] and
+// z [dp_pub] per unit, as prefill exports it -- into the workspace layout of
+// the segment states (ws_s_index, then z).  Taylor keeps the 160 packed
+// features of taylor_pack.cuh: a pair (i, j), i < j, stands for public rows
+// r0 = (i, j) and r1 = (j, i), and phi_packed(q) . S_packed equals
+// phi_pub(q) . S_pub with S_packed = (S[r0] + S[r1]) / sqrt2; the diagonal,
+// the constant and the linear features map one to one.
+__global__ void init_state_kernel(const float* __restrict__ S0, const float* __restrict__ z0,
+                                  float* __restrict__ init, int64_t units, int D, int dp_ws,
+                                  int dp_pub, int taylor) {
+  const int64_t per = (int64_t)dp_ws * D + dp_ws;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= units * per) return;
+  const int64_t u = i / per, e = i % per;
+  const float* Su = S0 + (size_t)u * dp_pub * D;
+  const float* zu = z0 + (size_t)u * dp_pub;
+  const bool is_z = e >= (int64_t)dp_ws * D;
+  const int f = is_z ? (int)(e - (int64_t)dp_ws * D) : (int)(e / D);
+  const int c = is_z ? 0 : (int)(e % D);
+  auto pub = [&](int r) { return is_z ? zu[r] : Su[(size_t)r * D + c]; };
+  float val = 0.f;
+  if (!taylor) {
+    val = f < dp_pub ? pub(f) : 0.f;
+  } else {
+    int r0 = 0, r1 = 0;
+    float scale = 1.f;
+    const int cnt = tp::public_rows(f, r0, r1, scale);
+    if (cnt == 1) val = pub(r0);
+    else if (cnt == 2) val = (pub(r0) + pub(r1)) * scale;
+  }
+  float* dst = init + (size_t)u * per;
+  if (is_z) dst[(size_t)dp_ws * D + f] = val;
+  else dst[ws_s_index(f, c, D)] = val;
 }
 
 }  // namespace
@@ -828,6 +876,13 @@ TcPlan plan_prefill_tc(const Problem& p) {
   pl.launches = pl.P > 2 ? 3 : (pl.P > 1 ? 2 : 1);
   pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * (size_t)ws_segment_floats(p) * sizeof(float)
                          : 0;
+  if (p.has_init) {
+    // the initial state in workspace layout follows the segment states; the
+    // scan also runs for two segments
+    pl.init_offset = pl.ws_bytes;
+    pl.ws_bytes += (size_t)U * (size_t)ws_segment_floats(p) * sizeof(float);
+    pl.launches = 1 + (pl.P > 1 ? 3 : 1);
+  }
   return pl;
 }
 
@@ -870,21 +925,35 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   a.NT = pl.NT;
   a.sep_wk = p.Wk ? 1 : 0;
   const size_t smem = smem_bytes<KIND, D>();
+  float* init = nullptr;
+  if (p.S0) {
+    if (!p.has_init || !p.z0) return cudaErrorInvalidValue;
+    init = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + pl.init_offset);
+    const int64_t per = ws_segment_floats(p);
+    const int64_t total = (int64_t)U * per;
+    init_state_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+        p.S0, p.z0, init, (int64_t)U, D, (int)(per / (D + 1)), p.dpp,
+        KIND == HH_FMAP_TAYLOR2 ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  a.init = init;
   if (pl.P > 1) {
     cudaError_t e = launch_state_tc(p, pl, k, v, ws, dev_status, s);
     if (e != cudaSuccess) return e;
-    if (pl.P > 2) {
+    if (pl.P > 2 || init) {
       const int64_t elems4 = ws_segment_floats(p) / 4;
       const int64_t n4 = (int64_t)U * elems4;
       segment_scan_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-          reinterpret_cast<float4*>(ws), (int64_t)U, pl.P - 1, elems4);
+          reinterpret_cast<float4*>(ws), reinterpret_cast<const float4*>(init), (int64_t)U,
+          pl.P - 1, elems4);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
   if (KIND == HH_FMAP_HEDGEHOG && D == 64 && !p.Wk)
-    return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
+    return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
   if constexpr (KIND == HH_FMAP_TAYLOR2) {
-    return launch_prefill_out_taylor(p, pl, q, k, v, y, S_out, z_out, ws, dev_status, s);
+    return launch_prefill_out_taylor(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
   } else {
     auto kern = prefill_tc_kernel<KIND, D>;
     cudaError_t e =

@@ -72,6 +72,7 @@ struct Args2 {
   CUtensorMap tq, tk, tv, tw;
   __nv_bfloat16* y;
   const float* ws;   // [U][P-1][DP*D + DP] inclusive prefixes of segment states
+  const float* init; // [U][DP*D + DP] initial state (continuation), same layout, or null
   float* S_out;
   float* z_out;
   const float* bias;
@@ -172,11 +173,13 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // initial state: zeros, or the prefix of the preceding segments
+  // initial state: the prefix of the preceding segments, the given initial
+  // state (continuation, first segment) or zeros
   if (warp < 4) {
     const int f = 32 * warp + lane;  // feature = TMEM lane
     const float* prefix =
-        seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * (size_t)(DP * D + DP) : nullptr;
+        seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * (size_t)(DP * D + DP)
+                : (A.init ? A.init + (size_t)unit * (DP * D + DP) : nullptr);
     uint32_t r[32];
     for (int c0 = 0; c0 < D; c0 += 32) {
 #pragma unroll
@@ -580,7 +583,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 // feature map shared by queries and keys.
 cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const void* q,
                                    const void* k, const void* v, void* y, float* S_out,
-                                   float* z_out, const void* ws, int* dev_status, cudaStream_t s) {
+                                   float* z_out, const void* ws, const float* init,
+                                   int* dev_status, cudaStream_t s) {
   Args2 a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
@@ -590,6 +594,7 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
+  a.init = init;
   a.S_out = S_out;
   a.z_out = z_out;
   a.bias = p.bq;

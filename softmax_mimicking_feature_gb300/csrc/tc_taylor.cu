@@ -59,6 +59,7 @@ struct ArgsT {
   CUtensorMap tq, tk, tv;
   __nv_bfloat16* y;
   const float* ws;   // [U][P-1][DP*D + DP] inclusive prefixes (ws_s_index layout, then z)
+  const float* init; // [U][DP*D + DP] initial state (continuation), same layout, or null
   float* S_out;      // [U][288][D] (public feature order) or null
   float* z_out;      // [U][288]
   int* dev_status;
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
   if (warp < 8) {
     const int c = warp >> 2;
     const float* prefix =
-        seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * (size_t)(DP * D + DP) : nullptr;
+        seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * (size_t)(DP * D + DP)
+                : (A.init ? A.init + (size_t)unit * (DP * D + DP) : nullptr);
     for (int mb = c; mb < 2; mb += 2) {
       const int f = 128 * mb + 32 * (warp & 3) + lane;
       uint32_t r[32];
@@ -532,8 +534,8 @@ bool make_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes
 // Output pass of the Taylor (d = 16) prefill: U * P CTAs, one per segment.
 cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const void* q,
                                       const void* k, const void* v, void* y, float* S_out,
-                                      float* z_out, const void* ws, int* dev_status,
-                                      cudaStream_t s) {
+                                      float* z_out, const void* ws, const float* init,
+                                      int* dev_status, cudaStream_t s) {
   ArgsT a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
@@ -543,6 +545,7 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
+  a.init = init;
   a.S_out = S_out;
   a.z_out = z_out;
   a.dev_status = dev_status;
