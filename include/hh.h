@@ -110,6 +110,12 @@ typedef struct {
   const float* bq;     /* [H][d] float32 or NULL                            */
   const void* Wk;      /* [H][d][d] or NULL (shared with Wq)                */
   const float* bk;     /* [H][d] or NULL; ignored when Wk is NULL           */
+  int32_t kv_heads;    /* key/value heads Hkv: 0 or H for one per query head;
+                        * else H is a multiple of Hkv and query head h reads
+                        * key/value head h / (H / Hkv) (grouped-query
+                        * attention): k, v are [B][Hkv][n][d] ([B][Hkv][d] for
+                        * decode).  Maps, states and outputs stay per query
+                        * head.                                              */
 } hh_fmap;
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -27,7 +27,8 @@ EXPORTED = ("hh_version", "hh_status_str", "hh_fmap_dim", "hh_feature_map",
 class HHFmap(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("Wq", ctypes.c_void_p), ("bq", ctypes.c_void_p),
-                ("Wk", ctypes.c_void_p), ("bk", ctypes.c_void_p)]
+                ("Wk", ctypes.c_void_p), ("bk", ctypes.c_void_p),
+                ("kv_heads", ctypes.c_int32)]
 
 
 class HHError(RuntimeError):

@@ -62,6 +62,7 @@ class FeatureMap:
     bq: Optional[torch.Tensor] = None
     Wk: Optional[torch.Tensor] = None
     bk: Optional[torch.Tensor] = None
+    kv_heads: int = 0    # grouped-query attention: k, v have this many heads (0: one per head)
 
     @property
     def kind_id(self) -> int:
@@ -75,6 +76,7 @@ class FeatureMap:
         s.bq = _ptr(self.bq)
         s.Wk = _ptr(self.Wk)
         s.bk = _ptr(self.bk)
+        s.kv_heads = int(self.kv_heads)
         return s
 
     def dim(self, padded: bool = True) -> int:

@@ -35,7 +35,7 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
               float* __restrict__ S, float* __restrict__ z, T* __restrict__ y,
               const T* __restrict__ Wq, const float* __restrict__ bq,
               const T* __restrict__ Wk, const float* __restrict__ bk, int kind, int softmax,
-              int d, int dpp, int H) {
+              int d, int dpp, int H, int G) {
   __shared__ float qs[128], ks[128], vs[128];
   __shared__ float phq[320], phk[320];
   __shared__ __align__(16) float ypart[kDecThreads * 4];
@@ -46,8 +46,9 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
   const int h = (int)(u % H);
   const int tid = threadIdx.x;
   load_vec(q + (size_t)u * d, qs, d, tid);
-  load_vec(k + (size_t)u * d, ks, d, tid);
-  load_vec(v + (size_t)u * d, vs, d, tid);
+  const int64_t ukv = kv_unit(u, H, G);   // k, v of this query head
+  load_vec(k + (size_t)ukv * d, ks, d, tid);
+  load_vec(v + (size_t)ukv * d, vs, d, tid);
   __syncthreads();
 
   // phi(q_t), phi(k_t)
@@ -202,11 +203,11 @@ static cudaError_t decode_t(const Problem& p, const void* q, const void* k, cons
   if (p.d % 4 == 0)
     decode_kernel<T, 4><<<(unsigned)units, kDecThreads, 0, s>>>(
         (const T*)q, (const T*)k, (const T*)v, S, z, (T*)y, (const T*)p.Wq, p.bq, Wk, bk,
-        p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H);
+        p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.G);
   else
     decode_kernel<T, 1><<<(unsigned)units, kDecThreads, 0, s>>>(
         (const T*)q, (const T*)k, (const T*)v, S, z, (T*)y, (const T*)p.Wq, p.bq, Wk, bk,
-        p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H);
+        p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.G);
   return cudaGetLastError();
 }
 

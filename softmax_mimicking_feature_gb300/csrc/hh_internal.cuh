@@ -18,6 +18,7 @@ struct Problem {
   int dpp;         // padded feature dim (row length of phi and S)
   int64_t B;
   int H;
+  int G = 1;       // query heads per key/value head (grouped-query attention)
   int64_t n;
   const void* Wq;
   const float* bq;
@@ -52,6 +53,12 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 constexpr float kInvSqrt2 = 0.70710678118654752440f;
 
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+// Key/value unit (batch * Hkv + key/value head) of query unit u = b * H + h
+// when G query heads share one key/value head.
+__host__ __device__ __forceinline__ int64_t kv_unit(int64_t u, int H, int G) {
+  return G == 1 ? u : (u / H) * (H / G) + (u % H) / G;
+}
+
 // Row stride of the softmax-map offset arrays.
 inline int64_t off_stride(int64_t n) { return (n + 127) / 128 * 128; }
 

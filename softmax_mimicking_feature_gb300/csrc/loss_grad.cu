@@ -106,7 +106,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_query_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
     const T* __restrict__ phk, float* __restrict__ stats, float* __restrict__ dhq, int d, int dpp,
-    int64_t n, int ntiles) {
+    int64_t n, int ntiles, int H, int G) {
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
   float m = -INFINITY, z = 0.f, asum = 0.f;
   for (int kt = 0; kt <= qt; ++kt) {
     __syncthreads();
-    load_tile(S.ys, k + u * n * d, (int64_t)kt * kT, n, d);
+    load_tile(S.ys, k + kv_unit(u, H, G) * n * d, (int64_t)kt * kT, n, d);
     load_tile(S.pys, phk + u * n * dpp, (int64_t)kt * kT, n, dpp);
     __syncthreads();
     for (int c = slot; c < kT; c += 8) {
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
   const int nf = dpp / 8;
   for (int kt = 0; kt <= qt; ++kt) {
     __syncthreads();
-    load_tile(S.ys, k + u * n * d, (int64_t)kt * kT, n, d);
+    load_tile(S.ys, k + kv_unit(u, H, G) * n * d, (int64_t)kt * kT, n, d);
     load_tile(S.pys, phk + u * n * dpp, (int64_t)kt * kT, n, dpp);
     __syncthreads();
     for (int c = slot; c < kT; c += 8) {
@@ -194,7 +194,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_key_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
     const T* __restrict__ phk, const float* __restrict__ stats, float* __restrict__ dhk, int d,
-    int dpp, int64_t n, int ntiles) {
+    int dpp, int64_t n, int ntiles, int H, int G) {
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) grad_key_kernel(
   const int64_t k0 = (int64_t)kt * kT;
   const int t = threadIdx.x, r = t / 8, slot = t % 8;   // r: key row of the tile
   const float scale = rsqrtf((float)d);
-  load_tile(S.xs, k + u * n * d, k0, n, d);
+  load_tile(S.xs, k + kv_unit(u, H, G) * n * d, k0, n, d);
   load_tile(S.pxs, phk + u * n * dpp, k0, n, dpp);
   float acc[32];
 #pragma unroll
@@ -241,14 +241,15 @@ __global__ void __launch_bounds__(kThreads) grad_key_kernel(
   write_dh(acc, S.pys, S.pxs, r, slot, d, dpp, n - k0, dhk + (u * n + k0) * d);
 }
 
-// dW[h][a][l] = sum_{b, t} x[b,h,t,a] dh[b,h,t,l] (+ the key side when shared),
+// dW[h][a][l] = sum_{b, t} x[b,h,t,a] dh[b,h,t,l] (+ the key side when shared);
+// a side whose x is raw k reads key/value head h / G (kvx1, kvx2),
 // db[h][l] = sum dh.  grid: (H * ceil(d / 32) * ceil(d / 32)), 256 threads:
 // thread -> (a, l) pairs of one 32 x 32 block; tokens in smem chunks of 32.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
     const T* __restrict__ x1, const float* __restrict__ dh1, const T* __restrict__ x2,
     const float* __restrict__ dh2, float* __restrict__ dW, float* __restrict__ db, int64_t B,
-    int H, int64_t n, int d) {
+    int H, int64_t n, int d, int G1, int G2) {
   __shared__ float xs[32][33];
   __shared__ float hs[32][33];
   const int nb = (d + 31) / 32;
@@ -261,12 +262,13 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
     const float* dh = side ? dh2 : dh1;
     for (int64_t b = 0; b < B; ++b) {
       const size_t base = ((size_t)b * H + h) * n;
+      const size_t xbase = (size_t)kv_unit((int64_t)b * H + h, H, side ? G2 : G1) * n;
       for (int64_t t0 = 0; t0 < n; t0 += 32) {
         __syncthreads();
         for (int i = t; i < 32 * 32; i += kThreads) {
           const int rr = i / 32, cc = i % 32;
           const bool ok = t0 + rr < n;
-          xs[rr][cc] = ok && a0 + cc < d ? to_f(x[(base + t0 + rr) * d + a0 + cc]) : 0.f;
+          xs[rr][cc] = ok && a0 + cc < d ? to_f(x[(xbase + t0 + rr) * d + a0 + cc]) : 0.f;
           hs[rr][cc] = ok && l0 + cc < d ? dh[(base + t0 + rr) * d + l0 + cc] : 0.f;
         }
         __syncthreads();
@@ -304,10 +306,12 @@ cudaError_t grad_t(const Problem& p, const void* q, const void* k, const void* p
                                 (int)smem)) != cudaSuccess)
     return e;
   grad_query_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
-      (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhq, p.d, p.dpp, p.n, ntiles);
+      (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhq, p.d, p.dpp, p.n, ntiles,
+      p.H, p.G);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   grad_key_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
-      (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhk, p.d, p.dpp, p.n, ntiles);
+      (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhk, p.d, p.dpp, p.n, ntiles,
+      p.H, p.G);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_grad_reduce(p, q, k, dhq, dhk, dWq, dbq, dWk, dbk, s);
 }
@@ -320,14 +324,14 @@ cudaError_t reduce_t(const Problem& p, const void* q, const void* k, const float
   const unsigned grid = (unsigned)(p.H * nb * nb);
   if (dWk) {   // separate key map: each side to its own parameters
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)q, dhq, (const T*)nullptr, nullptr,
-                                                    dWq, dbq, p.B, p.H, p.n, p.d);
+                                                    dWq, dbq, p.B, p.H, p.n, p.d, 1, 1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)k, dhk, (const T*)nullptr, nullptr,
-                                                    dWk, dbk, p.B, p.H, p.n, p.d);
+                                                    dWk, dbk, p.B, p.H, p.n, p.d, p.G, 1);
   } else {
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)q, dhq, (const T*)k, dhk, dWq, dbq,
-                                                    p.B, p.H, p.n, p.d);
+                                                    p.B, p.H, p.n, p.d, 1, p.G);
   }
   return cudaGetLastError();
 }

@@ -94,7 +94,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* __restrict__ bias,
                  T* __restrict__ phi, float2* __restrict__ off, int kind, int softmax, int d,
-                 int dpp, int H, int64_t n, int64_t rows) {
+                 int dpp, int H, int G, int64_t n, int64_t rows) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = kThreads / 32;
@@ -102,7 +102,9 @@ fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* 
   float* out = xs + 128;
   for (int64_t r = (int64_t)blockIdx.x * nwarps + warp; r < rows; r += (int64_t)gridDim.x * nwarps) {
     const int h = (int)((r / n) % H);
-    for (int k = lane; k < d; k += 32) xs[k] = to_f(x[r * d + k]);
+    // x row: of this query head, or of its key/value head (G > 1: keys)
+    const int64_t xr = kv_unit(r / n, H, G) * n + r % n;
+    for (int k = lane; k < d; k += 32) xs[k] = to_f(x[xr * d + k]);
     __syncwarp();
     const T* Wh = W ? W + (size_t)h * d * d : nullptr;
     const float* bh = bias ? bias + (size_t)h * d : nullptr;
@@ -127,7 +129,7 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
                     const float* __restrict__ S0, const float* __restrict__ z0,
                     const T* __restrict__ Wq, const float* __restrict__ bq,
                     const T* __restrict__ Wk, const float* __restrict__ bk, int kind,
-                    int softmax, int d, int dpp, int H, int64_t n, int C) {
+                    int softmax, int d, int dpp, int H, int G, int64_t n, int C) {
   extern __shared__ float sm[];
   float* S = sm;                       // [dpp][d]
   float* z = S + (size_t)dpp * d;      // [dpp]
@@ -142,6 +144,7 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
   const int64_t bh = blockIdx.x;
   const int h = (int)(bh % H);
   const size_t base = (size_t)bh * n * d;
+  const size_t kvbase = (size_t)kv_unit(bh, H, G) * n * d;   // k, v of this query head
   const T* Wqh = Wq ? Wq + (size_t)h * d * d : nullptr;
   const T* Wkh = Wk ? Wk + (size_t)h * d * d : nullptr;
   const float* bqh = bq ? bq + (size_t)h * d : nullptr;
@@ -160,8 +163,8 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       const int r = i / d;
       const bool ok = r < nc;
       xs[i] = ok ? to_f(q[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
-      xk[i] = ok ? to_f(k[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
-      vv[i] = ok ? to_f(v[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
+      xk[i] = ok ? to_f(k[kvbase + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
+      vv[i] = ok ? to_f(v[kvbase + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
     }
     __syncthreads();
     for (int r = warp; r < C; r += kThreads / 32) {
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads)
 loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
                  const T* __restrict__ phk, float* __restrict__ loss_rows,
                  float* __restrict__ partial, float4* __restrict__ rows4, int d, int dpp,
-                 int64_t n, int ntiles) {
+                 int64_t n, int ntiles, int H, int G) {
   extern __shared__ float sm[];
   float* qs = sm;                                  // [64][d]
   float* pq = qs + kLossRows * d;                  // [64][dpp]
@@ -280,7 +283,7 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     __syncthreads();
     for (int e = tid; e < kLossKeys * d; e += kThreads) {
       const int64_t j = k0 + e / d;
-      ks[e] = j < n ? to_f(k[((size_t)bh * n + j) * d + e % d]) : 0.f;
+      ks[e] = j < n ? to_f(k[((size_t)kv_unit(bh, H, G) * n + j) * d + e % d]) : 0.f;
     }
     for (int e = tid; e < kLossKeys * dpp; e += kThreads) {
       const int64_t j = k0 + e / dpp;
@@ -374,7 +377,8 @@ static cudaError_t fmap_simt_t(const Problem& p, const void* x, int is_key, void
   const size_t smem = sizeof(float) * warps * (128 + 320);
   fmap_simt_kernel<T><<<blocks, kThreads, smem, s>>>((const T*)x, W, b, (T*)phi,
                                                      p.softmax ? off : nullptr, p.kind,
-                                                     p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.n, rows);
+                                                     p.softmax ? 1 : 0, p.d, p.dpp, p.H,
+                                                     is_key ? p.G : 1, p.n, rows);
   return cudaGetLastError();
 }
 
@@ -402,7 +406,7 @@ static cudaError_t prefill_simt_t(const Problem& p, const void* q, const void* k
   prefill_simt_kernel<T><<<(unsigned)units, kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)v, (T*)y, S_out, z_out, p.S0, p.z0, (const T*)p.Wq,
       p.bq, Wk, bk,
-      p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.n, C);
+      p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.G, p.n, C);
   return cudaGetLastError();
 }
 
@@ -430,7 +434,7 @@ static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, c
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     loss_simt_kernel<T><<<(unsigned)blocks, kThreads, smem, s>>>((const T*)q, (const T*)k, (const T*)phq,
                                                      (const T*)phk, loss_rows, partial, rows4,
-                                                     p.d, p.dpp, p.n, ntiles);
+                                                     p.d, p.dpp, p.n, ntiles, p.H, p.G);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

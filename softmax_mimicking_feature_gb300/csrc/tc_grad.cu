@@ -81,6 +81,7 @@ struct GradArgs {
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n, U;
+  int H, G;              // heads; query heads per key/value head
   int NT;                // 128-row tiles per sequence
   int npad;              // NT * 128
   float s_scale;         // log2(e) / sqrt(d)
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
   const int side = blockIdx.x & 1;
   const int rank = (int)((blockIdx.x >> 1) / A.U);
   const int64_t unit = (blockIdx.x >> 1) % A.U;
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
   const int rt = side ? rank : A.NT - 1 - rank;   // resident tile
   const int64_t r0 = (int64_t)rt * kRT;
   // streamed rows: keys 0 .. min(r0 + 128, n) (query side) or queries r0 .. n (key side)
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       bool ok = true;
       mbar_expect_tx(bar_x, C::X_BYTES + C::PX_BYTES);
       for (int i = 0; i < D / 64; ++i)
-        tma_load_3d(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0, (int)unit);
+        tma_load_3d(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0,
+                    (int)(side ? kvu : unit));
       for (int i = 0; i < DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PX + i * 16384, &A.tpx[side], bar_x, 64 * i, (int)r0, (int)unit);
       // Y(t) after S/A(t-2) read its stage; phi(Y)(t) after G phi(Y)(t-3)
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
         for (int i = 0; i < D / 64; ++i)
           tma_load_3d(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
-                      64 * i, (int)y0, (int)unit);
+                      64 * i, (int)y0, (int)(side ? unit : kvu));
         if (t >= 3) ok = mbar_wait_poll(bar_pyfree + 8 * p, (t / 3 - 1) & 1, wp);
         if (!ok) break;
         mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (side ? C::ST_BYTES : 0));
@@ -515,9 +518,10 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   const void* px[2] = {phq, phk};
   bool ok = true;
   for (int side = 0; side < 2; ++side) {
-    ok = ok && make_map(&a.tx[side], x[side], D, p.n, U, kRT) &&
+    // raw k (x[1]) has U / G planes under grouped key/value heads
+    ok = ok && make_map(&a.tx[side], x[side], D, p.n, side ? U / p.G : U, kRT) &&
          make_map(&a.tpx[side], px[side], 2 * D, p.n, U, kRT) &&
-         make_map(&a.ty[side], x[1 - side], D, p.n, U, kST) &&
+         make_map(&a.ty[side], x[1 - side], D, p.n, side ? U : U / p.G, kST) &&
          make_map(&a.tpy[side], px[1 - side], 2 * D, p.n, U, kST);
   }
   if (!ok) return cudaErrorInvalidValue;
@@ -528,6 +532,8 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
   a.n = p.n;
   a.U = (int64_t)U;
+  a.H = p.H;
+  a.G = p.G;
   a.NT = ceil_div(p.n, kRT);
   a.npad = a.NT * kRT;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);

@@ -92,6 +92,8 @@ struct FmapArgs {
   __nv_bfloat16* phi[2];   // [U][n][2D] or null
   float2* off[2];          // [U][NT*128] softmax-map offsets (log2 units) or null
   const float* bias[2];    // [H][D] or null
+  int kv[2];               // input indexed by key/value head (keys under grouping)
+  int G;                   // query heads per key/value head
   int sides;
   int softmax;
   int* dev_status;
@@ -138,7 +140,8 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
     mbar_expect_tx(bar_load, W_BYTES + X_BYTES);
     for (int i = 0; i < D / 64; ++i) {
       tma_load_3d(sb + OFF_W + i * (D * 128), &A.tw[side], bar_load, 64 * i, 0, h);
-      tma_load_3d(sb + OFF_X + i * 16384, &A.tx[side], bar_load, 64 * i, (int)r0, (int)unit);
+      tma_load_3d(sb + OFF_X + i * 16384, &A.tx[side], bar_load, 64 * i, (int)r0,
+                  (int)(A.kv[side] ? kv_unit(unit, A.H, A.G) : unit));
     }
   }
   if (warp == 0) {
@@ -259,6 +262,7 @@ struct LossArgs {
   int64_t n;
   int64_t U;
   int NT;
+  int H, G;            // heads; query heads per key/value head
   float s_scale;       // log2(e) / sqrt(d)
 };
 
@@ -305,6 +309,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   // heavy query tiles first: block b -> query tile NT-1 - b / U
   const int qt = A.NT - 1 - (int)(blockIdx.x / A.U);
   const int64_t unit = blockIdx.x % A.U;
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
   const int64_t q0 = (int64_t)qt * kTile;
   const int nkt = qt + 1;
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       auto load_k = [&](int j) {
         mbar_expect_tx(bar_k, C::Q_BYTES);
         for (int i = 0; i < D / 64; ++i)
-          tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, (int)unit);
+          tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, (int)kvu);
       };
       auto load_pk = [&](int j) {
         mbar_expect_tx(bar_pk, C::PQ_BYTES);
@@ -564,13 +569,16 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
   const uint64_t U = (uint64_t)p.B * p.H;
   for (int i = 0; i < sides; ++i) {
     const void* W = is_key[i] && p.Wk ? p.Wk : p.Wq;
-    if (!make_map(&a.tx[i], x[i], D, p.n, U, kTile) || !make_map(&a.tw[i], W, D, D, p.H, D))
+    a.kv[i] = is_key[i] && p.G > 1;
+    if (!make_map(&a.tx[i], x[i], D, p.n, a.kv[i] ? U / p.G : U, kTile) ||
+        !make_map(&a.tw[i], W, D, D, p.H, D))
       return cudaErrorInvalidValue;
     a.phi[i] = reinterpret_cast<__nv_bfloat16*>(phi[i]);
     a.off[i] = p.softmax ? off[i] : nullptr;
     a.bias[i] = is_key[i] && p.Wk ? p.bk : p.bq;
   }
   a.sides = sides;
+  a.G = p.G;
   a.softmax = p.softmax ? 1 : 0;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
@@ -612,7 +620,7 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   LossArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
-  bool ok = make_map(&a.tq, q, D, p.n, U, kTile) && make_map(&a.tk, k, D, p.n, U, kTile) &&
+  bool ok = make_map(&a.tq, q, D, p.n, U, kTile) && make_map(&a.tk, k, D, p.n, U / p.G, kTile) &&
             make_map(&a.tpq, phq, 2 * D, p.n, U, kTile) && make_map(&a.tpk, phk, 2 * D, p.n, U, kTile);
   if (!ok) return cudaErrorInvalidValue;
   a.loss_rows = loss_rows;
@@ -625,6 +633,8 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.n = p.n;
   a.U = (int64_t)U;
   a.NT = ceil_div(p.n, kTile);
+  a.H = p.H;
+  a.G = p.G;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   const size_t smem = LossCfg<D>::ALLOC;
   auto kern = rows4 ? loss_tc_kernel<D, true> : loss_tc_kernel<D, false>;

@@ -135,6 +135,7 @@ struct PrefillArgs {
   int L;            // tiles per segment
   int NT;           // tiles per unit
   int sep_wk;       // distinct key map loaded in the second W buffer
+  int G;            // query heads per key/value head
 };
 
 // ---------------------------------------------------------------------------
@@ -248,6 +249,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   const int row = 32 * g + lane;  // TMEM lane / tile row owned by this thread
 
   const int64_t unit = blockIdx.x / A.P;
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   const int seg = blockIdx.x % A.P;
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -275,13 +277,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     if (KIND == HH_FMAP_HEDGEHOG) {
       for (int i = 0; i < D / 64; ++i) {
         tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, (int)unit);
-        tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, (int)unit);
-        tma_load_3d(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, (int)unit);
+        tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, (int)kvu);
+        tma_load_3d(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, (int)kvu);
       }
     } else {
       tma_load_3d(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, (int)unit);
-      tma_load_3d(sb + C::OFF_K, &A.tk, bar_load, 0, r0, (int)unit);
-      tma_load_3d(sb + C::OFF_V, &A.tv, bar_load, 0, r0, (int)unit);
+      tma_load_3d(sb + C::OFF_K, &A.tk, bar_load, 0, r0, (int)kvu);
+      tma_load_3d(sb + C::OFF_V, &A.tv, bar_load, 0, r0, (int)kvu);
     }
   };
   __syncthreads();  // barriers initialised before the first copy is issued
@@ -896,14 +898,14 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   bool ok = true;
   if (KIND == HH_FMAP_HEDGEHOG) {
     ok &= make_map(&a.tq, q, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= make_map(&a.tk, k, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= make_map(&a.tv, v, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&a.tk, k, D, p.n, U / p.G, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&a.tv, v, D, p.n, U / p.G, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
     ok &= make_map(&a.twq, p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
     ok &= make_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     ok &= make_map(&a.tq, q, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok &= make_map(&a.tk, k, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok &= make_map(&a.tv, v, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_32B);
+    ok &= make_map(&a.tk, k, 16, p.n, U / p.G, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&a.tv, v, 16, p.n, U / p.G, 16, kTile, CU_TENSOR_MAP_SWIZZLE_32B);
   }
   if (!ok) return cudaErrorInvalidValue;
   a.y = y;
@@ -924,6 +926,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   a.L = pl.L;
   a.NT = pl.NT;
   a.sep_wk = p.Wk ? 1 : 0;
+  a.G = p.G;
   const size_t smem = smem_bytes<KIND, D>();
   float* init = nullptr;
   if (p.S0) {

@@ -82,6 +82,7 @@ struct Args2 {
   uint64_t soft_ns, hard_ns;
   int64_t n;
   int H, P, L, NT;
+  int G;               // query heads per key/value head
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / A.P;
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   const int seg = blockIdx.x % A.P;
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -138,12 +140,12 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     const uint32_t base = sb + slot_off(s);
     mbar_expect_tx(bar(B_LDQK + s), 2 * 16384);
     tma_load_3d(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, (int)unit);
-    tma_load_3d(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, (int)unit);
+    tma_load_3d(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, (int)kvu);
   };
   auto load_v = [&](int i) {
     const int s = i & 1;
     mbar_expect_tx(bar(B_LDV + s), 16384);
-    tma_load_3d(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, (int)unit);
+    tma_load_3d(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, (int)kvu);
   };
   if (warp == 8 && lane == 0) {
     mbar_expect_tx(bar(B_W), 8192u);
@@ -589,8 +591,9 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
   if (p.Wk) return cudaErrorInvalidValue;  // one map shared by queries and keys
-  bool ok = make_map(&a.tq, q, D, p.n, U, TILE) && make_map(&a.tk, k, D, p.n, U, TILE) &&
-            make_map(&a.tv, v, D, p.n, U, TILE) && make_map(&a.tw, p.Wq, D, D, p.H, D);
+  const uint64_t Ukv = U / p.G;
+  bool ok = make_map(&a.tq, q, D, p.n, U, TILE) && make_map(&a.tk, k, D, p.n, Ukv, TILE) &&
+            make_map(&a.tv, v, D, p.n, Ukv, TILE) && make_map(&a.tw, p.Wq, D, D, p.H, D);
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
@@ -609,6 +612,7 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
+  a.G = p.G;
   auto kern = p.softmax ? prefill_tc2_kernel<true> : prefill_tc2_kernel<false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);

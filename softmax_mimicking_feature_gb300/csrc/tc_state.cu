@@ -103,6 +103,7 @@ struct StateArgs {
   uint64_t soft_ns, hard_ns;
   int64_t n;
   int H, P, L, NT;
+  int G;              // query heads per key/value head
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   const int seg = blockIdx.x % (A.P - 1);
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -163,14 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     const uint32_t b = bar(SB_LDK + (i & 1));
     mbar_expect_tx(b, C::XT);
     for (int x = 0; x < (D + 63) / 64; ++x)
-      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
   };
   auto load_v = [&](int i) {
     const uint32_t dst = sb + C::OFF_V + (i % NV) * C::XT;
     const uint32_t b = bar(SB_LDV + (i % NV));
     mbar_expect_tx(b, C::XT);
     for (int x = 0; x < (D + 63) / 64; ++x)
-      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
   };
   if (warp == 8 && lane == 0 && nt > 0) {
     if (HH) {
@@ -440,6 +442,7 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   const int seg = blockIdx.x % (A.P - 1);
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const uint32_t dst = sb + OFF_K + (i & 1) * XT, b = bar(B_LDK + (i & 1));
     mbar_expect_tx(b, XT);
     for (int x = 0; x < 2; ++x)
-      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
   };
   // V(i) (and, for the softmax map, the tile's per-token offsets, whose smem
   // buffer is free for the same reason as V's: E1(i-2) and G2(i-2) are done)
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const uint32_t dst = sb + OFF_V + (i & 1) * XT, b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT + (A.off ? TILE * 8 : 0));
     for (int x = 0; x < 2; ++x)
-      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)unit);
+      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
     if (A.off)
       bulk_load(sb + OFF_OX + (i & 1) * TILE * 8,
                 A.off + (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE, TILE * 8, b);
@@ -694,6 +697,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   const int seg = blockIdx.x % (A.P - 1);
   const int t_begin = seg * A.L;
   const int nt = min(A.NT, t_begin + A.L) - t_begin;
@@ -708,12 +712,12 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   auto load_k = [&](int i) {
     const uint32_t b = bar(B_LDK + (i & 1));
     mbar_expect_tx(b, XT);
-    tma_load_3d(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, (int)unit);
+    tma_load_3d(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, (int)kvu);
   };
   auto load_v = [&](int i) {
     const uint32_t b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT);
-    tma_load_3d(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, (int)unit);
+    tma_load_3d(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, (int)kvu);
   };
   if (warp == 8 && lane == 0)
     for (int i = 0; i < 2 && i < nt; ++i) {
@@ -910,12 +914,12 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   const uint64_t U = (uint64_t)p.B * p.H;
   bool ok;
   if (KIND == HH_FMAP_HEDGEHOG) {
-    ok = make_map(&a.tk, k, D, p.n, U, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(&a.tv, v, D, p.n, U, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
+    ok = make_map(&a.tk, k, D, p.n, U / p.G, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&a.tv, v, D, p.n, U / p.G, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_map(&a.tw, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    ok = make_map(&a.tk, k, 16, p.n, U, 16, TILE, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_map(&a.tv, v, 16, p.n, U, 16, TILE, CU_TENSOR_MAP_SWIZZLE_32B);
+    ok = make_map(&a.tk, k, 16, p.n, U / p.G, 16, TILE, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_map(&a.tv, v, 16, p.n, U / p.G, 16, TILE, CU_TENSOR_MAP_SWIZZLE_32B);
   }
   if (!ok) return cudaErrorInvalidValue;
   a.ws = reinterpret_cast<float*>(ws);
@@ -930,6 +934,7 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
+  a.G = p.G;
   if (KIND == HH_FMAP_TAYLOR2) {
     cudaError_t e = cudaFuncSetAttribute(state_taylor_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -66,6 +66,7 @@ struct ArgsT {
   uint64_t soft_ns, hard_ns;
   int64_t n;
   int P, L, NT;
+  int H, G;          // heads; query heads per key/value head
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / A.P;
+  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   const int seg = blockIdx.x % A.P;
   const int t_begin = seg * A.L;
   const int nt = min(A.NT, t_begin + A.L) - t_begin;
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     const int r0 = (t_begin + i) * TILE;
     mbar_expect_tx(bar(B_LD + s), 3 * XT);
     tma_load_3d(sb + OFF_Q + s * XT, &A.tq, bar(B_LD + s), 0, r0, (int)unit);
-    tma_load_3d(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, (int)unit);
-    tma_load_3d(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, (int)unit);
+    tma_load_3d(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, (int)kvu);
+    tma_load_3d(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, (int)kvu);
   };
   if (warp == 8 && lane == 0)
     for (int i = 0; i < 2 && i < nt; ++i) load(i);
@@ -540,8 +542,8 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
   if (p.kind != HH_FMAP_TAYLOR2 || p.d != 16) return cudaErrorInvalidValue;
-  bool ok = make_map16(&a.tq, q, p.n, U) && make_map16(&a.tk, k, p.n, U) &&
-            make_map16(&a.tv, v, p.n, U);
+  bool ok = make_map16(&a.tq, q, p.n, U) && make_map16(&a.tk, k, p.n, U / p.G) &&
+            make_map16(&a.tv, v, p.n, U / p.G);
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
@@ -555,6 +557,8 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
+  a.H = p.H;
+  a.G = p.G;
   cudaError_t e = cudaFuncSetAttribute(taylor_out_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);

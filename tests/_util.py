@@ -6,6 +6,14 @@ import torch
 
 BF16_TOL = 5e-3   # max per-head relative L2 error, bf16 inputs / fp32 accumulate
 F32_TOL = 1e-5    # max per-head relative L2 error, float32 workloads
+# Bias gradient of the mimicry loss with bf16 inputs.  db = sum_t dL/dh_t over
+# every token cancels heavily (|sum| is a small fraction of sum |dL/dh_t|), so
+# the bf16 rounding of the features (2^-9 relative, entering a_ij, the
+# dPhi = G phi contraction and dL/dh = dPhi_+ e^h - dPhi_- e^-h) is amplified
+# in db more than in dW or the forward outputs; an fp64 emulation that rounds
+# only the features to bf16 reproduces the GPU's db error (3.9e-3 vs 3.9e-3
+# on 2 x 3 x 300, d = 64), up to 5.7e-3 over 14 heads.  Bound: twice BF16_TOL.
+DB_TOL_BF16 = 1e-2
 
 
 def f64(t):

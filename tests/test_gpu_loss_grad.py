@@ -4,7 +4,8 @@ hh_mimicry_loss_grad is compared with the oracle's fp64 chain rule
 (loss_grad_causal), itself pinned to finite differences of the loss.  The
 sizes span several 32-token tiles and a ragged tail.  Tolerances are the
 per-head relative L2 bounds of the forward path: 1e-5 for float32 and 5e-3
-for bf16 inputs, whose features are rounded to bf16 before the fp32 sums."""
+for bf16 inputs, whose features are rounded to bf16 before the fp32 sums;
+the bias gradient of bf16 inputs has the bound DB_TOL_BF16 (tests/_util.py)."""
 
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import torch
 import oracle as O
 import softmax_mimicking_feature_gb300 as hh
 from softmax_mimicking_feature_gb300 import workloads as wl
-from tests._util import BF16_TOL, F32_TOL, f64, need_gpu, rel_l2_per_head
+from tests._util import BF16_TOL, DB_TOL_BF16, F32_TOL, f64, need_gpu, rel_l2_per_head
 
 pytestmark = pytest.mark.gpu
 
@@ -39,12 +40,13 @@ def _tol(w):
 
 
 def _check(got, ref, tol):
-    for g, r in zip(got, ref):
+    for i, (g, r) in enumerate(zip(got, ref)):
         if r is None:
             assert g is None
             continue
         err = rel_l2_per_head(f64(g), r, lead=1)
-        assert err <= tol, err
+        # dW at tol; db (odd positions) of bf16 inputs at its own bound
+        assert err <= (tol if (i % 2 == 0 or tol == F32_TOL) else DB_TOL_BF16), err
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
