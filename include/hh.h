@@ -85,6 +85,16 @@ typedef enum {
 
 typedef enum { HH_F32 = 0, HH_BF16 = 1 } hh_dtype;
 
+/* Layout of the [B] x [H] x [n] x [d] tensors q, k, v, y of the prefill, loss,
+ * statistics and gradient calls and x of hh_feature_map (d contiguous in both):
+ *   HH_LAYOUT_BHND  [B][H][n][d]
+ *   HH_LAYOUT_BNHD  [B][n][H][d]  (the head-interleaved output of a fused
+ *                                  projection, used without a transpose)
+ * Under grouped key/value heads k, v are [B][Hkv][n][d] / [B][n][Hkv][d].
+ * States, per-row outputs (loss rows, statistics) and phi from
+ * hh_feature_map stay [B][H][...]. */
+typedef enum { HH_LAYOUT_BHND = 0, HH_LAYOUT_BNHD = 1 } hh_layout;
+
 /* HH_FMAP_HEDGEHOG: [exp(xW + b); exp(-(xW + b))] ("The Hedgehog MLP
  *   Feature Map", Choices 1 and 3).
  * HH_FMAP_TAYLOR2: [1, x, vec(x x^T) / sqrt 2] ("The Taylor Exponential as a
@@ -116,6 +126,7 @@ typedef struct {
                         * attention): k, v are [B][Hkv][n][d] ([B][Hkv][d] for
                         * decode).  Maps, states and outputs stay per query
                         * head.                                              */
+  int32_t layout;      /* hh_layout of q, k, v, y (0: [B][H][n][d])           */
 } hh_fmap;
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -16,6 +16,7 @@ HH_OK, HH_ERR_INVALID_ARG, HH_ERR_UNSUPPORTED, HH_ERR_ALIGNMENT = 0, 1, 2, 3
 HH_ERR_WORKSPACE, HH_ERR_CUDA, HH_ERR_TIMEOUT = 4, 5, 6
 HH_F32, HH_BF16 = 0, 1
 HH_FMAP_HEDGEHOG, HH_FMAP_TAYLOR2, HH_FMAP_HEDGEHOG_SOFTMAX = 0, 1, 2
+HH_LAYOUT_BHND, HH_LAYOUT_BNHD = 0, 1
 
 EXPORTED = ("hh_version", "hh_status_str", "hh_fmap_dim", "hh_feature_map",
             "hh_fwd_workspace_bytes", "hh_fwd_plan", "hh_linattn_fwd_causal", "hh_linattn_decode_step",
@@ -28,7 +29,7 @@ class HHFmap(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("Wq", ctypes.c_void_p), ("bq", ctypes.c_void_p),
                 ("Wk", ctypes.c_void_p), ("bk", ctypes.c_void_p),
-                ("kv_heads", ctypes.c_int32)]
+                ("kv_heads", ctypes.c_int32), ("layout", ctypes.c_int32)]
 
 
 class HHError(RuntimeError):

@@ -45,6 +45,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _dims(fm, t: torch.Tensor):
+    """(B, H, n, d) of a q / k / v / y tensor in the map's layout."""
+    if fm.layout == "bnhd":
+        B, n, H, d = t.shape
+    else:
+        B, H, n, d = t.shape
+    return B, H, n, d
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -63,6 +72,7 @@ class FeatureMap:
     Wk: Optional[torch.Tensor] = None
     bk: Optional[torch.Tensor] = None
     kv_heads: int = 0    # grouped-query attention: k, v have this many heads (0: one per head)
+    layout: str = "bhnd"  # q, k, v, y as [B, H, n, d] ("bhnd") or [B, n, H, d] ("bnhd")
 
     @property
     def kind_id(self) -> int:
@@ -77,6 +87,7 @@ class FeatureMap:
         s.Wk = _ptr(self.Wk)
         s.bk = _ptr(self.bk)
         s.kv_heads = int(self.kv_heads)
+        s.layout = {"bhnd": _abi.HH_LAYOUT_BHND, "bnhd": _abi.HH_LAYOUT_BNHD}[self.layout]
         return s
 
     def dim(self, padded: bool = True) -> int:
@@ -91,7 +102,7 @@ def fmap_dim(kind: str, d: int, padded: bool = True) -> int:
 def feature_map(fm: FeatureMap, x: torch.Tensor, is_key: bool = False,
                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """phi(x) for x [B, H, n, d] -> [B, H, n, d'p] (hh_feature_map)."""
-    B, H, n, d = x.shape
+    B, H, n, d = _dims(fm, x)
     if out is None:
         out = torch.empty(B, H, n, fm.dim(), dtype=x.dtype, device=x.device)
     s = fm.struct()
@@ -124,7 +135,7 @@ def linattn_fwd_causal(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, v: torc
     Returns y, or (y, S, z) with ``return_state``: S [B,H,d'p,d] and
     z [B,H,d'p] float32 hold the state after the last token.
     """
-    B, H, n, d = q.shape
+    B, H, n, d = _dims(fm, q)
     if y is None:
         y = torch.empty_like(q)
     S = z = None
@@ -162,7 +173,7 @@ def linattn_fwd_causal_from_state(fm: FeatureMap, q: torch.Tensor, k: torch.Tens
     Returns y, or (y, S, z) with ``return_state``; ``in_place`` writes the
     final state over S0, z0 (and returns them as S, z).
     """
-    B, H, n, d = q.shape
+    B, H, n, d = _dims(fm, q)
     if y is None:
         y = torch.empty_like(q)
     S = z = None
@@ -206,7 +217,7 @@ def mimicry_loss(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor, return_rows: 
                  workspace: Optional[torch.Tensor] = None,
                  dev_status: Optional[torch.Tensor] = None, stream=None):
     """Distillation cross-entropy (hh_mimicry_loss): returns (rows [B,H,n] or None, head_sum [B,H])."""
-    B, H, n, d = q.shape
+    B, H, n, d = _dims(fm, q)
     rows = torch.empty(B, H, n, dtype=torch.float32, device=q.device) if return_rows else None
     head = torch.empty(B, H, dtype=torch.float32, device=q.device)
     need = loss_workspace_bytes(fm, q.dtype, B, H, n)
@@ -224,7 +235,7 @@ def mimicry_stats(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
                   workspace: Optional[torch.Tensor] = None,
                   dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Per-query (CE, KL, H(p), H(w)) as float32 [B, H, n, 4] (hh_mimicry_stats)."""
-    B, H, n, d = q.shape
+    B, H, n, d = _dims(fm, q)
     out = torch.empty(B, H, n, 4, dtype=torch.float32, device=q.device)
     need = loss_workspace_bytes(fm, q.dtype, B, H, n)
     if workspace is None and need > 0:
@@ -250,7 +261,7 @@ def mimicry_loss_grad(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
     Returns (dWq, dbq, dWk, dbk), float32, summed over the batch; dWk, dbk are
     None when the keys share the query map (both sides are then in dWq, dbq).
     """
-    B, H, n, d = q.shape
+    B, H, n, d = _dims(fm, q)
     dev = q.device
     separate = fm.Wk is not None and fm.Wk.data_ptr() != fm.Wq.data_ptr()
     dWq = torch.empty(H, d, d, dtype=torch.float32, device=dev)

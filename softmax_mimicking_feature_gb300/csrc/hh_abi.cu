@@ -102,6 +102,8 @@ hh_status make_problem(const hh_fmap* fm, int dtype, int64_t B, int H, int64_t n
   const int hkv = fm->kv_heads;
   if (hkv < 0 || (hkv > 0 && (hkv > H || H % hkv != 0))) return HH_ERR_INVALID_ARG;
   p->G = hkv > 0 ? H / hkv : 1;
+  if (fm->layout != HH_LAYOUT_BHND && fm->layout != HH_LAYOUT_BNHD) return HH_ERR_INVALID_ARG;
+  p->seq_major = fm->layout == HH_LAYOUT_BNHD ? 1 : 0;
   if (p->kind == HH_FMAP_HEDGEHOG) {
     p->Wq = fm->Wq;
     p->bq = fm->bq;

@@ -19,6 +19,7 @@ struct Problem {
   int64_t B;
   int H;
   int G = 1;       // query heads per key/value head (grouped-query attention)
+  int seq_major = 0;  // q, k, v, y are [B][n][H][d] (else [B][H][n][d])
   int64_t n;
   const void* Wq;
   const float* bq;
@@ -57,6 +58,13 @@ inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 // when G query heads share one key/value head.
 __host__ __device__ __forceinline__ int64_t kv_unit(int64_t u, int H, int G) {
   return G == 1 ? u : (u / H) * (H / G) + (u % H) / G;
+}
+
+// Row of token t of head unit u (= b * H + h) in a [B][H][n][.] tensor, or in
+// a [B][n][H][.] one (seq_major); multiply by the row length for the offset.
+__host__ __device__ __forceinline__ int64_t row_index(int64_t u, int64_t t, int H, int64_t n,
+                                                      int seq_major) {
+  return seq_major ? ((u / H) * n + t) * H + u % H : u * n + t;
 }
 
 // Row stride of the softmax-map offset arrays.

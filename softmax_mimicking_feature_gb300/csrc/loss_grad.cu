@@ -54,11 +54,15 @@ __device__ inline GradSmem carve(float* sm, int d, int dpp) {
   return g;
 }
 
+// Rows [row0, row0 + kT) of head unit `unit` of a tensor with Hx heads in the
+// [B][Hx][n][width] layout, or [B][n][Hx][width] (seq); zero past n.
 template <typename T>
-__device__ inline void load_tile(float* dst, const T* src, int64_t row0, int64_t n, int width) {
+__device__ inline void load_tile(float* dst, const T* src, int64_t unit, int Hx, int seq,
+                                 int64_t row0, int64_t n, int width) {
   for (int i = threadIdx.x; i < kT * width; i += kThreads) {
     const int r = i / width;
-    dst[i] = row0 + r < n ? to_f(src[(row0 + r) * width + i % width]) : 0.f;
+    dst[i] = row0 + r < n ? to_f(src[row_index(unit, row0 + r, Hx, n, seq) * width + i % width])
+                          : 0.f;
   }
 }
 
@@ -106,7 +110,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_query_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
     const T* __restrict__ phk, float* __restrict__ stats, float* __restrict__ dhq, int d, int dpp,
-    int64_t n, int ntiles, int H, int G) {
+    int64_t n, int ntiles, int H, int G, int seq) {
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
@@ -115,15 +119,15 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
   const int t = threadIdx.x, r = t / 8, slot = t % 8;
   const int64_t qi = q0 + r;
   const float scale = rsqrtf((float)d);
-  load_tile(S.xs, q + u * n * d, q0, n, d);
-  load_tile(S.pxs, phq + u * n * dpp, q0, n, dpp);
+  load_tile(S.xs, q, u, H, seq, q0, n, d);
+  load_tile(S.pxs, phq, u, 1, 0, q0, n, dpp);
 
   // sweep 1: M_i = max s, Z_i = sum e^{s - M}, A_i = sum a over j <= i
   float m = -INFINITY, z = 0.f, asum = 0.f;
   for (int kt = 0; kt <= qt; ++kt) {
     __syncthreads();
-    load_tile(S.ys, k + kv_unit(u, H, G) * n * d, (int64_t)kt * kT, n, d);
-    load_tile(S.pys, phk + u * n * dpp, (int64_t)kt * kT, n, dpp);
+    load_tile(S.ys, k, kv_unit(u, H, G), H / G, seq, (int64_t)kt * kT, n, d);
+    load_tile(S.pys, phk, u, 1, 0, (int64_t)kt * kT, n, dpp);
     __syncthreads();
     for (int c = slot; c < kT; c += 8) {
       const int64_t kj = (int64_t)kt * kT + c;
@@ -164,8 +168,8 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
   const int nf = dpp / 8;
   for (int kt = 0; kt <= qt; ++kt) {
     __syncthreads();
-    load_tile(S.ys, k + kv_unit(u, H, G) * n * d, (int64_t)kt * kT, n, d);
-    load_tile(S.pys, phk + u * n * dpp, (int64_t)kt * kT, n, dpp);
+    load_tile(S.ys, k, kv_unit(u, H, G), H / G, seq, (int64_t)kt * kT, n, d);
+    load_tile(S.pys, phk, u, 1, 0, (int64_t)kt * kT, n, dpp);
     __syncthreads();
     for (int c = slot; c < kT; c += 8) {
       const int64_t kj = (int64_t)kt * kT + c;
@@ -194,7 +198,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_key_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
     const T* __restrict__ phk, const float* __restrict__ stats, float* __restrict__ dhk, int d,
-    int dpp, int64_t n, int ntiles, int H, int G) {
+    int dpp, int64_t n, int ntiles, int H, int G, int seq) {
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
@@ -202,16 +206,16 @@ __global__ void __launch_bounds__(kThreads) grad_key_kernel(
   const int64_t k0 = (int64_t)kt * kT;
   const int t = threadIdx.x, r = t / 8, slot = t % 8;   // r: key row of the tile
   const float scale = rsqrtf((float)d);
-  load_tile(S.xs, k + kv_unit(u, H, G) * n * d, k0, n, d);
-  load_tile(S.pxs, phk + u * n * dpp, k0, n, dpp);
+  load_tile(S.xs, k, kv_unit(u, H, G), H / G, seq, k0, n, d);
+  load_tile(S.pxs, phk, u, 1, 0, k0, n, dpp);
   float acc[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) acc[i] = 0.f;
   const int nf = dpp / 8;
   for (int qt = kt; qt < ntiles; ++qt) {
     __syncthreads();
-    load_tile(S.ys, q + u * n * d, (int64_t)qt * kT, n, d);
-    load_tile(S.pys, phq + u * n * dpp, (int64_t)qt * kT, n, dpp);
+    load_tile(S.ys, q, u, H, seq, (int64_t)qt * kT, n, d);
+    load_tile(S.pys, phq, u, 1, 0, (int64_t)qt * kT, n, dpp);
     for (int i = threadIdx.x; i < kT * 3; i += kThreads) {
       const int64_t row = (int64_t)qt * kT + i / 3;
       S.st[i] = row < n ? stats[(u * n + row) * 3 + i % 3] : 1.f;
@@ -249,7 +253,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
     const T* __restrict__ x1, const float* __restrict__ dh1, const T* __restrict__ x2,
     const float* __restrict__ dh2, float* __restrict__ dW, float* __restrict__ db, int64_t B,
-    int H, int64_t n, int d, int G1, int G2) {
+    int H, int64_t n, int d, int G1, int G2, int seq) {
   __shared__ float xs[32][33];
   __shared__ float hs[32][33];
   const int nb = (d + 31) / 32;
@@ -262,13 +266,16 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
     const float* dh = side ? dh2 : dh1;
     for (int64_t b = 0; b < B; ++b) {
       const size_t base = ((size_t)b * H + h) * n;
-      const size_t xbase = (size_t)kv_unit((int64_t)b * H + h, H, side ? G2 : G1) * n;
+      const int Gs = side ? G2 : G1;
+      const int64_t ux = kv_unit((int64_t)b * H + h, H, Gs);   // unit of x (k under grouping)
       for (int64_t t0 = 0; t0 < n; t0 += 32) {
         __syncthreads();
         for (int i = t; i < 32 * 32; i += kThreads) {
           const int rr = i / 32, cc = i % 32;
           const bool ok = t0 + rr < n;
-          xs[rr][cc] = ok && a0 + cc < d ? to_f(x[(xbase + t0 + rr) * d + a0 + cc]) : 0.f;
+          xs[rr][cc] = ok && a0 + cc < d
+                           ? to_f(x[row_index(ux, t0 + rr, H / Gs, n, seq) * d + a0 + cc])
+                           : 0.f;
           hs[rr][cc] = ok && l0 + cc < d ? dh[(base + t0 + rr) * d + l0 + cc] : 0.f;
         }
         __syncthreads();
@@ -307,11 +314,11 @@ cudaError_t grad_t(const Problem& p, const void* q, const void* k, const void* p
     return e;
   grad_query_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhq, p.d, p.dpp, p.n, ntiles,
-      p.H, p.G);
+      p.H, p.G, p.seq_major);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   grad_key_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhk, p.d, p.dpp, p.n, ntiles,
-      p.H, p.G);
+      p.H, p.G, p.seq_major);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_grad_reduce(p, q, k, dhq, dhk, dWq, dbq, dWk, dbk, s);
 }
@@ -324,14 +331,14 @@ cudaError_t reduce_t(const Problem& p, const void* q, const void* k, const float
   const unsigned grid = (unsigned)(p.H * nb * nb);
   if (dWk) {   // separate key map: each side to its own parameters
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)q, dhq, (const T*)nullptr, nullptr,
-                                                    dWq, dbq, p.B, p.H, p.n, p.d, 1, 1);
+                                                    dWq, dbq, p.B, p.H, p.n, p.d, 1, 1, p.seq_major);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)k, dhk, (const T*)nullptr, nullptr,
-                                                    dWk, dbk, p.B, p.H, p.n, p.d, p.G, 1);
+                                                    dWk, dbk, p.B, p.H, p.n, p.d, p.G, 1, p.seq_major);
   } else {
     grad_reduce_kernel<T><<<grid, kThreads, 0, s>>>((const T*)q, dhq, (const T*)k, dhk, dWq, dbq,
-                                                    p.B, p.H, p.n, p.d, 1, p.G);
+                                                    p.B, p.H, p.n, p.d, 1, p.G, p.seq_major);
   }
   return cudaGetLastError();
 }

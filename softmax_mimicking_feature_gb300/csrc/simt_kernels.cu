@@ -94,7 +94,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* __restrict__ bias,
                  T* __restrict__ phi, float2* __restrict__ off, int kind, int softmax, int d,
-                 int dpp, int H, int G, int64_t n, int64_t rows) {
+                 int dpp, int H, int G, int seq, int64_t n, int64_t rows) {
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = kThreads / 32;
@@ -103,7 +103,7 @@ fmap_simt_kernel(const T* __restrict__ x, const T* __restrict__ W, const float* 
   for (int64_t r = (int64_t)blockIdx.x * nwarps + warp; r < rows; r += (int64_t)gridDim.x * nwarps) {
     const int h = (int)((r / n) % H);
     // x row: of this query head, or of its key/value head (G > 1: keys)
-    const int64_t xr = kv_unit(r / n, H, G) * n + r % n;
+    const int64_t xr = row_index(kv_unit(r / n, H, G), r % n, H / G, n, seq);
     for (int k = lane; k < d; k += 32) xs[k] = to_f(x[xr * d + k]);
     __syncwarp();
     const T* Wh = W ? W + (size_t)h * d * d : nullptr;
@@ -129,7 +129,7 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
                     const float* __restrict__ S0, const float* __restrict__ z0,
                     const T* __restrict__ Wq, const float* __restrict__ bq,
                     const T* __restrict__ Wk, const float* __restrict__ bk, int kind,
-                    int softmax, int d, int dpp, int H, int G, int64_t n, int C) {
+                    int softmax, int d, int dpp, int H, int G, int seq, int64_t n, int C) {
   extern __shared__ float sm[];
   float* S = sm;                       // [dpp][d]
   float* z = S + (size_t)dpp * d;      // [dpp]
@@ -143,8 +143,10 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 
   const int64_t bh = blockIdx.x;
   const int h = (int)(bh % H);
-  const size_t base = (size_t)bh * n * d;
-  const size_t kvbase = (size_t)kv_unit(bh, H, G) * n * d;   // k, v of this query head
+  const int64_t kvu = kv_unit(bh, H, G);   // k, v of this query head
+  // element offset of token t of this head in q / y, and in k / v
+  auto qrow = [&](int64_t t) { return (size_t)row_index(bh, t, H, n, seq) * d; };
+  auto kvrow = [&](int64_t t) { return (size_t)row_index(kvu, t, H / G, n, seq) * d; };
   const T* Wqh = Wq ? Wq + (size_t)h * d * d : nullptr;
   const T* Wkh = Wk ? Wk + (size_t)h * d * d : nullptr;
   const float* bqh = bq ? bq + (size_t)h * d : nullptr;
@@ -162,9 +164,9 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     for (int i = tid; i < C * d; i += kThreads) {
       const int r = i / d;
       const bool ok = r < nc;
-      xs[i] = ok ? to_f(q[base + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
-      xk[i] = ok ? to_f(k[kvbase + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
-      vv[i] = ok ? to_f(v[kvbase + (size_t)(c0 + r) * d + (i % d)]) : 0.f;
+      xs[i] = ok ? to_f(q[qrow(c0 + r) + (i % d)]) : 0.f;
+      xk[i] = ok ? to_f(k[kvrow(c0 + r) + (i % d)]) : 0.f;
+      vv[i] = ok ? to_f(v[kvrow(c0 + r) + (i % d)]) : 0.f;
     }
     __syncthreads();
     for (int r = warp; r < C; r += kThreads / 32) {
@@ -198,7 +200,7 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       for (int j = 0; j <= r; ++j) num = fmaf(A[r * C + j], vv[j * d + c], num);
       float ni = 0.f;
       for (int f = 0; f < dpp; ++f) ni = fmaf(phq[(size_t)r * dpp + f], S[(size_t)f * d + c], ni);
-      y[base + (size_t)(c0 + r) * d + c] = from_f<T>((num + ni) / den[r]);
+      y[qrow(c0 + r) + c] = from_f<T>((num + ni) / den[r]);
     }
     __syncthreads();
     for (int i = tid; i < dpp * d; i += kThreads) {
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kThreads)
 loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
                  const T* __restrict__ phk, float* __restrict__ loss_rows,
                  float* __restrict__ partial, float4* __restrict__ rows4, int d, int dpp,
-                 int64_t n, int ntiles, int H, int G) {
+                 int64_t n, int ntiles, int H, int G, int seq) {
   extern __shared__ float sm[];
   float* qs = sm;                                  // [64][d]
   float* pq = qs + kLossRows * d;                  // [64][dpp]
@@ -271,7 +273,7 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 
   for (int e = tid; e < kLossRows * d; e += kThreads) {
     const int64_t rr = r0 + e / d;
-    qs[e] = rr < n ? to_f(q[((size_t)bh * n + rr) * d + e % d]) : 0.f;
+    qs[e] = rr < n ? to_f(q[(size_t)row_index(bh, rr, H, n, seq) * d + e % d]) : 0.f;
   }
   for (int e = tid; e < kLossRows * dpp; e += kThreads) {
     const int64_t rr = r0 + e / dpp;
@@ -283,7 +285,8 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     __syncthreads();
     for (int e = tid; e < kLossKeys * d; e += kThreads) {
       const int64_t j = k0 + e / d;
-      ks[e] = j < n ? to_f(k[((size_t)kv_unit(bh, H, G) * n + j) * d + e % d]) : 0.f;
+      ks[e] = j < n ? to_f(k[(size_t)row_index(kv_unit(bh, H, G), j, H / G, n, seq) * d + e % d])
+                    : 0.f;
     }
     for (int e = tid; e < kLossKeys * dpp; e += kThreads) {
       const int64_t j = k0 + e / dpp;
@@ -378,7 +381,7 @@ static cudaError_t fmap_simt_t(const Problem& p, const void* x, int is_key, void
   fmap_simt_kernel<T><<<blocks, kThreads, smem, s>>>((const T*)x, W, b, (T*)phi,
                                                      p.softmax ? off : nullptr, p.kind,
                                                      p.softmax ? 1 : 0, p.d, p.dpp, p.H,
-                                                     is_key ? p.G : 1, p.n, rows);
+                                                     is_key ? p.G : 1, p.seq_major, p.n, rows);
   return cudaGetLastError();
 }
 
@@ -406,7 +409,7 @@ static cudaError_t prefill_simt_t(const Problem& p, const void* q, const void* k
   prefill_simt_kernel<T><<<(unsigned)units, kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)v, (T*)y, S_out, z_out, p.S0, p.z0, (const T*)p.Wq,
       p.bq, Wk, bk,
-      p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.G, p.n, C);
+      p.kind, p.softmax ? 1 : 0, p.d, p.dpp, p.H, p.G, p.seq_major, p.n, C);
   return cudaGetLastError();
 }
 
@@ -434,7 +437,8 @@ static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, c
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     loss_simt_kernel<T><<<(unsigned)blocks, kThreads, smem, s>>>((const T*)q, (const T*)k, (const T*)phq,
                                                      (const T*)phk, loss_rows, partial, rows4,
-                                                     p.d, p.dpp, p.n, ntiles, p.H, p.G);
+                                                     p.d, p.dpp, p.n, ntiles, p.H, p.G,
+                                                     p.seq_major);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

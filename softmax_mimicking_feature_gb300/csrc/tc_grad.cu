@@ -33,6 +33,7 @@
 #include <algorithm>
 
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace hh {
 namespace {
@@ -82,6 +83,7 @@ struct GradArgs {
   uint64_t soft_ns, hard_ns;
   int64_t n, U;
   int H, G;              // heads; query heads per key/value head
+  int seq;               // q, k are [B][n][H][D]
   int NT;                // 128-row tiles per sequence
   int npad;              // NT * 128
   float s_scale;         // log2(e) / sqrt(d)
@@ -220,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       bool ok = true;
       mbar_expect_tx(bar_x, C::X_BYTES + C::PX_BYTES);
       for (int i = 0; i < D / 64; ++i)
-        tma_load_3d(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0,
-                    (int)(side ? kvu : unit));
+        tma_load_rows(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0,
+                      side ? kvu : unit, side ? A.H / A.G : A.H, A.seq);
       for (int i = 0; i < DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PX + i * 16384, &A.tpx[side], bar_x, 64 * i, (int)r0, (int)unit);
       // Y(t) after S/A(t-2) read its stage; phi(Y)(t) after G phi(Y)(t-3)
@@ -232,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         if (!ok) break;
         mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
         for (int i = 0; i < D / 64; ++i)
-          tma_load_3d(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
-                      64 * i, (int)y0, (int)(side ? unit : kvu));
+          tma_load_rows(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
+                        64 * i, (int)y0, side ? unit : kvu, side ? A.H : A.H / A.G, A.seq);
         if (t >= 3) ok = mbar_wait_poll(bar_pyfree + 8 * p, (t / 3 - 1) & 1, wp);
         if (!ok) break;
         mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (side ? C::ST_BYTES : 0));
@@ -519,9 +521,12 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   bool ok = true;
   for (int side = 0; side < 2; ++side) {
     // raw k (x[1]) has U / G planes under grouped key/value heads
-    ok = ok && make_map(&a.tx[side], x[side], D, p.n, side ? U / p.G : U, kRT) &&
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    ok = ok && make_rows_map(&a.tx[side], x[side], D, p.n, side ? p.H / p.G : p.H, p.B, 64, kRT, sw,
+                             p.seq_major) &&
          make_map(&a.tpx[side], px[side], 2 * D, p.n, U, kRT) &&
-         make_map(&a.ty[side], x[1 - side], D, p.n, side ? U : U / p.G, kST) &&
+         make_rows_map(&a.ty[side], x[1 - side], D, p.n, side ? p.H : p.H / p.G, p.B, 64, kST, sw,
+                       p.seq_major) &&
          make_map(&a.tpy[side], px[1 - side], 2 * D, p.n, U, kST);
   }
   if (!ok) return cudaErrorInvalidValue;
@@ -534,6 +539,7 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   a.U = (int64_t)U;
   a.H = p.H;
   a.G = p.G;
+  a.seq = p.seq_major;
   a.NT = ceil_div(p.n, kRT);
   a.npad = a.NT * kRT;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);

@@ -36,6 +36,7 @@
 #include <algorithm>
 
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace hh {
 namespace {
@@ -94,6 +95,7 @@ struct FmapArgs {
   const float* bias[2];    // [H][D] or null
   int kv[2];               // input indexed by key/value head (keys under grouping)
   int G;                   // query heads per key/value head
+  int seq;                 // inputs are [B][n][H][D]
   int sides;
   int softmax;
   int* dev_status;
@@ -140,8 +142,9 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
     mbar_expect_tx(bar_load, W_BYTES + X_BYTES);
     for (int i = 0; i < D / 64; ++i) {
       tma_load_3d(sb + OFF_W + i * (D * 128), &A.tw[side], bar_load, 64 * i, 0, h);
-      tma_load_3d(sb + OFF_X + i * 16384, &A.tx[side], bar_load, 64 * i, (int)r0,
-                  (int)(A.kv[side] ? kv_unit(unit, A.H, A.G) : unit));
+      tma_load_rows(sb + OFF_X + i * 16384, &A.tx[side], bar_load, 64 * i, (int)r0,
+                    A.kv[side] ? kv_unit(unit, A.H, A.G) : unit,
+                    A.kv[side] ? A.H / A.G : A.H, A.seq);
     }
   }
   if (warp == 0) {
@@ -263,6 +266,7 @@ struct LossArgs {
   int64_t U;
   int NT;
   int H, G;            // heads; query heads per key/value head
+  int seq;             // q, k are [B][n][H][D]
   float s_scale;       // log2(e) / sqrt(d)
 };
 
@@ -346,7 +350,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       auto load_k = [&](int j) {
         mbar_expect_tx(bar_k, C::Q_BYTES);
         for (int i = 0; i < D / 64; ++i)
-          tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, (int)kvu);
+          tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, kvu,
+                        A.H / A.G, A.seq);
       };
       auto load_pk = [&](int j) {
         mbar_expect_tx(bar_pk, C::PQ_BYTES);
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       };
       mbar_expect_tx(bar_q, C::Q_BYTES + C::PQ_BYTES);
       for (int i = 0; i < D / 64; ++i)
-        tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, (int)unit);
+        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, unit, A.H, A.seq);
       for (int i = 0; i < C::DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PQ + i * 16384, &A.tpq, bar_q, 64 * i, (int)q0, (int)unit);
       load_k(0);
@@ -570,7 +575,8 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
   for (int i = 0; i < sides; ++i) {
     const void* W = is_key[i] && p.Wk ? p.Wk : p.Wq;
     a.kv[i] = is_key[i] && p.G > 1;
-    if (!make_map(&a.tx[i], x[i], D, p.n, a.kv[i] ? U / p.G : U, kTile) ||
+    if (!make_rows_map(&a.tx[i], x[i], D, p.n, a.kv[i] ? p.H / p.G : p.H, p.B, 64, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_128B, p.seq_major) ||
         !make_map(&a.tw[i], W, D, D, p.H, D))
       return cudaErrorInvalidValue;
     a.phi[i] = reinterpret_cast<__nv_bfloat16*>(phi[i]);
@@ -579,6 +585,7 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
   }
   a.sides = sides;
   a.G = p.G;
+  a.seq = p.seq_major;
   a.softmax = p.softmax ? 1 : 0;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
@@ -620,7 +627,9 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   LossArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
-  bool ok = make_map(&a.tq, q, D, p.n, U, kTile) && make_map(&a.tk, k, D, p.n, U / p.G, kTile) &&
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major) &&
+            make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
             make_map(&a.tpq, phq, 2 * D, p.n, U, kTile) && make_map(&a.tpk, phk, 2 * D, p.n, U, kTile);
   if (!ok) return cudaErrorInvalidValue;
   a.loss_rows = loss_rows;
@@ -635,6 +644,7 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.NT = ceil_div(p.n, kTile);
   a.H = p.H;
   a.G = p.G;
+  a.seq = p.seq_major;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   const size_t smem = LossCfg<D>::ALLOC;
   auto kern = rows4 ? loss_tc_kernel<D, true> : loss_tc_kernel<D, false>;

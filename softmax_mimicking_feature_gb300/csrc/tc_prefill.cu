@@ -35,6 +35,7 @@
 
 #include "taylor_pack.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace hh {
 namespace {
@@ -136,6 +137,7 @@ struct PrefillArgs {
   int NT;           // tiles per unit
   int sep_wk;       // distinct key map loaded in the second W buffer
   int G;            // query heads per key/value head
+  int seq;          // q, k, v, y are [B][n][H][D]
 };
 
 // ---------------------------------------------------------------------------
@@ -276,14 +278,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     mbar_expect_tx(bar_load, bytes);
     if (KIND == HH_FMAP_HEDGEHOG) {
       for (int i = 0; i < D / 64; ++i) {
-        tma_load_3d(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, (int)unit);
-        tma_load_3d(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, (int)kvu);
-        tma_load_3d(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, (int)kvu);
+        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, unit, A.H, A.seq);
+        tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, kvu, A.H / A.G,
+                      A.seq);
+        tma_load_rows(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, kvu, A.H / A.G,
+                      A.seq);
       }
     } else {
-      tma_load_3d(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, (int)unit);
-      tma_load_3d(sb + C::OFF_K, &A.tk, bar_load, 0, r0, (int)kvu);
-      tma_load_3d(sb + C::OFF_V, &A.tv, bar_load, 0, r0, (int)kvu);
+      tma_load_rows(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, unit, A.H, A.seq);
+      tma_load_rows(sb + C::OFF_K, &A.tk, bar_load, 0, r0, kvu, A.H / A.G, A.seq);
+      tma_load_rows(sb + C::OFF_V, &A.tv, bar_load, 0, r0, kvu, A.H / A.G, A.seq);
     }
   };
   __syncthreads();  // barriers initialised before the first copy is issued
@@ -677,7 +681,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
       const float inv = 1.f / den;
       const bool valid = row < nvalid;
       __nv_bfloat16* yrow =
-          reinterpret_cast<__nv_bfloat16*>(A.y) + ((size_t)unit * A.n + r0 + row) * D;
+          reinterpret_cast<__nv_bfloat16*>(A.y) + (size_t)row_index(unit, r0 + row, A.H, A.n, A.seq) * D;
       if (KIND == HH_FMAP_HEDGEHOG) {
         constexpr int HC = D / 2;
 #pragma unroll
@@ -897,15 +901,19 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   const uint64_t U = (uint64_t)p.B * p.H;
   bool ok = true;
   if (KIND == HH_FMAP_HEDGEHOG) {
-    ok &= make_map(&a.tq, q, D, p.n, U, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= make_map(&a.tk, k, D, p.n, U / p.G, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= make_map(&a.tv, v, D, p.n, U / p.G, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B);
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    ok &= make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major);
+    ok &= make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major);
+    ok &= make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major);
     ok &= make_map(&a.twq, p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
     ok &= make_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    ok &= make_map(&a.tq, q, 16, p.n, U, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok &= make_map(&a.tk, k, 16, p.n, U / p.G, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok &= make_map(&a.tv, v, 16, p.n, U / p.G, 16, kTile, CU_TENSOR_MAP_SWIZZLE_32B);
+    ok &= make_rows_map(&a.tq, q, 16, p.n, p.H, p.B, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        p.seq_major);
+    ok &= make_rows_map(&a.tk, k, 16, p.n, p.H / p.G, p.B, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        p.seq_major);
+    ok &= make_rows_map(&a.tv, v, 16, p.n, p.H / p.G, p.B, 16, kTile, CU_TENSOR_MAP_SWIZZLE_32B,
+                        p.seq_major);
   }
   if (!ok) return cudaErrorInvalidValue;
   a.y = y;
@@ -927,6 +935,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   a.NT = pl.NT;
   a.sep_wk = p.Wk ? 1 : 0;
   a.G = p.G;
+  a.seq = p.seq_major;
   const size_t smem = smem_bytes<KIND, D>();
   float* init = nullptr;
   if (p.S0) {

@@ -35,6 +35,7 @@
 #include <algorithm>
 
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace hh {
 namespace {
@@ -83,6 +84,7 @@ struct Args2 {
   int64_t n;
   int H, P, L, NT;
   int G;               // query heads per key/value head
+  int seq;             // q, k, v, y are [B][n][H][D]
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -139,13 +141,14 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     const int r0 = (t_begin + i) * TILE;
     const uint32_t base = sb + slot_off(s);
     mbar_expect_tx(bar(B_LDQK + s), 2 * 16384);
-    tma_load_3d(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, (int)unit);
-    tma_load_3d(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, (int)kvu);
+    tma_load_rows(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, unit, A.H, A.seq);
+    tma_load_rows(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, kvu, A.H / A.G, A.seq);
   };
   auto load_v = [&](int i) {
     const int s = i & 1;
     mbar_expect_tx(bar(B_LDV + s), 16384);
-    tma_load_3d(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, (int)kvu);
+    tma_load_rows(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, kvu,
+                  A.H / A.G, A.seq);
   };
   if (warp == 8 && lane == 0) {
     mbar_expect_tx(bar(B_W), 8192u);
@@ -506,7 +509,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       tmem_ld2(tmem + lb + TM_X(s) + 64, d0, d1);   // rowsum(P) + phi(q) . z_hi, phi(q) . z_lo
       const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
       if (r0 + row < A.n) {
-        uint4* dst = reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D + 32 * c);
+        uint4* dst = reinterpret_cast<uint4*>(
+            A.y + (size_t)row_index(unit, r0 + row, A.H, A.n, A.seq) * D + 32 * c);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int j = 8 * q4;
@@ -591,9 +595,12 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
   if (p.Wk) return cudaErrorInvalidValue;  // one map shared by queries and keys
-  const uint64_t Ukv = U / p.G;
-  bool ok = make_map(&a.tq, q, D, p.n, U, TILE) && make_map(&a.tk, k, D, p.n, Ukv, TILE) &&
-            make_map(&a.tv, v, D, p.n, Ukv, TILE) && make_map(&a.tw, p.Wq, D, D, p.H, D);
+  const int Hkv = p.H / p.G;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, TILE, sw, p.seq_major) &&
+            make_rows_map(&a.tk, k, D, p.n, Hkv, p.B, 64, TILE, sw, p.seq_major) &&
+            make_rows_map(&a.tv, v, D, p.n, Hkv, p.B, 64, TILE, sw, p.seq_major) &&
+            make_map(&a.tw, p.Wq, D, D, p.H, D);
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
@@ -613,6 +620,7 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   a.L = pl.L;
   a.NT = pl.NT;
   a.G = p.G;
+  a.seq = p.seq_major;
   auto kern = p.softmax ? prefill_tc2_kernel<true> : prefill_tc2_kernel<false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);

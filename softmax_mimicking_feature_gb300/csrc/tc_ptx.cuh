@@ -148,6 +148,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cta.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+// Rows [row, row + box) of head unit `unit` (= b * H + h) of a q/k/v tensor
+// through its 4-D map (tmap.cuh): dims (cols, n, H, B) for the [B][H][n][cols]
+// layout, (cols, H, n, B) for [B][n][H][cols] (seq_major).
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                              int x, int row, int64_t unit, int H,
+                                              int seq_major) {
+  const int b = (int)(unit / H), h = (int)(unit % H);
+  if (seq_major) tma_load_4d(dst, map, bar, x, h, row, b);
+  else tma_load_4d(dst, map, bar, x, row, h, b);
+}
+
 // Untiled bulk copy global -> shared; both addresses 16-byte aligned, bytes a
 // multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,

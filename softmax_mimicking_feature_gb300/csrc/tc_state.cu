@@ -28,6 +28,7 @@
 
 #include "taylor_pack.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace hh {
 namespace {
@@ -104,6 +105,7 @@ struct StateArgs {
   int64_t n;
   int H, P, L, NT;
   int G;              // query heads per key/value head
+  int seq;            // k, v are [B][n][Hkv][D]
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -165,14 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     const uint32_t b = bar(SB_LDK + (i & 1));
     mbar_expect_tx(b, C::XT);
     for (int x = 0; x < (D + 63) / 64; ++x)
-      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
+      tma_load_rows(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, kvu,
+                    A.H / A.G, A.seq);
   };
   auto load_v = [&](int i) {
     const uint32_t dst = sb + C::OFF_V + (i % NV) * C::XT;
     const uint32_t b = bar(SB_LDV + (i % NV));
     mbar_expect_tx(b, C::XT);
     for (int x = 0; x < (D + 63) / 64; ++x)
-      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
+      tma_load_rows(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, kvu,
+                    A.H / A.G, A.seq);
   };
   if (warp == 8 && lane == 0 && nt > 0) {
     if (HH) {
@@ -459,7 +463,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const uint32_t dst = sb + OFF_K + (i & 1) * XT, b = bar(B_LDK + (i & 1));
     mbar_expect_tx(b, XT);
     for (int x = 0; x < 2; ++x)
-      tma_load_3d(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
+      tma_load_rows(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, kvu,
+                    A.H / A.G, A.seq);
   };
   // V(i) (and, for the softmax map, the tile's per-token offsets, whose smem
   // buffer is free for the same reason as V's: E1(i-2) and G2(i-2) are done)
@@ -467,7 +472,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const uint32_t dst = sb + OFF_V + (i & 1) * XT, b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT + (A.off ? TILE * 8 : 0));
     for (int x = 0; x < 2; ++x)
-      tma_load_3d(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, (int)kvu);
+      tma_load_rows(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, kvu,
+                    A.H / A.G, A.seq);
     if (A.off)
       bulk_load(sb + OFF_OX + (i & 1) * TILE * 8,
                 A.off + (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE, TILE * 8, b);
@@ -712,12 +718,14 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   auto load_k = [&](int i) {
     const uint32_t b = bar(B_LDK + (i & 1));
     mbar_expect_tx(b, XT);
-    tma_load_3d(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, (int)kvu);
+    tma_load_rows(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, kvu,
+                    A.H / A.G, A.seq);
   };
   auto load_v = [&](int i) {
     const uint32_t b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT);
-    tma_load_3d(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, (int)kvu);
+    tma_load_rows(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, kvu,
+                    A.H / A.G, A.seq);
   };
   if (warp == 8 && lane == 0)
     for (int i = 0; i < 2 && i < nt; ++i) {
@@ -914,12 +922,15 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   const uint64_t U = (uint64_t)p.B * p.H;
   bool ok;
   if (KIND == HH_FMAP_HEDGEHOG) {
-    ok = make_map(&a.tk, k, D, p.n, U / p.G, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(&a.tv, v, D, p.n, U / p.G, 64, TILE, CU_TENSOR_MAP_SWIZZLE_128B) &&
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    ok = make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, TILE, sw, p.seq_major) &&
+         make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, TILE, sw, p.seq_major) &&
          make_map(&a.tw, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    ok = make_map(&a.tk, k, 16, p.n, U / p.G, 16, TILE, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_map(&a.tv, v, 16, p.n, U / p.G, 16, TILE, CU_TENSOR_MAP_SWIZZLE_32B);
+    ok = make_rows_map(&a.tk, k, 16, p.n, p.H / p.G, p.B, 16, TILE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       p.seq_major) &&
+         make_rows_map(&a.tv, v, 16, p.n, p.H / p.G, p.B, 16, TILE, CU_TENSOR_MAP_SWIZZLE_32B,
+                       p.seq_major);
   }
   if (!ok) return cudaErrorInvalidValue;
   a.ws = reinterpret_cast<float*>(ws);
@@ -935,6 +946,7 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   a.L = pl.L;
   a.NT = pl.NT;
   a.G = p.G;
+  a.seq = p.seq_major;
   if (KIND == HH_FMAP_TAYLOR2) {
     cudaError_t e = cudaFuncSetAttribute(state_taylor_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

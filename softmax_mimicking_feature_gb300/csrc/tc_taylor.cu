@@ -28,6 +28,7 @@
 
 #include "taylor_pack.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace hh {
 namespace {
@@ -67,6 +68,7 @@ struct ArgsT {
   int64_t n;
   int P, L, NT;
   int H, G;          // heads; query heads per key/value head
+  int seq;           // q, k, v, y are [B][n][H][16]
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -142,9 +144,9 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     const int s = i & 1;
     const int r0 = (t_begin + i) * TILE;
     mbar_expect_tx(bar(B_LD + s), 3 * XT);
-    tma_load_3d(sb + OFF_Q + s * XT, &A.tq, bar(B_LD + s), 0, r0, (int)unit);
-    tma_load_3d(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, (int)kvu);
-    tma_load_3d(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, (int)kvu);
+    tma_load_rows(sb + OFF_Q + s * XT, &A.tq, bar(B_LD + s), 0, r0, unit, A.H, A.seq);
+    tma_load_rows(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, kvu, A.H / A.G, A.seq);
+    tma_load_rows(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, kvu, A.H / A.G, A.seq);
   };
   if (warp == 8 && lane == 0)
     for (int i = 0; i < 2 && i < nt; ++i) load(i);
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
       if (r0 + row < A.n) {
         const int j = 8 * c;
-        *reinterpret_cast<uint4*>(A.y + ((size_t)unit * A.n + r0 + row) * D + j) = make_uint4(
+        *reinterpret_cast<uint4*>(A.y + (size_t)row_index(unit, r0 + row, A.H, A.n, A.seq) * D + j) = make_uint4(
             pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
             pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
             pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
@@ -503,34 +505,6 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// [planes][rows][16] bf16 with a {16, 128, 1} box and the 32-byte swizzle
-bool make_map16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes) {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  if (!fn) return false;
-  cuuint64_t dims[3] = {16, rows, planes};
-  cuuint64_t strides[2] = {32, 32 * rows};
-  cuuint32_t box[3] = {16, TILE, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 // Output pass of the Taylor (d = 16) prefill: U * P CTAs, one per segment.
@@ -542,8 +516,11 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
   if (p.kind != HH_FMAP_TAYLOR2 || p.d != 16) return cudaErrorInvalidValue;
-  bool ok = make_map16(&a.tq, q, p.n, U) && make_map16(&a.tk, k, p.n, U / p.G) &&
-            make_map16(&a.tv, v, p.n, U / p.G);
+  // 16-column rows (32 bytes), 32-byte swizzle: the layout the MMA descriptors expect
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 16, TILE, sw, p.seq_major) &&
+            make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 16, TILE, sw, p.seq_major) &&
+            make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 16, TILE, sw, p.seq_major);
   if (!ok) return cudaErrorInvalidValue;
   a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
@@ -559,6 +536,7 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
   a.NT = pl.NT;
   a.H = p.H;
   a.G = p.G;
+  a.seq = p.seq_major;
   cudaError_t e = cudaFuncSetAttribute(taylor_out_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
