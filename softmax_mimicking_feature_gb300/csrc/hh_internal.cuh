@@ -67,6 +67,12 @@ __host__ __device__ __forceinline__ int64_t row_index(int64_t u, int64_t t, int 
   return seq_major ? ((u / H) * n + t) * H + u % H : u * n + t;
 }
 
+// The same for head h of batch b, without a division.
+__host__ __device__ __forceinline__ int64_t row_of(int b, int h, int64_t t, int H, int64_t n,
+                                                   int seq_major) {
+  return seq_major ? ((int64_t)b * n + t) * H + h : ((int64_t)b * H + h) * n + t;
+}
+
 // Row stride of the softmax-map offset arrays.
 inline int64_t off_stride(int64_t n) { return (n + 127) / 128 * 128; }
 

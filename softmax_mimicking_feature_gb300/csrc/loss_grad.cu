@@ -54,14 +54,14 @@ __device__ inline GradSmem carve(float* sm, int d, int dpp) {
   return g;
 }
 
-// Rows [row0, row0 + kT) of head unit `unit` of a tensor with Hx heads in the
+// Rows [row0, row0 + kT) of head h of batch b of a tensor with Hx heads in the
 // [B][Hx][n][width] layout, or [B][n][Hx][width] (seq); zero past n.
 template <typename T>
-__device__ inline void load_tile(float* dst, const T* src, int64_t unit, int Hx, int seq,
+__device__ inline void load_tile(float* dst, const T* src, int b, int h, int Hx, int seq,
                                  int64_t row0, int64_t n, int width) {
   for (int i = threadIdx.x; i < kT * width; i += kThreads) {
     const int r = i / width;
-    dst[i] = row0 + r < n ? to_f(src[row_index(unit, row0 + r, Hx, n, seq) * width + i % width])
+    dst[i] = row0 + r < n ? to_f(src[row_of(b, h, row0 + r, Hx, n, seq) * width + i % width])
                           : 0.f;
   }
 }
@@ -114,20 +114,21 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
+  const int ub = (int)(u / H), uh = (int)(u % H), kh = uh / G;   // batch, q head, kv head
   const int qt = blockIdx.x % ntiles;
   const int64_t q0 = (int64_t)qt * kT;
   const int t = threadIdx.x, r = t / 8, slot = t % 8;
   const int64_t qi = q0 + r;
   const float scale = rsqrtf((float)d);
-  load_tile(S.xs, q, u, H, seq, q0, n, d);
-  load_tile(S.pxs, phq, u, 1, 0, q0, n, dpp);
+  load_tile(S.xs, q, ub, uh, H, seq, q0, n, d);
+  load_tile(S.pxs, phq, (int)u, 0, 1, 0, q0, n, dpp);
 
   // sweep 1: M_i = max s, Z_i = sum e^{s - M}, A_i = sum a over j <= i
   float m = -INFINITY, z = 0.f, asum = 0.f;
   for (int kt = 0; kt <= qt; ++kt) {
     __syncthreads();
-    load_tile(S.ys, k, kv_unit(u, H, G), H / G, seq, (int64_t)kt * kT, n, d);
-    load_tile(S.pys, phk, u, 1, 0, (int64_t)kt * kT, n, dpp);
+    load_tile(S.ys, k, ub, kh, H / G, seq, (int64_t)kt * kT, n, d);
+    load_tile(S.pys, phk, (int)u, 0, 1, 0, (int64_t)kt * kT, n, dpp);
     __syncthreads();
     for (int c = slot; c < kT; c += 8) {
       const int64_t kj = (int64_t)kt * kT + c;
@@ -168,8 +169,8 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
   const int nf = dpp / 8;
   for (int kt = 0; kt <= qt; ++kt) {
     __syncthreads();
-    load_tile(S.ys, k, kv_unit(u, H, G), H / G, seq, (int64_t)kt * kT, n, d);
-    load_tile(S.pys, phk, u, 1, 0, (int64_t)kt * kT, n, dpp);
+    load_tile(S.ys, k, ub, kh, H / G, seq, (int64_t)kt * kT, n, d);
+    load_tile(S.pys, phk, (int)u, 0, 1, 0, (int64_t)kt * kT, n, dpp);
     __syncthreads();
     for (int c = slot; c < kT; c += 8) {
       const int64_t kj = (int64_t)kt * kT + c;
@@ -202,20 +203,21 @@ __global__ void __launch_bounds__(kThreads) grad_key_kernel(
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
+  const int ub = (int)(u / H), uh = (int)(u % H), kh = uh / G;   // batch, q head, kv head
   const int kt = blockIdx.x % ntiles;
   const int64_t k0 = (int64_t)kt * kT;
   const int t = threadIdx.x, r = t / 8, slot = t % 8;   // r: key row of the tile
   const float scale = rsqrtf((float)d);
-  load_tile(S.xs, k, kv_unit(u, H, G), H / G, seq, k0, n, d);
-  load_tile(S.pxs, phk, u, 1, 0, k0, n, dpp);
+  load_tile(S.xs, k, ub, kh, H / G, seq, k0, n, d);
+  load_tile(S.pxs, phk, (int)u, 0, 1, 0, k0, n, dpp);
   float acc[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) acc[i] = 0.f;
   const int nf = dpp / 8;
   for (int qt = kt; qt < ntiles; ++qt) {
     __syncthreads();
-    load_tile(S.ys, q, u, H, seq, (int64_t)qt * kT, n, d);
-    load_tile(S.pys, phq, u, 1, 0, (int64_t)qt * kT, n, dpp);
+    load_tile(S.ys, q, ub, uh, H, seq, (int64_t)qt * kT, n, d);
+    load_tile(S.pys, phq, (int)u, 0, 1, 0, (int64_t)qt * kT, n, dpp);
     for (int i = threadIdx.x; i < kT * 3; i += kThreads) {
       const int64_t row = (int64_t)qt * kT + i / 3;
       S.st[i] = row < n ? stats[(u * n + row) * 3 + i % 3] : 1.f;
@@ -267,14 +269,14 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
     for (int64_t b = 0; b < B; ++b) {
       const size_t base = ((size_t)b * H + h) * n;
       const int Gs = side ? G2 : G1;
-      const int64_t ux = kv_unit((int64_t)b * H + h, H, Gs);   // unit of x (k under grouping)
+      const int hx = h / Gs;   // head of x (the key/value head when x is k under grouping)
       for (int64_t t0 = 0; t0 < n; t0 += 32) {
         __syncthreads();
         for (int i = t; i < 32 * 32; i += kThreads) {
           const int rr = i / 32, cc = i % 32;
           const bool ok = t0 + rr < n;
           xs[rr][cc] = ok && a0 + cc < d
-                           ? to_f(x[row_index(ux, t0 + rr, H / Gs, n, seq) * d + a0 + cc])
+                           ? to_f(x[row_of((int)b, hx, t0 + rr, H / Gs, n, seq) * d + a0 + cc])
                            : 0.f;
           hs[rr][cc] = ok && l0 + cc < d ? dh[(base + t0 + rr) * d + l0 + cc] : 0.f;
         }

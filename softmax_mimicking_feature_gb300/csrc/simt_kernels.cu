@@ -143,10 +143,11 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 
   const int64_t bh = blockIdx.x;
   const int h = (int)(bh % H);
-  const int64_t kvu = kv_unit(bh, H, G);   // k, v of this query head
-  // element offset of token t of this head in q / y, and in k / v
-  auto qrow = [&](int64_t t) { return (size_t)row_index(bh, t, H, n, seq) * d; };
-  auto kvrow = [&](int64_t t) { return (size_t)row_index(kvu, t, H / G, n, seq) * d; };
+  // batch, query head and key/value head of this unit; element offset of
+  // token t of this head in q / y, and in k / v
+  const int ub = (int)(bh / H), uh = (int)(bh % H), kh = uh / G;
+  auto qrow = [&](int64_t t) { return (size_t)row_of(ub, uh, t, H, n, seq) * d; };
+  auto kvrow = [&](int64_t t) { return (size_t)row_of(ub, kh, t, H / G, n, seq) * d; };
   const T* Wqh = Wq ? Wq + (size_t)h * d * d : nullptr;
   const T* Wkh = Wk ? Wk + (size_t)h * d * d : nullptr;
   const float* bqh = bq ? bq + (size_t)h * d : nullptr;
@@ -270,10 +271,11 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
   const int row = tid >> 2, part = tid & 3;
   const int64_t i = r0 + row;
   const float scale = rsqrtf((float)d);
+  const int ub = (int)(bh / H), uh = (int)(bh % H), kh = uh / G;   // batch, q head, kv head
 
   for (int e = tid; e < kLossRows * d; e += kThreads) {
     const int64_t rr = r0 + e / d;
-    qs[e] = rr < n ? to_f(q[(size_t)row_index(bh, rr, H, n, seq) * d + e % d]) : 0.f;
+    qs[e] = rr < n ? to_f(q[(size_t)row_of(ub, uh, rr, H, n, seq) * d + e % d]) : 0.f;
   }
   for (int e = tid; e < kLossRows * dpp; e += kThreads) {
     const int64_t rr = r0 + e / dpp;
@@ -285,8 +287,7 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     __syncthreads();
     for (int e = tid; e < kLossKeys * d; e += kThreads) {
       const int64_t j = k0 + e / d;
-      ks[e] = j < n ? to_f(k[(size_t)row_index(kv_unit(bh, H, G), j, H / G, n, seq) * d + e % d])
-                    : 0.f;
+      ks[e] = j < n ? to_f(k[(size_t)row_of(ub, kh, j, H / G, n, seq) * d + e % d]) : 0.f;
     }
     for (int e = tid; e < kLossKeys * dpp; e += kThreads) {
       const int64_t j = k0 + e / dpp;

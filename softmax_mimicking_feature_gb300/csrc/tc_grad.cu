@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
   const int rank = (int)((blockIdx.x >> 1) / A.U);
   const int64_t unit = (blockIdx.x >> 1) % A.U;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int rt = side ? rank : A.NT - 1 - rank;   // resident tile
   const int64_t r0 = (int64_t)rt * kRT;
   // streamed rows: keys 0 .. min(r0 + 128, n) (query side) or queries r0 .. n (key side)
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       mbar_expect_tx(bar_x, C::X_BYTES + C::PX_BYTES);
       for (int i = 0; i < D / 64; ++i)
         tma_load_rows(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0,
-                      side ? kvu : unit, side ? A.H / A.G : A.H, A.seq);
+                      ub, side ? kh : uh, A.seq);
       for (int i = 0; i < DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PX + i * 16384, &A.tpx[side], bar_x, 64 * i, (int)r0, (int)unit);
       // Y(t) after S/A(t-2) read its stage; phi(Y)(t) after G phi(Y)(t-3)
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
         for (int i = 0; i < D / 64; ++i)
           tma_load_rows(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
-                        64 * i, (int)y0, side ? unit : kvu, side ? A.H : A.H / A.G, A.seq);
+                        64 * i, (int)y0, ub, side ? uh : kh, A.seq);
         if (t >= 3) ok = mbar_wait_poll(bar_pyfree + 8 * p, (t / 3 - 1) & 1, wp);
         if (!ok) break;
         mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (side ? C::ST_BYTES : 0));

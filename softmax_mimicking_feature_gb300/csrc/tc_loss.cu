@@ -143,8 +143,7 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
     for (int i = 0; i < D / 64; ++i) {
       tma_load_3d(sb + OFF_W + i * (D * 128), &A.tw[side], bar_load, 64 * i, 0, h);
       tma_load_rows(sb + OFF_X + i * 16384, &A.tx[side], bar_load, 64 * i, (int)r0,
-                    A.kv[side] ? kv_unit(unit, A.H, A.G) : unit,
-                    A.kv[side] ? A.H / A.G : A.H, A.seq);
+                    (int)(unit / A.H), A.kv[side] ? h / A.G : h, A.seq);
     }
   }
   if (warp == 0) {
@@ -314,6 +313,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   const int qt = A.NT - 1 - (int)(blockIdx.x / A.U);
   const int64_t unit = blockIdx.x % A.U;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int64_t q0 = (int64_t)qt * kTile;
   const int nkt = qt + 1;
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
@@ -350,8 +351,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       auto load_k = [&](int j) {
         mbar_expect_tx(bar_k, C::Q_BYTES);
         for (int i = 0; i < D / 64; ++i)
-          tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, kvu,
-                        A.H / A.G, A.seq);
+          tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, ub,
+                        kh, A.seq);
       };
       auto load_pk = [&](int j) {
         mbar_expect_tx(bar_pk, C::PQ_BYTES);
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       };
       mbar_expect_tx(bar_q, C::Q_BYTES + C::PQ_BYTES);
       for (int i = 0; i < D / 64; ++i)
-        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, unit, A.H, A.seq);
+        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, ub, uh, A.seq);
       for (int i = 0; i < C::DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PQ + i * 16384, &A.tpq, bar_q, 64 * i, (int)q0, (int)unit);
       load_k(0);

@@ -252,6 +252,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 
   const int64_t unit = blockIdx.x / A.P;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % A.P;
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -278,16 +280,14 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     mbar_expect_tx(bar_load, bytes);
     if (KIND == HH_FMAP_HEDGEHOG) {
       for (int i = 0; i < D / 64; ++i) {
-        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, unit, A.H, A.seq);
-        tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, kvu, A.H / A.G,
-                      A.seq);
-        tma_load_rows(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, kvu, A.H / A.G,
-                      A.seq);
+        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, ub, uh, A.seq);
+        tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, ub, kh, A.seq);
+        tma_load_rows(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, ub, kh, A.seq);
       }
     } else {
-      tma_load_rows(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, unit, A.H, A.seq);
-      tma_load_rows(sb + C::OFF_K, &A.tk, bar_load, 0, r0, kvu, A.H / A.G, A.seq);
-      tma_load_rows(sb + C::OFF_V, &A.tv, bar_load, 0, r0, kvu, A.H / A.G, A.seq);
+      tma_load_rows(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, ub, uh, A.seq);
+      tma_load_rows(sb + C::OFF_K, &A.tk, bar_load, 0, r0, ub, kh, A.seq);
+      tma_load_rows(sb + C::OFF_V, &A.tv, bar_load, 0, r0, ub, kh, A.seq);
     }
   };
   __syncthreads();  // barriers initialised before the first copy is issued
@@ -681,7 +681,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
       const float inv = 1.f / den;
       const bool valid = row < nvalid;
       __nv_bfloat16* yrow =
-          reinterpret_cast<__nv_bfloat16*>(A.y) + (size_t)row_index(unit, r0 + row, A.H, A.n, A.seq) * D;
+          reinterpret_cast<__nv_bfloat16*>(A.y) + (size_t)row_of(ub, uh, r0 + row, A.H, A.n, A.seq) * D;
       if (KIND == HH_FMAP_HEDGEHOG) {
         constexpr int HC = D / 2;
 #pragma unroll

@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / A.P;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % A.P;
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -141,14 +143,14 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     const int r0 = (t_begin + i) * TILE;
     const uint32_t base = sb + slot_off(s);
     mbar_expect_tx(bar(B_LDQK + s), 2 * 16384);
-    tma_load_rows(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, unit, A.H, A.seq);
-    tma_load_rows(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, kvu, A.H / A.G, A.seq);
+    tma_load_rows(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, ub, uh, A.seq);
+    tma_load_rows(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, ub, kh, A.seq);
   };
   auto load_v = [&](int i) {
     const int s = i & 1;
     mbar_expect_tx(bar(B_LDV + s), 16384);
-    tma_load_rows(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, kvu,
-                  A.H / A.G, A.seq);
+    tma_load_rows(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, ub,
+                  kh, A.seq);
   };
   if (warp == 8 && lane == 0) {
     mbar_expect_tx(bar(B_W), 8192u);
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
       if (r0 + row < A.n) {
         uint4* dst = reinterpret_cast<uint4*>(
-            A.y + (size_t)row_index(unit, r0 + row, A.H, A.n, A.seq) * D + 32 * c);
+            A.y + (size_t)row_of(ub, uh, r0 + row, A.H, A.n, A.seq) * D + 32 * c);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int j = 8 * q4;

@@ -156,13 +156,12 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
-// Rows [row, row + box) of head unit `unit` (= b * H + h) of a q/k/v tensor
-// through its 4-D map (tmap.cuh): dims (cols, n, H, B) for the [B][H][n][cols]
-// layout, (cols, H, n, B) for [B][n][H][cols] (seq_major).
+// Rows [row, row + box) of head h of batch b of a q/k/v tensor through its
+// 4-D map (tmap.cuh): dims (cols, n, H, B) for the [B][H][n][cols] layout,
+// (cols, H, n, B) for [B][n][H][cols] (seq_major).  Kernels split their unit
+// into (b, h) once: a 64-bit division per load would sit on the loader's path.
 __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                              int x, int row, int64_t unit, int H,
-                                              int seq_major) {
-  const int b = (int)(unit / H), h = (int)(unit % H);
+                                              int x, int row, int b, int h, int seq_major) {
   if (seq_major) tma_load_4d(dst, map, bar, x, h, row, b);
   else tma_load_4d(dst, map, bar, x, row, h, b);
 }

@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % (A.P - 1);
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -167,16 +169,16 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     const uint32_t b = bar(SB_LDK + (i & 1));
     mbar_expect_tx(b, C::XT);
     for (int x = 0; x < (D + 63) / 64; ++x)
-      tma_load_rows(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, kvu,
-                    A.H / A.G, A.seq);
+      tma_load_rows(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, ub,
+                    kh, A.seq);
   };
   auto load_v = [&](int i) {
     const uint32_t dst = sb + C::OFF_V + (i % NV) * C::XT;
     const uint32_t b = bar(SB_LDV + (i % NV));
     mbar_expect_tx(b, C::XT);
     for (int x = 0; x < (D + 63) / 64; ++x)
-      tma_load_rows(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, kvu,
-                    A.H / A.G, A.seq);
+      tma_load_rows(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, ub,
+                    kh, A.seq);
   };
   if (warp == 8 && lane == 0 && nt > 0) {
     if (HH) {
@@ -447,6 +449,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % (A.P - 1);
   const int h = (int)(unit % A.H);
   const int t_begin = seg * A.L;
@@ -463,8 +467,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const uint32_t dst = sb + OFF_K + (i & 1) * XT, b = bar(B_LDK + (i & 1));
     mbar_expect_tx(b, XT);
     for (int x = 0; x < 2; ++x)
-      tma_load_rows(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, kvu,
-                    A.H / A.G, A.seq);
+      tma_load_rows(dst + x * 16384, &A.tk, b, 64 * x, (t_begin + i) * TILE, ub,
+                    kh, A.seq);
   };
   // V(i) (and, for the softmax map, the tile's per-token offsets, whose smem
   // buffer is free for the same reason as V's: E1(i-2) and G2(i-2) are done)
@@ -472,8 +476,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     const uint32_t dst = sb + OFF_V + (i & 1) * XT, b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT + (A.off ? TILE * 8 : 0));
     for (int x = 0; x < 2; ++x)
-      tma_load_rows(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, kvu,
-                    A.H / A.G, A.seq);
+      tma_load_rows(dst + x * 16384, &A.tv, b, 64 * x, (t_begin + i) * TILE, ub,
+                    kh, A.seq);
     if (A.off)
       bulk_load(sb + OFF_OX + (i & 1) * TILE * 8,
                 A.off + (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE, TILE * 8, b);
@@ -704,6 +708,8 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % (A.P - 1);
   const int t_begin = seg * A.L;
   const int nt = min(A.NT, t_begin + A.L) - t_begin;
@@ -718,14 +724,14 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   auto load_k = [&](int i) {
     const uint32_t b = bar(B_LDK + (i & 1));
     mbar_expect_tx(b, XT);
-    tma_load_rows(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, kvu,
-                    A.H / A.G, A.seq);
+    tma_load_rows(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, ub,
+                    kh, A.seq);
   };
   auto load_v = [&](int i) {
     const uint32_t b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT);
-    tma_load_rows(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, kvu,
-                    A.H / A.G, A.seq);
+    tma_load_rows(sb + OFF_V + (i & 1) * XT, &A.tv, b, 0, (t_begin + i) * TILE, ub,
+                    kh, A.seq);
   };
   if (warp == 8 && lane == 0)
     for (int i = 0; i < 2 && i < nt; ++i) {

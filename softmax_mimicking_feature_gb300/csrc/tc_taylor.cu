@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / A.P;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
+  // batch, query head and key/value head of this unit (split once)
+  const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % A.P;
   const int t_begin = seg * A.L;
   const int nt = min(A.NT, t_begin + A.L) - t_begin;
@@ -144,9 +146,9 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     const int s = i & 1;
     const int r0 = (t_begin + i) * TILE;
     mbar_expect_tx(bar(B_LD + s), 3 * XT);
-    tma_load_rows(sb + OFF_Q + s * XT, &A.tq, bar(B_LD + s), 0, r0, unit, A.H, A.seq);
-    tma_load_rows(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, kvu, A.H / A.G, A.seq);
-    tma_load_rows(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, kvu, A.H / A.G, A.seq);
+    tma_load_rows(sb + OFF_Q + s * XT, &A.tq, bar(B_LD + s), 0, r0, ub, uh, A.seq);
+    tma_load_rows(sb + OFF_K + s * XT, &A.tk, bar(B_LD + s), 0, r0, ub, kh, A.seq);
+    tma_load_rows(sb + OFF_V + s * XT, &A.tv, bar(B_LD + s), 0, r0, ub, kh, A.seq);
   };
   if (warp == 8 && lane == 0)
     for (int i = 0; i < 2 && i < nt; ++i) load(i);
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
       if (r0 + row < A.n) {
         const int j = 8 * c;
-        *reinterpret_cast<uint4*>(A.y + (size_t)row_index(unit, r0 + row, A.H, A.n, A.seq) * D + j) = make_uint4(
+        *reinterpret_cast<uint4*>(A.y + (size_t)row_of(ub, uh, r0 + row, A.H, A.n, A.seq) * D + j) = make_uint4(
             pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
             pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
             pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
