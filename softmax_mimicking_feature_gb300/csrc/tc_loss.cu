@@ -89,8 +89,8 @@ __device__ __forceinline__ uint32_t lane_base(int warp) {
 // One launch maps one or two inputs ("sides", e.g. q and k); the grid is
 // sides x U x NT tiles.
 struct FmapArgs {
-  CUtensorMap tx[2], tw[2];
-  __nv_bfloat16* phi[2];   // [U][n][2D] or null
+  CUtensorMap tx[2], tw[2], tphi[2];
+  __nv_bfloat16* phi[2];   // [U][n][2D] or null (written through tphi)
   float2* off[2];          // [U][NT*128] softmax-map offsets (log2 units) or null
   const float* bias[2];    // [H][D] or null
   int kv[2];               // input indexed by key/value head (keys under grouping)
@@ -108,13 +108,17 @@ struct FmapArgs {
 template <int D>
 __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ FmapArgs A) {
   constexpr uint32_t W_BYTES = D * D * 2, X_BYTES = kTile * D * 2;
+  // the phi tile ([128 rows][2D], 64-feature panels of 16 KB, 128B swizzle) is
+  // staged over W and X once the MMA has read them, then stored by TMA
+  constexpr uint32_t PHI_BYTES = kTile * 2 * D * 2;
+  constexpr uint32_t AREA = (W_BYTES + X_BYTES) > PHI_BYTES ? (W_BYTES + X_BYTES) : PHI_BYTES;
   constexpr uint32_t TM_COLS = D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const uint32_t OFF_W = 0, OFF_X = W_BYTES;
-  float* bias_s = reinterpret_cast<float*>(sm + W_BYTES + X_BYTES);
+  float* bias_s = reinterpret_cast<float*>(sm + AREA);
   float2* red = reinterpret_cast<float2*>(bias_s + 136);   // [2 halves][128 rows]
   const uint32_t bar_load = smem_u32(bias_s + 128);
   const uint32_t bar_mma = bar_load + 8;
@@ -218,11 +222,10 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
       if (A.off[side] && half == 0 && valid)
         A.off[side][(size_t)unit * A.NT * kTile + r0 + row] = make_float2(op, on);
     }
-    __nv_bfloat16* prow =
-        A.phi[side] ? A.phi[side] + ((size_t)unit * A.n + r0 + row) * (2 * D) : nullptr;
+    const bool write_phi = A.phi[side] != nullptr;
 #pragma unroll
     for (int c = 0; c < HC; c += 32) {
-      if (!prow) break;
+      if (!write_phi) break;
       uint32_t hv[32];
       tmem_ld32(trow + c, hv);
       uint32_t pp[16], pn[16];
@@ -234,14 +237,26 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
         pp[j / 2] = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -op)), ex2_approx(fmaf(h1, kLog2e, -op)));
         pn[j / 2] = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -on)), ex2_approx(fmaf(-h1, kLog2e, -on)));
       }
-      if (valid) {
-        uint4* dp = reinterpret_cast<uint4*>(prow + half * HC + c);
-        uint4* dn = reinterpret_cast<uint4*>(prow + D + half * HC + c);
+      // features f = half*HC + c .. +32 (positive) and D + f (negative):
+      // four 16-byte chunks each in the swizzled panel of their feature block
+      const int fp = half * HC + c, fn = D + half * HC + c;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          dp[q4] = make_uint4(pp[4 * q4], pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
-          dn[q4] = make_uint4(pn[4 * q4], pn[4 * q4 + 1], pn[4 * q4 + 2], pn[4 * q4 + 3]);
-        }
+      for (int q4 = 0; q4 < 4; ++q4) {
+        st_shared_v4(sb + (fp / 64) * 16384 + sw128_chunk(row, (fp % 64) / 8 + q4), pp[4 * q4],
+                     pp[4 * q4 + 1], pp[4 * q4 + 2], pp[4 * q4 + 3]);
+        st_shared_v4(sb + (fn / 64) * 16384 + sw128_chunk(row, (fn % 64) / 8 + q4), pn[4 * q4],
+                     pn[4 * q4 + 1], pn[4 * q4 + 2], pn[4 * q4 + 3]);
+      }
+    }
+    if (write_phi) {
+      // whole 128-byte rows per panel; rows past n are clipped by the store
+      fence_proxy_async();
+      __syncthreads();
+      if (tid == 0) {
+        for (int i = 0; i < 2 * D / 64; ++i)
+          tma_store_3d(&A.tphi[side], sb + i * 16384, 64 * i, (int)r0, (int)unit);
+        tma_store_commit();
+        tma_store_wait_all();
       }
     }
   }
@@ -581,6 +596,7 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
         !make_map(&a.tw[i], W, D, D, p.H, D))
       return cudaErrorInvalidValue;
     a.phi[i] = reinterpret_cast<__nv_bfloat16*>(phi[i]);
+    if (phi[i] && !make_map(&a.tphi[i], phi[i], 2 * D, p.n, U, kTile)) return cudaErrorInvalidValue;
     a.off[i] = p.softmax ? off[i] : nullptr;
     a.bias[i] = is_key[i] && p.Wk ? p.bk : p.bq;
   }
@@ -594,7 +610,8 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
   a.n = p.n;
   a.H = p.H;
   a.NT = ceil_div(p.n, kTile);
-  const size_t smem = D * D * 2 + kTile * D * 2 + 136 * 4 + 256 * 8 + 1024;
+  const size_t area = std::max<size_t>((size_t)D * D * 2 + kTile * D * 2, (size_t)kTile * 2 * D * 2);
+  const size_t smem = area + 136 * 4 + 256 * 8 + 1024;
   cudaError_t e =
       cudaFuncSetAttribute(fmap_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
