@@ -45,34 +45,6 @@ constexpr int kST = 64;            // streamed rows per step
 constexpr int kThreads = 320;      // 8 epilogue warps, MMA issuer warp, loader warp
 constexpr int kIssuerWarp = 8, kLoaderWarp = 9;
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// 3-D bf16 tensor map over [planes][rows][cols], {64, box_rows, 1} boxes, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-              uint32_t box_rows) {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, planes};
-  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 struct GradArgs {
   // [0]: query side (X = q, Y = k), [1]: key side (X = k, Y = q)
@@ -526,10 +498,10 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
     ok = ok && make_rows_map(&a.tx[side], x[side], D, p.n, side ? p.H / p.G : p.H, p.B, 64, kRT, sw,
                              p.seq_major) &&
-         make_map(&a.tpx[side], px[side], 2 * D, p.n, U, kRT) &&
+         make_plane_map(&a.tpx[side], px[side], 2 * D, p.n, U, 64, kRT, sw) &&
          make_rows_map(&a.ty[side], x[1 - side], D, p.n, side ? p.H : p.H / p.G, p.B, 64, kST, sw,
                        p.seq_major) &&
-         make_map(&a.tpy[side], px[1 - side], 2 * D, p.n, U, kST);
+         make_plane_map(&a.tpy[side], px[1 - side], 2 * D, p.n, U, 64, kST, sw);
   }
   if (!ok) return cudaErrorInvalidValue;
   a.stats = reinterpret_cast<const float2*>(stats);

@@ -45,39 +45,6 @@ using namespace tc;
 
 constexpr int kTile = 128;
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// 3-D bf16 tensor map over [planes][rows][cols], {64, box_rows, 1} boxes, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-              uint32_t box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cols, rows, planes};
-  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
   return (uint32_t)(32 * (warp & 3)) << 16;
@@ -593,10 +560,12 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
     a.kv[i] = is_key[i] && p.G > 1;
     if (!make_rows_map(&a.tx[i], x[i], D, p.n, a.kv[i] ? p.H / p.G : p.H, p.B, 64, kTile,
                        CU_TENSOR_MAP_SWIZZLE_128B, p.seq_major) ||
-        !make_map(&a.tw[i], W, D, D, p.H, D))
+        !make_plane_map(&a.tw[i], W, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     a.phi[i] = reinterpret_cast<__nv_bfloat16*>(phi[i]);
-    if (phi[i] && !make_map(&a.tphi[i], phi[i], 2 * D, p.n, U, kTile)) return cudaErrorInvalidValue;
+    if (phi[i] && !make_plane_map(&a.tphi[i], phi[i], 2 * D, p.n, U, 64, kTile,
+                                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
     a.off[i] = p.softmax ? off[i] : nullptr;
     a.bias[i] = is_key[i] && p.Wk ? p.bk : p.bq;
   }
@@ -648,7 +617,8 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major) &&
             make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
-            make_map(&a.tpq, phq, 2 * D, p.n, U, kTile) && make_map(&a.tpk, phk, 2 * D, p.n, U, kTile);
+            make_plane_map(&a.tpq, phq, 2 * D, p.n, U, 64, kTile, sw) &&
+            make_plane_map(&a.tpk, phk, 2 * D, p.n, U, 64, kTile, sw);
   if (!ok) return cudaErrorInvalidValue;
   a.loss_rows = loss_rows;
   a.partial = partial;

@@ -3,11 +3,13 @@
 // "The Hedgehog & the Porcupine" summary: section 2 (paper Eq. 2) defines
 //   y_i = phi(q_i) sum_{j<=i} phi(k_j)^T v_j / phi(q_i) sum_{j<=i} phi(k_j),
 // "Complexity Analysis" the running sums S = sum phi(k)^T v and z = sum phi(k);
-// the maps are "The Hedgehog MLP Feature Map" (Choices 1 and 3) and "The
-// Taylor Exponential as a Bridge Result".
+// the map is "The Hedgehog MLP Feature Map" (Choices 1 and 3).  This file holds
+// the planning, the scan and the generic output pass (d = 128, and d = 64 with
+// a separate key map); the shared-map d = 64 pass is tc_prefill2.cu, the
+// Taylor pass tc_taylor.cu, the state passes tc_state.cu.
 //
 // Evaluation order (per 128-token tile t of one (batch, head) sequence segment):
-//   H_Q = Q_t W, H_K = K_t W                          (tcgen05, Hedgehog only)
+//   H_Q = Q_t W, H_K = K_t W                          (tcgen05)
 //   phi(Q_t) -> TMEM (bf16 pairs, the A operand of the next MMAs)
 //   phi(K_t) -> shared memory (bf16, 128B-swizzled panels); z += colsum phi(K_t)
 //   S_bf16 <- S (TMEM fp32 state of the tokens before tile t)
@@ -46,12 +48,9 @@ constexpr int kTile = 128;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
-template <int KIND, int D>
-struct Cfg;
-
 // Hedgehog, d in {64, 128}: features [exp(h_0..h_{d-1}), exp(-h_0..-h_{d-1})].
 template <int D>
-struct Cfg<HH_FMAP_HEDGEHOG, D> {
+struct Cfg {
   static constexpr int DP = 2 * D;           // feature dim
   static constexpr int DPP = 2 * D;          // padded feature dim (rows of S)
   static constexpr int NMB = DP / 128;       // 128-feature M blocks of S
@@ -77,32 +76,9 @@ struct Cfg<HH_FMAP_HEDGEHOG, D> {
   static_assert(DP * D * 2 <= 2 * XT_BYTES, "S_bf16 must fit in the Q/K region");
 };
 
-// Taylor, d = 16: features [1, x, x_i x_j / sqrt2], 273 used, 288 stored.
-template <>
-struct Cfg<HH_FMAP_TAYLOR2, 16> {
-  static constexpr int D = 16;
-  static constexpr int DP = 288;             // padded feature dim used by the MMAs
-  static constexpr int DPP = 288;
-  static constexpr int NMB = 3;              // S rows as 3 blocks of 128 (384 >= 288)
-  static constexpr int PHK_PANELS = 6;       // 384 features; 288.. are zero
-  static constexpr int KSTEPS_F = DP / 16;   // 18
-  static constexpr uint32_t TM_S = 0;
-  static constexpr uint32_t TM_Y = 64;       // phi(Q): 144 columns of bf16 pairs
-  static constexpr uint32_t TM_X = 256;      // Sc -> O
-  static constexpr uint32_t TM_COLS = 512;
-  static constexpr uint32_t XT_BYTES = kTile * D * 2;     // 4 KB
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + XT_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + XT_BYTES;
-  static constexpr uint32_t OFF_SB = OFF_V + XT_BYTES;    // [288][16] bf16, 32B-swizzled
-  static constexpr uint32_t OFF_PHK = 24576;              // 1024-aligned, after SB (9 KB)
-  static constexpr uint32_t OFF_END = OFF_PHK + PHK_PANELS * 16384;
-  static constexpr uint32_t OFF_W = 0, OFF_WK = 0, W_BYTES = 0;
-};
-
-template <int KIND, int D>
+template <int D>
 struct Smem {
-  using C = Cfg<KIND, D>;
+  using C = Cfg<D>;
   static constexpr int ZN = 384;
   // scalars after the operand area
   static constexpr uint32_t OFF_Z = C::OFF_END;                  // float[ZN]
@@ -168,68 +144,19 @@ __device__ __forceinline__ void st_panel_chunk(uint32_t panel, int r, int chunk,
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
-// ---- Taylor feature construction with compile-time feature indices ----
-// feature f of [1, x, x_i x_j / sqrt2 (i-major)], zero past 1 + 16 + 256
-__device__ __forceinline__ float taylor_feature(int f, const float (&x)[16]) {
-  if (f == 0) return 1.f;
-  if (f <= 16) return x[f - 1];
-  if (f <= 272) return x[(f - 17) >> 4] * x[(f - 17) & 15] * kInvSqrt2;
-  return 0.f;
-}
-
-// 32 features starting at FB as 16 bf16 pairs
-template <int FB>
-__device__ __forceinline__ void taylor_chunk(const float (&x)[16], uint32_t (&w)[16]) {
-#pragma unroll
-  for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(taylor_feature(FB + j, x), taylor_feature(FB + j + 1, x));
-}
-
-// phi(q) chunk into TMEM (packed column FB/2), adding its part of phi(q) . z
-template <int FB>
-__device__ __forceinline__ void taylor_q_chunk(const float (&x)[16], const float* z, uint32_t taddr,
-                                               float& dq) {
-  uint32_t w[16];
-  taylor_chunk<FB>(x, w);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) dq += bf16_lo(w[j]) * z[FB + 2 * j] + bf16_hi(w[j]) * z[FB + 2 * j + 1];
-  tmem_st16(taddr + FB / 2, w);
-}
-
-// phi(k) chunk into the swizzled panels, column sums of the warp into zp[FB + lane]
-template <int FB>
-__device__ __forceinline__ void taylor_k_chunk(const float (&x)[16], bool valid, uint32_t phk,
-                                               int row, float* zp, int lane) {
-  uint32_t w[16];
-  taylor_chunk<FB>(x, w);
-  float e[32];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (!valid) w[j] = 0u;
-    e[2 * j] = bf16_lo(w[j]);
-    e[2 * j + 1] = bf16_hi(w[j]);
-  }
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4)
-    st_shared_v4(phk + (FB / 64) * 16384 + sw128_chunk(row, (FB % 64) / 8 + q4), w[4 * q4],
-                 w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-  warp_transpose_sum(e, lane);
-  zp[FB + lane] = e[0];
-}
-
-
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 // Hedgehog d = 64 needs 256 TMEM columns and ~108 KB of shared memory, so two
 // CTAs share an SM (one's MMAs overlap the other's epilogues).
-template <int KIND, int D>
-constexpr int min_blocks() { return (KIND == HH_FMAP_HEDGEHOG && D == 64) ? 2 : 1; }
+template <int D>
+constexpr int min_blocks() { return D == 64 ? 2 : 1; }
 
-template <int KIND, int D>
-__global__ void __launch_bounds__(kThreads, min_blocks<KIND, D>())
+template <int D>
+__global__ void __launch_bounds__(kThreads, min_blocks<D>())
 prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
-  using C = Cfg<KIND, D>;
-  using SM = Smem<KIND, D>;
+  using C = Cfg<D>;
+  using SM = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -278,27 +205,19 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     const int r0 = t * kTile;
     uint32_t bytes = C::XT_BYTES * 3;
     mbar_expect_tx(bar_load, bytes);
-    if (KIND == HH_FMAP_HEDGEHOG) {
-      for (int i = 0; i < D / 64; ++i) {
-        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, ub, uh, A.seq);
-        tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, ub, kh, A.seq);
-        tma_load_rows(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, ub, kh, A.seq);
-      }
-    } else {
-      tma_load_rows(sb + C::OFF_Q, &A.tq, bar_load, 0, r0, ub, uh, A.seq);
-      tma_load_rows(sb + C::OFF_K, &A.tk, bar_load, 0, r0, ub, kh, A.seq);
-      tma_load_rows(sb + C::OFF_V, &A.tv, bar_load, 0, r0, ub, kh, A.seq);
+    for (int i = 0; i < D / 64; ++i) {
+      tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_load, 64 * i, r0, ub, uh, A.seq);
+      tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_load, 64 * i, r0, ub, kh, A.seq);
+      tma_load_rows(sb + C::OFF_V + i * 16384, &A.tv, bar_load, 64 * i, r0, ub, kh, A.seq);
     }
   };
   __syncthreads();  // barriers initialised before the first copy is issued
   if (tid == 0) {
-    if (KIND == HH_FMAP_HEDGEHOG) {
-      const int nmaps = A.sep_wk ? 2 : 1;
-      mbar_expect_tx(bar_w, C::W_BYTES * nmaps);
-      for (int i = 0; i < D / 64; ++i) {
-        tma_load_3d(sb + C::OFF_W + i * (D * 128), &A.twq, bar_w, 64 * i, 0, h);
-        if (A.sep_wk) tma_load_3d(sb + C::OFF_WK + i * (D * 128), &A.twk, bar_w, 64 * i, 0, h);
-      }
+    const int nmaps = A.sep_wk ? 2 : 1;
+    mbar_expect_tx(bar_w, C::W_BYTES * nmaps);
+    for (int i = 0; i < D / 64; ++i) {
+      tma_load_3d(sb + C::OFF_W + i * (D * 128), &A.twq, bar_w, 64 * i, 0, h);
+      if (A.sep_wk) tma_load_3d(sb + C::OFF_WK + i * (D * 128), &A.twk, bar_w, 64 * i, 0, h);
     }
     issue_loads(t_begin);
   }
@@ -306,11 +225,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
     tmem_relinquish();
   }
-  if (KIND == HH_FMAP_HEDGEHOG) {
-    for (int i = tid; i < D; i += kThreads) {
-      bq_s[i] = A.bq ? A.bq[(size_t)h * D + i] : 0.f;
-      bk_s[i] = A.bk ? A.bk[(size_t)h * D + i] : 0.f;
-    }
+  for (int i = tid; i < D; i += kThreads) {
+    bq_s[i] = A.bq ? A.bq[(size_t)h * D + i] : 0.f;
+    bk_s[i] = A.bk ? A.bk[(size_t)h * D + i] : 0.f;
   }
   const size_t seg_elems = (size_t)C::DPP * D + C::DPP;
   // the state before this segment: the scanned prefix, the initial state
@@ -320,11 +237,6 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   // initial z: the state of the tokens before this segment
   for (int f = tid; f < SM::ZN; f += kThreads)
     z_s[f] = (prefix && f < C::DPP) ? __ldcg(prefix + (size_t)C::DPP * D + f) : 0.f;
-  if (KIND == HH_FMAP_TAYLOR2) {
-    // zero the phi(K) panels once: features >= 288 stay zero for the whole run
-    for (uint32_t i = tid * 16; i < C::PHK_PANELS * 16384u; i += kThreads * 16)
-      st_shared_v4(sb + C::OFF_PHK + i, 0, 0, 0, 0);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -375,52 +287,45 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   constexpr uint32_t IDESC_QS = idesc_bf16(128, D, 0, 1);      // phiQ[tmem] * S_bf16[MN]
   // V as an MN-major B operand (rows = tokens = K, columns = d = N)
   auto v_desc = [&](int ks) -> uint64_t {
-    if (KIND == HH_FMAP_HEDGEHOG)
-      return smem_desc(sb + C::OFF_V + ks * 2048, kTile * 128, 1024, 2);
-    return smem_desc(sb + C::OFF_V + ks * 512, 16, 256, 6);
+    return smem_desc(sb + C::OFF_V + ks * 2048, kTile * 128, 1024, 2);
   };
-  const uint32_t w_key_off = (KIND == HH_FMAP_HEDGEHOG && A.sep_wk) ? C::OFF_WK : C::OFF_W;
+  const uint32_t w_key_off = A.sep_wk ? C::OFF_WK : C::OFF_W;
 
   for (int t = t_begin; t < t_end && !failed; ++t) {
     const int r0 = t * kTile;
     const int nvalid = (int)min((int64_t)kTile, A.n - r0);
 
     // ================= group 1: H = X W (Hedgehog) =================
-    if (KIND == HH_FMAP_HEDGEHOG) {
-      if (tid == 0) {
-        bool ok = mbar_wait(bar_load, ph_load, wp);
-        if (t == t_begin) ok = ok && mbar_wait(bar_w, ph_w, wp);
-        tc_fence_after();
-        if (ok) {
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
-            const uint64_t bq = smem_desc(sb + C::OFF_W + ks * 2048, D * 128, 1024, 2);
-            const uint64_t bk = smem_desc(sb + w_key_off + ks * 2048, D * 128, 1024, 2);
-            mma_ss(tmem + C::TM_Y, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2), bq, IDESC_H,
-                   ks > 0);
-            mma_ss(tmem + C::TM_X, smem_desc(sb + C::OFF_K + koff, 16, 1024, 2), bk, IDESC_H,
-                   ks > 0);
-          }
-          mma_commit(bar_mma);
-        } else {
-          failed = true;
-        }
-      }
-      ph_load ^= 1;
-      if (t == t_begin) ph_w ^= 1;
-      if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
-      ph_mma ^= 1;
+    if (tid == 0) {
+      bool ok = mbar_wait(bar_load, ph_load, wp);
+      if (t == t_begin) ok = ok && mbar_wait(bar_w, ph_w, wp);
       tc_fence_after();
-    } else {
-      if (!mbar_wait(bar_load, ph_load, wp)) failed = true;
-      ph_load ^= 1;
+      if (ok) {
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
+          const uint64_t bq = smem_desc(sb + C::OFF_W + ks * 2048, D * 128, 1024, 2);
+          const uint64_t bk = smem_desc(sb + w_key_off + ks * 2048, D * 128, 1024, 2);
+          mma_ss(tmem + C::TM_Y, smem_desc(sb + C::OFF_Q + koff, 16, 1024, 2), bq, IDESC_H,
+                 ks > 0);
+          mma_ss(tmem + C::TM_X, smem_desc(sb + C::OFF_K + koff, 16, 1024, 2), bk, IDESC_H,
+                 ks > 0);
+        }
+        mma_commit(bar_mma);
+      } else {
+        failed = true;
+      }
     }
+    ph_load ^= 1;
+    if (t == t_begin) ph_w ^= 1;
+    if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
+    ph_mma ^= 1;
+    tc_fence_after();
     if (__syncthreads_or(failed)) { failed = true; break; }
 
     // ================= epilogue 1: features, S_bf16, z =================
     // softmax map: phi = [exp(h - c+); exp(-h - c-)] with this row's offsets
     float2 oq = make_float2(0.f, 0.f), ok_ = make_float2(0.f, 0.f);
-    if (KIND == HH_FMAP_HEDGEHOG && A.offq && row < nvalid) {
+    if (A.offq && row < nvalid) {
       const size_t r = (size_t)unit * A.NT * kTile + (size_t)r0 + row;
       oq = A.offq[r];
       ok_ = A.offk[r];
@@ -428,60 +333,38 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     // -- phi(Q) into TMEM, denominator part phi(q) . z_before
     {
       float dq = 0.f;
-      if (KIND == HH_FMAP_HEDGEHOG) {
-        constexpr int HC = D / 2;  // H columns per warp half
-        uint32_t hv[HC];
+      constexpr int HC = D / 2;  // H columns per warp half
+      uint32_t hv[HC];
 #pragma unroll
-        for (int c = 0; c < HC; c += 32)
-          tmem_ld32(tmem + lane_base(warp) + C::TM_Y + half * HC + c,
-                    *reinterpret_cast<uint32_t(*)[32]>(&hv[c]));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncthreads();  // every warp holds its H_Q columns before any overwrite
-        tc_fence_after();
-        uint32_t pp[HC / 2], pn[HC / 2];
+      for (int c = 0; c < HC; c += 32)
+        tmem_ld32(tmem + lane_base(warp) + C::TM_Y + half * HC + c,
+                  *reinterpret_cast<uint32_t(*)[32]>(&hv[c]));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncthreads();  // every warp holds its H_Q columns before any overwrite
+      tc_fence_after();
+      uint32_t pp[HC / 2], pn[HC / 2];
 #pragma unroll
-        for (int j = 0; j < HC; j += 2) {
-          const int l = half * HC + j;
-          const float h0 = __uint_as_float(hv[j]) + bq_s[l];
-          const float h1 = __uint_as_float(hv[j + 1]) + bq_s[l + 1];
-          const uint32_t p = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -oq.x)),
-                                       ex2_approx(fmaf(h1, kLog2e, -oq.x)));
-          const uint32_t m = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -oq.y)),
-                                       ex2_approx(fmaf(-h1, kLog2e, -oq.y)));
-          pp[j / 2] = p;
-          pn[j / 2] = m;
-          dq += bf16_lo(p) * z_s[l] + bf16_hi(p) * z_s[l + 1] + bf16_lo(m) * z_s[D + l] +
-                bf16_hi(m) * z_s[D + l + 1];
-        }
-        // feature f -> packed column f/2: positive block at half*HC/2, negative at D/2 + half*HC/2
+      for (int j = 0; j < HC; j += 2) {
+        const int l = half * HC + j;
+        const float h0 = __uint_as_float(hv[j]) + bq_s[l];
+        const float h1 = __uint_as_float(hv[j + 1]) + bq_s[l + 1];
+        const uint32_t p = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -oq.x)),
+                                     ex2_approx(fmaf(h1, kLog2e, -oq.x)));
+        const uint32_t m = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -oq.y)),
+                                     ex2_approx(fmaf(-h1, kLog2e, -oq.y)));
+        pp[j / 2] = p;
+        pn[j / 2] = m;
+        dq += bf16_lo(p) * z_s[l] + bf16_hi(p) * z_s[l + 1] + bf16_lo(m) * z_s[D + l] +
+              bf16_hi(m) * z_s[D + l + 1];
+      }
+      // feature f -> packed column f/2: positive block at half*HC/2, negative at D/2 + half*HC/2
 #pragma unroll
-        for (int c = 0; c < HC / 2; c += 16) {
-          tmem_st16(tmem + lane_base(warp) + C::TM_Y + half * (HC / 2) + c,
-                    *reinterpret_cast<const uint32_t(*)[16]>(&pp[c]));
-          tmem_st16(tmem + lane_base(warp) + C::TM_Y + D / 2 + half * (HC / 2) + c,
-                    *reinterpret_cast<const uint32_t(*)[16]>(&pn[c]));
-        }
-      } else {
-        // Taylor: features of row `row` from the q tile (no swizzle, 32 B per row)
-        const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_Q) + row * 16;
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(qrow[i]);
-        // half 0 builds features [0, 160) = packed columns [0, 80); half 1 [160, 288)
-        const uint32_t ty = tmem + lane_base(warp) + C::TM_Y;
-        if (half == 0) {
-          taylor_q_chunk<0>(x, z_s, ty, dq);
-          taylor_q_chunk<32>(x, z_s, ty, dq);
-          taylor_q_chunk<64>(x, z_s, ty, dq);
-          taylor_q_chunk<96>(x, z_s, ty, dq);
-          taylor_q_chunk<128>(x, z_s, ty, dq);
-        } else {
-          taylor_q_chunk<160>(x, z_s, ty, dq);
-          taylor_q_chunk<192>(x, z_s, ty, dq);
-          taylor_q_chunk<224>(x, z_s, ty, dq);
-          taylor_q_chunk<256>(x, z_s, ty, dq);
-        }
+      for (int c = 0; c < HC / 2; c += 16) {
+        tmem_st16(tmem + lane_base(warp) + C::TM_Y + half * (HC / 2) + c,
+                  *reinterpret_cast<const uint32_t(*)[16]>(&pp[c]));
+        tmem_st16(tmem + lane_base(warp) + C::TM_Y + D / 2 + half * (HC / 2) + c,
+                  *reinterpret_cast<const uint32_t(*)[16]>(&pn[c]));
       }
       dq_s[half * 128 + row] = dq;
     }
@@ -489,109 +372,67 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     // -- phi(K) into shared memory panels, column sums into zp
     {
       const bool valid = row < nvalid;
-      if (KIND == HH_FMAP_HEDGEHOG) {
-        constexpr int HC = D / 2;
+      constexpr int HC = D / 2;
 #pragma unroll
-        for (int c = 0; c < HC; c += 32) {
-          uint32_t hv[32];
-          tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, hv);
-          tmem_ld_wait();
-          float ep[32], en[32];
-          uint32_t wp_[16], wn_[16];
+      for (int c = 0; c < HC; c += 32) {
+        uint32_t hv[32];
+        tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, hv);
+        tmem_ld_wait();
+        float ep[32], en[32];
+        uint32_t wp_[16], wn_[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int l = half * HC + c + j;
-            const float h0 = __uint_as_float(hv[j]) + bk_s[l];
-            const float h1 = __uint_as_float(hv[j + 1]) + bk_s[l + 1];
-            uint32_t p = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -ok_.x)),
-                                   ex2_approx(fmaf(h1, kLog2e, -ok_.x)));
-            uint32_t m = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -ok_.y)),
-                                   ex2_approx(fmaf(-h1, kLog2e, -ok_.y)));
-            if (!valid) p = m = 0u;
-            wp_[j / 2] = p;
-            wn_[j / 2] = m;
-            ep[j] = bf16_lo(p); ep[j + 1] = bf16_hi(p);
-            en[j] = bf16_lo(m); en[j + 1] = bf16_hi(m);
-          }
-          const int fpos = half * HC + c;          // first positive feature of this chunk
-          const int fneg = D + half * HC + c;      // first negative feature
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            st_panel_chunk(sb + C::OFF_PHK + (fpos / 64) * 16384, row, (fpos % 64) / 8 + q4,
-                           wp_[4 * q4], wp_[4 * q4 + 1], wp_[4 * q4 + 2], wp_[4 * q4 + 3]);
-            st_panel_chunk(sb + C::OFF_PHK + (fneg / 64) * 16384, row, (fneg % 64) / 8 + q4,
-                           wn_[4 * q4], wn_[4 * q4 + 1], wn_[4 * q4 + 2], wn_[4 * q4 + 3]);
-          }
-          warp_transpose_sum(ep, lane);
-          warp_transpose_sum(en, lane);
-          zp_s[g * SM::ZN + fpos + lane] = ep[0];
-          zp_s[g * SM::ZN + fneg + lane] = en[0];
+        for (int j = 0; j < 32; j += 2) {
+          const int l = half * HC + c + j;
+          const float h0 = __uint_as_float(hv[j]) + bk_s[l];
+          const float h1 = __uint_as_float(hv[j + 1]) + bk_s[l + 1];
+          uint32_t p = pack_bf16(ex2_approx(fmaf(h0, kLog2e, -ok_.x)),
+                                 ex2_approx(fmaf(h1, kLog2e, -ok_.x)));
+          uint32_t m = pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -ok_.y)),
+                                 ex2_approx(fmaf(-h1, kLog2e, -ok_.y)));
+          if (!valid) p = m = 0u;
+          wp_[j / 2] = p;
+          wn_[j / 2] = m;
+          ep[j] = bf16_lo(p); ep[j + 1] = bf16_hi(p);
+          en[j] = bf16_lo(m); en[j + 1] = bf16_hi(m);
         }
-      } else {
-        const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_K) + row * 16;
-        float x[16];
+        const int fpos = half * HC + c;          // first positive feature of this chunk
+        const int fneg = D + half * HC + c;      // first negative feature
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(krow[i]);
-        const uint32_t phk = sb + C::OFF_PHK;
-        float* zp = zp_s + g * SM::ZN;
-        if (half == 0) {
-          taylor_k_chunk<0>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<32>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<64>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<96>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<128>(x, valid, phk, row, zp, lane);
-        } else {
-          taylor_k_chunk<160>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<192>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<224>(x, valid, phk, row, zp, lane);
-          taylor_k_chunk<256>(x, valid, phk, row, zp, lane);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          st_panel_chunk(sb + C::OFF_PHK + (fpos / 64) * 16384, row, (fpos % 64) / 8 + q4,
+                         wp_[4 * q4], wp_[4 * q4 + 1], wp_[4 * q4 + 2], wp_[4 * q4 + 3]);
+          st_panel_chunk(sb + C::OFF_PHK + (fneg / 64) * 16384, row, (fneg % 64) / 8 + q4,
+                         wn_[4 * q4], wn_[4 * q4 + 1], wn_[4 * q4 + 2], wn_[4 * q4 + 3]);
         }
+        warp_transpose_sum(ep, lane);
+        warp_transpose_sum(en, lane);
+        zp_s[g * SM::ZN + fpos + lane] = ep[0];
+        zp_s[g * SM::ZN + fneg + lane] = en[0];
       }
     }
 
     // -- S_bf16 <- S (state before this tile), the B operand of phi(Q) S
     {
-      if (KIND == HH_FMAP_HEDGEHOG) {
-        // S_bf16 panel: [DP rows][D cols] as D/64 column blocks of [DP rows x 128 B]
-        constexpr int CPW = (C::NMB == 2) ? D : D / 2;   // columns handled by this warp
-        const int mb = (C::NMB == 2) ? half : 0;
-        const int cbase = (C::NMB == 2) ? 0 : half * (D / 2);
-        const int f = mb * 128 + row;
+      // S_bf16 panel: [DP rows][D cols] as D/64 column blocks of [DP rows x 128 B]
+      constexpr int CPW = (C::NMB == 2) ? D : D / 2;   // columns handled by this warp
+      const int mb = (C::NMB == 2) ? half : 0;
+      const int cbase = (C::NMB == 2) ? 0 : half * (D / 2);
+      const int f = mb * 128 + row;
 #pragma unroll
-        for (int c = 0; c < CPW; c += 32) {
-          uint32_t sv[32];
-          tmem_ld32(tmem + lane_base(warp) + C::TM_S + mb * D + cbase + c, sv);
-          tmem_ld_wait();
-          const int col = cbase + c;
-          const uint32_t panel = sb + C::OFF_SB + (col / 64) * (C::DP * 128);
+      for (int c = 0; c < CPW; c += 32) {
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base(warp) + C::TM_S + mb * D + cbase + c, sv);
+        tmem_ld_wait();
+        const int col = cbase + c;
+        const uint32_t panel = sb + C::OFF_SB + (col / 64) * (C::DP * 128);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int j = 8 * q4;
-            st_panel_chunk(panel, f, (col % 64) / 8 + q4,
-                           pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
-                           pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
-                           pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
-                           pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
-          }
-        }
-      } else {
-        // Taylor: S_bf16 [288 rows][16 cols] 32B-swizzled (16B chunk ^= bit 2 of the row)
-        for (int mb = half; mb < C::NMB; mb += 2) {
-          const int f = mb * 128 + row;
-          uint32_t sv[16];
-          tmem_ld16(tmem + lane_base(warp) + C::TM_S + mb * D, sv);
-          tmem_ld_wait();
-          if (f < C::DP) {
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-              const int j = 8 * ch;
-              const uint32_t addr = sb + C::OFF_SB + f * 32 + ((ch ^ ((f >> 2) & 1)) << 4);
-              st_shared_v4(addr, pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
-                           pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
-                           pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
-                           pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
-            }
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = 8 * q4;
+          st_panel_chunk(panel, f, (col % 64) / 8 + q4,
+                         pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                         pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
+                         pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
+                         pack_bf16(__uint_as_float(sv[j + 6]), __uint_as_float(sv[j + 7])));
         }
       }
     }
@@ -661,11 +502,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
                IDESC_PV, ks > 0);
       }
       for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
-        uint64_t bdesc;
-        if (KIND == HH_FMAP_HEDGEHOG)
-          bdesc = smem_desc(sb + C::OFF_SB + ks * 2048, C::DP * 128, 1024, 2);
-        else
-          bdesc = smem_desc(sb + C::OFF_SB + ks * 512, 16, 256, 6);
+        const uint64_t bdesc = smem_desc(sb + C::OFF_SB + ks * 2048, C::DP * 128, 1024, 2);
         mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8, bdesc, IDESC_QS, 1);
       }
       mma_commit(bar_mma);
@@ -682,44 +519,23 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
       const bool valid = row < nvalid;
       __nv_bfloat16* yrow =
           reinterpret_cast<__nv_bfloat16*>(A.y) + (size_t)row_of(ub, uh, r0 + row, A.H, A.n, A.seq) * D;
-      if (KIND == HH_FMAP_HEDGEHOG) {
-        constexpr int HC = D / 2;
+      constexpr int HC = D / 2;
 #pragma unroll
-        for (int c = 0; c < HC; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, ov);
-          tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + half * HC + c);
+      for (int c = 0; c < HC; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, ov);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + half * HC + c);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int j = 8 * q4;
-              uint4 v4;
-              v4.x = pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-              v4.y = pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-              v4.z = pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-              v4.w = pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-              dst[q4] = v4;
-            }
-          }
-        }
-      } else {
-        if (half == 0) {
-          uint32_t ov[16];
-          tmem_ld16(tmem + lane_base(warp) + C::TM_X, ov);
-          tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow);
-#pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4) {
-              const int j = 8 * q4;
-              uint4 v4;
-              v4.x = pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-              v4.y = pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-              v4.z = pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-              v4.w = pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-              dst[q4] = v4;
-            }
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int j = 8 * q4;
+            uint4 v4;
+            v4.x = pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+            v4.y = pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+            v4.z = pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+            v4.w = pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+            dst[q4] = v4;
           }
         }
       }
@@ -825,43 +641,7 @@ __global__ void init_state_kernel(const float* __restrict__ S0, const float* __r
 // host side
 // ---------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// 3-D bf16 tensor map over [planes][rows][cols] with a {box_cols, box_rows, 1} box.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-                     uint64_t planes, uint32_t box_cols, uint32_t box_rows,
-                     CUtensorMapSwizzle swz) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cols, rows, planes};
-  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {box_cols, box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int KIND, int D>
-static size_t smem_bytes() { return Smem<KIND, D>::ALLOC; }
 
 TcPlan plan_prefill_tc(const Problem& p) {
   TcPlan pl;
@@ -892,51 +672,14 @@ TcPlan plan_prefill_tc(const Problem& p) {
   return pl;
 }
 
+// Initial state (continuation), segment-state pass and scan, then the output
+// pass of the map: the Taylor and the shared-map d = 64 passes have kernels of
+// their own, the rest (d = 128, separate key maps) runs prefill_tc_kernel.
 template <int KIND, int D>
 static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q, const void* k,
                                const void* v, void* y, float* S_out, float* z_out, void* ws,
                                int* dev_status, cudaStream_t s) {
-  PrefillArgs a;
-  memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
-  bool ok = true;
-  if (KIND == HH_FMAP_HEDGEHOG) {
-    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-    ok &= make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major);
-    ok &= make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major);
-    ok &= make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major);
-    ok &= make_map(&a.twq, p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= make_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    ok &= make_rows_map(&a.tq, q, 16, p.n, p.H, p.B, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        p.seq_major);
-    ok &= make_rows_map(&a.tk, k, 16, p.n, p.H / p.G, p.B, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        p.seq_major);
-    ok &= make_rows_map(&a.tv, v, 16, p.n, p.H / p.G, p.B, 16, kTile, CU_TENSOR_MAP_SWIZZLE_32B,
-                        p.seq_major);
-  }
-  if (!ok) return cudaErrorInvalidValue;
-  a.y = y;
-  a.ws = reinterpret_cast<float*>(ws);
-  a.S_out = S_out;
-  a.z_out = z_out;
-  a.bq = p.bq;
-  a.bk = p.Wk ? p.bk : p.bq;
-  a.offq = p.offq;
-  a.offk = p.offk;
-  if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
-  a.dev_status = dev_status;
-  a.soft_ns = wait_soft_limit_ns();
-  a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
-  a.n = p.n;
-  a.H = p.H;
-  a.P = pl.P;
-  a.L = pl.L;
-  a.NT = pl.NT;
-  a.sep_wk = p.Wk ? 1 : 0;
-  a.G = p.G;
-  a.seq = p.seq_major;
-  const size_t smem = smem_bytes<KIND, D>();
   float* init = nullptr;
   if (p.S0) {
     if (!p.has_init || !p.z0) return cudaErrorInvalidValue;
@@ -949,7 +692,6 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  a.init = init;
   if (pl.P > 1) {
     cudaError_t e = launch_state_tc(p, pl, k, v, ws, dev_status, s);
     if (e != cudaSuccess) return e;
@@ -962,12 +704,43 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
-  if (KIND == HH_FMAP_HEDGEHOG && D == 64 && !p.Wk)
-    return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
   if constexpr (KIND == HH_FMAP_TAYLOR2) {
     return launch_prefill_out_taylor(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
   } else {
-    auto kern = prefill_tc_kernel<KIND, D>;
+    if (D == 64 && !p.Wk)
+      return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
+    PrefillArgs a;
+    memset(&a, 0, sizeof(a));
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major) &&
+              make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
+              make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
+              make_plane_map(&a.twq, p.Wq, D, D, p.H, 64, D, sw) &&
+              make_plane_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, sw);
+    if (!ok) return cudaErrorInvalidValue;
+    a.y = y;
+    a.ws = reinterpret_cast<float*>(ws);
+    a.init = init;
+    a.S_out = S_out;
+    a.z_out = z_out;
+    a.bq = p.bq;
+    a.bk = p.Wk ? p.bk : p.bq;
+    a.offq = p.offq;
+    a.offk = p.offk;
+    if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
+    a.dev_status = dev_status;
+    a.soft_ns = wait_soft_limit_ns();
+    a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+    a.n = p.n;
+    a.H = p.H;
+    a.P = pl.P;
+    a.L = pl.L;
+    a.NT = pl.NT;
+    a.sep_wk = p.Wk ? 1 : 0;
+    a.G = p.G;
+    a.seq = p.seq_major;
+    const size_t smem = Smem<D>::ALLOC;
+    auto kern = prefill_tc_kernel<D>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

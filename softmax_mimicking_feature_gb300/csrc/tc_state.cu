@@ -8,16 +8,19 @@
 // degree-2 Taylor map ("The Taylor Exponential as a Bridge Result").  The
 // output pass starts segment s from the inclusive scan of segments < s.
 //
-// One CTA per segment.  Warp 8 (one lane) issues TMA loads and MMAs; warps
-// 0-7 build phi(K) (warp w owns TMEM lanes 32*(w%4).. and column half w/4).
+// Three kernels, one CTA per segment each: state_tc_kernel (Hedgehog,
+// d = 64), state_t128_kernel (Hedgehog, d = 128, phi(K) kept in TMEM) and
+// state_taylor_kernel (Taylor, d = 16).
+//
+// state_tc_kernel: warp 8 (one lane) issues TMA loads and MMAs; warps 0-7
+// build phi(K) (warp w owns TMEM lanes 32*(w%4).. and column half w/4).
 // Per 128-token tile t:
-//   G1(t): H_K = K_t W into TMEM                          (Hedgehog)
+//   G1(t): H_K = K_t W into TMEM
 //   E1(t): H_K -> registers ("H read"), exponentials, then phi(K_t) ->
 //          128B-swizzled shared panels once G2(t-1) has consumed the old ones
 //   G2(t): S += phi(K_t)^T V_t,  z += phi(K_t)^T 1         (tcgen05)
 // G1(t+1) is issued as soon as E1(t) has read H_K, so it and G2(t) run
-// under the exponentials of the next tile.  K is double-buffered; V is
-// double-buffered where shared memory allows (single at d = 128).
+// under the exponentials of the next tile.  K and V are double-buffered.
 // Every mbarrier wait is bounded in time (tc_ptx.cuh).
 
 #include <math.h>
@@ -38,12 +41,9 @@ using namespace tc;
 constexpr int TILE = 128;
 constexpr int kThreads = 288;  // 8 feature warps + 1 issue warp
 
-template <int KIND, int D>
-struct SCfg;
-
 // Hedgehog, d in {64, 128}: 2d features, S rows as 128-feature M blocks.
 template <int D>
-struct SCfg<HH_FMAP_HEDGEHOG, D> {
+struct SCfg {
   static constexpr int DPP = 2 * D;
   static constexpr int NMB = 2 * D / 128;
   static constexpr int NV = D == 128 ? 1 : 2;                  // V stages
@@ -61,33 +61,14 @@ struct SCfg<HH_FMAP_HEDGEHOG, D> {
   static constexpr uint32_t OFF_END = OFF_PHK + (2 * D / 64) * 16384;
 };
 
-// Taylor, d = 16: 273 features stored as 288, panels cover 384 (tail zero).
-template <>
-struct SCfg<HH_FMAP_TAYLOR2, 16> {
-  static constexpr int DPP = 288;
-  static constexpr int NMB = 3;
-  static constexpr int NV = 2;
-  static constexpr uint32_t TM_S = 0;                          // 3 x [128 x 16]
-  static constexpr uint32_t TM_Z = 48;                         // 3 x [128 x 16]
-  static constexpr uint32_t TM_H = 0;                          // unused
-  static constexpr uint32_t TM_COLS = 128;
-  static constexpr uint32_t XT = TILE * 16 * 2;                // 4 KB
-  static constexpr uint32_t OFF_W = 0;                         // unused
-  static constexpr uint32_t OFF_ONES = 0;
-  static constexpr uint32_t OFF_K = 4096;
-  static constexpr uint32_t OFF_V = OFF_K + 2 * XT;            // 256-aligned for SW32
-  static constexpr uint32_t OFF_PHK = 24576;
-  static constexpr uint32_t OFF_END = OFF_PHK + 6 * 16384;
-};
-
 enum {
   SB_W = 0, SB_LDK = 1 /* 2 */, SB_LDV = 3 /* 2 */, SB_G1 = 5, SB_HREAD = 6, SB_E1 = 7,
   SB_G2 = 8, SB_COUNT = 9
 };
 
-template <int KIND, int D>
+template <int D>
 struct SSmem {
-  using C = SCfg<KIND, D>;
+  using C = SCfg<D>;
   static constexpr uint32_t OFF_B = C::OFF_END;                // bias float[128]
   static constexpr uint32_t OFF_BAR = OFF_B + 512;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * SB_COUNT; // tmem base, abort flag
@@ -112,28 +93,10 @@ __device__ __forceinline__ uint32_t lane_base(int warp) {
   return (uint32_t)(32 * (warp & 3)) << 16;
 }
 
-// Taylor feature f of [1, x, x_i x_j / sqrt2 (i-major)]; zero past 272.
-__device__ __forceinline__ float taylor_feature(int f, const float (&x)[16]) {
-  if (f == 0) return 1.f;
-  if (f <= 16) return x[f - 1];
-  if (f <= 272) return x[(f - 17) >> 4] * x[(f - 17) & 15] * kInvSqrt2;
-  return 0.f;
-}
-
-// 32 features from FB as 16 bf16 pairs into w[WB..WB+16)
-template <int FB, int WB, int NW>
-__device__ __forceinline__ void taylor_pack(const float (&x)[16], bool valid, uint32_t (&w)[NW]) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    w[WB + j] = valid ? pack_bf16(taylor_feature(FB + 2 * j, x), taylor_feature(FB + 2 * j + 1, x))
-                      : 0u;
-}
-
-template <int KIND, int D>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_constant__ StateArgs A) {
-  using C = SCfg<KIND, D>;
-  using SM = SSmem<KIND, D>;
-  constexpr bool HH = KIND == HH_FMAP_HEDGEHOG;
+  using C = SCfg<D>;
+  using SM = SSmem<D>;
   constexpr int NV = C::NV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -181,11 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
                     kh, A.seq);
   };
   if (warp == 8 && lane == 0 && nt > 0) {
-    if (HH) {
-      mbar_expect_tx(bar(SB_W), D * D * 2);
-      for (int x = 0; x < D / 64; ++x)
-        tma_load_3d(sb + C::OFF_W + x * (D * 128), &A.tw, bar(SB_W), 64 * x, 0, h);
-    }
+    mbar_expect_tx(bar(SB_W), D * D * 2);
+    for (int x = 0; x < D / 64; ++x)
+      tma_load_3d(sb + C::OFF_W + x * (D * 128), &A.tw, bar(SB_W), 64 * x, 0, h);
     load_k(0);
     load_v(0);
     if (nt > 1) {
@@ -197,16 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
     tmem_relinquish();
   }
-  if (HH)
-    for (int i = tid; i < D; i += kThreads) b_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
+  for (int i = tid; i < D; i += kThreads) b_s[i] = A.bias ? A.bias[(size_t)h * D + i] : 0.f;
   // ones operand of the z MMA ([128 tokens x 16] bf16)
   for (int i = tid; i < 4096 / 16; i += kThreads)
     st_shared_v4(sb + C::OFF_ONES + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-  if (!HH) {
-    // Taylor: features 288..383 of the panels stay zero for the whole run
-    for (uint32_t i = tid * 16; i < 6 * 16384u; i += kThreads * 16)
-      st_shared_v4(sb + C::OFF_PHK + i, 0, 0, 0, 0);
-  }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -245,14 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
           mma_ss(tmem + C::TM_H, dk + (ks / 4) * 1024 + (ks % 4) * 2, dw + ks * 128, ID_H, ks > 0);
         mma_commit(bar(SB_G1));
       };
-      bool ok = true;
-      if (HH) {
-        ok = mbar_wait_poll(bar(SB_W), 0, wp) && mbar_wait_poll(bar(SB_LDK), 0, wp);
-        tc_fence_after();
-        if (ok) g1(0);
-      }
+      bool ok = mbar_wait_poll(bar(SB_W), 0, wp) && mbar_wait_poll(bar(SB_LDK), 0, wp);
+      tc_fence_after();
+      if (ok) g1(0);
       for (int i = 0; i < nt && ok; ++i) {
-        if (HH && i + 1 < nt) {
+        if (i + 1 < nt) {
           // H_K is free once every feature warp has read H_K(i)
           ok = mbar_wait_poll(bar(SB_LDK + ((i + 1) & 1)), ((i + 1) >> 1) & 1, wp) &&
                mbar_wait_poll(bar(SB_HREAD), i & 1, wp);
@@ -266,18 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
         tc_fence_after();
         const uint32_t vb = sb + C::OFF_V + (i % NV) * C::XT;
         const uint64_t dphk = smem_desc(sb + C::OFF_PHK, 16384, 1024, 2);
-        const uint64_t dv = HH ? smem_desc(vb, TILE * 128, 1024, 2) : smem_desc(vb, 16, 256, 6);
+        const uint64_t dv = smem_desc(vb, TILE * 128, 1024, 2);
         const uint64_t dones = smem_desc(sb + C::OFF_ONES, 16, 256, 6);
 #pragma unroll
         for (int mb = 0; mb < C::NMB; ++mb)
 #pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks) {
             const uint64_t a = dphk + (2 * mb) * 1024 + ks * 128;
-            mma_ss(tmem + C::TM_S + mb * D, a, dv + ks * (HH ? 128 : 32), ID_SU, 1);
+            mma_ss(tmem + C::TM_S + mb * D, a, dv + ks * 128, ID_SU, 1);
             mma_ss(tmem + C::TM_Z + 16 * mb, a, dones + ks * 32, ID_Z, 1);
           }
         mma_commit(bar(SB_G2));
-        // K stage i&1: G1(i) (Hedgehog) or the feature warps (Taylor) are done with it
+        // K stage i&1: G1(i) is done with it
         if (i + 2 < nt) load_k(i + 2);
         if (NV == 2) {
           // V stage (i+1)&1 held V(i-1), consumed by G2(i-1) (E1(i) waited for it)
@@ -296,75 +248,41 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     const uint32_t phk = sb + C::OFF_PHK;
     for (int i = 0; i < nt; ++i) {
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
-      if constexpr (HH) {
-        constexpr int HC = D / 2;  // H columns of this warp's half
-        // softmax map: phi = [exp(h - c+); exp(-h - c-)], offsets in log2 units
-        float2 o = make_float2(0.f, 0.f);
-        if (A.off && valid)
-          o = A.off[(size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE + row];
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(SB_G1), i & 1, wp))) break;
-        tc_fence_after();
-        uint32_t hv[HC];
-        if constexpr (HC == 64) tmem_ld64(tmem + lane_base(warp) + C::TM_H + HC * c, hv);
-        else tmem_ld32(tmem + lane_base(warp) + C::TM_H + HC * c, hv);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(SB_HREAD));
-        uint32_t wpos[HC / 2], wneg[HC / 2];
+      constexpr int HC = D / 2;  // H columns of this warp's half
+      // softmax map: phi = [exp(h - c+); exp(-h - c-)], offsets in log2 units
+      float2 o = make_float2(0.f, 0.f);
+      if (A.off && valid)
+        o = A.off[(size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE + row];
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(SB_G1), i & 1, wp))) break;
+      tc_fence_after();
+      uint32_t hv[HC];
+      if constexpr (HC == 64) tmem_ld64(tmem + lane_base(warp) + C::TM_H + HC * c, hv);
+      else tmem_ld32(tmem + lane_base(warp) + C::TM_H + HC * c, hv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SB_HREAD));
+      uint32_t wpos[HC / 2], wneg[HC / 2];
 #pragma unroll
-        for (int j = 0; j < HC; j += 2) {
-          const float h0 = __uint_as_float(hv[j]) + b_s[HC * c + j];
-          const float h1 = __uint_as_float(hv[j + 1]) + b_s[HC * c + j + 1];
-          wpos[j / 2] = valid ? pack_bf16(ex2_approx(fmaf(h0, kLog2e, -o.x)),
-                                          ex2_approx(fmaf(h1, kLog2e, -o.x)))
-                              : 0u;
-          wneg[j / 2] = valid ? pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -o.y)),
-                                          ex2_approx(fmaf(-h1, kLog2e, -o.y)))
-                              : 0u;
-        }
-        // the panels are free once G2(i-1) has read them
-        if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(SB_G2), (i - 1) & 1, wp))) break;
+      for (int j = 0; j < HC; j += 2) {
+        const float h0 = __uint_as_float(hv[j]) + b_s[HC * c + j];
+        const float h1 = __uint_as_float(hv[j + 1]) + b_s[HC * c + j + 1];
+        wpos[j / 2] = valid ? pack_bf16(ex2_approx(fmaf(h0, kLog2e, -o.x)),
+                                        ex2_approx(fmaf(h1, kLog2e, -o.x)))
+                            : 0u;
+        wneg[j / 2] = valid ? pack_bf16(ex2_approx(fmaf(-h0, kLog2e, -o.y)),
+                                        ex2_approx(fmaf(-h1, kLog2e, -o.y)))
+                            : 0u;
+      }
+      // the panels are free once G2(i-1) has read them
+      if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(SB_G2), (i - 1) & 1, wp))) break;
 #pragma unroll
-        for (int q = 0; q < HC / 8; ++q) {
-          const int fp = HC * c + 8 * q;      // positive feature of this 16-byte chunk
-          const int fn = D + HC * c + 8 * q;  // its negative twin
-          st_shared_v4(phk + (fp / 64) * 16384 + sw128_chunk(row, (fp % 64) / 8), wpos[4 * q],
-                       wpos[4 * q + 1], wpos[4 * q + 2], wpos[4 * q + 3]);
-          st_shared_v4(phk + (fn / 64) * 16384 + sw128_chunk(row, (fn % 64) / 8), wneg[4 * q],
-                       wneg[4 * q + 1], wneg[4 * q + 2], wneg[4 * q + 3]);
-        }
-      } else {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(SB_LDK + (i & 1)), (i >> 1) & 1, wp))) break;
-        const __nv_bfloat16* krow =
-            reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_K + (i & 1) * C::XT) + row * 16;
-        float x[16];
-#pragma unroll
-        for (int k2 = 0; k2 < 16; ++k2) x[k2] = __bfloat162float(krow[k2]);
-        // half 0: features [0, 160), half 1: [160, 288)
-        uint32_t w[80];
-        if (c == 0) {
-          taylor_pack<0, 0>(x, valid, w);
-          taylor_pack<32, 16>(x, valid, w);
-          taylor_pack<64, 32>(x, valid, w);
-          taylor_pack<96, 48>(x, valid, w);
-          taylor_pack<128, 64>(x, valid, w);
-        } else {
-          taylor_pack<160, 0>(x, valid, w);
-          taylor_pack<192, 16>(x, valid, w);
-          taylor_pack<224, 32>(x, valid, w);
-          taylor_pack<256, 48>(x, valid, w);
-        }
-        if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(SB_G2), (i - 1) & 1, wp))) break;
-        const int f0 = c == 0 ? 0 : 160;
-        const int nq = c == 0 ? 20 : 16;   // 16-byte chunks (8 features each)
-#pragma unroll
-        for (int q = 0; q < 20; ++q) {
-          if (q < nq) {
-            const int f = f0 + 8 * q;
-            st_shared_v4(phk + (f / 64) * 16384 + sw128_chunk(row, (f % 64) / 8), w[4 * q],
-                         w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-          }
-        }
+      for (int q = 0; q < HC / 8; ++q) {
+        const int fp = HC * c + 8 * q;      // positive feature of this 16-byte chunk
+        const int fn = D + HC * c + 8 * q;  // its negative twin
+        st_shared_v4(phk + (fp / 64) * 16384 + sw128_chunk(row, (fp % 64) / 8), wpos[4 * q],
+                     wpos[4 * q + 1], wpos[4 * q + 2], wpos[4 * q + 3]);
+        st_shared_v4(phk + (fn / 64) * 16384 + sw128_chunk(row, (fn % 64) / 8), wneg[4 * q],
+                     wneg[4 * q + 1], wneg[4 * q + 2], wneg[4 * q + 3]);
       }
       fence_proxy_async();
       __syncwarp();
@@ -891,34 +809,6 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// 3-D bf16 tensor map over [planes][rows][cols] with a {box_cols, box_rows, 1} box.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-              uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, planes};
-  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {box_cols, box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int KIND, int D>
 cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const void* v, void* ws,
@@ -931,7 +821,7 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
     ok = make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, TILE, sw, p.seq_major) &&
          make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, TILE, sw, p.seq_major) &&
-         make_map(&a.tw, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
+         make_plane_map(&a.tw, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     ok = make_rows_map(&a.tk, k, 16, p.n, p.H / p.G, p.B, 16, TILE, CU_TENSOR_MAP_SWIZZLE_NONE,
                        p.seq_major) &&
@@ -970,11 +860,11 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
     return cudaGetLastError();
   }
   if constexpr (KIND == HH_FMAP_HEDGEHOG && D == 64) {
-    const size_t smem = SSmem<KIND, D>::ALLOC;
-    cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<KIND, D>,
+    const size_t smem = SSmem<D>::ALLOC;
+    cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    state_tc_kernel<KIND, D><<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
+    state_tc_kernel<D><<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
     return cudaGetLastError();
   }
   return cudaErrorInvalidValue;

@@ -1,4 +1,5 @@
-// Host-side tensor maps of the q, k, v (and y) tensors handed to the library.
+// Host-side tensor maps: the q, k, v tensors handed to the library (two
+// layouts) and the library's own [planes][rows][cols] buffers.
 //
 // The library takes two layouts of a [B] x [H] x [n] x [cols] tensor
 // (cols contiguous):
@@ -35,6 +36,22 @@ inline TmapEncodeFn tmap_encode_fn() {
       fn = reinterpret_cast<TmapEncodeFn>(p);
   }
   return fn;
+}
+
+// bf16 map over [planes][rows][cols] (library-owned buffers: weights,
+// features, states) with {box_cols, box_rows, 1} boxes.
+inline bool make_plane_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                           uint64_t planes, uint32_t box_cols, uint32_t box_rows,
+                           CUtensorMapSwizzle swz) {
+  TmapEncodeFn enc = tmap_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // bf16 map over heads x rows of a [B][H][n][cols] or [B][n][H][cols] tensor;
