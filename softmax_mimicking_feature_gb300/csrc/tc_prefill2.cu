@@ -10,7 +10,7 @@
 //   can stall while the tensor pipe is busy, so
 //   warp 9 (loader) issues the TMA loads of the next tiles on its own
 //     G1(t): H_Q = Q_t W, H_K = K_t W
-//     G2(t): Sc = phi(Q_t) phi(K_t)^T;  [S z] += phi(K_t)^T [V_t 1]
+//     G2(t): Sc = phi(Q_t) phi(K_t)^T (committed on its own);  [S z] += phi(K_t)^T [V_t 1]
 //     G3(t): [O den] = P_t [V_t e0] + phi(Q_t) [S_bf16(t) z2(t)]
 //   The normaliser rides along as extra columns of the same MMAs (N = 80):
 //   column 64 of the state is z; for the output, e0 = (1, 0, ...) gives the
@@ -23,11 +23,15 @@
 //          tokens before t)                                         (after G2(t-1))
 //          -- only then may G2(t) update S --
 //     E2 : P_t = bf16(tril(Sc)); blocks above the diagonal are zero
-//          without reading Sc, blocks below it need no mask         (after G2(t))
-//     E3 : y = O / den                                              (after G3(t))
-// Each tile owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (Q -> S_bf16,
-// K, V, phi(K) -> P, z2); the running state [S z] (fp32) stays in TMEM and
-// passes between the groups in tile order.  All mbarrier waits are bounded (tc_ptx.cuh).
+//          without reading Sc, blocks below it need no mask; built
+//          after the Sc MMAs, stored over phi(K) after all of G2(t)
+//     E3 : y = O / den, staged in the P panel (free once G3(t) has read it)
+//          and stored by TMA, one 32-row slab per warp pair       (after G3(t))
+// Each tile owns one slot of TMEM (H_Q/phi(Q), H_K/Sc/O) and smem (V, phi(K) ->
+// P -> y, S_bf16, z2); Q and K sit in a separate two-stage ring that is
+// refilled as soon as G1 has read it, so the loads of tile t+2 do not wait for
+// G3(t).  The running state [S z] (fp32) stays in TMEM and passes between the
+// groups in tile order.  All mbarrier waits are bounded (tc_ptx.cuh).
 
 #include <math.h>
 #include <string.h>
@@ -52,26 +56,35 @@ __host__ __device__ constexpr uint32_t TM_X(int s) { return 128 + 192 * s + 64; 
 
 // shared memory
 constexpr uint32_t OFF_W = 0;
-constexpr uint32_t SLOT_BASE = 8192, SLOT_BYTES = 98304;
-// per slot: Q (free once H = X W has run) -> S_bf16 (read by G3), K, V, phi(K) -> P,
-// z2 ([128 features x 64] panel whose first 16 columns extend S_bf16 to N = 80)
-constexpr uint32_t S_Q = 0, S_SB = 0, S_K = 16384, S_V = 32768, S_PHK = 49152, S_Z2 = 81920;
+constexpr uint32_t OFF_QK = 8192;                         // 2 stages of Q, K (16 KB each)
+__host__ __device__ constexpr uint32_t qk_off(int st) { return OFF_QK + st * 32768; }
+constexpr uint32_t SLOT_BASE = OFF_QK + 2 * 32768, SLOT_BYTES = 65536;
+// per slot: V, phi(K) -> P -> y (two panels), S_bf16 (read by G3)
+constexpr uint32_t S_V = 0, S_PHK = 16384, S_SB = 49152;
 __host__ __device__ constexpr uint32_t slot_off(int s) { return SLOT_BASE + s * SLOT_BYTES; }
-// e0: [128 x 64] panel, row r = (1, 0, ...), the extra N block of V
+// [128 x 64] SW128 panel holding three 16-column N blocks: logical columns
+// 0..15 are e0 (row r = (1, 0, ...), the extra N block of V), 16 + 16s.. are
+// z2 of slot s (row f = (z_hi, z_lo, 0, ...), the extra N block of S_bf16).
+// A descriptor reaches block j by a start address 32j bytes into the row; it
+// sits after the slots because the leading-byte offset field is unsigned.
 constexpr uint32_t OFF_E0 = SLOT_BASE + 2 * SLOT_BYTES;
 constexpr uint32_t OFF_BQ = OFF_E0 + 16384;               // float[64]: b * log2(e)
-constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 20 x u64
+constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 19 x u64 (20 reserved)
 constexpr uint32_t OFF_TM = OFF_BAR + 160;
 constexpr uint32_t SMEM_BYTES = OFF_TM + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// leading-byte offsets from the V and S_bf16 blocks to their e0 / z2 blocks:
+// positive and within the descriptor's 14-bit field (16-byte units)
+static_assert(OFF_E0 > slot_off(1) + S_SB && OFF_E0 + 64 - slot_off(0) - S_V < (16384u << 4),
+              "descriptor offsets");
 
 enum Bar {
-  B_W = 0, B_LDQK = 1, B_LDV = 3, B_G1 = 5, B_G2 = 7, B_G3 = 9, B_E1A = 11, B_E12 = 13, B_E3 = 15
+  B_W = 0, B_LDQK = 1, B_LDV = 3, B_G1 = 5, B_G2 = 7, B_G3 = 9, B_E1A = 11, B_E12 = 13, B_E3 = 15,
+  B_G2A = 17   // the score MMAs of G2 (Sc) alone
 };
 
 struct Args2 {
-  CUtensorMap tq, tk, tv, tw;
-  __nv_bfloat16* y;
+  CUtensorMap tq, tk, tv, tw, ty;   // ty: y rows, 32-row boxes
   const float* ws;   // [U][P-1][DP*D + DP] inclusive prefixes of segment states
   const float* init; // [U][DP*D + DP] initial state (continuation), same layout, or null
   float* S_out;
@@ -129,22 +142,24 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       mbar_init(bar(B_E1A + s), 8);
       mbar_init(bar(B_E12 + s), 8);
       mbar_init(bar(B_E3 + s), 8);
+      mbar_init(bar(B_G2A + s), 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&A.tq);
     prefetch_tmap(&A.tk);
     prefetch_tmap(&A.tv);
+    prefetch_tmap(&A.ty);
   }
   __syncthreads();
 
   auto load_qk = [&](int i) {
     const int s = i & 1;
     const int r0 = (t_begin + i) * TILE;
-    const uint32_t base = sb + slot_off(s);
+    const uint32_t base = sb + qk_off(s);
     mbar_expect_tx(bar(B_LDQK + s), 2 * 16384);
-    tma_load_rows(base + S_Q, &A.tq, bar(B_LDQK + s), 0, r0, ub, uh, A.seq);
-    tma_load_rows(base + S_K, &A.tk, bar(B_LDQK + s), 0, r0, ub, kh, A.seq);
+    tma_load_rows(base, &A.tq, bar(B_LDQK + s), 0, r0, ub, uh, A.seq);
+    tma_load_rows(base + 16384, &A.tk, bar(B_LDQK + s), 0, r0, ub, kh, A.seq);
   };
   auto load_v = [&](int i) {
     const int s = i & 1;
@@ -166,11 +181,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
   }
   for (int i = tid; i < D; i += kThreads)
     bq_s[i] = A.bias ? A.bias[(size_t)h * D + i] * kLog2e : 0.f;
-  for (int i = tid; i < 2 * 1024; i += kThreads) {   // z2 panels: zero (row chunks 1.. stay zero)
-    const int s2 = i >> 10, j = i & 1023;
-    st_shared_v4(sb + slot_off(s2) + S_Z2 + 16 * j, 0u, 0u, 0u, 0u);
-  }
-  for (int i = tid; i < 1024; i += kThreads) {       // e0: logical column 0 of every row = 1
+  for (int i = tid; i < 1024; i += kThreads) {
+    // e0 block: logical column 0 of every row = 1; z2 blocks: zero until E1
+    // writes columns (z_hi, z_lo) of their first chunk
     const int r = i >> 3, ch = i & 7;
     st_shared_v4(sb + OFF_E0 + sw128_chunk(r, ch), ch == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
@@ -228,51 +241,57 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       auto slot_desc = [&](int s2) {
         const uint32_t base = sb + slot_off(s2);
         SlotDesc d;
-        d.q = smem_desc(base + S_Q, 16, 1024, 2);         // K-major, 32 B per k-step
-        d.k = smem_desc(base + S_K, 16, 1024, 2);
+        d.q = smem_desc(sb + qk_off(s2), 16, 1024, 2);           // K-major, 32 B per k-step
+        d.k = smem_desc(sb + qk_off(s2) + 16384, 16, 1024, 2);
         d.pk = smem_desc(base + S_PHK, 16, 1024, 2);      // phi(K) / P as K-major operand
         d.pm = smem_desc(base + S_PHK, 16384, 1024, 2);   // phi(K)^T as MN-major operand
-        d.v = smem_desc(base + S_V, OFF_E0 - (slot_off(s2) + S_V), 1024, 2);  // 2048 B per k-step
-        d.sbf = smem_desc(base + S_SB, S_Z2 - S_SB, 1024, 2);
+        // MN-major, 2048 B per k-step; the second N block is e0 / z2 of this slot
+        d.v = smem_desc(base + S_V, OFF_E0 - (slot_off(s2) + S_V), 1024, 2);
+        d.sbf = smem_desc(base + S_SB, OFF_E0 + 32 * (1 + s2) - (slot_off(s2) + S_SB), 1024, 2);
         return d;
       };
       const SlotDesc sd0 = slot_desc(0), sd1 = slot_desc(1);
       const uint64_t dW = smem_desc(sb + OFF_W, D * 128, 1024, 2);
       // k-step offsets in 16-byte units: K-major inside 64-element panels, MN-major rows
       auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
+      // descriptors of a slot picked field by field (a reference to one of the
+      // two structs would put them in local memory)
       auto G1 = [&](int i) {
         const int s = i & 1;
-        const SlotDesc& d = s ? sd1 : sd0;
+        const uint64_t dq = s ? sd1.q : sd0.q, dk = s ? sd1.k : sd0.k;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          mma_ss(tmem + TM_Y(s), d.q + 2 * ks, dW + 128 * ks, ID_H, ks > 0);
-          mma_ss(tmem + TM_X(s), d.k + 2 * ks, dW + 128 * ks, ID_H, ks > 0);
+          mma_ss(tmem + TM_Y(s), dq + 2 * ks, dW + 128 * ks, ID_H, ks > 0);
+          mma_ss(tmem + TM_X(s), dk + 2 * ks, dW + 128 * ks, ID_H, ks > 0);
         }
         mma_commit(bar(B_G1 + s));
       };
       auto G2 = [&](int i) {
         const int s = i & 1;
-        const SlotDesc& d = s ? sd1 : sd0;
+        const uint64_t pk = s ? sd1.pk : sd0.pk, pm = s ? sd1.pm : sd0.pm;
+        const uint64_t dv = s ? sd1.v : sd0.v;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks)
-          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.pk + kmaj(ks), ID_SC, ks > 0);
+          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, pk + kmaj(ks), ID_SC, ks > 0);
+        mma_commit(bar(B_G2A + s));   // E2 may read Sc while the state update runs
 #pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks)
-          mma_ss(tmem + TM_S, d.pm + 128 * ks, d.v + 128 * ks, ID_SU, 1);
+          mma_ss(tmem + TM_S, pm + 128 * ks, dv + 128 * ks, ID_SU, 1);
         mma_commit(bar(B_G2 + s));
       };
       auto G3 = [&](int i) {
         const int s = i & 1;
-        const SlotDesc& d = s ? sd1 : sd0;
+        const uint64_t pk = s ? sd1.pk : sd0.pk, dv = s ? sd1.v : sd0.v;
+        const uint64_t sbf = s ? sd1.sbf : sd0.sbf;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < TILE / 16; ++ks)
-          mma_ss(tmem + TM_X(s), d.pk + kmaj(ks), d.v + 128 * ks, ID_PV, ks > 0);
+          mma_ss(tmem + TM_X(s), pk + kmaj(ks), dv + 128 * ks, ID_PV, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks)
-          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, d.sbf + 128 * ks, ID_PV, 1);
+          mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, sbf + 128 * ks, ID_PV, 1);
         mma_commit(bar(B_G3 + s));
       };
       // Each action runs once its inputs are ready; per kind they run in tile order.
@@ -314,8 +333,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     }
   } else if (warp == 9) {
     // ======================= loader =======================
-    //   LQK(i)  Q, K into slot i&1   once G3(i-2) has completed (it read S_bf16, which
-    //           replaces Q in the slot)
+    //   LQK(i)  Q, K into stage i&1  once G1(i-2) has completed (H = X W read them)
     //   LV(i)   V into slot i&1      once G3(i-2) has completed (S += phi(K)^T V, P V done)
     if (lane == 0) {
       int nqk = nt < 2 ? nt : 2, nv = nqk;
@@ -323,7 +341,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       bool reported = false;
       while ((nqk < nt || nv < nt) && !*(volatile int*)abort_flag) {
         bool progress = false;
-        if (nqk < nt && mbar_probe(bar(B_G3 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
+        if (nqk < nt && mbar_probe(bar(B_G1 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
           load_qk(nqk++);
           progress = true;
         }
@@ -371,42 +389,55 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + s), par, wp))) { good = false; return; }
       tc_fence_after();
-      // phi(Q): H_Q columns [32c, 32c+32) -> packed columns [16c, +16) and [32 + 16c, +16)
-      {
-        uint32_t hv[32];
-        tmem_ld32(tmem + lb + TM_Y(s) + 32 * c, hv);
-        uint32_t pp[16], pn[16];
+      // H_Q and H_K columns [32c, 32c+32) of this warp's rows, one wait for both
+      uint32_t hv[32], hk[32];
+      tmem_ld32x2(tmem + lb + TM_Y(s) + 32 * c, hv, tmem + lb + TM_X(s) + 32 * c, hk);
+      // in place: (h + b) log2(e), one FFMA each (the bias is stored pre-scaled and
+      // re-read from shared memory every tile rather than held in registers)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 b4 = ld_shared_f4_volatile(sb + OFF_BQ + 4 * (32 * c + 4 * q));
+        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hv[4 * q + e] = __float_as_uint(fmaf(__uint_as_float(hv[4 * q + e]), kLog2e, bb[e]));
+          hk[4 * q + e] = __float_as_uint(fmaf(__uint_as_float(hk[4 * q + e]), kLog2e, bb[e]));
+        }
+      }
+      // phi(Q) overwrites H_Q in place, and phi(K) below the y slab E3(i-2)
+      // staged in these rows of panel 0: wait for both warps of these lanes to
+      // hold their H_Q columns and for the slab's store to have read it
+      if (c == 0 && lane == 0 && i >= 2) tma_store_wait_read_all();
+      __syncwarp();
+      tc_fence_before();
+      named_bar_sync(2 + g, 64);
+      tc_fence_after();
+      // phi(Q): H_Q columns [32c, 32c+32) -> packed columns [16c, +16) (exp(+h))
+      // and [32 + 16c, +16) (exp(-h)), one half at a time
+#pragma unroll
+      for (int sgn = 0; sgn < 2; ++sgn) {
+        const float sg = sgn ? -1.f : 1.f;
+        float oo = 0.f;
+        if constexpr (SM) oo = sgn ? oq.y : oq.x;
+        uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          // (h + b) log2(e) in one FFMA: the bias is stored pre-scaled
-          const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, bq_s[32 * c + j]);
-          const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, bq_s[32 * c + j + 1]);
-          if constexpr (SM) {
-            pp[j / 2] = pack_bf16(ex2_approx(a0 - oq.x), ex2_approx(a1 - oq.x));
-            pn[j / 2] = pack_bf16(ex2_approx(-a0 - oq.y), ex2_approx(-a1 - oq.y));
-          } else {
-            pp[j / 2] = pack_bf16(ex2_approx(a0), ex2_approx(a1));
-            pn[j / 2] = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
-          }
+          const float a0 = __uint_as_float(hv[j]), a1 = __uint_as_float(hv[j + 1]);
+          if constexpr (SM) pk[j / 2] = pack_bf16(ex2_approx(sg * a0 - oo), ex2_approx(sg * a1 - oo));
+          else pk[j / 2] = pack_bf16(ex2_approx(sg * a0), ex2_approx(sg * a1));
         }
-        tc_fence_before();
-        named_bar_sync(2 + g, 64);   // both warps of these lanes hold their H_Q columns
-        tc_fence_after();
-        tmem_st16(tmem + lb + TM_Y(s) + 16 * c, pp);
-        tmem_st16(tmem + lb + TM_Y(s) + 32 + 16 * c, pn);
+        tmem_st16(tmem + lb + TM_Y(s) + 32 * sgn + 16 * c, pk);
       }
       // phi(K): features [32c, +32) -> panel 0 chunks [4c, +4); [64 + 32c, +32) -> panel 1
       {
-        uint32_t hv[32];
-        tmem_ld32(tmem + lb + TM_X(s) + 32 * c, hv);
+        const uint32_t (&hv)[32] = hk;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t wpos[4], wneg[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = 8 * q4 + 2 * e;
-            const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, bq_s[32 * c + j]);
-            const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, bq_s[32 * c + j + 1]);
+            const float a0 = __uint_as_float(hv[j]), a1 = __uint_as_float(hv[j + 1]);
             if constexpr (SM) {
               wpos[e] = valid ? pack_bf16(ex2_approx(a0 - ok_.x), ex2_approx(a1 - ok_.x)) : 0u;
               wneg[e] = valid ? pack_bf16(ex2_approx(-a0 - ok_.y), ex2_approx(-a1 - ok_.y)) : 0u;
@@ -430,8 +461,10 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
         tc_fence_after();
       }
       {
-        uint32_t sv[32];
-        tmem_ld32(tmem + lb + TM_S + 32 * c, sv);   // feature `row`, columns [32c, +32)
+        uint32_t sv[32], z0 = 0u, z1;
+        // feature `row`, columns [32c, +32); warps of column half 0 also take z
+        if (c == 0) tmem_ld32_ld2(tmem + lb + TM_S, sv, tmem + lb + TM_S + 64, z0, z1);
+        else tmem_ld32(tmem + lb + TM_S + 32, sv);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int j = 8 * q4;
@@ -443,11 +476,10 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
         }
         if (c == 0) {
           // z of feature `row` as z_hi + z_lo (both bf16) in columns 0, 1 of its z2 row
-          uint32_t z0, z1;
-          tmem_ld2(tmem + lb + TM_S + 64, z0, z1);
+          // (G3(i-2), the last reader of this slot's z2 block, completed before E3(i-2))
           const float z = __uint_as_float(z0);
           const float zl = z - __bfloat162float(__float2bfloat16_rn(z));
-          st_shared_v4(base + S_Z2 + sw128_chunk(row, 0), pack_bf16(z, zl), 0u, 0u, 0u);
+          st_shared_v4(sb + OFF_E0 + sw128_chunk(row, 2 + 2 * s), pack_bf16(z, zl), 0u, 0u, 0u);
         }
       }
       tmem_st_wait();
@@ -461,39 +493,35 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       const int s = i & 1;
       const uint32_t par = (i >> 1) & 1;
       const uint32_t base = sb + slot_off(s);
-      // phi(K) in the P panels has been read once G2 completes
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + s), par, wp))) { good = false; return; }
+      // Sc is complete once the score MMAs of G2 are; the state update of G2
+      // still reads phi(K) from the panels P goes to, so P is built in registers
+      // first and stored once all of G2 has completed
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2A + s), par, wp))) { good = false; return; }
       tc_fence_after();
-      if (c == 1 && g < 2) {
-        // keys 64..127 of rows 0..63: above the diagonal
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(base + S_PHK + 16384 + sw128_chunk(row, q), 0u, 0u, 0u, 0u);
-      } else {
+      uint32_t w[32];
+      const bool zero = c == 1 && g < 2;   // keys 64..127 of rows 0..63: above the diagonal
+      if (!zero) {
         const bool diag = (c == 0) == (g < 2);   // the 64 x 64 blocks on the diagonal
+        uint32_t sc[64];
+        tmem_ld64(tmem + lb + TM_X(s) + 64 * c, sc);   // keys [64c, +64)
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {   // keys [64c + 32 h2, +32)
-          uint32_t sv[32];
-          tmem_ld32(tmem + lb + TM_X(s) + 64 * c + 32 * h2, sv);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int key = 64 * c + 32 * h2 + 8 * q4 + 2 * e;
-              float a0 = __uint_as_float(sv[8 * q4 + 2 * e]);
-              float a1 = __uint_as_float(sv[8 * q4 + 2 * e + 1]);
-              if (diag) {
-                a0 = key <= row ? a0 : 0.f;
-                a1 = key + 1 <= row ? a1 : 0.f;
-              }
-              w4[e] = pack_bf16(a0, a1);
-            }
-            st_shared_v4(base + S_PHK + c * 16384 + sw128_chunk(row, 4 * h2 + q4), w4[0], w4[1],
-                         w4[2], w4[3]);
+        for (int j = 0; j < 64; j += 2) {
+          const int key = 64 * c + j;
+          float a0 = __uint_as_float(sc[j]);
+          float a1 = __uint_as_float(sc[j + 1]);
+          if (diag) {
+            a0 = key <= row ? a0 : 0.f;
+            a1 = key + 1 <= row ? a1 : 0.f;
           }
+          w[j / 2] = pack_bf16(a0, a1);
         }
       }
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + s), par, wp))) { good = false; return; }
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)   // keys [64c + 8q, +8) -> chunk q of panel c
+        st_shared_v4(base + S_PHK + c * 16384 + sw128_chunk(row, q), zero ? 0u : w[4 * q],
+                     zero ? 0u : w[4 * q + 1], zero ? 0u : w[4 * q + 2], zero ? 0u : w[4 * q + 3]);
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
@@ -507,23 +535,29 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G3 + s), par, wp))) { good = false; return; }
       tc_fence_after();
       uint32_t ov[32], d0, d1;
-      tmem_ld32(tmem + lb + TM_X(s) + 32 * c, ov);
-      tmem_ld2(tmem + lb + TM_X(s) + 64, d0, d1);   // rowsum(P) + phi(q) . z_hi, phi(q) . z_lo
+      // columns [32c, +32) of O; 64, 65: rowsum(P) + phi(q) . z_hi, phi(q) . z_lo
+      tmem_ld32_ld2(tmem + lb + TM_X(s) + 32 * c, ov, tmem + lb + TM_X(s) + 64, d0, d1);
       const float inv = __frcp_rn(__uint_as_float(d0) + __uint_as_float(d1));
-      if (r0 + row < A.n) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            A.y + (size_t)row_of(ub, uh, r0 + row, A.H, A.n, A.seq) * D + 32 * c);
+      // y row `row`, columns [32c, +32) -> panel 0 of the P buffer (SW128 rows)
+      const uint32_t ys = sb + slot_off(s) + S_PHK;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int j = 8 * q4;
-          dst[q4] = make_uint4(
-              pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
-              pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
-              pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
-              pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
-        }
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int j = 8 * q4;
+        st_shared_v4(ys + sw128_chunk(row, 4 * c + q4),
+                     pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
+                     pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
+                     pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
+                     pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
       }
+      fence_proxy_async();
       tc_fence_before();
+      named_bar_sync(2 + g, 64);   // rows 32g.. of both column halves are staged
+      // one store per 32-row slab; the map clips rows past n, and a slab that
+      // starts past n is not stored at all
+      if (c == 0 && lane == 0 && r0 + 32 * g < A.n) {
+        tma_store_rows(&A.ty, ys + 32 * g * 128, 0, (int)r0 + 32 * g, ub, uh, A.seq);
+        tma_store_commit();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_E3 + s));
     };
@@ -533,6 +567,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       if (step < nt && good) E1(step);
       if (step >= 1 && good) E3(step - 1);
     }
+    if (c == 0 && lane == 0) tma_store_wait_all();   // y written before the CTA retires
   }
 
   // ---- export the final state of the last segment ----
@@ -575,9 +610,9 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, TILE, sw, p.seq_major) &&
             make_rows_map(&a.tk, k, D, p.n, Hkv, p.B, 64, TILE, sw, p.seq_major) &&
             make_rows_map(&a.tv, v, D, p.n, Hkv, p.B, 64, TILE, sw, p.seq_major) &&
-            make_plane_map(&a.tw, p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B);
+            make_plane_map(&a.tw, p.Wq, D, D, p.H, 64, D, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_rows_map(&a.ty, y, D, p.n, p.H, p.B, 64, 32, sw, p.seq_major);
   if (!ok) return cudaErrorInvalidValue;
-  a.y = reinterpret_cast<__nv_bfloat16*>(y);
   a.ws = reinterpret_cast<const float*>(ws);
   a.init = init;
   a.S_out = S_out;

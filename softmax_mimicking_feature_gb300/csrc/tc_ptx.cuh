@@ -98,15 +98,12 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
-// Bounded wait for the given phase parity of an mbarrier.  The elapsed time
-// counts from entry, including any time try_wait spends suspended.
+// Bounded wait for the given phase parity of an mbarrier.  A phase that is
+// complete at the first test costs no timer read; otherwise the elapsed time
+// counts from that first (possibly suspended) test.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitPolicy& w) {
-  const uint64_t t0 = globaltimer();
-  if (mbar_test(bar, parity)) {
-    if (globaltimer() - t0 >= w.soft_ns) report_timeout(w);
-    return true;
-  }
-  return mbar_wait_slow(bar, parity, w, t0);
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, w, globaltimer());
 }
 
 // Bounded wait for a single issuing thread: polls with test_wait (never
@@ -175,12 +172,32 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          map),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+// Rows [row, row + box) of head h of batch b through a 4-D map (the store twin
+// of tma_load_rows); rows past the sequence end are not written.
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, uint32_t src, int x, int row,
+                                               int b, int h, int seq_major) {
+  if (seq_major) tma_store_4d(map, src, x, h, row, b);
+  else tma_store_4d(map, src, x, row, h, b);
+}
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 // Wait until every committed store group has finished writing global memory.
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Wait until every committed store group has finished reading shared memory
+// (the source may then be overwritten; global writes can still be in flight).
+__device__ __forceinline__ void tma_store_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Untiled bulk copy global -> shared; both addresses 16-byte aligned, bytes a
@@ -383,6 +400,23 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint
       : "memory");
 }
 // Two consecutive columns (32 lanes x 2 x 32 bit), load and wait.
+// A 32-column and a 2-column load in flight, then one wait.
+__device__ __forceinline__ void tmem_ld32_ld2(uint32_t ta, uint32_t (&a)[32], uint32_t tb,
+                                              uint32_t& b0, uint32_t& b1) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%34];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%32,%33}, [%35];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+        "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]),
+        "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]),
+        "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]),
+        "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+        "=r"(b0), "=r"(b1)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& r0, uint32_t& r1) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];\n\t"
@@ -462,6 +496,16 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int chunk) {
   return (uint32_t)r * 128u + ((uint32_t)(chunk ^ (r & 7)) << 4);
 }
 
+// 16-byte shared load the compiler may not hoist or merge (keeps loop-invariant
+// values out of registers where register pressure matters).
+__device__ __forceinline__ float4 ld_shared_f4_volatile(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
