@@ -94,8 +94,7 @@ struct Smem {
 };
 
 struct PrefillArgs {
-  CUtensorMap tq, tk, tv, twq, twk;
-  void* y;
+  CUtensorMap tq, tk, tv, twq, twk, ty;   // ty: y rows, 128-row boxes
   float* ws;        // [U][P-1][DPP*D + DPP]: segment states (S then z), scanned in place
   const float* init;  // [U][DPP*D + DPP] initial state in the same layout, or null
   float* S_out;     // [U][DPP][D] or null
@@ -297,6 +296,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 
     // ================= group 1: H = X W (Hedgehog) =================
     if (tid == 0) {
+      // epilogue 1 below overwrites the y tile of the previous tile, staged in
+      // the phi(K) panels; every thread passes the group-1 barrier first
+      tma_store_wait_read_all();
       bool ok = mbar_wait(bar_load, ph_load, wp);
       if (t == t_begin) ok = ok && mbar_wait(bar_w, ph_w, wp);
       tc_fence_after();
@@ -513,37 +515,42 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     if (tid == 0 && t + 1 < t_end && !failed) issue_loads(t + 1);
 
     // ================= epilogue 3: y = O / den =================
+    // y is staged in the phi(K) / P panels (group 3 has read P) as 128B-swizzled
+    // [128 x 64] panels and written by one TMA store per panel; the map clips
+    // rows past n.
     {
       const float den = (dq_s[row] + dq_s[128 + row]) + (rs_s[row] + rs_s[128 + row]);
       const float inv = 1.f / den;
-      const bool valid = row < nvalid;
-      __nv_bfloat16* yrow =
-          reinterpret_cast<__nv_bfloat16*>(A.y) + (size_t)row_of(ub, uh, r0 + row, A.H, A.n, A.seq) * D;
       constexpr int HC = D / 2;
 #pragma unroll
       for (int c = 0; c < HC; c += 32) {
         uint32_t ov[32];
         tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * HC + c, ov);
         tmem_ld_wait();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(yrow + half * HC + c);
+        const int col = half * HC + c;   // 32 columns from col
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int j = 8 * q4;
-            uint4 v4;
-            v4.x = pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-            v4.y = pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-            v4.z = pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-            v4.w = pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-            dst[q4] = v4;
-          }
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int j = 8 * q4;
+          st_panel_chunk(sb + C::OFF_PHK + (col / 64) * 16384, row, (col % 64) / 8 + q4,
+                         pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
+                         pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
+                         pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
+                         pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
         }
       }
+      fence_proxy_async();
     }
     tc_fence_before();
     if (__syncthreads_or(failed)) { failed = true; break; }
     tc_fence_after();
+    if (tid == 0) {
+#pragma unroll
+      for (int x = 0; x < D / 64; ++x)
+        tma_store_rows(&A.ty, sb + C::OFF_PHK + x * 16384, 64 * x, r0, ub, uh, A.seq);
+      tma_store_commit();
+    }
   }
+  if (tid == 0) tma_store_wait_all();   // y written (and its panels read) before the export
 
   // ---- export the final state of the last segment (row-major S_out, z_out) ----
   __syncthreads();
@@ -716,9 +723,9 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
               make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
               make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
               make_plane_map(&a.twq, p.Wq, D, D, p.H, 64, D, sw) &&
-              make_plane_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, sw);
+              make_plane_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, sw) &&
+              make_rows_map(&a.ty, y, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major);
     if (!ok) return cudaErrorInvalidValue;
-    a.y = y;
     a.ws = reinterpret_cast<float*>(ws);
     a.init = init;
     a.S_out = S_out;

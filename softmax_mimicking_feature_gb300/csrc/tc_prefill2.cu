@@ -294,40 +294,32 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
           mma_ts(tmem + TM_X(s), tmem + TM_Y(s) + ks * 8, sbf + 128 * ks, ID_PV, 1);
         mma_commit(bar(B_G3 + s));
       };
-      // Each action runs once its inputs are ready; per kind they run in tile order.
-      //   G1(i)                        needs LQK(i) landed and E3(i-2) done (TMEM slot free)
-      //   G2(i)                        needs E1(i) done and LV(i) landed
-      //   G3(i)                        needs E2(i) done
-      int n1 = 0, n2 = 0, n3 = 0;
-      uint64_t t_last = globaltimer();
-      bool reported = false;
-      while (ok && n3 < nt) {
-        bool progress = false;
-        if (n2 < n1 && mbar_probe(bar(B_E1A + (n2 & 1)), (n2 >> 1) & 1) &&
-            mbar_probe(bar(B_LDV + (n2 & 1)), (n2 >> 1) & 1)) {
-          G2(n2++);
-          progress = true;
-        } else if (n1 < nt && mbar_probe(bar(B_LDQK + (n1 & 1)), (n1 >> 1) & 1) &&
-                   (n1 < 2 || mbar_probe(bar(B_E3 + (n1 & 1)), ((n1 - 2) >> 1) & 1))) {
-          G1(n1++);
-          progress = true;
-        } else if (n3 < n2 && mbar_probe(bar(B_E12 + (n3 & 1)), (n3 >> 1) & 1)) {
-          G3(n3++);
-          progress = true;
+      // The groups run in the order the epilogue consumes them.  Its step i is
+      // E2(i-1), E1(i), E3(i-1), so the producer's step i is
+      //   G3(i-1)  once E2(i-1) is done
+      //   G2(i)    once E1(i) is done and V(i) has landed
+      //   G1(i+1)  once Q(i+1), K(i+1) have landed and E3(i-1) has freed the TMEM slot
+      // Each wait is on the one barrier the next group needs (polled, bounded).
+      if (ok && nt > 0) ok = mbar_wait_poll(bar(B_LDQK), 0, wp);
+      if (ok && nt > 0) G1(0);
+      for (int i = 0; i <= nt && ok; ++i) {
+        if (i >= 1) {
+          ok = mbar_wait_poll(bar(B_E12 + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wp);
+          if (!ok) break;
+          G3(i - 1);
         }
-        if (progress) {
-          t_last = globaltimer();
-        } else {
-          const uint64_t dt = globaltimer() - t_last;
-          if (!reported && dt >= A.soft_ns) {
-            reported = true;
-            report_timeout(wp);
-          }
-          if (dt >= A.hard_ns) {
-            *(volatile int*)abort_flag = 1;
-            ok = false;
-          }
-          if (*(volatile int*)abort_flag) ok = false;
+        if (i < nt) {
+          ok = mbar_wait_poll(bar(B_E1A + (i & 1)), (i >> 1) & 1, wp) &&
+               mbar_wait_poll(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
+          if (!ok) break;
+          G2(i);
+        }
+        if (i + 1 < nt) {
+          const int j = i + 1;
+          ok = mbar_wait_poll(bar(B_LDQK + (j & 1)), (j >> 1) & 1, wp) &&
+               (j < 2 || mbar_wait_poll(bar(B_E3 + (j & 1)), ((j - 2) >> 1) & 1, wp));
+          if (!ok) break;
+          G1(j);
         }
       }
     }
@@ -337,9 +329,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     //   LV(i)   V into slot i&1      once G3(i-2) has completed (S += phi(K)^T V, P V done)
     if (lane == 0) {
       int nqk = nt < 2 ? nt : 2, nv = nqk;
-      uint64_t t_last = globaltimer();
-      bool reported = false;
-      while ((nqk < nt || nv < nt) && !*(volatile int*)abort_flag) {
+      IdleClock clk;
+      bool ok = true;
+      while ((nqk < nt || nv < nt) && ok) {
         bool progress = false;
         if (nqk < nt && mbar_probe(bar(B_G1 + (nqk & 1)), ((nqk - 2) >> 1) & 1)) {
           load_qk(nqk++);
@@ -350,14 +342,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
           progress = true;
         }
         if (progress) {
-          t_last = globaltimer();
+          clk.progress();
         } else {
-          const uint64_t dt = globaltimer() - t_last;
-          if (!reported && dt >= A.soft_ns) {
-            reported = true;
-            report_timeout(wp);
-          }
-          if (dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
+          ok = clk.idle(wp);
           __nanosleep(32);
         }
       }

@@ -73,67 +73,70 @@ __device__ __forceinline__ void report_timeout(const WaitPolicy& w) {
   if (w.dev_status) atomicExch(w.dev_status, (int)HH_ERR_TIMEOUT);
 }
 
-// Slow path: t0 is the time the wait began (try_wait may already have
-// blocked inside the hardware for a while).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitPolicy& w,
-                                            uint64_t t0) {
+// Time limits of a polling loop (a thread that probes several barriers and
+// acts on whichever is ready).  The timer is read once every 64 iterations
+// without progress, not on every one (a read sits on the loop's path), so an
+// idle stretch is measured from its 64th iteration.  idle() returns false once
+// the stretch has passed the hard limit (after raising the abort flag) or the
+// flag is up; progress() starts a new stretch.
+struct IdleClock {
+  uint32_t n = 0;
+  uint64_t t0 = 0;
   bool reported = false;
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test(bar, parity)) {
-      if (!reported && globaltimer() - t0 >= w.soft_ns) report_timeout(w);
-      return true;
-    }
-    if (it == 1 || (it & 31) == 0) {
-      if (*(volatile int*)w.abort_flag) return false;
-      const uint64_t dt = globaltimer() - t0;
-      if (!reported && dt >= w.soft_ns) {
+  __device__ __forceinline__ void progress() { n = 0; }
+  __device__ __forceinline__ bool idle(const WaitPolicy& w) {
+    if ((++n & 63u) != 0) {
+      // a zero soft limit: any stretch without progress is already past it
+      if (n == 1 && w.soft_ns == 0 && !reported) {
         reported = true;
         report_timeout(w);
       }
-      if (dt >= w.hard_ns) {
-        *(volatile int*)w.abort_flag = 1;
-        return false;
-      }
+      return true;
     }
+    const uint64_t now = globaltimer();
+    if (n == 64) t0 = now;
+    const uint64_t dt = now - t0;
+    if (!reported && dt >= w.soft_ns) {
+      reported = true;
+      report_timeout(w);
+    }
+    if (dt >= w.hard_ns) *(volatile int*)w.abort_flag = 1;
+    return !*(volatile int*)w.abort_flag;
+  }
+};
+
+// Bounded wait for the given phase parity of an mbarrier (try_wait, which
+// may suspend the thread until the phase completes).  A phase complete at the
+// first test costs no timer read; past it the time limits are kept by an
+// IdleClock.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                  const WaitPolicy& w) {
+  IdleClock clk;
+  for (;;) {
+    if (mbar_test(bar, parity)) return true;
+    if (!clk.idle(w)) return false;
   }
 }
-
-// Bounded wait for the given phase parity of an mbarrier.  A phase that is
-// complete at the first test costs no timer read; otherwise the elapsed time
-// counts from that first (possibly suspended) test.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitPolicy& w) {
   if (mbar_test(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, w, globaltimer());
+  return mbar_wait_slow(bar, parity, w);
 }
 
 // Bounded wait for a single issuing thread: polls with test_wait (never
 // suspends), so the thread resumes as soon as the phase completes.  Same
-// time limits and abort behaviour as mbar_wait.
+// time limits and abort behaviour as mbar_wait, the timer read once every 64
+// polls (IdleClock).
 static __device__ __noinline__ bool mbar_wait_poll_slow(uint32_t bar, uint32_t parity,
-                                                       const WaitPolicy& w, uint64_t t0) {
-  bool reported = false;
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_probe(bar, parity)) {
-      if (!reported && globaltimer() - t0 >= w.soft_ns) report_timeout(w);
-      return true;
-    }
-    if ((it & 63) == 0) {
-      if (*(volatile int*)w.abort_flag) return false;
-      const uint64_t dt = globaltimer() - t0;
-      if (!reported && dt >= w.soft_ns) {
-        reported = true;
-        report_timeout(w);
-      }
-      if (dt >= w.hard_ns) {
-        *(volatile int*)w.abort_flag = 1;
-        return false;
-      }
-    }
+                                                       const WaitPolicy& w) {
+  IdleClock clk;
+  for (;;) {
+    if (mbar_probe(bar, parity)) return true;
+    if (!clk.idle(w)) return false;
   }
 }
 __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, const WaitPolicy& w) {
   if (mbar_probe(bar, parity)) return true;
-  return mbar_wait_poll_slow(bar, parity, w, globaltimer());
+  return mbar_wait_poll_slow(bar, parity, w);
 }
 
 // ---- TMA ------------------------------------------------------------------

@@ -478,9 +478,9 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     //   K(i) into stage i&1 once G1(i-2) has read K(i-2); V(i) once G2(i-2) has read V(i-2)
     if (lane == 0) {
       int nk = nt < 2 ? nt : 2, nv = nk;
-      uint64_t t_last = globaltimer();
-      bool reported = false;
-      while ((nk < nt || nv < nt) && !*(volatile int*)abort_flag) {
+      IdleClock clk;
+      bool alive = true;
+      while ((nk < nt || nv < nt) && alive) {
         bool progress = false;
         if (nk < nt && mbar_probe(bar(B_G1 + (nk & 1)), ((nk - 2) >> 1) & 1)) {
           load_k(nk++);
@@ -490,16 +490,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
           load_v(nv++);
           progress = true;
         }
-        if (progress) {
-          t_last = globaltimer();
-        } else {
-          const uint64_t dt = globaltimer() - t_last;
-          if (!reported && dt >= A.soft_ns) {
-            reported = true;
-            report_timeout(wp);
-          }
-          if (dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
-        }
+        if (progress) clk.progress();
+        else alive = clk.idle(wp);
       }
     }
   } else {
@@ -712,9 +704,9 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     //   K(i) once the feature warps have read K(i-2); V(i) once G2(i-2) has read V(i-2)
     if (lane == 0) {
       int nk = nt < 2 ? nt : 2, nv = nk;
-      uint64_t t_last = globaltimer();
-      bool reported = false;
-      while ((nk < nt || nv < nt) && !*(volatile int*)abort_flag) {
+      IdleClock clk;
+      bool alive = true;
+      while ((nk < nt || nv < nt) && alive) {
         bool progress = false;
         if (nk < nt && mbar_probe(bar(B_E1 + (nk & 1)), ((nk - 2) >> 1) & 1)) {
           load_k(nk++);
@@ -724,16 +716,8 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
           load_v(nv++);
           progress = true;
         }
-        if (progress) {
-          t_last = globaltimer();
-        } else {
-          const uint64_t dt = globaltimer() - t_last;
-          if (!reported && dt >= A.soft_ns) {
-            reported = true;
-            report_timeout(wp);
-          }
-          if (dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
-        }
+        if (progress) clk.progress();
+        else alive = clk.idle(wp);
       }
     }
   } else {

@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
       //   SU(i)  needs Sc(i) issued and E1(i) done (phi(K) written)
       //   G3(i)  needs SU(i) issued and E2(i) done (P written; E1(i) came before E2(i))
       int na = 0, nb = 0, n3 = 0;
-      uint64_t t_last = globaltimer();
-      bool reported = false, ok = true;
+      IdleClock clk;
+      bool ok = true;
       while (ok && n3 < nt) {
         bool progress = false;
         if (n3 < nb && probe(B_E2 + (n3 & 1), (n3 >> 1) & 1)) {
@@ -288,14 +288,12 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
           progress = true;
         }
         if (progress) {
-          t_last = globaltimer();
+          clk.progress();
         } else {
-          const uint64_t dt = globaltimer() - t_last;
-          if (leader && !reported && dt >= A.soft_ns) report_timeout(wp);
-          if (dt >= A.soft_ns) reported = true;
-          if (leader && dt >= A.hard_ns) *(volatile int*)abort_flag = 1;
+          // every lane keeps the same count; lane 0's verdict decides for the warp
+          const bool alive = clk.idle(wp);
           __syncwarp();
-          ok = __shfl_sync(0xffffffffu, (int)!*(volatile int*)abort_flag, 0) != 0;
+          ok = __shfl_sync(0xffffffffu, (int)alive, 0) != 0;
         }
       }
     }
