@@ -120,11 +120,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "samples_in_region": len(inside)}
 
 
-def source_digest():
-    """Hash of the CUDA sources, to tell whether stored ncu counters are current."""
+def source_digest(files=None):
+    """Hash of CUDA sources (the named files of csrc/, else all of them), to
+    tell whether stored ncu counters are current."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "softmax_mimicking_feature_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files if files else os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -138,9 +139,14 @@ def stored_traffic(kernel: str, workload: str):
             entries = json.load(f)
     except Exception:
         return None
-    digest = source_digest()
     for e in entries:
-        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source") == digest:
+        if e.get("kernel") != kernel or e.get("workload") != workload:
+            continue
+        try:
+            current = source_digest(e.get("sources"))
+        except OSError:
+            continue
+        if e.get("source") == current:
             return e.get("bytes_per_launch")
     return None
 

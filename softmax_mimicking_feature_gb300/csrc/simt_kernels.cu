@@ -131,11 +131,14 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
                     const T* __restrict__ Wk, const float* __restrict__ bk, int kind,
                     int softmax, int d, int dpp, int H, int G, int seq, int64_t n, int C) {
   extern __shared__ float sm[];
+  // phi rows are padded to an odd stride so that a warp reading one feature of
+  // 32 consecutive rows hits 32 different banks
+  const int ps = dpp + 1;
   float* S = sm;                       // [dpp][d]
   float* z = S + (size_t)dpp * d;      // [dpp]
-  float* phq = z + dpp;                // [C][dpp]
-  float* phk = phq + (size_t)C * dpp;  // [C][dpp]
-  float* vv = phk + (size_t)C * dpp;   // [C][d]
+  float* phq = z + dpp;                // [C][ps]
+  float* phk = phq + (size_t)C * ps;   // [C][ps]
+  float* vv = phk + (size_t)C * ps;    // [C][d]
   float* A = vv + (size_t)C * d;       // [C][C]
   float* xs = A + (size_t)C * C;       // [C][d]  raw rows
   float* xk = xs + (size_t)C * d;      // [C][d]
@@ -171,19 +174,19 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     }
     __syncthreads();
     for (int r = warp; r < C; r += kThreads / 32) {
-      phi_row<T>(kind, softmax != 0, d, dpp, xs + (size_t)r * d, Wqh, bqh, phq + (size_t)r * dpp,
+      phi_row<T>(kind, softmax != 0, d, dpp, xs + (size_t)r * d, Wqh, bqh, phq + (size_t)r * ps,
                  nullptr, lane);
-      phi_row<T>(kind, softmax != 0, d, dpp, xk + (size_t)r * d, Wkh, bkh, phk + (size_t)r * dpp,
+      phi_row<T>(kind, softmax != 0, d, dpp, xk + (size_t)r * d, Wkh, bkh, phk + (size_t)r * ps,
                  nullptr, lane);
       if (r >= nc)  // ragged tail: padded keys contribute nothing
-        for (int f = lane; f < dpp; f += 32) phk[(size_t)r * dpp + f] = 0.f;
+        for (int f = lane; f < dpp; f += 32) phk[(size_t)r * ps + f] = 0.f;
     }
     __syncthreads();
     for (int i = tid; i < C * C; i += kThreads) {
       const int r = i / C, j = i % C;
       float a = 0.f;
       if (j <= r)
-        for (int f = 0; f < dpp; ++f) a = fmaf(phq[(size_t)r * dpp + f], phk[(size_t)j * dpp + f], a);
+        for (int f = 0; f < dpp; ++f) a = fmaf(phq[(size_t)r * ps + f], phk[(size_t)j * ps + f], a);
       A[i] = a;
     }
     __syncthreads();
@@ -191,7 +194,7 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       float dn = 0.f;
       for (int j = 0; j <= r; ++j) dn += A[r * C + j];
       float di = 0.f;
-      for (int f = 0; f < dpp; ++f) di = fmaf(phq[(size_t)r * dpp + f], z[f], di);
+      for (int f = 0; f < dpp; ++f) di = fmaf(phq[(size_t)r * ps + f], z[f], di);
       den[r] = dn + di;
     }
     __syncthreads();
@@ -200,19 +203,19 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       float num = 0.f;
       for (int j = 0; j <= r; ++j) num = fmaf(A[r * C + j], vv[j * d + c], num);
       float ni = 0.f;
-      for (int f = 0; f < dpp; ++f) ni = fmaf(phq[(size_t)r * dpp + f], S[(size_t)f * d + c], ni);
+      for (int f = 0; f < dpp; ++f) ni = fmaf(phq[(size_t)r * ps + f], S[(size_t)f * d + c], ni);
       y[qrow(c0 + r) + c] = from_f<T>((num + ni) / den[r]);
     }
     __syncthreads();
     for (int i = tid; i < dpp * d; i += kThreads) {
       const int f = i / d, c = i % d;
       float acc = 0.f;
-      for (int j = 0; j < nc; ++j) acc = fmaf(phk[(size_t)j * dpp + f], vv[j * d + c], acc);
+      for (int j = 0; j < nc; ++j) acc = fmaf(phk[(size_t)j * ps + f], vv[j * d + c], acc);
       S[i] += acc;
     }
     for (int f = tid; f < dpp; f += kThreads) {
       float acc = 0.f;
-      for (int j = 0; j < nc; ++j) acc += phk[(size_t)j * dpp + f];
+      for (int j = 0; j < nc; ++j) acc += phk[(size_t)j * ps + f];
       z[f] += acc;
     }
     __syncthreads();
@@ -258,11 +261,14 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  float* __restrict__ partial, float4* __restrict__ rows4, int d, int dpp,
                  int64_t n, int ntiles, int H, int G, int seq) {
   extern __shared__ float sm[];
-  float* qs = sm;                                  // [64][d]
-  float* pq = qs + kLossRows * d;                  // [64][dpp]
-  float* ks = pq + (size_t)kLossRows * dpp;        // [32][d]
-  float* pk = ks + kLossKeys * d;                  // [32][dpp]
-  float* rowL = pk + (size_t)kLossKeys * dpp;      // [64]
+  // rows padded to odd strides: the lanes of a warp read one element of 8
+  // query rows and 4 key rows, which then sit in different banks
+  const int ds = d + 1, ps = dpp + 1;
+  float* qs = sm;                                  // [64][ds]
+  float* pq = qs + kLossRows * ds;                 // [64][ps]
+  float* ks = pq + (size_t)kLossRows * ps;         // [32][ds]
+  float* pk = ks + kLossKeys * ds;                 // [32][ps]
+  float* rowL = pk + (size_t)kLossKeys * ps;       // [64]
 
   const int64_t bh = blockIdx.x / ntiles;
   const int tile = (int)(blockIdx.x % ntiles);
@@ -275,11 +281,11 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 
   for (int e = tid; e < kLossRows * d; e += kThreads) {
     const int64_t rr = r0 + e / d;
-    qs[e] = rr < n ? to_f(q[(size_t)row_of(ub, uh, rr, H, n, seq) * d + e % d]) : 0.f;
+    qs[(e / d) * ds + e % d] = rr < n ? to_f(q[(size_t)row_of(ub, uh, rr, H, n, seq) * d + e % d]) : 0.f;
   }
   for (int e = tid; e < kLossRows * dpp; e += kThreads) {
     const int64_t rr = r0 + e / dpp;
-    pq[e] = rr < n ? to_f(phq[((size_t)bh * n + rr) * dpp + e % dpp]) : 0.f;
+    pq[(e / dpp) * ps + e % dpp] = rr < n ? to_f(phq[((size_t)bh * n + rr) * dpp + e % dpp]) : 0.f;
   }
   OnlineCE st = {-INFINITY, 0.f, 0.f, 0.f, 0.f, 0.f};
   const int64_t last = min(n, r0 + kLossRows) - 1;
@@ -287,11 +293,11 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     __syncthreads();
     for (int e = tid; e < kLossKeys * d; e += kThreads) {
       const int64_t j = k0 + e / d;
-      ks[e] = j < n ? to_f(k[(size_t)row_of(ub, kh, j, H / G, n, seq) * d + e % d]) : 0.f;
+      ks[(e / d) * ds + e % d] = j < n ? to_f(k[(size_t)row_of(ub, kh, j, H / G, n, seq) * d + e % d]) : 0.f;
     }
     for (int e = tid; e < kLossKeys * dpp; e += kThreads) {
       const int64_t j = k0 + e / dpp;
-      pk[e] = j < n ? to_f(phk[((size_t)bh * n + j) * dpp + e % dpp]) : 0.f;
+      pk[(e / dpp) * ps + e % dpp] = j < n ? to_f(phk[((size_t)bh * n + j) * dpp + e % dpp]) : 0.f;
     }
     __syncthreads();
     if (i < n) {
@@ -300,8 +306,8 @@ loss_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         const int64_t j = k0 + jl;
         if (j > i) break;
         float s = 0.f, a = 0.f;
-        for (int t = 0; t < d; ++t) s = fmaf(qs[row * d + t], ks[jl * d + t], s);
-        for (int f = 0; f < dpp; ++f) a = fmaf(pq[(size_t)row * dpp + f], pk[(size_t)jl * dpp + f], a);
+        for (int t = 0; t < d; ++t) s = fmaf(qs[row * ds + t], ks[jl * ds + t], s);
+        for (int f = 0; f < dpp; ++f) a = fmaf(pq[(size_t)row * ps + f], pk[(size_t)jl * ps + f], a);
         s *= scale;
         if (s > st.M) {
           const float c = (st.M == -INFINITY) ? 0.f : expf(st.M - s);
@@ -360,7 +366,7 @@ __global__ void sum_partials_kernel(const float* __restrict__ partial, float* __
 }
 
 size_t prefill_smem_bytes(int d, int dpp, int C) {
-  return sizeof(float) * ((size_t)dpp * d + dpp + 2 * (size_t)C * dpp + (size_t)C * d +
+  return sizeof(float) * ((size_t)dpp * d + dpp + 2 * (size_t)C * (dpp + 1) + (size_t)C * d +
                           (size_t)C * C + 2 * (size_t)C * d + C);
 }
 
@@ -427,9 +433,10 @@ static cudaError_t loss_simt_t(const Problem& p, const void* q, const void* k, c
   const int64_t units = p.B * p.H;
   if (units == 0) return cudaSuccess;
   const int ntiles = ceil_div(p.n, kLossRows);
-  const size_t smem = sizeof(float) * ((size_t)kLossRows * p.d + (size_t)kLossRows * p.dpp +
-                                       (size_t)kLossKeys * p.d + (size_t)kLossKeys * p.dpp +
-                                       kLossRows);
+  const size_t smem = sizeof(float) * ((size_t)kLossRows * (p.d + 1) +
+                                       (size_t)kLossRows * (p.dpp + 1) +
+                                       (size_t)kLossKeys * (p.d + 1) +
+                                       (size_t)kLossKeys * (p.dpp + 1) + kLossRows);
   cudaError_t e = cudaFuncSetAttribute(loss_simt_kernel<T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
