@@ -60,6 +60,11 @@ uint64_t wait_soft_limit_ns() {
   return 1000000000ull;
 }
 
+bool pdl_enabled() {
+  const char* e = getenv("HH_PDL");
+  return !(e && e[0] == '0');
+}
+
 // ---- validation -----------------------------------------------------------
 namespace {
 

@@ -81,6 +81,29 @@ int device_sm_count();
 int device_max_smem_optin();
 // Soft wait limit for device-side bounded waits, from HH_WAIT_SOFT_LIMIT_NS.
 uint64_t wait_soft_limit_ns();
+// Whether kernels that support it are launched as programmatic dependents
+// (HH_PDL=0 turns it off).
+bool pdl_enabled();
+
+// Launch as a programmatic dependent of the previous kernel on the stream: its
+// CTAs may be scheduled, and run up to griddepcontrol.wait, while that kernel
+// finishes.  Only kernels that execute griddepcontrol.wait before their first
+// global-memory access (read or write) may be launched this way.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // ---- launchers (return cudaSuccess or the launch error) ------------------
 // SIMT kernels: float32 arithmetic, any supported d; T = float or bf16.

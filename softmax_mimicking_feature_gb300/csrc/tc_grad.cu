@@ -180,6 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -464,6 +468,10 @@ __global__ void grad_partials_kernel(const float* __restrict__ part, float* __re
                                      float* __restrict__ db0, float* __restrict__ dW1,
                                      float* __restrict__ db1, int64_t B, int H, int NT, int D,
                                      int separate) {
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   const int per = D * D + D;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= per) return;
@@ -521,8 +529,7 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  grad_tc_kernel<D><<<(unsigned)(2 * U * a.NT), kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(grad_tc_kernel<D>, dim3((unsigned)(2 * U * a.NT)), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace
@@ -554,9 +561,8 @@ cudaError_t launch_loss_grad_tc(const Problem& p, const void* q, const void* k, 
   const int per = p.d * p.d + p.d;
   const int separate = dWk != nullptr;
   dim3 grid((unsigned)ceil_div(per, 256), (unsigned)p.H, separate ? 2u : 1u);
-  grad_partials_kernel<<<grid, 256, 0, s>>>(part, dWq, dbq, dWk, dbk, p.B, p.H,
-                                            ceil_div(p.n, kRT), p.d, separate);
-  return cudaGetLastError();
+  return launch_pdl(grad_partials_kernel, grid, dim3(256), 0, s, (const float*)part, dWq, dbq, dWk,
+                    dbk, (int64_t)p.B, (int)p.H, (int)ceil_div(p.n, kRT), (int)p.d, separate);
 }
 
 }  // namespace hh

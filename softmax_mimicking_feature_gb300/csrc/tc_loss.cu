@@ -108,6 +108,10 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   if (tid == 0) {
     mbar_expect_tx(bar_load, W_BYTES + X_BYTES);
@@ -314,6 +318,10 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -530,6 +538,10 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 
 __global__ void sum_partials_tc_kernel(const float* __restrict__ partial, float* __restrict__ out,
                                        int64_t heads, int ntiles) {
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t bh = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (bh >= heads) return;
   float acc = 0.f;
@@ -584,8 +596,7 @@ static cudaError_t fmap_tc_t(const Problem& p, int sides, const void* const* x,
   cudaError_t e =
       cudaFuncSetAttribute(fmap_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  fmap_tc_kernel<D><<<(unsigned)(sides * U * a.NT), 256, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(fmap_tc_kernel<D>, dim3((unsigned)(sides * U * a.NT)), dim3(256), smem, s, a);
 }
 
 cudaError_t launch_fmap_tc(const Problem& p, const void* x, int is_key, void* phi, float2* off,
@@ -638,10 +649,11 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   auto kern = rows4 ? loss_tc_kernel<D, true> : loss_tc_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(U * a.NT), kLossThreads, smem, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  sum_partials_tc_kernel<<<ceil_div(U, 128), 128, 0, s>>>(partial, head_sum, (int64_t)U, a.NT);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3((unsigned)(U * a.NT)), dim3(kLossThreads), smem, s, a);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(sum_partials_tc_kernel, dim3((unsigned)ceil_div(U, 128)), dim3(128), 0, s,
+                 (const float*)partial, head_sum, (int64_t)U, a.NT);
+  return e;
 }
 
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,

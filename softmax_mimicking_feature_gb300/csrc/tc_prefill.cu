@@ -154,6 +154,10 @@ constexpr int min_blocks() { return D == 64 ? 2 : 1; }
 template <int D>
 __global__ void __launch_bounds__(kThreads, min_blocks<D>())
 prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   using C = Cfg<D>;
   using SM = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -584,6 +588,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 // state (continuation) when there is one.
 __global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __restrict__ init,
                                     int64_t units, int pm1, int64_t elems4) {
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units * elems4) return;
   const int64_t u = i / elems4, e = i % elems4;
@@ -617,6 +625,10 @@ __global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __res
 __global__ void init_state_kernel(const float* __restrict__ S0, const float* __restrict__ z0,
                                   float* __restrict__ init, int64_t units, int D, int dp_ws,
                                   int dp_pub, int taylor) {
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t per = (int64_t)dp_ws * D + dp_ws;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units * per) return;
@@ -693,10 +705,9 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     init = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + pl.init_offset);
     const int64_t per = ws_segment_floats(p);
     const int64_t total = (int64_t)U * per;
-    init_state_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-        p.S0, p.z0, init, (int64_t)U, D, (int)(per / (D + 1)), p.dpp,
-        KIND == HH_FMAP_TAYLOR2 ? 1 : 0);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(init_state_kernel, dim3((unsigned)((total + 255) / 256)), dim3(256),
+                               0, s, p.S0, p.z0, init, (int64_t)U, D, (int)(per / (D + 1)),
+                               p.dpp, KIND == HH_FMAP_TAYLOR2 ? 1 : 0);
     if (e != cudaSuccess) return e;
   }
   if (pl.P > 1) {
@@ -705,10 +716,10 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     if (pl.P > 2 || init) {
       const int64_t elems4 = ws_segment_floats(p) / 4;
       const int64_t n4 = (int64_t)U * elems4;
-      segment_scan_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-          reinterpret_cast<float4*>(ws), reinterpret_cast<const float4*>(init), (int64_t)U,
-          pl.P - 1, elems4);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      e = launch_pdl(segment_scan_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s,
+                     reinterpret_cast<float4*>(ws), reinterpret_cast<const float4*>(init),
+                     (int64_t)U, pl.P - 1, elems4);
+      if (e != cudaSuccess) return e;
     }
   }
   if constexpr (KIND == HH_FMAP_TAYLOR2) {
@@ -751,8 +762,7 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(U * pl.P), kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)(U * pl.P)), dim3(kThreads), smem, s, a);
   }
 }
 

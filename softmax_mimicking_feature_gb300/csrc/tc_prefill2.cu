@@ -151,6 +151,21 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     prefetch_tmap(&A.tv);
     prefetch_tmap(&A.ty);
   }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  for (int i = tid; i < 1024; i += kThreads) {
+    // e0 block: logical column 0 of every row = 1; z2 blocks: zero until E1
+    // writes columns (z_hi, z_lo) of their first chunk
+    const int r = i >> 3, ch = i & 7;
+    st_shared_v4(sb + OFF_E0 + sw128_chunk(r, ch), ch == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+  }
+  // everything above touches only this CTA's shared memory and TMEM; the next
+  // kernel may be scheduled now, and this one reads and writes global memory
+  // only once the kernels before it have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
 
   auto load_qk = [&](int i) {
@@ -175,18 +190,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       load_v(i);
     }
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
   for (int i = tid; i < D; i += kThreads)
     bq_s[i] = A.bias ? A.bias[(size_t)h * D + i] * kLog2e : 0.f;
-  for (int i = tid; i < 1024; i += kThreads) {
-    // e0 block: logical column 0 of every row = 1; z2 blocks: zero until E1
-    // writes columns (z_hi, z_lo) of their first chunk
-    const int r = i >> 3, ch = i & 7;
-    st_shared_v4(sb + OFF_E0 + sw128_chunk(r, ch), ch == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
-  }
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -622,8 +627,7 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(U * pl.P), kThreads, SMEM_BYTES, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)(U * pl.P)), dim3(kThreads), SMEM_BYTES, s, a);
 }
 
 }  // namespace hh

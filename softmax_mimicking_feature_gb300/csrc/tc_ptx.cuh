@@ -139,6 +139,18 @@ __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, co
   return mbar_wait_poll_slow(bar, parity, w);
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// Let the next kernel on the stream be scheduled (its CTAs still wait in
+// pdl_wait for this grid to complete).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding kernels on the stream have completed and their
+// memory operations are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- TMA ------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y, int z) {

@@ -125,6 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
 
   auto load_k = [&](int i) {
@@ -380,6 +384,10 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   auto load_k = [&](int i) {
     const uint32_t dst = sb + OFF_K + (i & 1) * XT, b = bar(B_LDK + (i & 1));
@@ -630,6 +638,10 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   auto load_k = [&](int i) {
     const uint32_t b = bar(B_LDK + (i & 1));
@@ -832,24 +844,23 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tay::ALLOC);
     if (e != cudaSuccess) return e;
-    state_taylor_kernel<<<(unsigned)(U * (pl.P - 1)), tay::kThreads, tay::ALLOC, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(state_taylor_kernel, dim3((unsigned)(U * (pl.P - 1))), dim3(tay::kThreads),
+                      (size_t)tay::ALLOC, s, a);
   }
   if (KIND == HH_FMAP_HEDGEHOG && D == 128) {
     cudaError_t e = cudaFuncSetAttribute(state_t128_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)t128::ALLOC);
     if (e != cudaSuccess) return e;
-    state_t128_kernel<<<(unsigned)(U * (pl.P - 1)), t128::kThreads, t128::ALLOC, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(state_t128_kernel, dim3((unsigned)(U * (pl.P - 1))), dim3(t128::kThreads),
+                      (size_t)t128::ALLOC, s, a);
   }
   if constexpr (KIND == HH_FMAP_HEDGEHOG && D == 64) {
     const size_t smem = SSmem<D>::ALLOC;
     cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    state_tc_kernel<D><<<(unsigned)(U * (pl.P - 1)), kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(state_tc_kernel<D>, dim3((unsigned)(U * (pl.P - 1))), dim3(kThreads), smem, s, a);
   }
   return cudaErrorInvalidValue;
 }

@@ -141,6 +141,10 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     prefetch_tmap(&A.tk);
     prefetch_tmap(&A.tv);
   }
+  // the next kernel may be scheduled now; global memory is touched only after
+  // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   __syncthreads();
   auto load = [&](int i) {
     const int s = i & 1;
@@ -541,8 +545,8 @@ cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  taylor_out_kernel<<<(unsigned)(U * pl.P), kThreads, SMEM_BYTES, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(taylor_out_kernel, dim3((unsigned)(U * pl.P)), dim3(kThreads),
+                    (size_t)SMEM_BYTES, s, a);
 }
 
 }  // namespace hh
