@@ -211,47 +211,36 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
 
   if (warp == 8) {
     // ======================= MMA issuer =======================
-    // The whole warp runs the issue loop (warp-uniform control flow and
-    // descriptors); lane 0 alone executes the tcgen05 instructions.
-    if (nt > 0) {
+    // Lane 0 issues every tcgen05 instruction, in the order the epilogue
+    // consumes the groups, waiting on one barrier at a time.
+    if (nt > 0 && lane == 0) {
       constexpr uint32_t ID_SC = idesc_bf16(128, 128, 0, 0);   // Q[K-major] K[K-major]
       constexpr uint32_t ID_SU = idesc_bf16(128, 32, 1, 1);    // phiK^T[MN] [V e0][MN]
       constexpr uint32_t ID_O = idesc_bf16(128, 32, 0, 1);     // P or phiQ x [V e0] or [S z2]
-      const bool leader = lane == 0;
       // descriptor bases; a k-step only moves the start-address field (16-byte units)
       const uint64_t dphk = smem_desc(sb + OFF_PHK, 16384, 1024, 2);
       const uint64_t dp0 = smem_desc(sb + OFF_P, 16, 1024, 2);
       auto dv = [&](int s) {   // [V e0]: the e0 block one leading-byte offset after V
         return smem_desc(sb + OFF_V + s * XT, OFF_E0 - (OFF_V + s * XT), 256, 6);
       };
-      auto probe = [&](int b, uint32_t parity) {   // lane 0's view, broadcast
-        return __shfl_sync(0xffffffffu, (int)mbar_probe(bar(b), parity), 0) != 0;
-      };
       auto Sc = [&](int i) {
         const int s = i & 1;
         const uint64_t da = smem_desc(sb + OFF_Q + s * XT, 16, 256, 6);
         const uint64_t db = smem_desc(sb + OFF_K + s * XT, 16, 256, 6);
         tc_fence_after();
-        if (leader) {
-          mma_ss(tmem + TM_X(s), da, db, ID_SC, 0);
-          mma_commit(bar(B_SC + s));
-        }
-        __syncwarp();
+        mma_ss(tmem + TM_X(s), da, db, ID_SC, 0);
+        mma_commit(bar(B_SC + s));
       };
       auto SU = [&](int i) {
         const int s = i & 1;
         const uint64_t v = dv(s);
         tc_fence_after();
-        if (leader) {
 #pragma unroll
-          for (int mb = 0; mb < 2; ++mb)
+        for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-            for (int ks = 0; ks < TILE / 16; ++ks)
-              mma_ss(tmem + TM_S + 32 * mb, dphk + (2 * mb) * 1024 + ks * 128, v + ks * 32, ID_SU,
-                     1);
-          mma_commit(bar(B_SU + s));
-        }
-        __syncwarp();
+          for (int ks = 0; ks < TILE / 16; ++ks)
+            mma_ss(tmem + TM_S + 32 * mb, dphk + (2 * mb) * 1024 + ks * 128, v + ks * 32, ID_SU, 1);
+        mma_commit(bar(B_SU + s));
       };
       auto G3 = [&](int i) {
         const int s = i & 1;
@@ -259,46 +248,39 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
         const uint64_t dsb = smem_desc(sb + OFF_SB + s * 2 * SB_BYTES, SB_BYTES, 256, 6);
         const uint32_t ty = tmem + TM_Y(s);
         tc_fence_after();
-        if (leader) {
 #pragma unroll
-          for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ss(tmem + TM_X(s), dp0 + s * 2048 + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32,
-                   ID_O, ks > 0);
+        for (int ks = 0; ks < TILE / 16; ++ks)
+          mma_ss(tmem + TM_X(s), dp0 + s * 2048 + (ks >> 2) * 1024 + (ks & 3) * 2, v + ks * 32,
+                 ID_O, ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < DP / 16; ++ks)
-            mma_ts(tmem + TM_X(s), ty + ks * 8, dsb + ks * 32, ID_O, 1);
-          mma_commit(bar(B_G3 + s));
-        }
-        __syncwarp();
+        for (int ks = 0; ks < DP / 16; ++ks)
+          mma_ts(tmem + TM_X(s), ty + ks * 8, dsb + ks * 32, ID_O, 1);
+        mma_commit(bar(B_G3 + s));
       };
-      // Per tile the MMAs go in the order Sc, SU, G3:
-      //   Sc(i)  needs Q, K landed and E3(i-2) done (its X columns free)
-      //   SU(i)  needs Sc(i) issued and E1(i) done (phi(K) written)
-      //   G3(i)  needs SU(i) issued and E2(i) done (P written; E1(i) came before E2(i))
-      int na = 0, nb = 0, n3 = 0;
-      IdleClock clk;
+      // The epilogue runs E1(i), E2(i), E3(i-1) per step, so the groups are
+      // consumed in the order Sc(0), Sc(1), then per tile i
+      //   Sc(i)   (i >= 2) once Q, K of tile i have landed and E3(i-2) has freed
+      //           its score / output columns
+      //   SU(i)   once E1(i) has written phi(K_i) and the snapshot
+      //   G3(i)   once E2(i) has written P_i
       bool ok = true;
-      while (ok && n3 < nt) {
-        bool progress = false;
-        if (n3 < nb && probe(B_E2 + (n3 & 1), (n3 >> 1) & 1)) {
-          G3(n3++);
-          progress = true;
-        } else if (na < nt && probe(B_LD + (na & 1), (na >> 1) & 1) &&
-                   (na < 2 || probe(B_E3 + (na & 1), ((na - 2) >> 1) & 1))) {
-          Sc(na++);
-          progress = true;
-        } else if (nb < na && probe(B_E1 + (nb & 1), (nb >> 1) & 1)) {
-          SU(nb++);
-          progress = true;
+      for (int i = 0; i < 2 && i < nt && ok; ++i) {
+        ok = mbar_wait_poll(bar(B_LD + i), 0, wp);
+        if (ok) Sc(i);
+      }
+      for (int i = 0; i < nt && ok; ++i) {
+        if (i >= 2) {
+          ok = mbar_wait_poll(bar(B_LD + (i & 1)), (i >> 1) & 1, wp) &&
+               mbar_wait_poll(bar(B_E3 + (i & 1)), ((i - 2) >> 1) & 1, wp);
+          if (!ok) break;
+          Sc(i);
         }
-        if (progress) {
-          clk.progress();
-        } else {
-          // every lane keeps the same count; lane 0's verdict decides for the warp
-          const bool alive = clk.idle(wp);
-          __syncwarp();
-          ok = __shfl_sync(0xffffffffu, (int)alive, 0) != 0;
-        }
+        ok = mbar_wait_poll(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp);
+        if (!ok) break;
+        SU(i);
+        ok = mbar_wait_poll(bar(B_E2 + (i & 1)), (i >> 1) & 1, wp);
+        if (!ok) break;
+        G3(i);
       }
     }
   } else if (warp == 9) {
