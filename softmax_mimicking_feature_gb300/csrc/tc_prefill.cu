@@ -173,6 +173,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   const uint32_t bar_load = sb + SM::OFF_BAR;
   const uint32_t bar_w = bar_load + 8;
   const uint32_t bar_mma = bar_load + 16;
+  const uint32_t bar_sc = bar_load + 24;   // the score MMAs of group 2 alone
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM::OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + SM::OFF_MISC + 4);
 
@@ -197,6 +198,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
     mbar_init(bar_load, 1);
     mbar_init(bar_w, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_sc, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&A.tk);
@@ -278,7 +280,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   __syncthreads();
   tc_fence_after();
 
-  uint32_t ph_load = 0, ph_w = 0, ph_mma = 0;
+  uint32_t ph_load = 0, ph_w = 0, ph_mma = 0, ph_sc = 0;
 
 
 
@@ -452,12 +454,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
       z_s[f] += ((zp_s[f] + zp_s[SM::ZN + f]) + zp_s[2 * SM::ZN + f]) + zp_s[3 * SM::ZN + f];
 
     // ================= group 2: Sc, S update =================
+    // The scores are committed on their own: epilogue 2 reads them while the
+    // state update runs, and group 3's phi(Q) S half is issued as soon as they
+    // are out of TMEM (O reuses their columns); only P V waits for P.
     if (tid == 0) {
       for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
         const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
         mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8,
                smem_desc(sb + C::OFF_PHK + koff, 16, 1024, 2), IDESC_SC, ks > 0);
       }
+      mma_commit(bar_sc);
       for (int mb = 0; mb < C::NMB; ++mb)
         for (int ks = 0; ks < kTile / 16; ++ks)
           mma_ss(tmem + C::TM_S + mb * D,
@@ -465,11 +471,12 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
                  v_desc(ks), IDESC_SU, 1);
       mma_commit(bar_mma);
     }
-    if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
-    ph_mma ^= 1;
+    if (!mbar_wait(bar_sc, ph_sc, wp)) failed = true;
+    ph_sc ^= 1;
     tc_fence_after();
 
     // ================= epilogue 2: P = bf16(tril(Sc)), row sums =================
+    uint32_t pw[32];   // this thread's 64 keys of P as bf16 pairs
     {
       float rs = 0.f;
 #pragma unroll
@@ -477,41 +484,50 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
         uint32_t sv[32];
         tmem_ld32(tmem + lane_base(warp) + C::TM_X + half * 64 + c, sv);
         tmem_ld_wait();
-        uint32_t pw[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int key = half * 64 + c + j;
           const float a0 = (key <= row) ? __uint_as_float(sv[j]) : 0.f;
           const float a1 = (key + 1 <= row) ? __uint_as_float(sv[j + 1]) : 0.f;
           const uint32_t w2 = pack_bf16(a0, a1);
-          pw[j / 2] = w2;
+          pw[(c + j) / 2] = w2;
           rs += bf16_lo(w2) + bf16_hi(w2);
         }
-        // P panel: [128 rows][128 keys] K-major, key block = half (16 KB each)
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_panel_chunk(sb + C::OFF_PHK + half * 16384, row, c / 8 + q4, pw[4 * q4],
-                         pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
       }
       rs_s[half * 128 + row] = rs;
     }
+    tc_fence_before();
+    __syncthreads();   // every read of Sc is done: its columns take O
+    tc_fence_after();
+    // ================= group 3a: O = phi(Q) S_bf16 =================
+    if (tid == 0) {
+      for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
+        const uint64_t bdesc = smem_desc(sb + C::OFF_SB + ks * 2048, C::DP * 128, 1024, 2);
+        mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8, bdesc, IDESC_QS, ks > 0);
+      }
+    }
+    // P overwrites phi(K), which the state update reads
+    if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
+    ph_mma ^= 1;
+    tc_fence_after();
+    // P panel: [128 rows][128 keys] K-major, key block = half (16 KB each)
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4)
+      st_panel_chunk(sb + C::OFF_PHK + half * 16384, row, q4, pw[4 * q4], pw[4 * q4 + 1],
+                     pw[4 * q4 + 2], pw[4 * q4 + 3]);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ================= group 3: O = P V + phi(Q) S_bf16 =================
+    // ================= group 3b: O += P V =================
     if (tid == 0) {
       for (int ks = 0; ks < kTile / 16; ++ks) {
         const uint32_t koff = (ks * 16 / 64) * 16384 + ((ks * 16) % 64) * 2;
         mma_ss(tmem + C::TM_X, smem_desc(sb + C::OFF_PHK + koff, 16, 1024, 2), v_desc(ks),
-               IDESC_PV, ks > 0);
+               IDESC_PV, 1);
       }
-      for (int ks = 0; ks < C::KSTEPS_F; ++ks) {
-        const uint64_t bdesc = smem_desc(sb + C::OFF_SB + ks * 2048, C::DP * 128, 1024, 2);
-        mma_ts(tmem + C::TM_X, tmem + C::TM_Y + ks * 8, bdesc, IDESC_QS, 1);
-      }
-      mma_commit(bar_mma);
+      mma_commit(bar_mma);   // covers group 3a too
     }
     if (!mbar_wait(bar_mma, ph_mma, wp)) failed = true;
     ph_mma ^= 1;
