@@ -319,6 +319,14 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
                  ks > 0);
         }
         mma_commit(bar_mma);
+        // the next tile's Q, K, V into L2 now: their loads wait for group 3
+        // (S_bf16 replaces Q / K) and then hit L2
+        if (t + 1 < t_end)
+          for (int i = 0; i < D / 64; ++i) {
+            tma_prefetch_rows(&A.tq, 64 * i, (t + 1) * kTile, ub, uh, A.seq);
+            tma_prefetch_rows(&A.tk, 64 * i, (t + 1) * kTile, ub, kh, A.seq);
+            tma_prefetch_rows(&A.tv, 64 * i, (t + 1) * kTile, ub, kh, A.seq);
+          }
       } else {
         failed = true;
       }

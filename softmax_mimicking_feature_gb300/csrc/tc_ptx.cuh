@@ -178,6 +178,26 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* m
   else tma_load_4d(dst, map, bar, x, row, h, b);
 }
 
+// Bring a tile into L2 ahead of its load (no shared memory, no barrier): the
+// later TMA load of the same box then reads L2 instead of waiting on HBM.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z,
+                                                int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+// The prefetch twin of tma_load_rows.
+__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int x, int row, int b,
+                                                  int h, int seq_major) {
+  if (seq_major) tma_prefetch_4d(map, x, h, row, b);
+  else tma_prefetch_4d(map, x, row, h, b);
+}
+
 // Tile shared -> global through a tensor map, in the current bulk-async
 // group.  The innermost coordinate must be 16-byte aligned and none negative.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
