@@ -182,12 +182,31 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
         for (int f = lane; f < dpp; f += 32) phk[(size_t)r * ps + f] = 0.f;
     }
     __syncthreads();
-    for (int i = tid; i < C * C; i += kThreads) {
-      const int r = i / C, j = i % C;
-      float a = 0.f;
-      if (j <= r)
-        for (int f = 0; f < dpp; ++f) a = fmaf(phq[(size_t)r * ps + f], phk[(size_t)j * ps + f], a);
-      A[i] = a;
+    // The three contractions below run on 4 x 4 register blocks (8 shared
+    // loads per 16 FMAs instead of 32); every output still sums its terms in
+    // the same order as a plain loop, so results do not depend on the blocking.
+    // A = tril(phi(Q) phi(K)^T): blocks wholly above the diagonal are zero.
+    for (int blk = tid; blk < (C / 4) * (C / 4); blk += kThreads) {
+      const int r0 = 4 * (blk / (C / 4)), j0 = 4 * (blk % (C / 4));
+      float a[4][4] = {};
+      if (j0 <= r0) {
+        for (int f = 0; f < dpp; ++f) {
+          float qv[4], kv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            qv[e] = phq[(size_t)(r0 + e) * ps + f];
+            kv[e] = phk[(size_t)(j0 + e) * ps + f];
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) a[r][c] = fmaf(qv[r], kv[c], a[r][c]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) A[(r0 + r) * C + j0 + c] = (j0 + c <= r0 + r) ? a[r][c] : 0.f;
     }
     __syncthreads();
     for (int r = tid; r < C; r += kThreads) {
@@ -198,20 +217,67 @@ prefill_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       den[r] = dn + di;
     }
     __syncthreads();
-    for (int i = tid; i < nc * d; i += kThreads) {
-      const int r = i / d, c = i % d;
-      float num = 0.f;
-      for (int j = 0; j <= r; ++j) num = fmaf(A[r * C + j], vv[j * d + c], num);
-      float ni = 0.f;
-      for (int f = 0; f < dpp; ++f) ni = fmaf(phq[(size_t)r * ps + f], S[(size_t)f * d + c], ni);
-      y[qrow(c0 + r) + c] = from_f<T>((num + ni) / den[r]);
+    // y = (A V + phi(Q) S) / den on 4 rows x 4 columns per thread (A is zero
+    // above the diagonal, so running j to the block's last row adds exact zeros)
+    const int dq4 = (d + 3) / 4;
+    for (int blk = tid; blk < (C / 4) * dq4; blk += kThreads) {
+      const int r0 = 4 * (blk / dq4), c0v = 4 * (blk % dq4);
+      if (r0 >= nc) continue;
+      float num[4][4] = {}, ni[4][4] = {};
+      const int jmax = min(r0 + 3, nc - 1);
+      for (int j = 0; j <= jmax; ++j) {
+        float av[4], vc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          av[e] = A[(r0 + e) * C + j];
+          vc[e] = c0v + e < d ? vv[j * d + c0v + e] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) num[r][c] = fmaf(av[r], vc[c], num[r][c]);
+      }
+      for (int f = 0; f < dpp; ++f) {
+        float qv[4], sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qv[e] = phq[(size_t)(r0 + e) * ps + f];
+          sc[e] = c0v + e < d ? S[(size_t)f * d + c0v + e] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ni[r][c] = fmaf(qv[r], sc[c], ni[r][c]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (r0 + r < nc && c0v + c < d)
+            y[qrow(c0 + r0 + r) + c0v + c] = from_f<T>((num[r][c] + ni[r][c]) / den[r0 + r]);
     }
     __syncthreads();
-    for (int i = tid; i < dpp * d; i += kThreads) {
-      const int f = i / d, c = i % d;
-      float acc = 0.f;
-      for (int j = 0; j < nc; ++j) acc = fmaf(phk[(size_t)j * ps + f], vv[j * d + c], acc);
-      S[i] += acc;
+    // S += phi(K)^T V on 4 features x 4 columns per thread
+    for (int blk = tid; blk < ((dpp + 3) / 4) * dq4; blk += kThreads) {
+      const int f0 = 4 * (blk / dq4), c0v = 4 * (blk % dq4);
+      float acc[4][4] = {};
+      for (int j = 0; j < nc; ++j) {
+        float kv[4], vc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kv[e] = f0 + e < dpp ? phk[(size_t)j * ps + f0 + e] : 0.f;
+          vc[e] = c0v + e < d ? vv[j * d + c0v + e] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(kv[r], vc[c], acc[r][c]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (f0 + r < dpp && c0v + c < d) S[(size_t)(f0 + r) * d + c0v + c] += acc[r][c];
     }
     for (int f = tid; f < dpp; f += kThreads) {
       float acc = 0.f;
