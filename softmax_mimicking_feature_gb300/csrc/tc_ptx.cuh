@@ -178,13 +178,6 @@ __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* m
   else tma_load_4d(dst, map, bar, x, row, h, b);
 }
 
-// Bring a tile into L2 ahead of its load (no shared memory, no barrier): the
-// later TMA load of the same box then reads L2 instead of waiting on HBM.
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z,
                                                 int w) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map),
@@ -361,56 +354,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "r"(taddr)
       : "memory");
 }
-// Issue a 64-column load without waiting; the registers may only be used after
-// tmem_ld_wait_regs64 on the same array, whose "+r" operands make every later
-// use depend on the wait.  (Callers check that ptxas reports no spills: a
-// spill between the two statements would capture the registers too early.)
-__device__ __forceinline__ void tmem_ld64_issue(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,"
-      "%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,"
-      "%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-      : HH_R8(0), HH_R8(8), HH_R8(16), HH_R8(24), HH_R8(32), HH_R8(40), HH_R8(48), HH_R8(56)
-      : "r"(taddr)
-      : "memory");
-}
-#define HH_W8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
-                 "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
-__device__ __forceinline__ void tmem_ld_wait_regs64(uint32_t (&r)[64]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : HH_W8(0), HH_W8(8), HH_W8(16), HH_W8(24), HH_W8(32), HH_W8(40), HH_W8(48),
-                 HH_W8(56)
-               :
-               : "memory");
-}
-#undef HH_W8
-
-// Two 64-column loads in flight, then one wait.
-#define HH_RA8(i) "=r"(a[i]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), \
-                  "=r"(a[i + 4]), "=r"(a[i + 5]), "=r"(a[i + 6]), "=r"(a[i + 7])
-#define HH_RB8(i) "=r"(b[i]), "=r"(b[i + 1]), "=r"(b[i + 2]), "=r"(b[i + 3]), \
-                  "=r"(b[i + 4]), "=r"(b[i + 5]), "=r"(b[i + 6]), "=r"(b[i + 7])
-__device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t (&a)[64], uint32_t tb,
-                                            uint32_t (&b)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,"
-      "%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,"
-      "%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,"
-      "%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,"
-      "%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,"
-      "%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : HH_RA8(0), HH_RA8(8), HH_RA8(16), HH_RA8(24), HH_RA8(32), HH_RA8(40), HH_RA8(48),
-        HH_RA8(56), HH_RB8(0), HH_RB8(8), HH_RB8(16), HH_RB8(24), HH_RB8(32), HH_RB8(40),
-        HH_RB8(48), HH_RB8(56)
-      : "r"(ta), "r"(tb)
-      : "memory");
-}
-#undef HH_RA8
-#undef HH_RB8
 #undef HH_R8
 // Two 32-column loads in flight, then one wait.
 __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb,
