@@ -253,7 +253,7 @@ def mimicry_loss_rows(q, k, phi_q, phi_k, rows) -> np.ndarray:
     return out
 
 
-def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None):
+def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
     """Gradient of sum_i L_i (paper Eq. 4, one head) w.r.t. the Hedgehog map.
 
     HH summary, "The Attention Weight Distillation Loss": only the feature-map
@@ -268,15 +268,32 @@ def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None):
     over the query rows (query map) and the key rows (key map).  Returns
     (dWq, dbq, dWk, dbk); with one shared map (Wk None) the gradient with
     respect to it is dWq + dWk, dbq + dbk.
+
+    kind="hedgehog_softmax": the map of Choice 4 (Eq. 5), h = xW (no bias),
+    phi = [softmax(h); softmax(-h)].  Only the step from dL/dphi to dL/dh
+    changes: the Jacobian of s = softmax(u) maps an upstream gradient y to
+    s * (y - <y, s>), and the negated half enters with a minus sign, so
+        dL/dh = phi_+ * (dL/dphi_+ - <dL/dphi_+, phi_+>)
+              - phi_- * (dL/dphi_- - <dL/dphi_-, phi_->).
+    b and bk are ignored and dbq, dbk are returned as None.
     """
     q, k = _f64(q), _f64(k)
-    Wq, bq = _f64(W), _f64(b)
-    Wk_, bk_ = (Wq, bq) if Wk is None else (_f64(Wk), _f64(bk))
     d = q.shape[-1]
-    hq = q @ Wq + bq
-    hk = k @ Wk_ + bk_
-    pq = np.concatenate([np.exp(hq), np.exp(-hq)], axis=-1)
-    pk = np.concatenate([np.exp(hk), np.exp(-hk)], axis=-1)
+    soft = kind == "hedgehog_softmax"
+    if not soft and kind != "hedgehog":
+        raise ValueError(f"no parameters to differentiate for {kind!r}")
+    Wq = _f64(W)
+    Wk_ = Wq if Wk is None else _f64(Wk)
+    if soft:
+        pq = hedgehog_softmax_feature_map(q, Wq)
+        pk = hedgehog_softmax_feature_map(k, Wk_)
+    else:
+        bq = _f64(b)
+        bk_ = bq if Wk is None else _f64(bk)
+        hq = q @ Wq + bq
+        hk = k @ Wk_ + bk_
+        pq = np.concatenate([np.exp(hq), np.exp(-hq)], axis=-1)
+        pk = np.concatenate([np.exp(hk), np.exp(-hk)], axis=-1)
     n = q.shape[0]
     mask = np.tril(np.ones((n, n), dtype=bool))
     a = pq @ pk.T
@@ -285,9 +302,22 @@ def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None):
     g = np.where(mask, 1.0 / A[:, None] - p / np.where(mask, a, 1.0), 0.0)
     dpq = g @ pk
     dpk = g.T @ pq
+    if soft:
+        dhq = _softmax_vjp(dpq[:, :d], pq[:, :d]) - _softmax_vjp(dpq[:, d:], pq[:, d:])
+        dhk = _softmax_vjp(dpk[:, :d], pk[:, :d]) - _softmax_vjp(dpk[:, d:], pk[:, d:])
+        return q.T @ dhq, None, k.T @ dhk, None
     dhq = dpq[:, :d] * pq[:, :d] - dpq[:, d:] * pq[:, d:]
     dhk = dpk[:, :d] * pk[:, :d] - dpk[:, d:] * pk[:, d:]
     return q.T @ dhq, dhq.sum(axis=0), k.T @ dhk, dhk.sum(axis=0)
+
+
+def _softmax_vjp(y, s) -> np.ndarray:
+    """Row-wise vector-Jacobian product of softmax: s * (y - sum_l y_l s_l).
+
+    s = softmax(u) over the last axis has ds_l/du_m = s_l (delta_lm - s_m),
+    so sum_l y_l ds_l/du_m = s_m (y_m - <y, s>).
+    """
+    return s * (y - (y * s).sum(axis=-1, keepdims=True))
 
 
 def attention_entropy(weights) -> np.ndarray:
@@ -374,28 +404,34 @@ def stats_causal(kind, q, k, W=None, b=None):
     return out
 
 
-def loss_grad_causal(q, k, W, b, Wk=None, bk=None):
+def loss_grad_causal(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
     """Gradient of the loss summed over [B, H, n] w.r.t. per-head maps.
 
     Returns (dWq [H, d, d], dbq [H, d], dWk, dbk), each summed over the batch.
     With one shared map (Wk None) dWk and dbk are None and the query and key
-    sides are added into dWq, dbq.
+    sides are added into dWq, dbq.  kind="hedgehog_softmax" (no bias): the
+    bias gradients are None.
     """
     q, k = _f64(q), _f64(k)
     B, H, n, d = q.shape
+    soft = kind == "hedgehog_softmax"
     dWq = np.zeros((H, d, d))
     dbq = np.zeros((H, d))
     dWk = np.zeros((H, d, d))
     dbk = np.zeros((H, d))
     for bi in range(B):
         for h in range(H):
-            g = mimicry_loss_grad(q[bi, h], k[bi, h], _f64(W)[h], _f64(b)[h],
+            g = mimicry_loss_grad(q[bi, h], k[bi, h], _f64(W)[h],
+                                  None if soft else _f64(b)[h],
                                   None if Wk is None else _f64(Wk)[h],
-                                  None if bk is None else _f64(bk)[h])
+                                  None if (bk is None or soft) else _f64(bk)[h], kind=kind)
             dWq[h] += g[0]
-            dbq[h] += g[1]
             dWk[h] += g[2]
-            dbk[h] += g[3]
+            if not soft:
+                dbq[h] += g[1]
+                dbk[h] += g[3]
+    if soft:
+        dbq = dbk = None
     if Wk is None:
-        return dWq + dWk, dbq + dbk, None, None
+        return dWq + dWk, (None if soft else dbq + dbk), None, None
     return dWq, dbq, dWk, dbk

@@ -277,6 +277,76 @@ def check_softmax_feature_map(O, golden):
     np.testing.assert_allclose(O.hedgehog_softmax_feature_map(np.zeros((2, d)), W), 1.0 / d, rtol=1e-15)
 
 
+def check_softmax_map_loss_grad(O, golden):
+    """Gradient through the Choice 4 (Eq. 5) map against central differences.
+
+    Also an invariant of the map itself: adding one vector u to every column
+    of W leaves phi unchanged, so the loss is flat along W + u 1^T and every
+    row of dW sums to zero; the negation block alone (phi_- only) is checked
+    by flipping the sign of W, which swaps the two halves and keeps the loss.
+    """
+    rng = np.random.default_rng(29)
+    n, d, eps = 6, 3, 1e-6
+    kind = "hedgehog_softmax"
+
+    def total(Wq, Wk, q, k):
+        pq = O.hedgehog_softmax_feature_map(q, Wq)
+        pk = O.hedgehog_softmax_feature_map(k, Wk)
+        return O.mimicry_loss(q, k, pq, pk).sum()
+
+    def fd(f, X):
+        g = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            g[idx] = (f(Xp) - f(Xm)) / (2 * eps)
+        return g
+
+    for trial in range(2):
+        q, k = rng.normal(size=(2, n, d)) * 0.8
+        Wq, Wk = rng.normal(size=(2, d, d)) * 0.9
+        g = O.mimicry_loss_grad(q, k, Wq, None, kind=kind)
+        assert g[1] is None and g[3] is None
+        shared = g[0] + g[2]
+        np.testing.assert_allclose(shared, fd(lambda X: total(X, X, q, k), Wq), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(shared.sum(axis=1), 0.0, atol=1e-12)
+        # phi(x; -W) = [phi_-; phi_+]: a_ij and the loss are unchanged, dW flips sign
+        gm = O.mimicry_loss_grad(q, k, -Wq, None, kind=kind)
+        np.testing.assert_allclose(gm[0] + gm[2], -shared, rtol=1e-10, atol=1e-13)
+        g = O.mimicry_loss_grad(q, k, Wq, None, Wk, None, kind=kind)
+        np.testing.assert_allclose(g[0], fd(lambda X: total(X, Wk, q, k), Wq), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(g[2], fd(lambda X: total(Wq, X, q, k), Wk), rtol=1e-6, atol=1e-8)
+    # batched wrapper: sum over the batch of per-head gradients of the summed loss
+    B, H = 2, 2
+    q = rng.normal(size=(B, H, 4, d)) * 0.8
+    k = rng.normal(size=(B, H, 4, d)) * 0.8
+    W = rng.normal(size=(H, d, d)) * 0.9
+    dW, db, dWk, dbk = O.loss_grad_causal(q, k, W, None, kind=kind)
+    assert db is None and dWk is None and dbk is None
+
+    def batch_total(Wx):
+        return O.loss_causal(kind, q, k, Wx, None)[1].sum()
+
+    for h in range(H):
+        for idx in [(0, 1), (2, 0)]:
+            Wp, Wm = W.copy(), W.copy()
+            Wp[(h,) + idx] += eps
+            Wm[(h,) + idx] -= eps
+            f = (batch_total(Wp) - batch_total(Wm)) / (2 * eps)
+            assert abs(f - dW[(h,) + idx]) <= 1e-6 * max(1.0, abs(f))
+    Wk2 = rng.normal(size=(H, d, d)) * 0.9
+    sq, _, sk, _ = O.loss_grad_causal(q, k, W, None, Wk2, None, kind=kind)
+    rq, rk = np.zeros_like(sq), np.zeros_like(sk)
+    for bi in range(B):
+        for h in range(H):
+            g = O.mimicry_loss_grad(q[bi, h], k[bi, h], W[h], None, Wk2[h], None, kind=kind)
+            rq[h] += g[0]
+            rk[h] += g[2]
+    np.testing.assert_allclose(sq, rq, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(sk, rk, rtol=1e-13, atol=1e-15)
+
+
 def check_entropies_and_kl(O, golden):
     """H(a_i) of the spikiness section, KL = CE - H(p) (Gibbs), known extremes."""
     n = 7
@@ -331,7 +401,8 @@ PINS = [check_hand_worked, check_taylor_closed_form, check_hedgehog_cosh,
         check_identity_and_zero_maps, check_orientation, check_weight_rows,
         check_constant_values_and_first_row, check_uniform_cases,
         check_quadratic_vs_recurrent, check_softmax_target, check_loss_properties,
-        check_loss_grad_finite_differences, check_softmax_feature_map, check_entropies_and_kl]
+        check_loss_grad_finite_differences, check_softmax_feature_map, check_entropies_and_kl,
+        check_softmax_map_loss_grad]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -372,6 +443,12 @@ MUTANTS = {
     "softmax_map_negation_dropped": ("    neg = np.exp(-h)\n", "    neg = np.exp(h)\n"),
     "softmax_map_raw_dispatch": ("return hedgehog_softmax_feature_map(x, W)\n",
                                  "return hedgehog_feature_map(x, W, b)\n"),
+    "softmax_grad_uncentred": ("return s * (y - (y * s).sum(axis=-1, keepdims=True))", "return s * y"),
+    "softmax_grad_negative_half_added": ("dhq = _softmax_vjp(dpq[:, :d], pq[:, :d]) - _softmax_vjp",
+                                         "dhq = _softmax_vjp(dpq[:, :d], pq[:, :d]) + _softmax_vjp"),
+    "softmax_grad_key_side_query_features": ("dhk = _softmax_vjp(dpk[:, :d], pk[:, :d])",
+                                             "dhk = _softmax_vjp(dpk[:, :d], pq[:, :d])"),
+    "softmax_grad_centred_over_rows": ("(y * s).sum(axis=-1, keepdims=True)", "(y * s).sum(axis=0, keepdims=True)"),
     "entropy_log2": ("out[i] = -np.sum(nz * np.log(nz))", "out[i] = -np.sum(nz * np.log2(nz))"),
     "kl_sign_flipped": ("np.stack([ce, ce - hp, hp, hw]", "np.stack([ce, hp - ce, hp, hw]"),
     "model_entropy_of_target": ("hw = attention_entropy(w)", "hw = attention_entropy(p)"),
