@@ -322,9 +322,9 @@ def bench_loss(torch, hh, wl, w, K, W, dev):
     return {"ms_total": ms, "K": K, "counts": loss_counts(w)}
 
 
-def bench_grad(torch, hh, wl, w, K, W, dev):
+def bench_grad(torch, hh, wl, w, K, W, dev, kind=None):
     x = wl.make_inputs(w, seed=500, device=dev)
-    fm = _fm(hh, w, x)
+    fm = _fm(hh, w, x, kind)
     need = hh.loss_grad_workspace_bytes(fm, w.torch_dtype, w.B, w.H, w.n)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     fns = [lambda: hh.mimicry_loss_grad(fm, x["q"], x["k"], workspace=ws)]
@@ -588,25 +588,27 @@ def other_rows(torch, hh, wl, dev, peaks, l2):
             rows["loss:" + name] = {"error": repr(e)}
         torch.cuda.empty_cache()
 
-    for name in ("llama2_prefill_1x32x4096_d128", "gpt2_prefill_8x12x1024_d64"):
+    for key, name, kind in (("grad", "llama2_prefill_1x32x4096_d128", None),
+                            ("grad", "gpt2_prefill_8x12x1024_d64", None),
+                            ("softmax_grad", "gpt2_prefill_8x12x1024_d64", "hedgehog_softmax")):
         try:
             w = wl.WORKLOADS[name]
-            r = bench_grad(torch, hh, wl, w, 5, 2, dev)
+            r = bench_grad(torch, hh, wl, w, 5, 2, dev, kind)
             s = r["ms_total"] / 1e3 / r["K"]
             c = r["counts"]
-            rows["grad:" + name] = {"ms_per_call": s * 1e3, "pairs_per_s": c["pairs"] / s,
+            rows[key + ":" + name] = {"ms_per_call": s * 1e3, "pairs_per_s": c["pairs"] / s,
                                     "tensor_frac_alg": c["flops"] / s / 1e12 / peaks["bf16_tflops"],
                                     "tensor_frac_executed":
                                         c["flops_executed"] / s / 1e12 / peaks["bf16_tflops"]}
         except Exception as e:
-            rows["grad:" + name] = {"error": repr(e)}
+            rows[key + ":" + name] = {"error": repr(e)}
         torch.cuda.empty_cache()
     return rows
 
 
 def run_row(args):
     """One hot-path row alone (for profiling): prefill:, softmax_prefill:, loss:,
-    grad:<workload>, or decode."""
+    grad:, softmax_grad:<workload>, or decode."""
     import torch
     import softmax_mimicking_feature_gb300 as hh
     from softmax_mimicking_feature_gb300 import workloads as wl
@@ -628,9 +630,10 @@ def run_row(args):
         r = bench_loss(torch, hh, wl, w, args.steps, args.warmup, dev)
         s = r["ms_total"] / 1e3 / args.steps
         out = {"row": args.row, "us_per_call": s * 1e6, "pairs_per_s": r["counts"]["pairs"] / s}
-    elif kind == "grad":
+    elif kind in ("grad", "softmax_grad"):
         w = wl.WORKLOADS[name]
-        r = bench_grad(torch, hh, wl, w, args.steps, args.warmup, dev)
+        r = bench_grad(torch, hh, wl, w, args.steps, args.warmup, dev,
+                       "hedgehog_softmax" if kind == "softmax_grad" else None)
         s = r["ms_total"] / 1e3 / args.steps
         out = {"row": args.row, "us_per_call": s * 1e6, "pairs_per_s": r["counts"]["pairs"] / s}
     elif kind == "decode":

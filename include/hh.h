@@ -273,8 +273,13 @@ HH_API size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64
  * gradient w.r.t. Wq, bq summed over the batch (overwritten, not accumulated).
  * With a separate key map (fmap->Wk set and != Wq) dWk [H][d][d] and dbk [H][d]
  * receive the key-side gradient and must be non-NULL; with one shared map both
- * sides are summed into dWq, dbq and dWk, dbk are ignored.  Hedgehog only
- * (Taylor has no parameters: HH_ERR_UNSUPPORTED); d a multiple of 8, at most 128.
+ * sides are summed into dWq, dbq and dWk, dbk are ignored.
+ * Softmax map (HH_FMAP_HEDGEHOG_SOFTMAX, Choice 4, Eq. 5: no bias): each half
+ * goes through the softmax Jacobian instead,
+ *   dL/dh = phi_+ (dL/dphi_+ - <dL/dphi_+, phi_+>) - phi_- (dL/dphi_- - <dL/dphi_-, phi_->),
+ * only dWq (and dWk) are written and dbq, dbk are ignored (may be NULL).
+ * Hedgehog maps only (Taylor has no parameters: HH_ERR_UNSUPPORTED); d a
+ * multiple of 8, at most 128.
  * workspace: at least hh_loss_grad_workspace_bytes(...) bytes. */
 HH_API hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q,
                                       const void* k, int64_t B, int H, int64_t n, float* dWq,

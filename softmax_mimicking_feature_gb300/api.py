@@ -260,14 +260,16 @@ def mimicry_loss_grad(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
 
     Returns (dWq, dbq, dWk, dbk), float32, summed over the batch; dWk, dbk are
     None when the keys share the query map (both sides are then in dWq, dbq).
+    The softmax map has no bias: dbq and dbk are None for it.
     """
     B, H, n, d = _dims(fm, q)
     dev = q.device
     separate = fm.Wk is not None and fm.Wk.data_ptr() != fm.Wq.data_ptr()
+    bias = fm.kind != "hedgehog_softmax"
     dWq = torch.empty(H, d, d, dtype=torch.float32, device=dev)
-    dbq = torch.empty(H, d, dtype=torch.float32, device=dev)
+    dbq = torch.empty(H, d, dtype=torch.float32, device=dev) if bias else None
     dWk = torch.empty_like(dWq) if separate else None
-    dbk = torch.empty_like(dbq) if separate else None
+    dbk = torch.empty(H, d, dtype=torch.float32, device=dev) if separate and bias else None
     need = loss_grad_workspace_bytes(fm, q.dtype, B, H, n)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

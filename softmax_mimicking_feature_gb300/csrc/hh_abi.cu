@@ -432,7 +432,7 @@ static GradWs loss_grad_ws(const Problem& p) {
 size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H, int64_t n) {
   Problem p;
   if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
-  if (p.kind != HH_FMAP_HEDGEHOG || p.softmax || B * H * n == 0) return 0;
+  if (p.kind != HH_FMAP_HEDGEHOG || B * H * n == 0) return 0;
   return loss_grad_ws(p).total;
 }
 
@@ -443,11 +443,12 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   Problem p;
   hh_status st = make_problem(fmap, dtype, B, H, n, &p);
   if (st != HH_OK) return st;
-  if (p.kind != HH_FMAP_HEDGEHOG || p.softmax || p.d % 8 != 0 || p.d > 128)
-    return HH_ERR_UNSUPPORTED;
+  if (p.kind != HH_FMAP_HEDGEHOG || p.d % 8 != 0 || p.d > 128) return HH_ERR_UNSUPPORTED;
   const bool separate = fmap->Wk && fmap->Wk != fmap->Wq;
-  if (!dWq || !dbq || (separate && (!dWk || !dbk))) return HH_ERR_INVALID_ARG;
+  const bool bias = !p.softmax;   // the softmax map has no bias, so no db
+  if (!dWq || (bias && !dbq) || (separate && (!dWk || (bias && !dbk)))) return HH_ERR_INVALID_ARG;
   if (!separate) dWk = dbk = nullptr;
+  if (!bias) dbq = dbk = nullptr;
   if (B * n > 0 && (!q || !k)) return HH_ERR_INVALID_ARG;
   if ((st = check_ptrs_aligned({q, k, dWq, dbq, dWk, dbk, p.Wq, p.bq, p.Wk, p.bk, workspace})) !=
       HH_OK)
@@ -460,7 +461,7 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   const size_t wbytes = sizeof(float) * H * p.d * p.d, bbytes = sizeof(float) * H * p.d;
   if (B * n == 0) {   // empty sum: zero gradient
     cudaError_t e = cudaMemsetAsync(dWq, 0, wbytes, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dbq, 0, bbytes, s);
+    if (e == cudaSuccess && dbq) e = cudaMemsetAsync(dbq, 0, bbytes, s);
     if (e == cudaSuccess && dWk) e = cudaMemsetAsync(dWk, 0, wbytes, s);
     if (e == cudaSuccess && dbk) e = cudaMemsetAsync(dbk, 0, bbytes, s);
     return cuda_status(e);

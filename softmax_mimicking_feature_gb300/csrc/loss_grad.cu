@@ -9,6 +9,8 @@
 //   dL/dh = dL/dphi_+ * e^h - dL/dphi_- * e^-h   (phi = [e^h; e^-h], "The Hedgehog
 //   MLP Feature Map", Choices 1 and 3)
 //   dL/dW = sum_x x^T dL/dh(x),  dL/db = sum_x dL/dh(x)
+// For the softmax map (Choice 4, Eq. 5, no bias) the step to dL/dh is the
+// softmax Jacobian of each half instead, and there is no db (write_dh).
 // Three CUDA-core kernels, fp32 arithmetic on phi(q), phi(k) precomputed by
 // the feature-map kernel:
 //   grad_query_kernel: per 32-query tile, a first sweep over the keys gives the
@@ -89,19 +91,34 @@ __device__ inline void pair(const float* qs, const float* pqs, const float* ks, 
 // dL/dh of the tile's rows: each thread parks its dL/dphi slots (features
 // slot + 8 i) in scratch [kT][dpp] (the streamed-feature buffer, free once
 // the sweep is done), then combines dL/dphi_+ e^h - dL/dphi_- e^-h.
-__device__ inline void write_dh(const float (&acc)[32], float* scratch, const float* px, int r,
-                                int slot, int d, int dpp, int64_t rows_left, float* dh) {
+// Softmax map (Choice 4, Eq. 5; px holds phi_+ = softmax(h), phi_- =
+// softmax(-h)): each half goes through the softmax Jacobian,
+//   dL/dh = phi_+ (dL/dphi_+ - <dL/dphi_+, phi_+>) - phi_- (dL/dphi_- - <dL/dphi_-, phi_->),
+// with the 2 kT row dots in `dots` (the g tile, also free by then).
+__device__ inline void write_dh(const float (&acc)[32], float* scratch, const float* px,
+                                float* dots, int r, int slot, int d, int dpp, int64_t rows_left,
+                                bool softmax, float* dh) {
   const int nf = dpp / 8;
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < 32; ++i)
     if (i < nf) scratch[r * dpp + slot + 8 * i] = acc[i];
   __syncthreads();
+  if (softmax) {
+    if (threadIdx.x < 2 * kT) {
+      const int rr = threadIdx.x >> 1, f0 = (threadIdx.x & 1) * d;
+      float s = 0.f;
+      for (int f = f0; f < f0 + d; ++f) s = fmaf(scratch[rr * dpp + f], px[rr * dpp + f], s);
+      dots[threadIdx.x] = s;
+    }
+    __syncthreads();
+  }
   for (int e = threadIdx.x; e < kT * d; e += kThreads) {
     const int rr = e / d, f = e % d;
-    if (rr < rows_left)
-      dh[(int64_t)rr * d + f] =
-          scratch[rr * dpp + f] * px[rr * dpp + f] - scratch[rr * dpp + f + d] * px[rr * dpp + f + d];
+    if (rr >= rows_left) continue;
+    const float cp = softmax ? dots[2 * rr] : 0.f, cn = softmax ? dots[2 * rr + 1] : 0.f;
+    dh[(int64_t)rr * d + f] = (scratch[rr * dpp + f] - cp) * px[rr * dpp + f] -
+                              (scratch[rr * dpp + f + d] - cn) * px[rr * dpp + f + d];
   }
 }
 
@@ -110,7 +127,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_query_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
     const T* __restrict__ phk, float* __restrict__ stats, float* __restrict__ dhq, int d, int dpp,
-    int64_t n, int ntiles, int H, int G, int seq) {
+    int64_t n, int ntiles, int H, int G, int seq, int softmax) {
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
@@ -191,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) grad_query_kernel(
         if (i < nf) acc[i] = fmaf(gv, pk[slot + 8 * i], acc[i]);
     }
   }
-  write_dh(acc, S.pys, S.pxs, r, slot, d, dpp, n - q0, dhq + (u * n + q0) * d);
+  write_dh(acc, S.pys, S.pxs, S.G, r, slot, d, dpp, n - q0, softmax != 0, dhq + (u * n + q0) * d);
 }
 
 // grid: (U * ceil(n / kT)); block: key tile kt of unit u
@@ -199,7 +216,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_key_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ phq,
     const T* __restrict__ phk, const float* __restrict__ stats, float* __restrict__ dhk, int d,
-    int dpp, int64_t n, int ntiles, int H, int G, int seq) {
+    int dpp, int64_t n, int ntiles, int H, int G, int seq, int softmax) {
   extern __shared__ float sm[];
   const GradSmem S = carve(sm, d, dpp);
   const int64_t u = blockIdx.x / ntiles;
@@ -244,12 +261,12 @@ __global__ void __launch_bounds__(kThreads) grad_key_kernel(
         if (i < nf) acc[i] = fmaf(gv, pq[slot + 8 * i], acc[i]);
     }
   }
-  write_dh(acc, S.pys, S.pxs, r, slot, d, dpp, n - k0, dhk + (u * n + k0) * d);
+  write_dh(acc, S.pys, S.pxs, S.G, r, slot, d, dpp, n - k0, softmax != 0, dhk + (u * n + k0) * d);
 }
 
 // dW[h][a][l] = sum_{b, t} x[b,h,t,a] dh[b,h,t,l] (+ the key side when shared);
 // a side whose x is raw k reads key/value head h / G (kvx1, kvx2),
-// db[h][l] = sum dh.  grid: (H * ceil(d / 32) * ceil(d / 32)), 256 threads:
+// db[h][l] = sum dh (skipped when db is null: the softmax map has no bias).  grid: (H * ceil(d / 32) * ceil(d / 32)), 256 threads:
 // thread -> (a, l) pairs of one 32 x 32 block; tokens in smem chunks of 32.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
@@ -295,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(
   if (a0 + ta < d)
     for (int j = 0; j < 4; ++j)
       if (l0 + tl + j < d) dW[((size_t)h * d + a0 + ta) * d + l0 + tl + j] = acc[j];
-  if (a0 == 0 && ta == 0)
+  if (db && a0 == 0 && ta == 0)
     for (int j = 0; j < 4; ++j)
       if (l0 + tl + j < d) db[(size_t)h * d + l0 + tl + j] = dbacc[j];
 }
@@ -316,11 +333,11 @@ cudaError_t grad_t(const Problem& p, const void* q, const void* k, const void* p
     return e;
   grad_query_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhq, p.d, p.dpp, p.n, ntiles,
-      p.H, p.G, p.seq_major);
+      p.H, p.G, p.seq_major, p.softmax ? 1 : 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   grad_key_kernel<T><<<(unsigned)(U * ntiles), kThreads, smem, s>>>(
       (const T*)q, (const T*)k, (const T*)phq, (const T*)phk, stats, dhk, p.d, p.dpp, p.n, ntiles,
-      p.H, p.G, p.seq_major);
+      p.H, p.G, p.seq_major, p.softmax ? 1 : 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_grad_reduce(p, q, k, dhq, dhk, dWq, dbq, dWk, dbk, s);
 }

@@ -26,6 +26,11 @@
 //   dL/dW = X^T dL/dh,  dL/db = 1^T dL/dh
 // written to a per-CTA partial; grad_partials_kernel sums the partials of each
 // head in a fixed order.
+// Softmax map (Choice 4, Eq. 5: phi_+ = softmax(h), phi_- = softmax(-h), no
+// bias): dL/dh = phi_+ (dPhi_+ - <dPhi_+, phi_+>) - phi_- (dPhi_- - <dPhi_-,
+// phi_->), the softmax Jacobian of each half.  The two warps that share a row
+// each hold half of its columns; they swap their partial dots through shared
+// memory before forming dL/dh.  There is no db.
 
 #include <math.h>
 #include <string.h>
@@ -59,6 +64,7 @@ struct GradArgs {
   int NT;                // 128-row tiles per sequence
   int npad;              // NT * 128
   float s_scale;         // log2(e) / sqrt(d)
+  int softmax;           // phi(X), phi(Y) are the softmax map
 };
 
 template <int D>
@@ -84,6 +90,9 @@ struct GradCfg {
   static constexpr uint32_t DH_BYTES = kRT * D * 2;
   static constexpr uint32_t OFF_ONES = OFF_Y;
   static_assert(2 * DH_BYTES <= 3 * PY_BYTES, "dh tiles exceed the phi(Y) stages");
+  // softmax map: per-row partial dots [2 halves][128 rows] float2, after the dh tiles
+  static constexpr uint32_t OFF_DOT = OFF_PY + 2 * DH_BYTES;
+  static_assert(2 * DH_BYTES + 2 * kRT * 8 <= 3 * PY_BYTES, "row dots exceed the phi(Y) stages");
   static_assert(2 * Y_BYTES >= (D == 64 ? 16384u : 32768u), "ones operand exceeds the Y stages");
   // TMEM columns: S(s) = 128 s, A(s) = 128 s + 64, dPhi = 256 .. 256 + DP.
   // G(s): D = 64 has room for two stages of its own at 384 + 32 s, so S/A of
@@ -339,8 +348,44 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       if (lane == 0) mbar_arrive(bar_g + 8 * s);
     }
     ok = ok && mbar_wait(bar_acc, 0, wp);
+    if (ok) tc_fence_after();
+    // softmax map: the row dots <dPhi_+, phi_+>, <dPhi_-, phi_->, from this
+    // thread's half of the columns and the partner warp's (warp ^ 4)
+    float cp = 0.f, cn = 0.f;
+    if (A.softmax) {
+      float sp = 0.f, sn = 0.f;
+      if (ok) {
+#pragma unroll
+        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+          uint32_t vp[32], vn[32];
+          tmem_ld32x2(tmem + lb + C::TM_ACC + c0, vp, tmem + lb + C::TM_ACC + D + c0, vn);
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            const int fp = c0 + 8 * q8, fn = D + c0 + 8 * q8;
+            const uint4 pp = *reinterpret_cast<const uint4*>(
+                sm + C::OFF_PX + (fp >> 6) * 16384 + sw128_chunk(row, (fp & 63) >> 3));
+            const uint4 pn = *reinterpret_cast<const uint4*>(
+                sm + C::OFF_PX + (fn >> 6) * 16384 + sw128_chunk(row, (fn & 63) >> 3));
+            const uint32_t wpp[4] = {pp.x, pp.y, pp.z, pp.w}, wpn[4] = {pn.x, pn.y, pn.z, pn.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int e = 8 * q8 + 2 * w;
+              sp = fmaf(__uint_as_float(vp[e]), bf16_lo(wpp[w]), sp);
+              sp = fmaf(__uint_as_float(vp[e + 1]), bf16_hi(wpp[w]), sp);
+              sn = fmaf(__uint_as_float(vn[e]), bf16_lo(wpn[w]), sn);
+              sn = fmaf(__uint_as_float(vn[e + 1]), bf16_hi(wpn[w]), sn);
+            }
+          }
+        }
+      }
+      float2* dots = reinterpret_cast<float2*>(sm + C::OFF_DOT);
+      dots[half * kRT + row] = make_float2(sp, sn);
+      named_bar_sync(2, 256);
+      const float2 o = dots[(half ^ 1) * kRT + row];
+      cp = sp + o.x;   // the same sum on both warps: addition commutes
+      cn = sn + o.y;
+    }
     if (ok) {
-      tc_fence_after();
       // dL/dh of this row's half of the columns -> bf16 hi + lo tiles
 #pragma unroll
       for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
@@ -358,10 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const int e = 8 * q8 + 2 * w;
-            const float d0 = __uint_as_float(vp[e]) * bf16_lo(wpp[w]) -
-                             __uint_as_float(vn[e]) * bf16_lo(wpn[w]);
-            const float d1 = __uint_as_float(vp[e + 1]) * bf16_hi(wpp[w]) -
-                             __uint_as_float(vn[e + 1]) * bf16_hi(wpn[w]);
+            const float d0 = (__uint_as_float(vp[e]) - cp) * bf16_lo(wpp[w]) -
+                             (__uint_as_float(vn[e]) - cn) * bf16_lo(wpn[w]);
+            const float d1 = (__uint_as_float(vp[e + 1]) - cp) * bf16_hi(wpp[w]) -
+                             (__uint_as_float(vn[e + 1]) - cn) * bf16_hi(wpn[w]);
             const uint32_t h = pack_bf16(d0, d1);
             hw[e / 2] = h;
             lw[e / 2] = pack_bf16(d0 - bf16_lo(h), d1 - bf16_hi(h));
@@ -488,7 +533,7 @@ __global__ void grad_partials_kernel(const float* __restrict__ part, float* __re
   float* dW = out ? dW1 : dW0;
   float* db = out ? db1 : db0;
   if (e < D * D) dW[(size_t)h * D * D + e] = acc;
-  else db[(size_t)h * D + (e - D * D)] = acc;
+  else if (db) db[(size_t)h * D + (e - D * D)] = acc;   // null: the softmax map has no bias
 }
 
 template <int D>
@@ -525,6 +570,7 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   a.NT = ceil_div(p.n, kRT);
   a.npad = a.NT * kRT;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
+  a.softmax = p.softmax ? 1 : 0;
   const size_t smem = GradCfg<D>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -4,7 +4,8 @@ The map ("The Hedgehog MLP Feature Map", Choice 4 / Eq. 5, negation block
 normalised the same way, no bias) runs through every call that takes a
 Hedgehog map: feature map, prefill (one- and multi-segment, shared and
 separate key maps, float32), state export + decode, loss.  hh_mimicry_stats
-(CE, KL, H(p), H(w)) is checked for every map kind.  Reference: the fp64
+(CE, KL, H(p), H(w)) is checked for every map kind, and the loss gradient
+through the map's softmax Jacobian (dW only: no bias) against the oracle.  Reference: the fp64
 oracle on the same (bf16-rounded) inputs; tolerances as elsewhere: per-head
 relative L2 <= 5e-3 (bf16 inputs) or 1e-5 (float32)."""
 
@@ -161,9 +162,58 @@ def test_mimicry_stats(case):
     np.testing.assert_allclose(got[..., 0], f64(rows), rtol=1e-5, atol=1e-6)
 
 
-def test_softmax_map_rejects_bias_and_gradient():
+def test_softmax_map_rejects_bias():
     w, x, xd, fm = _setup("d64", 1)
     with pytest.raises(hh.HHError):
         hh.feature_map(hh.FeatureMap("hedgehog_softmax", w.d, xd["W"], xd["b"]), xd["q"])
-    with pytest.raises(hh.HHError):
-        hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
+
+
+def _check_grad(got, ref, tol):
+    assert got[1] is None and got[3] is None   # no bias, no db
+    for g, r in ((got[0], ref[0]), (got[2], ref[2])):
+        if r is None:
+            assert g is None
+            continue
+        assert rel_l2_per_head(f64(g), r, lead=1) <= tol
+        # W + u 1^T leaves the map unchanged: every row of dW sums to zero
+        rs = f64(g).sum(-1)
+        assert np.abs(rs).max() <= 20 * tol * np.abs(f64(g)).max()
+
+
+# tensor-core gradient (bf16, d 64 / 128, several 128-row tiles and a ragged
+# tail), the CUDA-core one (float32; one row), both sides of the loss
+GRAD_CASES = ["d64", "d128", "d64_long", "f32_d64", "d64_n1"]
+
+
+@pytest.mark.parametrize("case", GRAD_CASES)
+def test_softmax_map_loss_gradient(case):
+    w, x, xd, fm = _setup(case, 31)
+    got = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
+    torch.cuda.synchronize()
+    ref = O.loss_grad_causal(f64(x["q"]), f64(x["k"]), f64(x["W"]), None,
+                             kind="hedgehog_softmax")
+    _check_grad(got, ref, _tol(w))
+
+
+@pytest.mark.parametrize("case", ["d64", "d128", "f32_d64"])
+def test_softmax_map_loss_gradient_separate_maps(case):
+    w, x, xd, _ = _setup(case, 41)
+    Wk = wl.make_inputs(w, seed=42)["W"]
+    fm = hh.FeatureMap("hedgehog_softmax", w.d, xd["W"], None, Wk.cuda(), None)
+    got = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
+    torch.cuda.synchronize()
+    ref = O.loss_grad_causal(f64(x["q"]), f64(x["k"]), f64(x["W"]), None, f64(Wk), None,
+                             kind="hedgehog_softmax")
+    _check_grad(got, ref, _tol(w))
+
+
+def test_softmax_map_gradient_descends_the_loss():
+    """A small step against the gradient lowers the kernel's own loss."""
+    w, x, xd, fm = _setup("f32_d64", 51)
+    dW, _, _, _ = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
+    L0 = f64(hh.mimicry_loss(fm, xd["q"], xd["k"])[0]).sum()
+    eta = 1e-4 * L0 / dW.double().square().sum().item()
+    fm2 = hh.FeatureMap("hedgehog_softmax", w.d, (xd["W"] - eta * dW).contiguous())
+    L1 = f64(hh.mimicry_loss(fm2, xd["q"], xd["k"])[0]).sum()
+    # first-order prediction of the drop: eta |dW|^2 = 1e-4 L0
+    assert 0.5e-4 * L0 < L0 - L1 < 2e-4 * L0
