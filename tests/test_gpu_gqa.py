@@ -123,19 +123,25 @@ def test_gqa_loss_and_stats(case):
         assert rel_l2_per_head(f64(st)[..., c], ref[..., c]) <= _tol(w)
 
 
-@pytest.mark.parametrize("case", ["hedgehog_d64_14q2kv", "hedgehog_d128", "f32_d64"])
+@pytest.mark.parametrize("case", ["hedgehog_d64_14q2kv", "hedgehog_d128", "softmax_d64",
+                                  "f32_d64"])
 @pytest.mark.parametrize("separate", [False, True])
 def test_gqa_loss_gradient(case, separate):
     w, x, xd, fm, kind, hkv = _setup(case, 37)
     Wk = bk = None
     if separate:
         x2 = wl.make_inputs(w, seed=38)
-        Wk, bk = x2["W"], x2["b"]
-        fm = hh.FeatureMap("hedgehog", w.d, xd["W"], xd["b"], Wk.cuda(), bk.cuda(), kv_heads=hkv)
+        Wk = x2["W"]
+        if kind == "hedgehog":
+            bk = x2["b"]
+            fm = hh.FeatureMap(kind, w.d, xd["W"], xd["b"], Wk.cuda(), bk.cuda(), kv_heads=hkv)
+        else:
+            fm = hh.FeatureMap(kind, w.d, xd["W"], None, Wk.cuda(), None, kv_heads=hkv)
     got = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
     torch.cuda.synchronize()
-    ref = O.loss_grad_causal(f64(x["q"]), _expand(x["k"], w.H), f64(x["W"]), f64(x["b"]),
-                             None if Wk is None else f64(Wk), None if bk is None else f64(bk))
+    ref = O.loss_grad_causal(f64(x["q"]), _expand(x["k"], w.H), f64(x["W"]), _b(kind, x),
+                             None if Wk is None else f64(Wk), None if bk is None else f64(bk),
+                             kind=kind)
     for i, (g, r) in enumerate(zip(got, ref)):
         if r is None:
             assert g is None

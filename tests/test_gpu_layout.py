@@ -85,7 +85,7 @@ def test_layout_loss_stats_feature_map(case):
     assert torch.equal(phi_s, phi)
 
 
-@pytest.mark.parametrize("case", ["hedgehog_d64", "hedgehog_d128_gqa", "f32_d64"])
+@pytest.mark.parametrize("case", ["hedgehog_d64", "hedgehog_d128_gqa", "softmax_d64", "f32_d64"])
 def test_layout_loss_gradient(case):
     w, x, xd, sq, fm, fs, kind = _maps(case, 45)
     g = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
