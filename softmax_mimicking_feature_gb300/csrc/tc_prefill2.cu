@@ -71,7 +71,10 @@ constexpr uint32_t OFF_E0 = SLOT_BASE + 2 * SLOT_BYTES;
 constexpr uint32_t OFF_BQ = OFF_E0 + 16384;               // float[64]: b * log2(e)
 constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 19 x u64 (20 reserved)
 constexpr uint32_t OFF_TM = OFF_BAR + 160;
-constexpr uint32_t SMEM_BYTES = OFF_TM + 16 + 1024;
+// softmax map: the q and k offsets of each slot's tile ([2 slots][q, k][128] float2),
+// copied in with the slot's V
+constexpr uint32_t OFF_OFS = OFF_TM + 16;
+constexpr uint32_t SMEM_BYTES = OFF_OFS + 2 * 2048 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // leading-byte offsets from the V and S_bf16 blocks to their e0 / z2 blocks:
 // positive and within the descriptor's 14-bit field (16-byte units)
@@ -178,9 +181,15 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
   };
   auto load_v = [&](int i) {
     const int s = i & 1;
-    mbar_expect_tx(bar(B_LDV + s), 16384);
+    mbar_expect_tx(bar(B_LDV + s), SM ? 16384 + 2048 : 16384);
     tma_load_rows(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, ub,
                   kh, A.seq);
+    if constexpr (SM) {
+      // the tile's 128 q and 128 k offsets (rows past n are padding, never used)
+      const size_t r = (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE;
+      bulk_load(sb + OFF_OFS + s * 2048, A.offq + r, 1024, bar(B_LDV + s));
+      bulk_load(sb + OFF_OFS + s * 2048 + 1024, A.offk + r, 1024, bar(B_LDV + s));
+    }
   };
   if (warp == 8 && lane == 0) {
     mbar_expect_tx(bar(B_W), 8192u);
@@ -373,10 +382,13 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
       float2 oq = make_float2(0.f, 0.f), ok_ = make_float2(0.f, 0.f);
       if constexpr (SM) {
+        // the offsets came in with V(i), long landed by now; the slot's next V
+        // load waits for G3(i), which runs after this phase
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_LDV + s), par, wp))) { good = false; return; }
         if (valid) {
-          const size_t r = (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE + row;
-          oq = A.offq[r];
-          ok_ = A.offk[r];
+          const float2* os = reinterpret_cast<const float2*>(sm + OFF_OFS + s * 2048);
+          oq = os[row];
+          ok_ = os[TILE + row];
         }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + s), par, wp))) { good = false; return; }
