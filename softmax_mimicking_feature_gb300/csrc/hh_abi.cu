@@ -290,7 +290,9 @@ static hh_status fwd_impl(const hh_fmap* fmap, int dtype, const void* q, const v
   p.z0 = z0;
   const TcPlan pl = plan_prefill_tc(p);
   if (pl.supported) {
-    if (p.softmax) {
+    // the shared-map d = 64 output pass forms the softmax-map offsets itself;
+    // every other output pass, and the segment-state pass, reads them
+    if (p.softmax && !(p.d == 64 && !p.Wk && pl.P == 1)) {
       // per-row offsets of the softmax map, from the feature-map kernel
       char* ob = (char*)workspace + align256(pl.ws_bytes);
       float2* offq = (float2*)ob;

@@ -71,10 +71,10 @@ constexpr uint32_t OFF_E0 = SLOT_BASE + 2 * SLOT_BYTES;
 constexpr uint32_t OFF_BQ = OFF_E0 + 16384;               // float[64]: b * log2(e)
 constexpr uint32_t OFF_BAR = OFF_BQ + 256;                // 19 x u64 (20 reserved)
 constexpr uint32_t OFF_TM = OFF_BAR + 160;
-// softmax map: the q and k offsets of each slot's tile ([2 slots][q, k][128] float2),
-// copied in with the slot's V
-constexpr uint32_t OFF_OFS = OFF_TM + 16;
-constexpr uint32_t SMEM_BYTES = OFF_OFS + 2 * 2048 + 1024;
+// softmax map: per-row partial maxima, then sums, swapped between the two warps
+// that hold a row's column halves ([2 slots][2 halves][128 rows] float4)
+constexpr uint32_t OFF_XCH = OFF_TM + 16;
+constexpr uint32_t SMEM_BYTES = OFF_XCH + 2 * 4096 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // leading-byte offsets from the V and S_bf16 blocks to their e0 / z2 blocks:
 // positive and within the descriptor's 14-bit field (16-byte units)
@@ -93,8 +93,6 @@ struct Args2 {
   float* S_out;
   float* z_out;
   const float* bias;
-  const float2* offq;   // softmax map: [U][NT*128] per-row offsets (log2 units) of q and k
-  const float2* offk;
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -109,8 +107,8 @@ __device__ __forceinline__ uint32_t lane_base(int warp) {
 
 // The bound of 384 threads caps registers at 168 per thread: warps 0, 4, 8
 // (and 1, 5, 9) share one SM sub-partition's 16K registers.
-// SM: softmax-over-features map, phi = [exp(h - c+); exp(-h - c-)] with the
-// per-row offsets from offq / offk (no bias).
+// SM: softmax-over-features map, phi = [exp(h - c+); exp(-h - c-)] (no bias),
+// the per-row offsets c+- = logsumexp(+-h) formed in the exponential phase.
 template <bool SM>
 __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_constant__ Args2 A) {
   extern __shared__ uint8_t smem_raw[];
@@ -181,15 +179,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
   };
   auto load_v = [&](int i) {
     const int s = i & 1;
-    mbar_expect_tx(bar(B_LDV + s), SM ? 16384 + 2048 : 16384);
+    mbar_expect_tx(bar(B_LDV + s), 16384);
     tma_load_rows(sb + slot_off(s) + S_V, &A.tv, bar(B_LDV + s), 0, (t_begin + i) * TILE, ub,
                   kh, A.seq);
-    if constexpr (SM) {
-      // the tile's 128 q and 128 k offsets (rows past n are padding, never used)
-      const size_t r = (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE;
-      bulk_load(sb + OFF_OFS + s * 2048, A.offq + r, 1024, bar(B_LDV + s));
-      bulk_load(sb + OFF_OFS + s * 2048 + 1024, A.offk + r, 1024, bar(B_LDV + s));
-    }
   };
   if (warp == 8 && lane == 0) {
     mbar_expect_tx(bar(B_W), 8192u);
@@ -381,16 +373,6 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       const uint32_t base = sb + slot_off(s);
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
       float2 oq = make_float2(0.f, 0.f), ok_ = make_float2(0.f, 0.f);
-      if constexpr (SM) {
-        // the offsets came in with V(i), long landed by now; the slot's next V
-        // load waits for G3(i), which runs after this phase
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_LDV + s), par, wp))) { good = false; return; }
-        if (valid) {
-          const float2* os = reinterpret_cast<const float2*>(sm + OFF_OFS + s * 2048);
-          oq = os[row];
-          ok_ = os[TILE + row];
-        }
-      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + s), par, wp))) { good = false; return; }
       tc_fence_after();
       // H_Q and H_K columns [32c, 32c+32) of this warp's rows, one wait for both
@@ -408,6 +390,26 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
           hk[4 * q + e] = __float_as_uint(fmaf(__uint_as_float(hk[4 * q + e]), kLog2e, bb[e]));
         }
       }
+      // softmax map: the row offsets c+- = log2 sum_l 2^(+-a_l), a = h log2 e, of
+      // this row of Q and of K, each as max + log2 sum 2^(. - max).  The row's
+      // 64 columns sit in two warps (c = 0, 1); each posts its partial maxima,
+      // then its partial sums, in this slot's exchange area (slot i & 1: the
+      // pair's barriers of E1(i + 1) order the reuse) and adds the partner's.
+      float4 mx4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4* xch = reinterpret_cast<float4*>(sm + OFF_XCH + s * 4096);
+      if constexpr (SM) {
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = __uint_as_float(hv[j]), y = __uint_as_float(hk[j]);
+          m0 = fmaxf(m0, x);
+          m1 = fmaxf(m1, -x);
+          m2 = fmaxf(m2, y);
+          m3 = fmaxf(m3, -y);
+        }
+        mx4 = make_float4(m0, m1, m2, m3);
+        xch[c * TILE + row] = mx4;
+      }
       // phi(Q) overwrites H_Q in place, and phi(K) below the y slab E3(i-2)
       // staged in these rows of panel 0: wait for both warps of these lanes to
       // hold their H_Q columns and for the slab's store to have read it
@@ -416,6 +418,27 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
       tc_fence_before();
       named_bar_sync(2 + g, 64);
       tc_fence_after();
+      if constexpr (SM) {
+        const float4 o = xch[(c ^ 1) * TILE + row];
+        mx4 = make_float4(fmaxf(mx4.x, o.x), fmaxf(mx4.y, o.y), fmaxf(mx4.z, o.z),
+                          fmaxf(mx4.w, o.w));
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = __uint_as_float(hv[j]), y = __uint_as_float(hk[j]);
+          s0 += ex2_approx(x - mx4.x);
+          s1 += ex2_approx(-x - mx4.y);
+          s2 += ex2_approx(y - mx4.z);
+          s3 += ex2_approx(-y - mx4.w);
+        }
+        named_bar_sync(2 + g, 64);   // the partner has read the maxima
+        xch[c * TILE + row] = make_float4(s0, s1, s2, s3);
+        named_bar_sync(2 + g, 64);
+        const float4 o2 = xch[(c ^ 1) * TILE + row];
+        // own + partner on both warps: the same sums (addition commutes)
+        oq = make_float2(mx4.x + __log2f(s0 + o2.x), mx4.y + __log2f(s1 + o2.y));
+        ok_ = make_float2(mx4.z + __log2f(s2 + o2.z), mx4.w + __log2f(s3 + o2.w));
+      }
       // phi(Q): H_Q columns [32c, 32c+32) -> packed columns [16c, +16) (exp(+h))
       // and [32 + 16c, +16) (exp(-h)), one half at a time
 #pragma unroll
@@ -622,9 +645,6 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
   a.S_out = S_out;
   a.z_out = z_out;
   a.bias = p.bq;
-  a.offq = p.offq;
-  a.offk = p.offk;
-  if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
