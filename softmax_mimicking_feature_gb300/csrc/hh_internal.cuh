@@ -30,6 +30,7 @@ struct Problem {
   // from h = x W read the offsets, in log2 units (c * log2 e), from offq /
   // offk, set once they have been computed: pairs [U][off_stride(n)] (rows
   // padded to whole 128-row tiles, so a tile's offsets start 16-byte aligned).
+  // The shared-map d = 64 output pass forms its own and reads neither.
   bool softmax = false;
   const float2* offq = nullptr;
   const float2* offk = nullptr;
