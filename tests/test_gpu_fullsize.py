@@ -1,5 +1,8 @@
 """Parity at the full benchmark sizes, in the configuration bench.py times.
 
+The GPT-2-shaped workload is checked on every output: the prefill with both
+Hedgehog maps and the loss gradient (dW, db) with both.
+
 Where the oracle is too slow for every output, sampled rows are computed one
 by one from the definition (row i needs tokens 0..i only); the decode workload
 is also checked GPU-against-GPU over all sequences: a 2048-token prefill
@@ -90,6 +93,40 @@ def test_llama_loss_sampled_rows():
     # the head sums are the row sums, and every row obeys L_i >= 0 (Gibbs)
     np.testing.assert_allclose(f64(head), Lg.sum(-1), rtol=1e-5)
     assert np.all(Lg > -1e-3) and abs(Lg[0, :, 0]).max() < 1e-3
+
+
+def test_gpt2_softmax_map_prefill_all_rows():
+    """The softmax-over-features map at the benchmark size: the d = 64 output
+    pass forms every row's offsets itself."""
+    w = wl.WORKLOADS["gpt2_prefill_8x12x1024_d64"]
+    x = wl.make_inputs(w, seed=3)
+    xd = {k: t.cuda() for k, t in x.items()}
+    fm = hh.FeatureMap("hedgehog_softmax", w.d, xd["W"])
+    y = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"])
+    torch.cuda.synchronize()
+    ref = O.fwd_causal("hedgehog_softmax", f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["W"]))
+    assert rel_l2_per_head(f64(y), ref) <= BF16_TOL
+
+
+@pytest.mark.parametrize("kind", ["hedgehog", "hedgehog_softmax"])
+def test_gpt2_loss_gradient(kind):
+    """dW (and db) of the summed loss over all 96 heads of the benchmark size,
+    against the oracle's chain rule; db of bf16 inputs at its own bound."""
+    from tests._util import DB_TOL_BF16
+    w = wl.WORKLOADS["gpt2_prefill_8x12x1024_d64"]
+    x = wl.make_inputs(w, seed=4)
+    xd = {k: t.cuda() for k, t in x.items()}
+    soft = kind == "hedgehog_softmax"
+    fm = hh.FeatureMap(kind, w.d, xd["W"], None if soft else xd["b"])
+    got = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
+    torch.cuda.synchronize()
+    ref = O.loss_grad_causal(f64(x["q"]), f64(x["k"]), f64(x["W"]), None if soft else f64(x["b"]),
+                             kind=kind)
+    assert rel_l2_per_head(f64(got[0]), ref[0], lead=1) <= BF16_TOL
+    if soft:
+        assert got[1] is None and ref[1] is None
+    else:
+        assert rel_l2_per_head(f64(got[1]), ref[1], lead=1) <= DB_TOL_BF16
 
 
 def test_decode_after_prefill_equals_long_prefill():
