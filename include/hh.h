@@ -10,7 +10,8 @@
  *                  phi_t2(x) = [1, x, (x_i x_j / sqrt 2)_{i,j}]       (R^d -> R^{1+d+d^2})
  *                  ("The Taylor Exponential as a Bridge Result")
  *   causal output  y_i = sum_{j<=i} (phi(q_i).phi(k_j)) v_j / sum_{j<=i} phi(q_i).phi(k_j)
- *                  (section 2, paper Eq. 2; running sums S, z in "Complexity Analysis")
+ *                  ("2. Context and Motivation", paper Eq. 2; running sums S, z
+ *                  in "Complexity Analysis")
  *   mimicry loss   L_i = -sum_{j<=i} softmax_j(q_i.k_j / sqrt d) log(a_ij / sum_{m<=i} a_im),
  *                  a_ij = phi(q_i).phi(k_j)
  *                  ("The Attention Weight Distillation Loss", paper Eq. 4)
@@ -163,7 +164,9 @@ HH_API hh_status hh_fwd_plan(const hh_fmap* fmap, int dtype, int64_t B, int H, i
                              int chunk, int* segments, int* launches);
 
 /* Causal linear attention over whole sequences (chunked prefill).
- * Source: section 2 (paper Eq. 2) for y; "Complexity Analysis" for the
+ * Source: "The Hedgehog & the Porcupine: Expressive Linear Attentions with
+ * Softmax Mimicry", section "2. Context and Motivation" (the linear-attention
+ * equation for y_i, paper Eq. 2); "Complexity Analysis" for the
  * running sums S_i = sum_{j<=i} phi(k_j)^T v_j and z_i = sum_{j<=i} phi(k_j).
  * q, k, v: [B][H][n][d] (dtype); y: [B][H][n][d] (dtype), overwritten.
  * chunk: 0 (library default), 64 or 128 -- the intra-chunk block length of
@@ -184,14 +187,21 @@ HH_API hh_status hh_linattn_fwd_causal(const hh_fmap* fmap, int dtype, const voi
  * device memory when they run the prefill (a plugin interface that only
  * passes its input and output buffers, a serving loop that forbids allocation
  * after start-up, a C host program without a device allocator).  Arguments
- * and results are those of hh_linattn_fwd_causal.
+ * and results are those of hh_linattn_fwd_causal, and they are checked in the
+ * same order (pointers, alignment and shapes, then the device) before the
+ * size check below.
  * Scratch: a fixed 16 MiB device array inside the library, present on every
  * GPU that loads the library until the process exits.  A problem needing more
  * scratch than that (hh_fwd_workspace_bytes > 16 MiB) returns
- * HH_ERR_WORKSPACE and launches nothing.  The first call on each device looks
- * up the array's address once; make it before any stream capture.  All calls
- * share the array: calls that overlap on the GPU race and must not be issued.
- * Nothing is allocated by this call. */
+ * HH_ERR_WORKSPACE and launches nothing.
+ * First call: with CUDA's lazy module loading, the first call in a context
+ * that needs scratch loads the library's device module, whose 16 MiB array is
+ * then committed; that call can fail for lack of device memory
+ * (HH_ERR_CUDA).  It also looks up the array's address, once per device and
+ * CUDA context (a call in a new context, e.g. after cudaDeviceReset, looks it
+ * up again); make it before any stream capture.  After it, no call allocates.
+ * All calls share the array: calls that overlap on the GPU race and must not
+ * be issued. */
 HH_API hh_status hh_linattn_fwd_causal_noalloc(const hh_fmap* fmap, int dtype, const void* q,
                                                const void* k, const void* v, int64_t B, int H,
                                                int64_t n, int chunk, void* y, float* S_out,

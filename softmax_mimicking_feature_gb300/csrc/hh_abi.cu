@@ -155,6 +155,33 @@ size_t loss_ws(const Problem& p) {
 }  // namespace
 }  // namespace hh
 
+namespace hh {
+
+// Host-side argument checks of the prefill, in the order the entry points
+// apply them (the workspace itself is not looked at).  Nothing touches a
+// device.  On HH_OK, *p describes the problem.
+hh_status fwd_check_args(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                         const void* v, int64_t B, int H, int64_t n, int chunk, const float* S0,
+                         const float* z0, const void* y, const float* S_out, const float* z_out,
+                         const void* workspace, const int* dev_status, Problem* p) {
+  hh_status st = make_problem(fmap, dtype, B, H, n, p);
+  if (st != HH_OK) return st;
+  if (chunk != 0 && chunk != 64 && chunk != 128) return HH_ERR_UNSUPPORTED;
+  if ((S_out == nullptr) != (z_out == nullptr)) return HH_ERR_INVALID_ARG;
+  if (S0 != nullptr && !z0) return HH_ERR_INVALID_ARG;
+  if (B == 0) return HH_OK;
+  if (n > 0 && (!q || !k || !v || !y)) return HH_ERR_INVALID_ARG;
+  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, S0, z0, p->Wq, p->bq, p->Wk, p->bk,
+                                workspace})) != HH_OK)
+    return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
+  return HH_OK;
+}
+
+bool device_is_supported() { return device_ok(); }
+
+}  // namespace hh
+
 using namespace hh;
 
 extern "C" {
@@ -251,18 +278,11 @@ static hh_status fwd_impl(const hh_fmap* fmap, int dtype, const void* q, const v
                           const float* z0, void* y, float* S_out, float* z_out, void* workspace,
                           size_t ws_bytes, int* dev_status, void* stream) {
   Problem p;
-  hh_status st = make_problem(fmap, dtype, B, H, n, &p);
+  hh_status st = fwd_check_args(fmap, dtype, q, k, v, B, H, n, chunk, S0, z0, y, S_out, z_out,
+                                workspace, dev_status, &p);
   if (st != HH_OK) return st;
-  if (chunk != 0 && chunk != 64 && chunk != 128) return HH_ERR_UNSUPPORTED;
-  if ((S_out == nullptr) != (z_out == nullptr)) return HH_ERR_INVALID_ARG;
-  const bool from_state = S0 != nullptr;
-  if (from_state && !z0) return HH_ERR_INVALID_ARG;
   if (B == 0) return HH_OK;
-  if (n > 0 && (!q || !k || !v || !y)) return HH_ERR_INVALID_ARG;
-  if ((st = check_ptrs_aligned({q, k, v, y, S_out, z_out, S0, z0, p.Wq, p.bq, p.Wk, p.bk,
-                                workspace})) != HH_OK)
-    return st;
-  if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
+  const bool from_state = S0 != nullptr;
   const size_t need = fwd_ws_bytes(fmap, dtype, B, H, n, from_state);
   if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;

@@ -77,6 +77,15 @@ __host__ __device__ __forceinline__ int64_t row_of(int b, int h, int64_t t, int 
 // Row stride of the softmax-map offset arrays.
 inline int64_t off_stride(int64_t n) { return (n + 127) / 128 * 128; }
 
+// Host-side argument checks shared by the prefill entry points (pointers,
+// alignment, shapes; the workspace size is not checked).  No device work.
+hh_status fwd_check_args(const hh_fmap* fmap, int dtype, const void* q, const void* k,
+                         const void* v, int64_t B, int H, int64_t n, int chunk, const float* S0,
+                         const float* z0, const void* y, const float* S_out, const float* z_out,
+                         const void* workspace, const int* dev_status, Problem* p);
+// Whether the current device runs this library's kernels (sm_103).
+bool device_is_supported();
+
 // Cached device attributes (the only state the library keeps).
 int device_sm_count();
 int device_max_smem_optin();

@@ -5,7 +5,7 @@
 //
 // Math follows "The Hedgehog & the Porcupine" summary: Choices 1/3 of "The
 // Hedgehog MLP Feature Map", "The Taylor Exponential as a Bridge Result",
-// section 2 / paper Eq. 2 and "Complexity Analysis" for the causal output,
+// "2. Context and Motivation" (paper Eq. 2) and "Complexity Analysis" for the causal output,
 // and "The Attention Weight Distillation Loss" (paper Eq. 4).
 
 #include <math.h>

@@ -1,6 +1,6 @@
 // Chunked causal linear attention on the 5th-generation tensor cores.
 //
-// "The Hedgehog & the Porcupine" summary: section 2 (paper Eq. 2) defines
+// "The Hedgehog & the Porcupine" summary: "2. Context and Motivation" (paper Eq. 2) defines
 //   y_i = phi(q_i) sum_{j<=i} phi(k_j)^T v_j / phi(q_i) sum_{j<=i} phi(k_j),
 // "Complexity Analysis" the running sums S = sum phi(k)^T v and z = sum phi(k);
 // the map is "The Hedgehog MLP Feature Map" (Choices 1 and 3).  This file holds

@@ -1,6 +1,6 @@
 // Chunked causal prefill for Hedgehog d = 64 with two tiles in flight.
 //
-// Same mathematics as prefill_tc_kernel (section 2 / paper Eq. 2 and
+// Same mathematics as prefill_tc_kernel ("2. Context and Motivation", paper Eq. 2, and
 // "Complexity Analysis" of "The Hedgehog & the Porcupine" summary; the map of
 // "The Hedgehog MLP Feature Map", Choices 1 and 3), reorganised so that the
 // serial chain of one 128-token tile overlaps the next tile's:

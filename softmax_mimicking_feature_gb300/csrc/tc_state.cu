@@ -3,7 +3,7 @@
 // For each segment of a (batch, head) sequence it writes
 //   S_seg = sum_j phi(k_j)^T v_j   and   z_seg = sum_j phi(k_j)
 // over the segment's tokens: the running sums of "Complexity Analysis" in
-// "The Hedgehog & the Porcupine" summary (section 2, paper Eq. 2), for the
+// "The Hedgehog & the Porcupine" summary ("2. Context and Motivation", paper Eq. 2), for the
 // Hedgehog map ("The Hedgehog MLP Feature Map", Choices 1 and 3) or the
 // degree-2 Taylor map ("The Taylor Exponential as a Bridge Result").  The
 // output pass starts segment s from the inclusive scan of segments < s.

@@ -4,7 +4,7 @@
 // gives phi(x) = [1, x, vec(x x^T) / sqrt2], so phi(q) . phi(k) = 1 + s + s^2/2
 // with s = q . k.  The intra-tile scores therefore need one K = 16 MMA of
 // Q K^T and two FMAs per element instead of a 288-deep feature contraction;
-// the running state (section 2, paper Eq. 2; "Complexity Analysis") still
+// the running state ("2. Context and Motivation", paper Eq. 2; "Complexity Analysis") still
 // needs features, kept as the 160 packed features of taylor_pack.cuh (the 136
 // unordered pairs carry the same dot products as the 256 ordered ones):
 //   Sc(t) = Q_t K_t^T                         -> P = bf16(tril(1 + Sc + Sc^2/2))

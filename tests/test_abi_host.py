@@ -126,3 +126,32 @@ def test_workspace_queries_are_consistent(L):
     b = L.hh_loss_workspace_bytes(ctypes.byref(fm), 1, 2, 3, 200)
     assert 0 < a < b and a % 256 == 0
     assert L.hh_loss_workspace_bytes(ctypes.byref(fm), 1, 2, 3, 0) == 0
+
+
+def _noalloc(L, fm, q=P(256), k=P(512), v=P(768), B=1, H=32, n=1 << 20, y=P(1024), st=None):
+    return L.hh_linattn_fwd_causal_noalloc(ctypes.byref(fm), 1, q, k, v, B, H, n, 0, y, None,
+                                           None, st, None)
+
+
+def test_noalloc_checks_arguments_before_its_size(L, monkeypatch):
+    # a problem far beyond the 16 MiB scratch (63 segment states of 32 heads
+    # at d = 128): bad pointers are still reported as such, not as a
+    # workspace shortage
+    monkeypatch.setenv("HH_PREFILL_SEGMENTS", "64")
+    fm = _fm(d=128)
+    assert L.hh_fwd_workspace_bytes(ctypes.byref(fm), 1, 1, 32, 1 << 20, 0) > 16 << 20
+    assert _noalloc(L, fm, q=None) == _abi.HH_ERR_INVALID_ARG
+    assert _noalloc(L, fm, k=P(520)) == _abi.HH_ERR_ALIGNMENT
+    assert _noalloc(L, fm, st=P(1026)) == _abi.HH_ERR_ALIGNMENT
+    assert _noalloc(L, _fm(d=96)) == _abi.HH_ERR_UNSUPPORTED
+    assert _noalloc(L, fm, B=0) == _abi.HH_OK
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="with a device present the call would be enqueued")
+def test_noalloc_without_a_supported_device_is_unsupported(L):
+    # valid arguments and no sm_103 device: the device check comes before the
+    # size check and before any lookup of the scratch array
+    assert _noalloc(L, _fm(d=128)) == _abi.HH_ERR_UNSUPPORTED
+    assert _noalloc(L, _fm(d=128), n=300) == _abi.HH_ERR_UNSUPPORTED
+

@@ -6,8 +6,10 @@ the prefill's workspace.  This entry point keeps that scratch in a fixed
 device array inside the library.  The test calls it through the C ABI, twice
 in a row on different inputs, and checks each result against the ordinary
 entry point (which is given a freshly allocated workspace) within the usual
-bf16 tolerance; it also checks that a problem needing more scratch than the
-array holds is refused before anything runs.
+bf16 tolerance.  The first call loads the array; the test checks that the
+second call leaves the device's free memory unchanged, i.e. allocates
+nothing.  It also checks that a problem needing more scratch than the array
+holds is refused before anything runs.
 """
 
 import ctypes
@@ -46,7 +48,7 @@ def _noalloc(fm, q, k, v, y, S, z, status):
 def test_noalloc_matches_the_allocating_entry_point_twice():
     w = wl.WORKLOADS["llama2_prefill_1x32x4096_d128"].with_(B=1, H=8, n=1500)
     fm_inputs = [wl.make_inputs(w, seed=s, device="cuda") for s in (71, 72)]
-    for x in fm_inputs:
+    for call, x in enumerate(fm_inputs):
         fm = hh.FeatureMap("hedgehog", w.d, x["W"], x["b"])
         segs, _ = hh.fwd_plan(fm, torch.bfloat16, w.B, w.H, w.n, 64)
         assert segs > 1, "the case must use the scratch"
@@ -54,7 +56,13 @@ def test_noalloc_matches_the_allocating_entry_point_twice():
         S = torch.empty(w.B, w.H, 2 * w.d, w.d, dtype=torch.float32, device="cuda")
         z = torch.empty(w.B, w.H, 2 * w.d, dtype=torch.float32, device="cuda")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         assert _noalloc(fm, x["q"], x["k"], x["v"], y, S, z, status) == _abi.HH_OK
+        torch.cuda.synchronize()
+        if call > 0:
+            # the array was loaded by the first call; this one allocates nothing
+            assert torch.cuda.mem_get_info()[0] == free_before
         y_ref, S_ref, z_ref = hh.linattn_fwd_causal(fm, x["q"], x["k"], x["v"], chunk=64,
                                                     return_state=True)
         torch.cuda.synchronize()
