@@ -136,7 +136,7 @@ def feature_map(kind: str, x, W=None, b=None) -> np.ndarray:
 def causal_weights(phi_q, phi_k) -> np.ndarray:
     """Row-normalised linear-attention weights a_ij / sum_{m<=i} a_im, j <= i.
 
-    HH summary, section 2 (the kernel form, paper Eq. 2): the unnormalised
+    HH summary, "2. Context and Motivation" (the kernel form, paper Eq. 2): the unnormalised
     weight of key j for query i is phi(q_i) . phi(k_j); entries above the
     diagonal are zero.  ``phi_q``, ``phi_k``: [n, d'] -> [n, n].
     """
@@ -148,7 +148,7 @@ def causal_weights(phi_q, phi_k) -> np.ndarray:
 def linattn_quadratic(phi_q, phi_k, v) -> np.ndarray:
     """Quadratic (brute-force) causal linear attention for one head.
 
-    HH summary, section 2 and "Complexity Analysis" (paper Eq. 2):
+    HH summary, "2. Context and Motivation" and "Complexity Analysis" (paper Eq. 2):
     y_i = sum_{j<=i} (phi(q_i).phi(k_j)) v_j / sum_{j<=i} phi(q_i).phi(k_j).
     ``phi_q``, ``phi_k``: [n, d']; ``v``: [n, d] -> y [n, d].
     """
@@ -253,7 +253,7 @@ def mimicry_loss_rows(q, k, phi_q, phi_k, rows) -> np.ndarray:
     return out
 
 
-def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
+def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None, kind="hedgehog", feature_rounding=None):
     """Gradient of sum_i L_i (paper Eq. 4, one head) w.r.t. the Hedgehog map.
 
     HH summary, "The Attention Weight Distillation Loss": only the feature-map
@@ -276,6 +276,11 @@ def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
         dL/dh = phi_+ * (dL/dphi_+ - <dL/dphi_+, phi_+>)
               - phi_- * (dL/dphi_- - <dL/dphi_-, phi_->).
     b and bk are ignored and dbq, dbk are returned as None.
+
+    feature_rounding: None, or a function applied to phi(q) and phi(k) right
+    after the map, so that every later step uses the rounded features (an
+    error-budget experiment: rounding them to the storage precision of a
+    kernel's operands); the arithmetic is otherwise unchanged.
     """
     q, k = _f64(q), _f64(k)
     d = q.shape[-1]
@@ -294,6 +299,8 @@ def mimicry_loss_grad(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
         hk = k @ Wk_ + bk_
         pq = np.concatenate([np.exp(hq), np.exp(-hq)], axis=-1)
         pk = np.concatenate([np.exp(hk), np.exp(-hk)], axis=-1)
+    if feature_rounding is not None:
+        pq, pk = _f64(feature_rounding(pq)), _f64(feature_rounding(pk))
     n = q.shape[0]
     mask = np.tril(np.ones((n, n), dtype=bool))
     a = pq @ pk.T
@@ -404,7 +411,7 @@ def stats_causal(kind, q, k, W=None, b=None):
     return out
 
 
-def loss_grad_causal(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
+def loss_grad_causal(q, k, W, b, Wk=None, bk=None, kind="hedgehog", feature_rounding=None):
     """Gradient of the loss summed over [B, H, n] w.r.t. per-head maps.
 
     Returns (dWq [H, d, d], dbq [H, d], dWk, dbk), each summed over the batch.
@@ -424,7 +431,8 @@ def loss_grad_causal(q, k, W, b, Wk=None, bk=None, kind="hedgehog"):
             g = mimicry_loss_grad(q[bi, h], k[bi, h], _f64(W)[h],
                                   None if soft else _f64(b)[h],
                                   None if Wk is None else _f64(Wk)[h],
-                                  None if (bk is None or soft) else _f64(bk)[h], kind=kind)
+                                  None if (bk is None or soft) else _f64(bk)[h], kind=kind,
+                                  feature_rounding=feature_rounding)
             dWq[h] += g[0]
             dWk[h] += g[2]
             if not soft:

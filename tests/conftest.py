@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -18,3 +19,21 @@ def golden():
     import json
     with open(os.path.join(ROOT, "tests", "golden", "hand_worked.json")) as f:
         return json.load(f)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The largest relative L2 error each test measured (parity margins)."""
+    from tests import _util
+    per = {}
+    for test, val in _util.MEASURED:
+        per[test] = max(per.get(test, 0.0), val)
+    if not per:
+        return
+    terminalreporter.write_sep("-", "largest relative L2 error measured, per test")
+    for test in sorted(per):
+        terminalreporter.write_line(f"{per[test]:.3e}  {test}")
+    path = os.environ.get("HH_ERROR_REPORT")
+    if path:
+        with open(path, "w") as f:
+            json.dump(per, f, indent=1, sort_keys=True)
+
