@@ -161,6 +161,13 @@ cudaError_t launch_prefill_out_d64(const Problem& p, const TcPlan& pl, const voi
                                    float* z_out, const void* ws, const float* init,
                                    int* dev_status, cudaStream_t s);
 
+// Output pass of the d = 128 Hedgehog prefill (shared map): warp-specialised,
+// phi(K) built with the hidden units on the TMEM lanes.
+cudaError_t launch_prefill_out_d128(const Problem& p, const TcPlan& pl, const void* q,
+                                    const void* k, const void* v, void* y, float* S_out,
+                                    float* z_out, const void* ws, const float* init,
+                                    int* dev_status, cudaStream_t s);
+
 // Output pass of the Taylor (d = 16) prefill: scores from the closed form
 // 1 + s + s^2/2 with s = q . k, state contractions on the features.
 cudaError_t launch_prefill_out_taylor(const Problem& p, const TcPlan& pl, const void* q,

@@ -752,6 +752,8 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   } else {
     if (D == 64 && !p.Wk)
       return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
+    if constexpr (D == 128)
+      return launch_prefill_out_d128(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
     PrefillArgs a;
     memset(&a, 0, sizeof(a));
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
