@@ -4,9 +4,9 @@
 //   y_i = phi(q_i) sum_{j<=i} phi(k_j)^T v_j / phi(q_i) sum_{j<=i} phi(k_j),
 // "Complexity Analysis" the running sums S = sum phi(k)^T v and z = sum phi(k);
 // the map is "The Hedgehog MLP Feature Map" (Choices 1 and 3).  This file holds
-// the planning, the scan and the generic output pass (d = 128, and d = 64 with
-// a separate key map); the shared-map d = 64 pass is tc_prefill2.cu, the
-// Taylor pass tc_taylor.cu, the state passes tc_state.cu.
+// the planning, the scan and the generic output pass (d = 64 with a separate
+// key map); the shared-map d = 64 pass is tc_prefill2.cu, the d = 128 pass
+// tc_prefill128.cu, the Taylor pass tc_taylor.cu, the state passes tc_state.cu.
 //
 // Evaluation order (per 128-token tile t of one (batch, head) sequence segment):
 //   H_Q = Q_t W, H_K = K_t W                          (tcgen05)
@@ -717,8 +717,9 @@ TcPlan plan_prefill_tc(const Problem& p) {
 }
 
 // Initial state (continuation), segment-state pass and scan, then the output
-// pass of the map: the Taylor and the shared-map d = 64 passes have kernels of
-// their own, the rest (d = 128, separate key maps) runs prefill_tc_kernel.
+// pass of the map: the Taylor, the shared-map d = 64 and the d = 128 passes
+// have kernels of their own; d = 64 with a separate key map runs
+// prefill_tc_kernel.
 template <int KIND, int D>
 static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q, const void* k,
                                const void* v, void* y, float* S_out, float* z_out, void* ws,
@@ -752,44 +753,46 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   } else {
     if (D == 64 && !p.Wk)
       return launch_prefill_out_d64(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
-    if constexpr (D == 128)
+    if constexpr (D == 128) {
       return launch_prefill_out_d128(p, pl, q, k, v, y, S_out, z_out, ws, init, dev_status, s);
-    PrefillArgs a;
-    memset(&a, 0, sizeof(a));
-    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-    bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major) &&
-              make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
-              make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
-              make_plane_map(&a.twq, p.Wq, D, D, p.H, 64, D, sw) &&
-              make_plane_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, sw) &&
-              make_rows_map(&a.ty, y, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major);
-    if (!ok) return cudaErrorInvalidValue;
-    a.ws = reinterpret_cast<float*>(ws);
-    a.init = init;
-    a.S_out = S_out;
-    a.z_out = z_out;
-    a.bq = p.bq;
-    a.bk = p.Wk ? p.bk : p.bq;
-    a.offq = p.offq;
-    a.offk = p.offk;
-    if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
-    a.dev_status = dev_status;
-    a.soft_ns = wait_soft_limit_ns();
-    a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
-    a.n = p.n;
-    a.H = p.H;
-    a.P = pl.P;
-    a.L = pl.L;
-    a.NT = pl.NT;
-    a.sep_wk = p.Wk ? 1 : 0;
-    a.G = p.G;
-    a.seq = p.seq_major;
-    const size_t smem = Smem<D>::ALLOC;
-    auto kern = prefill_tc_kernel<D>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3((unsigned)(U * pl.P)), dim3(kThreads), smem, s, a);
+    } else {
+      PrefillArgs a;
+      memset(&a, 0, sizeof(a));
+      const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+      bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major) &&
+                make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
+                make_rows_map(&a.tv, v, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
+                make_plane_map(&a.twq, p.Wq, D, D, p.H, 64, D, sw) &&
+                make_plane_map(&a.twk, p.Wk ? p.Wk : p.Wq, D, D, p.H, 64, D, sw) &&
+                make_rows_map(&a.ty, y, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major);
+      if (!ok) return cudaErrorInvalidValue;
+      a.ws = reinterpret_cast<float*>(ws);
+      a.init = init;
+      a.S_out = S_out;
+      a.z_out = z_out;
+      a.bq = p.bq;
+      a.bk = p.Wk ? p.bk : p.bq;
+      a.offq = p.offq;
+      a.offk = p.offk;
+      if (p.softmax && (!p.offq || !p.offk)) return cudaErrorInvalidValue;
+      a.dev_status = dev_status;
+      a.soft_ns = wait_soft_limit_ns();
+      a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
+      a.n = p.n;
+      a.H = p.H;
+      a.P = pl.P;
+      a.L = pl.L;
+      a.NT = pl.NT;
+      a.sep_wk = p.Wk ? 1 : 0;
+      a.G = p.G;
+      a.seq = p.seq_major;
+      const size_t smem = Smem<D>::ALLOC;
+      auto kern = prefill_tc_kernel<D>;
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(kern, dim3((unsigned)(U * pl.P)), dim3(kThreads), smem, s, a);
+    }
   }
 }
 
