@@ -60,6 +60,7 @@ struct GradArgs {
   uint64_t soft_ns, hard_ns;
   int64_t n, U;
   int H, G;              // heads; query heads per key/value head
+  int HG;                // (batch, head) units per scheduling group
   int seq;               // q, k are [B][n][H][D]
   int NT;                // 128-row tiles per sequence
   int npad;              // NT * 128
@@ -157,10 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
   // bar_acc is reused for the final dW / db product (phase 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heavy tiles first, the two sides interleaved
-  const int side = blockIdx.x & 1;
-  const int rank = (int)((blockIdx.x >> 1) / A.U);
-  const int64_t unit = (blockIdx.x >> 1) % A.U;
+  // Units in groups of HG; within a group heavy tiles first, the two sides
+  // interleaved.  The CTAs in flight then stream the rows of a few heads
+  // only, which stay in L2 across that group's tiles.
+  const int64_t GT = 2 * (int64_t)A.HG * A.NT;
+  const int64_t grp = blockIdx.x / GT, within = blockIdx.x % GT;
+  const int64_t gsz = min((int64_t)A.HG, A.U - grp * A.HG);
+  const int side = (int)(within & 1);
+  const int rank = (int)((within >> 1) / gsz);
+  const int64_t unit = grp * A.HG + (within >> 1) % gsz;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
@@ -566,6 +572,17 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   a.U = (int64_t)U;
   a.H = p.H;
   a.G = p.G;
+  // scheduling groups: q, k and their features (bf16, 3D values per token
+  // each) of a group's heads within about a third of the L2
+  {
+    const double per_unit = (double)p.n * 6.0 * D * 2.0;
+    const int64_t hg = std::max<int64_t>(1, (int64_t)(40e6 / std::max(per_unit, 1.0)));
+    // equal groups (the largest divisor of U within the budget), so that no
+    // short group runs its heavy tiles last
+    int64_t g = std::min<int64_t>((int64_t)U, hg);
+    while ((int64_t)U % g) --g;
+    a.HG = (int)g;
+  }
   a.seq = p.seq_major;
   a.NT = ceil_div(p.n, kRT);
   a.npad = a.NT * kRT;

@@ -251,6 +251,7 @@ struct LossArgs {
   int64_t U;
   int NT;
   int H, G;            // heads; query heads per key/value head
+  int HG;              // (batch, head) units per scheduling group
   int seq;             // q, k are [B][n][H][D]
   float s_scale;       // log2(e) / sqrt(d)
 };
@@ -295,9 +296,15 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heavy query tiles first: block b -> query tile NT-1 - b / U
-  const int qt = A.NT - 1 - (int)(blockIdx.x / A.U);
-  const int64_t unit = blockIdx.x % A.U;
+  // Units are taken in groups of HG, each group's query tiles heavy first:
+  // the CTAs in flight at any time then read the keys of a few heads only,
+  // whose K and phi(K) stay in L2 while every query tile of those heads
+  // streams them (all heads at once would not fit).
+  const int64_t GT = (int64_t)A.HG * A.NT;
+  const int64_t grp = blockIdx.x / GT, within = blockIdx.x % GT;
+  const int64_t gsz = min((int64_t)A.HG, A.U - grp * A.HG);
+  const int qt = A.NT - 1 - (int)(within / gsz);
+  const int64_t unit = grp * A.HG + within % gsz;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
@@ -643,6 +650,17 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.NT = ceil_div(p.n, kTile);
   a.H = p.H;
   a.G = p.G;
+  // scheduling groups: the K and phi(K) of a group's heads (bf16, 3D values
+  // per token) within about a third of the L2
+  {
+    const double per_unit = (double)p.n * 3.0 * D * 2.0;
+    const int64_t hg = std::max<int64_t>(1, (int64_t)(40e6 / std::max(per_unit, 1.0)));
+    // equal groups (the largest divisor of U within the budget), so that no
+    // short group runs its heavy tiles last
+    int64_t g = std::min<int64_t>((int64_t)U, hg);
+    while ((int64_t)U % g) --g;
+    a.HG = (int)g;
+  }
   a.seq = p.seq_major;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   const size_t smem = LossCfg<D>::ALLOC;
