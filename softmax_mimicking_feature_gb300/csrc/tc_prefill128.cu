@@ -9,9 +9,11 @@
 // At d = 128 the fp32 state S [256 x 128] alone takes half of the tensor
 // memory, so one 128-token tile is in flight.  The pass is organised to keep
 // that tile's chain short:
-//   warp 8 (MMA issuer) issues every group as soon as its inputs are ready,
-//   warp 9 (loads and stores) moves tiles by TMA,
-//   warps 0-7 (epilogue) run the CUDA-core phases.
+//   warp 16 (MMA issuer) issues every group as soon as its inputs are ready,
+//   warp 17 (loads and stores) moves tiles by TMA,
+//   warps 0-15 (epilogue) run the CUDA-core phases, four warps per TMEM lane
+//   quarter, each on a quarter of the columns (the phases are latency-bound,
+//   so more warps with less work each finish them sooner).
 // Per tile t (groups G on the tensor pipe, phases E on the epilogue), in the
 // order of the chain:
 //   G1K  H_K^T = W^T K_t^T        hidden units on the TMEM lanes, tokens on columns
@@ -62,7 +64,9 @@ using namespace tc;
 
 namespace p128 {
 constexpr int D = 128, DP = 256, TILE = 128;
-constexpr int kThreads = 320;   // warps 0-7 epilogue, warp 8 MMA issue, warp 9 loads / stores
+constexpr int kEpi = 16;                 // epilogue warps 0-15
+constexpr int kMmaWarp = kEpi, kLoadWarp = kEpi + 1;
+constexpr int kThreads = 32 * (kEpi + 2);
 
 // TMEM columns
 constexpr uint32_t TM_S = 0;     // S: block c (internal features 128c..) x 128 columns at 128 c
@@ -84,11 +88,13 @@ constexpr uint32_t OFF_SB = OFF_Q;              // S_bf16 [256 features][128]: 2
 constexpr uint32_t OFF_SB1 = OFF_SB + 32768;    //   its second panel
 constexpr uint32_t OFF_OK = OFF_SB1;            // float2[128] key offsets of the tile (softmax
                                                 //   map), read before the snapshot overwrites them
+constexpr uint32_t OFF_ZT = OFF_SB1 + 1024;     // float[4][256] column sums of phi(K) per token
+                                                //   quarter, likewise before the snapshot
 constexpr uint32_t OFF_V = OFF_SB + 65536;      // V tile: 2 panels [128 tokens x 64]; then y
 constexpr uint32_t OFF_PHK = OFF_V + 32768;     // phi(K) [256 features][128 tokens]: 2 panels
                                                 // [256 x 64]; then P (2 panels [128 x 64])
-constexpr uint32_t OFF_DQ = OFF_PHK + 32768;    // float[2][128] phi(q) . z partials  } upper half of
-constexpr uint32_t OFF_RS = OFF_DQ + 1024;      // float[2][128] row sums of P        } phi(K), P's time
+constexpr uint32_t OFF_DQ = OFF_PHK + 32768;    // float[4][128] phi(q) . z partials  } upper half of
+constexpr uint32_t OFF_RS = OFF_DQ + 2048;      // float[4][128] row sums of P        } phi(K), P's time
 constexpr uint32_t OFF_Z = OFF_PHK + 65536;     // float[256] z before the tile (internal order)
 constexpr uint32_t OFF_BS = OFF_Z + 1024;       // float[128] b * log2(e)
 constexpr uint32_t OFF_BAR = OFF_BS + 512;
@@ -132,11 +138,11 @@ __device__ __forceinline__ int internal_feature(int u, int s) {
   return 4 * (u >> 1) + 2 * s + (u & 1);
 }
 
-// The bound of 384 threads caps registers at 168 per thread: warps 0, 4, 8
-// (and 1, 5, 9) share one SM sub-partition's registers.
+// The bound of 640 threads caps registers at 96 per thread: five warps (0, 4,
+// 8, 12, 16 and 1, 5, 9, 13, 17) share one SM sub-partition's registers.
 // SM: softmax-over-features map (offsets from the feature-map kernel).
 template <bool SM>
-__global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_constant__ Args128 A) {
+__global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_constant__ Args128 A) {
   using namespace p128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -147,6 +153,7 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 4);
   float* z_s = reinterpret_cast<float*>(sm + OFF_Z);
+  float* zt_s = reinterpret_cast<float*>(sm + OFF_ZT);
   float* dq_s = reinterpret_cast<float*>(sm + OFF_DQ);
   float* rs_s = reinterpret_cast<float*>(sm + OFF_RS);
   float* bs_s = reinterpret_cast<float*>(sm + OFF_BS);
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
     for (int b = 0; b < B_COUNT; ++b) {
       const bool by_warps =
           b == B_E1K || b == B_E1Q || b == B_E1S || b == B_E2A || b == B_E2B || b == B_E3;
-      mbar_init(bar(b), by_warps ? 8 : 1);
+      mbar_init(bar(b), by_warps ? kEpi : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       tma_prefetch_rows(&A.tv, 64 * x, r0, ub, kh, A.seq);
     }
   };
-  if (warp == 9 && lane == 0 && nt > 0) {
+  if (warp == kLoadWarp && lane == 0 && nt > 0) {
     mbar_expect_tx(bar(B_W), D * D * 2);
     for (int x = 0; x < 2; ++x) tma_load_3d(sb + OFF_W + x * 16384, &A.tw, bar(B_W), 64 * x, 0, uh);
     load_k(0);
@@ -233,14 +240,16 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
 
   // initial state: the prefix of the preceding segments, the given initial
   // state (continuation, first segment) or zeros; public -> internal order
-  if (warp < 8) {
-    const int c = warp >> 2, r = 32 * (warp & 3) + lane;
+  // warp w: lane quarter w % 4, column quarter w / 4: feature row 128 c + r
+  // (c = w / 8) and state columns [64 ((w / 4) % 2), +64)
+  if (warp < kEpi) {
+    const int q = warp >> 2, c = q >> 1, r = 32 * (warp & 3) + lane;
     const int fp = public_feature(128 * c + r);
     const size_t per = (size_t)DP * D + DP;
     const float* prefix = seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * per
                                   : (A.init ? A.init + (size_t)unit * per : nullptr);
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 64 * (q & 1); c0 < 64 * (q & 1) + 64; c0 += 32) {
       uint32_t v[32];
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
@@ -253,14 +262,14 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       }
       tmem_st32(tmem + lane_base(warp) + TM_S + 128 * c + c0, v);
     }
-    z_s[128 * c + r] = prefix ? __ldcg(prefix + (size_t)DP * D + fp) : 0.f;
+    if ((q & 1) == 0) z_s[128 * c + r] = prefix ? __ldcg(prefix + (size_t)DP * D + fp) : 0.f;
     tmem_st_wait();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     // ======================= MMA issuer =======================
     if (lane == 0 && nt > 0) {
       constexpr uint32_t ID_HKT = idesc_bf16(128, 128, 1, 0);  // W^T[MN-major] K^T[K-major]
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       }
       if (!ok) *(volatile int*)abort_flag = 1;
     }
-  } else if (warp == 9) {
+  } else if (warp == kLoadWarp) {
     // ======================= loads and stores =======================
     //   K (i+1) once G1K(i) has read K(i);
     //   Q (i+1) once G3a(i) has read S_bf16, whose first panel overwrites Q;
@@ -379,11 +388,12 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
     }
   } else {
     // ======================= epilogue warps =======================
-    // Warp w owns TMEM lanes 32 (w % 4).. and half c = w / 4: in E1K hidden
-    // unit j = lane and tokens [64c, +64); elsewhere tile row r = lane and
-    // columns [64c, +64).
-    const int c = warp >> 2;
-    const int r = 32 * (warp & 3) + lane;
+    // Warp w owns TMEM lanes 32 (w % 4).. and column quarter q = w / 4: in E1K
+    // hidden unit j = lane and tokens [32q, +32); elsewhere tile row r = lane
+    // and columns [32q, +32).
+    const int q = warp >> 2;
+    const int g = warp & 3;
+    const int r = 32 * g + lane;
     const uint32_t lb = lane_base(warp);
     const float2* okey = reinterpret_cast<const float2*>(sm + OFF_OK);
     // A wait that gives up (hard time limit) clears `good`: the warp then
@@ -394,6 +404,7 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       good = good && __all_sync(0xffffffffu, mbar_wait(bar(b), par, wp));
       return good;
     };
+    auto epi_sync = [&]() { named_bar_sync(1, 32 * kEpi); };
     for (int i = 0; i < nt; ++i) {
       const uint32_t par = i & 1;
       const int64_t r0 = (int64_t)(t_begin + i) * TILE;
@@ -404,63 +415,63 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       // ---------------- E1K: phi(K) rows of hidden unit j = r ----------------
       // phi(K) overwrites the dq / rs partials of the previous tile: every
       // warp must be past its E3 (G1K no longer waits for E3)
-      if (i > 0) named_bar_sync(1, 256);
+      if (i > 0) epi_sync();
       wait_all(B_G1K, par);
       if (SM) wait_all(B_LDO, par);
       tc_fence_after();
-      // this thread's share of z for its hidden unit: column sums of phi(K) over
-      // the tokens of half c (added to z once every reader of z_before is done)
-      float zp = 0.f, zn = 0.f;
       const int fpos = internal_feature(r, 0), fneg = internal_feature(r, 1);
       if (good) {
         const float bj = bs_s[r];
+        float zp = 0.f, zn = 0.f;
         // two rows per thread; lanes with bit 2 set store their negative row
         // first, so each store's 32 rows cover all eight 16-byte bank groups
         // of the swizzle four times (no extra wavefronts)
         const bool neg_first = (r & 4) != 0;
         const int f0 = neg_first ? fneg : fpos, f1 = neg_first ? fpos : fneg;
-        const uint32_t panel = sb + OFF_PHK + c * 32768;
-#pragma unroll 1
-        for (int t0 = 0; t0 < 64; t0 += 32) {
-          uint32_t hk[32];
-          tmem_ld32(tmem + lb + TM_A(i) + 64 * c + t0, hk);
-          // tokens of this chunk inside the sequence (32 except in the last tile)
-          const int64_t left = A.n - (r0 + 64 * c + t0);
-          const int nv = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
+        const uint32_t panel = sb + OFF_PHK + (q >> 1) * 32768;   // tokens [64 (q/2), +64)
+        uint32_t hk[32];
+        tmem_ld32(tmem + lb + TM_A(i) + 32 * q, hk);
+        // tokens of this quarter inside the sequence (32 except in the last tile)
+        const int64_t left = A.n - (r0 + 32 * q);
+        const int nv = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t wpos[4], wneg[4];
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t wpos[4], wneg[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tt = 8 * q + 2 * e;
-              const float a0 = fmaf(__uint_as_float(hk[tt]), kLog2e, bj);
-              const float a1 = fmaf(__uint_as_float(hk[tt + 1]), kLog2e, bj);
-              uint32_t p, m;
-              if (SM) {
-                const float4 o2 = *reinterpret_cast<const float4*>(okey + 64 * c + t0 + tt);
-                p = pack_bf16(ex2_approx(a0 - o2.x), ex2_approx(a1 - o2.z));
-                m = pack_bf16(ex2_approx(-a0 - o2.y), ex2_approx(-a1 - o2.w));
-              } else {
-                p = pack_bf16(ex2_approx(a0), ex2_approx(a1));
-                m = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
-              }
-              // tokens past the end of the sequence contribute nothing
-              if (tt >= nv) p = m = 0u;
-              else if (tt + 1 >= nv) { p &= 0xFFFFu; m &= 0xFFFFu; }
-              wpos[e] = p;
-              wneg[e] = m;
-              zp += bf16_lo(p) + bf16_hi(p);
-              zn += bf16_lo(m) + bf16_hi(m);
+          for (int e = 0; e < 4; ++e) {
+            const int tt = 8 * qq + 2 * e;
+            const float a0 = fmaf(__uint_as_float(hk[tt]), kLog2e, bj);
+            const float a1 = fmaf(__uint_as_float(hk[tt + 1]), kLog2e, bj);
+            uint32_t p, m;
+            if (SM) {
+              const float4 o2 = *reinterpret_cast<const float4*>(okey + 32 * q + tt);
+              p = pack_bf16(ex2_approx(a0 - o2.x), ex2_approx(a1 - o2.z));
+              m = pack_bf16(ex2_approx(-a0 - o2.y), ex2_approx(-a1 - o2.w));
+            } else {
+              p = pack_bf16(ex2_approx(a0), ex2_approx(a1));
+              m = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
             }
-            const int ch = t0 / 8 + q;   // 16-byte chunk of the 128-byte row
-            st_shared_v4(panel + sw128_chunk(f0, ch), neg_first ? wneg[0] : wpos[0],
-                         neg_first ? wneg[1] : wpos[1], neg_first ? wneg[2] : wpos[2],
-                         neg_first ? wneg[3] : wpos[3]);
-            st_shared_v4(panel + sw128_chunk(f1, ch), neg_first ? wpos[0] : wneg[0],
-                         neg_first ? wpos[1] : wneg[1], neg_first ? wpos[2] : wneg[2],
-                         neg_first ? wpos[3] : wneg[3]);
+            // tokens past the end of the sequence contribute nothing
+            if (tt >= nv) p = m = 0u;
+            else if (tt + 1 >= nv) { p &= 0xFFFFu; m &= 0xFFFFu; }
+            wpos[e] = p;
+            wneg[e] = m;
+            zp += bf16_lo(p) + bf16_hi(p);
+            zn += bf16_lo(m) + bf16_hi(m);
           }
+          const int ch = 4 * (q & 1) + qq;   // 16-byte chunk of the 128-byte row
+          st_shared_v4(panel + sw128_chunk(f0, ch), neg_first ? wneg[0] : wpos[0],
+                       neg_first ? wneg[1] : wpos[1], neg_first ? wneg[2] : wpos[2],
+                       neg_first ? wneg[3] : wpos[3]);
+          st_shared_v4(panel + sw128_chunk(f1, ch), neg_first ? wpos[0] : wneg[0],
+                       neg_first ? wpos[1] : wneg[1], neg_first ? wpos[2] : wneg[2],
+                       neg_first ? wpos[3] : wneg[3]);
         }
+        // this thread's share of z: the column sums of phi(K) for its hidden
+        // unit over its token quarter (added to z once every reader of
+        // z_before is done)
+        zt_s[256 * q + fpos] = zp;
+        zt_s[256 * q + fneg] = zn;
       }
       fence_proxy_async();
       tc_fence_before();
@@ -468,68 +479,68 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       if (good && lane == 0) mbar_arrive(bar(B_E1K));
 
       // ---------------- E1Q: phi(Q) in place, phi(q) . z_before ----------------
-      float dq = 0.f;   // this thread's half of phi(q) . z_before (shared with E3 after G2U)
+      float dq = 0.f;   // this thread's quarter of phi(q) . z_before (shared after G2U)
       wait_all(B_G1Q, par);
       tc_fence_after();
       if (good) {
-        // columns 64c + u, u + 1 (u even) of H_Q become packed columns u
-        // (exp(+h) of both) and u + 1 (exp(-h) of both): internal features
-        // 128c + 2u .. 128c + 2u + 3.  Bias and z are re-read from shared
+        // columns 32q + u, u + 1 (u even) of H_Q become packed columns 32q + u
+        // (exp(+h) of both) and 32q + u + 1 (exp(-h) of both): internal
+        // features 4 (16q + u/2) .. + 3.  Bias and z are re-read from shared
         // memory at their point of use (volatile loads: hoisted, they would
         // cost registers).
-#pragma unroll 1
-        for (int u0 = 0; u0 < 64; u0 += 32) {
-          uint32_t hq[32];
-          tmem_ld32(tmem + lb + TM_B(i) + 64 * c + u0, hq);
-          const uint32_t zaddr = sb + OFF_Z + 4 * (128 * c + 2 * u0);
-          const uint32_t baddr = sb + OFF_BS + 4 * (64 * c + u0);
+        uint32_t hq[32];
+        tmem_ld32(tmem + lb + TM_B(i) + 32 * q, hq);
+        const uint32_t zaddr = sb + OFF_Z + 4 * 64 * q;
+        const uint32_t baddr = sb + OFF_BS + 4 * 32 * q;
 #pragma unroll
-          for (int u = 0; u < 32; u += 4) {
-            const float4 b4 = ld_shared_f4_volatile(baddr + 4 * u);
-            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+        for (int u = 0; u < 32; u += 4) {
+          const float4 b4 = ld_shared_f4_volatile(baddr + 4 * u);
+          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-              const float a0 = fmaf(__uint_as_float(hq[u + e]), kLog2e, bb[e]);
-              const float a1 = fmaf(__uint_as_float(hq[u + e + 1]), kLog2e, bb[e + 1]);
-              const uint32_t p = pack_bf16(ex2_approx(a0 - oq.x), ex2_approx(a1 - oq.x));
-              const uint32_t m = pack_bf16(ex2_approx(-a0 - oq.y), ex2_approx(-a1 - oq.y));
-              hq[u + e] = p;
-              hq[u + e + 1] = m;
-              const float4 zz = ld_shared_f4_volatile(zaddr + 8 * (u + e));
-              dq += bf16_lo(p) * zz.x + bf16_hi(p) * zz.y + bf16_lo(m) * zz.z + bf16_hi(m) * zz.w;
-            }
+          for (int e = 0; e < 4; e += 2) {
+            const float a0 = fmaf(__uint_as_float(hq[u + e]), kLog2e, bb[e]);
+            const float a1 = fmaf(__uint_as_float(hq[u + e + 1]), kLog2e, bb[e + 1]);
+            const uint32_t p = pack_bf16(ex2_approx(a0 - oq.x), ex2_approx(a1 - oq.x));
+            const uint32_t m = pack_bf16(ex2_approx(-a0 - oq.y), ex2_approx(-a1 - oq.y));
+            hq[u + e] = p;
+            hq[u + e + 1] = m;
+            const float4 zz = ld_shared_f4_volatile(zaddr + 8 * (u + e));
+            dq += bf16_lo(p) * zz.x + bf16_hi(p) * zz.y + bf16_lo(m) * zz.z + bf16_hi(m) * zz.w;
           }
-          tmem_st32(tmem + lb + TM_B(i) + 64 * c + u0, hq);
         }
+        tmem_st32(tmem + lb + TM_B(i) + 32 * q, hq);
         tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
       if (good && lane == 0) mbar_arrive(bar(B_E1Q));
 
-      // Every warp is past its reads of z_before (E1Q) and of the key offsets
-      // (E1K), which the snapshot overwrites: z takes the first half's column
-      // sums now, the second half's after the snapshot (a fixed order).
-      named_bar_sync(1, 256);
-      if (good && c == 0) {
-        z_s[fpos] += zp;
-        z_s[fneg] += zn;
+      // Every warp is past its reads of z_before (E1Q) and has written its
+      // column sums: z takes the four token quarters' sums in order; then the
+      // snapshot may overwrite them and the key offsets (same panel).
+      epi_sync();
+      if (good && q < 2) {
+        const int f = 128 * q + r;   // one internal feature per thread of the first half
+        z_s[f] = z_s[f] + ((zt_s[f] + zt_s[256 + f]) + (zt_s[512 + f] + zt_s[768 + f]));
       }
+      epi_sync();
 
       // ---------------- E1S: S_bf16 <- S (the state before this tile) ----------------
-      // over Q, which G1Q (complete) has read; G2U of the previous tile
-      // completed before G1K of this one
+      // feature row 128 (q / 2) + r, columns [64 (q % 2), +64); over Q, which
+      // G1Q (complete) has read; G2U of the previous tile completed before G1K
+      // of this one
       if (good) {
+        const int c = q >> 1;
         const int f = 128 * c + r;
+        const uint32_t panel = sb + OFF_SB + (q & 1) * 32768;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t sv[32];
-          tmem_ld32(tmem + lb + TM_S + 128 * c + c0, sv);
-          const uint32_t panel = sb + OFF_SB + (c0 / 64) * 32768;
+          tmem_ld32(tmem + lb + TM_S + 128 * c + 64 * (q & 1) + c0, sv);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int j = 8 * q4;
-            st_shared_v4(panel + sw128_chunk(f, (c0 % 64) / 8 + q4),
+            st_shared_v4(panel + sw128_chunk(f, c0 / 8 + q4),
                          pack_bf16(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
                          pack_bf16(__uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3])),
                          pack_bf16(__uint_as_float(sv[j + 4]), __uint_as_float(sv[j + 5])),
@@ -541,38 +552,31 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (good && lane == 0) mbar_arrive(bar(B_E1S));
-      named_bar_sync(1, 256);
-      if (good && c == 1) {
-        z_s[fpos] += zp;
-        z_s[fneg] += zn;
-      }
 
       // ---------------- E2: P = bf16(tril(Sc)), row sums ----------------
       wait_all(B_G2S, par);
       tc_fence_after();
       if (good) {
-        uint32_t pw[32];   // keys [64c, +64) of row r as bf16 pairs
+        uint32_t pw[16];   // keys [32q, +32) of row r as bf16 pairs
         float rs = 0.f;
-        if (32 * (warp & 3) + 31 < 64 * c) {
-          // every row of this warp lies above the keys of half c: P = 0
+        if (g < q) {
+          // every row of this warp lies above the keys of quarter q: P = 0
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_E2A));
 #pragma unroll
-          for (int j = 0; j < 32; ++j) pw[j] = 0u;
+          for (int j = 0; j < 16; ++j) pw[j] = 0u;
         } else {
-          uint32_t s0[32], s1[32];
-          tmem_ld32x2(tmem + lb + TM_A(i) + 64 * c, s0, tmem + lb + TM_A(i) + 64 * c + 32, s1);
+          uint32_t sv[32];
+          tmem_ld32(tmem + lb + TM_A(i) + 32 * q, sv);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_E2A));   // Sc is out of A: G3a may overwrite it
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const int key = 64 * c + j;
-            const uint32_t x0 = j < 32 ? s0[j] : s1[j - 32];
-            const uint32_t x1 = j < 32 ? s0[j + 1] : s1[j - 31];
-            const float a0 = key <= r ? __uint_as_float(x0) : 0.f;
-            const float a1 = key + 1 <= r ? __uint_as_float(x1) : 0.f;
+          for (int j = 0; j < 32; j += 2) {
+            const int key = 32 * q + j;
+            const float a0 = key <= r ? __uint_as_float(sv[j]) : 0.f;
+            const float a1 = key + 1 <= r ? __uint_as_float(sv[j + 1]) : 0.f;
             const uint32_t w2 = pack_bf16(a0, a1);
             pw[j / 2] = w2;
             rs += bf16_lo(w2) + bf16_hi(w2);
@@ -581,39 +585,38 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
         // P, and the row's dq and rs partials, over phi(K) once G2U, the last
         // reader of phi(K), has completed
         if (wait_all(B_G2U, par)) {
+          const uint32_t panel = sb + OFF_PHK + (q >> 1) * 16384;   // keys [64 (q/2), +64)
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(sb + OFF_PHK + c * 16384 + sw128_chunk(r, q), pw[4 * q], pw[4 * q + 1],
-                         pw[4 * q + 2], pw[4 * q + 3]);
-          dq_s[128 * c + r] = dq;
-          rs_s[128 * c + r] = rs;
+          for (int qq = 0; qq < 4; ++qq)
+            st_shared_v4(panel + sw128_chunk(r, 4 * (q & 1) + qq), pw[4 * qq], pw[4 * qq + 1],
+                         pw[4 * qq + 2], pw[4 * qq + 3]);
+          dq_s[128 * q + r] = dq;
+          rs_s[128 * q + r] = rs;
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_E2B));
         }
       }
-      named_bar_sync(1, 256);   // every row's dq and rs partials are in shared memory
+      epi_sync();   // every row's dq and rs partials are in shared memory
 
       // ---------------- E3: y = O / den ----------------
       wait_all(B_G3, par);
       tc_fence_after();
       if (good) {
-        const float den = (dq_s[r] + dq_s[128 + r]) + (rs_s[r] + rs_s[128 + r]);
+        const float den = ((dq_s[r] + dq_s[128 + r]) + (dq_s[256 + r] + dq_s[384 + r])) +
+                          ((rs_s[r] + rs_s[128 + r]) + (rs_s[256 + r] + rs_s[384 + r]));
         const float inv = 1.f / den;
-        const uint32_t panel = sb + OFF_V + c * 16384;   // y columns [64c, +64), over V
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lb + TM_A(i) + 64 * c + c0, ov);
+        const uint32_t panel = sb + OFF_V + (q >> 1) * 16384;   // y columns [64 (q/2), +64), over V
+        uint32_t ov[32];
+        tmem_ld32(tmem + lb + TM_A(i) + 32 * q, ov);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int j = 8 * q;
-            st_shared_v4(panel + sw128_chunk(r, c0 / 8 + q),
-                         pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
-                         pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
-                         pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
-                         pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
-          }
+        for (int qq = 0; qq < 4; ++qq) {
+          const int j = 8 * qq;
+          st_shared_v4(panel + sw128_chunk(r, 4 * (q & 1) + qq),
+                       pack_bf16(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv),
+                       pack_bf16(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
+                       pack_bf16(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv),
+                       pack_bf16(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv));
         }
       }
       fence_proxy_async();
@@ -627,13 +630,13 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (A.S_out && seg == A.P - 1 && warp < 8 && nt > 0 && !*(volatile int*)abort_flag) {
+  if (A.S_out && seg == A.P - 1 && warp < kEpi && nt > 0 && !*(volatile int*)abort_flag) {
     // the last G2U is complete: E2 of the last tile waited for it
-    const int c = warp >> 2, r = 32 * (warp & 3) + lane;
+    const int q = warp >> 2, c = q >> 1, r = 32 * (warp & 3) + lane;
     const int fp = public_feature(128 * c + r);
     float4* dst = reinterpret_cast<float4*>(A.S_out + ((size_t)unit * DP + fp) * D);
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 64 * (q & 1); c0 < 64 * (q & 1) + 64; c0 += 32) {
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base(warp) + TM_S + 128 * c + c0, sv);
 #pragma unroll
@@ -641,7 +644,7 @@ __global__ void __launch_bounds__(384, 1) prefill_t128_kernel(const __grid_const
         dst[c0 / 4 + j] = make_float4(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]),
                                       __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
     }
-    A.z_out[(size_t)unit * DP + fp] = z_s[128 * c + r];
+    if ((q & 1) == 0) A.z_out[(size_t)unit * DP + fp] = z_s[128 * c + r];
   }
   tc_fence_before();
   __syncthreads();
