@@ -442,22 +442,27 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
             const int tt = 8 * qq + 2 * e;
             const float a0 = fmaf(__uint_as_float(hk[tt]), kLog2e, bj);
             const float a1 = fmaf(__uint_as_float(hk[tt + 1]), kLog2e, bj);
-            uint32_t p, m;
+            float e0, e1, f0, f1;
             if (SM) {
               const float4 o2 = *reinterpret_cast<const float4*>(okey + 32 * q + tt);
-              p = pack_bf16(ex2_approx(a0 - o2.x), ex2_approx(a1 - o2.z));
-              m = pack_bf16(ex2_approx(-a0 - o2.y), ex2_approx(-a1 - o2.w));
+              e0 = ex2_approx(a0 - o2.x); e1 = ex2_approx(a1 - o2.z);
+              f0 = ex2_approx(-a0 - o2.y); f1 = ex2_approx(-a1 - o2.w);
             } else {
-              p = pack_bf16(ex2_approx(a0), ex2_approx(a1));
-              m = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+              e0 = ex2_approx(a0); e1 = ex2_approx(a1);
+              f0 = ex2_approx(-a0); f1 = ex2_approx(-a1);
             }
             // tokens past the end of the sequence contribute nothing
-            if (tt >= nv) p = m = 0u;
-            else if (tt + 1 >= nv) { p &= 0xFFFFu; m &= 0xFFFFu; }
-            wpos[e] = p;
-            wneg[e] = m;
-            zp += bf16_lo(p) + bf16_hi(p);
-            zn += bf16_lo(m) + bf16_hi(m);
+            if (nv < 32) {
+              if (tt >= nv) e0 = f0 = 0.f;
+              if (tt + 1 >= nv) e1 = f1 = 0.f;
+            }
+            // z sums the fp32 features; the MMA operand is their bf16 rounding
+            // (a relative mismatch of at most 2^-9 per term, inside the output's
+            // own bf16 rounding)
+            zp += e0 + e1;
+            zn += f0 + f1;
+            wpos[e] = pack_bf16(e0, e1);
+            wneg[e] = pack_bf16(f0, f1);
           }
           const int ch = 4 * (q & 1) + qq;   // 16-byte chunk of the 128-byte row
           st_shared_v4(panel + sw128_chunk(f0, ch), neg_first ? wneg[0] : wpos[0],
