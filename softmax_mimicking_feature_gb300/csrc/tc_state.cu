@@ -329,12 +329,19 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 // Hedgehog d = 128: transposed form.  H_K^T = W^T K_t^T lands in TMEM with the
 // 128 hidden units on the lanes and the tile's tokens on the columns; the
-// feature warps overwrite it in place with phi(K_t)^T as bf16 pairs
-// (exp(+h) and exp(-h) blocks), which is directly the A operand of
+// feature warps overwrite it in place with phi(K_t)^T as bf16 pairs, which is
+// directly the A operand of
 //   S[+/-] += phi(K_t)^T[+/-] V_t     (A from TMEM, M = 128 features)
 // so phi(K) never goes through shared memory, and z is a per-thread running
 // sum over the thread's tokens.  Two H buffers let G1(t+1) run while the
-// feature warps work on tile t; warp 8 issues MMAs, warp 9 issues loads.
+// feature warps work on tile t.  Warps 0-15 build the features (warp w: TMEM
+// lane quarter w % 4, token quarter w / 4 of the tile: the exponential phase
+// is latency-bound, so more warps with fewer tokens each finish it sooner);
+// warp 16 issues the MMAs, warp 17 the loads.
+// Packed layout of one H buffer after the feature phase: the 32 tokens of
+// quarter q occupy columns [32 q, +32) before and after, exp(+h) pairs in
+// [32 q, +16) and exp(-h) pairs in [32 q + 16, +16), so each warp rewrites
+// only the columns it has read.
 // ---------------------------------------------------------------------------
 namespace t128 {
 constexpr int D = 128;
@@ -342,8 +349,8 @@ constexpr uint32_t XT = TILE * D * 2;                  // 32 KB
 constexpr uint32_t OFF_W = 0;                          // W: 2 panels [128 i x 64 j]
 constexpr uint32_t OFF_K = 32768;                      // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * XT;             // 2 stages
-constexpr uint32_t OFF_ZX = OFF_V + 2 * XT;            // float[2][128] z exchange
-constexpr uint32_t OFF_OX = OFF_ZX + 1024;             // float2[2][128] softmax-map offsets
+constexpr uint32_t OFF_ZX = OFF_V + 2 * XT;            // float[4][256] z exchange
+constexpr uint32_t OFF_OX = OFF_ZX + 4096;             // float2[2][128] softmax-map offsets
 constexpr uint32_t OFF_BAR = OFF_OX + 2048;
 enum { B_W = 0, B_LDK = 1, B_LDV = 3, B_G1 = 5, B_E1 = 7, B_G2 = 9, B_COUNT = 11 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
@@ -351,12 +358,14 @@ constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
 static_assert(ALLOC <= 227 * 1024, "shared memory");
 constexpr uint32_t TM_S = 0;                           // S+ [0,128), S- [128,256)
 __host__ __device__ constexpr uint32_t TM_H(int b) { return 256 + 128 * b; }
-constexpr int kThreads = 320;
+constexpr int kFeat = 16;                              // feature warps 0-15
+constexpr int kMmaWarp = kFeat, kLoadWarp = kFeat + 1;
+constexpr int kThreads = 32 * (kFeat + 2);
 }  // namespace t128
 
-// The bound of 384 threads caps registers at 168 per thread (warps 0, 4, 8
-// and 1, 5, 9 share one SM sub-partition's registers).
-__global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constant__ StateArgs A) {
+// The bound of 640 threads caps registers at 96 per thread: five warps (0, 4,
+// 8, 12, 16 and 1, 5, 9, 13, 17) share one SM sub-partition's registers.
+__global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constant__ StateArgs A) {
   using namespace t128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -370,7 +379,6 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = blockIdx.x / (A.P - 1);
-  const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int seg = blockIdx.x % (A.P - 1);
@@ -380,7 +388,8 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
 
   if (tid == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(bar(b), (b == B_E1 || b == B_E1 + 1) ? 8 : 1);
+    for (int b = 0; b < B_COUNT; ++b)
+      mbar_init(bar(b), (b == B_E1 || b == B_E1 + 1) ? kFeat : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -408,7 +417,7 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
       bulk_load(sb + OFF_OX + (i & 1) * TILE * 8,
                 A.off + (size_t)unit * A.NT * TILE + (size_t)(t_begin + i) * TILE, TILE * 8, b);
   };
-  if (warp == 8 && lane == 0 && nt > 0) {
+  if (warp == kLoadWarp && lane == 0 && nt > 0) {
     mbar_expect_tx(bar(B_W), D * D * 2);
     for (int x = 0; x < 2; ++x) tma_load_3d(sb + OFF_W + x * 16384, &A.tw, bar(B_W), 64 * x, 0, h);
     for (int i = 0; i < 2 && i < nt; ++i) {
@@ -424,19 +433,21 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) {   // S = 0
+  if (warp < kFeat) {   // S = 0: warp w clears lane quarter w % 4, columns [64 (w / 4), +64)
     uint32_t zr[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) zr[j] = 0u;
-    for (int c0 = 0; c0 < 256; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
+    const uint32_t t0 = tmem + lane_base(warp) + TM_S + 64 * (warp >> 2);
+    tmem_st32(t0, zr);
+    tmem_st32(t0 + 32, zr);
     tmem_st_wait();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  float zp = 0.f, zn = 0.f;   // this thread's share of z (hidden unit j, tokens of its half)
-  if (warp == 8) {
+  float zp = 0.f, zn = 0.f;   // this thread's share of z (hidden unit j, tokens of its quarter)
+  if (warp == kMmaWarp) {
     // ======================= MMA issuer =======================
     if (lane == 0 && nt > 0) {
       constexpr uint32_t ID_H = idesc_bf16(128, 128, 1, 0);   // W^T[MN-major] K^T[K-major]
@@ -471,17 +482,18 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
         const uint32_t vb = sb + OFF_V + (i & 1) * XT;
         const uint64_t dv = smem_desc(vb, 16384, 1024, 2);
         const uint32_t th = tmem + TM_H(i & 1);
+        // k-step ks covers tokens [16 ks, +16): quarter ks / 2, half ks % 2 of it
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
           for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ts(tmem + TM_S + 128 * mb, th + 64 * (ks >> 2) + 8 * (ks & 3) + 32 * mb,
+            mma_ts(tmem + TM_S + 128 * mb, th + 32 * (ks >> 1) + 8 * (ks & 1) + 16 * mb,
                    dv + ks * 128, ID_S, 1);
         mma_commit(bar(B_G2 + (i & 1)));
       }
       if (!ok) *(volatile int*)abort_flag = 1;
     }
-  } else if (warp == 9) {
+  } else if (warp == kLoadWarp) {
     // ======================= loader =======================
     //   K(i) into stage i&1 once G1(i-2) has read K(i-2); V(i) once G2(i-2) has read V(i-2)
     if (lane == 0) {
@@ -504,46 +516,52 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
     }
   } else {
     // ======================= feature warps =======================
-    // warp w: hidden unit j = 32 (w % 4) + lane (TMEM lane), tokens [64 c, 64 c + 64) of the tile
-    const int c = warp >> 2;
+    // warp w: hidden unit j = 32 (w % 4) + lane (TMEM lane), tokens [32 q, +32) of the tile
+    const int q = warp >> 2;
     const int j = 32 * (warp & 3) + lane;
     const uint32_t lb = lane_base(warp);
     const float bj = A.bias ? A.bias[(size_t)h * D + j] * kLog2e : 0.f;
-    float2* ox = reinterpret_cast<float2*>(sm + OFF_OX);
+    const float2* ox = reinterpret_cast<const float2*>(sm + OFF_OX);
     for (int i = 0; i < nt; ++i) {
       const int b = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_G1 + b), (i >> 1) & 1, wp))) break;
       // softmax map: the offsets of tile i landed with V(i)
       if (A.off && !__all_sync(0xffffffffu, mbar_wait(bar(B_LDV + b), (i >> 1) & 1, wp))) break;
       tc_fence_after();
-      const int64_t tok0 = (int64_t)(t_begin + i) * TILE + 64 * c;
-      uint32_t hv[64];
-      tmem_ld64(tmem + lb + TM_H(b) + 64 * c, hv);
-      uint32_t pp[32], pn[32];
-      const float2* oxt = ox + b * TILE + 64 * c;
+      const uint32_t tq = tmem + lb + TM_H(b) + 32 * q;
+      uint32_t hv[32];
+      tmem_ld32(tq, hv);
+      // tokens of this quarter inside the sequence (32 except in the last tile)
+      const int64_t left = A.n - ((int64_t)(t_begin + i) * TILE + 32 * q);
+      const int nv = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
+      uint32_t pp[16], pn[16];
+      const float2* oxt = ox + b * TILE + 32 * q;
 #pragma unroll
-      for (int t = 0; t < 64; t += 2) {
+      for (int t = 0; t < 32; t += 2) {
         const float a0 = fmaf(__uint_as_float(hv[t]), kLog2e, bj);
         const float a1 = fmaf(__uint_as_float(hv[t + 1]), kLog2e, bj);
-        uint32_t wpos, wneg;
+        float e0, e1, f0, f1;
         if (A.off) {
           const float4 o2 = *reinterpret_cast<const float4*>(oxt + t);   // tokens t, t+1
-          wpos = pack_bf16(ex2_approx(a0 - o2.x), ex2_approx(a1 - o2.z));
-          wneg = pack_bf16(ex2_approx(-a0 - o2.y), ex2_approx(-a1 - o2.w));
+          e0 = ex2_approx(a0 - o2.x); e1 = ex2_approx(a1 - o2.z);
+          f0 = ex2_approx(-a0 - o2.y); f1 = ex2_approx(-a1 - o2.w);
         } else {
-          wpos = pack_bf16(ex2_approx(a0), ex2_approx(a1));
-          wneg = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+          e0 = ex2_approx(a0); e1 = ex2_approx(a1);
+          f0 = ex2_approx(-a0); f1 = ex2_approx(-a1);
         }
-        if (tok0 + t >= A.n) wpos = wneg = 0u;
-        else if (tok0 + t + 1 >= A.n) { wpos &= 0xFFFFu; wneg &= 0xFFFFu; }
-        pp[t / 2] = wpos;
-        pn[t / 2] = wneg;
-        zp += bf16_lo(wpos) + bf16_hi(wpos);
-        zn += bf16_lo(wneg) + bf16_hi(wneg);
+        // tokens past the end of the sequence contribute nothing
+        if (nv < 32) {
+          if (t >= nv) e0 = f0 = 0.f;
+          if (t + 1 >= nv) e1 = f1 = 0.f;
+        }
+        // z sums the fp32 features; the MMA operand is their bf16 rounding
+        zp += e0 + e1;
+        zn += f0 + f1;
+        pp[t / 2] = pack_bf16(e0, e1);
+        pn[t / 2] = pack_bf16(f0, f1);
       }
-      // tokens [64c, +64) -> packed columns [64c, +32) (exp(+h)) and [64c + 32, +32) (exp(-h))
-      tmem_st32(tmem + lb + TM_H(b) + 64 * c, pp);
-      tmem_st32(tmem + lb + TM_H(b) + 64 * c + 32, pn);
+      tmem_st16(tq, pp);
+      tmem_st16(tq + 16, pn);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -557,17 +575,21 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
   if (nt > 0 && !*(volatile int*)abort_flag)
     mbar_wait(bar(B_G2 + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, wp);
   tc_fence_after();
-  if (warp >= 4 && warp < 8) {
-    zx[32 * (warp & 3) + lane] = zp;
-    zx[128 + 32 * (warp & 3) + lane] = zn;
+  if (warp < kFeat) {
+    const int q = warp >> 2, j = 32 * (warp & 3) + lane;
+    zx[256 * q + j] = zp;
+    zx[256 * q + 128 + j] = zn;
   }
   __syncthreads();
-  if (warp < 8 && !*(volatile int*)abort_flag) {
-    const int c = warp >> 2;   // feature block: exp(+h) for c = 0, exp(-h) for c = 1
+  if (warp < kFeat && !*(volatile int*)abort_flag) {
+    // warp w: feature block c = (w / 4) % 2 (exp(+h) for c = 0, exp(-h) for
+    // c = 1), hidden unit j, state columns [64 (w / 8), +64)
+    const int c = (warp >> 2) & 1;
     const int j = 32 * (warp & 3) + lane;
     float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)2 * D * D + 2 * D);
     const int f = 128 * c + j;
-    for (int c0 = 0; c0 < D; c0 += 32) {
+#pragma unroll 1
+    for (int c0 = 64 * (warp >> 3); c0 < 64 * (warp >> 3) + 64; c0 += 32) {
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base(warp) + TM_S + 128 * c + c0, sv);
 #pragma unroll
@@ -576,10 +598,9 @@ __global__ void __launch_bounds__(384, 1) state_t128_kernel(const __grid_constan
             make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
                         __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
     }
-    if (c == 0) {
-      dst[(size_t)2 * D * D + j] = zp + zx[j];
-      dst[(size_t)2 * D * D + D + j] = zn + zx[128 + j];
-    }
+    // z: the four token quarters' sums in a fixed order
+    if (warp >> 3 == 0)
+      dst[(size_t)2 * D * D + f] = (zx[f] + zx[256 + f]) + (zx[512 + f] + zx[768 + f]);
   }
   tc_fence_before();
   __syncthreads();
