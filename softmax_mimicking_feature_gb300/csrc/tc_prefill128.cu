@@ -86,10 +86,10 @@ constexpr uint32_t OFF_K = 32768;               // K tile: 2 panels [128 tokens 
 constexpr uint32_t OFF_Q = OFF_K + 32768;       // Q tile: 2 panels [128 tokens x 64]
 constexpr uint32_t OFF_SB = OFF_Q;              // S_bf16 [256 features][128]: 2 panels [256 x 64]
 constexpr uint32_t OFF_SB1 = OFF_SB + 32768;    //   its second panel
-constexpr uint32_t OFF_OK = OFF_SB1;            // float2[128] key offsets of the tile (softmax
-                                                //   map), read before the snapshot overwrites them
-constexpr uint32_t OFF_ZT = OFF_SB1 + 1024;     // float[4][256] column sums of phi(K) per token
-                                                //   quarter, likewise before the snapshot
+constexpr uint32_t OFF_ZT = OFF_SB1;           // float[4][256] column sums of phi(K) per token
+                                                //   quarter, read before the snapshot overwrites them
+constexpr uint32_t OFF_OK = OFF_SB1 + 4096;     // float2[16 warps][32] key offsets of each warp's
+                                                //   token quarter (softmax map), likewise
 constexpr uint32_t OFF_V = OFF_SB + 65536;      // V tile: 2 panels [128 tokens x 64]; then y
 constexpr uint32_t OFF_PHK = OFF_V + 32768;     // phi(K) [256 features][128 tokens]: 2 panels
                                                 // [256 x 64]; then P (2 panels [128 x 64])
@@ -99,7 +99,7 @@ constexpr uint32_t OFF_Z = OFF_PHK + 65536;     // float[256] z before the tile 
 constexpr uint32_t OFF_BS = OFF_Z + 1024;       // float[128] b * log2(e)
 constexpr uint32_t OFF_BAR = OFF_BS + 512;
 enum Bar {
-  B_W, B_LDK, B_LDQ, B_LDV, B_LDO, B_G1K, B_G1Q, B_E1K, B_E1Q, B_E1S, B_G2S, B_G2U, B_E2A, B_E2B,
+  B_W, B_LDK, B_LDQ, B_LDV, B_G1K, B_G1Q, B_E1K, B_E1Q, B_E1S, B_G2S, B_G2U, B_E2A, B_E2B,
   B_G3A, B_G3, B_E3, B_COUNT
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;   // tmem base, abort flag
@@ -210,13 +210,6 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     for (int x = 0; x < 2; ++x)
       tma_load_rows(sb + OFF_V + x * 16384, &A.tv, bar(B_LDV), 64 * x, r0, ub, kh, A.seq);
   };
-  // softmax map: the tile's per-token key offsets
-  auto load_off = [&](int i) {
-    const int r0 = (t_begin + i) * TILE;
-    mbar_expect_tx(bar(B_LDO), TILE * 8);
-    bulk_load(sb + OFF_OK, A.offk + (size_t)unit * A.NT * TILE + (size_t)r0, TILE * 8,
-              bar(B_LDO));
-  };
   auto prefetch_tile = [&](int i) {
     const int r0 = (t_begin + i) * TILE;
     for (int x = 0; x < 2; ++x) {
@@ -231,7 +224,6 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     load_k(0);
     load_q(0);
     load_v(0);
-    if (SM) load_off(0);
     if (nt > 1) prefetch_tile(1);
   }
   for (int i = tid; i < D; i += kThreads) bs_s[i] = A.bias ? A.bias[(size_t)uh * D + i] * kLog2e : 0.f;
@@ -352,7 +344,6 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     // ======================= loads and stores =======================
     //   K (i+1) once G1K(i) has read K(i);
     //   Q (i+1) once G3a(i) has read S_bf16, whose first panel overwrites Q;
-    //   key offsets (i+1), over S_bf16's second panel, once G3(i) is done;
     //   y(i), staged over V(i), once E3(i) has written it; then V(i+1).
     if (lane == 0 && nt > 0) {
       bool ok = true;
@@ -365,11 +356,6 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
           ok = mbar_wait_poll(bar(B_G3A), par, wp);
           if (!ok) break;
           load_q(i + 1);
-          if (SM) {
-            ok = mbar_wait_poll(bar(B_G3), par, wp);
-            if (!ok) break;
-            load_off(i + 1);
-          }
         }
         ok = mbar_wait_poll(bar(B_E3), par, wp);
         if (!ok) break;
@@ -395,7 +381,6 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     const int g = warp & 3;
     const int r = 32 * g + lane;
     const uint32_t lb = lane_base(warp);
-    const float2* okey = reinterpret_cast<const float2*>(sm + OFF_OK);
     // A wait that gives up (hard time limit) clears `good`: the warp then
     // skips all further work but still passes every named barrier, so the
     // other epilogue warps never wait for it there.  `good` is warp-uniform.
@@ -405,6 +390,11 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
       return good;
     };
     auto epi_sync = [&]() { named_bar_sync(1, 32 * kEpi); };
+    // softmax map: lane l holds the key offsets of token 32 q + l of the next
+    // tile, loaded a tile ahead
+    const float2* offk_u = A.offk + (size_t)unit * A.NT * TILE + (size_t)t_begin * TILE + 32 * q + lane;
+    float2 ok_next = make_float2(0.f, 0.f);
+    if (SM && nt > 0) ok_next = __ldg(offk_u);
     for (int i = 0; i < nt; ++i) {
       const uint32_t par = i & 1;
       const int64_t r0 = (int64_t)(t_begin + i) * TILE;
@@ -417,8 +407,16 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
       // warp must be past its E3 (G1K no longer waits for E3)
       if (i > 0) epi_sync();
       wait_all(B_G1K, par);
-      if (SM) wait_all(B_LDO, par);
       tc_fence_after();
+      // softmax map: this warp's copy of its quarter's key offsets, over the
+      // snapshot panel (G3a of the previous tile, its last reader, completed
+      // before G1K was issued); the next tile's are requested at once
+      float2* okw = reinterpret_cast<float2*>(sm + OFF_OK) + 32 * warp;
+      if (SM) {
+        okw[lane] = ok_next;
+        __syncwarp();
+        if (i + 1 < nt) ok_next = __ldg(offk_u + (size_t)(i + 1) * TILE);
+      }
       const int fpos = internal_feature(r, 0), fneg = internal_feature(r, 1);
       if (good) {
         const float bj = bs_s[r];
@@ -444,7 +442,7 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
             const float a1 = fmaf(__uint_as_float(hk[tt + 1]), kLog2e, bj);
             float e0, e1, f0, f1;
             if (SM) {
-              const float4 o2 = *reinterpret_cast<const float4*>(okey + 32 * q + tt);
+              const float4 o2 = *reinterpret_cast<const float4*>(okw + tt);
               e0 = ex2_approx(a0 - o2.x); e1 = ex2_approx(a1 - o2.z);
               f0 = ex2_approx(-a0 - o2.y); f1 = ex2_approx(-a1 - o2.w);
             } else {
