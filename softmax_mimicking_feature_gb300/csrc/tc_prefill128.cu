@@ -184,6 +184,18 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  // W and the first tile into L2 while the kernels before this one finish: a
+  // prefetch only warms the cache, so it may run before the wait below (any
+  // later write to these rows still reaches L2 before the loads read them)
+  if (warp == kLoadWarp && lane == 0 && nt > 0) {
+    const int r0 = t_begin * TILE;
+    for (int x = 0; x < 2; ++x) {
+      tma_prefetch_3d(&A.tw, 64 * x, 0, uh);
+      tma_prefetch_rows(&A.tk, 64 * x, r0, ub, kh, A.seq);
+      tma_prefetch_rows(&A.tq, 64 * x, r0, ub, uh, A.seq);
+      tma_prefetch_rows(&A.tv, 64 * x, r0, ub, kh, A.seq);
+    }
+  }
   // everything above touches only this CTA's shared memory and TMEM; the next
   // kernel may be scheduled now, and this one reads and writes global memory
   // only once the kernels before it have completed

@@ -184,6 +184,11 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, i
                "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
 }
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // The prefetch twin of tma_load_rows.
 __device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int x, int row, int b,
                                                   int h, int seq_major) {
