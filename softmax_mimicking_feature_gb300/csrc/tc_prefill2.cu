@@ -162,6 +162,18 @@ __global__ void __launch_bounds__(384, 1) prefill_tc2_kernel(const __grid_consta
     const int r = i >> 3, ch = i & 7;
     st_shared_v4(sb + OFF_E0 + sw128_chunk(r, ch), ch == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
+  // W and the first two tiles into L2 while the kernels before this one
+  // finish: a prefetch only warms the cache, so it may run before the wait
+  // below (any later write to these rows still reaches L2 before the loads)
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_3d(&A.tw, 0, 0, h);
+    for (int i = 0; i < 2 && i < nt; ++i) {
+      const int r0 = (t_begin + i) * TILE;
+      tma_prefetch_rows(&A.tq, 0, r0, ub, uh, A.seq);
+      tma_prefetch_rows(&A.tk, 0, r0, ub, kh, A.seq);
+      tma_prefetch_rows(&A.tv, 0, r0, ub, kh, A.seq);
+    }
+  }
   // everything above touches only this CTA's shared memory and TMEM; the next
   // kernel may be scheduled now, and this one reads and writes global memory
   // only once the kernels before it have completed

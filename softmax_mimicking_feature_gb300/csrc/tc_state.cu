@@ -125,6 +125,16 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // W and the first two tiles into L2 while the kernels before this one
+  // finish (a prefetch only warms the cache, so it may precede the wait)
+  if (warp == 8 && lane == 0 && nt > 0)
+    for (int x = 0; x < (D + 63) / 64; ++x) {
+      tma_prefetch_3d(&A.tw, 64 * x, 0, h);
+      for (int i = 0; i < 2 && i < nt; ++i) {
+        tma_prefetch_rows(&A.tk, 64 * x, (t_begin + i) * TILE, ub, kh, A.seq);
+        tma_prefetch_rows(&A.tv, 64 * x, (t_begin + i) * TILE, ub, kh, A.seq);
+      }
+    }
   // the next kernel may be scheduled now; global memory is touched only after
   // the kernels before this one have completed
   pdl_launch_dependents();
@@ -670,6 +680,13 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the first two tiles into L2 while the kernels before this one finish (a
+  // prefetch only warms the cache, so it may precede the wait)
+  if (warp == 8 && lane == 0)
+    for (int i = 0; i < 2 && i < nt; ++i) {
+      tma_prefetch_rows(&A.tk, 0, (t_begin + i) * TILE, ub, kh, A.seq);
+      tma_prefetch_rows(&A.tv, 0, (t_begin + i) * TILE, ub, kh, A.seq);
+    }
   // the next kernel may be scheduled now; global memory is touched only after
   // the kernels before this one have completed
   pdl_launch_dependents();

@@ -141,6 +141,15 @@ __global__ void __launch_bounds__(384, 1) taylor_out_kernel(const __grid_constan
     prefetch_tmap(&A.tk);
     prefetch_tmap(&A.tv);
   }
+  // the first two tiles into L2 while the kernels before this one finish (a
+  // prefetch only warms the cache, so it may precede the wait)
+  if (warp == 8 && lane == 0)
+    for (int i = 0; i < 2 && i < nt; ++i) {
+      const int r0 = (t_begin + i) * TILE;
+      tma_prefetch_rows(&A.tq, 0, r0, ub, uh, A.seq);
+      tma_prefetch_rows(&A.tk, 0, r0, ub, kh, A.seq);
+      tma_prefetch_rows(&A.tv, 0, r0, ub, kh, A.seq);
+    }
   // the next kernel may be scheduled now; global memory is touched only after
   // the kernels before this one have completed
   pdl_launch_dependents();
