@@ -610,7 +610,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
 
 // In-place inclusive scan over the P-1 segment states of every unit, one
 // float4 position per thread, summed in segment order after the initial
-// state (continuation) when there is one.
+// state (continuation) when there is one.  The segments are read in batches
+// of four, all loads of a batch issued before its stores, so a thread waits
+// for one round trip per batch rather than one per segment.
 __global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __restrict__ init,
                                     int64_t units, int pm1, int64_t elems4) {
   // the next kernel may be scheduled now; global memory is touched only after
@@ -621,22 +623,26 @@ __global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __res
   if (i >= units * elems4) return;
   const int64_t u = i / elems4, e = i % elems4;
   float4* p = ws + (size_t)u * pm1 * elems4 + e;
-  float4 acc = p[0];
-  if (init) {
-    const float4 x = init[(size_t)u * elems4 + e];
-    acc.x += x.x;
-    acc.y += x.y;
-    acc.z += x.z;
-    acc.w += x.w;
-    p[0] = acc;
-  }
-  for (int s = 1; s < pm1; ++s) {
-    const float4 x = p[(size_t)s * elems4];
-    acc.x += x.x;
-    acc.y += x.y;
-    acc.z += x.z;
-    acc.w += x.w;
-    p[(size_t)s * elems4] = acc;
+  float4 acc = init ? __ldcg(init + (size_t)u * elems4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kBatch = 4;
+  for (int s0 = 0; s0 < pm1; s0 += kBatch) {
+    float4 x[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (s0 + j < pm1) x[j] = __ldcg(p + (size_t)(s0 + j) * elems4);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (s0 + j >= pm1) break;
+      if (s0 + j == 0 && !init) {
+        acc = x[0];   // the first segment's own sum stays as written
+        continue;
+      }
+      acc.x += x[j].x;
+      acc.y += x[j].y;
+      acc.z += x[j].z;
+      acc.w += x[j].w;
+      __stcg(p + (size_t)(s0 + j) * elems4, acc);
+    }
   }
 }
 
