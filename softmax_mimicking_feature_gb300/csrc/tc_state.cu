@@ -632,10 +632,14 @@ __global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constan
 // Taylor, d = 16.  The state is kept over the 160 packed features of
 // taylor_pack.cuh (the same dot products as the 288 public ones).  phi(K_t)
 // is built row-wise (thread = token) into one of two shared-memory buffers,
-// so tile t+1's features are written while G2(t) still reads tile t's.  z
-// rides along the state update as an extra column:
-//   [S z] += phi(K_t)^T [V_t e0]     (N = 32, e0 = (1, 0, ..., 0))
-// Warp 8 issues MMAs, warp 9 issues loads.
+// so tile t+1's features are written while G2(t) still reads tile t's.  The
+// state is kept transposed, so one MMA per 16 tokens spans every feature:
+//   [S z]^T += [V_t e0]^T phi(K_t)   (M = 64, N = 160, e0 = (1, 0, ..., 0))
+// [V e0]^T is the MN-major [V e0] tile read as A: rows 0-15 are V's columns,
+// row 16 the ones of e0 (z), rows 17-31 zero and rows 32-63 whatever lies
+// one and two blocks further (never read back).  An M = 64 accumulator holds
+// row m in TMEM lane 32 (m / 16) + m % 16, so S^T sits in lanes 0-15 and
+// z in lane 32.  Warp 8 issues MMAs, warp 9 issues loads.
 // ---------------------------------------------------------------------------
 namespace tay {
 constexpr int DP = tp::F;                              // packed features (153 used)
@@ -650,7 +654,8 @@ enum { B_LDK = 0, B_LDV = 2, B_E1 = 4, B_G2 = 6, B_COUNT = 8 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
 static_assert(ALLOC <= 227 * 1024, "shared memory");
-constexpr uint32_t TM_S = 0;                           // 2 blocks x [S (16) | z, 0... (16)]
+constexpr uint32_t TM_S = 0;                           // [S z]^T: 160 feature columns
+constexpr uint32_t TM_COLS = 256;
 constexpr int kThreads = 320;
 }  // namespace tay
 
@@ -710,7 +715,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
       load_v(i);
     }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), 128);
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     tmem_relinquish();
   }
   // e0 rows (1, 0, ..., 0) with the 32-byte swizzle; phi(K) buffers zero (features 160.. stay 0)
@@ -726,11 +731,11 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) {   // [S z] = 0
+  if (warp < 4) {   // [S z]^T = 0 (every lane, so whichever rows the MMA uses start at zero)
     uint32_t zr[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) zr[j] = 0u;
-    for (int c0 = 0; c0 < 64; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
+    for (int c0 = 0; c0 < DP; c0 += 32) tmem_st32(tmem + lane_base(warp) + TM_S + c0, zr);
     tmem_st_wait();
   }
   tc_fence_before();
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   if (warp == 8) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_bf16(128, 32, 1, 1);   // phiK^T[MN] [V e0][MN]
+      constexpr uint32_t ID_S = idesc_bf16(64, DP, 1, 1);   // [V e0]^T[MN] phiK[MN]
       bool ok = true;
       for (int i = 0; i < nt && ok; ++i) {
         ok = mbar_wait_poll(bar(B_E1 + (i & 1)), (i >> 1) & 1, wp) &&
@@ -749,13 +754,13 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
         tc_fence_after();
         const uint32_t pb = sb + OFF_PHK + (i & 1) * PHK_BYTES;
         const uint32_t vb = sb + OFF_V + (i & 1) * XT;
-        const uint64_t da = smem_desc(pb, 16384, 1024, 2);
+        // A = [V e0]^T: 16-row blocks one leading-byte offset apart (V, e0,
+        // then two blocks never read back); B = phi(K), 64-feature panels
         const uint64_t dv = smem_desc(vb, OFF_E0 - (OFF_V + (i & 1) * XT), 256, 6);
+        const uint64_t dk = smem_desc(pb, 16384, 1024, 2);
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-          for (int ks = 0; ks < TILE / 16; ++ks)
-            mma_ss(tmem + TM_S + 32 * mb, da + (2 * mb) * 1024 + ks * 128, dv + ks * 32, ID_S, 1);
+        for (int ks = 0; ks < TILE / 16; ++ks)
+          mma_ss(tmem + TM_S, dv + ks * 32, dk + ks * 128, ID_S, 1);
         mma_commit(bar(B_G2 + (i & 1)));
       }
       if (!ok) *(volatile int*)abort_flag = 1;
@@ -832,26 +837,26 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     mbar_wait(bar(B_G2 + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, wp);
   tc_fence_after();
   __syncthreads();
-  if (warp < 8 && !*(volatile int*)abort_flag) {
-    const int c = warp >> 2;
+  // S^T row v (TMEM lane v < 16, warp 0) holds column v of S over the 160
+  // features; row 16 (lane 32, warp 1) holds z
+  if (warp < 2 && !*(volatile int*)abort_flag) {
     float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)DP * 16 + DP);
-    for (int mb = c; mb < 2; mb += 2) {
-      const int f = mb * 128 + 32 * (warp & 3) + lane;
+#pragma unroll 1
+    for (int c0 = 0; c0 < DP; c0 += 32) {
       uint32_t sv[32];
-      tmem_ld32(tmem + lane_base(warp) + TM_S + 32 * mb, sv);
-      if (f < DP) {
+      tmem_ld32(tmem + lane_base(warp) + TM_S + c0, sv);
+      if (warp == 0 && lane < 16) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<float4*>(dst + ws_s_index(f, 4 * q, 16)) =
-              make_float4(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]),
-                          __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
-        dst[(size_t)DP * 16 + f] = __uint_as_float(sv[16]);
+        for (int j = 0; j < 32; ++j) dst[ws_s_index(c0 + j, lane, 16)] = __uint_as_float(sv[j]);
+      } else if (warp == 1 && lane == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(size_t)DP * 16 + c0 + j] = __uint_as_float(sv[j]);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
 
