@@ -261,20 +261,30 @@ struct LossCfg {
   static constexpr int DP = 2 * D;
   static constexpr uint32_t Q_BYTES = kTile * D * 2;
   static constexpr uint32_t PQ_BYTES = kTile * DP * 2;
+  // Q resident; K and phi(K) in two stages each.  phi(Q) is staged once in
+  // the second phi(K) stage and copied into TMEM, where it stays.
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_PQ = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_K = OFF_PQ + PQ_BYTES;
-  static constexpr uint32_t OFF_PK = OFF_K + Q_BYTES;
-  static constexpr uint32_t OFF_END = OFF_PK + PQ_BYTES;
-  // scalars
-  static constexpr uint32_t OFF_ST = OFF_END;              // float[6][128]: m, Z, T, Asum, U, V (half 1)
-  static constexpr uint32_t OFF_RL = OFF_ST + 6 * 128 * 4; // float[128] row losses
-  static constexpr uint32_t OFF_BAR = OFF_RL + 128 * 4;    // 9 x u64
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 9 * 8;
+  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;          // 2 stages
+  static constexpr uint32_t OFF_PK = OFF_K + 2 * Q_BYTES;     // 2 stages
+  static constexpr uint32_t OFF_END = OFF_PK + 2 * PQ_BYTES;
+  // row scalars for merging the two column halves, over the first K stage
+  // once every MMA has completed
+  static constexpr uint32_t OFF_ST = OFF_K;                   // float[6][128]: m, Z, T, Asum, U, V
+  static constexpr uint32_t OFF_RL = OFF_ST + 6 * 128 * 4;    // float[128] row losses
+  static_assert(OFF_RL + 128 * 4 <= OFF_K + Q_BYTES, "row scalars fit one K stage");
+  // barriers: per stage K, phi(K) landed; K, phi(K) read; S ready; S drained
+  // (6 x 2); Q + phi(Q) landed; phi(Q) in TMEM; A ready; A read
+  enum { B_K = 0, B_PK = 2, B_KR = 4, B_PKR = 6, B_S = 8, B_SF = 10, B_Q = 12, B_QT = 13,
+         B_A = 14, B_AF = 15, B_COUNT = 16 };
+  static constexpr uint32_t OFF_BAR = OFF_END;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
+  static_assert(ALLOC <= 232448, "shared memory");
+  // TMEM: S stages at 0 and 128, A at 256, phi(Q) (bf16 pairs) at 384
+  static constexpr uint32_t TM_A = 256, TM_PQ = 384;
 };
 
-constexpr int kLossThreads = 288;  // 8 epilogue warps + 1 producer warp
+constexpr int kLossThreads = 320;  // 8 epilogue warps, MMA issuer warp 8, loader warp 9
 
 template <int D, bool STATS>
 __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_constant__ LossArgs A) {
@@ -285,13 +295,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   const uint32_t sb = smem_u32(sm);
   float* st_s = reinterpret_cast<float*>(sm + C::OFF_ST);
   float* rl_s = reinterpret_cast<float*>(sm + C::OFF_RL);
-  const uint32_t bar_q = sb + C::OFF_BAR;        // Q, phi(Q) loaded
-  const uint32_t bar_k = bar_q + 8;              // K_j loaded
-  const uint32_t bar_mma0 = bar_q + 16;          // stage 0 MMAs done (2 barriers)
-  const uint32_t bar_free0 = bar_q + 32;         // stage 0 drained by the epilogue (2 barriers)
-  const uint32_t bar_pk = bar_q + 48;            // phi(K_j) loaded
-  const uint32_t bar_kread = bar_q + 56;         // the Q K_j^T MMAs have read K_j
-  const uint32_t bar_pkread = bar_q + 64;        // the phi(Q) phi(K_j)^T MMAs have read phi(K_j)
+  const uint32_t bars = sb + C::OFF_BAR;
+  auto bar = [&](int b) { return bars + 8u * b; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
 
@@ -305,7 +310,6 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   const int64_t gsz = min((int64_t)A.HG, A.U - grp * A.HG);
   const int qt = A.NT - 1 - (int)(within / gsz);
   const int64_t unit = grp * A.HG + within % gsz;
-  const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
   const int64_t q0 = (int64_t)qt * kTile;
@@ -313,15 +317,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
 
   if (tid == 0) {
-    mbar_init(bar_q, 1);
-    mbar_init(bar_k, 1);
-    mbar_init(bar_mma0, 1);
-    mbar_init(bar_mma0 + 8, 1);
-    mbar_init(bar_free0, 8);
-    mbar_init(bar_free0 + 8, 8);
-    mbar_init(bar_pk, 1);
-    mbar_init(bar_kread, 1);
-    mbar_init(bar_pkread, 1);
+    for (int b = 0; b < C::B_COUNT; ++b)
+      mbar_init(bar(b), (b == C::B_SF || b == C::B_SF + 1 || b == C::B_QT || b == C::B_AF) ? 8 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -340,85 +337,150 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
 
-  if (warp == 8) {
-    // ---------------- producer: TMA + MMA issue ----------------
+  auto load_k = [&](int j) {
+    const int s = j & 1;
+    mbar_expect_tx(bar(C::B_K + s), C::Q_BYTES);
+    for (int i = 0; i < D / 64; ++i)
+      tma_load_rows(sb + C::OFF_K + s * C::Q_BYTES + i * 16384, &A.tk, bar(C::B_K + s), 64 * i,
+                    j * kTile, ub, kh, A.seq);
+  };
+  auto load_pk = [&](int j) {
+    const int s = j & 1;
+    mbar_expect_tx(bar(C::B_PK + s), C::PQ_BYTES);
+    for (int i = 0; i < C::DP / 64; ++i)
+      tma_load_3d(sb + C::OFF_PK + s * C::PQ_BYTES + i * 16384, &A.tpk, bar(C::B_PK + s), 64 * i,
+                  j * kTile, (int)unit);
+  };
+
+  if (warp == 9) {
+    // ---------------- loader ----------------
+    //   Q and phi(Q) (into the second phi(K) stage) first, K(0), phi(K)(0), K(1);
+    //   phi(K)(1) once phi(Q) has gone to TMEM; then K(j), phi(K)(j) into
+    //   stage j & 1 as soon as the MMAs of tile j - 2 have read that stage
     if (lane == 0) {
-      // K_j and phi(K_j) arrive on separate barriers: the next K is fetched as
-      // soon as the Q K^T MMAs have read the current one, under the phi MMAs.
-      auto load_k = [&](int j) {
-        mbar_expect_tx(bar_k, C::Q_BYTES);
-        for (int i = 0; i < D / 64; ++i)
-          tma_load_rows(sb + C::OFF_K + i * 16384, &A.tk, bar_k, 64 * i, j * kTile, ub,
-                        kh, A.seq);
-      };
-      auto load_pk = [&](int j) {
-        mbar_expect_tx(bar_pk, C::PQ_BYTES);
-        for (int i = 0; i < C::DP / 64; ++i)
-          tma_load_3d(sb + C::OFF_PK + i * 16384, &A.tpk, bar_pk, 64 * i, j * kTile, (int)unit);
-      };
-      mbar_expect_tx(bar_q, C::Q_BYTES + C::PQ_BYTES);
+      mbar_expect_tx(bar(C::B_Q), C::Q_BYTES + C::PQ_BYTES);
       for (int i = 0; i < D / 64; ++i)
-        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar_q, 64 * i, (int)q0, ub, uh, A.seq);
+        tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar(C::B_Q), 64 * i, (int)q0, ub, uh, A.seq);
       for (int i = 0; i < C::DP / 64; ++i)
-        tma_load_3d(sb + C::OFF_PQ + i * 16384, &A.tpq, bar_q, 64 * i, (int)q0, (int)unit);
+        tma_load_3d(sb + C::OFF_PK + C::PQ_BYTES + i * 16384, &A.tpq, bar(C::B_Q), 64 * i,
+                    (int)q0, (int)unit);
       load_k(0);
       load_pk(0);
-      bool ok = mbar_wait_poll(bar_q, 0, wp);
+      if (nkt > 1) load_k(1);
+      int nk = nkt < 2 ? nkt : 2, npk = 1;
+      IdleClock clk;
+      bool ok = true;
+      while ((nk < nkt || npk < nkt) && ok) {
+        bool progress = false;
+        if (nk < nkt && mbar_probe(bar(C::B_KR + (nk & 1)), ((nk - 2) >> 1) & 1)) {
+          load_k(nk++);
+          progress = true;
+        }
+        if (npk < nkt &&
+            (npk == 1 ? mbar_probe(bar(C::B_QT), 0)
+                      : mbar_probe(bar(C::B_PKR + (npk & 1)), ((npk - 2) >> 1) & 1))) {
+          load_pk(npk++);
+          progress = true;
+        }
+        if (progress) clk.progress();
+        else ok = clk.idle(wp);
+      }
+      if (!ok) failed = true;
+    }
+  } else if (warp == 8) {
+    // ---------------- MMA issuer ----------------
+    //   S(j) = Q K_j^T into S stage j & 1 once K_j landed and the epilogue has
+    //   drained that stage (tile j - 2);  A(j) = phi(Q) phi(K_j)^T (phi(Q)
+    //   from TMEM) once phi(K_j) landed and the epilogue has copied A(j - 1)
+    //   out of the accumulator
+    if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
-      // descriptor bases (K-major, 128B-swizzled 64-element panels); a k-step
-      // only moves the start-address field (16-byte units)
-      const uint64_t dq = smem_desc(sb + C::OFF_Q, 16, 1024, 2);
-      const uint64_t dk = smem_desc(sb + C::OFF_K, 16, 1024, 2);
-      const uint64_t dpq = smem_desc(sb + C::OFF_PQ, 16, 1024, 2);
-      const uint64_t dpk = smem_desc(sb + C::OFF_PK, 16, 1024, 2);
       auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
+      const uint64_t dq = smem_desc(sb + C::OFF_Q, 16, 1024, 2);
+      bool ok = mbar_wait_poll(bar(C::B_QT), 0, wp);
       for (int j = 0; j < nkt && ok; ++j) {
-        const int stg = j & 1;
-        ok = mbar_wait_poll(bar_k, j & 1, wp);                           // K_j landed
-        if (ok && j >= 2) ok = mbar_wait_poll(bar_free0 + 8 * stg, ((j >> 1) - 1) & 1, wp);
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        ok = mbar_wait_poll(bar(C::B_K + s), ph, wp) &&
+             (j < 2 || mbar_wait_poll(bar(C::B_SF + s), ph ^ 1, wp));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t ts = tmem + stg * 256;
+        const uint64_t dk = smem_desc(sb + C::OFF_K + s * C::Q_BYTES, 16, 1024, 2);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(ts, dq + kmaj(ks), dk + kmaj(ks), IDESC, ks > 0);
-        mma_commit(bar_kread);
-        ok = mbar_wait_poll(bar_pk, j & 1, wp);                          // phi(K_j) landed
+          mma_ss(tmem + s * 128, dq + kmaj(ks), dk + kmaj(ks), IDESC, ks > 0);
+        mma_commit(bar(C::B_S + s));
+        mma_commit(bar(C::B_KR + s));
+        ok = mbar_wait_poll(bar(C::B_PK + s), ph, wp) &&
+             (j < 1 || mbar_wait_poll(bar(C::B_AF), (j - 1) & 1, wp));
         if (!ok) break;
         tc_fence_after();
+        const uint64_t dpk = smem_desc(sb + C::OFF_PK + s * C::PQ_BYTES, 16, 1024, 2);
 #pragma unroll
         for (int ks = 0; ks < C::DP / 16; ++ks)
-          mma_ss(ts + 128, dpq + kmaj(ks), dpk + kmaj(ks), IDESC, ks > 0);
-        mma_commit(bar_mma0 + 8 * stg);
-        mma_commit(bar_pkread);
-        if (j + 1 < nkt) {
-          ok = mbar_wait_poll(bar_kread, j & 1, wp);
-          if (ok) load_k(j + 1);
-          ok = ok && mbar_wait_poll(bar_pkread, j & 1, wp);
-          if (ok) load_pk(j + 1);
-        }
+          mma_ts(tmem + C::TM_A, tmem + C::TM_PQ + ks * 8, dpk + kmaj(ks), IDESC, ks > 0);
+        mma_commit(bar(C::B_A));
+        mma_commit(bar(C::B_PKR + s));
       }
       if (!ok) failed = true;
     }
   } else {
     // ---------------- epilogue warps ----------------
     const int half = warp >> 2, row = 32 * (warp & 3) + lane;
+    const uint32_t lb = lane_base(warp);
     const int64_t qi = q0 + row;
+    // phi(Q) into TMEM once: row `row`, features [DP/2 * half, +DP/2) from the
+    // staged tile (DP/64 panels of [128 rows x 64], 128-byte swizzle) as bf16
+    // pairs, columns [D/2 * half, +D/2) of the phi(Q) block
+    if (!mbar_wait(bar(C::B_Q), 0, wp)) {
+      failed = true;
+    } else {
+      const uint32_t pq = sb + C::OFF_PK + C::PQ_BYTES;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {   // 32 packed columns = 64 features
+        const int f0 = (C::DP / 2) * half + 2 * c0;
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(
+              sm + (pq - sb) + (f0 / 64) * 16384 + sw128_chunk(row, q));
+          w[4 * q] = v4.x;
+          w[4 * q + 1] = v4.y;
+          w[4 * q + 2] = v4.z;
+          w[4 * q + 3] = v4.w;
+        }
+        tmem_st32(tmem + lb + C::TM_PQ + (D / 2) * half + c0, w);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(C::B_QT));   // phi(Q) is in TMEM; its staging stage is free
+
     // online state; Z, T and the weight sum are kept as two interleaved partial
     // sums so consecutive keys do not form one long dependency chain
     float m = -INFINITY, Z0 = 0.f, Z1 = 0.f, T0 = 0.f, T1 = 0.f, A0 = 0.f, A1 = 0.f;
     float U0 = 0.f, U1 = 0.f, V0 = 0.f, V1 = 0.f;   // STATS only
     const int64_t kmax = min(qi, A.n - 1);   // last key admitted for this row
-    for (int j = 0; j < nkt; ++j) {
-      const int stg = j & 1;
-      if (!mbar_wait(bar_mma0 + 8 * stg, (j >> 1) & 1, wp)) { failed = true; break; }
+    for (int j = 0; j < nkt && !failed; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait(bar(C::B_A), j & 1, wp) || !mbar_wait(bar(C::B_S + s), (j >> 1) & 1, wp)) {
+        failed = true;
+        break;
+      }
       tc_fence_after();
+      // A(j) out of the accumulator first, so A(j+1) can start under this tile
+      uint32_t av[64];
+      tmem_ld32x2(tmem + lb + C::TM_A + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&av[0]),
+                  tmem + lb + C::TM_A + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&av[32]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_AF));
       const int64_t k0 = (int64_t)j * kTile + half * 64;
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
-        uint32_t sv[32], av[32];
-        tmem_ld32x2(tmem + lane_base(warp) + stg * 256 + half * 64 + c, sv,
-                    tmem + lane_base(warp) + stg * 256 + 128 + half * 64 + c, av);
+        uint32_t sv[32];
+        tmem_ld32(tmem + lb + s * 128 + half * 64 + c, sv);
         const int nval = (int)max((int64_t)0, min((int64_t)32, kmax - (k0 + c) + 1));
         if (nval == 32) {
           // every key of the chunk is admitted: no masking
@@ -438,7 +500,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           m = mn;
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float a0 = __uint_as_float(av[e]), a1 = __uint_as_float(av[e + 1]);
+            const float a0 = __uint_as_float(av[c + e]), a1 = __uint_as_float(av[c + e + 1]);
             const float l0 = __log2f(a0), l1 = __log2f(a1);
             if constexpr (STATS) {
               const float s0 = __uint_as_float(sv[e]) * A.s_scale;
@@ -476,7 +538,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             if (e < nval) {
-              const float a = __uint_as_float(av[e]);
+              const float a = __uint_as_float(av[c + e]);
               const float la = __log2f(a);
               const float sl = __uint_as_float(sv[e]) * A.s_scale;
               const float p = ex2_approx(sl - m);
@@ -493,9 +555,13 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_free0 + 8 * stg);
+      if (lane == 0) mbar_arrive(bar(C::B_SF + s));
     }
     float Z = Z0 + Z1, T = T0 + T1, As = A0 + A1, Us = U0 + U1, Vs = V0 + V1;
+    // the row scalars go over the first K stage: wait until every MMA has read
+    // it (the last A, which follows the last S in issue order)
+    if (!failed && nkt > 0) failed = !mbar_wait(bar(C::B_A), (nkt - 1) & 1, wp);
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     // merge the two column halves of each row
     if (half == 1) {
       st_s[row] = m;
