@@ -395,10 +395,15 @@ static hh_status mimicry_loss_impl(const hh_fmap* fmap, int dtype, const void* q
   float* partial = (float*)(ws + 2 * phi_bytes);
   float* head = loss_head_sum ? loss_head_sum : partial + (size_t)B * H * ceil_div(n, 64);
   if (fmap_tc_supported(p)) {
-    cudaError_t e = launch_fmap_tc_qk(p, q, k, phq, phk, nullptr, nullptr, dev_status, s);
+    // the Hedgehog map: phi(k) from the feature-map kernel (each key tile is
+    // read by every later query tile), phi(q) formed inside the loss kernel;
+    // the softmax map: both from the feature-map kernel
+    cudaError_t e = p.softmax
+                        ? launch_fmap_tc_qk(p, q, k, phq, phk, nullptr, nullptr, dev_status, s)
+                        : launch_fmap_tc(p, k, 1, phk, nullptr, dev_status, s);
     if (e == cudaSuccess)
-      e = launch_loss_tc(p, q, k, phq, phk, loss_rows, partial, head, nullptr, rows4, dev_status,
-                         s);
+      e = launch_loss_tc(p, q, k, p.softmax ? phq : nullptr, phk, loss_rows, partial, head, nullptr,
+                         rows4, dev_status, s);
     return cuda_status(e);
   }
   cudaError_t e = launch_fmap_simt(p, q, 0, phq, nullptr, s);

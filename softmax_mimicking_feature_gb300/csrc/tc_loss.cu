@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
 // ===========================================================================
 struct LossArgs {
   CUtensorMap tq, tk, tpq, tpk;
+  CUtensorMap tw;      // fuse_q: W [H][D][D] of the query map
+  const float* bias;   // fuse_q: b [H][D] of the query map, or null
+  int fuse_q;          // phi(Q) formed here from Q W + b (Hedgehog map) instead of read
   float* loss_rows;    // [U][n] or null
   float* partial;      // [U][NT]
   float2* stats;       // [U][NT * 128] (c_i, 1 / A_i) or null; c_i = m_i + log2 Z_i
@@ -273,9 +276,9 @@ struct LossCfg {
   static constexpr uint32_t OFF_RL = OFF_ST + 6 * 128 * 4;    // float[128] row losses
   static_assert(OFF_RL + 128 * 4 <= OFF_K + Q_BYTES, "row scalars fit one K stage");
   // barriers: per stage K, phi(K) landed; K, phi(K) read; S ready; S drained
-  // (6 x 2); Q + phi(Q) landed; phi(Q) in TMEM; A ready; A read
+  // (6 x 2); Q + phi(Q) (or W) landed; phi(Q) in TMEM; A ready; A read; H = Q W ready
   enum { B_K = 0, B_PK = 2, B_KR = 4, B_PKR = 6, B_S = 8, B_SF = 10, B_Q = 12, B_QT = 13,
-         B_A = 14, B_AF = 15, B_COUNT = 16 };
+         B_A = 14, B_AF = 15, B_H = 16, B_COUNT = 17 };
   static constexpr uint32_t OFF_BAR = OFF_END;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
@@ -354,16 +357,23 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 
   if (warp == 9) {
     // ---------------- loader ----------------
-    //   Q and phi(Q) (into the second phi(K) stage) first, K(0), phi(K)(0), K(1);
-    //   phi(K)(1) once phi(Q) has gone to TMEM; then K(j), phi(K)(j) into
-    //   stage j & 1 as soon as the MMAs of tile j - 2 have read that stage
+    //   Q and phi(Q), or W (into the second phi(K) stage) first, K(0),
+    //   phi(K)(0), K(1); phi(K)(1) once phi(Q) has gone to TMEM; then K(j),
+    //   phi(K)(j) into stage j & 1 as soon as the MMAs of tile j - 2 have read
+    //   that stage
     if (lane == 0) {
-      mbar_expect_tx(bar(C::B_Q), C::Q_BYTES + C::PQ_BYTES);
+      mbar_expect_tx(bar(C::B_Q), C::Q_BYTES + (A.fuse_q ? D * D * 2 : C::PQ_BYTES));
       for (int i = 0; i < D / 64; ++i)
         tma_load_rows(sb + C::OFF_Q + i * 16384, &A.tq, bar(C::B_Q), 64 * i, (int)q0, ub, uh, A.seq);
-      for (int i = 0; i < C::DP / 64; ++i)
-        tma_load_3d(sb + C::OFF_PK + C::PQ_BYTES + i * 16384, &A.tpq, bar(C::B_Q), 64 * i,
-                    (int)q0, (int)unit);
+      if (A.fuse_q) {
+        for (int i = 0; i < D / 64; ++i)
+          tma_load_3d(sb + C::OFF_PK + C::PQ_BYTES + i * (D * 128), &A.tw, bar(C::B_Q), 64 * i, 0,
+                      uh);
+      } else {
+        for (int i = 0; i < C::DP / 64; ++i)
+          tma_load_3d(sb + C::OFF_PK + C::PQ_BYTES + i * 16384, &A.tpq, bar(C::B_Q), 64 * i,
+                      (int)q0, (int)unit);
+      }
       load_k(0);
       load_pk(0);
       if (nkt > 1) load_k(1);
@@ -397,7 +407,21 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
       auto kmaj = [](int ks) { return (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2); };
       const uint64_t dq = smem_desc(sb + C::OFF_Q, 16, 1024, 2);
-      bool ok = mbar_wait_poll(bar(C::B_QT), 0, wp);
+      bool ok = true;
+      if (A.fuse_q) {
+        // H_Q = Q W into the A accumulator (free until A(0)), W as the MN-major B
+        constexpr uint32_t ID_H = idesc_bf16(128, D, 0, 1);
+        ok = mbar_wait_poll(bar(C::B_Q), 0, wp);
+        if (ok) {
+          tc_fence_after();
+          const uint64_t dw = smem_desc(sb + C::OFF_PK + C::PQ_BYTES, D * 128, 1024, 2);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + C::TM_A, dq + kmaj(ks), dw + ks * 128, ID_H, ks > 0);
+          mma_commit(bar(C::B_H));
+        }
+      }
+      ok = ok && mbar_wait_poll(bar(C::B_QT), 0, wp);
       for (int j = 0; j < nkt && ok; ++j) {
         const int s = j & 1;
         const uint32_t ph = (j >> 1) & 1;
@@ -429,11 +453,35 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
     const int half = warp >> 2, row = 32 * (warp & 3) + lane;
     const uint32_t lb = lane_base(warp);
     const int64_t qi = q0 + row;
-    // phi(Q) into TMEM once: row `row`, features [DP/2 * half, +DP/2) from the
-    // staged tile (DP/64 panels of [128 rows x 64], 128-byte swizzle) as bf16
-    // pairs, columns [D/2 * half, +D/2) of the phi(Q) block
-    if (!mbar_wait(bar(C::B_Q), 0, wp)) {
+    // phi(Q) into TMEM once, as bf16 pairs in the public feature order
+    // (exp(+h) in packed columns [0, D/2), exp(-h) in [D/2, D)).  Read:
+    // row `row`, features [DP/2 * half, +DP/2) from the staged tile (DP/64
+    // panels of [128 rows x 64], 128-byte swizzle) into columns
+    // [D/2 * half, +D/2).  Formed: hidden units [D/2 * half, +D/2) of
+    // H_Q = Q W, a = (h + b) log2(e), exp2(+-a).
+    if (!mbar_wait(bar(A.fuse_q ? C::B_H : C::B_Q), 0, wp)) {
       failed = true;
+    } else if (A.fuse_q) {
+      tc_fence_after();
+      const float* bq = A.bias ? A.bias + (size_t)uh * D : nullptr;
+#pragma unroll 1
+      for (int u0 = (D / 2) * half; u0 < (D / 2) * half + D / 2; u0 += 32) {
+        uint32_t hv[32];
+        tmem_ld32(tmem + lb + C::TM_A + u0, hv);
+        uint32_t pp[16], pn[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float b0 = bq ? __ldg(bq + u0 + j) * kLog2e : 0.f;
+          const float b1 = bq ? __ldg(bq + u0 + j + 1) * kLog2e : 0.f;
+          const float a0 = fmaf(__uint_as_float(hv[j]), kLog2e, b0);
+          const float a1 = fmaf(__uint_as_float(hv[j + 1]), kLog2e, b1);
+          pp[j / 2] = pack_bf16(ex2_approx(a0), ex2_approx(a1));
+          pn[j / 2] = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
+        }
+        tmem_st16(tmem + lb + C::TM_PQ + u0 / 2, pp);
+        tmem_st16(tmem + lb + C::TM_PQ + D / 2 + u0 / 2, pn);
+      }
+      tmem_st_wait();
     } else {
       const uint32_t pq = sb + C::OFF_PK + C::PQ_BYTES;
 #pragma unroll 1
@@ -699,11 +747,18 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  // no phi(q) given: the kernel forms phi(Q) from Q W + b (the Hedgehog map;
+  // the softmax map needs its row offsets first and comes with phi(q))
+  const bool fuse = phq == nullptr;
+  if (fuse && p.softmax) return cudaErrorInvalidValue;
   bool ok = make_rows_map(&a.tq, q, D, p.n, p.H, p.B, 64, kTile, sw, p.seq_major) &&
             make_rows_map(&a.tk, k, D, p.n, p.H / p.G, p.B, 64, kTile, sw, p.seq_major) &&
-            make_plane_map(&a.tpq, phq, 2 * D, p.n, U, 64, kTile, sw) &&
+            (fuse ? make_plane_map(&a.tw, p.Wq, D, D, p.H, 64, D, sw)
+                  : make_plane_map(&a.tpq, phq, 2 * D, p.n, U, 64, kTile, sw)) &&
             make_plane_map(&a.tpk, phk, 2 * D, p.n, U, 64, kTile, sw);
   if (!ok) return cudaErrorInvalidValue;
+  a.fuse_q = fuse ? 1 : 0;
+  a.bias = fuse ? p.bq : nullptr;
   a.loss_rows = loss_rows;
   a.partial = partial;
   a.stats = reinterpret_cast<float2*>(stats);
