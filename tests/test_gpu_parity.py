@@ -177,6 +177,30 @@ def test_separate_query_and_key_maps():
     assert rel_l2_per_head(f64(y), ref) <= BF16_TOL
 
 
+@pytest.mark.parametrize("name,d", [("gpt2_prefill_8x12x1024_d64", 64),
+                                    ("llama2_prefill_1x32x4096_d128", 128)])
+def test_loss_with_separate_query_and_key_maps(name, d):
+    # the loss kernel forms phi(q) from the query map itself while phi(k) comes
+    # from the feature-map kernel with the key map: both maps, both biases
+    w = wl.WORKLOADS[name].with_(B=1, H=2, n=300)
+    x = wl.make_inputs(w, seed=23)
+    x2 = wl.make_inputs(w, seed=24)
+    xd = _dev(x)
+    bq = torch.randn(w.H, d, generator=torch.Generator().manual_seed(5)) * 0.1
+    bk = torch.randn(w.H, d, generator=torch.Generator().manual_seed(6)) * 0.1
+    fm = hh.FeatureMap("hedgehog", d, xd["W"], bq.cuda(), x2["W"].cuda(), bk.cuda())
+    rows, head = hh.mimicry_loss(fm, xd["q"], xd["k"])
+    torch.cuda.synchronize()
+    q, k = f64(x["q"]), f64(x["k"])
+    ref = np.empty((1, w.H, w.n))
+    for h in range(w.H):
+        pq = O.hedgehog_feature_map(q[0, h], f64(x["W"])[h], f64(bq)[h])
+        pk = O.hedgehog_feature_map(k[0, h], f64(x2["W"])[h], f64(bk)[h])
+        ref[0, h] = O.mimicry_loss(q[0, h], k[0, h], pq, pk)
+    assert rel_l2_per_head(f64(rows), ref) <= BF16_TOL
+    np.testing.assert_allclose(f64(head)[0], ref[0].sum(-1), rtol=BF16_TOL)
+
+
 # ---------------------------------------------------------------------------
 # state export and decode
 # ---------------------------------------------------------------------------
