@@ -135,8 +135,10 @@ struct TcPlan {
   int NT = 0;        // 128-token tiles per sequence
   int P = 1;         // segments per sequence
   int L = 1;         // tiles per segment
+  int M = 1;         // state-pass pieces per segment (one CTA each)
   int launches = 1;  // kernel launches per call
   size_t ws_bytes = 0;
+  size_t raw_offset = 0;    // M > 1: byte offset of the piece states in the workspace
   size_t init_offset = 0;   // continuation: byte offset of the initial state in the workspace
 };
 TcPlan plan_prefill_tc(const Problem& p);

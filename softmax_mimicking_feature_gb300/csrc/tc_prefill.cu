@@ -608,13 +608,17 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-// In-place inclusive scan over the P-1 segment states of every unit, one
-// float4 position per thread, summed in segment order after the initial
-// state (continuation) when there is one.  The segments are read in batches
-// of four, all loads of a batch issued before its stores, so a thread waits
-// for one round trip per batch rather than one per segment.
-__global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __restrict__ init,
-                                    int64_t units, int pm1, int64_t elems4) {
+// Inclusive scan over the segment states of every unit, one float4 position
+// per thread, summed in order after the initial state (continuation) when
+// there is one.  With one piece per segment (m = 1) it runs in place over the
+// pm1 states in ws; with m > 1 it reads the pm1 * m piece states of a unit
+// from raw and writes the running sum after each segment's last piece to ws.
+// The states are read in batches of four, all loads of a batch issued before
+// its stores, so a thread waits for one round trip per batch rather than one
+// per state.
+__global__ void segment_scan_kernel(float4* ws, const float4* raw,
+                                    const float4* __restrict__ init, int64_t units, int pm1,
+                                    int m, int64_t elems4) {
   // the next kernel may be scheduled now; global memory is touched only after
   // the kernels before this one have completed
   pdl_launch_dependents();
@@ -622,26 +626,27 @@ __global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __res
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units * elems4) return;
   const int64_t u = i / elems4, e = i % elems4;
-  float4* p = ws + (size_t)u * pm1 * elems4 + e;
+  const int np = pm1 * m;
+  const float4* src = raw + (size_t)u * np * elems4 + e;
+  float4* dst = ws + (size_t)u * pm1 * elems4 + e;
   float4 acc = init ? __ldcg(init + (size_t)u * elems4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int kBatch = 4;
-  for (int s0 = 0; s0 < pm1; s0 += kBatch) {
+  for (int s0 = 0; s0 < np; s0 += kBatch) {
     float4 x[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j)
-      if (s0 + j < pm1) x[j] = __ldcg(p + (size_t)(s0 + j) * elems4);
+      if (s0 + j < np) x[j] = __ldcg(src + (size_t)(s0 + j) * elems4);
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      if (s0 + j >= pm1) break;
-      if (s0 + j == 0 && !init) {
-        acc = x[0];   // the first segment's own sum stays as written
-        continue;
-      }
+      const int t = s0 + j;
+      if (t >= np) break;
       acc.x += x[j].x;
       acc.y += x[j].y;
       acc.z += x[j].z;
       acc.w += x[j].w;
-      __stcg(p + (size_t)(s0 + j) * elems4, acc);
+      // in place, the first segment's own sum stays as written
+      if ((t + 1) % m == 0 && !(m == 1 && t == 0 && !init))
+        __stcg(dst + (size_t)((t + 1) / m - 1) * elems4, acc);
     }
   }
 }
@@ -709,9 +714,21 @@ TcPlan plan_prefill_tc(const Problem& p) {
   P = std::min<int64_t>(P, std::max(1, pl.NT));
   pl.L = pl.NT > 0 ? ceil_div(pl.NT, P) : 1;
   pl.P = pl.NT > 0 ? ceil_div(pl.NT, pl.L) : 1;
-  pl.launches = pl.P > 2 ? 3 : (pl.P > 1 ? 2 : 1);
-  pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * (size_t)ws_segment_floats(p) * sizeof(float)
-                         : 0;
+  // The Taylor state pass runs two CTAs per SM: split each segment's state
+  // into pieces so that its grid fills both slots of every SM once.
+  if (pl.P > 1) {
+    int64_t m = p.kind == HH_FMAP_TAYLOR2 ? 2 * slots / (U * (pl.P - 1)) : 1;
+    const char* em = getenv("HH_STATE_PIECES");
+    if (em && *em) m = atoi(em);
+    pl.M = (int)std::max<int64_t>(1, std::min<int64_t>(m, pl.L));
+  }
+  pl.launches = (pl.P > 2 || pl.M > 1) ? 3 : (pl.P > 1 ? 2 : 1);
+  const size_t per = (size_t)ws_segment_floats(p) * sizeof(float);
+  pl.ws_bytes = pl.P > 1 ? (size_t)U * (pl.P - 1) * per : 0;
+  if (pl.M > 1) {
+    pl.raw_offset = pl.ws_bytes;
+    pl.ws_bytes += (size_t)U * (pl.P - 1) * pl.M * per;
+  }
   if (p.has_init) {
     // the initial state in workspace layout follows the segment states; the
     // scan also runs for two segments
@@ -745,12 +762,14 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
   if (pl.P > 1) {
     cudaError_t e = launch_state_tc(p, pl, k, v, ws, dev_status, s);
     if (e != cudaSuccess) return e;
-    if (pl.P > 2 || init) {
+    if (pl.P > 2 || pl.M > 1 || init) {
       const int64_t elems4 = ws_segment_floats(p) / 4;
       const int64_t n4 = (int64_t)U * elems4;
+      const float4* raw = reinterpret_cast<const float4*>(
+          reinterpret_cast<const char*>(ws) + (pl.M > 1 ? pl.raw_offset : 0));
       e = launch_pdl(segment_scan_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s,
-                     reinterpret_cast<float4*>(ws), reinterpret_cast<const float4*>(init),
-                     (int64_t)U, pl.P - 1, elems4);
+                     reinterpret_cast<float4*>(ws), raw, reinterpret_cast<const float4*>(init),
+                     (int64_t)U, pl.P - 1, pl.M, elems4);
       if (e != cudaSuccess) return e;
     }
   }

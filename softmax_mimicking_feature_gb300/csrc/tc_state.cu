@@ -78,16 +78,40 @@ struct SSmem {
 
 struct StateArgs {
   CUtensorMap tk, tv, tw;
-  float* ws;          // [U][P-1][DPP*D + DPP]: S (ws_s_index layout) then z
+  const __nv_bfloat16* kraw;   // k itself (the Taylor pass reads its rows directly)
+  float* ws;          // [U][(P-1)*M][DPP*D + DPP]: S (ws_s_index layout) then z
   const float* bias;  // [H][D] of the key map (Hedgehog) or null
   const float2* off;  // [U][NT*128] softmax-map offsets of the keys (log2 units) or null
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
   int H, P, L, NT;
+  int M;              // pieces per segment: each CTA sums one piece of a segment
   int G;              // query heads per key/value head
   int seq;            // k, v are [B][n][Hkv][D]
 };
+
+// The piece of a segment this CTA sums: piece j of segment s covers tiles
+// [s L + j Lp, s L + (j + 1) Lp) with Lp = ceil(L / M), cut at the segment's
+// end (a piece past it is empty and exports zeros).  `index` orders the
+// pieces of a unit by position, which is the order the scan adds them in.
+struct StatePiece {
+  int64_t unit;
+  int index, t_begin, nt;
+};
+__device__ __forceinline__ StatePiece state_piece(const StateArgs& A) {
+  const int npc = (A.P - 1) * A.M;
+  StatePiece r;
+  r.unit = blockIdx.x / npc;
+  r.index = blockIdx.x % npc;
+  const int seg = r.index / A.M, j = r.index % A.M;
+  const int lp = (A.L + A.M - 1) / A.M;
+  const int b = seg * A.L + min(j * lp, A.L);
+  const int e = min(seg * A.L + min((j + 1) * lp, A.L), A.NT);
+  r.t_begin = b;
+  r.nt = max(0, e - b);
+  return r;
+}
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
   return (uint32_t)(32 * (warp & 3)) << 16;
@@ -109,14 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
   int* abort_flag = reinterpret_cast<int*>(sm + SM::OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t unit = blockIdx.x / (A.P - 1);
+  const StatePiece pc = state_piece(A);
+  const int64_t unit = pc.unit;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
-  const int seg = blockIdx.x % (A.P - 1);
   const int h = (int)(unit % A.H);
-  const int t_begin = seg * A.L;
-  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  const int t_begin = pc.t_begin;
+  const int nt = pc.nt;
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
 
   if (tid == 0) {
@@ -312,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
   __syncthreads();
   if (warp < 8 && !*(volatile int*)abort_flag) {
     const int c = warp >> 2;
-    float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)C::DPP * D + C::DPP);
+    float* dst = A.ws + ((size_t)unit * (A.P - 1) * A.M + pc.index) * ((size_t)C::DPP * D + C::DPP);
     for (int mb = c; mb < C::NMB; mb += 2) {
       const int f = mb * 128 + 32 * (warp & 3) + lane;
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -388,13 +412,13 @@ __global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constan
   float* zx = reinterpret_cast<float*>(sm + OFF_ZX);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t unit = blockIdx.x / (A.P - 1);
+  const StatePiece pc = state_piece(A);
+  const int64_t unit = pc.unit;
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
-  const int seg = blockIdx.x % (A.P - 1);
   const int h = (int)(unit % A.H);
-  const int t_begin = seg * A.L;
-  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  const int t_begin = pc.t_begin;
+  const int nt = pc.nt;
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
 
   if (tid == 0) {
@@ -607,7 +631,7 @@ __global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constan
     // c = 1), hidden unit j, state columns [64 (w / 8), +64)
     const int c = (warp >> 2) & 1;
     const int j = 32 * (warp & 3) + lane;
-    float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)2 * D * D + 2 * D);
+    float* dst = A.ws + ((size_t)unit * (A.P - 1) * A.M + pc.index) * ((size_t)2 * D * D + 2 * D);
     const int f = 128 * c + j;
 #pragma unroll 1
     for (int c0 = 64 * (warp >> 3); c0 < 64 * (warp >> 3) + 64; c0 += 32) {
@@ -631,9 +655,12 @@ __global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constan
 // ---------------------------------------------------------------------------
 // Taylor, d = 16.  The state is kept over the 160 packed features of
 // taylor_pack.cuh (the same dot products as the 288 public ones).  phi(K_t)
-// is built row-wise (thread = token) into one of two shared-memory buffers,
-// so tile t+1's features are written while G2(t) still reads tile t's.  The
-// state is kept transposed, so one MMA per 16 tokens spans every feature:
+// is built row-wise (thread = token, its 32-byte row of K loaded from global
+// memory a tile ahead) into one of two shared-memory buffers, so tile t+1's
+// features are written while G2(t) still reads tile t's.  With ~109 KB of
+// shared memory and 256 TMEM columns two CTAs share an SM, so the pass runs
+// one piece of a segment per CTA over both slots of every SM.  The state is
+// kept transposed, so one MMA per 16 tokens spans every feature:
 //   [S z]^T += [V_t e0]^T phi(K_t)   (M = 64, N = 160, e0 = (1, 0, ..., 0))
 // [V e0]^T is the MN-major [V e0] tile read as A: rows 0-15 are V's columns,
 // row 16 the ones of e0 (z), rows 17-31 zero and rows 32-63 whatever lies
@@ -644,22 +671,22 @@ __global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constan
 namespace tay {
 constexpr int DP = tp::F;                              // packed features (153 used)
 constexpr uint32_t XT = TILE * 16 * 2;                 // 4 KB
-constexpr uint32_t OFF_K = 0;                          // 2 stages, 32 B rows
-constexpr uint32_t OFF_V = 8192;                       // 2 stages, 32B-swizzled
-constexpr uint32_t OFF_E0 = 16384;                     // [128 x 16], column 0 = 1
-constexpr uint32_t OFF_PHK = 24576;                    // 2 buffers x 4 panels of 16 KB
-constexpr uint32_t PHK_BYTES = 4 * 16384;              // features 160..255 stay zero
-constexpr uint32_t OFF_BAR = OFF_PHK + 2 * PHK_BYTES;
-enum { B_LDK = 0, B_LDV = 2, B_E1 = 4, B_G2 = 6, B_COUNT = 8 };
+constexpr uint32_t OFF_V = 0;                          // 2 stages, 32B-swizzled
+constexpr uint32_t OFF_E0 = 8192;                      // [128 x 16], column 0 = 1
+constexpr int NB = 2;                                  // phi(K) buffers
+constexpr uint32_t OFF_PHK = 12288;                    // NB buffers x 3 panels of 16 KB
+constexpr uint32_t PHK_BYTES = 3 * 16384;              // features 160..191 stay zero
+constexpr uint32_t OFF_BAR = OFF_PHK + NB * PHK_BYTES;
+enum { B_LDV = 0, B_E1 = 2, B_G2 = 4, B_COUNT = 6 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
-static_assert(ALLOC <= 227 * 1024, "shared memory");
+static_assert(ALLOC <= 113 * 1024, "shared memory: two CTAs per SM");
 constexpr uint32_t TM_S = 0;                           // [S z]^T: 160 feature columns
-constexpr uint32_t TM_COLS = 256;
+constexpr uint32_t TM_COLS = 256;                      // two CTAs per SM
 constexpr int kThreads = 320;
 }  // namespace tay
 
-__global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_constant__ StateArgs A) {
+__global__ void __launch_bounds__(tay::kThreads, 2) state_taylor_kernel(const __grid_constant__ StateArgs A) {
   using namespace tay;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -671,13 +698,13 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t unit = blockIdx.x / (A.P - 1);
+  const StatePiece pc = state_piece(A);
+  const int64_t unit = pc.unit;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // k, v of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
-  const int seg = blockIdx.x % (A.P - 1);
-  const int t_begin = seg * A.L;
-  const int nt = min(A.NT, t_begin + A.L) - t_begin;
+  const int t_begin = pc.t_begin;
+  const int nt = pc.nt;
   WaitPolicy wp{A.soft_ns, A.hard_ns, A.dev_status, abort_flag};
 
   if (tid == 0) {
@@ -697,12 +724,6 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   pdl_launch_dependents();
   pdl_wait();
   __syncthreads();
-  auto load_k = [&](int i) {
-    const uint32_t b = bar(B_LDK + (i & 1));
-    mbar_expect_tx(b, XT);
-    tma_load_rows(sb + OFF_K + (i & 1) * XT, &A.tk, b, 0, (t_begin + i) * TILE, ub,
-                    kh, A.seq);
-  };
   auto load_v = [&](int i) {
     const uint32_t b = bar(B_LDV + (i & 1));
     mbar_expect_tx(b, XT);
@@ -710,10 +731,10 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
                     kh, A.seq);
   };
   if (warp == 8 && lane == 0)
-    for (int i = 0; i < 2 && i < nt; ++i) {
-      load_k(i);
-      load_v(i);
-    }
+    for (int i = 0; i < 2 && i < nt; ++i) load_v(i);
+  // the rest of the piece's K rows into L2 for the feature warps' loads
+  if (warp == 9 && lane == 0)
+    for (int i = 2; i < nt; ++i) tma_prefetch_rows(&A.tk, 0, (t_begin + i) * TILE, ub, kh, A.seq);
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     tmem_relinquish();
@@ -724,7 +745,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     st_shared_v4(sb + OFF_E0 + r * 32 + c0, 0x3F80u, 0u, 0u, 0u);
     st_shared_v4(sb + OFF_E0 + r * 32 + (16 - c0), 0u, 0u, 0u, 0u);
   }
-  for (uint32_t i = tid * 16; i < 2 * PHK_BYTES; i += tay::kThreads * 16)
+  for (uint32_t i = tid * 16; i < NB * PHK_BYTES; i += tay::kThreads * 16)
     st_shared_v4(sb + OFF_PHK + i, 0u, 0u, 0u, 0u);
   fence_proxy_async();
   tc_fence_before();
@@ -752,7 +773,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
              mbar_wait_poll(bar(B_LDV + (i & 1)), (i >> 1) & 1, wp);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t pb = sb + OFF_PHK + (i & 1) * PHK_BYTES;
+        const uint32_t pb = sb + OFF_PHK + (i % NB) * PHK_BYTES;
         const uint32_t vb = sb + OFF_V + (i & 1) * XT;
         // A = [V e0]^T: 16-row blocks one leading-byte offset apart (V, e0,
         // then two blocks never read back); B = phi(K), 64-feature panels
@@ -767,38 +788,53 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
     }
   } else if (warp == 9) {
     // ======================= loader =======================
-    //   K(i) once the feature warps have read K(i-2); V(i) once G2(i-2) has read V(i-2)
+    //   V(i) once G2(i-2) has read V(i-2)
     if (lane == 0) {
-      int nk = nt < 2 ? nt : 2, nv = nk;
+      int nv = nt < 2 ? nt : 2;
       IdleClock clk;
       bool alive = true;
-      while ((nk < nt || nv < nt) && alive) {
-        bool progress = false;
-        if (nk < nt && mbar_probe(bar(B_E1 + (nk & 1)), ((nk - 2) >> 1) & 1)) {
-          load_k(nk++);
-          progress = true;
-        }
-        if (nv < nt && mbar_probe(bar(B_G2 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
+      while (nv < nt && alive) {
+        if (mbar_probe(bar(B_G2 + (nv & 1)), ((nv - 2) >> 1) & 1)) {
           load_v(nv++);
-          progress = true;
+          clk.progress();
+        } else {
+          alive = clk.idle(wp);
         }
-        if (progress) clk.progress();
-        else alive = clk.idle(wp);
       }
     }
   } else {
     // ======================= feature warps =======================
     const int c = warp >> 2;
     const int row = 32 * (warp & 3) + lane;
+    // this thread's token rows of K: [B][Hkv][n][16], or [B][n][Hkv][16]
+    const int hkv = A.H / A.G;
+    const size_t rs = A.seq ? (size_t)hkv * 16 : 16;
+    const __nv_bfloat16* kb = A.kraw + (A.seq ? ((size_t)ub * A.n * hkv + kh) * 16
+                                              : ((size_t)ub * hkv + kh) * (size_t)A.n * 16);
+    auto load_row = [&](int i, uint4& lo, uint4& hi) {
+      const int64_t t = (int64_t)(t_begin + i) * TILE + row;
+      if (t < A.n) {
+        const uint4* src = reinterpret_cast<const uint4*>(kb + (size_t)t * rs);
+        lo = __ldg(src);
+        hi = __ldg(src + 1);
+      } else {
+        lo = hi = make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    uint4 nlo, nhi;
+    if (nt > 0) load_row(0, nlo, nhi);
     for (int i = 0; i < nt; ++i) {
       const int b = i & 1;
       const bool valid = (int64_t)(t_begin + i) * TILE + row < A.n;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_LDK + b), (i >> 1) & 1, wp))) break;
-      const __nv_bfloat16* krow =
-          reinterpret_cast<const __nv_bfloat16*>(sm + OFF_K + b * XT) + row * 16;
+      const uint4 klo = nlo, khi = nhi;
+      if (i + 1 < nt) load_row(i + 1, nlo, nhi);   // in flight while this tile's features form
+      const uint32_t kw[8] = {klo.x, klo.y, klo.z, klo.w, khi.x, khi.y, khi.z, khi.w};
       float x[16];
 #pragma unroll
-      for (int k2 = 0; k2 < 16; ++k2) x[k2] = __bfloat162float(krow[k2]);
+      for (int k2 = 0; k2 < 8; ++k2) {
+        x[2 * k2] = __uint_as_float(kw[k2] << 16);
+        x[2 * k2 + 1] = __uint_as_float(kw[k2] & 0xFFFF0000u);
+      }
       // packed features: half 0 [0, 80), half 1 [80, 160); 16-byte chunks of 8
       uint32_t w[10][4];
       if (c == 0) {
@@ -814,10 +850,11 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
         tp::chunk8<128>(x, valid, w[6]); tp::chunk8<136>(x, valid, w[7]);
         tp::chunk8<144>(x, valid, w[8]); tp::chunk8<152>(x, valid, w[9]);
       }
-      // buffer b held phi(K(i-2)), read by G2(i-2)
-      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B_G2 + b), ((i - 2) >> 1) & 1, wp)))
+      // the buffer held phi(K(i-NB)), read by G2(i-NB)
+      if (i >= NB && !__all_sync(0xffffffffu,
+                                 mbar_wait(bar(B_G2 + ((i - NB) & 1)), ((i - NB) >> 1) & 1, wp)))
         break;
-      const uint32_t phk = sb + OFF_PHK + b * PHK_BYTES;
+      const uint32_t phk = sb + OFF_PHK + (i % NB) * PHK_BYTES;
 #pragma unroll
       for (int q = 0; q < 10; ++q) {
         const int f = 80 * c + 8 * q;
@@ -840,7 +877,7 @@ __global__ void __launch_bounds__(384, 1) state_taylor_kernel(const __grid_const
   // S^T row v (TMEM lane v < 16, warp 0) holds column v of S over the 160
   // features; row 16 (lane 32, warp 1) holds z
   if (warp < 2 && !*(volatile int*)abort_flag) {
-    float* dst = A.ws + ((size_t)unit * (A.P - 1) + seg) * ((size_t)DP * 16 + DP);
+    float* dst = A.ws + ((size_t)unit * (A.P - 1) * A.M + pc.index) * ((size_t)DP * 16 + DP);
 #pragma unroll 1
     for (int c0 = 0; c0 < DP; c0 += 32) {
       uint32_t sv[32];
@@ -879,7 +916,10 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
                        p.seq_major);
   }
   if (!ok) return cudaErrorInvalidValue;
-  a.ws = reinterpret_cast<float*>(ws);
+  // one segment per CTA: the states go straight to the scanned area; pieces
+  // of segments: to the area after it, which the scan sums per segment
+  a.ws = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + (pl.M > 1 ? pl.raw_offset : 0));
+  a.kraw = reinterpret_cast<const __nv_bfloat16*>(k);
   a.bias = p.Wk ? p.bk : p.bq;
   a.off = p.offk;
   if (p.softmax && !p.offk) return cudaErrorInvalidValue;
@@ -891,14 +931,20 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
   a.P = pl.P;
   a.L = pl.L;
   a.NT = pl.NT;
+  a.M = pl.M;
   a.G = p.G;
   a.seq = p.seq_major;
+  const dim3 grid((unsigned)(U * (pl.P - 1) * pl.M));
   if (KIND == HH_FMAP_TAYLOR2) {
     cudaError_t e = cudaFuncSetAttribute(state_taylor_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tay::ALLOC);
+    // two CTAs per SM need the largest shared-memory carveout
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(state_taylor_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               100);
     if (e != cudaSuccess) return e;
-    return launch_pdl(state_taylor_kernel, dim3((unsigned)(U * (pl.P - 1))), dim3(tay::kThreads),
+    return launch_pdl(state_taylor_kernel, grid, dim3(tay::kThreads),
                       (size_t)tay::ALLOC, s, a);
   }
   if (KIND == HH_FMAP_HEDGEHOG && D == 128) {
@@ -906,7 +952,7 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)t128::ALLOC);
     if (e != cudaSuccess) return e;
-    return launch_pdl(state_t128_kernel, dim3((unsigned)(U * (pl.P - 1))), dim3(t128::kThreads),
+    return launch_pdl(state_t128_kernel, grid, dim3(t128::kThreads),
                       (size_t)t128::ALLOC, s, a);
   }
   if constexpr (KIND == HH_FMAP_HEDGEHOG && D == 64) {
@@ -914,7 +960,7 @@ cudaError_t state_t(const Problem& p, const TcPlan& pl, const void* k, const voi
     cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(state_tc_kernel<D>, dim3((unsigned)(U * (pl.P - 1))), dim3(kThreads), smem, s, a);
+    return launch_pdl(state_tc_kernel<D>, grid, dim3(kThreads), smem, s, a);
   }
   return cudaErrorInvalidValue;
 }

@@ -58,7 +58,9 @@ def test_segment_count_does_not_change_the_result(case, segments, env):
     w, x, xd, fm = _setup(case, seed=31)
     P, launches = hh.fwd_plan(fm, w.torch_dtype, w.B, w.H, w.n, 64)
     assert P == min(segments, (w.n + 127) // 128) or P <= segments
-    assert launches == (1 if P == 1 else (2 if P == 2 else 3))
+    # state pass and output pass, plus the scan for more than two segments or
+    # for a state pass split into pieces (the Taylor default)
+    assert launches in ((1,) if P == 1 else ((2, 3) if P == 2 else (3,)))
     y, S, z = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"], chunk=64, return_state=True)
     torch.cuda.synchronize()
     W = None if x["W"] is None else f64(x["W"])
@@ -73,6 +75,30 @@ def test_segment_count_does_not_change_the_result(case, segments, env):
         assert np.linalg.norm(Sg[:dp] - S_ref) <= BF16_TOL * np.linalg.norm(S_ref)
         assert np.linalg.norm(zg[:dp] - z_ref) <= BF16_TOL * np.linalg.norm(z_ref)
         assert np.all(Sg[dp:] == 0) and np.all(zg[dp:] == 0)
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("pieces", [1, 2, 5])
+def test_state_pass_pieces_do_not_change_the_result(case, pieces, env):
+    # each segment's state summed by up to `pieces` CTAs (at most one per
+    # tile) and the pieces added up by the scan: the same result
+    env.setenv("HH_PREFILL_SEGMENTS", "3")
+    env.setenv("HH_STATE_PIECES", str(pieces))
+    w, x, xd, fm = _setup(case, seed=32)
+    P, launches = hh.fwd_plan(fm, w.torch_dtype, w.B, w.H, w.n, 64)
+    assert P == 3 and launches == 3
+    y, S, z = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"], return_state=True)
+    torch.cuda.synchronize()
+    W = None if x["W"] is None else f64(x["W"])
+    b = None if x["b"] is None else f64(x["b"])
+    y_ref = O.fwd_causal(w.kind, f64(x["q"]), f64(x["k"]), f64(x["v"]), W, b)
+    assert rel_l2_per_head(f64(y), y_ref) <= BF16_TOL
+    for h in range(w.H):
+        pk = _phi(w, x, "k", h)
+        S_ref = pk.T @ f64(x["v"])[0, h]
+        dp = pk.shape[1]
+        Sg = f64(S)[0, h]
+        assert np.linalg.norm(Sg[:dp] - S_ref) <= BF16_TOL * np.linalg.norm(S_ref)
 
 
 def test_plan_splits_long_sequences():
