@@ -432,10 +432,11 @@ hh_status hh_mimicry_stats(const hh_fmap* fmap, int dtype, const void* q, const 
 // Workspace of hh_mimicry_loss_grad.
 //   tensor-core path (bf16, d in {64, 128}): phi(q) | phi(k) | row stats
 //     [U][NT*128] (c_i, 1/A_i) | loss partials [U][NT] | loss sums [U] |
-//     per-CTA dW, db shares [2][U][NT][d*d + d]
+//     per-CTA dW, db shares [2][U][NT][d*d + d] | the causal 128 x 128 tiles
+//     of g in bf16 [U][NT (NT + 1) / 2][128][128]
 //   CUDA-core path: phi(q) | phi(k) | row stats [U][n][3] | dL/dh(q) | dL/dh(k)
 struct GradWs {
-  size_t phi, stats, a, b, c, total;
+  size_t phi, stats, a, b, c, g, total;
 };
 static GradWs loss_grad_ws(const Problem& p) {
   GradWs w;
@@ -447,12 +448,13 @@ static GradWs loss_grad_ws(const Problem& p) {
     w.a = align256(U * NT * sizeof(float));
     w.b = align256(U * sizeof(float));
     w.c = align256(loss_grad_tc_partial_floats(p) * sizeof(float));
+    w.g = align256(loss_grad_tc_g_bytes(p));
   } else {
     w.stats = align256(U * p.n * 3 * sizeof(float));
     w.a = w.b = align256(U * p.n * p.d * sizeof(float));
-    w.c = 0;
+    w.c = w.g = 0;
   }
-  w.total = 2 * w.phi + w.stats + w.a + w.b + w.c;
+  w.total = 2 * w.phi + w.stats + w.a + w.b + w.c + w.g;
   return w;
 }
 
@@ -505,6 +507,7 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   float* wa = (float*)(ws + 2 * w.phi + w.stats);
   float* wb = (float*)(ws + 2 * w.phi + w.stats + w.a);
   float* wc = (float*)(ws + 2 * w.phi + w.stats + w.a + w.b);
+  void* wg = ws + 2 * w.phi + w.stats + w.a + w.b + w.c;
   cudaError_t e;
   if (fmap_tc_supported(p)) {
     e = launch_fmap_tc_qk(p, q, k, phq, phk, nullptr, nullptr, dev_status, s);
@@ -513,11 +516,12 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
     if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, nullptr, s);
   }
   if (tc) {
-    // wa: loss partials, wb: loss sums, wc: dW, db shares
+    // wa: loss partials, wb: loss sums, wc: dW, db shares, wg: G tiles
     if (e == cudaSuccess)
       e = launch_loss_tc(p, q, k, phq, phk, nullptr, wa, wb, stats, nullptr, dev_status, s);
     if (e == cudaSuccess)
-      e = launch_loss_grad_tc(p, q, k, phq, phk, stats, wc, dWq, dbq, dWk, dbk, dev_status, s);
+      e = launch_loss_grad_tc(p, q, k, phq, phk, stats, wc, wg, dWq, dbq, dWk, dbk, dev_status,
+                              s);
   } else if (e == cudaSuccess) {
     // wa, wb: dL/dh of the query and key rows
     e = launch_loss_grad(p, q, k, phq, phk, stats, wa, wb, dWq, dbq, dWk, dbk, s);

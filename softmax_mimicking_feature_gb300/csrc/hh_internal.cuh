@@ -204,13 +204,16 @@ int loss_tc_tile();
 // {64, 128}: from phi(q), phi(k) and the loss kernel's row stats, per-CTA
 // dW, db shares in `part` (loss_grad_tc_partial_floats floats), then summed
 // per head in a fixed order into dWq, dbq (and dWk, dbk for a separate key map).
+// gbuf (loss_grad_tc_g_bytes, or null to form g on both sides): the causal
+// tiles of G, written by the query side and read back by the key side.
 bool loss_grad_tc_shape(const Problem& p);
 bool loss_grad_tc_supported(const Problem& p);
 size_t loss_grad_tc_smem_bytes(const Problem& p);
 size_t loss_grad_tc_partial_floats(const Problem& p);
+size_t loss_grad_tc_g_bytes(const Problem& p);
 cudaError_t launch_loss_grad_tc(const Problem& p, const void* q, const void* k, const void* phq,
-                                const void* phk, const float* stats, float* part, float* dWq,
-                                float* dbq, float* dWk, float* dbk, int* dev_status,
+                                const void* phk, const float* stats, float* part, void* gbuf,
+                                float* dWq, float* dbq, float* dWk, float* dbk, int* dev_status,
                                 cudaStream_t s);
 // dW[h] = sum x^T dh, db[h] = sum dh over the batch (CUDA cores); with one
 // shared map (dWk null) both sides go into dWq, dbq.

@@ -11,7 +11,11 @@
 //
 // grad_tc_kernel: one CTA per 128-row resident tile, query side (resident
 // queries, streamed keys) or key side (resident keys, streamed later
-// queries), both sides in one launch.  Per 64-row streamed step:
+// queries).  Given room for G in the workspace the query side runs first and
+// stores every causal 128 x 128 tile of G (bf16, the values its own
+// dPhi product uses), and the key side, a second launch, streams those tiles
+// with phi(q) instead of forming S, A and g again: each pair is scored once.
+// Otherwise both sides form g, in one launch.  Per 64-row streamed step:
 //   S = X Y^T and A = phi(X) phi(Y)^T on tcgen05 into one of two TMEM stages;
 //   eight epilogue warps turn (S, A) and the query rows' (c_i, 1/A_i) from the
 //   loss kernel (p_ij = 2^(s_ij log2e / sqrt d - c_i)) into g, rounded to bf16
@@ -54,8 +58,12 @@ constexpr int kIssuerWarp = 8, kLoaderWarp = 9;
 struct GradArgs {
   // [0]: query side (X = q, Y = k), [1]: key side (X = k, Y = q)
   CUtensorMap tx[2], tpx[2], ty[2], tpy[2];
+  CUtensorMap tg;        // G tiles as [tile][128 query rows][128 keys], 64 x 64 boxes
   const float2* stats;   // [U][npad] (c_i, 1/A_i) of the query rows
   float* part;           // [2][U][NT][D * D + D] per-CTA dW, db shares
+  __nv_bfloat16* gbuf;   // [U][NT (NT + 1) / 2][128][128]: G tile (i, j <= i) at i (i + 1) / 2 + j
+  int sides;             // 0: both sides form g; 1: query side, storing G; 2: key side, reading G
+  int64_t ntt;           // G tiles per unit, NT (NT + 1) / 2
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n, U;
@@ -76,12 +84,18 @@ struct GradCfg {
   static constexpr uint32_t Y_BYTES = kST * D * 2;
   static constexpr uint32_t PY_BYTES = kST * DP * 2;
   static constexpr uint32_t ST_BYTES = kST * 8;
+  // a stored G chunk, 64 query rows x 128 keys: two 8 KB panels of 64 keys
+  static constexpr uint32_t G_BYTES = kST * kRT * 2;
   static constexpr uint32_t OFF_X = 0;                       // D/64 panels of 16 KB
   static constexpr uint32_t OFF_PX = OFF_X + X_BYTES;        // DP/64 panels of 16 KB
   static constexpr uint32_t OFF_Y = OFF_PX + PX_BYTES;       // 2 stages, D/64 panels of 8 KB
   static constexpr uint32_t OFF_PY = OFF_Y + 2 * Y_BYTES;    // 3 stages, DP/64 panels of 8 KB
   static constexpr uint32_t OFF_ST = OFF_PY + 3 * PY_BYTES;  // 3 stages of 64 (c, 1/A)
-  static constexpr uint32_t OFF_BAR = OFF_ST + 3 * ST_BYTES; // 18 barriers
+  // G chunks (key side reading G, 2 stages): over the Y stages, which that
+  // side does not load, where they fit (D = 128), else after the stats
+  static constexpr bool G_IN_Y = Y_BYTES >= G_BYTES;
+  static constexpr uint32_t OFF_GS = G_IN_Y ? OFF_Y : (OFF_ST + 3 * ST_BYTES + 1023) / 1024 * 1024;
+  static constexpr uint32_t OFF_BAR = G_IN_Y ? OFF_ST + 3 * ST_BYTES : OFF_GS + 2 * G_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 18 * 8;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
   // end phase: dL/dh as bf16 hi and lo tiles [128 rows][D] (MN-major, 16 KB
@@ -159,14 +173,18 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Units in groups of HG; within a group heavy tiles first, the two sides
-  // interleaved.  The CTAs in flight then stream the rows of a few heads
-  // only, which stay in L2 across that group's tiles.
-  const int64_t GT = 2 * (int64_t)A.HG * A.NT;
+  // interleaved (when one launch holds both).  The CTAs in flight then
+  // stream the rows of a few heads only, which stay in L2 across that
+  // group's tiles.
+  const int nsides = A.sides == 0 ? 2 : 1;
+  const int64_t GT = nsides * (int64_t)A.HG * A.NT;
   const int64_t grp = blockIdx.x / GT, within = blockIdx.x % GT;
   const int64_t gsz = min((int64_t)A.HG, A.U - grp * A.HG);
-  const int side = (int)(within & 1);
-  const int rank = (int)((within >> 1) / gsz);
-  const int64_t unit = grp * A.HG + (within >> 1) % gsz;
+  const int side = A.sides == 0 ? (int)(within & 1) : A.sides - 1;
+  const int64_t wu = A.sides == 0 ? within >> 1 : within;
+  const int rank = (int)(wu / gsz);
+  const int64_t unit = grp * A.HG + wu % gsz;
+  const bool store_g = A.sides == 1, read_g = A.sides == 2;
   const int64_t kvu = kv_unit(unit, A.H, A.G);   // raw k of this query head
   // batch, query head and key/value head of this unit (split once)
   const int ub = (int)(unit / A.H), uh = (int)(unit % A.H), kh = uh / A.G;
@@ -219,23 +237,35 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
                       ub, side ? kh : uh, A.seq);
       for (int i = 0; i < DP / 64; ++i)
         tma_load_3d(sb + C::OFF_PX + i * 16384, &A.tpx[side], bar_x, 64 * i, (int)r0, (int)unit);
-      // Y(t) after S/A(t-2) read its stage; phi(Y)(t) after G phi(Y)(t-3)
+      // Y(t) (or the G chunk) after S/A(t-2) (or G phi(Y)(t-2)) read its
+      // stage; phi(Y)(t) after G phi(Y)(t-3)
       for (int t = 0; t < T && ok; ++t) {
         const int s = t & 1, p = t % 3;
         const int64_t y0 = y_begin + (int64_t)t * kST;
         if (t >= 2) ok = mbar_wait_poll(bar_sa + 8 * s, ((t >> 1) - 1) & 1, wp);
         if (!ok) break;
-        mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
-        for (int i = 0; i < D / 64; ++i)
-          tma_load_rows(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
-                        64 * i, (int)y0, ub, side ? uh : kh, A.seq);
+        if (read_g) {
+          // rows y0 .. y0 + 63 of G tile (query tile y0 / 128, key tile rt)
+          const int qi = (int)(y0 / kRT);
+          const int tile = (int)(unit * A.ntt + (int64_t)qi * (qi + 1) / 2 + rt);
+          mbar_expect_tx(bar_y + 8 * s, C::G_BYTES);
+          for (int i = 0; i < 2; ++i)
+            tma_load_3d(sb + C::OFF_GS + s * C::G_BYTES + i * 8192, &A.tg, bar_y + 8 * s, 64 * i,
+                        (int)(y0 % kRT), tile);
+        } else {
+          mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
+          for (int i = 0; i < D / 64; ++i)
+            tma_load_rows(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
+                          64 * i, (int)y0, ub, side ? uh : kh, A.seq);
+        }
         if (t >= 3) ok = mbar_wait_poll(bar_pyfree + 8 * p, (t / 3 - 1) & 1, wp);
         if (!ok) break;
-        mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (side ? C::ST_BYTES : 0));
+        const bool with_stats = side && !read_g;
+        mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (with_stats ? C::ST_BYTES : 0));
         for (int i = 0; i < DP / 64; ++i)
           tma_load_3d(sb + C::OFF_PY + p * C::PY_BYTES + i * 8192, &A.tpy[side], bar_py + 8 * p,
                       64 * i, (int)y0, (int)unit);
-        if (side)
+        if (with_stats)
           bulk_load(sb + C::OFF_ST + p * C::ST_BYTES, A.stats + unit * A.npad + y0, C::ST_BYTES,
                     bar_py + 8 * p);
       }
@@ -271,7 +301,29 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         return true;
       };
       bool ok = mbar_wait_poll(bar_x, 0, wp);
-      for (int t = 0; t < T && ok; ++t) {
+      if (read_g) {
+        // dPhi += G^T phi(Y): A = the stored G chunk as an MN-major operand
+        // (keys contiguous: 64-key panels 8 KB apart, 8-row groups 1 KB
+        // apart), B = phi(Y) MN-major as above; 16 query rows per k-step
+        constexpr uint32_t ID_GS = idesc_bf16(128, DP, 1, 1);
+        for (int t = 0; t < T && ok; ++t) {
+          const int s = t & 1, p = t % 3;
+          ok = mbar_wait_poll(bar_y + 8 * s, (t >> 1) & 1, wp) &&
+               mbar_wait_poll(bar_py + 8 * p, (t / 3) & 1, wp);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dG = smem_desc(sb + C::OFF_GS + s * C::G_BYTES, 8192, 1024, 2);
+          const uint64_t dPYmn = smem_desc(sb + C::OFF_PY + p * C::PY_BYTES, 8192, 1024, 2);
+#pragma unroll
+          for (int ks = 0; ks < kST / 16; ++ks)
+            mma_ss(tmem + C::TM_ACC, dG + 128 * ks, dPYmn + 128 * ks, ID_GS,
+                   (t > 0 || ks > 0) ? 1 : 0);
+          mma_commit(bar_sa + 8 * s);   // the G stage is free
+          mma_commit(bar_pyfree + 8 * p);
+        }
+        if (ok) mma_commit(bar_acc);
+      }
+      for (int t = 0; t < (read_g ? 0 : T) && ok; ++t) {
         const int s = t & 1, p = t % 3;
         ok = mbar_wait_poll(bar_y + 8 * s, (t >> 1) & 1, wp);
         ok = ok && mbar_wait_poll(bar_py + 8 * p, (t / 3) & 1, wp);
@@ -292,8 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         mma_commit(bar_sa + 8 * s);
         if (t >= 1) ok = issue_g(t - 1);
       }
-      if (ok) ok = issue_g(T - 1);
-      if (ok) mma_commit(bar_acc);
+      if (!read_g && ok) {
+        ok = issue_g(T - 1);
+        if (ok) mma_commit(bar_acc);
+      }
     }
   } else {
     // ---------------- epilogue warps ----------------
@@ -308,7 +362,12 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       ia_row = st.y;
     }
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    // this thread's row of the stored G tiles (query side): tile (rt, j) at
+    // rt (rt + 1) / 2 + j, row `row`, 128 keys
+    __nv_bfloat16* grow = store_g ? A.gbuf + ((size_t)unit * A.ntt + (size_t)rt * (rt + 1) / 2) *
+                                                 (size_t)(kRT * kRT) + (size_t)row * kRT
+                                  : nullptr;
+    for (int t = 0; t < (read_g ? 0 : T); ++t) {
       const int s = t & 1, p = t % 3;
       if (!mbar_wait(bar_sa + 8 * s, (t >> 1) & 1, wp)) { ok = false; break; }
       tc_fence_after();
@@ -340,6 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         make_g<true>(sv, av, c_row, ia_row, stc, lo, hi, A.s_scale, gw);
       else
         make_g<false>(sv, av, c_row, ia_row, stc, lo, hi, A.s_scale, gw);
+      if (store_g) {   // keys cbase .. cbase + 31: key tile cbase / 128
+        uint4* d4 = reinterpret_cast<uint4*>(grow + (size_t)(cbase / kRT) * (kRT * kRT) +
+                                             (int)(cbase % kRT));
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4)
+          d4[w4] = make_uint4(gw[4 * w4], gw[4 * w4 + 1], gw[4 * w4 + 2], gw[4 * w4 + 3]);
+      }
       if (C::SEP_G) {
         // G stage s: free once G phi(Y) of step t-2 is done
         if (t >= 2 && !mbar_wait(bar_gphi + 8 * s, ((t >> 1) - 1) & 1, wp)) { ok = false; break; }
@@ -352,6 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_g + 8 * s);
+    }
+    // a last query tile of at most 64 rows streams only the first 64 keys of
+    // its diagonal tile: the other 64 (all past the sequence) are stored as
+    // zeros, so that the key side reads written values only
+    if (store_g && (int64_t)T * kST < r0 + kRT) {
+      uint4* d4 = reinterpret_cast<uint4*>(grow + (size_t)rt * (kRT * kRT) +
+                                           (int)((int64_t)T * kST - r0) + 32 * half);
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) d4[w4] = make_uint4(0u, 0u, 0u, 0u);
     }
     ok = ok && mbar_wait(bar_acc, 0, wp);
     if (ok) tc_fence_after();
@@ -544,8 +619,8 @@ __global__ void grad_partials_kernel(const float* __restrict__ part, float* __re
 
 template <int D>
 cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void* phq,
-                      const void* phk, const float* stats, float* part, int* dev_status,
-                      cudaStream_t s) {
+                      const void* phk, const float* stats, float* part, void* gbuf,
+                      int* dev_status, cudaStream_t s) {
   GradArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
@@ -562,9 +637,15 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
                        p.seq_major) &&
          make_plane_map(&a.tpy[side], px[1 - side], 2 * D, p.n, U, 64, kST, sw);
   }
+  a.NT = ceil_div(p.n, kRT);
+  a.ntt = (int64_t)a.NT * (a.NT + 1) / 2;
+  if (gbuf)
+    ok = ok && make_plane_map(&a.tg, gbuf, kRT, kRT, U * (uint64_t)a.ntt, 64, kST,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   a.stats = reinterpret_cast<const float2*>(stats);
   a.part = part;
+  a.gbuf = reinterpret_cast<__nv_bfloat16*>(gbuf);
   a.dev_status = dev_status;
   a.soft_ns = wait_soft_limit_ns();
   a.hard_ns = std::max<uint64_t>(a.soft_ns, 4000000000ull);
@@ -584,7 +665,6 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
     a.HG = (int)g;
   }
   a.seq = p.seq_major;
-  a.NT = ceil_div(p.n, kRT);
   a.npad = a.NT * kRT;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   a.softmax = p.softmax ? 1 : 0;
@@ -592,7 +672,16 @@ cudaError_t grad_tc_t(const Problem& p, const void* q, const void* k, const void
   cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(grad_tc_kernel<D>, dim3((unsigned)(2 * U * a.NT)), dim3(kThreads), smem, s, a);
+  if (!gbuf) {
+    a.sides = 0;
+    return launch_pdl(grad_tc_kernel<D>, dim3((unsigned)(2 * U * a.NT)), dim3(kThreads), smem, s, a);
+  }
+  // the query side stores G; the key side, launched after it, reads it
+  a.sides = 1;
+  e = launch_pdl(grad_tc_kernel<D>, dim3((unsigned)(U * a.NT)), dim3(kThreads), smem, s, a);
+  if (e != cudaSuccess) return e;
+  a.sides = 2;
+  return launch_pdl(grad_tc_kernel<D>, dim3((unsigned)(U * a.NT)), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace
@@ -613,13 +702,18 @@ size_t loss_grad_tc_partial_floats(const Problem& p) {
   return (size_t)2 * p.B * p.H * ceil_div(p.n, kRT) * ((size_t)p.d * p.d + p.d);
 }
 
+size_t loss_grad_tc_g_bytes(const Problem& p) {
+  const size_t nt = (size_t)ceil_div(p.n, kRT);
+  return (size_t)p.B * p.H * (nt * (nt + 1) / 2) * kRT * kRT * 2;
+}
+
 cudaError_t launch_loss_grad_tc(const Problem& p, const void* q, const void* k, const void* phq,
-                                const void* phk, const float* stats, float* part, float* dWq,
-                                float* dbq, float* dWk, float* dbk, int* dev_status,
+                                const void* phk, const float* stats, float* part, void* gbuf,
+                                float* dWq, float* dbq, float* dWk, float* dbk, int* dev_status,
                                 cudaStream_t s) {
   if (p.B * p.H * p.n == 0) return cudaSuccess;
-  cudaError_t e = p.d == 64 ? grad_tc_t<64>(p, q, k, phq, phk, stats, part, dev_status, s)
-                            : grad_tc_t<128>(p, q, k, phq, phk, stats, part, dev_status, s);
+  cudaError_t e = p.d == 64 ? grad_tc_t<64>(p, q, k, phq, phk, stats, part, gbuf, dev_status, s)
+                            : grad_tc_t<128>(p, q, k, phq, phk, stats, part, gbuf, dev_status, s);
   if (e != cudaSuccess) return e;
   const int per = p.d * p.d + p.d;
   const int separate = dWk != nullptr;
