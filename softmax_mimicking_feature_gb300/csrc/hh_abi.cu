@@ -517,8 +517,10 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   }
   if (tc) {
     // wa: loss partials, wb: loss sums, wc: dW, db shares, wg: G tiles
+    // the row statistics (c_i, 1/A_i) alone: no loss is returned
     if (e == cudaSuccess)
-      e = launch_loss_tc(p, q, k, phq, phk, nullptr, wa, wb, stats, nullptr, dev_status, s);
+      e = launch_loss_tc(p, q, k, phq, phk, nullptr, nullptr, nullptr, stats, nullptr, dev_status,
+                         s);
     if (e == cudaSuccess)
       e = launch_loss_grad_tc(p, q, k, phq, phk, stats, wc, wg, dWq, dbq, dWk, dbk, dev_status,
                               s);

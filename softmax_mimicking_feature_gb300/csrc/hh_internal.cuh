@@ -194,7 +194,9 @@ cudaError_t launch_fmap_tc_qk(const Problem& p, const void* q, const void* k, vo
                               cudaStream_t s);
 // stats (nullable): [U][NT * 128] pairs (c_i, 1 / A_i) with c_i = m_i + log2 Z_i,
 // so that the target weight is p_ij = 2^(s_ij log2(e) / sqrt(d) - c_i).
-// rows4 (nullable): per-row (CE, KL, H(p), H(w)).
+// rows4 (nullable): per-row (CE, KL, H(p), H(w)).  partial null (and
+// loss_rows, head_sum, rows4 null): the row statistics alone, without the
+// loss and its log a per pair.
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
                            float* stats, float4* rows4, int* dev_status, cudaStream_t s);

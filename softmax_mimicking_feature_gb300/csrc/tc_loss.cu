@@ -289,9 +289,12 @@ struct LossCfg {
 
 constexpr int kLossThreads = 320;  // 8 epilogue warps, MMA issuer warp 8, loader warp 9
 
-template <int D, bool STATS>
+// MODE 0: the loss; 1: the loss and the per-row statistics (rows4); 2: only
+// the row statistics (c_i, 1/A_i) the gradient takes (no log a, no loss).
+template <int D, int MODE>
 __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_constant__ LossArgs A) {
   using C = LossCfg<D>;
+  constexpr bool STATS = MODE == 1, ROWSTATS = MODE == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -549,6 +552,13 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float a0 = __uint_as_float(av[c + e]), a1 = __uint_as_float(av[c + e + 1]);
+            if constexpr (ROWSTATS) {
+              Z0 += ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
+              Z1 += ex2_approx(fmaf(__uint_as_float(sv[e + 1]), A.s_scale, -m));
+              A0 += a0;
+              A1 += a1;
+              continue;
+            }
             const float l0 = __log2f(a0), l1 = __log2f(a1);
             if constexpr (STATS) {
               const float s0 = __uint_as_float(sv[e]) * A.s_scale;
@@ -587,6 +597,11 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           for (int e = 0; e < 32; ++e) {
             if (e < nval) {
               const float a = __uint_as_float(av[c + e]);
+              if constexpr (ROWSTATS) {
+                Z0 += ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
+                A0 += a;
+                continue;
+              }
               const float la = __log2f(a);
               const float sl = __uint_as_float(sv[e]) * A.s_scale;
               const float p = ex2_approx(sl - m);
@@ -629,7 +644,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       const float f2 = (m2 == -INFINITY) ? 0.f : ex2_approx(m2 - mn);
       const float Zt = Z * f1 + Z2 * f2, Tt = T * f1 + T2 * f2, At = As + A2;
       const bool valid = qi < A.n;
-      const float L = valid ? (logf(At) - 0.69314718055994531f * (Tt / Zt)) : 0.f;
+      const float L = valid && !ROWSTATS ? (logf(At) - 0.69314718055994531f * (Tt / Zt)) : 0.f;
       rl_s[row] = L;
       if (valid && A.loss_rows) A.loss_rows[(size_t)unit * A.n + qi] = L;
       // row statistics for the gradient: p_ij = 2^(s_ij log2e / sqrt d - c_i)
@@ -645,7 +660,7 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       }
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (tid == 0) {
+    if (!ROWSTATS && tid == 0) {
       float acc = 0.f;
       for (int r = 0; r < kTile; ++r) acc += rl_s[r];
       A.partial[(size_t)unit * A.NT + qt] = acc;
@@ -785,11 +800,14 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.seq = p.seq_major;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   const size_t smem = LossCfg<D>::ALLOC;
-  auto kern = rows4 ? loss_tc_kernel<D, true> : loss_tc_kernel<D, false>;
+  // no loss asked for (no partial sums): the row statistics alone
+  const bool rowstats = !partial;
+  if (rowstats && (!stats || loss_rows || head_sum || rows4)) return cudaErrorInvalidValue;
+  auto kern = rows4 ? loss_tc_kernel<D, 1> : (rowstats ? loss_tc_kernel<D, 2> : loss_tc_kernel<D, 0>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3((unsigned)(U * a.NT)), dim3(kLossThreads), smem, s, a);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || rowstats) return e;
   e = launch_pdl(sum_partials_tc_kernel, dim3((unsigned)ceil_div(U, 128)), dim3(128), 0, s,
                  (const float*)partial, head_sum, (int64_t)U, a.NT);
   return e;
