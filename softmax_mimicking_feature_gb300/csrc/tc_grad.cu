@@ -91,11 +91,13 @@ struct GradCfg {
   static constexpr uint32_t OFF_Y = OFF_PX + PX_BYTES;       // 2 stages, D/64 panels of 8 KB
   static constexpr uint32_t OFF_PY = OFF_Y + 2 * Y_BYTES;    // 3 stages, DP/64 panels of 8 KB
   static constexpr uint32_t OFF_ST = OFF_PY + 3 * PY_BYTES;  // 3 stages of 64 (c, 1/A)
-  // G chunks (key side reading G, 2 stages): over the Y stages, which that
-  // side does not load, where they fit (D = 128), else after the stats
-  static constexpr bool G_IN_Y = Y_BYTES >= G_BYTES;
-  static constexpr uint32_t OFF_GS = G_IN_Y ? OFF_Y : (OFF_ST + 3 * ST_BYTES + 1023) / 1024 * 1024;
-  static constexpr uint32_t OFF_BAR = G_IN_Y ? OFF_ST + 3 * ST_BYTES : OFF_GS + 2 * G_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_ST + 3 * ST_BYTES; // 18 barriers
+  // key side reading G: RG_NS stages of [G chunk | phi(Y) chunk] from offset
+  // 0, over everything else; X and phi(X) are loaded once the last stage
+  // has been read, for the end phase only
+  static constexpr uint32_t RG_STAGE = G_BYTES + PY_BYTES;
+  static constexpr int RG_NS = OFF_BAR / RG_STAGE < 4 ? (int)(OFF_BAR / RG_STAGE) : 4;
+  static_assert(RG_NS * RG_STAGE <= OFF_BAR, "stored-G stages exceed shared memory");
   static constexpr uint32_t OFF_MISC = OFF_BAR + 18 * 8;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
   // end phase: dL/dh as bf16 hi and lo tiles [128 rows][D] (MN-major, 16 KB
@@ -167,6 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
   const uint32_t bar_gphi = bar_x + 104;    // (2) G phi(Y) of TMEM stage s done
   const uint32_t bar_acc = bar_x + 120;     // all accumulation done (one barrier)
   const uint32_t bar_free = bar_x + 128;    // (2) epilogue has read S, A of stage s (SEP_G)
+  // key side reading G: (RG_NS) stage landed / read by its MMAs, over the
+  // Y, phi(Y) and S/A barriers that side does not use (all of count 1)
+  const uint32_t rg_full = bar_x + 8, rg_empty = bar_x + 48;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
   // bar_acc is reused for the final dW / db product (phase 1)
@@ -231,41 +236,56 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
     // ---------------- loader: TMA ----------------
     if (lane == 0) {
       bool ok = true;
-      mbar_expect_tx(bar_x, C::X_BYTES + C::PX_BYTES);
-      for (int i = 0; i < D / 64; ++i)
-        tma_load_rows(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0,
-                      ub, side ? kh : uh, A.seq);
-      for (int i = 0; i < DP / 64; ++i)
-        tma_load_3d(sb + C::OFF_PX + i * 16384, &A.tpx[side], bar_x, 64 * i, (int)r0, (int)unit);
-      // Y(t) (or the G chunk) after S/A(t-2) (or G phi(Y)(t-2)) read its
-      // stage; phi(Y)(t) after G phi(Y)(t-3)
-      for (int t = 0; t < T && ok; ++t) {
+      auto load_x = [&]() {
+        mbar_expect_tx(bar_x, C::X_BYTES + C::PX_BYTES);
+        for (int i = 0; i < D / 64; ++i)
+          tma_load_rows(sb + C::OFF_X + i * 16384, &A.tx[side], bar_x, 64 * i, (int)r0,
+                        ub, side ? kh : uh, A.seq);
+        for (int i = 0; i < DP / 64; ++i)
+          tma_load_3d(sb + C::OFF_PX + i * 16384, &A.tpx[side], bar_x, 64 * i, (int)r0,
+                      (int)unit);
+      };
+      if (read_g) {
+        // rows y0 .. y0 + 63 of G tile (query tile y0 / 128, key tile rt)
+        // and of phi(Y), into stage t % RG_NS once its last reader is done
+        for (int t = 0; t < T && ok; ++t) {
+          const int s = t % C::RG_NS;
+          const int64_t y0 = y_begin + (int64_t)t * kST;
+          if (t >= C::RG_NS) ok = mbar_wait_poll(rg_empty + 8 * s, (t / C::RG_NS - 1) & 1, wp);
+          if (!ok) break;
+          const uint32_t st = sb + s * C::RG_STAGE;
+          const int qi = (int)(y0 / kRT);
+          const int tile = (int)(unit * A.ntt + (int64_t)qi * (qi + 1) / 2 + rt);
+          mbar_expect_tx(rg_full + 8 * s, C::G_BYTES + C::PY_BYTES);
+          for (int i = 0; i < 2; ++i)
+            tma_load_3d(st + i * 8192, &A.tg, rg_full + 8 * s, 64 * i, (int)(y0 % kRT), tile);
+          for (int i = 0; i < DP / 64; ++i)
+            tma_load_3d(st + C::G_BYTES + i * 8192, &A.tpy[side], rg_full + 8 * s, 64 * i,
+                        (int)y0, (int)unit);
+        }
+        // X, phi(X) over the stages once every MMA has read them
+        ok = ok && mbar_wait_poll(bar_acc, 0, wp);
+        if (ok) load_x();
+      } else {
+        load_x();
+      }
+      // Y(t) after S/A(t-2) read its stage; phi(Y)(t) after G phi(Y)(t-3)
+      for (int t = 0; t < (read_g ? 0 : T) && ok; ++t) {
         const int s = t & 1, p = t % 3;
         const int64_t y0 = y_begin + (int64_t)t * kST;
         if (t >= 2) ok = mbar_wait_poll(bar_sa + 8 * s, ((t >> 1) - 1) & 1, wp);
         if (!ok) break;
-        if (read_g) {
-          // rows y0 .. y0 + 63 of G tile (query tile y0 / 128, key tile rt)
-          const int qi = (int)(y0 / kRT);
-          const int tile = (int)(unit * A.ntt + (int64_t)qi * (qi + 1) / 2 + rt);
-          mbar_expect_tx(bar_y + 8 * s, C::G_BYTES);
-          for (int i = 0; i < 2; ++i)
-            tma_load_3d(sb + C::OFF_GS + s * C::G_BYTES + i * 8192, &A.tg, bar_y + 8 * s, 64 * i,
-                        (int)(y0 % kRT), tile);
-        } else {
-          mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
-          for (int i = 0; i < D / 64; ++i)
-            tma_load_rows(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
-                          64 * i, (int)y0, ub, side ? uh : kh, A.seq);
-        }
+        mbar_expect_tx(bar_y + 8 * s, C::Y_BYTES);
+        for (int i = 0; i < D / 64; ++i)
+          tma_load_rows(sb + C::OFF_Y + s * C::Y_BYTES + i * 8192, &A.ty[side], bar_y + 8 * s,
+                        64 * i, (int)y0, ub, side ? uh : kh, A.seq);
         if (t >= 3) ok = mbar_wait_poll(bar_pyfree + 8 * p, (t / 3 - 1) & 1, wp);
         if (!ok) break;
-        const bool with_stats = side && !read_g;
-        mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (with_stats ? C::ST_BYTES : 0));
+        mbar_expect_tx(bar_py + 8 * p, C::PY_BYTES + (side ? C::ST_BYTES : 0));
         for (int i = 0; i < DP / 64; ++i)
           tma_load_3d(sb + C::OFF_PY + p * C::PY_BYTES + i * 8192, &A.tpy[side], bar_py + 8 * p,
                       64 * i, (int)y0, (int)unit);
-        if (with_stats)
+        if (side)
           bulk_load(sb + C::OFF_ST + p * C::ST_BYTES, A.stats + unit * A.npad + y0, C::ST_BYTES,
                     bar_py + 8 * p);
       }
@@ -300,26 +320,26 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
         mma_commit(bar_pyfree + 8 * p);
         return true;
       };
-      bool ok = mbar_wait_poll(bar_x, 0, wp);
+      // (the key side reading G loads X only for the end phase)
+      bool ok = read_g || mbar_wait_poll(bar_x, 0, wp);
       if (read_g) {
         // dPhi += G^T phi(Y): A = the stored G chunk as an MN-major operand
         // (keys contiguous: 64-key panels 8 KB apart, 8-row groups 1 KB
         // apart), B = phi(Y) MN-major as above; 16 query rows per k-step
         constexpr uint32_t ID_GS = idesc_bf16(128, DP, 1, 1);
         for (int t = 0; t < T && ok; ++t) {
-          const int s = t & 1, p = t % 3;
-          ok = mbar_wait_poll(bar_y + 8 * s, (t >> 1) & 1, wp) &&
-               mbar_wait_poll(bar_py + 8 * p, (t / 3) & 1, wp);
+          const int s = t % C::RG_NS;
+          ok = mbar_wait_poll(rg_full + 8 * s, (t / C::RG_NS) & 1, wp);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t dG = smem_desc(sb + C::OFF_GS + s * C::G_BYTES, 8192, 1024, 2);
-          const uint64_t dPYmn = smem_desc(sb + C::OFF_PY + p * C::PY_BYTES, 8192, 1024, 2);
+          const uint32_t st = sb + s * C::RG_STAGE;
+          const uint64_t dG = smem_desc(st, 8192, 1024, 2);
+          const uint64_t dPYmn = smem_desc(st + C::G_BYTES, 8192, 1024, 2);
 #pragma unroll
           for (int ks = 0; ks < kST / 16; ++ks)
             mma_ss(tmem + C::TM_ACC, dG + 128 * ks, dPYmn + 128 * ks, ID_GS,
                    (t > 0 || ks > 0) ? 1 : 0);
-          mma_commit(bar_sa + 8 * s);   // the G stage is free
-          mma_commit(bar_pyfree + 8 * p);
+          mma_commit(rg_empty + 8 * s);
         }
         if (ok) mma_commit(bar_acc);
       }
@@ -429,6 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
       for (int w4 = 0; w4 < 4; ++w4) d4[w4] = make_uint4(0u, 0u, 0u, 0u);
     }
     ok = ok && mbar_wait(bar_acc, 0, wp);
+    // the key side reading G loads X, phi(X) only now
+    if (read_g) ok = ok && mbar_wait(bar_x, 0, wp);
     if (ok) tc_fence_after();
     // softmax map: the row dots <dPhi_+, phi_+>, <dPhi_-, phi_->, from this
     // thread's half of the columns and the partner warp's (warp ^ 4)
