@@ -403,7 +403,7 @@ static hh_status mimicry_loss_impl(const hh_fmap* fmap, int dtype, const void* q
                         : launch_fmap_tc(p, k, 1, phk, nullptr, dev_status, s);
     if (e == cudaSuccess)
       e = launch_loss_tc(p, q, k, p.softmax ? phq : nullptr, phk, loss_rows, partial, head, nullptr,
-                         rows4, dev_status, s);
+                         rows4, nullptr, dev_status, s);
     return cuda_status(e);
   }
   cudaError_t e = launch_fmap_simt(p, q, 0, phq, nullptr, s);
@@ -431,7 +431,7 @@ hh_status hh_mimicry_stats(const hh_fmap* fmap, int dtype, const void* q, const 
 
 // Workspace of hh_mimicry_loss_grad.
 //   tensor-core path (bf16, d in {64, 128}): phi(q) | phi(k) | row stats
-//     [U][NT*128] (c_i, 1/A_i) | loss partials [U][NT] | loss sums [U] |
+//     [U][NT*128] (c_i, 1/A_i) | phi(k) column sums per tile [U][NT][2d] |
 //     per-CTA dW, db shares [2][U][NT][d*d + d] | the causal 128 x 128 tiles
 //     of g in bf16 [U][NT (NT + 1) / 2][128][128]
 //   CUDA-core path: phi(q) | phi(k) | row stats [U][n][3] | dL/dh(q) | dL/dh(k)
@@ -445,8 +445,8 @@ static GradWs loss_grad_ws(const Problem& p) {
   w.phi = align256(U * p.n * p.dpp * elem_size(p.dtype));
   if (loss_grad_tc_shape(p)) {
     w.stats = align256(U * NT * 128 * 2 * sizeof(float));
-    w.a = align256(U * NT * sizeof(float));
-    w.b = align256(U * sizeof(float));
+    w.a = align256(U * NT * 2 * p.d * sizeof(float));   // column sums of phi(k) per tile
+    w.b = 0;
     w.c = align256(loss_grad_tc_partial_floats(p) * sizeof(float));
     w.g = align256(loss_grad_tc_g_bytes(p));
   } else {
@@ -516,11 +516,11 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
     if (e == cudaSuccess) e = launch_fmap_simt(p, k, 1, phk, nullptr, s);
   }
   if (tc) {
-    // wa: loss partials, wb: loss sums, wc: dW, db shares, wg: G tiles
+    // wa: phi(k) column sums, wc: dW, db shares, wg: G tiles
     // the row statistics (c_i, 1/A_i) alone: no loss is returned
     if (e == cudaSuccess)
-      e = launch_loss_tc(p, q, k, phq, phk, nullptr, nullptr, nullptr, stats, nullptr, dev_status,
-                         s);
+      e = launch_loss_tc(p, q, k, phq, phk, nullptr, nullptr, nullptr, stats, nullptr, wa,
+                         dev_status, s);
     if (e == cudaSuccess)
       e = launch_loss_grad_tc(p, q, k, phq, phk, stats, wc, wg, dWq, dbq, dWk, dbk, dev_status,
                               s);

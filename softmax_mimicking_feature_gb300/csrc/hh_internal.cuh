@@ -196,10 +196,12 @@ cudaError_t launch_fmap_tc_qk(const Problem& p, const void* q, const void* k, vo
 // so that the target weight is p_ij = 2^(s_ij log2(e) / sqrt(d) - c_i).
 // rows4 (nullable): per-row (CE, KL, H(p), H(w)).  partial null (and
 // loss_rows, head_sum, rows4 null): the row statistics alone, without the
-// loss and its log a per pair.
+// loss and its log a per pair; then colsum ([U][NT][2d] floats) receives the
+// per-tile column sums of phi(k) that give A_i's off-diagonal part.
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
-                           float* stats, float4* rows4, int* dev_status, cudaStream_t s);
+                           float* stats, float4* rows4, float* colsum, int* dev_status,
+                           cudaStream_t s);
 int loss_tc_tile();
 
 // Tensor-core gradient of the summed mimicry loss for bf16 Hedgehog d in

@@ -248,6 +248,7 @@ struct LossArgs {
   float* partial;      // [U][NT]
   float2* stats;       // [U][NT * 128] (c_i, 1 / A_i) or null; c_i = m_i + log2 Z_i
   float4* rows4;       // [U][n] (CE, KL, H(p), H(w)); used by the STATS variant
+  const float* colsum; // [U][NT][DP] per-tile column sums of phi(k); row statistics mode
   int* dev_status;
   uint64_t soft_ns, hard_ns;
   int64_t n;
@@ -281,7 +282,9 @@ struct LossCfg {
          B_A = 14, B_AF = 15, B_H = 16, B_COUNT = 17 };
   static constexpr uint32_t OFF_BAR = OFF_END;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
-  static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
+  // row statistics mode: sum of phi(k) over the key tiles before this query tile
+  static constexpr uint32_t OFF_ZP = OFF_MISC + 16;           // float[DP]
+  static constexpr uint32_t ALLOC = OFF_ZP + DP * 4 + 1024;
   static_assert(ALLOC <= 232448, "shared memory");
   // TMEM: S stages at 0 and 128, A at 256, phi(Q) (bf16 pairs) at 384
   static constexpr uint32_t TM_A = 256, TM_PQ = 384;
@@ -290,11 +293,14 @@ struct LossCfg {
 constexpr int kLossThreads = 320;  // 8 epilogue warps, MMA issuer warp 8, loader warp 9
 
 // MODE 0: the loss; 1: the loss and the per-row statistics (rows4); 2: only
-// the row statistics (c_i, 1/A_i) the gradient takes (no log a, no loss).
+// the row statistics (c_i, 1/A_i) the gradient takes (no log a, no loss);
+// 3: as 2, with the weights a_ij formed for the diagonal key tile only: the
+// earlier key tiles add phi(q_i) . sum_j phi(k_j) to A_i (the linear form of
+// the causal row sum), from the per-tile column sums of phi(k).
 template <int D, int MODE>
 __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_constant__ LossArgs A) {
   using C = LossCfg<D>;
-  constexpr bool STATS = MODE == 1, ROWSTATS = MODE == 2;
+  constexpr bool STATS = MODE == 1, ROWSTATS = MODE >= 2, LINA = MODE == 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -378,9 +384,17 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
                       (int)q0, (int)unit);
       }
       load_k(0);
-      load_pk(0);
+      if (LINA) {
+        // the diagonal key tile's phi(K) only, into the first stage
+        mbar_expect_tx(bar(C::B_PK), C::PQ_BYTES);
+        for (int i = 0; i < C::DP / 64; ++i)
+          tma_load_3d(sb + C::OFF_PK + i * 16384, &A.tpk, bar(C::B_PK), 64 * i, (nkt - 1) * kTile,
+                      (int)unit);
+      } else {
+        load_pk(0);
+      }
       if (nkt > 1) load_k(1);
-      int nk = nkt < 2 ? nkt : 2, npk = 1;
+      int nk = nkt < 2 ? nkt : 2, npk = LINA ? nkt : 1;
       IdleClock clk;
       bool ok = true;
       while ((nk < nkt || npk < nkt) && ok) {
@@ -438,16 +452,18 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           mma_ss(tmem + s * 128, dq + kmaj(ks), dk + kmaj(ks), IDESC, ks > 0);
         mma_commit(bar(C::B_S + s));
         mma_commit(bar(C::B_KR + s));
-        ok = mbar_wait_poll(bar(C::B_PK + s), ph, wp) &&
-             (j < 1 || mbar_wait_poll(bar(C::B_AF), (j - 1) & 1, wp));
+        if (LINA && j < nkt - 1) continue;   // weights of the diagonal tile only
+        const int ps = LINA ? 0 : s;
+        ok = mbar_wait_poll(bar(C::B_PK + ps), LINA ? 0u : ph, wp) &&
+             (LINA || j < 1 || mbar_wait_poll(bar(C::B_AF), (j - 1) & 1, wp));
         if (!ok) break;
         tc_fence_after();
-        const uint64_t dpk = smem_desc(sb + C::OFF_PK + s * C::PQ_BYTES, 16, 1024, 2);
+        const uint64_t dpk = smem_desc(sb + C::OFF_PK + ps * C::PQ_BYTES, 16, 1024, 2);
 #pragma unroll
         for (int ks = 0; ks < C::DP / 16; ++ks)
           mma_ts(tmem + C::TM_A, tmem + C::TM_PQ + ks * 8, dpk + kmaj(ks), IDESC, ks > 0);
         mma_commit(bar(C::B_A));
-        mma_commit(bar(C::B_PKR + s));
+        mma_commit(bar(C::B_PKR + ps));
       }
       if (!ok) failed = true;
     }
@@ -456,6 +472,21 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
     const int half = warp >> 2, row = 32 * (warp & 3) + lane;
     const uint32_t lb = lane_base(warp);
     const int64_t qi = q0 + row;
+    // row statistics mode: the sum of phi(k) over key tiles 0 .. qt-1 (in tile
+    // order) into shared memory, and phi(q_i) . that sum over this thread's
+    // features, formed below from the same bf16 phi(q) the MMAs read
+    float zdot = 0.f;
+    const float* zp_s = reinterpret_cast<const float*>(sm + C::OFF_ZP);
+    if constexpr (LINA) {
+      float* zw = reinterpret_cast<float*>(sm + C::OFF_ZP);
+      for (int f = tid; f < C::DP; f += 256) {
+        const float* cs = A.colsum + (size_t)unit * A.NT * C::DP + f;
+        float acc = 0.f;
+        for (int t = 0; t < qt; ++t) acc += __ldg(cs + (size_t)t * C::DP);
+        zw[f] = acc;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
     // phi(Q) into TMEM once, as bf16 pairs in the public feature order
     // (exp(+h) in packed columns [0, D/2), exp(-h) in [D/2, D)).  Read:
     // row `row`, features [DP/2 * half, +DP/2) from the staged tile (DP/64
@@ -481,6 +512,16 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           pp[j / 2] = pack_bf16(ex2_approx(a0), ex2_approx(a1));
           pn[j / 2] = pack_bf16(ex2_approx(-a0), ex2_approx(-a1));
         }
+        if constexpr (LINA) {
+#pragma unroll
+          for (int j2 = 0; j2 < 16; ++j2) {
+            const int f = u0 + 2 * j2;
+            zdot = fmaf(bf16_lo(pp[j2]), zp_s[f], zdot);
+            zdot = fmaf(bf16_hi(pp[j2]), zp_s[f + 1], zdot);
+            zdot = fmaf(bf16_lo(pn[j2]), zp_s[D + f], zdot);
+            zdot = fmaf(bf16_hi(pn[j2]), zp_s[D + f + 1], zdot);
+          }
+        }
         tmem_st16(tmem + lb + C::TM_PQ + u0 / 2, pp);
         tmem_st16(tmem + lb + C::TM_PQ + D / 2 + u0 / 2, pn);
       }
@@ -500,6 +541,13 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           w[4 * q + 2] = v4.z;
           w[4 * q + 3] = v4.w;
         }
+        if constexpr (LINA) {
+#pragma unroll
+          for (int k2 = 0; k2 < 32; ++k2) {
+            zdot = fmaf(bf16_lo(w[k2]), zp_s[f0 + 2 * k2], zdot);
+            zdot = fmaf(bf16_hi(w[k2]), zp_s[f0 + 2 * k2 + 1], zdot);
+          }
+        }
         tmem_st32(tmem + lb + C::TM_PQ + (D / 2) * half + c0, w);
       }
       tmem_st_wait();
@@ -515,18 +563,24 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
     const int64_t kmax = min(qi, A.n - 1);   // last key admitted for this row
     for (int j = 0; j < nkt && !failed; ++j) {
       const int s = j & 1;
-      if (!mbar_wait(bar(C::B_A), j & 1, wp) || !mbar_wait(bar(C::B_S + s), (j >> 1) & 1, wp)) {
+      // weights of this key tile (mode 3: the diagonal tile only)
+      const bool wj = !LINA || j == nkt - 1;
+      if ((wj && !mbar_wait(bar(C::B_A), LINA ? 0u : (uint32_t)(j & 1), wp)) ||
+          !mbar_wait(bar(C::B_S + s), (j >> 1) & 1, wp)) {
         failed = true;
         break;
       }
       tc_fence_after();
       // A(j) out of the accumulator first, so A(j+1) can start under this tile
       uint32_t av[64];
-      tmem_ld32x2(tmem + lb + C::TM_A + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&av[0]),
-                  tmem + lb + C::TM_A + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&av[32]));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_AF));
+      if (wj) {
+        tmem_ld32x2(tmem + lb + C::TM_A + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&av[0]),
+                    tmem + lb + C::TM_A + half * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&av[32]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_AF));
+      }
       const int64_t k0 = (int64_t)j * kTile + half * 64;
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
@@ -551,14 +605,16 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
           m = mn;
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float a0 = __uint_as_float(av[c + e]), a1 = __uint_as_float(av[c + e + 1]);
             if constexpr (ROWSTATS) {
               Z0 += ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
               Z1 += ex2_approx(fmaf(__uint_as_float(sv[e + 1]), A.s_scale, -m));
-              A0 += a0;
-              A1 += a1;
+              if (wj) {
+                A0 += __uint_as_float(av[c + e]);
+                A1 += __uint_as_float(av[c + e + 1]);
+              }
               continue;
             }
+            const float a0 = __uint_as_float(av[c + e]), a1 = __uint_as_float(av[c + e + 1]);
             const float l0 = __log2f(a0), l1 = __log2f(a1);
             if constexpr (STATS) {
               const float s0 = __uint_as_float(sv[e]) * A.s_scale;
@@ -596,12 +652,12 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             if (e < nval) {
-              const float a = __uint_as_float(av[c + e]);
               if constexpr (ROWSTATS) {
                 Z0 += ex2_approx(fmaf(__uint_as_float(sv[e]), A.s_scale, -m));
-                A0 += a;
+                if (wj) A0 += __uint_as_float(av[c + e]);
                 continue;
               }
+              const float a = __uint_as_float(av[c + e]);
               const float la = __log2f(a);
               const float sl = __uint_as_float(sv[e]) * A.s_scale;
               const float p = ex2_approx(sl - m);
@@ -620,10 +676,11 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_SF + s));
     }
-    float Z = Z0 + Z1, T = T0 + T1, As = A0 + A1, Us = U0 + U1, Vs = V0 + V1;
+    float Z = Z0 + Z1, T = T0 + T1, As = A0 + A1 + zdot, Us = U0 + U1, Vs = V0 + V1;
     // the row scalars go over the first K stage: wait until every MMA has read
     // it (the last A, which follows the last S in issue order)
-    if (!failed && nkt > 0) failed = !mbar_wait(bar(C::B_A), (nkt - 1) & 1, wp);
+    if (!failed && nkt > 0)
+      failed = !mbar_wait(bar(C::B_A), LINA ? 0u : (uint32_t)((nkt - 1) & 1), wp);
     asm volatile("bar.sync 1, 256;" ::: "memory");
     // merge the two column halves of each row
     if (half == 1) {
@@ -670,6 +727,44 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_tc_kernel(const __grid_c
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
   (void)failed;
+}
+
+// Column sums of phi(k) over each 128-row tile (rows < n), for the row
+// statistics mode: one CTA per (unit, tile), 256 threads; thread t sums the
+// 8 features 8 (t % (DP/8)) .. +7 over rows t / (DP/8) + r (256 / (DP/8)),
+// then the row groups are added in a fixed order.
+template <int DP>
+__global__ void __launch_bounds__(256) phi_colsum_kernel(const __nv_bfloat16* __restrict__ phk,
+                                                         float* __restrict__ colsum, int64_t n,
+                                                         int NT, int dpp) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int FG = DP / 8, RG = 256 / FG;   // feature groups, row groups
+  __shared__ float part[RG][DP];
+  const int64_t unit = blockIdx.x / NT;
+  const int tile = blockIdx.x % NT;
+  const int fg = threadIdx.x % FG, rg = threadIdx.x / FG;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int64_t r0 = (int64_t)tile * 128;
+  const __nv_bfloat16* base = phk + ((size_t)unit * n) * dpp + 8 * fg;
+  for (int r = rg; r < 128; r += RG) {
+    if (r0 + r >= n) break;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (size_t)(r0 + r) * dpp));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[2 * k] += bf16_lo(w[k]);
+      acc[2 * k + 1] += bf16_hi(w[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) part[rg][8 * fg + k] = acc[k];
+  __syncthreads();
+  for (int f = threadIdx.x; f < DP; f += 256) {
+    float t = 0.f;
+    for (int g = 0; g < RG; ++g) t += part[g][f];
+    colsum[((size_t)unit * NT + tile) * DP + f] = t;
+  }
 }
 
 __global__ void sum_partials_tc_kernel(const float* __restrict__ partial, float* __restrict__ out,
@@ -757,7 +852,8 @@ cudaError_t launch_fmap_tc_qk(const Problem& p, const void* q, const void* k, vo
 template <int D>
 static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, const void* phq,
                              const void* phk, float* loss_rows, float* partial, float* head_sum,
-                             float* stats, float4* rows4, int* dev_status, cudaStream_t s) {
+                             float* stats, float4* rows4, float* colsum, int* dev_status,
+                             cudaStream_t s) {
   LossArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t U = (uint64_t)p.B * p.H;
@@ -800,10 +896,24 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
   a.seq = p.seq_major;
   a.s_scale = 1.4426950408889634f / sqrtf((float)D);
   const size_t smem = LossCfg<D>::ALLOC;
-  // no loss asked for (no partial sums): the row statistics alone
+  // no loss asked for (no partial sums): the row statistics alone; at d = 128
+  // with the off-diagonal row sums in linear form, from column sums of phi(k)
+  // per key tile (at d = 64 the weight MMAs cost less than that extra launch:
+  // 226 vs 219 us per GPT-2-shaped gradient call)
   const bool rowstats = !partial;
+  const bool lina = rowstats && D == 128;
   if (rowstats && (!stats || loss_rows || head_sum || rows4)) return cudaErrorInvalidValue;
-  auto kern = rows4 ? loss_tc_kernel<D, 1> : (rowstats ? loss_tc_kernel<D, 2> : loss_tc_kernel<D, 0>);
+  if (lina && (!colsum || !phk)) return cudaErrorInvalidValue;
+  a.colsum = colsum;
+  if (lina) {
+    cudaError_t e = launch_pdl(phi_colsum_kernel<2 * D>, dim3((unsigned)(U * a.NT)), dim3(256), 0, s,
+                               reinterpret_cast<const __nv_bfloat16*>(phk), colsum, (int64_t)p.n,
+                               a.NT, 2 * D);
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = rows4 ? loss_tc_kernel<D, 1>
+                    : (lina ? loss_tc_kernel<D, 3>
+                            : (rowstats ? loss_tc_kernel<D, 2> : loss_tc_kernel<D, 0>));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3((unsigned)(U * a.NT)), dim3(kLossThreads), smem, s, a);
@@ -815,11 +925,12 @@ static cudaError_t loss_tc_t(const Problem& p, const void* q, const void* k, con
 
 cudaError_t launch_loss_tc(const Problem& p, const void* q, const void* k, const void* phq,
                            const void* phk, float* loss_rows, float* partial, float* head_sum,
-                           float* stats, float4* rows4, int* dev_status, cudaStream_t s) {
+                           float* stats, float4* rows4, float* colsum, int* dev_status,
+                           cudaStream_t s) {
   return p.d == 64 ? loss_tc_t<64>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, rows4,
-                                   dev_status, s)
+                                   colsum, dev_status, s)
                    : loss_tc_t<128>(p, q, k, phq, phk, loss_rows, partial, head_sum, stats, rows4,
-                                    dev_status, s);
+                                    colsum, dev_status, s);
 }
 
 int loss_tc_tile() { return kTile; }
