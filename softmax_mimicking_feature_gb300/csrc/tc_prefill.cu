@@ -608,19 +608,50 @@ prefill_tc_kernel(const __grid_constant__ PrefillArgs A) {
   if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
 }
 
-// Inclusive scan over the segment states of every unit, one float4 position
-// per thread, summed in order after the initial state (continuation) when
-// there is one.  With one piece per segment (m = 1) it runs in place over the
-// pm1 states in ws; with m > 1 it reads the pm1 * m piece states of a unit
-// from raw and writes the running sum after each segment's last piece to ws.
-// The states are read in batches of four, all loads of a batch issued before
-// its stores, so a thread waits for one round trip per batch rather than one
-// per state.
-__global__ void segment_scan_kernel(float4* ws, const float4* raw,
-                                    const float4* __restrict__ init, int64_t units, int pm1,
-                                    int m, int64_t elems4) {
+// In-place inclusive scan over the P-1 segment states of every unit, one
+// float4 position per thread, summed in segment order after the initial
+// state (continuation) when there is one.  The segments are read in batches
+// of four, all loads of a batch issued before its stores, so a thread waits
+// for one round trip per batch rather than one per segment.
+__global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __restrict__ init,
+                                    int64_t units, int pm1, int64_t elems4) {
   // the next kernel may be scheduled now; global memory is touched only after
   // the kernels before this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= units * elems4) return;
+  const int64_t u = i / elems4, e = i % elems4;
+  float4* p = ws + (size_t)u * pm1 * elems4 + e;
+  float4 acc = init ? __ldcg(init + (size_t)u * elems4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kBatch = 4;
+  for (int s0 = 0; s0 < pm1; s0 += kBatch) {
+    float4 x[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (s0 + j < pm1) x[j] = __ldcg(p + (size_t)(s0 + j) * elems4);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (s0 + j >= pm1) break;
+      if (s0 + j == 0 && !init) {
+        acc = x[0];   // the first segment's own sum stays as written
+        continue;
+      }
+      acc.x += x[j].x;
+      acc.y += x[j].y;
+      acc.z += x[j].z;
+      acc.w += x[j].w;
+      __stcg(p + (size_t)(s0 + j) * elems4, acc);
+    }
+  }
+}
+
+// The same scan when the state pass summed each segment in m > 1 pieces:
+// the pm1 * m piece states of a unit are read from raw in order and the
+// running sum after each segment's last piece is written to ws.
+__global__ void piece_scan_kernel(float4* __restrict__ ws, const float4* __restrict__ raw,
+                                  const float4* __restrict__ init, int64_t units, int pm1, int m,
+                                  int64_t elems4) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -644,9 +675,7 @@ __global__ void segment_scan_kernel(float4* ws, const float4* raw,
       acc.y += x[j].y;
       acc.z += x[j].z;
       acc.w += x[j].w;
-      // in place, the first segment's own sum stays as written
-      if ((t + 1) % m == 0 && !(m == 1 && t == 0 && !init))
-        __stcg(dst + (size_t)((t + 1) / m - 1) * elems4, acc);
+      if ((t + 1) % m == 0) __stcg(dst + (size_t)((t + 1) / m - 1) * elems4, acc);
     }
   }
 }
@@ -765,11 +794,15 @@ static cudaError_t launch_kind(const Problem& p, const TcPlan& pl, const void* q
     if (pl.P > 2 || pl.M > 1 || init) {
       const int64_t elems4 = ws_segment_floats(p) / 4;
       const int64_t n4 = (int64_t)U * elems4;
-      const float4* raw = reinterpret_cast<const float4*>(
-          reinterpret_cast<const char*>(ws) + (pl.M > 1 ? pl.raw_offset : 0));
-      e = launch_pdl(segment_scan_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s,
-                     reinterpret_cast<float4*>(ws), raw, reinterpret_cast<const float4*>(init),
-                     (int64_t)U, pl.P - 1, pl.M, elems4);
+      const dim3 grid((unsigned)((n4 + 255) / 256));
+      if (pl.M > 1)
+        e = launch_pdl(piece_scan_kernel, grid, dim3(256), 0, s, reinterpret_cast<float4*>(ws),
+                       reinterpret_cast<const float4*>(reinterpret_cast<const char*>(ws) +
+                                                       pl.raw_offset),
+                       reinterpret_cast<const float4*>(init), (int64_t)U, pl.P - 1, pl.M, elems4);
+      else
+        e = launch_pdl(segment_scan_kernel, grid, dim3(256), 0, s, reinterpret_cast<float4*>(ws),
+                       reinterpret_cast<const float4*>(init), (int64_t)U, pl.P - 1, elems4);
       if (e != cudaSuccess) return e;
     }
   }

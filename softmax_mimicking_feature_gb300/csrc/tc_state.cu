@@ -100,8 +100,15 @@ struct StatePiece {
   int index, t_begin, nt;
 };
 __device__ __forceinline__ StatePiece state_piece(const StateArgs& A) {
-  const int npc = (A.P - 1) * A.M;
   StatePiece r;
+  if (A.M == 1) {   // one piece per segment
+    r.unit = blockIdx.x / (A.P - 1);
+    r.index = blockIdx.x % (A.P - 1);
+    r.t_begin = r.index * A.L;
+    r.nt = min(A.NT, r.t_begin + A.L) - r.t_begin;
+    return r;
+  }
+  const int npc = (A.P - 1) * A.M;
   r.unit = blockIdx.x / npc;
   r.index = blockIdx.x % npc;
   const int seg = r.index / A.M, j = r.index % A.M;
