@@ -30,6 +30,9 @@ CASES = {
     "f32_d64": ("hedgehog_f32_1x1x256_d64", dict(B=2, H=2, n=190)),
     "bf16_d64": ("gpt2_prefill_8x12x1024_d64", dict(B=2, H=3, n=300)),
     "bf16_d128": ("llama2_prefill_1x32x4096_d128", dict(B=1, H=3, n=389)),
+    # a last tile of more than 64 rows, and nine query tiles (45 stored g tiles)
+    "bf16_d128_tail100": ("llama2_prefill_1x32x4096_d128", dict(B=1, H=2, n=356)),
+    "bf16_d128_long": ("llama2_prefill_1x32x4096_d128", dict(B=1, H=2, n=1100)),
     "bf16_n1": ("gpt2_prefill_8x12x1024_d64", dict(B=1, H=2, n=1)),
     "f32_n33": ("hedgehog_f32_1x1x256_d64", dict(B=1, H=1, n=33)),
 }
