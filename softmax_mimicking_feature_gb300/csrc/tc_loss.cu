@@ -108,10 +108,11 @@ __global__ void __launch_bounds__(256) fmap_tc_kernel(const __grid_constant__ Fm
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // the next kernel may be scheduled now; global memory is touched only after
-  // the kernels before this one have completed
-  pdl_launch_dependents();
+  // global memory is touched only after the kernels before this one have
+  // completed; only then may the next kernel be scheduled (this kernel can be
+  // the first of a call, whose later kernels may read the call's inputs early)
   pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   if (tid == 0) {
     mbar_expect_tx(bar_load, W_BYTES + X_BYTES);

@@ -690,10 +690,11 @@ __global__ void piece_scan_kernel(float4* __restrict__ ws, const float4* __restr
 __global__ void init_state_kernel(const float* __restrict__ S0, const float* __restrict__ z0,
                                   float* __restrict__ init, int64_t units, int D, int dp_ws,
                                   int dp_pub, int taylor) {
-  // the next kernel may be scheduled now; global memory is touched only after
-  // the kernels before this one have completed
-  pdl_launch_dependents();
+  // the first kernel of a call: the next one is scheduled only once this one
+  // has waited for the work before the call (later kernels of the call may
+  // read its inputs before their own wait)
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t per = (int64_t)dp_ws * D + dp_ws;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units * per) return;

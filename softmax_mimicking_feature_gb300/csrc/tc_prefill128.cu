@@ -122,6 +122,8 @@ struct Args128 {
   int H, P, L, NT;
   int G;      // query heads per key/value head
   int seq;    // q, k, v, y are [B][n][H][D]
+  int early;  // an earlier kernel of this call has waited for the work before
+              // the call: q, k, v and W may be read before this kernel's wait
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) {
@@ -184,26 +186,6 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  // W and the first tile into L2 while the kernels before this one finish: a
-  // prefetch only warms the cache, so it may run before the wait below (any
-  // later write to these rows still reaches L2 before the loads read them)
-  if (warp == kLoadWarp && lane == 0 && nt > 0) {
-    const int r0 = t_begin * TILE;
-    for (int x = 0; x < 2; ++x) {
-      tma_prefetch_3d(&A.tw, 64 * x, 0, uh);
-      tma_prefetch_rows(&A.tk, 64 * x, r0, ub, kh, A.seq);
-      tma_prefetch_rows(&A.tq, 64 * x, r0, ub, uh, A.seq);
-      tma_prefetch_rows(&A.tv, 64 * x, r0, ub, kh, A.seq);
-    }
-  }
-  // everything above touches only this CTA's shared memory and TMEM; the next
-  // kernel may be scheduled now, and this one reads and writes global memory
-  // only once the kernels before it have completed
-  pdl_launch_dependents();
-  pdl_wait();
-  tc_fence_before();
-  __syncthreads();
-
   auto load_k = [&](int i) {
     const int r0 = (t_begin + i) * TILE;
     mbar_expect_tx(bar(B_LDK), 32768);
@@ -230,14 +212,41 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
       tma_prefetch_rows(&A.tv, 64 * x, r0, ub, kh, A.seq);
     }
   };
-  if (warp == kLoadWarp && lane == 0 && nt > 0) {
+  auto first_loads = [&]() {
     mbar_expect_tx(bar(B_W), D * D * 2);
     for (int x = 0; x < 2; ++x) tma_load_3d(sb + OFF_W + x * 16384, &A.tw, bar(B_W), 64 * x, 0, uh);
     load_k(0);
     load_q(0);
     load_v(0);
     if (nt > 1) prefetch_tile(1);
+  };
+  const bool loader = warp == kLoadWarp && lane == 0 && nt > 0;
+  if (A.early) {
+    // The inputs of this call (q, k, v, W) are final: the first kernel of the
+    // call let the next one be scheduled only after its own wait for the
+    // work before the call, and every later kernel of it after that.  So W
+    // and the first tile may land while the kernels before this one finish;
+    // the workspace (segment prefixes) is read only after the wait below.
+    __syncthreads();   // the barriers are initialised
+    if (loader) first_loads();
+  } else if (loader) {
+    // this kernel may be the call's first: W and the first tile into L2
+    // only (a prefetch just warms the cache, so it may precede the wait)
+    const int r0 = t_begin * TILE;
+    for (int x = 0; x < 2; ++x) {
+      tma_prefetch_3d(&A.tw, 64 * x, 0, uh);
+      tma_prefetch_rows(&A.tk, 64 * x, r0, ub, kh, A.seq);
+      tma_prefetch_rows(&A.tq, 64 * x, r0, ub, uh, A.seq);
+      tma_prefetch_rows(&A.tv, 64 * x, r0, ub, kh, A.seq);
+    }
   }
+  // the next kernel may be scheduled now; this one reads the workspace and
+  // writes global memory only once the kernels before it have completed
+  pdl_launch_dependents();
+  pdl_wait();
+  tc_fence_before();
+  __syncthreads();
+  if (!A.early && loader) first_loads();
   for (int i = tid; i < D; i += kThreads) bs_s[i] = A.bias ? A.bias[(size_t)uh * D + i] * kLog2e : 0.f;
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -704,6 +713,9 @@ cudaError_t launch_prefill_out_d128(const Problem& p, const TcPlan& pl, const vo
   a.NT = pl.NT;
   a.G = p.G;
   a.seq = p.seq_major;
+  // a state pass, an initial-state kernel or the softmax-map offsets ran
+  // first in this call (each of them waits before it lets the next start)
+  a.early = (pl.P > 1 || init || p.softmax) ? 1 : 0;
   auto kern = p.softmax ? prefill_t128_kernel<true> : prefill_t128_kernel<false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);

@@ -166,10 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const __grid_cons
         tma_prefetch_rows(&A.tv, 64 * x, (t_begin + i) * TILE, ub, kh, A.seq);
       }
     }
-  // the next kernel may be scheduled now; global memory is touched only after
-  // the kernels before this one have completed
-  pdl_launch_dependents();
+  // global memory is touched only after the kernels before this one have
+  // completed; only then may the next kernel be scheduled, so the kernels
+  // after this one in a call may read the call's inputs before their own wait
   pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
 
   auto load_k = [&](int i) {
@@ -445,10 +446,11 @@ __global__ void __launch_bounds__(640, 1) state_t128_kernel(const __grid_constan
       }
     }
   }
-  // the next kernel may be scheduled now; global memory is touched only after
-  // the kernels before this one have completed
-  pdl_launch_dependents();
+  // global memory is touched only after the kernels before this one have
+  // completed; only then may the next kernel be scheduled, so the kernels
+  // after this one in a call may read the call's inputs before their own wait
   pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   auto load_k = [&](int i) {
     const uint32_t dst = sb + OFF_K + (i & 1) * XT, b = bar(B_LDK + (i & 1));
@@ -726,10 +728,11 @@ __global__ void __launch_bounds__(tay::kThreads, 2) state_taylor_kernel(const __
       tma_prefetch_rows(&A.tk, 0, (t_begin + i) * TILE, ub, kh, A.seq);
       tma_prefetch_rows(&A.tv, 0, (t_begin + i) * TILE, ub, kh, A.seq);
     }
-  // the next kernel may be scheduled now; global memory is touched only after
-  // the kernels before this one have completed
-  pdl_launch_dependents();
+  // global memory is touched only after the kernels before this one have
+  // completed; only then may the next kernel be scheduled, so the kernels
+  // after this one in a call may read the call's inputs before their own wait
   pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   auto load_v = [&](int i) {
     const uint32_t b = bar(B_LDV + (i & 1));
