@@ -261,21 +261,23 @@ __global__ void __launch_bounds__(640, 1) prefill_t128_kernel(const __grid_const
     const size_t per = (size_t)DP * D + DP;
     const float* prefix = seg > 0 ? A.ws + ((size_t)unit * (A.P - 1) + seg - 1) * per
                                   : (A.init ? A.init + (size_t)unit * per : nullptr);
-#pragma unroll 1
-    for (int c0 = 64 * (q & 1); c0 < 64 * (q & 1) + 64; c0 += 32) {
-      uint32_t v[32];
+    // all 64 values of this thread requested at once (one L2 round trip)
+    const int cb = 64 * (q & 1);
+    uint32_t v[64];
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 v4 = prefix ? __ldcg(reinterpret_cast<const float4*>(prefix + ws_s_index(fp, c0 + j, D)))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[j] = __float_as_uint(v4.x);
-        v[j + 1] = __float_as_uint(v4.y);
-        v[j + 2] = __float_as_uint(v4.z);
-        v[j + 3] = __float_as_uint(v4.w);
-      }
-      tmem_st32(tmem + lane_base(warp) + TM_S + 128 * c + c0, v);
+    for (int j = 0; j < 64; j += 4) {
+      const float4 v4 = prefix ? __ldcg(reinterpret_cast<const float4*>(prefix + ws_s_index(fp, cb + j, D)))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[j] = __float_as_uint(v4.x);
+      v[j + 1] = __float_as_uint(v4.y);
+      v[j + 2] = __float_as_uint(v4.z);
+      v[j + 3] = __float_as_uint(v4.w);
     }
-    if ((q & 1) == 0) z_s[128 * c + r] = prefix ? __ldcg(prefix + (size_t)DP * D + fp) : 0.f;
+    const float zv = ((q & 1) == 0 && prefix) ? __ldcg(prefix + (size_t)DP * D + fp) : 0.f;
+    tmem_st32(tmem + lane_base(warp) + TM_S + 128 * c + cb, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+    tmem_st32(tmem + lane_base(warp) + TM_S + 128 * c + cb + 32,
+              *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+    if ((q & 1) == 0) z_s[128 * c + r] = zv;
     tmem_st_wait();
   }
   tc_fence_before();

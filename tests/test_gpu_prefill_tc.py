@@ -101,6 +101,22 @@ def test_state_pass_pieces_do_not_change_the_result(case, pieces, env):
         assert np.linalg.norm(Sg[:dp] - S_ref) <= BF16_TOL * np.linalg.norm(S_ref)
 
 
+def test_state_pass_empty_pieces(env):
+    # 15 tiles in 3 segments of 5, each summed in 4 pieces of at most 2 tiles:
+    # 2 + 2 + 1 + an empty piece (zeros) per segment
+    env.setenv("HH_PREFILL_SEGMENTS", "3")
+    env.setenv("HH_STATE_PIECES", "4")
+    w = wl.WORKLOADS["taylor2_prefill_4x8x8192_d16"].with_(B=1, H=2, n=15 * 128)
+    x = wl.make_inputs(w, seed=33)
+    xd = {k: (None if t is None else t.cuda()) for k, t in x.items()}
+    fm = hh.FeatureMap("taylor2", w.d)
+    assert hh.fwd_plan(fm, w.torch_dtype, w.B, w.H, w.n, 64) == (3, 3)
+    y = hh.linattn_fwd_causal(fm, xd["q"], xd["k"], xd["v"])
+    torch.cuda.synchronize()
+    y_ref = O.fwd_causal("taylor2", f64(x["q"]), f64(x["k"]), f64(x["v"]), None, None)
+    assert rel_l2_per_head(f64(y), y_ref) <= BF16_TOL
+
+
 def test_plan_splits_long_sequences():
     w, x, xd, fm = _setup("llama_d128", seed=1)
     P, launches = hh.fwd_plan(fm, torch.bfloat16, 1, 32, 4096, 64)
