@@ -619,29 +619,31 @@ __global__ void segment_scan_kernel(float4* __restrict__ ws, const float4* __res
   // the kernels before this one have completed
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= units * elems4) return;
-  const int64_t u = i / elems4, e = i % elems4;
-  float4* p = ws + (size_t)u * pm1 * elems4 + e;
-  float4 acc = init ? __ldcg(init + (size_t)u * elems4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int kBatch = 4;
-  for (int s0 = 0; s0 < pm1; s0 += kBatch) {
-    float4 x[kBatch];
+  const int64_t total = units * elems4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t u = i / elems4, e = i % elems4;
+    float4* p = ws + (size_t)u * pm1 * elems4 + e;
+    float4 acc = init ? __ldcg(init + (size_t)u * elems4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kBatch = 4;
+    for (int s0 = 0; s0 < pm1; s0 += kBatch) {
+      float4 x[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-      if (s0 + j < pm1) x[j] = __ldcg(p + (size_t)(s0 + j) * elems4);
+      for (int j = 0; j < kBatch; ++j)
+        if (s0 + j < pm1) x[j] = __ldcg(p + (size_t)(s0 + j) * elems4);
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      if (s0 + j >= pm1) break;
-      if (s0 + j == 0 && !init) {
-        acc = x[0];   // the first segment's own sum stays as written
-        continue;
+      for (int j = 0; j < kBatch; ++j) {
+        if (s0 + j >= pm1) break;
+        if (s0 + j == 0 && !init) {
+          acc = x[0];   // the first segment's own sum stays as written
+          continue;
+        }
+        acc.x += x[j].x;
+        acc.y += x[j].y;
+        acc.z += x[j].z;
+        acc.w += x[j].w;
+        __stcg(p + (size_t)(s0 + j) * elems4, acc);
       }
-      acc.x += x[j].x;
-      acc.y += x[j].y;
-      acc.z += x[j].z;
-      acc.w += x[j].w;
-      __stcg(p + (size_t)(s0 + j) * elems4, acc);
     }
   }
 }
