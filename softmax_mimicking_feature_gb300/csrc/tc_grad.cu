@@ -183,7 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1) grad_tc_kernel(const __grid_const
   // group's tiles.
   const int nsides = A.sides == 0 ? 2 : 1;
   const int64_t GT = nsides * (int64_t)A.HG * A.NT;
-  const int64_t grp = blockIdx.x / GT, within = blockIdx.x % GT;
+  // The query side storing g takes the groups in reverse order, so that it
+  // starts on the heads whose rows the statistics kernel read last and the
+  // key side (natural order) starts on the g tiles it wrote last, while they
+  // may still be in L2.
+  const int64_t ngrp = (A.U + A.HG - 1) / A.HG;
+  const int64_t grp = A.sides == 1 ? ngrp - 1 - (int64_t)blockIdx.x / GT : (int64_t)blockIdx.x / GT;
+  const int64_t within = blockIdx.x % GT;
   const int64_t gsz = min((int64_t)A.HG, A.U - grp * A.HG);
   const int side = A.sides == 0 ? (int)(within & 1) : A.sides - 1;
   const int64_t wu = A.sides == 0 ? within >> 1 : within;
