@@ -91,13 +91,15 @@ struct GradCfg {
   static constexpr uint32_t OFF_Y = OFF_PX + PX_BYTES;       // 2 stages, D/64 panels of 8 KB
   static constexpr uint32_t OFF_PY = OFF_Y + 2 * Y_BYTES;    // 3 stages, DP/64 panels of 8 KB
   static constexpr uint32_t OFF_ST = OFF_PY + 3 * PY_BYTES;  // 3 stages of 64 (c, 1/A)
-  static constexpr uint32_t OFF_BAR = OFF_ST + 3 * ST_BYTES; // 18 barriers
   // key side reading G: RG_NS stages of [G chunk | phi(Y) chunk] from offset
   // 0, over everything else; X and phi(X) are loaded once the last stage
-  // has been read, for the end phase only
+  // has been read, for the end phase only.  D = 64 grows its allocation for
+  // them; at D = 128 four stages fit below the stats.
   static constexpr uint32_t RG_STAGE = G_BYTES + PY_BYTES;
-  static constexpr int RG_NS = OFF_BAR / RG_STAGE < 4 ? (int)(OFF_BAR / RG_STAGE) : 4;
-  static_assert(RG_NS * RG_STAGE <= OFF_BAR, "stored-G stages exceed shared memory");
+  static constexpr int RG_NS = 4;
+  static constexpr uint32_t OFF_BAR = OFF_ST + 3 * ST_BYTES > RG_NS * RG_STAGE
+                                          ? OFF_ST + 3 * ST_BYTES
+                                          : RG_NS * RG_STAGE;   // 18 barriers
   static constexpr uint32_t OFF_MISC = OFF_BAR + 18 * 8;
   static constexpr uint32_t ALLOC = OFF_MISC + 16 + 1024;
   // end phase: dL/dh as bf16 hi and lo tiles [128 rows][D] (MN-major, 16 KB
