@@ -276,6 +276,15 @@ HH_API hh_status hh_mimicry_stats(const hh_fmap* fmap, int dtype, const void* q,
 HH_API size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, int H,
                                            int64_t n);
 
+/* The smallest workspace hh_mimicry_loss_grad accepts (0 when none): the
+ * O(n) part of hh_loss_grad_workspace_bytes without the tiles of dL/da.
+ * Given at least this much but less than hh_loss_grad_workspace_bytes, the
+ * call forms dL/da on both sides, the query and the key side each scoring
+ * every pair (one launch instead of two; slower, same result up to
+ * rounding), so that long sequences do not need about B H n^2 bytes. */
+HH_API size_t hh_loss_grad_workspace_bytes_min(const hh_fmap* fmap, int dtype, int64_t B, int H,
+                                               int64_t n);
+
 /* Gradient of the summed distillation loss sum_{b,h,i} L_i (paper Eq. 4) with
  * respect to the Hedgehog feature-map parameters.  Source: "The Attention
  * Weight Distillation Loss" (only the feature maps are trained; q, k and the
@@ -294,7 +303,9 @@ HH_API size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64
  * only dWq (and dWk) are written and dbq, dbk are ignored (may be NULL).
  * Hedgehog maps only (Taylor has no parameters: HH_ERR_UNSUPPORTED); d a
  * multiple of 8, at most 128.
- * workspace: at least hh_loss_grad_workspace_bytes(...) bytes. */
+ * workspace: at least hh_loss_grad_workspace_bytes(...) bytes, or at least
+ * hh_loss_grad_workspace_bytes_min(...) for the slower path that stores no
+ * tiles of dL/da; less than that returns HH_ERR_WORKSPACE. */
 HH_API hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q,
                                       const void* k, int64_t B, int H, int64_t n, float* dWq,
                                       float* dbq, float* dWk, float* dbk, void* workspace,

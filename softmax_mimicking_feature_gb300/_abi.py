@@ -21,7 +21,8 @@ HH_LAYOUT_BHND, HH_LAYOUT_BNHD = 0, 1
 EXPORTED = ("hh_version", "hh_status_str", "hh_fmap_dim", "hh_feature_map",
             "hh_fwd_workspace_bytes", "hh_fwd_plan", "hh_linattn_fwd_causal", "hh_linattn_decode_step",
             "hh_loss_workspace_bytes", "hh_mimicry_loss", "hh_linattn_fwd_causal_noalloc",
-            "hh_loss_grad_workspace_bytes", "hh_mimicry_loss_grad", "hh_mimicry_stats",
+            "hh_loss_grad_workspace_bytes", "hh_loss_grad_workspace_bytes_min",
+            "hh_mimicry_loss_grad", "hh_mimicry_stats",
             "hh_fwd_from_state_workspace_bytes", "hh_linattn_fwd_causal_from_state")
 
 
@@ -59,6 +60,7 @@ _SIGS = {
     "hh_linattn_fwd_causal_noalloc": ([_P, _i32, _vp, _vp, _vp, _i64, _i32, _i64, _i32, _vp, _vp,
                                        _vp, _vp, _vp], _i32),
     "hh_loss_grad_workspace_bytes": ([_P, _i32, _i64, _i32, _i64], _sz),
+    "hh_loss_grad_workspace_bytes_min": ([_P, _i32, _i64, _i32, _i64], _sz),
     "hh_fwd_from_state_workspace_bytes": ([_P, _i32, _i64, _i32, _i64, _i32], _sz),
     "hh_linattn_fwd_causal_from_state": ([_P, _i32, _vp, _vp, _vp, _i64, _i32, _i64, _i32, _vp,
                                           _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp], _i32),

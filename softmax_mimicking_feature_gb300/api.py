@@ -248,9 +248,15 @@ def mimicry_stats(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,
     return out
 
 
-def loss_grad_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int) -> int:
+def loss_grad_workspace_bytes(fm: FeatureMap, dtype: torch.dtype, B: int, H: int, n: int,
+                              minimal: bool = False) -> int:
+    """Workspace of mimicry_loss_grad (hh_loss_grad_workspace_bytes); minimal:
+    the smallest it accepts (hh_loss_grad_workspace_bytes_min), which selects
+    the path that stores no tiles of dL/da."""
     s = fm.struct()
-    return int(_abi.lib().hh_loss_grad_workspace_bytes(ctypes.byref(s), _DTYPES[dtype], B, H, n))
+    fn = (_abi.lib().hh_loss_grad_workspace_bytes_min if minimal
+          else _abi.lib().hh_loss_grad_workspace_bytes)
+    return int(fn(ctypes.byref(s), _DTYPES[dtype], B, H, n))
 
 
 def mimicry_loss_grad(fm: FeatureMap, q: torch.Tensor, k: torch.Tensor,

@@ -465,6 +465,15 @@ size_t hh_loss_grad_workspace_bytes(const hh_fmap* fmap, int dtype, int64_t B, i
   return loss_grad_ws(p).total;
 }
 
+size_t hh_loss_grad_workspace_bytes_min(const hh_fmap* fmap, int dtype, int64_t B, int H,
+                                        int64_t n) {
+  Problem p;
+  if (make_problem(fmap, dtype, B, H, n, &p) != HH_OK) return 0;
+  if (p.kind != HH_FMAP_HEDGEHOG || B * H * n == 0) return 0;
+  const GradWs w = loss_grad_ws(p);
+  return w.total - w.g;   // the g tiles come last
+}
+
 hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, const void* k,
                                int64_t B, int H, int64_t n, float* dWq, float* dbq, float* dWk,
                                float* dbk, void* workspace, size_t ws_bytes, int* dev_status,
@@ -483,7 +492,7 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
       HH_OK)
     return st;
   if (dev_status && ((uintptr_t)dev_status & 3u)) return HH_ERR_ALIGNMENT;
-  const size_t need = hh_loss_grad_workspace_bytes(fmap, dtype, B, H, n);
+  const size_t need = hh_loss_grad_workspace_bytes_min(fmap, dtype, B, H, n);
   if (need > 0 && (!workspace || ws_bytes < need)) return HH_ERR_WORKSPACE;
   if (!device_ok()) return HH_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
@@ -507,7 +516,8 @@ hh_status hh_mimicry_loss_grad(const hh_fmap* fmap, int dtype, const void* q, co
   float* wa = (float*)(ws + 2 * w.phi + w.stats);
   float* wb = (float*)(ws + 2 * w.phi + w.stats + w.a);
   float* wc = (float*)(ws + 2 * w.phi + w.stats + w.a + w.b);
-  void* wg = ws + 2 * w.phi + w.stats + w.a + w.b + w.c;
+  // the stored tiles of g when the workspace has room for them
+  void* wg = ws_bytes >= w.total && w.g > 0 ? ws + 2 * w.phi + w.stats + w.a + w.b + w.c : nullptr;
   cudaError_t e;
   if (fmap_tc_supported(p)) {
     e = launch_fmap_tc_qk(p, q, k, phq, phk, nullptr, nullptr, dev_status, s);

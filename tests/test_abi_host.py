@@ -155,3 +155,19 @@ def test_noalloc_without_a_supported_device_is_unsupported(L):
     assert _noalloc(L, _fm(d=128)) == _abi.HH_ERR_UNSUPPORTED
     assert _noalloc(L, _fm(d=128), n=300) == _abi.HH_ERR_UNSUPPORTED
 
+
+
+def test_loss_grad_workspace_sizes(L):
+    # the full workspace adds the causal 128 x 128 tiles of dL/da in bf16 to
+    # the minimal one (B H T (T + 1) / 2 tiles, T = ceil(n / 128), 256-byte
+    # aligned); float32 (CUDA-core path) stores none
+    fm = _fm(d=128)
+    for B, H, n in [(1, 32, 4096), (2, 3, 389), (1, 2, 1)]:
+        full = L.hh_loss_grad_workspace_bytes(ctypes.byref(fm), 1, B, H, n)
+        small = L.hh_loss_grad_workspace_bytes_min(ctypes.byref(fm), 1, B, H, n)
+        t = (n + 127) // 128
+        g = B * H * t * (t + 1) // 2 * 128 * 128 * 2
+        assert full - small == (g + 255) // 256 * 256 and small > 0
+    assert (L.hh_loss_grad_workspace_bytes(ctypes.byref(fm), 0, 1, 2, 300) ==
+            L.hh_loss_grad_workspace_bytes_min(ctypes.byref(fm), 0, 1, 2, 300))
+    assert L.hh_loss_grad_workspace_bytes_min(ctypes.byref(fm), 1, 0, 2, 300) == 0

@@ -65,6 +65,29 @@ def test_loss_grad_shared_map(case):
     _check(got, ref, _tol(w))
 
 
+@pytest.mark.parametrize("case", ["bf16_d64", "bf16_d128", "bf16_d128_tail100"])
+def test_loss_grad_minimal_workspace(case):
+    # with the minimal workspace both sides form g (no stored tiles): the
+    # oracle's result, and the stored-tile path's up to rounding
+    name, kw = CASES[case]
+    w = wl.WORKLOADS[name].with_(**kw)
+    x = wl.make_inputs(w, seed=37)
+    xd = {k: (None if t is None else t.cuda()) for k, t in x.items()}
+    fm = hh.FeatureMap("hedgehog", w.d, xd["W"], xd["b"])
+    full = hh.loss_grad_workspace_bytes(fm, w.torch_dtype, w.B, w.H, w.n)
+    small = hh.loss_grad_workspace_bytes(fm, w.torch_dtype, w.B, w.H, w.n, minimal=True)
+    assert 0 < small < full
+    ws = torch.empty(small, dtype=torch.uint8, device="cuda")
+    got = hh.mimicry_loss_grad(fm, xd["q"], xd["k"], workspace=ws)
+    fast = hh.mimicry_loss_grad(fm, xd["q"], xd["k"])
+    torch.cuda.synchronize()
+    ref = O.loss_grad_causal(f64(x["q"]), f64(x["k"]), f64(x["W"]), f64(x["b"]))
+    _check(got, ref, _tol(w))
+    _check(got, [None if t is None else f64(t) for t in fast], _tol(w))
+    with pytest.raises(RuntimeError):
+        hh.mimicry_loss_grad(fm, xd["q"], xd["k"], workspace=ws[: small - 256])
+
+
 @pytest.mark.parametrize("case", ["f32_d64", "bf16_d64", "bf16_d128"])
 def test_loss_grad_separate_maps(case):
     name, kw = CASES[case]
