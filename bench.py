@@ -270,6 +270,23 @@ def time_graphs(torch, step_fns, K, W, sampler=None, dist=None, cap=240):
     return e0.elapsed_time(e1)  # ms
 
 
+def job_time_ms(torch, ms, dist, device):
+    """The whole job's time for N ranks: the largest per-rank time, which
+    every rank receives (one all-reduce; the ranks run independent replicas,
+    so nothing else is exchanged)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(K, B, n, world, ms):
+    """Tokens per second of the whole job: every rank's K calls of B x n tokens
+    within the job's time."""
+    return K * B * n * world / (ms / 1e3)
+
+
 def n_rotation(bytes_per_set, l2_bytes):
     return max(2, math.ceil(2.2 * l2_bytes / max(bytes_per_set, 1)))
 
@@ -492,14 +509,9 @@ def run_ours(args):
     res = bench_prefill(torch, hh, wl, w, args.steps, args.warmup, dev, sampler, dist, l2)
     sampler.stop()
 
-    ms = res["ms_total"]
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = job_time_ms(torch, res["ms_total"], dist, dev)
     K = args.steps
-    tokens = K * w.B * w.n * world
-    value = tokens / (ms / 1e3)
+    value = job_tokens_per_s(K, w.B, w.n, world, ms)
     cnt = res["counts"]
     per_launch_s = (res["ms_total"] / 1e3) / K
     achieved_gbs = cnt["bytes"] / per_launch_s / 1e9
